@@ -1,0 +1,202 @@
+"""ctypes front end of the fp64 CPU oracle (``specverify_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` use this module.  The CUDA library never
+imports, links or runs it, and it shares no code with the CUDA library.
+
+Logit arrays are numpy arrays of shape ``[rows, width]`` whose rows may be
+strided (``arr.strides[1]`` must equal the item size).  ``np.uint16`` arrays
+hold raw bfloat16 bit patterns; ``np.float32`` arrays hold fp32 logits.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "specverify_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+BF16, F32 = 0, 1
+ST_TOKEN_RANGE, ST_BAD_LOGITS, ST_OFF_SUPPORT = 1, 2, 4
+ST_RESIDUAL_ZERO, ST_BAD_TEMP, ST_BAD_D2T = 8, 16, 32
+TAG_ACCEPT, TAG_RESIDUAL, TAG_BONUS = 0, 1, 2
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/liboracle.so`` (plain gcc, no OpenMP)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+        )
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = C.CDLL(build())
+            P = C.c_void_p
+            i32, i64, u32, u64, f32 = C.c_int32, C.c_int64, C.c_uint32, C.c_uint64, C.c_float
+            lib.or_philox4x32_10.argtypes = [P, P, P]
+            lib.or_philox4x32_10.restype = None
+            lib.or_uniform.argtypes = [u64, u32, u32, u32]
+            lib.or_uniform.restype = C.c_double
+            lib.or_uniform_from_word.argtypes = [u32]
+            lib.or_uniform_from_word.restype = C.c_double
+            lib.or_race.argtypes = [P, i32, u64, u32, u32, P]
+            lib.or_race.restype = i32
+            lib.or_accept_scan.argtypes = [P, P, P, i32, i32, P, P]
+            lib.or_accept_scan.restype = C.c_int
+            lib.or_verify_greedy.argtypes = [P, C.c_int, i64, i32, i32, i32, i32, P, P, P, P, P]
+            lib.or_verify_greedy.restype = C.c_int
+            lib.or_verify_sample.argtypes = [P, C.c_int, i64, i32, P, C.c_int, i64, i32, P, i32, i32,
+                                             P, P, P, P, P, P, P, P, P, P, P]
+            lib.or_verify_sample.restype = C.c_int
+            lib.or_cfg_merge_sample.argtypes = [P, P, C.c_int, i64, P, P, i32, i32, f32, P, C.c_int,
+                                                i64, i32, i32, P, P, P, P, P, P, P, P, P]
+            lib.or_cfg_merge_sample.restype = C.c_int
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(C.c_void_p)
+
+
+def _rows(a, name):
+    """(array, dtype code, row stride in elements, width) of a logit matrix."""
+    a = np.asarray(a)
+    if a.ndim != 2:
+        raise ValueError(f"{name} must be 2-D [rows, width]")
+    if a.dtype == np.uint16:
+        code = BF16
+    elif a.dtype == np.float32:
+        code = F32
+    else:
+        raise TypeError(f"{name}: uint16 (bf16 bits) or float32 expected, got {a.dtype}")
+    if a.shape[0] > 1 and a.strides[1] != a.itemsize:
+        raise ValueError(f"{name}: elements of a row must be contiguous")
+    if a.strides[1] != a.itemsize:
+        a = np.ascontiguousarray(a)
+    stride = a.strides[0] // a.itemsize if a.shape[0] > 1 else a.shape[1]
+    return a, code, stride, a.shape[1]
+
+
+def _i32(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def philox4x32_10(ctr, key):
+    lib = _load()
+    c = np.ascontiguousarray(np.asarray(ctr, dtype=np.uint32).reshape(4))
+    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint32).reshape(2))
+    out = np.zeros(4, dtype=np.uint32)
+    lib.or_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def uniform(seed: int, row: int, tag: int, x: int) -> float:
+    return _load().or_uniform(seed, row, tag, x)
+
+
+def uniform_from_word(r: int) -> float:
+    return _load().or_uniform_from_word(r)
+
+
+def race(w, seed: int, row: int, tag: int):
+    """(index, margin) of the exponential race over weights ``w``."""
+    w = np.ascontiguousarray(np.asarray(w, dtype=np.float64))
+    m = C.c_double(0.0)
+    idx = _load().or_race(_ptr(w), w.size, seed, row, tag, C.byref(m))
+    return int(idx), float(m.value)
+
+
+def accept_scan(accept, draft, fix):
+    accept = np.ascontiguousarray(np.asarray(accept, dtype=np.uint8))
+    R, k = accept.shape
+    draft, fix = _i32(draft), _i32(fix)
+    acc_len = np.zeros(R, np.int32)
+    tokens = np.zeros((R, k + 1), np.int32)
+    _load().or_accept_scan(_ptr(accept), _ptr(draft), _ptr(fix), R, k, _ptr(acc_len), _ptr(tokens))
+    return dict(accept_len=acc_len, tokens=tokens)
+
+
+def verify_greedy(target, R: int, k: int, branches: int, draft):
+    t, code, stride, V = _rows(target, "target")
+    rows_per_req = k + 1 if branches == 1 else 2 * k + 1
+    if t.shape[0] < R * rows_per_req:
+        raise ValueError("target has too few rows")
+    draft = _i32(draft).reshape(R, branches, k) if k else np.zeros((R, branches, 0), np.int32)
+    acc_len = np.zeros(R, np.int32)
+    tokens = np.zeros((R, k + 1), np.int32)
+    branch = np.zeros(R, np.int32)
+    status = np.zeros(R, np.int32)
+    rc = _load().or_verify_greedy(_ptr(t), code, stride, V, R, k, branches, _ptr(draft),
+                                  _ptr(acc_len), _ptr(tokens), _ptr(branch), _ptr(status))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments ({rc})")
+    return dict(accept_len=acc_len, tokens=tokens, branch=branch, status=status)
+
+
+def verify_sample(target, draft_logits, d2t, R: int, k: int, draft, seeds, temperature):
+    t, tcode, tstride, V = _rows(target, "target")
+    if draft_logits is None:
+        dl, dcode, dstride, Vd = None, F32, 0, (V if d2t is None else len(d2t))
+    else:
+        dl, dcode, dstride, Vd = _rows(draft_logits, "draft_logits")
+    d2t_a = None if d2t is None else _i32(d2t)
+    draft = _i32(draft).reshape(R, k) if k else np.zeros((R, 0), np.int32)
+    seeds = np.ascontiguousarray(np.asarray(seeds, dtype=np.uint64))
+    temperature = np.ascontiguousarray(np.asarray(temperature, dtype=np.float32))
+    acc_len = np.zeros(R, np.int32)
+    tokens = np.zeros((R, k + 1), np.int32)
+    tv = np.zeros((R, k)); pd = np.zeros((R, k)); qd = np.zeros((R, k))
+    status = np.zeros(R, np.int32)
+    am = np.zeros((R, k)); rm = np.zeros(R)
+    rc = _load().or_verify_sample(_ptr(t), tcode, tstride, V, _ptr(dl), dcode, dstride, Vd, _ptr(d2t_a),
+                                  R, k, _ptr(draft), _ptr(seeds), _ptr(temperature), _ptr(acc_len),
+                                  _ptr(tokens), _ptr(tv), _ptr(pd), _ptr(qd), _ptr(status), _ptr(am),
+                                  _ptr(rm))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments ({rc})")
+    return dict(accept_len=acc_len, tokens=tokens, tv=tv, p_draft=pd, q_draft=qd, status=status,
+                accept_margin=am, race_margin=rm)
+
+
+def cfg_merge_sample(cond, uncond, cb_id_base, cb_data_offset, S: int, W: int, w: float,
+                     draft_logits, R: int, k: int, draft, seeds, temperature):
+    c, code, stride, width = _rows(cond, "cond")
+    u, ucode, ustride, _ = _rows(uncond, "uncond")
+    if ucode != code or ustride != stride:
+        raise ValueError("cond and uncond must share dtype and row stride")
+    if draft_logits is None:
+        dl, dcode, dstride = None, F32, 0
+    else:
+        dl, dcode, dstride, _ = _rows(draft_logits, "draft_logits")
+    base = _i32(cb_id_base)
+    off = _i32(cb_data_offset)
+    draft = _i32(draft).reshape(R, k, S) if k else np.zeros((R, 0, S), np.int32)
+    seeds = np.ascontiguousarray(np.asarray(seeds, dtype=np.uint64))
+    temperature = np.ascontiguousarray(np.asarray(temperature, dtype=np.float32))
+    acc_len = np.zeros(R, np.int32)
+    tokens = np.zeros((R, k + 1, S), np.int32)
+    tv = np.zeros((R, k, S)); status = np.zeros(R, np.int32)
+    am = np.zeros((R, k, S)); rm = np.zeros((R, S))
+    rc = _load().or_cfg_merge_sample(_ptr(c), _ptr(u), code, stride, _ptr(base), _ptr(off), S, W, w,
+                                     _ptr(dl), dcode, dstride, R, k, _ptr(draft), _ptr(seeds),
+                                     _ptr(temperature), _ptr(acc_len), _ptr(tokens), _ptr(tv),
+                                     _ptr(status), _ptr(am), _ptr(rm))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments ({rc})")
+    return dict(accept_len=acc_len, tokens=tokens, tv=tv, status=status, accept_margin=am,
+                race_margin=rm)
