@@ -1,0 +1,218 @@
+/*
+ * specverify -- speculative-decoding verify-and-sample on one GPU (sm_103a).
+ *
+ * The library turns the target model's logit rows for a block of draft
+ * positions into committed tokens and accept lengths.  Three modes:
+ *
+ *   greedy verification  -- "Decode Before You Hear: Speculative Listening for
+ *       Chunk-Interleaved Full-Duplex Speech Language Models" (digest), section
+ *       "method steps", step 4 (accept the prefix before the first draft token
+ *       that differs from argmax p_i, then commit argmax p_{n+1}) and step 2
+ *       (a runner-up branch verified in the same forward pass);
+ *   speculative sampling -- "speculative decoding for Omni models" (blog),
+ *       section 2 (accept with probability min(1, p/q), resample from
+ *       norm(max(0, p - q)) on rejection, bonus token from p when every draft
+ *       is accepted, TV = 1/2 sum |p - q|) and section 4 (truncated draft
+ *       vocabulary mapped by d2t; ids outside it have q = 0);
+ *   CFG merge per codebook -- "An Efficient vLLM-Based Inference Pipeline for
+ *       Unified Audio Understanding and Generation" (digest), paired CFG
+ *       co-scheduling section and Figure 1 text (the conditional and
+ *       unconditional logits of each codebook are merged linearly with w > 1,
+ *       then one token per codebook is sampled from the audio partition).
+ *
+ * Conventions shared by every call
+ *  - Pointers are DEVICE pointers unless a comment says HOST.  The caller owns
+ *    every buffer; the library allocates and frees nothing.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream).  The return value reports host-side argument checks and
+ *    the launch status only; per-request data problems are reported in the
+ *    device-written `status` array (bits SV_ST_*), never by a trap.
+ *  - Results are a pure function of the inputs: they do not depend on the
+ *    batch size, the position of a request in the batch or the launch
+ *    geometry.  Random draws come from Philox4x32-10 keyed by the request's
+ *    seed, so a call repeated on the same inputs gives the same bits.
+ *  - Ties in an argmax or in the sampler go to the lowest index.  NaN logits
+ *    read as -inf.
+ *  - Workspace: calls that take one need at least the number of bytes the
+ *    matching *_workspace function returns, 256-byte aligned.  Its contents on
+ *    entry do not matter; calls sharing one workspace must not overlap.
+ *  - The library keeps no state between calls and is thread-safe.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* sv_stream_t; /* same type as cudaStream_t */
+
+/* return codes */
+enum {
+    SV_OK = 0,
+    SV_ERR_INVALID_ARG = -1, /* NULL where a buffer is required, negative size, bad enum */
+    SV_ERR_DTYPE = -2,       /* logit dtype is neither SV_BF16 nor SV_F32 */
+    SV_ERR_SHAPE = -3,       /* width / row_stride / offsets inconsistent */
+    SV_ERR_LIMIT = -4,       /* k, S or a size above the documented limits */
+    SV_ERR_LAUNCH = -5,      /* the CUDA launch failed (see cudaGetLastError) */
+    SV_ERR_WORKSPACE = -6,   /* workspace NULL, too small or not 256-byte aligned */
+    SV_ERR_ALIGN = -7,       /* a pointer is not aligned to its element size */
+    SV_ERR_DEVICE = -8       /* no usable CUDA device */
+};
+
+/* logit element types */
+enum { SV_BF16 = 0, SV_F32 = 1 };
+
+/* per-request status bits, written to status[r] (0 = nothing to report) */
+enum {
+    SV_ST_TOKEN_RANGE = 1,    /* a draft token is outside the vocabulary: it never matches */
+    SV_ST_BAD_LOGITS = 2,     /* a row holds NaN or +inf or is all -inf (sampling: greedy used) */
+    SV_ST_OFF_SUPPORT = 4,    /* a tested draft token has q = 0: rejected */
+    SV_ST_RESIDUAL_ZERO = 8,  /* max(0, p - q) had no mass: the correction was drawn from p */
+    SV_ST_BAD_TEMP = 16,      /* temperature negative or NaN: greedy verification used */
+    SV_ST_BAD_D2T = 32,       /* d2t holds an id outside [0, V) or a repeated id */
+    SV_ST_TIMEOUT = 64        /* a bounded device wait gave up; the request's outputs are invalid */
+};
+
+/* limits */
+#define SV_MAX_K 256       /* drafts per request (per branch) */
+#define SV_MAX_S 16        /* codebooks per CFG frame */
+#define SV_MAX_WIDTH (1 << 30)
+
+/* A matrix of logit rows: row i, entry x is at data + (i * row_stride + x)
+ * elements.  `data` must be aligned to the element size.  Rows whose start
+ * is 16-byte aligned (data 16-byte aligned and row_stride * element size a
+ * multiple of 16) take the bulk-copy path; other layouts are accepted and
+ * read with plain loads. */
+typedef struct sv_rows {
+    const void* data;
+    int32_t dtype;      /* SV_BF16 or SV_F32 */
+    int32_t width;      /* entries per row: V, Vd or W */
+    int64_t row_stride; /* elements between consecutive row starts, >= width */
+} sv_rows;
+
+/* Human-readable text for a return code. */
+const char* sv_status_string(int code);
+
+/* ------------------------------------------------------------------------
+ * sv_verify_greedy -- greedy verification with an optional runner-up branch.
+ * Source: "Decode Before You Hear ..." method steps 2 and 4.
+ *
+ *   target      rows of raw target logits, width V.  branches == 1: k + 1 rows
+ *               per request (positions 1..k and the row after the last
+ *               draft); branches == 2: 2k + 1 rows per request laid out as
+ *               [p_1 | main p_2..p_{k+1} | runner p_2..p_{k+1}] (row p_1 is
+ *               shared by both branches).  Request r's rows start at row
+ *               r * rows_per_request.
+ *   R           requests (>= 0; 0 is a no-op).
+ *   k           drafts per branch, 0 <= k <= SV_MAX_K (k >= 1 with 2 branches).
+ *   branches    1 or 2.
+ *   draft       int32 [R, branches, k] target ids.
+ *   accept_len  int32 [R] out: accepted drafts n in [0, k].
+ *   tokens      int32 [R, k + 1] out: the n accepted drafts then the
+ *               correction argmax p_{n+1}; remaining entries -1.
+ *   branch      int32 [R] out or NULL: the branch whose tokens were taken.
+ *   status      int32 [R] out or NULL: SV_ST_* bits.
+ * argmax is over raw logits (temperature cannot change it).  A branch is
+ * viable when its first draft equals argmax p_1; among viable branches the
+ * longer accepted prefix wins, ties to branch 0; with none viable n = 0.
+ * ---------------------------------------------------------------------- */
+size_t sv_verify_greedy_workspace(int32_t R, int32_t k, int32_t branches, int32_t V);
+int sv_verify_greedy(sv_rows target, int32_t R, int32_t k, int32_t branches,
+                     const int32_t* draft, int32_t* accept_len, int32_t* tokens,
+                     int32_t* branch, int32_t* status, void* workspace,
+                     size_t workspace_bytes, sv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * sv_verify_sample -- speculative sampling with a truncated draft vocabulary.
+ * Source: "speculative decoding for Omni models", sections 2 and 4.
+ *
+ *   target        target logits, width V, k + 1 rows per request (positions
+ *                 0..k-1 then the bonus row k).
+ *   draft_logits  draft-model logits, width Vd, k rows per request.  Read only
+ *                 for requests with temperature > 0.
+ *   d2t           int32 [Vd]: draft id -> target id, injective; NULL means the
+ *                 identity (then Vd must equal V).  Target ids outside the
+ *                 image of d2t have q = 0.
+ *   draft         int32 [R, k] draft tokens as TARGET ids.
+ *   seeds         uint64 [R] Philox key of each request.
+ *   temperature   float [R]; T > 0 samples, T <= 0 verifies greedily.
+ *   accept_len    int32 [R] out; tokens int32 [R, k + 1] out (-1 padded).
+ *   tv, p_draft, q_draft  float [R, k] out or NULL: TV(p_j, q_j) over the
+ *                 full target vocabulary, p_j(x_j) and q_j(x_j) for every
+ *                 position j (also after the first rejection); NaN for
+ *                 greedy requests.
+ *   status        int32 [R] out or NULL.
+ * Definition: p_j = softmax(z_j / T), q_j = softmax(y_j / T) pushed through
+ * d2t.  Position j is accepted when q_j(x_j) > 0 and u_j < p_j(x_j)/q_j(x_j)
+ * with u_j the Philox uniform (counter (0, j, 0, 0), word 0).  n = leading
+ * accepts.  n < k: the correction is argmin_{r_x > 0} E_x / r_x over
+ * r = max(0, p_n - q_n), E_x = -ln u_x with u_x from counter
+ * (x >> 2, n, 1, 0) word x & 3.  n == k: the bonus is argmin E_x / p_k(x)
+ * with counter (x >> 2, k, 2, 0).  A uniform from word w is
+ * (2 * (w >> 9) + 1) * 2^-24.
+ * ---------------------------------------------------------------------- */
+size_t sv_verify_sample_workspace(int32_t R, int32_t k, int32_t V, int32_t Vd);
+int sv_verify_sample(sv_rows target, sv_rows draft_logits, const int32_t* d2t, int32_t R,
+                     int32_t k, const int32_t* draft, const uint64_t* seeds,
+                     const float* temperature, int32_t* accept_len, int32_t* tokens,
+                     float* tv, float* p_draft, float* q_draft, int32_t* status,
+                     void* workspace, size_t workspace_bytes, sv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * sv_cfg_merge_sample -- CFG merge per RVQ codebook, then verification.
+ * Source: "An Efficient vLLM-Based Inference Pipeline ..." paired CFG
+ * co-scheduling and Figure 1 text; sampling rules as in sv_verify_sample.
+ *
+ *   cond, uncond    logit rows sharing dtype and row_stride; row
+ *                   (r * (k + 1) + j) * S + s holds frame j, codebook s of
+ *                   request r.  `width` is W, the codebook size.
+ *   cb_id_base      HOST int32 [S]: absolute vocabulary id of entry 0 of
+ *                   codebook s (the audio partition: the phase mask).
+ *   cb_data_offset  HOST int32 [S] or NULL (all 0): element offset of codebook
+ *                   s inside its row; offset + W <= row_stride.
+ *   S               codebooks, 1 <= S <= SV_MAX_S;  w  CFG weight.
+ *   draft_logits    draft rows, width W, row (r * k + j) * S + s; data == NULL
+ *                   selects greedy verification on the merged logits.
+ *   draft           int32 [R, k, S] absolute ids.
+ *   seeds, temperature  as in sv_verify_sample.
+ *   accept_len      int32 [R] out: accepted FRAMES.
+ *   tokens          int32 [R, k + 1, S] out: absolute ids, -1 padded.
+ *   tv              float [R, k, S] out or NULL;  status int32 [R] out or NULL.
+ * The merge is m = u + w (c - u) evaluated in fp32 as d = c - u then
+ * fmaf(w, d, u).  A frame is accepted when all S codebooks pass; at the
+ * first rejected frame n each codebook keeps its draft if its own test
+ * passed, else takes its residual sample (Philox row n * S + s); uniforms of
+ * (frame j, codebook s) use Philox row j * S + s.
+ * ---------------------------------------------------------------------- */
+size_t sv_cfg_merge_sample_workspace(int32_t R, int32_t k, int32_t S, int32_t W);
+int sv_cfg_merge_sample(sv_rows cond, sv_rows uncond, const int32_t* cb_id_base,
+                        const int32_t* cb_data_offset, int32_t S, float w,
+                        sv_rows draft_logits, int32_t R, int32_t k, const int32_t* draft,
+                        const uint64_t* seeds, const float* temperature,
+                        int32_t* accept_len, int32_t* tokens, float* tv, int32_t* status,
+                        void* workspace, size_t workspace_bytes, sv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * sv_accept_scan -- accept length and commit from caller-given accept flags.
+ * Source: "Decode Before You Hear ..." step 4 (the accepted prefix stops at
+ * the first failure); "speculative decoding for Omni models" section 3
+ * (draft i counts only when drafts 1..i-1 were accepted).
+ *
+ *   accept      uint8 [R, k], nonzero = accepted.
+ *   draft       int32 [R, k].
+ *   fix         int32 [R, k + 1]: the token to commit when the chain stops
+ *               at position j (j = k: every draft accepted).
+ *   accept_len  int32 [R] out;  tokens int32 [R, k + 1] out (-1 padded).
+ * ---------------------------------------------------------------------- */
+int sv_accept_scan(const uint8_t* accept, const int32_t* draft, const int32_t* fix, int32_t R,
+                   int32_t k, int32_t* accept_len, int32_t* tokens, sv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPECVERIFY_H */

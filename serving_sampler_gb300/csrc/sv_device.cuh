@@ -1,0 +1,173 @@
+// Device-side building blocks of the specverify kernels (sm_103a):
+// shared-memory barriers and bulk (TMA) copies written as inline PTX, bounded
+// waits, packed bf16 maxima, Philox4x32-10 and the uniform used by every
+// random draw.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "specverify.h"
+
+namespace sv {
+
+// Every wait on a barrier gives up after this many SM cycles (about two
+// seconds at the boost clock); the kernel then records SV_ST_TIMEOUT instead
+// of spinning forever.
+constexpr long long kWaitLimitCycles = 4000000000LL;
+
+// flags carried by per-row partial results
+enum : uint32_t { kFlagNaN = 1u, kFlagTimeout = 2u, kFlagPosInf = 4u };
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- mbarrier -------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+// make initialised barriers visible to the async (bulk-copy) proxy
+__device__ __forceinline__ void fence_barrier_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the given phase with a time limit.  Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > kWaitLimitCycles) return false;
+    }
+    return true;
+}
+
+// ---- bulk copies (TMA, 1-D) ------------------------------------------------
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// global -> shared copy of `bytes` (multiple of 16, both addresses 16-byte
+// aligned) that completes a transaction count on `bar`.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// ---- programmatic dependent launch ----------------------------------------
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primary()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ---- packed bf16 / fp32 maxima that propagate NaN ---------------------------
+__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ float fmax_nan(float a, float b)
+{
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+// the two bf16 halves of a 32-bit word, widened exactly to fp32
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// ---- Philox4x32-10 (Salmon et al., SC'11) ----------------------------------
+struct PhiloxKey {
+    uint32_t k0, k1;
+};
+
+__device__ __forceinline__ PhiloxKey philox_key(uint64_t seed)
+{
+    return PhiloxKey{static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32)};
+}
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, PhiloxKey key)
+{
+    uint32_t k0 = key.k0, k1 = key.k1;
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint32_t hi_a = __umulhi(0xD2511F53u, c.x);
+        const uint32_t lo_a = 0xD2511F53u * c.x;
+        const uint32_t hi_b = __umulhi(0xCD9E8D57u, c.z);
+        const uint32_t lo_b = 0xCD9E8D57u * c.z;
+        c = make_uint4(hi_b ^ c.y ^ k0, lo_b, hi_a ^ c.w ^ k1, lo_a);
+    }
+    return c;
+}
+
+// Uniform in (0, 1) from one 32-bit word: (2 * (w >> 9) + 1) * 2^-24.  The
+// mantissa trick builds 1 + (w >> 9) * 2^-23 and subtracts 1 - 2^-24; both
+// steps are exact in fp32.
+__device__ __forceinline__ float uniform_from_word(uint32_t w)
+{
+    return __uint_as_float(0x3F800000u | (w >> 9)) - __uint_as_float(0x3F7FFFFFu);
+}
+
+// counter layout of the library: (x >> 2, row, tag, 0), word x & 3
+enum : uint32_t { kTagAccept = 0, kTagResidual = 1, kTagBonus = 2 };
+
+__device__ __forceinline__ uint4 philox_block(PhiloxKey key, uint32_t x4, uint32_t row, uint32_t tag)
+{
+    return philox4x32_10(make_uint4(x4, row, tag, 0u), key);
+}
+
+// ---- (value, index) argmax state --------------------------------------------
+struct ArgMax {
+    float v;    // best value seen (never NaN); -inf when nothing was seen
+    int32_t i;  // its index; INT32_MAX when nothing beat -inf
+};
+
+__device__ __forceinline__ bool argmax_better(float v, int32_t i, const ArgMax& a)
+{
+    return v > a.v || (v == a.v && i < a.i);
+}
+
+}  // namespace sv

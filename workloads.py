@@ -1,0 +1,146 @@
+"""Seeded synthetic inputs for the verify-and-sample workloads.
+
+This module only draws inputs: logit rows, draft tokens, maps, seeds and
+temperatures.  It holds none of the verification arithmetic (no softmax,
+acceptance test, TV or sampler); argmax tokens are planted, never searched.
+Both the CUDA library's tests/benchmark and the CPU oracle read what it
+produces, so the two sides always see the same bytes.
+
+The stand-ins replace datasets and trained models that are not available
+(TickTock-Bench sessions, DSpark / EAGLE3 draft models on a 151,936-token
+target vocabulary, RVQ codec heads): shapes, vocabulary sizes, value
+spread and acceptance profile follow the workload descriptions.
+
+Workloads (names used by tests and the benchmark):
+  tiny      4 requests x 8 drafts (+1 row), V = 4096, fp32 logits ~ N(0, 2^2);
+            drafts = the planted argmax w.p. 0.7, else uniform; sampling
+            variant with draft logits = target + N(0, 1), T = 1, seed 0.
+  listen    64 sessions, a main draft of 32 tokens plus a 32-token runner-up
+            branch (65 rows per session), V = 151,936 bf16 ~ N(0, 3^2) with
+            the argmax planted 2.0 above the row maximum; 95% of main drafts
+            match fully, 88% of the mismatches sit at position 0.
+  d2t       128 requests x 7 drafts (+ bonus), V = 151,936 bf16, draft vocab
+            32,000 with a seeded random injective d2t, T = 0.7.
+  cfg       256 requests, 9 codebooks x 4096 entries, 4 drafted frames (+1),
+            bf16 cond / uncond rows, w = 3, T = 1, flat distributions.
+  sweep     batch x 9 rows (k = 8), V = 151,936, bf16 or fp32 ~ N(0, 3^2),
+            requests alternating greedy (T = 0) and sampling (T in {0.6, 1.0})
+            with d2t-truncated draft logits.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+V_QWEN = 151_936
+VD_DRAFT = 32_000
+
+
+def splitmix64(x: int) -> int:
+    """Seed scrambler for per-request Philox keys (Steele, Lea, Flood 2014)."""
+    x = (x + 0x9E3779B97F4A7C15) & 0xFFFFFFFFFFFFFFFF
+    z = x
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & 0xFFFFFFFFFFFFFFFF
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & 0xFFFFFFFFFFFFFFFF
+    return z ^ (z >> 31)
+
+
+def seeds_array(base: int, R: int) -> np.ndarray:
+    return np.array([splitmix64(base + r) for r in range(R)], dtype=np.uint64)
+
+
+def seeds_tensor(base: int, R: int, device) -> torch.Tensor:
+    """uint64 seeds stored in an int64 tensor (same bits)."""
+    return torch.from_numpy(seeds_array(base, R).view(np.int64)).to(device)
+
+
+def _gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def _plant(z: torch.Tensor, idx: torch.Tensor, above: float) -> None:
+    """Set z[i, idx[i]] = max_x z[i, x] + above (in place, fp32)."""
+    rowmax = z.amax(dim=1)
+    z.scatter_(1, idx.view(-1, 1), (rowmax + above).view(-1, 1))
+
+
+def _rand_other(g, avoid: torch.Tensor, V: int) -> torch.Tensor:
+    """Uniform token different from `avoid`, elementwise."""
+    r = torch.randint(0, V - 1, avoid.shape, generator=g, device=avoid.device, dtype=torch.int64)
+    return torch.where(r >= avoid, r + 1, r)
+
+
+# ---------------------------------------------------------------------------
+# greedy workloads
+# ---------------------------------------------------------------------------
+def greedy_batch(R: int, k: int, V: int, dtype=torch.bfloat16, sigma: float = 3.0, branches: int = 1,
+                 p_full: float = 0.95, p_first: float = 0.88, seed: int = 0, device="cuda", row_pad: int = 0):
+    """Target rows with planted argmaxes and drafts with a controlled accept profile.
+
+    Returns dict(target [rows, V] (row stride V + row_pad), draft [R, branches, k], R, k, branches, V,
+    planted [R, rows_per_request] argmax ids).
+    """
+    g = _gen(seed, device)
+    rpr = k + 1 if branches == 1 else 2 * k + 1
+    rows = R * rpr
+    z = torch.randn(rows, V + row_pad, generator=g, device=device, dtype=torch.float32) * sigma
+    top = torch.randint(0, V, (rows,), generator=g, device=device)
+    _plant(z[:, :V], top, 2.0)
+    top = top.view(R, rpr)
+    second = None
+    if branches == 2:
+        # second best of the shared first row: 1.0 above every other entry, 1.0 below the top
+        second = _rand_other(g, top[:, 0], V)
+        z0 = z.view(R, rpr, V + row_pad)[:, 0, :V]
+        z0.scatter_(1, second.view(-1, 1), z0.gather(1, top[:, 0:1]) - 1.0)
+    target = z.to(dtype)
+    if row_pad:
+        target = target[:, :V]
+    # main branch: position j is verified by row j (row 0 shared with the runner-up)
+    main = top[:, :k].clone()
+    if k > 0:
+        full = torch.rand(R, generator=g, device=device) < p_full
+        first = torch.rand(R, generator=g, device=device) < p_first
+        later = torch.randint(1, max(k, 2), (R,), generator=g, device=device).clamp(max=k - 1)
+        pos = torch.where(first, torch.zeros_like(later), later)
+        wrong = _rand_other(g, top.gather(1, pos.view(-1, 1)).view(-1), V)
+        bad = ~full
+        main[bad, pos[bad]] = wrong[bad]
+    drafts = [main]
+    if branches == 2:
+        runner = torch.empty(R, k, dtype=torch.int64, device=device)
+        # runner-up of row 0 excluding the main draft's first token
+        runner[:, 0] = torch.where(main[:, 0] == top[:, 0], second, top[:, 0])
+        runner[:, 1:] = top[:, k + 1:2 * k]
+        drafts.append(runner)
+    draft = torch.stack(drafts, dim=1).to(torch.int32).contiguous()
+    return dict(target=target, draft=draft, R=R, k=k, branches=branches, V=V, planted=top)
+
+
+def tiny_greedy(device="cuda", dtype=torch.float32):
+    """4 requests x 8 drafts, V = 4096, fp32 ~ N(0, 2^2), drafts = argmax w.p. 0.7."""
+    R, k, V = 4, 8, 4096
+    g = _gen(0, device)
+    rows = R * (k + 1)
+    z = torch.randn(rows, V, generator=g, device=device) * 2.0
+    top = torch.randint(0, V, (rows,), generator=g, device=device)
+    _plant(z, top, 0.5)
+    top = top.view(R, k + 1)
+    keep = torch.rand(R, k, generator=g, device=device) < 0.7
+    other = torch.randint(0, V, (R, k), generator=g, device=device)
+    draft = torch.where(keep, top[:, :k], other).to(torch.int32).view(R, 1, k).contiguous()
+    return dict(target=z.to(dtype), draft=draft, R=R, k=k, branches=1, V=V, planted=top)
+
+
+def listen(device="cuda", R: int = 64, seed: int = 1236):
+    """Speculative-listening greedy verify: 64 sessions x (32 main + 32 runner) drafts, 65 rows each."""
+    return greedy_batch(R, 32, V_QWEN, torch.bfloat16, 3.0, branches=2, seed=seed, device=device)
+
+
+def host_rows(t: torch.Tensor) -> np.ndarray:
+    """A CPU numpy copy of logit rows: bf16 -> uint16 bit patterns, fp32 as is."""
+    if t.dtype == torch.bfloat16:
+        return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    return t.detach().cpu().contiguous().numpy()
