@@ -1,3 +1,4 @@
+import json
 import os
 import sys
 
@@ -13,12 +14,21 @@ def pytest_configure(config):
 
 
 def golden(name):
-    import json
-
     with open(os.path.join(ROOT, "tests", "golden", name)) as f:
         return json.load(f)
 
 
-@pytest.fixture
-def golden_data():
-    return golden
+@pytest.fixture(scope="session")
+def sv():
+    """The CUDA binding, built in-tree; GPU tests fail loudly if it cannot load."""
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test selected but no CUDA device is visible")
+    from serving_sampler_gb300 import _build
+
+    _build.build()
+    import serving_sampler_gb300 as m
+
+    m.load()
+    return m

@@ -1,0 +1,115 @@
+"""The C-ABI library builds, loads and exports every entry point the header
+declares; host-side argument checks answer without touching a GPU."""
+import ctypes as C
+import os
+import re
+import shutil
+
+import pytest
+
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "specverify.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sv_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("nvcc not available")
+    from serving_sampler_gb300 import _build
+
+    _build.build()
+    import serving_sampler_gb300 as m
+
+    return m.load()
+
+
+def test_header_declares_the_four_calls():
+    names = _declared()
+    for n in ["sv_verify_greedy", "sv_verify_sample", "sv_cfg_merge_sample", "sv_accept_scan"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), f"{name} declared in specverify.h but not exported"
+
+
+def test_status_strings(lib):
+    for code in range(0, -9, -1):
+        s = lib.sv_status_string(code)
+        assert s and s != b"unknown status"
+    assert lib.sv_status_string(12345) == b"unknown status"
+
+
+def test_workspace_sizes(lib):
+    assert lib.sv_verify_greedy_workspace(64, 32, 2, 151936) >= 64 * 65 * 16
+    assert lib.sv_verify_greedy_workspace(-1, 2, 1, 10) == 0
+    assert lib.sv_verify_greedy_workspace(1, 2, 3, 10) == 0
+    assert lib.sv_verify_sample_workspace(128, 7, 151936, 32000) > 0
+    assert lib.sv_cfg_merge_sample_workspace(256, 4, 9, 4096) > 0
+    assert lib.sv_cfg_merge_sample_workspace(1, 1, 17, 4096) == 0
+
+
+def _rows(data=0x1000, dtype=0, width=16, stride=16):
+    import serving_sampler_gb300 as m
+
+    return m.SvRows(data, dtype, width, stride)
+
+
+def test_argument_checks_need_no_gpu(lib):
+    P = C.c_void_p
+    buf = P(0x10000)
+    ws = P(0x20000)
+    g = lib.sv_verify_greedy
+    # R == 0 is a no-op
+    assert g(_rows(), 0, 2, 1, buf, buf, buf, None, None, ws, 1 << 20, None) == 0
+    assert g(_rows(), -1, 2, 1, buf, buf, buf, None, None, ws, 1 << 20, None) == -1
+    assert g(_rows(), 1, 2, 3, buf, buf, buf, None, None, ws, 1 << 20, None) == -1
+    assert g(_rows(), 1, 0, 2, buf, buf, buf, None, None, ws, 1 << 20, None) == -1
+    assert g(_rows(), 1, 257, 1, buf, buf, buf, None, None, ws, 1 << 20, None) == -4
+    assert g(_rows(dtype=7), 1, 2, 1, buf, buf, buf, None, None, ws, 1 << 20, None) == -2
+    assert g(_rows(stride=8), 1, 2, 1, buf, buf, buf, None, None, ws, 1 << 20, None) == -3
+    assert g(_rows(data=0x1001), 1, 2, 1, buf, buf, buf, None, None, ws, 1 << 20, None) == -7
+    assert g(_rows(), 1, 2, 1, None, buf, buf, None, None, ws, 1 << 20, None) == -1
+    assert g(_rows(), 1, 2, 1, buf, buf, buf, None, None, ws, 16, None) == -6
+    assert g(_rows(), 1, 2, 1, buf, buf, buf, None, None, P(0x20010), 1 << 20, None) == -6
+    s = lib.sv_accept_scan
+    assert s(buf, buf, buf, -2, 3, buf, buf, None) == -1
+    assert s(buf, buf, buf, 0, 3, buf, buf, None) == 0
+    assert s(buf, buf, None, 2, 3, buf, buf, None) == -1
+    c = lib.sv_cfg_merge_sample
+    base = (C.c_int32 * 2)(0, 16)
+    assert c(_rows(), _rows(width=8), C.cast(base, P), None, 2, 3.0, _rows(data=None), 1, 1, buf, buf, buf, buf,
+             buf, None, None, ws, 1 << 20, None) == -3
+    assert c(_rows(), _rows(), C.cast(base, P), None, 17, 3.0, _rows(data=None), 1, 1, buf, buf, buf, buf,
+             buf, None, None, ws, 1 << 20, None) == -4
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    import serving_sampler_gb300 as m
+
+    saved = m._lib
+    m._lib = None
+    try:
+        with pytest.raises(RuntimeError):
+            m.load(str(tmp_path / "missing.so"))
+    finally:
+        m._lib = saved
+
+
+def test_valid_call_without_device_reports_no_device(lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    P = C.c_void_p
+    buf = P(0x10000)
+    rc = lib.sv_verify_greedy(_rows(), 1, 2, 1, buf, buf, buf, None, None, P(0x20000), 1 << 20, None)
+    assert rc == -8
