@@ -7,12 +7,12 @@
 // shared memory with 1-D bulk copies (TMA) in 8 KB chunks, one mbarrier per
 // chunk, and reduces (max, first index) while later chunks are in flight.
 // The inner step takes the NaN-propagating max of 8 bf16 values with three
-// packed max instructions; only a vector that beats the running maximum (or
-// holds a NaN) is searched element by element, so the common path costs
-// about one instruction per element and the kernel is bound by HBM.
+// packed max instructions and keeps (max, vector start) with two selects;
+// the first index inside the winning vector is found once per segment.  Only
+// a vector holding a NaN leaves the straight-line path.
 // Kernel 2 (greedy_finalize_kernel) merges the segment results of each row
-// and runs the per-request scan with one warp per request; it is launched
-// as a programmatic dependent of kernel 1 so its launch overlaps kernel 1.
+// and runs the per-request scan, one CTA per request; it is launched as a
+// programmatic dependent of kernel 1 so its launch overlaps kernel 1.
 #include <algorithm>
 #include <cfloat>
 #include <climits>
@@ -60,42 +60,62 @@ __device__ __forceinline__ float load_one(const char* p, int32_t e)
     }
 }
 
-__device__ __forceinline__ void argmax_scalar(ArgMax& st, uint32_t& flags, float f, int32_t x)
+// Running state of one thread: the largest value seen and the first index of
+// the 16-byte vector (or single tail element) where it was first seen.  The
+// exact index inside that vector is resolved once per segment, so the hot
+// loop has no divergent branch: a new maximum is taken with two selects.
+struct VecMax {
+    float v;
+    int32_t x;
+};
+
+__device__ __forceinline__ void vecmax_take(VecMax& st, float vm, int32_t x)
+{
+    const bool up = vm > st.v;
+    st.v = up ? vm : st.v;
+    st.x = up ? x : st.x;
+}
+
+__device__ __forceinline__ void scalar_take(VecMax& st, uint32_t& flags, float f, int32_t x)
 {
     if (f != f) {
         flags |= kFlagNaN;
-    } else if (f > st.v) {
-        st.v = f;
-        st.i = x;
+        return;
     }
+    vecmax_take(st, f, x);
 }
 
 // one 16-byte vector of 8 bf16 or 4 fp32 values whose first index is x
 template <int DT>
-__device__ __forceinline__ void argmax_vec(ArgMax& st, uint32_t& flags, uint4 q, int32_t x)
+__device__ __forceinline__ void vec_take(VecMax& st, uint32_t& flags, uint4 q, int32_t x)
 {
+    float vm;
     if constexpr (DT == SV_BF16) {
         const uint32_t m = bmax2_nan(bmax2_nan(q.x, q.y), bmax2_nan(q.z, q.w));
-        const float vm = fmax_nan(bf16_lo(m), bf16_hi(m));
-        if (!(vm <= st.v)) {  // a new maximum, or a NaN somewhere in the vector
-            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        vm = fmax_nan(bf16_lo(m), bf16_hi(m));
+    } else {
+        vm = fmax_nan(fmax_nan(__uint_as_float(q.x), __uint_as_float(q.y)),
+                      fmax_nan(__uint_as_float(q.z), __uint_as_float(q.w)));
+    }
+    if (vm != vm) {  // rare: a NaN in the vector; take the max of the others
+        flags |= kFlagNaN;
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        vm = -INFINITY;
+        if constexpr (DT == SV_BF16) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const float f = (e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1]);
-                argmax_scalar(st, flags, f, x + e);
+                vm = f > vm ? f : vm;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float f = __uint_as_float(w[e]);
+                vm = f > vm ? f : vm;
             }
         }
-    } else {
-        const float a = __uint_as_float(q.x), b = __uint_as_float(q.y);
-        const float c = __uint_as_float(q.z), d = __uint_as_float(q.w);
-        const float vm = fmax_nan(fmax_nan(a, b), fmax_nan(c, d));
-        if (!(vm <= st.v)) {
-            argmax_scalar(st, flags, a, x);
-            argmax_scalar(st, flags, b, x + 1);
-            argmax_scalar(st, flags, c, x + 2);
-            argmax_scalar(st, flags, d, x + 3);
-        }
     }
+    vecmax_take(st, vm, x);
 }
 
 template <int DT>
@@ -120,7 +140,7 @@ __global__ void __launch_bounds__(kArgThreads)
     const int32_t len = max(0, min(V, x0 + seg_len) - x0);
     const char* src = base + row * row_stride_bytes + static_cast<int64_t>(x0) * ES;
 
-    ArgMax st{-INFINITY, INT32_MAX};
+    VecMax st{-INFINITY, INT32_MAX};
     uint32_t flags = 0;
     int32_t nbulk = 0;
     if (use_bulk) {
@@ -153,7 +173,7 @@ __global__ void __launch_bounds__(kArgThreads)
             const int nv = static_cast<int>(nb / 16);
             const int32_t xc = x0 + static_cast<int32_t>(off / ES);
 #pragma unroll 4
-            for (int t = threadIdx.x; t < nv; t += kArgThreads) argmax_vec<DT>(st, flags, vp[t], xc + t * VEC);
+            for (int t = threadIdx.x; t < nv; t += kArgThreads) vec_take<DT>(st, flags, vp[t], xc + t * VEC);
         }
         if (!ok) {
             flags |= kFlagTimeout;
@@ -164,17 +184,17 @@ __global__ void __launch_bounds__(kArgThreads)
     // the sub-16-byte tail, or the whole segment when bulk copies are off;
     // every thread still visits its elements in ascending order
     for (int32_t e = nbulk + threadIdx.x; e < len; e += kArgThreads)
-        argmax_scalar(st, flags, load_one<DT>(src, e), x0 + e);
+        scalar_take(st, flags, load_one<DT>(src, e), x0 + e);
 
-    // block reduction of (value, lowest index) and flags
+    // block reduction of (value, first vector start) and flags
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, st.v, o);
-        const int32_t oi = __shfl_xor_sync(0xffffffffu, st.i, o);
-        if (argmax_better(ov, oi, st)) st = ArgMax{ov, oi};
+        const int32_t ox = __shfl_xor_sync(0xffffffffu, st.x, o);
+        if (ov > st.v || (ov == st.v && ox < st.x)) st = VecMax{ov, ox};
     }
     flags = __reduce_or_sync(0xffffffffu, flags);
-    __shared__ ArgMax wbest[kArgThreads / 32];
+    __shared__ VecMax wbest[kArgThreads / 32];
     __shared__ uint32_t wflags[kArgThreads / 32];
     const int warp = threadIdx.x >> 5;
     if ((threadIdx.x & 31) == 0) {
@@ -183,24 +203,47 @@ __global__ void __launch_bounds__(kArgThreads)
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        ArgMax b = wbest[0];
+        VecMax b = wbest[0];
         uint32_t f = wflags[0];
         for (int w = 1; w < kArgThreads / 32; ++w) {
-            if (argmax_better(wbest[w].v, wbest[w].i, b)) b = wbest[w];
+            if (wbest[w].v > b.v || (wbest[w].v == b.v && wbest[w].x < b.x)) b = wbest[w];
             f |= wflags[w];
         }
-        out[unit] = ArgPartial{b.v, b.i, f, 0u};
+        // the first element equal to the maximum, inside the winning vector
+        int32_t idx = INT32_MAX;
+        if (b.x != INT32_MAX) {
+            for (int e = 0; e < VEC; ++e) {
+                const int32_t le = b.x - x0 + e;
+                if (le >= len) break;
+                float f2;
+                if (le < nbulk) {
+                    if constexpr (DT == SV_BF16)
+                        f2 = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(buf)[le]) << 16);
+                    else
+                        f2 = reinterpret_cast<const float*>(buf)[le];
+                } else {
+                    f2 = load_one<DT>(src, le);
+                }
+                if (f2 == b.v) {
+                    idx = b.x + e;
+                    break;
+                }
+            }
+        }
+        out[unit] = ArgPartial{b.v, idx, f, 0u};
     }
 }
 
-constexpr int kFinWarps = 4;
+constexpr int kFinThreads = 256;
 
 __device__ __forceinline__ int32_t branch_row(int32_t b, int32_t j, int32_t k)
 {
     return j == 0 ? 0 : b * k + j;
 }
 
-__global__ void __launch_bounds__(kFinWarps * 32)
+// One CTA per request: every thread merges the segment results of some rows
+// (independent loads, several in flight), then warp 0 runs the scan.
+__global__ void __launch_bounds__(kFinThreads)
     greedy_finalize_kernel(const ArgPartial* __restrict__ part, int32_t nseg, int32_t R, int32_t k,
                            int32_t branches, int32_t V, const int32_t* __restrict__ draft,
                            int32_t* __restrict__ accept_len, int32_t* __restrict__ tokens,
@@ -208,26 +251,32 @@ __global__ void __launch_bounds__(kFinWarps * 32)
 {
     pdl_wait_primary();
     extern __shared__ int32_t fin_amax[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t r = static_cast<int64_t>(blockIdx.x) * kFinWarps + warp;
-    if (r >= R) return;
+    __shared__ uint32_t st_shared;
+    const int64_t r = blockIdx.x;
     const int32_t rpr = branches == 1 ? k + 1 : 2 * k + 1;
-    int32_t* amax = fin_amax + warp * rpr;
+    if (threadIdx.x == 0) st_shared = 0;
+    __syncthreads();
     uint32_t st = 0;
-    for (int32_t i = lane; i < rpr; i += 32) {
+    for (int32_t i = threadIdx.x; i < rpr; i += kFinThreads) {
         const ArgPartial* p = part + (r * rpr + i) * nseg;
         ArgMax best{-INFINITY, INT32_MAX};
         uint32_t fl = 0;
+#pragma unroll 8
         for (int32_t s = 0; s < nseg; ++s) {
             const ArgPartial q = p[s];
             fl |= q.flags;
             if (argmax_better(q.v, q.i, best)) best = ArgMax{q.v, q.i};
         }
-        amax[i] = best.i == INT32_MAX ? 0 : best.i;
+        fin_amax[i] = best.i == INT32_MAX ? 0 : best.i;
         if ((fl & kFlagNaN) || isinf(best.v)) st |= SV_ST_BAD_LOGITS;
         if (fl & kFlagTimeout) st |= SV_ST_TIMEOUT;
     }
-    __syncwarp();
+    if (st) atomicOr(&st_shared, st);
+    __syncthreads();
+    if (threadIdx.x >= 32) return;
+    const int lane = threadIdx.x;
+    const int32_t* amax = fin_amax;
+    st = 0;
     int32_t best_b = 0, best_n = 0;
     bool any = false;
     for (int32_t b = 0; b < branches; ++b) {
@@ -259,7 +308,7 @@ __global__ void __launch_bounds__(kFinWarps * 32)
     const int32_t fix = amax[branch_row(best_b, best_n, k)];
     for (int32_t j = lane; j <= k; j += 32)
         tokens[r * (k + 1) + j] = j < best_n ? d[j] : (j == best_n ? fix : -1);
-    st = __reduce_or_sync(0xffffffffu, st);
+    st = __reduce_or_sync(0xffffffffu, st) | st_shared;
     if (lane == 0) {
         accept_len[r] = best_n;
         if (branch_out) branch_out[r] = best_b;
@@ -304,9 +353,9 @@ cudaError_t launch_verify_greedy(const Rows& target, int32_t R, int32_t k, int32
 
     const int32_t rpr = branches == 2 ? 2 * k + 1 : k + 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>((R + kFinWarps - 1) / kFinWarps));
-    cfg.blockDim = dim3(kFinWarps * 32);
-    cfg.dynamicSmemBytes = static_cast<size_t>(kFinWarps) * rpr * sizeof(int32_t);
+    cfg.gridDim = dim3(static_cast<unsigned>(R));
+    cfg.blockDim = dim3(kFinThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(rpr) * sizeof(int32_t);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
