@@ -128,6 +128,32 @@ int sv_verify_greedy(sv_rows target, int32_t R, int32_t k, int32_t branches,
                      size_t workspace_bytes, sv_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * sv_verify_greedy_noalloc -- sv_verify_greedy without a workspace argument.
+ * The source pages have no counterpart; this is a convenience for callers
+ * that cannot allocate device memory: a plugin whose host framework owns all
+ * GPU memory through its own caching pool, or a serving loop that reserves
+ * every buffer up front and must not allocate while decoding.
+ *
+ * Arguments, outputs and results are those of sv_verify_greedy.  The scratch
+ * lives in a fixed device array of SV_NOALLOC_SCRATCH_BYTES compiled into the
+ * library; every GPU that loads the library keeps it until the process exits.
+ *  - Batches whose workspace (sv_verify_greedy_workspace) exceeds that size
+ *    are rejected with SV_ERR_LIMIT before anything is launched.
+ *  - The first call on a device looks up the array's device address for that
+ *    device (cudaGetSymbolAddress with the device current); make that first
+ *    call before any stream capture.
+ *  - All calls share the one array.  Calls that overlap on the GPU (other
+ *    streams, other host threads) race on it and give wrong results;
+ *    serialise them.  The array keeps the last call's contents, which no
+ *    later call depends on.
+ *  - Calls no cudaMalloc, cudaFree or other allocating routine.
+ * ---------------------------------------------------------------------- */
+#define SV_NOALLOC_SCRATCH_BYTES (8u << 20)
+int sv_verify_greedy_noalloc(sv_rows target, int32_t R, int32_t k, int32_t branches,
+                             const int32_t* draft, int32_t* accept_len, int32_t* tokens,
+                             int32_t* branch, int32_t* status, sv_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * sv_verify_sample -- speculative sampling with a truncated draft vocabulary.
  * Source: "speculative decoding for Omni models", sections 2 and 4.
  *
