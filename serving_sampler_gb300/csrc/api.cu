@@ -139,6 +139,7 @@ int sv_verify_sample(sv_rows target, sv_rows draft_logits, const int32_t* d2t, i
         d = Rows{nullptr, SV_F32, 4, draft_logits.width > 0 ? draft_logits.width : t.width, 0, false};
     }
     if (d2t == nullptr && d.width != t.width) return SV_ERR_SHAPE;
+    if (d2t != nullptr && t.width > sample_max_plan_width()) return SV_ERR_LIMIT;
     if (int rc = check_workspace(workspace, workspace_bytes,
                                  sample_workspace_bytes(R, k, t.width, d.width)))
         return rc;

@@ -1,18 +1,1068 @@
-// placeholder until the sampling kernels land
+// Speculative sampling with a truncated draft vocabulary ("speculative
+// decoding for Omni models", sections 2 and 4).
+//
+// Three kernels per call:
+//   d2t_plan_kernel    one CTA: a bitmap of the d2t image over the target
+//                      vocabulary, per-word prefix counts, and the support
+//                      sorted by target id (xs[pos], js[pos]).  Every later
+//                      pass visits the support in row order, so no pass
+//                      gathers at random from a 300 KB target row.
+//   sample_rows_kernel persistent CTAs, one (request, position) unit at a
+//                      time.  The draft row y_j streams through a ring of
+//                      bulk-copied 16 KB stages into a resident buffer Y
+//                      while its max / sum-exp at T are taken; then the
+//                      target row z_j streams through the same ring: max,
+//                      sum-exp, argmax, NaN/inf flags, and z at the support
+//                      positions (G[pos]).  A second pass over G and Y gives
+//                      TV over the full vocabulary, p(x_j), q(x_j) and the
+//                      accept test u_j < p/q.
+//   race_commit_kernel RC CTAs per request: the accept-length scan, then the
+//                      exponential race argmin E_x / w_x on the one selected
+//                      row (residual max(0, p - q) at the first rejection, or
+//                      p at the bonus row), Philox uniforms per element, CTA
+//                      results merged with a 64-bit atomicMin; the last CTA
+//                      of the request commits the tokens.
+// Temperature scaling works in log2 units: with c = log2(e) / T,
+// p(x) = 2^(z_x c - M) / S where M = max_x z_x c and S = sum 2^(z c - M).
+#include <algorithm>
+#include <cfloat>
+#include <climits>
+
+#include "sv_device.cuh"
 #include "sv_internal.h"
+
 namespace sv {
-size_t sample_workspace_bytes(int64_t, int32_t, int32_t, int32_t) { return 256; }
-cudaError_t launch_verify_sample(const Rows&, const Rows&, const int32_t*, int32_t, int32_t,
-                                 const int32_t*, const uint64_t*, const float*, int32_t*, int32_t*,
-                                 float*, float*, float*, int32_t*, void*, cudaStream_t)
+
+namespace {
+
+constexpr int kPlanThreads = 1024;
+constexpr int kRowThreads = 512;
+constexpr uint32_t kStageBytes = 16384;
+constexpr int kStages = 4;
+constexpr int kRowHeader = 128;
+constexpr uint32_t kSmemBudget = 220 * 1024;
+constexpr int kRaceThreads = 256;
+constexpr int32_t kRaceSeg = 8192;  // elements of the race row per CTA (fp32 q cache: 32 KB)
+constexpr int32_t kMaxPlanWords = 25600;  // d2t mode supports V <= 819,200
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum : uint32_t { kFlagAllNegInf = 8u, kFlagDraftBad = 16u, kFlagOffSupport = 32u };
+
+struct D2tPlan {
+    uint32_t* bitmap;  // [nw] support bits over target ids
+    int32_t* prefix;   // [nw + 1] set bits before each word
+    int32_t* xs;       // [Vd] support target ids, ascending
+    int32_t* js;       // [Vd] the draft id of xs[pos]
+    int32_t* bad;      // d2t out of range or repeated
+    int32_t nw;
+};
+
+struct RowStat {
+    float m, s;       // target: max of z c, sum 2^(z c - m)
+    float mq, sq;     // draft row (sampling positions < k)
+    float zx;         // z at the draft token
+    float p, q;       // p(x_j), q(x_j)
+    int32_t amax;     // raw argmax of the target row
+    uint32_t flags;   // kFlag* of the target and draft rows
+    int32_t accept;   // accept decision of position j
+    int32_t pad[2];
+};
+
+struct RaceSlot {
+    unsigned long long best;  // (key bits << 32) | x, minimum over the race CTAs
+    unsigned int count;       // race CTAs done
+    unsigned int pad;
+};
+
+struct SampleArgs {
+    const char* tbase;
+    int64_t tstride;  // bytes
+    int32_t V;
+    const char* dbase;
+    int64_t dstride;  // bytes
+    int32_t Vd;
+    int identity;     // d2t == NULL
+    int tbulk, dbulk; // rows 16-byte aligned
+    D2tPlan plan;
+    int32_t R, k;
+    const int32_t* draft;
+    const uint64_t* seeds;
+    const float* temp;
+    float* tv;
+    float* pd;
+    float* qd;
+    int32_t* accept_len;
+    int32_t* tokens;
+    int32_t* status;
+    RowStat* stats;
+    RaceSlot* race;
+    char* gslots;        // global-memory Y / G buffers when they do not fit in shared memory
+    int64_t gslot_bytes;
+    int smem_mode;
+    int32_t race_ctas;   // CTAs per request in the race
+    int32_t race_seg;    // elements per race CTA
+};
+
+__host__ __device__ inline int64_t align256(int64_t b) { return (b + 255) / 256 * 256; }
+
+template <int DT>
+__device__ __forceinline__ float ld_elem(const char* p, int64_t e)
 {
-    return cudaErrorNotSupported;
+    if constexpr (DT == SV_BF16) {
+        const uint16_t h = reinterpret_cast<const uint16_t*>(p)[e];
+        return __uint_as_float(static_cast<uint32_t>(h) << 16);
+    } else {
+        return reinterpret_cast<const float*>(p)[e];
+    }
 }
-size_t cfg_workspace_bytes(int64_t, int32_t, int32_t, int32_t) { return 256; }
-cudaError_t launch_cfg_merge_sample(const Rows&, const Rows&, const CfgShape&, const Rows*, int32_t,
-                                    int32_t, const int32_t*, const uint64_t*, const float*, int32_t*,
-                                    int32_t*, float*, int32_t*, void*, cudaStream_t)
+
+template <int DT>
+__device__ __forceinline__ void st_elem(char* p, int64_t e, float v)
 {
-    return cudaErrorNotSupported;
+    if constexpr (DT == SV_BF16) {
+        reinterpret_cast<uint16_t*>(p)[e] = static_cast<uint16_t>(__float_as_uint(v) >> 16);
+    } else {
+        reinterpret_cast<float*>(p)[e] = v;
+    }
 }
+
+// number of support ids below x (x in [0, V])
+__device__ __forceinline__ int32_t support_rank(const D2tPlan& pl, int32_t x)
+{
+    const int32_t w = x >> 5, b = x & 31;
+    int32_t r = pl.prefix[w];
+    if (b) r += __popc(pl.bitmap[w] & ((1u << b) - 1u));
+    return r;
+}
+
+__device__ __forceinline__ bool in_support(const D2tPlan& pl, int32_t x)
+{
+    return (pl.bitmap[x >> 5] >> (x & 31)) & 1u;
+}
+
+// ---- block reductions (kRowThreads or kRaceThreads, any multiple of 32) ----
+template <int NT>
+__device__ __forceinline__ float block_sum(float v, float* scratch)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int w = threadIdx.x >> 5;
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) scratch[w] = v;
+    __syncthreads();
+    float t = 0.f;
+    for (int i = 0; i < NT / 32; ++i) t += scratch[i];
+    return t;
+}
+
+template <int NT>
+__device__ __forceinline__ float block_max(float v, float* scratch)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    const int w = threadIdx.x >> 5;
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) scratch[w] = v;
+    __syncthreads();
+    float t = -INFINITY;
+    for (int i = 0; i < NT / 32; ++i) t = fmaxf(t, scratch[i]);
+    return t;
+}
+
+template <int NT>
+__device__ __forceinline__ uint32_t block_or(uint32_t v, uint32_t* scratch)
+{
+    v = __reduce_or_sync(0xffffffffu, v);
+    const int w = threadIdx.x >> 5;
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) scratch[w] = v;
+    __syncthreads();
+    uint32_t t = 0;
+    for (int i = 0; i < NT / 32; ++i) t |= scratch[i];
+    return t;
+}
+
+// (value, first position) maximum over the block
+template <int NT>
+__device__ __forceinline__ void block_argmax(float& v, int32_t& x, float* sv, int32_t* sx)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+        const int32_t ox = __shfl_xor_sync(0xffffffffu, x, o);
+        if (ov > v || (ov == v && ox < x)) {
+            v = ov;
+            x = ox;
+        }
+    }
+    const int w = threadIdx.x >> 5;
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) {
+        sv[w] = v;
+        sx[w] = x;
+    }
+    __syncthreads();
+    v = sv[0];
+    x = sx[0];
+    for (int i = 1; i < NT / 32; ++i)
+        if (sv[i] > v || (sv[i] == v && sx[i] < x)) {
+            v = sv[i];
+            x = sx[i];
+        }
+}
+
+// ---- online (max, sum 2^(t - max)) over scaled logits t ----------------------
+struct Lse {
+    float m, s;
+};
+
+// target row: max, sum, and the sum over ids outside the d2t support
+struct Lse3 {
+    float m, s, so;
+};
+
+// values of one 16-byte vector, NaN replaced by -inf; returns the max and
+// whether a NaN was seen
+template <int DT>
+__device__ __forceinline__ int unpack_vec(uint4 q, float* f)
+{
+    if constexpr (DT == SV_BF16) {
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            f[2 * e] = bf16_lo(w[e]);
+            f[2 * e + 1] = bf16_hi(w[e]);
+        }
+        return 8;
+    } else {
+        f[0] = __uint_as_float(q.x);
+        f[1] = __uint_as_float(q.y);
+        f[2] = __uint_as_float(q.z);
+        f[3] = __uint_as_float(q.w);
+        return 4;
+    }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// d2t plan
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kPlanThreads)
+    d2t_plan_kernel(const int32_t* __restrict__ d2t, int32_t Vd, int32_t V, D2tPlan pl)
+{
+    extern __shared__ uint32_t plan_smem[];
+    uint32_t* bits = plan_smem;
+    int32_t* pref = reinterpret_cast<int32_t*>(plan_smem + pl.nw);
+    __shared__ int32_t warp_tot[kPlanThreads / 32];
+    __shared__ int bad_any;
+    const int tid = threadIdx.x;
+    pdl_launch_dependents();  // the row kernel streams rows while the plan is built
+    if (tid == 0) bad_any = 0;
+    for (int32_t w = tid; w < pl.nw; w += kPlanThreads) bits[w] = 0u;
+    __syncthreads();
+    int bad = 0;
+    for (int32_t j = tid; j < Vd; j += kPlanThreads) {
+        const int32_t x = d2t[j];
+        if (x < 0 || x >= V) {
+            bad = 1;
+            continue;
+        }
+        const uint32_t bit = 1u << (x & 31);
+        if (atomicOr(&bits[x >> 5], bit) & bit) bad = 1;
+    }
+    if (bad) atomicOr(&bad_any, 1);
+    __syncthreads();
+    // exclusive prefix of popcounts, each thread owning a contiguous block of words
+    const int32_t per = (pl.nw + kPlanThreads - 1) / kPlanThreads;
+    const int32_t w0 = min(pl.nw, tid * per), w1 = min(pl.nw, w0 + per);
+    int32_t local = 0;
+    for (int32_t w = w0; w < w1; ++w) local += __popc(bits[w]);
+    int32_t incl = local;
+    const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int32_t before = 0;
+    for (int i = 0; i < warp; ++i) before += warp_tot[i];
+    int32_t run = before + incl - local;
+    for (int32_t w = w0; w < w1; ++w) {
+        pref[w] = run;
+        run += __popc(bits[w]);
+    }
+    if (tid == kPlanThreads - 1) pref[pl.nw] = before + incl;  // total
+    __syncthreads();
+    for (int32_t w = tid; w < pl.nw; w += kPlanThreads) {
+        pl.bitmap[w] = bits[w];
+        pl.prefix[w] = pref[w];
+    }
+    if (tid == 0) {
+        pl.prefix[pl.nw] = pref[pl.nw];
+        *pl.bad = bad_any;
+    }
+    for (int32_t j = tid; j < Vd; j += kPlanThreads) {
+        const int32_t x = d2t[j];
+        if (x < 0 || x >= V) continue;
+        const int32_t w = x >> 5, b = x & 31;
+        const int32_t pos = pref[w] + (b ? __popc(bits[w] & ((1u << b) - 1u)) : 0);
+        if (pos >= 0 && pos < Vd) {
+            pl.xs[pos] = x;
+            pl.js[pos] = j;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// row pass
+// ---------------------------------------------------------------------------
+namespace {
+
+// One chunk of a row: bytes [off, off + nb) of the row, nb multiple of 16.
+struct ChunkRef {
+    const char* src;
+    uint32_t nb;
+};
+
+__device__ __forceinline__ void issue_chunk(unsigned char* stage, uint64_t* bar, ChunkRef c, uint64_t pol,
+                                            uint32_t& issued)
+{
+    ++issued;
+    mbar_arrive_expect_tx(bar, c.nb);
+    bulk_copy_g2s(stage, c.src, c.nb, bar, pol);
+}
+
+}  // namespace
+
+template <int DT, int DD>
+__global__ void __launch_bounds__(kRowThreads, 1) sample_rows_kernel(SampleArgs A)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    unsigned char* ring = smem + kRowHeader;
+    constexpr int ET = DT == SV_BF16 ? 2 : 4;
+    constexpr int ED = DD == SV_BF16 ? 2 : 4;
+    constexpr int VT = 16 / ET;
+    constexpr int VD = 16 / ED;
+    __shared__ float red_f[kRowThreads / 32];
+    __shared__ int32_t red_i[kRowThreads / 32];
+    __shared__ uint32_t red_u[kRowThreads / 32];
+    __shared__ float zx_shared;
+    const int tid = threadIdx.x;
+
+    pdl_launch_dependents();
+
+    // resident buffers of the draft row (Y, draft dtype) and of the target
+    // logits at the support positions (G, target dtype)
+    char* Y;
+    char* G;
+    if (A.smem_mode) {
+        Y = reinterpret_cast<char*>(ring + kStages * kStageBytes);
+        G = Y + align256(static_cast<int64_t>(A.Vd) * ED);
+    } else {
+        Y = A.gslots + static_cast<int64_t>(blockIdx.x) * A.gslot_bytes;
+        G = Y + align256(static_cast<int64_t>(A.Vd) * ED);
+    }
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const uint64_t pol = l2_policy_evict_first();
+    uint32_t gchunk = 0;   // chunks consumed by this CTA so far (stage / parity)
+    uint32_t gissued = 0;  // chunks issued (thread 0 only)
+    bool plan_ready = A.identity != 0;
+    uint32_t timeout = 0;
+
+    const int64_t units = static_cast<int64_t>(A.R) * (A.k + 1);
+    for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
+        const int32_t r = static_cast<int32_t>(unit / (A.k + 1));
+        const int32_t j = static_cast<int32_t>(unit - static_cast<int64_t>(r) * (A.k + 1));
+        const float T = A.temp[r];
+        const bool sampling = T > 0.f;
+        const bool has_draft = sampling && j < A.k;
+        const float c = sampling ? kLog2e / T : 0.f;
+        const char* trow = A.tbase + unit * A.tstride;
+        const char* drow = has_draft ? A.dbase + (static_cast<int64_t>(r) * A.k + j) * A.dstride : nullptr;
+        const int32_t xj = has_draft ? A.draft[static_cast<int64_t>(r) * A.k + j] : -1;
+
+        if (j == 0 && tid == 0) {
+            A.race[r].best = ~0ull;
+            A.race[r].count = 0u;
+        }
+        // chunk list: draft bulk chunks, then target bulk chunks
+        const uint32_t dbulk = has_draft && A.dbulk ? (static_cast<uint32_t>(A.Vd) * ED) & ~15u : 0u;
+        const uint32_t tbulk = A.tbulk ? (static_cast<uint32_t>(A.V) * ET) & ~15u : 0u;
+        const uint32_t nd = (dbulk + kStageBytes - 1) / kStageBytes;
+        const uint32_t nt = (tbulk + kStageBytes - 1) / kStageBytes;
+        const uint32_t nchunks = nd + nt;
+        auto chunk_ref = [&](uint32_t i) -> ChunkRef {
+            if (i < nd) return ChunkRef{drow + i * kStageBytes, min(kStageBytes, dbulk - i * kStageBytes)};
+            const uint32_t t = i - nd;
+            return ChunkRef{trow + t * kStageBytes, min(kStageBytes, tbulk - t * kStageBytes)};
+        };
+        if (tid == 0) zx_shared = NAN;
+        __syncthreads();  // every thread is done with the ring of the previous unit
+        if (tid == 0) {
+            for (uint32_t i = 0; i < nchunks && i < kStages; ++i)
+                issue_chunk(ring + ((gchunk + i) % kStages) * kStageBytes, &full[(gchunk + i) % kStages],
+                            chunk_ref(i), pol, gissued);
+        }
+
+        Lse dl{-INFINITY, 0.f};
+        uint32_t dflags = 0;
+        // ---- draft row: max / sum-exp, copy into Y --------------------------
+        if (has_draft) {
+            for (uint32_t i = 0; i < nd; ++i) {
+                const uint32_t g = gchunk + i, s = g % kStages;
+                if (!timeout && !mbar_wait_bounded(&full[s], (g / kStages) & 1u)) timeout = 1;
+                const ChunkRef cr = chunk_ref(i);
+                const uint4* vp = reinterpret_cast<const uint4*>(ring + s * kStageBytes);
+                const int nv = static_cast<int>(cr.nb / 16);
+                const int32_t e0 = static_cast<int32_t>(i * kStageBytes / ED);
+                for (int v = tid; v < nv; v += kRowThreads) {
+                    const uint4 q = vp[v];
+                    *reinterpret_cast<uint4*>(Y + (static_cast<int64_t>(e0) + v * VD) * ED) = q;
+                    float f[8];
+                    const int n = unpack_vec<DD>(q, f);
+                    float mx = -INFINITY;
+                    for (int e = 0; e < n; ++e) {
+                        if (f[e] != f[e]) {
+                            dflags |= kFlagNaN;
+                            f[e] = -INFINITY;
+                        }
+                        if (f[e] == INFINITY) dflags |= kFlagPosInf;
+                        mx = fmaxf(mx, f[e]);
+                    }
+                    const float mt = mx * c;
+                    if (mt > -INFINITY) {
+                        if (mt > dl.m) {
+                            dl.s = dl.m == -INFINITY ? 0.f : dl.s * exp2f(dl.m - mt);
+                            dl.m = mt;
+                        }
+                        float acc = 0.f;
+                        for (int e = 0; e < n; ++e) acc += exp2f(fmaf(f[e], c, -dl.m));
+                        dl.s += acc;
+                    }
+                }
+                __syncthreads();
+                if (tid == 0 && i + kStages < nchunks) {
+                    const uint32_t g2 = gchunk + i + kStages;
+                    issue_chunk(ring + (g2 % kStages) * kStageBytes, &full[g2 % kStages], chunk_ref(i + kStages), pol, gissued);
+                }
+            }
+            // unaligned draft rows, or the sub-16-byte tail
+            for (int32_t e = static_cast<int32_t>(dbulk / ED) + tid; e < A.Vd; e += kRowThreads) {
+                float f = ld_elem<DD>(drow, e);
+                st_elem<DD>(Y, e, f);
+                if (f != f) {
+                    dflags |= kFlagNaN;
+                    f = -INFINITY;
+                }
+                if (f == INFINITY) dflags |= kFlagPosInf;
+                const float t = f * c;
+                if (t > -INFINITY) {
+                    if (t > dl.m) {
+                        dl.s = dl.m == -INFINITY ? 0.f : dl.s * exp2f(dl.m - t);
+                        dl.m = t;
+                    }
+                    dl.s += exp2f(t - dl.m);
+                }
+            }
+        }
+
+        // ---- target row -------------------------------------------------
+        if (has_draft && !plan_ready) {
+            pdl_wait_primary();  // the d2t plan is complete
+            plan_ready = true;
+        }
+        Lse3 tl{-INFINITY, 0.f, 0.f};
+        const bool track_off = has_draft && !A.identity;
+        float bv = -INFINITY;  // argmax: value and the first index of its vector
+        int32_t bx = INT32_MAX;
+        uint32_t tflags = 0;
+        for (uint32_t i = nd; i < nchunks; ++i) {
+            const uint32_t g = gchunk + i, s = g % kStages;
+            if (!timeout && !mbar_wait_bounded(&full[s], (g / kStages) & 1u)) timeout = 1;
+            const ChunkRef cr = chunk_ref(i);
+            const unsigned char* st = ring + s * kStageBytes;
+            const uint4* vp = reinterpret_cast<const uint4*>(st);
+            const int nv = static_cast<int>(cr.nb / 16);
+            const int32_t x0 = static_cast<int32_t>((i - nd) * kStageBytes / ET);
+            for (int v = tid; v < nv; v += kRowThreads) {
+                float f[8];
+                const int n = unpack_vec<DT>(vp[v], f);
+                float mx = -INFINITY;
+                for (int e = 0; e < n; ++e) {
+                    if (f[e] != f[e]) {
+                        tflags |= kFlagNaN;
+                        f[e] = -INFINITY;
+                    }
+                    mx = fmaxf(mx, f[e]);
+                }
+                const bool up = mx > bv;
+                bv = up ? mx : bv;
+                bx = up ? x0 + v * VT : bx;
+                if (sampling) {
+                    const float mt = mx * c;
+                    if (mt > -INFINITY) {
+                        if (mt > tl.m) {
+                            const float sc = tl.m == -INFINITY ? 0.f : exp2f(tl.m - mt);
+                            tl.s *= sc;
+                            tl.so *= sc;
+                            tl.m = mt;
+                        }
+                        float acc = 0.f, acc_off = 0.f;
+                        if (track_off) {
+                            // support bits of the n ids of this vector (n divides 32)
+                            const int32_t x = x0 + v * VT;
+                            const uint32_t bits = A.plan.bitmap[x >> 5] >> (x & 31);
+                            for (int e = 0; e < n; ++e) {
+                                const float ex = exp2f(fmaf(f[e], c, -tl.m));
+                                acc += ex;
+                                acc_off += ((bits >> e) & 1u) ? 0.f : ex;
+                            }
+                        } else {
+                            for (int e = 0; e < n; ++e) acc += exp2f(fmaf(f[e], c, -tl.m));
+                        }
+                        tl.s += acc;
+                        tl.so += acc_off;
+                    }
+                }
+            }
+            const int32_t ne = static_cast<int32_t>(cr.nb / ET);
+            if (has_draft) {
+                // the support positions inside this chunk, in ascending order
+                if (A.identity) {
+                    for (int32_t e = tid; e < ne; e += kRowThreads) {
+                        if constexpr (DT == SV_BF16)
+                            reinterpret_cast<uint16_t*>(G)[x0 + e] = reinterpret_cast<const uint16_t*>(st)[e];
+                        else
+                            reinterpret_cast<float*>(G)[x0 + e] = reinterpret_cast<const float*>(st)[e];
+                    }
+                } else {
+                    const int32_t p0 = support_rank(A.plan, x0), p1 = support_rank(A.plan, x0 + ne);
+                    for (int32_t p = p0 + tid; p < p1; p += kRowThreads) {
+                        const int32_t le = A.plan.xs[p] - x0;
+                        if (le >= 0 && le < ne) {
+                            if constexpr (DT == SV_BF16)
+                                reinterpret_cast<uint16_t*>(G)[p] = reinterpret_cast<const uint16_t*>(st)[le];
+                            else
+                                reinterpret_cast<float*>(G)[p] = reinterpret_cast<const float*>(st)[le];
+                        }
+                    }
+                }
+                if (xj >= x0 && xj < x0 + ne && tid == 0)
+                    zx_shared = ld_elem<DT>(reinterpret_cast<const char*>(st), xj - x0);
+            }
+            __syncthreads();
+            if (tid == 0 && i + kStages < nchunks) {
+                const uint32_t g2 = gchunk + i + kStages;
+                issue_chunk(ring + (g2 % kStages) * kStageBytes, &full[g2 % kStages], chunk_ref(i + kStages), pol, gissued);
+            }
+        }
+        gchunk += nchunks;
+        // unaligned target rows, or the sub-16-byte tail
+        const int32_t tb0 = static_cast<int32_t>(tbulk / ET);
+        for (int32_t e = tb0 + tid; e < A.V; e += kRowThreads) {
+            float f = ld_elem<DT>(trow, e);
+            if (f != f) {
+                tflags |= kFlagNaN;
+                f = -INFINITY;
+            }
+            if (f > bv) {
+                bv = f;
+                bx = e;
+            }
+            if (sampling) {
+                const float t = f * c;
+                if (t > -INFINITY) {
+                    if (t > tl.m) {
+                        const float sc = tl.m == -INFINITY ? 0.f : exp2f(tl.m - t);
+                        tl.s *= sc;
+                        tl.so *= sc;
+                        tl.m = t;
+                    }
+                    const float ex = exp2f(fmaf(f, c, -tl.m));
+                    tl.s += ex;
+                    if (track_off && !in_support(A.plan, e)) tl.so += ex;
+                }
+            }
+            if (has_draft) {
+                if (A.identity) {
+                    st_elem<DT>(G, e, f);
+                } else if (in_support(A.plan, e)) {
+                    st_elem<DT>(G, support_rank(A.plan, e), f);
+                }
+                if (e == xj) zx_shared = f;
+            }
+        }
+
+        // ---- reductions ---------------------------------------------------
+        block_argmax<kRowThreads>(bv, bx, red_f, red_i);
+        const uint32_t fl_t = block_or<kRowThreads>(tflags, red_u);
+        const uint32_t fl_d = block_or<kRowThreads>(dflags, red_u);
+        int32_t amax = 0;
+        if (bx != INT32_MAX) {
+            amax = bx;
+            // first element equal to the maximum inside the winning vector
+            for (int e = 0; e < VT; ++e) {
+                const int32_t x = bx + e;
+                if (x >= A.V) break;
+                if (ld_elem<DT>(trow, x) == bv) {
+                    amax = x;
+                    break;
+                }
+            }
+        }
+        Lse T2{-INFINITY, 0.f}, D2{-INFINITY, 0.f};
+        float s_off = 0.f;  // target mass outside the d2t support, unnormalised
+        if (sampling) {
+            const float M = block_max<kRowThreads>(tl.m, red_f);
+            const float sc = (tl.m == -INFINITY || M == -INFINITY) ? 0.f : exp2f(tl.m - M);
+            T2 = Lse{M, block_sum<kRowThreads>(tl.s * sc, red_f)};
+            if (track_off) s_off = block_sum<kRowThreads>(tl.so * sc, red_f);
+        }
+        if (has_draft) {
+            const float M = block_max<kRowThreads>(dl.m, red_f);
+            const float part = dl.m == -INFINITY ? 0.f : dl.s * exp2f(dl.m - M);
+            D2 = Lse{M, block_sum<kRowThreads>(M == -INFINITY ? 0.f : part, red_f)};
+        }
+        uint32_t flags = 0;
+        if (fl_t & kFlagNaN) flags |= kFlagNaN;
+        if (bv == INFINITY) flags |= kFlagPosInf;
+        if (bv == -INFINITY) flags |= kFlagAllNegInf;
+        if (has_draft && ((fl_d & (kFlagNaN | kFlagPosInf)) || D2.m == -INFINITY)) flags |= kFlagDraftBad;
+        if (timeout) flags |= kFlagTimeout;
+
+        // ---- TV over the full vocabulary, p(x_j), q(x_j), accept -------------
+        float tvv = NAN, pj = NAN, qj = NAN;
+        int32_t acc = 0;
+        if (has_draft) {
+            __syncthreads();  // G and Y complete
+            const float invS = 1.f / T2.s, invSq = 1.f / D2.s;
+            float a_abs = 0.f;
+            const int32_t nsup = A.identity ? A.V : A.plan.prefix[A.plan.nw];
+            for (int32_t p = tid; p < nsup; p += kRowThreads) {
+                const int32_t jd = A.identity ? p : A.plan.js[p];
+                if (jd < 0 || jd >= A.Vd) continue;
+                float z = ld_elem<DT>(G, p);
+                float y = ld_elem<DD>(Y, jd);
+                z = z != z ? -INFINITY : z;
+                y = y != y ? -INFINITY : y;
+                const float pp = exp2f(fmaf(z, c, -T2.m)) * invS;
+                const float qq = exp2f(fmaf(y, c, -D2.m)) * invSq;
+                a_abs += fabsf(pp - qq);
+            }
+            a_abs = block_sum<kRowThreads>(a_abs, red_f);
+            // TV over the full vocabulary: the support terms plus p's mass off the
+            // support, summed directly (1 - sum_support p would cancel)
+            tvv = 0.5f * (a_abs + s_off * invS);
+            if (tid == 0) {
+                const bool in_range = xj >= 0 && xj < A.V;
+                float zx = zx_shared;
+                zx = zx != zx ? -INFINITY : zx;
+                pj = in_range ? exp2f(fmaf(zx, c, -T2.m)) * invS : 0.f;
+                qj = 0.f;
+                if (in_range && (A.identity || in_support(A.plan, xj))) {
+                    const int32_t jd = A.identity ? xj : A.plan.js[support_rank(A.plan, xj)];
+                    if (jd >= 0 && jd < A.Vd) {
+                        float y = ld_elem<DD>(Y, jd);
+                        y = y != y ? -INFINITY : y;
+                        qj = exp2f(fmaf(y, c, -D2.m)) * invSq;
+                    }
+                }
+                if (qj > 0.f) {
+                    const uint4 w = philox_block(philox_key(A.seeds[r]), 0u, static_cast<uint32_t>(j), kTagAccept);
+                    const float u = uniform_from_word(w.x);
+                    acc = u < __fdiv_rn(pj, qj) ? 1 : 0;
+                } else if (in_range) {
+                    flags |= kFlagOffSupport;
+                }
+            }
+        }
+        if (tid == 0) {
+            RowStat rs;
+            rs.m = T2.m;
+            rs.s = T2.s;
+            rs.mq = D2.m;
+            rs.sq = D2.s;
+            rs.zx = zx_shared;
+            rs.p = pj;
+            rs.q = qj;
+            rs.amax = amax;
+            rs.flags = flags;
+            rs.accept = acc;
+            rs.pad[0] = rs.pad[1] = 0;
+            A.stats[unit] = rs;
+            if (j < A.k) {
+                const int64_t o = static_cast<int64_t>(r) * A.k + j;
+                if (A.tv) A.tv[o] = tvv;
+                if (A.pd) A.pd[o] = pj;
+                if (A.qd) A.qd[o] = qj;
+            }
+        }
+    }
+    // Completion of this grid must imply completion of the plan kernel, which
+    // the race kernel reads after waiting on this grid only.
+    if (!plan_ready) pdl_wait_primary();
+    if (timeout && tid == 0) {
+        // give copies that may still be in flight a bounded chance to land
+        for (uint32_t g = gissued > kStages ? gissued - kStages : 0; g < gissued; ++g)
+            (void)mbar_wait_bounded(&full[g % kStages], (g / kStages) & 1u);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// scan + race + commit
+// ---------------------------------------------------------------------------
+namespace {
+
+// -ln(1 - v) for v = 1 - u in (0, 1), accurate also for tiny v
+__device__ __forceinline__ float neg_log_u(float v) { return -log1pf(-v); }
+
+__device__ __forceinline__ unsigned long long pack_key(float key, int32_t x)
+{
+    return (static_cast<unsigned long long>(__float_as_uint(key)) << 32) | static_cast<uint32_t>(x);
+}
+
+}  // namespace
+
+// race over row elements [x0, x1) of one request: returns this thread's best
+// (key, x).  w_x = p(x) - q(x) (residual) or p(x) (bonus); qloc holds q on
+// [x0, x1) for the residual race.
+template <int DT>
+__device__ __forceinline__ void race_range(const char* trow, int32_t x0, int32_t x1, float c, float M,
+                                           float invS, const float* qloc, bool residual, PhiloxKey key,
+                                           uint32_t row, uint32_t tag, float& best, int32_t& bx)
+{
+    // groups of 4 elements share one Philox block (counter x >> 2)
+    const int32_t g0 = x0 >> 2, g1 = (x1 + 3) >> 2;
+    for (int32_t g = g0 + static_cast<int32_t>(threadIdx.x); g < g1; g += kRaceThreads) {
+        const uint4 w4 = philox_block(key, static_cast<uint32_t>(g), row, tag);
+        const uint32_t words[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int32_t x = 4 * g + e;
+            if (x < x0 || x >= x1) continue;
+            float z = ld_elem<DT>(trow, x);
+            z = z != z ? -INFINITY : z;
+            float wt = exp2f(fmaf(z, c, -M)) * invS;
+            if (residual) wt = wt - qloc[x - x0];
+            if (!(wt > 0.f)) continue;
+            const float v = one_minus_uniform_from_word(words[e]);
+            if (!(v < best * wt)) continue;  // E >= v, so key >= v / w
+            const float k2 = __fdiv_rn(neg_log_u(v), wt);
+            if (k2 < best || (k2 == best && x < bx)) {
+                best = k2;
+                bx = x;
+            }
+        }
+    }
+}
+
+template <int DT, int DD>
+__global__ void __launch_bounds__(kRaceThreads) race_commit_kernel(SampleArgs A)
+{
+    pdl_wait_primary();
+    __shared__ float qloc[kRaceSeg];
+    __shared__ float red_f[kRaceThreads / 32];
+    __shared__ int32_t red_i[kRaceThreads / 32];
+    __shared__ int last_cta;
+    __shared__ int32_t n_shared;
+    const int tid = threadIdx.x;
+    const int32_t r = static_cast<int32_t>(blockIdx.x / A.race_ctas);
+    const int32_t rc = static_cast<int32_t>(blockIdx.x - static_cast<int64_t>(r) * A.race_ctas);
+    const int32_t k = A.k;
+    const RowStat* st = A.stats + static_cast<int64_t>(r) * (k + 1);
+    const int32_t* d = A.draft + static_cast<int64_t>(r) * k;
+    const float T = A.temp[r];
+
+    // request-level decisions, computed identically by every CTA of the request
+    uint32_t fl = 0;
+    for (int32_t j = tid; j <= k; j += kRaceThreads) fl |= st[j].flags;
+    fl = block_or<kRaceThreads>(fl, reinterpret_cast<uint32_t*>(red_i));
+    const bool bad_rows = (fl & (kFlagNaN | kFlagPosInf | kFlagAllNegInf | kFlagDraftBad)) != 0;
+    const bool greedy = !(T > 0.f) || bad_rows;
+    if (tid == 0) {
+        int32_t n = k;
+        for (int32_t j = 0; j < k; ++j) {
+            const bool ok = greedy ? d[j] == st[j].amax : st[j].accept != 0;
+            if (!ok) {
+                n = j;
+                break;
+            }
+        }
+        n_shared = n;
+    }
+    __syncthreads();
+    const int32_t n = n_shared;
+    int32_t token = -1;
+    uint32_t status = 0;
+    if (greedy) {
+        if (rc != 0) return;
+        token = st[n].amax;
+    } else {
+        const bool residual = n < k;
+        const RowStat& rs = st[n];
+        const float c = kLog2e / T;
+        const int32_t x0 = rc * A.race_seg, x1 = min(A.V, x0 + A.race_seg);
+        const char* trow = A.tbase + (static_cast<int64_t>(r) * (k + 1) + n) * A.tstride;
+        if (residual) {
+            for (int32_t i = tid; i < x1 - x0; i += kRaceThreads) qloc[i] = 0.f;
+            __syncthreads();
+            const char* drow = A.dbase + (static_cast<int64_t>(r) * k + n) * A.dstride;
+            const float invSq = 1.f / rs.sq;
+            if (A.identity) {
+                for (int32_t x = x0 + tid; x < x1; x += kRaceThreads) {
+                    float y = ld_elem<DD>(drow, x);
+                    y = y != y ? -INFINITY : y;
+                    qloc[x - x0] = exp2f(fmaf(y, c, -rs.mq)) * invSq;
+                }
+            } else if (x0 < x1) {
+                const int32_t p0 = support_rank(A.plan, x0), p1 = support_rank(A.plan, x1);
+                for (int32_t p = p0 + tid; p < p1; p += kRaceThreads) {
+                    const int32_t x = A.plan.xs[p], jd = A.plan.js[p];
+                    if (x < x0 || x >= x1 || jd < 0 || jd >= A.Vd) continue;
+                    float y = ld_elem<DD>(drow, jd);
+                    y = y != y ? -INFINITY : y;
+                    qloc[x - x0] = exp2f(fmaf(y, c, -rs.mq)) * invSq;
+                }
+            }
+            __syncthreads();
+        }
+        float best = INFINITY;
+        int32_t bx = INT32_MAX;
+        race_range<DT>(trow, x0, x1, c, rs.m, 1.f / rs.s, qloc, residual, philox_key(A.seeds[r]),
+                       static_cast<uint32_t>(n), residual ? kTagResidual : kTagBonus, best, bx);
+        // (key, lowest x) minimum over the CTA
+        float nb = -best;
+        int32_t nx = bx;
+        // reuse the argmax reduction on (-key, x): larger -key = smaller key
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, nb, o);
+            const int32_t ox = __shfl_xor_sync(0xffffffffu, nx, o);
+            if (ov > nb || (ov == nb && ox < nx)) {
+                nb = ov;
+                nx = ox;
+            }
+        }
+        if ((tid & 31) == 0) {
+            red_f[tid >> 5] = nb;
+            red_i[tid >> 5] = nx;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            for (int i = 1; i < kRaceThreads / 32; ++i)
+                if (red_f[i] > nb || (red_f[i] == nb && red_i[i] < nx)) {
+                    nb = red_f[i];
+                    nx = red_i[i];
+                }
+            RaceSlot* slot = A.race + r;
+            if (nx != INT32_MAX) atomicMin(&slot->best, pack_key(-nb, nx));
+            __threadfence();
+            const unsigned prev = atomicAdd(&slot->count, 1u);
+            last_cta = prev == static_cast<unsigned>(A.race_ctas - 1);
+        }
+        __syncthreads();
+        if (!last_cta) return;
+        __threadfence();
+        const unsigned long long packed = atomicOr(&A.race[r].best, 0ull);
+        if (packed != ~0ull) {
+            token = static_cast<int32_t>(packed & 0xffffffffull);
+        } else {
+            // no positive residual weight: draw the correction from p (rare)
+            status |= SV_ST_RESIDUAL_ZERO;
+            float b2 = INFINITY;
+            int32_t x2 = INT32_MAX;
+            race_range<DT>(trow, 0, A.V, c, rs.m, 1.f / rs.s, qloc, false, philox_key(A.seeds[r]),
+                           static_cast<uint32_t>(n), kTagResidual, b2, x2);
+            float nb2 = -b2;
+            block_argmax<kRaceThreads>(nb2, x2, red_f, red_i);
+            token = x2 == INT32_MAX ? 0 : x2;
+        }
+        if (residual && (rs.flags & kFlagOffSupport)) status |= SV_ST_OFF_SUPPORT;
+    }
+    // ---- commit (one CTA per request) ------------------------------------
+    for (int32_t j = tid; j < k; j += kRaceThreads)
+        if (d[j] < 0 || d[j] >= A.V) status |= SV_ST_TOKEN_RANGE;
+    if (fl & kFlagTimeout) status |= SV_ST_TIMEOUT;
+    if (bad_rows) status |= SV_ST_BAD_LOGITS;
+    if (T < 0.f || T != T) status |= SV_ST_BAD_TEMP;
+    if (!A.identity && *A.plan.bad) status |= SV_ST_BAD_D2T;
+    int32_t* out = A.tokens + static_cast<int64_t>(r) * (k + 1);
+    for (int32_t j = tid; j <= k; j += kRaceThreads) out[j] = j < n ? d[j] : (j == n ? token : -1);
+    if (greedy) {
+        // no sampling statistics for greedily verified requests
+        for (int32_t j = tid; j < k; j += kRaceThreads) {
+            const int64_t o = static_cast<int64_t>(r) * k + j;
+            if (A.tv) A.tv[o] = NAN;
+            if (A.pd) A.pd[o] = NAN;
+            if (A.qd) A.qd[o] = NAN;
+        }
+    }
+    status = block_or<kRaceThreads>(status, reinterpret_cast<uint32_t*>(red_i));
+    if (tid == 0) {
+        A.accept_len[r] = n;
+        if (A.status) A.status[r] = static_cast<int32_t>(status);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+namespace {
+
+struct SampleLayout {
+    int64_t plan_bitmap, plan_prefix, plan_xs, plan_js, plan_bad;
+    int64_t stats, race, gslots;
+    int64_t gslot_bytes;
+    int64_t total;
+    int smem_mode;
+    size_t smem_bytes;
+    int grid;
+};
+
+SampleLayout sample_layout(int64_t R, int32_t k, int32_t V, int32_t Vd, int et, int ed, int sms)
+{
+    SampleLayout L{};
+    const int64_t nw = (V + 31) / 32;
+    int64_t off = 0;
+    auto take = [&](int64_t bytes) {
+        const int64_t o = off;
+        off += align256(bytes);
+        return o;
+    };
+    L.plan_bitmap = take(nw * 4);
+    L.plan_prefix = take((nw + 1) * 4);
+    L.plan_xs = take(static_cast<int64_t>(Vd) * 4);
+    L.plan_js = take(static_cast<int64_t>(Vd) * 4);
+    L.plan_bad = take(4);
+    L.stats = take(R * (k + 1) * static_cast<int64_t>(sizeof(RowStat)));
+    L.race = take(R * static_cast<int64_t>(sizeof(RaceSlot)));
+    const int64_t units = R * (k + 1);
+    L.grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(units, sms > 0 ? sms : 148)));
+    const int64_t resident = align256(static_cast<int64_t>(Vd) * ed) + align256(static_cast<int64_t>(Vd) * et);
+    const size_t ring = kRowHeader + static_cast<size_t>(kStages) * kStageBytes;
+    L.smem_mode = ring + resident <= kSmemBudget ? 1 : 0;
+    L.smem_bytes = ring + (L.smem_mode ? resident : 0);
+    L.gslot_bytes = L.smem_mode ? 0 : resident;
+    L.gslots = take(L.smem_mode ? 0 : L.gslot_bytes * L.grid);
+    L.total = off + 256;
+    return L;
+}
+
+}  // namespace
+
+size_t sample_workspace_bytes(int64_t R, int32_t k, int32_t V, int32_t Vd)
+{
+    const int sms = device_sm_count();
+    int64_t best = 0;
+    for (int et : {2, 4})
+        for (int ed : {2, 4}) best = std::max(best, sample_layout(R, k, V, Vd, et, ed, sms).total);
+    return static_cast<size_t>(best);
+}
+
+template <int DT, int DD>
+static cudaError_t launch_sample_t(const Rows& t, const Rows& d, const int32_t* d2t, int32_t R, int32_t k,
+                                   const int32_t* draft, const uint64_t* seeds, const float* temperature,
+                                   int32_t* accept_len, int32_t* tokens, float* tv, float* p_draft,
+                                   float* q_draft, int32_t* status, void* workspace, cudaStream_t stream)
+{
+    const int sms = device_sm_count();
+    const SampleLayout L = sample_layout(R, k, t.width, d.width, t.esize, d.esize, sms);
+    char* ws = static_cast<char*>(workspace);
+    SampleArgs A{};
+    A.tbase = t.data;
+    A.tstride = t.stride * t.esize;
+    A.V = t.width;
+    A.dbase = d.data;
+    A.dstride = d.stride * d.esize;
+    A.Vd = d.width;
+    A.identity = d2t == nullptr;
+    A.tbulk = t.bulk_ok;
+    A.dbulk = d.bulk_ok && d.data != nullptr;
+    A.plan.nw = (t.width + 31) / 32;
+    A.plan.bitmap = reinterpret_cast<uint32_t*>(ws + L.plan_bitmap);
+    A.plan.prefix = reinterpret_cast<int32_t*>(ws + L.plan_prefix);
+    A.plan.xs = reinterpret_cast<int32_t*>(ws + L.plan_xs);
+    A.plan.js = reinterpret_cast<int32_t*>(ws + L.plan_js);
+    A.plan.bad = reinterpret_cast<int32_t*>(ws + L.plan_bad);
+    A.R = R;
+    A.k = k;
+    A.draft = draft;
+    A.seeds = seeds;
+    A.temp = temperature;
+    A.tv = tv;
+    A.pd = p_draft;
+    A.qd = q_draft;
+    A.accept_len = accept_len;
+    A.tokens = tokens;
+    A.status = status;
+    A.stats = reinterpret_cast<RowStat*>(ws + L.stats);
+    A.race = reinterpret_cast<RaceSlot*>(ws + L.race);
+    A.gslots = ws + L.gslots;
+    A.gslot_bytes = L.gslot_bytes;
+    A.smem_mode = L.smem_mode;
+    A.race_seg = kRaceSeg;
+    A.race_ctas = (t.width + kRaceSeg - 1) / kRaceSeg;
+
+    cudaError_t e;
+    if (!A.identity) {
+        const size_t psmem = static_cast<size_t>(2 * A.plan.nw + 1) * 4;
+        e = cudaFuncSetAttribute(d2t_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(psmem));
+        if (e != cudaSuccess) return e;
+        d2t_plan_kernel<<<1, kPlanThreads, psmem, stream>>>(d2t, d.width, t.width, A.plan);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    e = cudaFuncSetAttribute(sample_rows_kernel<DT, DD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(L.smem_bytes));
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(L.grid));
+    cfg.blockDim = dim3(kRowThreads);
+    cfg.dynamicSmemBytes = L.smem_bytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = A.identity ? 0 : 1;
+    e = cudaLaunchKernelEx(&cfg, sample_rows_kernel<DT, DD>, A);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg2 = {};
+    cfg2.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(R) * A.race_ctas));
+    cfg2.blockDim = dim3(kRaceThreads);
+    cfg2.dynamicSmemBytes = 0;
+    cfg2.stream = stream;
+    cfg2.attrs = attr;
+    cfg2.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg2, race_commit_kernel<DT, DD>, A);
+}
+
+cudaError_t launch_verify_sample(const Rows& target, const Rows& draft_logits, const int32_t* d2t,
+                                 int32_t R, int32_t k, const int32_t* draft, const uint64_t* seeds,
+                                 const float* temperature, int32_t* accept_len, int32_t* tokens,
+                                 float* tv, float* p_draft, float* q_draft, int32_t* status,
+                                 void* workspace, cudaStream_t stream)
+{
+    const bool tb = target.dtype == SV_BF16, db = draft_logits.dtype == SV_BF16;
+#define SV_SAMPLE_CALL(A_, B_)                                                                     \
+    launch_sample_t<A_, B_>(target, draft_logits, d2t, R, k, draft, seeds, temperature, accept_len, \
+                            tokens, tv, p_draft, q_draft, status, workspace, stream)
+    if (tb && db) return SV_SAMPLE_CALL(SV_BF16, SV_BF16);
+    if (tb && !db) return SV_SAMPLE_CALL(SV_BF16, SV_F32);
+    if (!tb && db) return SV_SAMPLE_CALL(SV_F32, SV_BF16);
+    return SV_SAMPLE_CALL(SV_F32, SV_F32);
+#undef SV_SAMPLE_CALL
+}
+
+int32_t sample_max_plan_width() { return kMaxPlanWords * 32; }
+
 }  // namespace sv

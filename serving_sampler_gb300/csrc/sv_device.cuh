@@ -153,6 +153,12 @@ __device__ __forceinline__ float uniform_from_word(uint32_t w)
     return __uint_as_float(0x3F800000u | (w >> 9)) - __uint_as_float(0x3F7FFFFFu);
 }
 
+// 1 - u for the same word, also exact: (2 * (2^23 - 1 - (w >> 9)) + 1) * 2^-24
+__device__ __forceinline__ float one_minus_uniform_from_word(uint32_t w)
+{
+    return uniform_from_word(~w);
+}
+
 // counter layout of the library: (x >> 2, row, tag, 0), word x & 3
 enum : uint32_t { kTagAccept = 0, kTagResidual = 1, kTagBonus = 2 };
 

@@ -52,6 +52,9 @@ cudaError_t launch_verify_sample(const Rows& target, const Rows& draft_logits, c
                                  float* tv, float* p_draft, float* q_draft, int32_t* status,
                                  void* workspace, cudaStream_t stream);
 
+// largest target vocabulary accepted together with a d2t map
+int32_t sample_max_plan_width();
+
 struct CfgShape {
     int32_t S, W;
     float w;

@@ -1,0 +1,53 @@
+"""Comparison of the CUDA sampling outputs with the oracle's (test helper).
+
+Tokens, accept lengths and status must be identical except for requests whose
+decision margin is below 1e-6 (|u - p/q| of a tested position, or the
+relative gap between the two smallest race keys), measured by the oracle in
+fp64; those requests are counted.  p(x_j) and q(x_j) must agree within 1e-5
+relative (absolute floor 1e-9, for values near fp32 underflow).  TV must
+agree within 1e-5 relative or 1e-6 absolute: the kernel evaluates every
+probability in fp32 with ~1e-6 relative error (rounding of c = log2(e)/T
+times the logit spread, exp2f's 2 ulp, the normaliser's sum), so a sum of
+|p - q| carries an absolute error of that order however small TV is.
+"""
+import numpy as np
+
+MARGIN = 1e-6
+REL = 1e-5
+ABS_FLOOR = {"tv": 1e-6, "p_draft": 1e-9, "q_draft": 1e-9}
+
+
+def close(got, want, name=""):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    nan_g, nan_w = np.isnan(got), np.isnan(want)
+    assert np.array_equal(nan_g, nan_w), "NaN pattern differs"
+    g, w = got[~nan_w], want[~nan_w]
+    tol = np.maximum(REL * np.abs(w), ABS_FLOOR.get(name, 1e-9))
+    bad = np.abs(g - w) > tol
+    if bad.any():
+        i = np.argmax(np.abs(g - w) - tol)
+        raise AssertionError(f"{name}: {bad.sum()} values off; worst got {g[i]:.9g} want {w[i]:.9g} "
+                             f"(rel {abs(g[i] - w[i]) / max(abs(w[i]), 1e-300):.3g}) at flat index {i}")
+
+
+def compare(got: dict, want: dict, stats=True):
+    """got: CUDA outputs (numpy); want: oracle outputs.  Returns the exempt count."""
+    am = want["accept_margin"]
+    am = am.reshape(am.shape[0], -1) if am.size else np.full((len(want["accept_len"]), 1), np.inf)
+    margin = np.minimum(am.min(axis=1), want["race_margin"].reshape(len(want["accept_len"]), -1).min(axis=1))
+    exempt = margin < MARGIN
+    R = len(want["accept_len"])
+    same = (got["accept_len"] == want["accept_len"]) & np.all(
+        got["tokens"].reshape(R, -1) == want["tokens"].reshape(R, -1), axis=1)
+    if "status" in got:
+        same &= got["status"] == want["status"]
+    bad = ~same & ~exempt
+    assert not bad.any(), (f"{bad.sum()} non-exempt requests differ, e.g. request {np.nonzero(bad)[0][:5]}: "
+                           f"got {got['accept_len'][bad][:5]} {got['tokens'].reshape(R, -1)[bad][:2]} want "
+                           f"{want['accept_len'][bad][:5]} {want['tokens'].reshape(R, -1)[bad][:2]}")
+    if stats:
+        for key in ("tv", "p_draft", "q_draft"):
+            if key in got and key in want:
+                close(got[key], want[key], key)
+    return int(exempt.sum())

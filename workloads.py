@@ -2,7 +2,10 @@
 
 This module only draws inputs: logit rows, draft tokens, maps, seeds and
 temperatures.  It holds none of the verification arithmetic (no softmax,
-acceptance test, TV or sampler); argmax tokens are planted, never searched.
+acceptance test, TV or sampler of the verifier).  Target argmax tokens are
+planted, never searched; draft tokens come from a stand-in drafter that
+draws from its own draft logits (Gumbel-max with torch's generator, or its
+argmax for greedy requests).
 Both the CUDA library's tests/benchmark and the CPU oracle read what it
 produces, so the two sides always see the same bytes.
 
@@ -144,3 +147,72 @@ def host_rows(t: torch.Tensor) -> np.ndarray:
     if t.dtype == torch.bfloat16:
         return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
     return t.detach().cpu().contiguous().numpy()
+
+
+# ---------------------------------------------------------------------------
+# sampling workloads
+# ---------------------------------------------------------------------------
+# Support bias and per-position draft noise of the d2t workload, chosen by
+# oracle/calibrate_d2t.py so that the mean off-support p-mass is about 0.10
+# and the mean single-position acceptance 1 - TV follows the DSpark profile
+# 0.714 ... 0.423 quoted in "speculative decoding for Omni models", section 3.
+D2T_DELTA = 2.73
+D2T_SIGMA = [0.48, 0.71, 0.9, 1.01, 1.12, 1.2, 1.27]
+
+
+def _draw_drafts(g, y: torch.Tensor, T: torch.Tensor, greedy: torch.Tensor) -> torch.Tensor:
+    """Draft ids from draft logits y [n, Vd]: Gumbel-max at temperature T (per row),
+    or the argmax for greedy rows."""
+    u = torch.rand(y.shape, generator=g, device=y.device).clamp_min_(1e-30)
+    gumbel = -torch.log(-torch.log(u))
+    Tpos = torch.where(T > 0, T, torch.ones_like(T)).view(-1, 1)
+    noisy = y / Tpos + gumbel
+    pick = torch.where(greedy.view(-1, 1), y, noisy)
+    return pick.argmax(dim=1)
+
+
+def sample_batch(R: int, k: int, V: int, Vd: int | None = None, dtype=torch.bfloat16, draft_dtype=None,
+                 T=1.0, sigma_pos=1.0, delta: float = 0.0, z_sigma: float = 3.0, seed: int = 0,
+                 seed_base: int = 1234, device="cuda", row_pad: int = 0, d2t_seed: int | None = None):
+    """Target rows [R*(k+1), V], draft rows [R*k, Vd] (= target restricted to the d2t
+    image, plus the support bias, plus N(0, sigma_j^2) noise), d2t (None when Vd is
+    None: identity), drafts x_j drawn from the draft distribution at T, seeds, T."""
+    draft_dtype = draft_dtype or dtype
+    g = _gen(seed, device)
+    rows = R * (k + 1)
+    z = torch.randn(rows, V + row_pad, generator=g, device=device, dtype=torch.float32) * z_sigma
+    d2t = None
+    if Vd is not None:
+        gd = _gen(seed + 7 if d2t_seed is None else d2t_seed, device)
+        d2t = torch.randperm(V, generator=gd, device=device)[:Vd].to(torch.int32)
+        z[:, d2t.long()] += delta
+    else:
+        Vd = V
+    Tt = torch.as_tensor(T, dtype=torch.float32, device=device).expand(R).contiguous()
+    sig = torch.as_tensor(sigma_pos, dtype=torch.float32, device=device).expand(k).contiguous()
+    zr = z.view(R, k + 1, V + row_pad)[:, :k, :V]
+    base = zr if d2t is None else zr[:, :, d2t.long()]
+    noise = torch.randn(base.shape, generator=g, device=device) * sig.view(1, k, 1)
+    y = (base + noise).reshape(R * k, Vd)
+    target = z.to(dtype)
+    if row_pad:
+        target = target[:, :V]
+    draft_logits = y.to(draft_dtype).contiguous()
+    greedy = (Tt <= 0).repeat_interleave(k)
+    ids = _draw_drafts(g, draft_logits.float(), Tt.repeat_interleave(k), greedy)
+    draft = (ids if d2t is None else d2t.long()[ids]).view(R, k).to(torch.int32).contiguous()
+    return dict(target=target, draft_logits=draft_logits, d2t=d2t, draft=draft,
+                seeds=seeds_tensor(seed_base, R, device), temperature=Tt, R=R, k=k, V=V, Vd=Vd)
+
+
+def tiny_sample(device="cuda"):
+    """4 requests x 8 drafts, V = 4096 fp32 ~ N(0, 2^2), draft logits = target + N(0, 1), T = 1, seed 0."""
+    return sample_batch(4, 8, 4096, None, torch.float32, T=1.0, sigma_pos=1.0, z_sigma=2.0, seed=0,
+                        seed_base=0, device=device)
+
+
+def d2t_workload(device="cuda", R: int = 128):
+    """128 requests x 7 drafts (+ bonus), V = 151,936 bf16, draft vocabulary 32,000 via a seeded
+    random injective d2t, T = 0.7, per-request seeds splitmix64(1234 + r)."""
+    return sample_batch(R, 7, V_QWEN, VD_DRAFT, torch.bfloat16, T=0.7, sigma_pos=D2T_SIGMA,
+                        delta=D2T_DELTA, z_sigma=3.0, seed=1237, seed_base=1234, device=device)
