@@ -40,7 +40,8 @@ def _args():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", choices=["listen"], default="listen")
+    ap.add_argument("--workload", choices=["listen", "d2t"], default="listen",
+                    help="listen: greedy verify with a runner-up branch (headline); d2t: speculative sampling")
     ap.add_argument("--sessions", type=int, default=64, help="listen sessions per step (64 = the workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
@@ -161,25 +162,122 @@ class Clocks:
 # ---------------------------------------------------------------------------
 # workloads
 # ---------------------------------------------------------------------------
-def _listen(device, sessions=64):
-    import torch
+class Workload:
+    """Inputs resident on the device, the library call of one step, and the
+    algorithmic bytes it must read."""
 
-    import workloads
+    def __init__(self, name, device, sessions):
+        import torch
 
-    w = workloads.listen(device=device, R=sessions)
-    if torch.cuda.is_available():
-        torch.cuda.empty_cache()  # drop the generator's fp32 temporaries
-    R, k = w["R"], w["k"]
-    rows = R * (2 * k + 1)
-    V = w["V"]
-    logit_bytes = rows * V * 2  # bf16, every row read once
-    return w, dict(R=R, k=k, rows=rows, V=V, logit_bytes=logit_bytes)
+        import serving_sampler_gb300 as sv
+        import workloads
+
+        self.name = name
+        self.sv = sv
+        if name == "listen":
+            w = workloads.listen(device=device, R=sessions)
+            R, k = w["R"], w["k"]
+            self.rows = R * (2 * k + 1)
+            self.logit_bytes = self.rows * w["V"] * 2
+            self.inputs = {"target": w["target"], "draft": w["draft"]}
+            self.out = dict(accept_len=torch.empty(R, dtype=torch.int32, device=device),
+                            tokens=torch.empty(R, k + 1, dtype=torch.int32, device=device),
+                            branch=torch.empty(R, dtype=torch.int32, device=device),
+                            status=torch.empty(R, dtype=torch.int32, device=device))
+            self.ws = torch.empty(sv.verify_greedy_workspace(R, k, 2, w["V"]), dtype=torch.uint8, device=device)
+            self.launches = sv.LAUNCHES["verify_greedy"]
+            self.kernel = "argmax_segments_kernel<bf16>"
+            self.kernel_file = "greedy.cu"
+            self.profile = "argmax_segments_listen.md"
+            self.desc = (f"listen: {R} sessions x (32 main + 32 runner-up drafts) = 65 rows x 151936 bf16 per "
+                         f"session ({self.logit_bytes / 1e9:.3f} GB of logits per step)")
+            self.metric = "verify logit GB/s (speculative-listening greedy verify, V=151936 bf16)"
+        else:
+            w = workloads.d2t_workload(device=device, R=sessions if sessions != 64 else 128)
+            R, k, V, Vd = w["R"], w["k"], w["V"], w["Vd"]
+            self.rows = R * (k + 1)
+            self.logit_bytes = R * (k + 1) * V * 2 + R * k * Vd * 2 + Vd * 4
+            self.inputs = {"target": w["target"], "draft_logits": w["draft_logits"], "d2t": w["d2t"],
+                           "draft": w["draft"], "seeds": w["seeds"], "temperature": w["temperature"]}
+            self.out = dict(accept_len=torch.empty(R, dtype=torch.int32, device=device),
+                            tokens=torch.empty(R, k + 1, dtype=torch.int32, device=device),
+                            status=torch.empty(R, dtype=torch.int32, device=device),
+                            tv=torch.empty(R, k, dtype=torch.float32, device=device),
+                            p_draft=torch.empty(R, k, dtype=torch.float32, device=device),
+                            q_draft=torch.empty(R, k, dtype=torch.float32, device=device))
+            self.ws = torch.empty(sv.verify_sample_workspace(R, k, V, Vd), dtype=torch.uint8, device=device)
+            self.launches = 3
+            self.kernel = "sample_rows_kernel<bf16,bf16> + race_commit_kernel"
+            self.kernel_file = "sample.cu"
+            self.profile = "sample_rows_d2t.md"
+            self.desc = (f"d2t: {R} requests x 7 drafts (+bonus) over V=151936 bf16, draft vocab 32000 bf16 via "
+                         f"d2t, T=0.7 ({self.logit_bytes / 1e9:.3f} GB of logits per step)")
+            self.metric = "verify+sample logit GB/s (speculative sampling, d2t 32000 -> 151936, bf16)"
+        self.w = w
+        if torch.cuda.is_available():
+            torch.cuda.empty_cache()  # drop the generator's fp32 temporaries
+
+    def call(self, inp, stream):
+        w = self.w
+        if self.name == "listen":
+            self.sv.verify_greedy(inp["target"], w["R"], w["k"], 2, inp["draft"], out=self.out, workspace=self.ws,
+                                  stream=stream)
+        else:
+            self.sv.verify_sample(inp["target"], inp["draft_logits"], inp["d2t"], w["R"], w["k"], inp["draft"],
+                                  inp["seeds"], inp["temperature"], out=self.out, workspace=self.ws, stream=stream)
+
+    def _host(self):
+        """CPU copies of the inputs for the oracle (made once)."""
+        if getattr(self, "_h", None) is None:
+            import numpy as np
+
+            import workloads
+
+            w = self.w
+            h = {"target": workloads.host_rows(w["target"]), "draft": w["draft"].cpu().numpy()}
+            if self.name != "listen":
+                h["draft_logits"] = workloads.host_rows(w["draft_logits"])
+                h["d2t"] = w["d2t"].cpu().numpy()
+                h["seeds"] = w["seeds"].cpu().numpy().view(np.uint64)
+                h["T"] = w["temperature"].cpu().numpy()
+            self._h = h
+        return self._h
+
+    def oracle_one(self, r):
+        """Run the oracle on request r; returns (logit bytes, rows) it covered."""
+        import oracle
+
+        w, h = self.w, self._host()
+        k = w["k"]
+        r = r % w["R"]
+        if self.name == "listen":
+            rpr = 2 * k + 1
+            oracle.verify_greedy(h["target"][r * rpr:(r + 1) * rpr], 1, k, 2, h["draft"][r:r + 1])
+            return rpr * w["V"] * 2, rpr
+        oracle.verify_sample(h["target"][r * (k + 1):(r + 1) * (k + 1)], h["draft_logits"][r * k:(r + 1) * k],
+                             h["d2t"], 1, k, h["draft"][r:r + 1], h["seeds"][r:r + 1], h["T"][r:r + 1])
+        return (k + 1) * w["V"] * 2 + k * w["Vd"] * 2, k + 1
+
+    def oracle_sample(self, seconds):
+        """(GB/s, rows/s, requests, seconds) of the oracle over about `seconds` of requests."""
+        self._host()
+        done = nbytes = nrows = 0
+        t0 = time.perf_counter()
+        while True:
+            b, rr = self.oracle_one(done)
+            done += 1
+            nbytes += b
+            nrows += rr
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                break
+        return nbytes / el / 1e9, nrows / el, done, el
 
 
-def _traffic_from_profile(kernel_file):
+def _traffic_from_profile(kernel_file, profile):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current source of the kernel's file; None otherwise."""
-    path = os.path.join(ROOT, "profiles", "argmax_segments_listen.md")
+    path = os.path.join(ROOT, "profiles", profile)
     src = os.path.join(ROOT, "serving_sampler_gb300", "csrc", kernel_file)
     try:
         text = open(path).read()
@@ -192,68 +290,42 @@ def _traffic_from_profile(kernel_file):
     return None
 
 
-# ---------------------------------------------------------------------------
-# the CPU oracle on a bounded sample
-# ---------------------------------------------------------------------------
-def _oracle_sample(host_target, draft_np, meta, seconds, max_requests=None):
-    """Run the oracle request by request until `seconds` of CPU work; returns
-    (GB/s, rows/s, requests done, seconds)."""
-    import oracle
-
-    R, k = meta["R"], meta["k"]
-    rpr = 2 * k + 1
-    done = 0
-    t0 = time.perf_counter()
-    while True:
-        r = done % R
-        oracle.verify_greedy(host_target[r * rpr:(r + 1) * rpr], 1, k, 2, draft_np[r:r + 1])
-        done += 1
-        el = time.perf_counter() - t0
-        if el >= seconds or (max_requests is not None and done >= max_requests):
-            break
-    bytes_done = done * rpr * meta["V"] * 2
-    return bytes_done / el / 1e9, done * rpr / el, done, el
-
-
 def run_reference(a):
     """Reference arm: the fp64 CPU oracle as it stands, one request per step."""
-    world, rank, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0
+    world, rank = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
     import torch
 
-    import workloads
-
-    dev = "cuda" if torch.cuda.is_available() else "cpu"
-    w, meta = _listen(dev, a.sessions)
-    host = workloads.host_rows(w["target"])
-    draft = w["draft"].cpu().numpy()
-    del w
     import oracle
 
     oracle.build()
-    k, rpr = meta["k"], 2 * meta["k"] + 1
-    for s in range(a.warmup):
-        r = s % meta["R"]
-        oracle.verify_greedy(host[r * rpr:(r + 1) * rpr], 1, k, 2, draft[r:r + 1])
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    wl = Workload(a.workload, dev, a.sessions)
+    # one request per step, timed as it stands
+    wl._host()
+    for s_ in range(a.warmup):
+        wl.oracle_one(s_)
+    nbytes = nrows = 0
     t0 = time.perf_counter()
-    for s in range(a.steps):
-        r = s % meta["R"]
-        oracle.verify_greedy(host[r * rpr:(r + 1) * rpr], 1, k, 2, draft[r:r + 1])
+    for s_ in range(a.steps):
+        b, rr = wl.oracle_one(a.warmup + s_)
+        nbytes += b
+        nrows += rr
     el = time.perf_counter() - t0
-    step_bytes = rpr * meta["V"] * 2
-    gbs = a.steps * step_bytes / el / 1e9
+    gbs = nbytes / el / 1e9
+    done = a.steps
     line = {
-        "impl": "reference", "metric": "verify logit GB/s (speculative-listening greedy verify, V=151936 bf16)",
+        "impl": "reference", "metric": wl.metric,
         "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
         "ms_per_step": el / a.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "listen: 64 sessions x (32 main + 32 runner-up drafts), 65 rows x 151936 bf16",
-                   "step": "one session (65 rows) through the CPU oracle", "l2": "n/a (CPU)"},
+        "config": {"workload": wl.desc, "step": "one request of the workload through the CPU oracle",
+                   "l2": "n/a (CPU)"},
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{a.steps} sessions of the listen workload, one per step"},
+                         "sample": f"{done} requests of the {a.workload} workload, one per step"},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        "rows_per_s": a.steps * rpr / el,
+        "rows_per_s": nrows / el,
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -264,7 +336,6 @@ def run_native(a):
 
     import serving_sampler_gb300 as sv
     from serving_sampler_gb300 import _build
-    import workloads
 
     world, rank, local = _dist()
     if not torch.cuda.is_available():
@@ -276,21 +347,11 @@ def run_native(a):
     _barrier(world)
     sv.load()
 
-    w, meta = _listen(device, a.sessions)
-    R, k = meta["R"], meta["k"]
-    target, draft = w["target"], w["draft"]
-    out = dict(accept_len=torch.empty(R, dtype=torch.int32, device=device),
-               tokens=torch.empty(R, k + 1, dtype=torch.int32, device=device),
-               branch=torch.empty(R, dtype=torch.int32, device=device),
-               status=torch.empty(R, dtype=torch.int32, device=device))
-    ws = torch.empty(sv.verify_greedy_workspace(R, k, 2, meta["V"]), dtype=torch.uint8, device=device)
+    wl = Workload(a.workload, device, a.sessions)
     stream = torch.cuda.current_stream(device)
 
-    def step():
-        sv.verify_greedy(target, R, k, 2, draft, out=out, workspace=ws, stream=stream)
-
     for _ in range(max(a.warmup, 3)):
-        step()
+        wl.call(wl.inputs, stream)
     torch.cuda.synchronize()
     clocks = Clocks(local)
     clocks.start()
@@ -299,7 +360,7 @@ def run_native(a):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(a.steps):
-        step()
+        wl.call(wl.inputs, stream)
     e1.record(stream)
     e1.synchronize()
     _barrier(world)
@@ -307,24 +368,24 @@ def run_native(a):
     clock_rows = clocks.stop()
     ms_local = e0.elapsed_time(e1) / a.steps
     ms = _max_over_ranks(ms_local, world, device)
-    value = world * meta["logit_bytes"] / (ms * 1e-3) / 1e9
-    rows_per_s = world * meta["rows"] / (ms * 1e-3)
+    value = world * wl.logit_bytes / (ms * 1e-3) / 1e9
+    rows_per_s = world * wl.rows / (ms * 1e-3)
 
     # end to end: pinned host inputs in, results out, every step
     e2e_steps = max(3, min(a.steps, 20))
-    h_target = torch.empty(target.shape, dtype=target.dtype, pin_memory=True)
-    h_target.copy_(target)
-    h_draft = torch.empty(draft.shape, dtype=draft.dtype, pin_memory=True)
-    h_draft.copy_(draft)
-    h_out = {key: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for key, v in out.items()}
-    d_target = torch.empty_like(target)
-    d_draft = torch.empty_like(draft)
+    h_in = {}
+    for key, t in wl.inputs.items():
+        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h.copy_(t)
+        h_in[key] = h
+    d_in = {key: torch.empty_like(t) for key, t in wl.inputs.items()}
+    h_out = {key: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for key, v in wl.out.items()}
 
     def e2e_step():
-        d_target.copy_(h_target, non_blocking=True)
-        d_draft.copy_(h_draft, non_blocking=True)
-        sv.verify_greedy(d_target, R, k, 2, d_draft, out=out, workspace=ws, stream=stream)
-        for key, v in out.items():
+        for key in d_in:
+            d_in[key].copy_(h_in[key], non_blocking=True)
+        wl.call(d_in, stream)
+        for key, v in wl.out.items():
             h_out[key].copy_(v, non_blocking=True)
 
     for _ in range(2):
@@ -339,43 +400,41 @@ def run_native(a):
     f1.synchronize()
     _barrier(world)
     e2e_ms = _max_over_ranks(f0.elapsed_time(f1) / e2e_steps, world, device)
-    h2d = h_target.numel() * h_target.element_size() + h_draft.numel() * h_draft.element_size()
+    h2d = sum(h.numel() * h.element_size() for h in h_in.values())
     d2h = sum(v.numel() * v.element_size() for v in h_out.values())
-    e2e_value = world * meta["logit_bytes"] / (e2e_ms * 1e-3) / 1e9
-    del h_target, d_target
+    e2e_value = world * wl.logit_bytes / (e2e_ms * 1e-3) / 1e9
+    del h_in, d_in
 
     peak, peak_kind = _peaks()
-    achieved = meta["logit_bytes"] / (ms_local * 1e-3) / 1e9
+    achieved = wl.logit_bytes / (ms_local * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": _traffic_from_profile("greedy.cu"),
-                "kernel": "argmax_segments_kernel<bf16> (+ greedy_finalize_kernel inside the same events)",
-                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                "traffic": _traffic_from_profile(wl.kernel_file, wl.profile),
+                "kernel": f"{wl.kernel} (all kernels of one call inside the same events)",
+                "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s"}
 
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
-        host = workloads.host_rows(target)
-        gbs, rps, done, el = _oracle_sample(host, draft.cpu().numpy(), meta, a.cpu_seconds)
+        gbs, rps, done, el = wl.oracle_sample(a.cpu_seconds)
         cpu = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"{done} sessions (65 rows x 151936 bf16 each) of the listen workload, {el:.1f} s, "
-                         f"single-threaded fp64 C", "rows_per_s": rps}
+               "sample": f"{done} requests of the {a.workload} workload, {el:.1f} s, single-threaded fp64 C",
+               "rows_per_s": rps}
 
     if rank == 0:
         line = {
-            "metric": "verify logit GB/s (speculative-listening greedy verify, V=151936 bf16)",
+            "metric": wl.metric,
             "value": value, "unit": "GB/s", "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": f"listen: {R} sessions x (32 main + 32 runner-up drafts) = 65 rows x 151936 "
-                                   f"bf16 per session ({meta['logit_bytes'] / 1e9:.3f} GB of logits per step)",
-                       "l2": f"inputs ({meta['logit_bytes'] / 1e9:.3f} GB) larger than L2 (129 MB); no flush",
+            "config": {"workload": wl.desc,
+                       "l2": f"inputs ({wl.logit_bytes / 1e9:.3f} GB) larger than L2 (129 MB); no flush",
                        "parallelism": f"replicas x{world}"},
             "rows_per_s": rows_per_s,
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps},
-            "gpu_launches": a.steps * sv.LAUNCHES["verify_greedy"],
+            "gpu_launches": a.steps * wl.launches,
             "clocks": Clocks.summarize(clock_rows),
         }
         print(json.dumps(line), flush=True)

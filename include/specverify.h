@@ -201,7 +201,7 @@ int sv_verify_sample(sv_rows target, sv_rows draft_logits, const int32_t* d2t, i
  *                   codebook s (the audio partition: the phase mask).
  *   cb_data_offset  HOST int32 [S] or NULL (all 0): element offset of codebook
  *                   s inside its row; offset + W <= row_stride.
- *   S               codebooks, 1 <= S <= SV_MAX_S;  w  CFG weight.
+ *   S               codebooks, 1 <= S <= SV_MAX_S;  w  CFG weight;  W <= 16384.
  *   draft_logits    draft rows, width W, row (r * k + j) * S + s; data == NULL
  *                   selects greedy verification on the merged logits.
  *   draft           int32 [R, k, S] absolute ids.

@@ -24,7 +24,7 @@ ST_BAD_TEMP, ST_BAD_D2T, ST_TIMEOUT = 16, 32, 64
 MAX_K, MAX_S = 256, 16
 
 # kernels launched by one call of each entry point (reported by the benchmark)
-LAUNCHES = {"verify_greedy": 2, "accept_scan": 1}
+LAUNCHES = {"verify_greedy": 2, "verify_sample": 3, "cfg_merge_sample": 3, "accept_scan": 1}
 
 
 class SpecVerifyError(RuntimeError):

@@ -164,6 +164,7 @@ int sv_cfg_merge_sample(sv_rows cond, sv_rows uncond, const int32_t* cb_id_base,
     if (R < 0 || k < 0 || S < 1) return SV_ERR_INVALID_ARG;
     if (k > SV_MAX_K || S > SV_MAX_S) return SV_ERR_LIMIT;
     if (cb_id_base == nullptr) return SV_ERR_INVALID_ARG;
+    if (cond.width > cfg_max_width()) return SV_ERR_LIMIT;
     if (cond.width != uncond.width || cond.dtype != uncond.dtype ||
         cond.row_stride != uncond.row_stride)
         return SV_ERR_SHAPE;

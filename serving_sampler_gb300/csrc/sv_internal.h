@@ -62,6 +62,8 @@ struct CfgShape {
     int32_t data_off[SV_MAX_S];
 };
 size_t cfg_workspace_bytes(int64_t R, int32_t k, int32_t S, int32_t W);
+// widest codebook accepted by sv_cfg_merge_sample
+int32_t cfg_max_width();
 cudaError_t launch_cfg_merge_sample(const Rows& cond, const Rows& uncond, const CfgShape& shape,
                                     const Rows* draft_logits, int32_t R, int32_t k,
                                     const int32_t* draft, const uint64_t* seeds,

@@ -216,3 +216,53 @@ def d2t_workload(device="cuda", R: int = 128):
     random injective d2t, T = 0.7, per-request seeds splitmix64(1234 + r)."""
     return sample_batch(R, 7, V_QWEN, VD_DRAFT, torch.bfloat16, T=0.7, sigma_pos=D2T_SIGMA,
                         delta=D2T_DELTA, z_sigma=3.0, seed=1237, seed_base=1234, device=device)
+
+
+# ---------------------------------------------------------------------------
+# CFG workload
+# ---------------------------------------------------------------------------
+CFG_TEXT_V = V_QWEN - 9 * 4096  # text partition size; audio codebook s starts at CFG_TEXT_V + 4096 s
+
+
+def cfg_batch(R: int, k: int, S: int, W: int, w: float = 3.0, T=1.0, dtype=torch.bfloat16, draft_dtype=None,
+              sigma_h: float = 0.5, sigma_e: float = 0.1, bump: float = 7.1, sigma_d: float = 1.0,
+              seed: int = 0, seed_base: int = 1234, device="cuda", row_len: int | None = None,
+              offsets=None, greedy_drafts: float = 0.0):
+    """cond / uncond rows [R*(k+1)*S, row_len] (codebook s at offsets[s], W entries):
+    c = h + e_c, u = h + e_u with a shared component h ~ N(0, sigma_h^2) and e ~ N(0, sigma_e^2);
+    one id per row is planted `bump` above h so the guided distribution has a top-1 near 0.2
+    (flat RVQ codebooks).  Draft rows [R*k*S, W] = the guided latent + N(0, sigma_d^2); drafts
+    are drawn from them (absolute ids cb_id_base[s] + local)."""
+    draft_dtype = draft_dtype or dtype
+    g = _gen(seed, device)
+    rows = R * (k + 1) * S
+    row_len = row_len or W
+    offsets = list(offsets) if offsets is not None else [0] * S
+    h = torch.randn(rows, W, generator=g, device=device) * sigma_h
+    top = torch.randint(0, W, (rows,), generator=g, device=device)
+    h.scatter_add_(1, top.view(-1, 1), torch.full((rows, 1), bump, device=device))
+    ec = torch.randn(rows, W, generator=g, device=device) * sigma_e
+    eu = torch.randn(rows, W, generator=g, device=device) * sigma_e
+    cond = torch.randn(rows, row_len, generator=g, device=device)
+    uncond = torch.randn(rows, row_len, generator=g, device=device)
+    svec = torch.arange(rows, device=device) % S
+    for s in range(S):
+        sel = svec == s
+        cond[sel, offsets[s]:offsets[s] + W] = h[sel] + ec[sel]
+        uncond[sel, offsets[s]:offsets[s] + W] = h[sel] + eu[sel]
+    guided = (h + w * ec - (w - 1.0) * eu).view(R, k + 1, S, W)[:, :k]
+    y = (guided + torch.randn(guided.shape, generator=g, device=device) * sigma_d).reshape(R * k * S, W)
+    draft_logits = y.to(draft_dtype).contiguous()
+    Tt = torch.as_tensor(T, dtype=torch.float32, device=device).expand(R).contiguous()
+    greedy = torch.rand(R * k * S, generator=g, device=device) < greedy_drafts
+    ids = _draw_drafts(g, draft_logits.float(), Tt.repeat_interleave(k * S), greedy)
+    base = torch.tensor([CFG_TEXT_V + 4096 * s for s in range(S)], dtype=torch.int64, device=device)
+    draft = (ids.view(R, k, S) + base.view(1, 1, S)).to(torch.int32).contiguous()
+    return dict(cond=cond.to(dtype), uncond=uncond.to(dtype), draft_logits=draft_logits, draft=draft,
+                cb_id_base=base.tolist(), cb_data_offset=offsets, S=S, W=W, w=w, R=R, k=k,
+                seeds=seeds_tensor(seed_base, R, device), temperature=Tt)
+
+
+def cfg_workload(device="cuda", R: int = 256):
+    """256 requests, 9 codebooks x 4096 entries, 4 drafted frames (+1), bf16, w = 3, T = 1."""
+    return cfg_batch(R, 4, 9, 4096, 3.0, 1.0, torch.bfloat16, seed=1238, seed_base=1234 + 3, device=device)
