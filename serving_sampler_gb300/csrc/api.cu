@@ -114,8 +114,8 @@ size_t sv_verify_sample_workspace(int32_t R, int32_t k, int32_t V, int32_t Vd)
     return sample_workspace_bytes(R, k, V, Vd);
 }
 
-int sv_verify_sample(sv_rows target, sv_rows draft_logits, const int32_t* d2t, int32_t R,
-                     int32_t k, const int32_t* draft, const uint64_t* seeds,
+int sv_verify_sample(sv_rows target, sv_rows draft_logits, const int32_t* d2t, const void* d2t_plan,
+                     int32_t R, int32_t k, const int32_t* draft, const uint64_t* seeds,
                      const float* temperature, int32_t* accept_len, int32_t* tokens, float* tv,
                      float* p_draft, float* q_draft, int32_t* status, void* workspace,
                      size_t workspace_bytes, sv_stream_t stream)
@@ -130,6 +130,7 @@ int sv_verify_sample(sv_rows target, sv_rows draft_logits, const int32_t* d2t, i
         !aligned(accept_len, 4) || !aligned(tokens, 4) || !aligned(tv, 4) ||
         !aligned(p_draft, 4) || !aligned(q_draft, 4) || !aligned(status, 4) || !aligned(d2t, 4))
         return SV_ERR_ALIGN;
+    if (!aligned(d2t_plan, 256)) return SV_ERR_WORKSPACE;
     Rows t{}, d{};
     if (int rc = check_rows(target, static_cast<int64_t>(R) * (k + 1), target.width, &t)) return rc;
     const int64_t drows = static_cast<int64_t>(R) * k;
@@ -138,14 +139,32 @@ int sv_verify_sample(sv_rows target, sv_rows draft_logits, const int32_t* d2t, i
     } else {
         d = Rows{nullptr, SV_F32, 4, draft_logits.width > 0 ? draft_logits.width : t.width, 0, false};
     }
-    if (d2t == nullptr && d.width != t.width) return SV_ERR_SHAPE;
-    if (d2t != nullptr && t.width > sample_max_plan_width()) return SV_ERR_LIMIT;
+    const bool mapped = d2t != nullptr || d2t_plan != nullptr;
+    if (!mapped && d.width != t.width) return SV_ERR_SHAPE;
+    if (mapped && t.width > sample_max_plan_width()) return SV_ERR_LIMIT;
     if (int rc = check_workspace(workspace, workspace_bytes,
                                  sample_workspace_bytes(R, k, t.width, d.width)))
         return rc;
     if (!have_device()) return SV_ERR_DEVICE;
-    return launched(launch_verify_sample(t, d, d2t, R, k, draft, seeds, temperature, accept_len,
+    return launched(launch_verify_sample(t, d, d2t, d2t_plan, R, k, draft, seeds, temperature, accept_len,
                                          tokens, tv, p_draft, q_draft, status, workspace, stream));
+}
+
+size_t sv_d2t_plan_bytes(int32_t V, int32_t Vd)
+{
+    if (V < 1 || Vd < 1) return 0;
+    return d2t_plan_bytes(V, Vd);
+}
+
+int sv_d2t_plan_build(const int32_t* d2t, int32_t Vd, int32_t V, void* plan, size_t plan_bytes,
+                      sv_stream_t stream)
+{
+    if (V < 1 || Vd < 1 || d2t == nullptr) return SV_ERR_INVALID_ARG;
+    if (V > sample_max_plan_width() || Vd > 65535) return SV_ERR_LIMIT;
+    if (!aligned(d2t, 4)) return SV_ERR_ALIGN;
+    if (int rc = check_workspace(plan, plan_bytes, d2t_plan_bytes(V, Vd))) return rc;
+    if (!have_device()) return SV_ERR_DEVICE;
+    return launched(launch_d2t_plan_build(d2t, Vd, V, plan, stream));
 }
 
 size_t sv_cfg_merge_sample_workspace(int32_t R, int32_t k, int32_t S, int32_t W)

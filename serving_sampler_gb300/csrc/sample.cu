@@ -53,7 +53,8 @@ struct D2tPlan {
     int32_t* prefix;   // [nw + 1] set bits before each word
     int32_t* xs;       // [Vd] support target ids, ascending
     int32_t* js;       // [Vd] the draft id of xs[pos]
-    int32_t* bad;      // d2t out of range or repeated
+    uint16_t* js16;    // [Vd] the same draft ids as 16-bit values (Vd <= 65535)
+    int32_t* header;   // [0] V, [1] Vd the plan was built for, [2] d2t out of range or repeated
     int32_t nw;
 };
 
@@ -302,7 +303,9 @@ __global__ void __launch_bounds__(kPlanThreads)
     }
     if (tid == 0) {
         pl.prefix[pl.nw] = pref[pl.nw];
-        *pl.bad = bad_any;
+        pl.header[0] = V;
+        pl.header[1] = Vd;
+        pl.header[2] = bad_any;
     }
     for (int32_t j = tid; j < Vd; j += kPlanThreads) {
         const int32_t x = d2t[j];
@@ -312,6 +315,7 @@ __global__ void __launch_bounds__(kPlanThreads)
         if (pos >= 0 && pos < Vd) {
             pl.xs[pos] = x;
             pl.js[pos] = j;
+            pl.js16[pos] = static_cast<uint16_t>(j);
         }
     }
 }
@@ -718,6 +722,472 @@ __global__ void __launch_bounds__(kRowThreads, 1) sample_rows_kernel(SampleArgs 
 }
 
 // ---------------------------------------------------------------------------
+// row pass, fast path: bf16 target and draft rows, d2t vocabulary <= 32768
+// ---------------------------------------------------------------------------
+// Warp 0 is the producer: its lane 0 walks the same (unit, chunk) sequence
+// as the consumers and keeps kFastStages stages in flight, each holding a
+// 16 KB slice of a row plus, for target chunks, the 16-bit draft ids of the
+// support positions inside that slice.  Warps 1..16 consume: for each chunk
+// they wait on its `full` barrier and each warp arrives on its `empty`
+// barrier when done, so no block-wide barrier runs per chunk.  The support
+// bitmap and prefix counts stay in shared memory for the whole kernel; the
+// target logit of every support id is scattered to G[draft id], so the TV
+// pass reads G and the (L2-resident) draft row in draft-id order.
+namespace {
+
+constexpr int kFastConsumerWarps = 16;
+constexpr int kFastConsumers = 32 * kFastConsumerWarps;
+constexpr int kFastThreads = kFastConsumers + 32;
+constexpr int kFastStages = 5;
+constexpr uint32_t kFastData = 16384;                       // 8192 bf16 per stage
+constexpr uint32_t kFastJsCap = 4096;                       // 2048 staged draft ids per stage
+constexpr uint32_t kFastStage = kFastData + kFastJsCap + 16;
+constexpr int kFastHeader = 256;
+constexpr int32_t kFastMaxVd = 32768;
+constexpr int32_t kFastMaxWords = 6144;                     // V <= 196,608
+
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void consumer_sync()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kFastConsumers) : "memory");
+}
+
+__device__ __forceinline__ float csum(float v, float* sc)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int w = (threadIdx.x >> 5) - 1;
+    consumer_sync();
+    if ((threadIdx.x & 31) == 0) sc[w] = v;
+    consumer_sync();
+    float t = 0.f;
+    for (int i = 0; i < kFastConsumerWarps; ++i) t += sc[i];
+    return t;
+}
+
+__device__ __forceinline__ float cmax(float v, float* sc)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    const int w = (threadIdx.x >> 5) - 1;
+    consumer_sync();
+    if ((threadIdx.x & 31) == 0) sc[w] = v;
+    consumer_sync();
+    float t = -INFINITY;
+    for (int i = 0; i < kFastConsumerWarps; ++i) t = fmaxf(t, sc[i]);
+    return t;
+}
+
+__device__ __forceinline__ uint32_t cor(uint32_t v, uint32_t* sc)
+{
+    v = __reduce_or_sync(0xffffffffu, v);
+    const int w = (threadIdx.x >> 5) - 1;
+    consumer_sync();
+    if ((threadIdx.x & 31) == 0) sc[w] = v;
+    consumer_sync();
+    uint32_t t = 0;
+    for (int i = 0; i < kFastConsumerWarps; ++i) t |= sc[i];
+    return t;
+}
+
+__device__ __forceinline__ void cargmax(float& v, int32_t& x, float* sv, int32_t* sx)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+        const int32_t ox = __shfl_xor_sync(0xffffffffu, x, o);
+        if (ov > v || (ov == v && ox < x)) {
+            v = ov;
+            x = ox;
+        }
+    }
+    const int w = (threadIdx.x >> 5) - 1;
+    consumer_sync();
+    if ((threadIdx.x & 31) == 0) {
+        sv[w] = v;
+        sx[w] = x;
+    }
+    consumer_sync();
+    v = sv[0];
+    x = sx[0];
+    for (int i = 1; i < kFastConsumerWarps; ++i)
+        if (sv[i] > v || (sv[i] == v && sx[i] < x)) {
+            v = sv[i];
+            x = sx[i];
+        }
+}
+
+// replace NaN halves of a bf16x2 word by -inf
+__device__ __forceinline__ uint32_t bf16x2_nan_to_ninf(uint32_t w)
+{
+    uint32_t lo = w & 0xFFFFu, hi = w >> 16;
+    if ((lo & 0x7FFFu) > 0x7F80u) lo = 0xFF80u;
+    if ((hi & 0x7FFFu) > 0x7F80u) hi = 0xFF80u;
+    return lo | (hi << 16);
+}
+
+struct FastUnit {
+    int32_t r, j;
+    bool sampling, has_draft;
+    const char* trow;
+    const char* drow;
+    uint32_t nd, nt;  // draft / target chunks
+};
+
+__device__ __forceinline__ FastUnit fast_unit(const SampleArgs& A, int64_t unit)
+{
+    FastUnit u;
+    u.r = static_cast<int32_t>(unit / (A.k + 1));
+    u.j = static_cast<int32_t>(unit - static_cast<int64_t>(u.r) * (A.k + 1));
+    const float T = A.temp[u.r];
+    u.sampling = T > 0.f;
+    u.has_draft = u.sampling && u.j < A.k;
+    u.trow = A.tbase + unit * A.tstride;
+    u.drow = u.has_draft ? A.dbase + (static_cast<int64_t>(u.r) * A.k + u.j) * A.dstride : nullptr;
+    u.nd = u.has_draft ? (static_cast<uint32_t>(A.Vd) * 2 + kFastData - 1) / kFastData : 0u;
+    u.nt = (static_cast<uint32_t>(A.V) * 2 + kFastData - 1) / kFastData;
+    return u;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(SampleArgs A)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + kFastStages;
+    unsigned char* ring = smem + kFastHeader;
+    uint16_t* G = reinterpret_cast<uint16_t*>(ring + kFastStages * kFastStage);
+    const int32_t nw = A.plan.nw;
+    uint32_t* sbits = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(G) + align256(static_cast<int64_t>(A.Vd) * 2));
+    int32_t* spref = reinterpret_cast<int32_t*>(sbits + nw);
+    __shared__ float red_f[kFastConsumerWarps];
+    __shared__ int32_t red_i[kFastConsumerWarps];
+    __shared__ uint32_t red_u[kFastConsumerWarps];
+    __shared__ float zx_shared;
+    const int tid = threadIdx.x;
+
+    pdl_wait_primary();  // a plan built in the same call must be complete
+    pdl_launch_dependents();
+    if (tid == 0) {
+        for (int s = 0; s < kFastStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kFastConsumerWarps);
+        }
+        fence_barrier_init();
+    }
+    for (int32_t w = tid; w < nw; w += kFastThreads) {
+        sbits[w] = A.plan.bitmap[w];
+        spref[w] = A.plan.prefix[w];
+    }
+    if (tid == 0) spref[nw] = A.plan.prefix[nw];
+    __syncthreads();
+
+    const int64_t units = static_cast<int64_t>(A.R) * (A.k + 1);
+    if (tid < 32) {
+        // ---------------- producer ----------------
+        if (tid != 0) return;
+        const uint64_t pol_t = l2_policy_evict_first();
+        uint64_t pol_d;
+        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_d));
+        uint32_t g = 0;
+        for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
+            const FastUnit u = fast_unit(A, unit);
+            const uint32_t n = u.nd + u.nt;
+            for (uint32_t i = 0; i < n; ++i, ++g) {
+                const uint32_t s = g % kFastStages;
+                if (!mbar_wait_bounded(&empty[s], ((g / kFastStages) & 1u) ^ 1u)) return;  // consumers record the timeout
+                unsigned char* st = ring + s * kFastStage;
+                if (i < u.nd) {
+                    const uint32_t off = i * kFastData;
+                    const uint32_t nb = min(kFastData, static_cast<uint32_t>(A.Vd) * 2 - off);
+                    mbar_arrive_expect_tx(&full[s], nb);
+                    bulk_copy_g2s(st, u.drow + off, nb, &full[s], pol_d);
+                } else {
+                    const uint32_t t = i - u.nd;
+                    const uint32_t off = t * kFastData;
+                    const uint32_t nb = min(kFastData, static_cast<uint32_t>(A.V) * 2 - off);
+                    uint32_t js_bytes = 0;
+                    int32_t p0a = 0;
+                    if (u.has_draft) {
+                        const int32_t x0 = static_cast<int32_t>(off / 2), x1 = x0 + static_cast<int32_t>(nb / 2);
+                        const int32_t p0 = spref[x0 >> 5];
+                        const int32_t w1 = x1 >> 5, b1 = x1 & 31;
+                        const int32_t p1 = spref[w1] + (b1 ? __popc(sbits[w1] & ((1u << b1) - 1u)) : 0);
+                        p0a = p0 & ~7;
+                        js_bytes = min(kFastJsCap, static_cast<uint32_t>((p1 - p0a) * 2 + 15) & ~15u);
+                        if (p1 <= p0) js_bytes = 0;
+                    }
+                    mbar_arrive_expect_tx(&full[s], nb + js_bytes);
+                    bulk_copy_g2s(st, u.trow + off, nb, &full[s], pol_t);
+                    if (js_bytes) bulk_copy_g2s(st + kFastData, A.plan.js16 + p0a, js_bytes, &full[s], pol_d);
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    const int ct = tid - 32;
+    uint32_t g = 0;
+    uint32_t timeout = 0;
+    for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
+        const FastUnit u = fast_unit(A, unit);
+        const float T = A.temp[u.r];
+        const float c = u.sampling ? kLog2e / T : 0.f;
+        const int32_t xj = u.has_draft ? A.draft[static_cast<int64_t>(u.r) * A.k + u.j] : -1;
+        if (u.j == 0 && ct == 0) {
+            A.race[u.r].best = ~0ull;
+            A.race[u.r].count = 0u;
+        }
+        if (ct == 0) zx_shared = NAN;
+        consumer_sync();  // G and zx of the previous unit are no longer read
+
+        // ---- draft row: max and sum 2^(y c - max) ----
+        float dm = -INFINITY, ds = 0.f;
+        uint32_t dflags = 0;
+        for (uint32_t i = 0; i < u.nd; ++i, ++g) {
+            const uint32_t s = g % kFastStages;
+            if (!timeout && !mbar_wait_bounded(&full[s], (g / kFastStages) & 1u)) timeout = 1;
+            const uint4* vp = reinterpret_cast<const uint4*>(ring + s * kFastStage);
+            const int nv = static_cast<int>(min(kFastData, static_cast<uint32_t>(A.Vd) * 2 - i * kFastData) / 16);
+            for (int v = ct; v < nv; v += kFastConsumers) {
+                uint4 q = vp[v];
+                const uint32_t m2 = bmax2_nan(bmax2_nan(q.x, q.y), bmax2_nan(q.z, q.w));
+                float vm = fmax_nan(bf16_lo(m2), bf16_hi(m2));
+                if (vm != vm) {
+                    dflags |= kFlagNaN;
+                    q = make_uint4(bf16x2_nan_to_ninf(q.x), bf16x2_nan_to_ninf(q.y), bf16x2_nan_to_ninf(q.z),
+                                   bf16x2_nan_to_ninf(q.w));
+                    const uint32_t m3 = bmax2_nan(bmax2_nan(q.x, q.y), bmax2_nan(q.z, q.w));
+                    vm = fmaxf(bf16_lo(m3), bf16_hi(m3));
+                }
+                if (vm == INFINITY) dflags |= kFlagPosInf;
+                const float mt = vm * c;
+                if (mt > dm) {
+                    ds = dm == -INFINITY ? 0.f : ds * ex2(dm - mt);
+                    dm = mt;
+                }
+                if (dm > -INFINITY) {
+                    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+                    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        a0 += ex2(fmaf(bf16_lo(w[e]), c, -dm));
+                        a1 += ex2(fmaf(bf16_hi(w[e]), c, -dm));
+                    }
+                    ds += a0 + a1;
+                }
+            }
+            __syncwarp();
+            if ((ct & 31) == 0) mbar_arrive(&empty[s]);
+        }
+
+        // ---- target row ----
+        float tm = -INFINITY, ts = 0.f;
+        float bv = -INFINITY;
+        int32_t bx = INT32_MAX;
+        uint32_t tflags = 0;
+        for (uint32_t t = 0; t < u.nt; ++t, ++g) {
+            const uint32_t s = g % kFastStages;
+            if (!timeout && !mbar_wait_bounded(&full[s], (g / kFastStages) & 1u)) timeout = 1;
+            const unsigned char* st = ring + s * kFastStage;
+            const uint4* vp = reinterpret_cast<const uint4*>(st);
+            const uint16_t* js_st = reinterpret_cast<const uint16_t*>(st + kFastData);
+            const uint32_t off = t * kFastData;
+            const uint32_t nb = min(kFastData, static_cast<uint32_t>(A.V) * 2 - off);
+            const int nv = static_cast<int>(nb / 16);
+            const int32_t x0 = static_cast<int32_t>(off / 2);
+            int32_t p0a = 0, nstaged = 0;
+            if (u.has_draft) {
+                const int32_t x1 = x0 + static_cast<int32_t>(nb / 2);
+                const int32_t p0 = spref[x0 >> 5];
+                const int32_t w1 = x1 >> 5, b1 = x1 & 31;
+                const int32_t p1 = spref[w1] + (b1 ? __popc(sbits[w1] & ((1u << b1) - 1u)) : 0);
+                p0a = p0 & ~7;
+                nstaged = p1 > p0 ? static_cast<int32_t>(min(kFastJsCap, static_cast<uint32_t>((p1 - p0a) * 2 + 15) & ~15u) / 2) : 0;
+            }
+            for (int v = ct; v < nv; v += kFastConsumers) {
+                uint4 q = vp[v];
+                const int32_t x = x0 + v * 8;
+                const uint32_t m2 = bmax2_nan(bmax2_nan(q.x, q.y), bmax2_nan(q.z, q.w));
+                float vm = fmax_nan(bf16_lo(m2), bf16_hi(m2));
+                if (vm != vm) {
+                    tflags |= kFlagNaN;
+                    q = make_uint4(bf16x2_nan_to_ninf(q.x), bf16x2_nan_to_ninf(q.y), bf16x2_nan_to_ninf(q.z),
+                                   bf16x2_nan_to_ninf(q.w));
+                    const uint32_t m3 = bmax2_nan(bmax2_nan(q.x, q.y), bmax2_nan(q.z, q.w));
+                    vm = fmaxf(bf16_lo(m3), bf16_hi(m3));
+                }
+                const bool up = vm > bv;
+                bv = up ? vm : bv;
+                bx = up ? x : bx;
+                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+                if (u.sampling) {
+                    const float mt = vm * c;
+                    if (mt > tm) {
+                        ts = tm == -INFINITY ? 0.f : ts * ex2(tm - mt);
+                        tm = mt;
+                    }
+                    if (tm > -INFINITY) {
+                        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            a0 += ex2(fmaf(bf16_lo(w[e]), c, -tm));
+                            a1 += ex2(fmaf(bf16_hi(w[e]), c, -tm));
+                        }
+                        ts += a0 + a1;
+                    }
+                }
+                if (u.has_draft) {
+                    // scatter the support logits of this vector to G[draft id]
+                    const int32_t wi = x >> 5, sh = x & 31;
+                    const uint32_t word = sbits[wi];
+                    uint32_t bits = (word >> sh) & 0xFFu;
+                    if (bits) {
+                        const int32_t base = spref[wi] + (sh ? __popc(word & ((1u << sh) - 1u)) : 0) - p0a;
+                        const uint32_t all = bits;
+                        while (bits) {
+                            const int e = __ffs(bits) - 1;
+                            bits &= bits - 1;
+                            const int32_t li = base + __popc(all & ((1u << e) - 1u));
+                            const int32_t jd = li < nstaged ? js_st[li] : A.plan.js16[p0a + li];
+                            if (jd < A.Vd) G[jd] = static_cast<uint16_t>((e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu));
+                        }
+                    }
+                    if (static_cast<uint32_t>(xj - x) < 8u) {
+                        const int e = xj - x;
+                        zx_shared = (e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1]);
+                    }
+                }
+            }
+            __syncwarp();
+            if ((ct & 31) == 0) mbar_arrive(&empty[s]);
+        }
+
+        // ---- reductions over the consumer warps ----
+        cargmax(bv, bx, red_f, red_i);
+        const uint32_t fl_t = cor(tflags, red_u);
+        const uint32_t fl_d = cor(dflags, red_u);
+        int32_t amax = 0;
+        if (bx != INT32_MAX) {
+            amax = bx;
+            for (int e = 0; e < 8; ++e) {
+                const int32_t x = bx + e;
+                if (x >= A.V) break;
+                if (ld_elem<SV_BF16>(u.trow, x) == bv) {
+                    amax = x;
+                    break;
+                }
+            }
+        }
+        float M = -INFINITY, S = 0.f, Mq = -INFINITY, Sq = 0.f;
+        if (u.sampling) {
+            M = cmax(tm, red_f);
+            const float sc = (tm == -INFINITY || M == -INFINITY) ? 0.f : ex2(tm - M);
+            S = csum(ts * sc, red_f);
+        }
+        if (u.has_draft) {
+            Mq = cmax(dm, red_f);
+            const float sc = (dm == -INFINITY || Mq == -INFINITY) ? 0.f : ex2(dm - Mq);
+            Sq = csum(ds * sc, red_f);
+        }
+        uint32_t flags = 0;
+        if (fl_t & kFlagNaN) flags |= kFlagNaN;
+        if (bv == INFINITY) flags |= kFlagPosInf;
+        if (bv == -INFINITY) flags |= kFlagAllNegInf;
+        if (u.has_draft && ((fl_d & (kFlagNaN | kFlagPosInf)) || Mq == -INFINITY)) flags |= kFlagDraftBad;
+        if (cor(timeout, red_u)) flags |= kFlagTimeout;
+
+        // ---- TV = sum over the support of max(0, q - p); p(x_j), q(x_j), accept ----
+        float tvv = NAN, pj = NAN, qj = NAN;
+        int32_t acc = 0;
+        if (u.has_draft) {
+            const float invS = 1.f / S, invSq = 1.f / Sq;
+            float a = 0.f;
+            const int32_t nv8 = A.Vd / 8;
+            const uint4* yv = reinterpret_cast<const uint4*>(u.drow);
+            const uint4* gv = reinterpret_cast<const uint4*>(G);
+            for (int32_t v = ct; v < nv8; v += kFastConsumers) {
+                const uint4 gq = gv[v];
+                const uint4 yq = yv[v];
+                const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
+                const uint32_t yw[4] = {yq.x, yq.y, yq.z, yq.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float p0 = ex2(fmaf(bf16_lo(gw[e]), c, -M)) * invS;
+                    const float p1 = ex2(fmaf(bf16_hi(gw[e]), c, -M)) * invS;
+                    const float q0 = ex2(fmaf(bf16_lo(yw[e]), c, -Mq)) * invSq;
+                    const float q1 = ex2(fmaf(bf16_hi(yw[e]), c, -Mq)) * invSq;
+                    a += fmaxf(q0 - p0, 0.f) + fmaxf(q1 - p1, 0.f);
+                }
+            }
+            for (int32_t jd = nv8 * 8 + ct; jd < A.Vd; jd += kFastConsumers) {
+                const float p = ex2(fmaf(__uint_as_float(static_cast<uint32_t>(G[jd]) << 16), c, -M)) * invS;
+                const float q = ex2(fmaf(ld_elem<SV_BF16>(u.drow, jd), c, -Mq)) * invSq;
+                a += fmaxf(q - p, 0.f);
+            }
+            tvv = csum(a, red_f);
+            if (ct == 0) {
+                const bool in_range = xj >= 0 && xj < A.V;
+                float zx = zx_shared;
+                zx = zx != zx ? -INFINITY : zx;
+                pj = in_range ? ex2(fmaf(zx, c, -M)) * invS : 0.f;
+                qj = 0.f;
+                if (in_range && ((sbits[xj >> 5] >> (xj & 31)) & 1u)) {
+                    const int32_t wi = xj >> 5, sh = xj & 31;
+                    const int32_t pos = spref[wi] + (sh ? __popc(sbits[wi] & ((1u << sh) - 1u)) : 0);
+                    const int32_t jd = A.plan.js16[pos];
+                    if (jd < A.Vd) {
+                        float y = ld_elem<SV_BF16>(u.drow, jd);
+                        y = y != y ? -INFINITY : y;
+                        qj = ex2(fmaf(y, c, -Mq)) * invSq;
+                    }
+                }
+                if (qj > 0.f) {
+                    const uint4 w = philox_block(philox_key(A.seeds[u.r]), 0u, static_cast<uint32_t>(u.j), kTagAccept);
+                    acc = uniform_from_word(w.x) < __fdiv_rn(pj, qj) ? 1 : 0;
+                } else if (in_range) {
+                    flags |= kFlagOffSupport;
+                }
+            }
+        }
+        if (ct == 0) {
+            RowStat rs;
+            rs.m = M;
+            rs.s = S;
+            rs.mq = Mq;
+            rs.sq = Sq;
+            rs.zx = zx_shared;
+            rs.p = pj;
+            rs.q = qj;
+            rs.amax = amax;
+            rs.flags = flags;
+            rs.accept = acc;
+            rs.pad[0] = rs.pad[1] = 0;
+            A.stats[unit] = rs;
+            if (u.j < A.k) {
+                const int64_t o = static_cast<int64_t>(u.r) * A.k + u.j;
+                if (A.tv) A.tv[o] = tvv;
+                if (A.pd) A.pd[o] = pj;
+                if (A.qd) A.qd[o] = qj;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // scan + race + commit
 // ---------------------------------------------------------------------------
 namespace {
@@ -894,7 +1364,8 @@ __global__ void __launch_bounds__(kRaceThreads) race_commit_kernel(SampleArgs A)
     if (fl & kFlagTimeout) status |= SV_ST_TIMEOUT;
     if (bad_rows) status |= SV_ST_BAD_LOGITS;
     if (T < 0.f || T != T) status |= SV_ST_BAD_TEMP;
-    if (!A.identity && *A.plan.bad) status |= SV_ST_BAD_D2T;
+    if (!A.identity && (A.plan.header[2] != 0 || A.plan.header[0] != A.V || A.plan.header[1] != A.Vd))
+        status |= SV_ST_BAD_D2T;
     int32_t* out = A.tokens + static_cast<int64_t>(r) * (k + 1);
     for (int32_t j = tid; j <= k; j += kRaceThreads) out[j] = j < n ? d[j] : (j == n ? token : -1);
     if (greedy) {
@@ -918,9 +1389,47 @@ __global__ void __launch_bounds__(kRaceThreads) race_commit_kernel(SampleArgs A)
 // ---------------------------------------------------------------------------
 namespace {
 
+struct PlanLayout {
+    int64_t header, bitmap, prefix, xs, js, js16, total;
+};
+
+PlanLayout plan_layout(int32_t V, int32_t Vd)
+{
+    PlanLayout L{};
+    const int64_t nw = (V + 31) / 32;
+    int64_t off = 0;
+    auto take = [&](int64_t bytes) {
+        const int64_t o = off;
+        off += align256(bytes + 16);  // 16 bytes of slack: bulk copies round up to 16
+        return o;
+    };
+    L.header = take(16);
+    L.bitmap = take(nw * 4);
+    L.prefix = take((nw + 1) * 4);
+    L.xs = take(static_cast<int64_t>(Vd) * 4);
+    L.js = take(static_cast<int64_t>(Vd) * 4);
+    L.js16 = take(static_cast<int64_t>(Vd) * 2);
+    L.total = off;
+    return L;
+}
+
+D2tPlan plan_view(void* base, int32_t V, int32_t Vd)
+{
+    const PlanLayout L = plan_layout(V, Vd);
+    char* b = static_cast<char*>(base);
+    D2tPlan pl{};
+    pl.header = reinterpret_cast<int32_t*>(b + L.header);
+    pl.bitmap = reinterpret_cast<uint32_t*>(b + L.bitmap);
+    pl.prefix = reinterpret_cast<int32_t*>(b + L.prefix);
+    pl.xs = reinterpret_cast<int32_t*>(b + L.xs);
+    pl.js = reinterpret_cast<int32_t*>(b + L.js);
+    pl.js16 = reinterpret_cast<uint16_t*>(b + L.js16);
+    pl.nw = (V + 31) / 32;
+    return pl;
+}
+
 struct SampleLayout {
-    int64_t plan_bitmap, plan_prefix, plan_xs, plan_js, plan_bad;
-    int64_t stats, race, gslots;
+    int64_t plan, stats, race, gslots;
     int64_t gslot_bytes;
     int64_t total;
     int smem_mode;
@@ -928,21 +1437,16 @@ struct SampleLayout {
     int grid;
 };
 
-SampleLayout sample_layout(int64_t R, int32_t k, int32_t V, int32_t Vd, int et, int ed, int sms)
+SampleLayout sample_layout(int64_t R, int32_t k, int32_t V, int32_t Vd, int et, int ed, int sms, bool own_plan)
 {
     SampleLayout L{};
-    const int64_t nw = (V + 31) / 32;
     int64_t off = 0;
     auto take = [&](int64_t bytes) {
         const int64_t o = off;
         off += align256(bytes);
         return o;
     };
-    L.plan_bitmap = take(nw * 4);
-    L.plan_prefix = take((nw + 1) * 4);
-    L.plan_xs = take(static_cast<int64_t>(Vd) * 4);
-    L.plan_js = take(static_cast<int64_t>(Vd) * 4);
-    L.plan_bad = take(4);
+    L.plan = take(own_plan ? plan_layout(V, Vd).total : 0);
     L.stats = take(R * (k + 1) * static_cast<int64_t>(sizeof(RowStat)));
     L.race = take(R * static_cast<int64_t>(sizeof(RaceSlot)));
     const int64_t units = R * (k + 1);
@@ -957,25 +1461,56 @@ SampleLayout sample_layout(int64_t R, int32_t k, int32_t V, int32_t Vd, int et, 
     return L;
 }
 
+size_t fast_smem_bytes(int32_t V, int32_t Vd)
+{
+    const int64_t nw = (V + 31) / 32;
+    return static_cast<size_t>(kFastHeader + kFastStages * static_cast<int64_t>(kFastStage) +
+                               align256(static_cast<int64_t>(Vd) * 2) + nw * 4 + (nw + 1) * 4);
+}
+
+bool fast_path_ok(const Rows& t, const Rows& d, bool identity)
+{
+    const int32_t nw = (t.width + 31) / 32;
+    return !identity && t.dtype == SV_BF16 && d.dtype == SV_BF16 && t.bulk_ok && d.bulk_ok && d.data != nullptr &&
+           t.width % 8 == 0 && d.width % 8 == 0 && d.width <= kFastMaxVd && nw <= kFastMaxWords &&
+           fast_smem_bytes(t.width, d.width) <= 227 * 1024;
+}
+
 }  // namespace
+
+size_t d2t_plan_bytes(int32_t V, int32_t Vd) { return static_cast<size_t>(plan_layout(V, Vd).total); }
+
+cudaError_t launch_d2t_plan_build(const int32_t* d2t, int32_t Vd, int32_t V, void* plan, cudaStream_t stream)
+{
+    const D2tPlan pl = plan_view(plan, V, Vd);
+    const size_t psmem = static_cast<size_t>(2 * pl.nw + 1) * 4;
+    cudaError_t e = cudaFuncSetAttribute(d2t_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(psmem));
+    if (e != cudaSuccess) return e;
+    d2t_plan_kernel<<<1, kPlanThreads, psmem, stream>>>(d2t, Vd, V, pl);
+    return cudaGetLastError();
+}
 
 size_t sample_workspace_bytes(int64_t R, int32_t k, int32_t V, int32_t Vd)
 {
     const int sms = device_sm_count();
     int64_t best = 0;
     for (int et : {2, 4})
-        for (int ed : {2, 4}) best = std::max(best, sample_layout(R, k, V, Vd, et, ed, sms).total);
+        for (int ed : {2, 4}) best = std::max(best, sample_layout(R, k, V, Vd, et, ed, sms, true).total);
     return static_cast<size_t>(best);
 }
 
 template <int DT, int DD>
-static cudaError_t launch_sample_t(const Rows& t, const Rows& d, const int32_t* d2t, int32_t R, int32_t k,
-                                   const int32_t* draft, const uint64_t* seeds, const float* temperature,
-                                   int32_t* accept_len, int32_t* tokens, float* tv, float* p_draft,
-                                   float* q_draft, int32_t* status, void* workspace, cudaStream_t stream)
+static cudaError_t launch_sample_t(const Rows& t, const Rows& d, const int32_t* d2t, const void* prebuilt,
+                                   int32_t R, int32_t k, const int32_t* draft, const uint64_t* seeds,
+                                   const float* temperature, int32_t* accept_len, int32_t* tokens, float* tv,
+                                   float* p_draft, float* q_draft, int32_t* status, void* workspace,
+                                   cudaStream_t stream)
 {
     const int sms = device_sm_count();
-    const SampleLayout L = sample_layout(R, k, t.width, d.width, t.esize, d.esize, sms);
+    const bool identity = d2t == nullptr && prebuilt == nullptr;
+    const bool own_plan = !identity && prebuilt == nullptr;
+    const SampleLayout L = sample_layout(R, k, t.width, d.width, t.esize, d.esize, sms, own_plan);
     char* ws = static_cast<char*>(workspace);
     SampleArgs A{};
     A.tbase = t.data;
@@ -984,15 +1519,10 @@ static cudaError_t launch_sample_t(const Rows& t, const Rows& d, const int32_t* 
     A.dbase = d.data;
     A.dstride = d.stride * d.esize;
     A.Vd = d.width;
-    A.identity = d2t == nullptr;
+    A.identity = identity;
     A.tbulk = t.bulk_ok;
     A.dbulk = d.bulk_ok && d.data != nullptr;
-    A.plan.nw = (t.width + 31) / 32;
-    A.plan.bitmap = reinterpret_cast<uint32_t*>(ws + L.plan_bitmap);
-    A.plan.prefix = reinterpret_cast<int32_t*>(ws + L.plan_prefix);
-    A.plan.xs = reinterpret_cast<int32_t*>(ws + L.plan_xs);
-    A.plan.js = reinterpret_cast<int32_t*>(ws + L.plan_js);
-    A.plan.bad = reinterpret_cast<int32_t*>(ws + L.plan_bad);
+    if (!identity) A.plan = plan_view(own_plan ? ws + L.plan : const_cast<void*>(prebuilt), t.width, d.width);
     A.R = R;
     A.k = k;
     A.draft = draft;
@@ -1013,28 +1543,34 @@ static cudaError_t launch_sample_t(const Rows& t, const Rows& d, const int32_t* 
     A.race_ctas = (t.width + kRaceSeg - 1) / kRaceSeg;
 
     cudaError_t e;
-    if (!A.identity) {
-        const size_t psmem = static_cast<size_t>(2 * A.plan.nw + 1) * 4;
-        e = cudaFuncSetAttribute(d2t_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(psmem));
-        if (e != cudaSuccess) return e;
-        d2t_plan_kernel<<<1, kPlanThreads, psmem, stream>>>(d2t, d.width, t.width, A.plan);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (own_plan) {
+        if ((e = launch_d2t_plan_build(d2t, d.width, t.width, ws + L.plan, stream)) != cudaSuccess) return e;
     }
-    e = cudaFuncSetAttribute(sample_rows_kernel<DT, DD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(L.smem_bytes));
-    if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(L.grid));
-    cfg.blockDim = dim3(kRowThreads);
-    cfg.dynamicSmemBytes = L.smem_bytes;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = A.identity ? 0 : 1;
-    e = cudaLaunchKernelEx(&cfg, sample_rows_kernel<DT, DD>, A);
+    cfg.numAttrs = own_plan ? 1 : 0;
+    if (fast_path_ok(t, d, identity)) {
+        const size_t smem = fast_smem_bytes(t.width, d.width);
+        e = cudaFuncSetAttribute(sample_rows_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        cfg.gridDim = dim3(static_cast<unsigned>(L.grid));
+        cfg.blockDim = dim3(kFastThreads);
+        cfg.dynamicSmemBytes = smem;
+        e = cudaLaunchKernelEx(&cfg, sample_rows_fast_kernel, A);
+    } else {
+        e = cudaFuncSetAttribute(sample_rows_kernel<DT, DD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(L.smem_bytes));
+        if (e != cudaSuccess) return e;
+        cfg.gridDim = dim3(static_cast<unsigned>(L.grid));
+        cfg.blockDim = dim3(kRowThreads);
+        cfg.dynamicSmemBytes = L.smem_bytes;
+        e = cudaLaunchKernelEx(&cfg, sample_rows_kernel<DT, DD>, A);
+    }
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg2 = {};
     cfg2.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(R) * A.race_ctas));
@@ -1047,14 +1583,14 @@ static cudaError_t launch_sample_t(const Rows& t, const Rows& d, const int32_t* 
 }
 
 cudaError_t launch_verify_sample(const Rows& target, const Rows& draft_logits, const int32_t* d2t,
-                                 int32_t R, int32_t k, const int32_t* draft, const uint64_t* seeds,
-                                 const float* temperature, int32_t* accept_len, int32_t* tokens,
-                                 float* tv, float* p_draft, float* q_draft, int32_t* status,
+                                 const void* d2t_plan, int32_t R, int32_t k, const int32_t* draft,
+                                 const uint64_t* seeds, const float* temperature, int32_t* accept_len,
+                                 int32_t* tokens, float* tv, float* p_draft, float* q_draft, int32_t* status,
                                  void* workspace, cudaStream_t stream)
 {
     const bool tb = target.dtype == SV_BF16, db = draft_logits.dtype == SV_BF16;
-#define SV_SAMPLE_CALL(A_, B_)                                                                     \
-    launch_sample_t<A_, B_>(target, draft_logits, d2t, R, k, draft, seeds, temperature, accept_len, \
+#define SV_SAMPLE_CALL(A_, B_)                                                                            \
+    launch_sample_t<A_, B_>(target, draft_logits, d2t, d2t_plan, R, k, draft, seeds, temperature, accept_len, \
                             tokens, tv, p_draft, q_draft, status, workspace, stream)
     if (tb && db) return SV_SAMPLE_CALL(SV_BF16, SV_BF16);
     if (tb && !db) return SV_SAMPLE_CALL(SV_BF16, SV_F32);

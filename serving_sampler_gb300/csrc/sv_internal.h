@@ -47,10 +47,12 @@ cudaError_t launch_accept_scan(const uint8_t* accept, const int32_t* draft, cons
 
 size_t sample_workspace_bytes(int64_t R, int32_t k, int32_t V, int32_t Vd);
 cudaError_t launch_verify_sample(const Rows& target, const Rows& draft_logits, const int32_t* d2t,
-                                 int32_t R, int32_t k, const int32_t* draft, const uint64_t* seeds,
-                                 const float* temperature, int32_t* accept_len, int32_t* tokens,
-                                 float* tv, float* p_draft, float* q_draft, int32_t* status,
+                                 const void* d2t_plan, int32_t R, int32_t k, const int32_t* draft,
+                                 const uint64_t* seeds, const float* temperature, int32_t* accept_len,
+                                 int32_t* tokens, float* tv, float* p_draft, float* q_draft, int32_t* status,
                                  void* workspace, cudaStream_t stream);
+size_t d2t_plan_bytes(int32_t V, int32_t Vd);
+cudaError_t launch_d2t_plan_build(const int32_t* d2t, int32_t Vd, int32_t V, void* plan, cudaStream_t stream);
 
 // largest target vocabulary accepted together with a d2t map
 int32_t sample_max_plan_width();

@@ -128,3 +128,30 @@ def test_d2t_workload_full_size(sv):
     again = _run(sv, w)
     for key in ("accept_len", "tokens", "tv"):
         assert np.array_equal(np.nan_to_num(again[key]), np.nan_to_num(got[key]))
+
+
+def test_prebuilt_plan_matches_in_call_plan(sv):
+    w = workloads.d2t_workload(R=24)
+    plan = sv.d2t_plan(w["d2t"], w["V"])
+    a = _run(sv, w)
+    got = sv.verify_sample(w["target"], w["draft_logits"], None, w["R"], w["k"], w["draft"], w["seeds"],
+                           w["temperature"], plan=plan)
+    torch.cuda.synchronize()
+    b = {key: v.cpu().numpy() for key, v in got.items()}
+    for key in a:
+        np.testing.assert_array_equal(np.nan_to_num(a[key]), np.nan_to_num(b[key]), err_msg=key)
+    compare(b, _oracle(w))
+
+
+def test_bad_and_mismatched_d2t_are_flagged(sv):
+    w = workloads.sample_batch(4, 3, 4096, 512, torch.bfloat16, T=1.0, sigma_pos=0.5, delta=2.0, seed=2)
+    d2t = w["d2t"].clone()
+    d2t[7] = d2t[3]  # repeated target id
+    got = sv.verify_sample(w["target"], w["draft_logits"], d2t, 4, 3, w["draft"], w["seeds"], w["temperature"])
+    torch.cuda.synchronize()
+    assert np.all(got["status"].cpu().numpy() & 32)
+    other = sv.d2t_plan(w["d2t"][:256].contiguous(), 4096)  # a plan for another draft vocabulary
+    got = sv.verify_sample(w["target"], w["draft_logits"], None, 4, 3, w["draft"], w["seeds"], w["temperature"],
+                           plan=other)
+    torch.cuda.synchronize()
+    assert np.all(got["status"].cpu().numpy() & 32)
