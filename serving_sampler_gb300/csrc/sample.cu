@@ -36,13 +36,14 @@ namespace sv {
 namespace {
 
 constexpr int kPlanThreads = 1024;
+constexpr int32_t kChunkElems = 2048;  // ids per bulk-copied chunk of the bf16 fast path (4 KB)
 constexpr int kRowThreads = 512;
 constexpr uint32_t kStageBytes = 16384;
 constexpr int kStages = 4;
 constexpr int kRowHeader = 128;
 constexpr uint32_t kSmemBudget = 220 * 1024;
 constexpr int kRaceThreads = 256;
-constexpr int32_t kRaceSeg = 8192;  // elements of the race row per CTA (fp32 q cache: 32 KB)
+constexpr int32_t kRaceSeg = 8192;  // elements of the race row per CTA
 constexpr int32_t kMaxPlanWords = 25600;  // d2t mode supports V <= 819,200
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -53,7 +54,9 @@ struct D2tPlan {
     int32_t* prefix;   // [nw + 1] set bits before each word
     int32_t* xs;       // [Vd] support target ids, ascending
     int32_t* js;       // [Vd] the draft id of xs[pos]
-    uint16_t* js16;    // [Vd] the same draft ids as 16-bit values (Vd <= 65535)
+    uint32_t* pairs;   // [Vd] (draft id << 16) | (xs & (kChunkElems - 1)), ascending xs (Vd <= 65535)
+    int32_t* chunk;    // [V / kChunkElems + 2] support rank at every multiple of kChunkElems
+    int32_t* x_of_j;   // [Vd] target id of every draft id (a copy of d2t)
     int32_t* header;   // [0] V, [1] Vd the plan was built for, [2] d2t out of range or repeated
     int32_t nw;
 };
@@ -66,7 +69,10 @@ struct RowStat {
     int32_t amax;     // raw argmax of the target row
     uint32_t flags;   // kFlag* of the target and draft rows
     int32_t accept;   // accept decision of position j
-    int32_t pad[2];
+    int32_t rx;       // target id of the largest residual p - q on the support (-1: none)
+    float rv;         // that residual
+    float bkey;       // race key of the candidate bx_c if this row is raced (+inf: no bound)
+    int32_t bxc;      // the candidate (-1: none)
 };
 
 struct RaceSlot {
@@ -301,6 +307,12 @@ __global__ void __launch_bounds__(kPlanThreads)
         pl.bitmap[w] = bits[w];
         pl.prefix[w] = pref[w];
     }
+    for (int32_t j = tid; j < Vd; j += kPlanThreads) pl.x_of_j[j] = d2t[j];
+    for (int32_t c = tid; c <= (V + kChunkElems - 1) / kChunkElems; c += kPlanThreads) {
+        const int32_t x = min(V, c * kChunkElems);
+        const int32_t w = x >> 5, b = x & 31;
+        pl.chunk[c] = pref[w] + (b ? __popc(bits[w] & ((1u << b) - 1u)) : 0);
+    }
     if (tid == 0) {
         pl.prefix[pl.nw] = pref[pl.nw];
         pl.header[0] = V;
@@ -315,7 +327,7 @@ __global__ void __launch_bounds__(kPlanThreads)
         if (pos >= 0 && pos < Vd) {
             pl.xs[pos] = x;
             pl.js[pos] = j;
-            pl.js16[pos] = static_cast<uint16_t>(j);
+            pl.pairs[pos] = (static_cast<uint32_t>(j) << 16) | static_cast<uint32_t>(x & (kChunkElems - 1));
         }
     }
 }
@@ -701,7 +713,10 @@ __global__ void __launch_bounds__(kRowThreads, 1) sample_rows_kernel(SampleArgs 
             rs.amax = amax;
             rs.flags = flags;
             rs.accept = acc;
-            rs.pad[0] = rs.pad[1] = 0;
+            rs.rx = -1;
+            rs.rv = 0.f;
+            rs.bkey = INFINITY;
+            rs.bxc = -1;
             A.stats[unit] = rs;
             if (j < A.k) {
                 const int64_t o = static_cast<int64_t>(r) * A.k + j;
@@ -724,27 +739,24 @@ __global__ void __launch_bounds__(kRowThreads, 1) sample_rows_kernel(SampleArgs 
 // ---------------------------------------------------------------------------
 // row pass, fast path: bf16 target and draft rows, d2t vocabulary <= 32768
 // ---------------------------------------------------------------------------
-// Warp 0 is the producer: its lane 0 walks the same (unit, chunk) sequence
-// as the consumers and keeps kFastStages stages in flight, each holding a
-// 16 KB slice of a row plus, for target chunks, the 16-bit draft ids of the
-// support positions inside that slice.  Warps 1..16 consume: for each chunk
-// they wait on its `full` barrier and each warp arrives on its `empty`
-// barrier when done, so no block-wide barrier runs per chunk.  The support
-// bitmap and prefix counts stay in shared memory for the whole kernel; the
-// target logit of every support id is scattered to G[draft id], so the TV
-// pass reads G and the (L2-resident) draft row in draft-id order.
+// Every warp streams its own share of a row: chunks of kChunkElems ids,
+// chunk c going to warp c % kFastWarps, through a private two-stage ring of
+// bulk copies that the warp's lane 0 issues one chunk ahead.  Each stage also
+// receives the chunk's support entries as packed (draft id, offset) pairs,
+// so the warp scatters the support logits to G[draft id] from shared memory.
+// Warps never wait for each other inside a row; only the row's reductions
+// and the TV pass (over G and the L2-resident draft row, in draft-id order)
+// synchronise the CTA, and each warp has already issued its first chunk of
+// the next row before they start.
 namespace {
 
-constexpr int kFastConsumerWarps = 16;
-constexpr int kFastConsumers = 32 * kFastConsumerWarps;
-constexpr int kFastThreads = kFastConsumers + 32;
-constexpr int kFastStages = 5;
-constexpr uint32_t kFastData = 16384;                       // 8192 bf16 per stage
-constexpr uint32_t kFastJsCap = 4096;                       // 2048 staged draft ids per stage
-constexpr uint32_t kFastStage = kFastData + kFastJsCap + 16;
+constexpr int kFastWarps = 12;
+constexpr int kFastThreads = 32 * kFastWarps;
+constexpr uint32_t kFastData = kChunkElems * 2;  // 4 KB of bf16 per stage
+constexpr uint32_t kFastPairCap = 512;           // staged support entries per stage
+constexpr uint32_t kFastStage = kFastData + kFastPairCap * 4;
 constexpr int kFastHeader = 256;
 constexpr int32_t kFastMaxVd = 32768;
-constexpr int32_t kFastMaxWords = 6144;                     // V <= 196,608
 
 __device__ __forceinline__ float ex2(float x)
 {
@@ -753,79 +765,69 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar)
+// two fp32 values in one 64-bit register, for the packed f32x2 instructions
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi)
 {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpack2(unsigned long long v, float& lo, float& hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c)
+{
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b)
+{
+    unsigned long long r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
 }
 
-__device__ __forceinline__ void consumer_sync()
+// the bf16x2 word w as two fp32 values (exact) in one 64-bit register
+__device__ __forceinline__ unsigned long long bf16x2_to_f32x2(uint32_t w)
 {
-    asm volatile("bar.sync 1, %0;" ::"n"(kFastConsumers) : "memory");
+    return pack2(bf16_lo(w), bf16_hi(w));
 }
 
-__device__ __forceinline__ float csum(float v, float* sc)
+// sum over the 8 bf16 values z of a vector of 2^(z c - m): packed fp32x2
+// arguments, eight independent MUFU operations, a tree of packed adds
+__device__ __forceinline__ float exp_sum8(uint4 q, unsigned long long c2, unsigned long long nm2)
 {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    const int w = (threadIdx.x >> 5) - 1;
-    consumer_sync();
-    if ((threadIdx.x & 31) == 0) sc[w] = v;
-    consumer_sync();
-    float t = 0.f;
-    for (int i = 0; i < kFastConsumerWarps; ++i) t += sc[i];
-    return t;
+    const unsigned long long t0 = fma2(bf16x2_to_f32x2(q.x), c2, nm2);
+    const unsigned long long t1 = fma2(bf16x2_to_f32x2(q.y), c2, nm2);
+    const unsigned long long t2 = fma2(bf16x2_to_f32x2(q.z), c2, nm2);
+    const unsigned long long t3 = fma2(bf16x2_to_f32x2(q.w), c2, nm2);
+    float a0, a1, a2, a3, a4, a5, a6, a7;
+    unpack2(t0, a0, a1);
+    unpack2(t1, a2, a3);
+    unpack2(t2, a4, a5);
+    unpack2(t3, a6, a7);
+    const unsigned long long e0 = pack2(ex2(a0), ex2(a1)), e1 = pack2(ex2(a2), ex2(a3));
+    const unsigned long long e2 = pack2(ex2(a4), ex2(a5)), e3 = pack2(ex2(a6), ex2(a7));
+    float lo, hi;
+    unpack2(add2(add2(e0, e1), add2(e2, e3)), lo, hi);
+    return lo + hi;
 }
 
-__device__ __forceinline__ float cmax(float v, float* sc)
+// 16-byte read-only global load
+__device__ __forceinline__ uint4 ld_nc_v4(const uint4* p)
 {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    const int w = (threadIdx.x >> 5) - 1;
-    consumer_sync();
-    if ((threadIdx.x & 31) == 0) sc[w] = v;
-    consumer_sync();
-    float t = -INFINITY;
-    for (int i = 0; i < kFastConsumerWarps; ++i) t = fmaxf(t, sc[i]);
-    return t;
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
 }
 
-__device__ __forceinline__ uint32_t cor(uint32_t v, uint32_t* sc)
+// order this thread's generic-proxy accesses to shared memory before later
+// bulk copies (async proxy) into the same bytes
+__device__ __forceinline__ void fence_proxy_async_smem()
 {
-    v = __reduce_or_sync(0xffffffffu, v);
-    const int w = (threadIdx.x >> 5) - 1;
-    consumer_sync();
-    if ((threadIdx.x & 31) == 0) sc[w] = v;
-    consumer_sync();
-    uint32_t t = 0;
-    for (int i = 0; i < kFastConsumerWarps; ++i) t |= sc[i];
-    return t;
-}
-
-__device__ __forceinline__ void cargmax(float& v, int32_t& x, float* sv, int32_t* sx)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-        const int32_t ox = __shfl_xor_sync(0xffffffffu, x, o);
-        if (ov > v || (ov == v && ox < x)) {
-            v = ov;
-            x = ox;
-        }
-    }
-    const int w = (threadIdx.x >> 5) - 1;
-    consumer_sync();
-    if ((threadIdx.x & 31) == 0) {
-        sv[w] = v;
-        sx[w] = x;
-    }
-    consumer_sync();
-    v = sv[0];
-    x = sx[0];
-    for (int i = 1; i < kFastConsumerWarps; ++i)
-        if (sv[i] > v || (sv[i] == v && sx[i] < x)) {
-            v = sv[i];
-            x = sx[i];
-        }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // replace NaN halves of a bf16x2 word by -inf
@@ -837,12 +839,19 @@ __device__ __forceinline__ uint32_t bf16x2_nan_to_ninf(uint32_t w)
     return lo | (hi << 16);
 }
 
+struct WarpRec {
+    float bv;
+    int32_t bx;
+    uint32_t tfl, dfl;
+    float tm, dm;
+};
+
 struct FastUnit {
     int32_t r, j;
     bool sampling, has_draft;
     const char* trow;
     const char* drow;
-    uint32_t nd, nt;  // draft / target chunks
+    int32_t nd, nt;  // draft / target chunks of the row
 };
 
 __device__ __forceinline__ FastUnit fast_unit(const SampleArgs& A, int64_t unit)
@@ -855,9 +864,44 @@ __device__ __forceinline__ FastUnit fast_unit(const SampleArgs& A, int64_t unit)
     u.has_draft = u.sampling && u.j < A.k;
     u.trow = A.tbase + unit * A.tstride;
     u.drow = u.has_draft ? A.dbase + (static_cast<int64_t>(u.r) * A.k + u.j) * A.dstride : nullptr;
-    u.nd = u.has_draft ? (static_cast<uint32_t>(A.Vd) * 2 + kFastData - 1) / kFastData : 0u;
-    u.nt = (static_cast<uint32_t>(A.V) * 2 + kFastData - 1) / kFastData;
+    u.nd = u.has_draft ? (A.Vd + kChunkElems - 1) / kChunkElems : 0;
+    u.nt = (A.V + kChunkElems - 1) / kChunkElems;
     return u;
+}
+
+// chunks of warp w in a row: draft chunks w, w + W, ... then target chunks w, w + W, ...
+__device__ __forceinline__ int32_t warp_chunks(int32_t n, int w)
+{
+    return n > w ? (n - w + kFastWarps - 1) / kFastWarps : 0;
+}
+
+// issue the i-th chunk of warp w of unit u into `stage` (lane 0 only)
+__device__ __forceinline__ void issue_warp_chunk(const SampleArgs& A, const FastUnit& u, int w, int32_t i,
+                                                 unsigned char* stage, uint64_t* bar, uint64_t pol_t,
+                                                 uint64_t pol_d, bool plan_ok)
+{
+    const int32_t ndw = warp_chunks(u.nd, w);
+    if (i < ndw) {
+        const int32_t c = w + i * kFastWarps;
+        const uint32_t off = static_cast<uint32_t>(c) * kFastData;
+        const uint32_t nb = min(kFastData, static_cast<uint32_t>(A.Vd) * 2 - off);
+        mbar_arrive_expect_tx(bar, nb);
+        bulk_copy_g2s(stage, u.drow + off, nb, bar, pol_d);
+        return;
+    }
+    const int32_t c = w + (i - ndw) * kFastWarps;
+    const uint32_t off = static_cast<uint32_t>(c) * kFastData;
+    const uint32_t nb = min(kFastData, static_cast<uint32_t>(A.V) * 2 - off);
+    uint32_t pb = 0;
+    int32_t p0a = 0;
+    if (u.has_draft && plan_ok) {
+        const int32_t p0 = A.plan.chunk[c], p1 = A.plan.chunk[c + 1];
+        p0a = p0 & ~3;
+        if (p1 > p0) pb = min(kFastPairCap * 4, static_cast<uint32_t>((p1 - p0a) * 4 + 15) & ~15u);
+    }
+    mbar_arrive_expect_tx(bar, nb + pb);
+    bulk_copy_g2s(stage, u.trow + off, nb, bar, pol_t);
+    if (pb) bulk_copy_g2s(stage + kFastData, A.plan.pairs + p0a, pb, bar, pol_d);
 }
 
 }  // namespace
@@ -865,250 +909,239 @@ __device__ __forceinline__ FastUnit fast_unit(const SampleArgs& A, int64_t unit)
 __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(SampleArgs A)
 {
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-    uint64_t* empty = full + kFastStages;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // [warp][2]
     unsigned char* ring = smem + kFastHeader;
-    uint16_t* G = reinterpret_cast<uint16_t*>(ring + kFastStages * kFastStage);
-    const int32_t nw = A.plan.nw;
-    uint32_t* sbits = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(G) + align256(static_cast<int64_t>(A.Vd) * 2));
-    int32_t* spref = reinterpret_cast<int32_t*>(sbits + nw);
-    __shared__ float red_f[kFastConsumerWarps];
-    __shared__ int32_t red_i[kFastConsumerWarps];
-    __shared__ uint32_t red_u[kFastConsumerWarps];
+    uint16_t* G = reinterpret_cast<uint16_t*>(ring + kFastWarps * 2 * kFastStage);
     __shared__ float zx_shared;
-    const int tid = threadIdx.x;
+    __shared__ int32_t rx_shared;
+    __shared__ float rv_shared;
+    __shared__ WarpRec wrec[kFastWarps];
+    __shared__ float wsum[kFastWarps][2];
+    __shared__ float wtv[kFastWarps], wrv[kFastWarps];
+    __shared__ int32_t wrj[kFastWarps];
+    __shared__ int32_t amax_shared;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
 
     pdl_wait_primary();  // a plan built in the same call must be complete
     pdl_launch_dependents();
     if (tid == 0) {
-        for (int s = 0; s < kFastStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kFastConsumerWarps);
-        }
+        for (int i = 0; i < 2 * kFastWarps; ++i) mbar_init(&bars[i], 1);
         fence_barrier_init();
     }
-    for (int32_t w = tid; w < nw; w += kFastThreads) {
-        sbits[w] = A.plan.bitmap[w];
-        spref[w] = A.plan.prefix[w];
-    }
-    if (tid == 0) spref[nw] = A.plan.prefix[nw];
     __syncthreads();
+    // a plan for other sizes, or built from a d2t with repeated / out-of-range ids, is not
+    // trusted for shared-memory indexing (the race kernel reports SV_ST_BAD_D2T)
+    const bool plan_ok = A.plan.header[0] == A.V && A.plan.header[1] == A.Vd && A.plan.header[2] == 0;
+    const uint64_t pol_t = l2_policy_evict_first();
+    uint64_t pol_d;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_d));
+    unsigned char* wst = ring + w * 2 * kFastStage;  // this warp's two stages
+    uint64_t* wbar = bars + 2 * w;
+    uint32_t gi = 0;  // chunks this warp has consumed so far (stage = gi & 1)
+    uint32_t timeout = 0;
+    bool prefetched = false;
 
     const int64_t units = static_cast<int64_t>(A.R) * (A.k + 1);
-    if (tid < 32) {
-        // ---------------- producer ----------------
-        if (tid != 0) return;
-        const uint64_t pol_t = l2_policy_evict_first();
-        uint64_t pol_d;
-        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_d));
-        uint32_t g = 0;
-        for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
-            const FastUnit u = fast_unit(A, unit);
-            const uint32_t n = u.nd + u.nt;
-            for (uint32_t i = 0; i < n; ++i, ++g) {
-                const uint32_t s = g % kFastStages;
-                if (!mbar_wait_bounded(&empty[s], ((g / kFastStages) & 1u) ^ 1u)) return;  // consumers record the timeout
-                unsigned char* st = ring + s * kFastStage;
-                if (i < u.nd) {
-                    const uint32_t off = i * kFastData;
-                    const uint32_t nb = min(kFastData, static_cast<uint32_t>(A.Vd) * 2 - off);
-                    mbar_arrive_expect_tx(&full[s], nb);
-                    bulk_copy_g2s(st, u.drow + off, nb, &full[s], pol_d);
-                } else {
-                    const uint32_t t = i - u.nd;
-                    const uint32_t off = t * kFastData;
-                    const uint32_t nb = min(kFastData, static_cast<uint32_t>(A.V) * 2 - off);
-                    uint32_t js_bytes = 0;
-                    int32_t p0a = 0;
-                    if (u.has_draft) {
-                        const int32_t x0 = static_cast<int32_t>(off / 2), x1 = x0 + static_cast<int32_t>(nb / 2);
-                        const int32_t p0 = spref[x0 >> 5];
-                        const int32_t w1 = x1 >> 5, b1 = x1 & 31;
-                        const int32_t p1 = spref[w1] + (b1 ? __popc(sbits[w1] & ((1u << b1) - 1u)) : 0);
-                        p0a = p0 & ~7;
-                        js_bytes = min(kFastJsCap, static_cast<uint32_t>((p1 - p0a) * 2 + 15) & ~15u);
-                        if (p1 <= p0) js_bytes = 0;
-                    }
-                    mbar_arrive_expect_tx(&full[s], nb + js_bytes);
-                    bulk_copy_g2s(st, u.trow + off, nb, &full[s], pol_t);
-                    if (js_bytes) bulk_copy_g2s(st + kFastData, A.plan.js16 + p0a, js_bytes, &full[s], pol_d);
-                }
-            }
-        }
-        return;
-    }
-
-    // ---------------- consumers ----------------
-    const int ct = tid - 32;
-    uint32_t g = 0;
-    uint32_t timeout = 0;
     for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
         const FastUnit u = fast_unit(A, unit);
         const float T = A.temp[u.r];
         const float c = u.sampling ? kLog2e / T : 0.f;
+        const unsigned long long c2 = pack2(c, c);
         const int32_t xj = u.has_draft ? A.draft[static_cast<int64_t>(u.r) * A.k + u.j] : -1;
-        if (u.j == 0 && ct == 0) {
+        const int32_t ndw = warp_chunks(u.nd, w), ntw = warp_chunks(u.nt, w);
+        const int32_t nw_chunks = ndw + ntw;
+        if (u.j == 0 && tid == 0) {
             A.race[u.r].best = ~0ull;
             A.race[u.r].count = 0u;
         }
-        if (ct == 0) zx_shared = NAN;
-        consumer_sync();  // G and zx of the previous unit are no longer read
+        if (tid == 0) zx_shared = NAN;
+        __syncthreads();  // G, zx and the exchange arrays of the previous row are no longer read
+        if (lane == 0 && !prefetched && nw_chunks > 0)
+            issue_warp_chunk(A, u, w, 0, wst + (gi & 1) * kFastStage, &wbar[gi & 1], pol_t, pol_d, plan_ok);
 
-        // ---- draft row: max and sum 2^(y c - max) ----
-        float dm = -INFINITY, ds = 0.f;
-        uint32_t dflags = 0;
-        for (uint32_t i = 0; i < u.nd; ++i, ++g) {
-            const uint32_t s = g % kFastStages;
-            if (!timeout && !mbar_wait_bounded(&full[s], (g / kFastStages) & 1u)) timeout = 1;
-            const uint4* vp = reinterpret_cast<const uint4*>(ring + s * kFastStage);
-            const int nv = static_cast<int>(min(kFastData, static_cast<uint32_t>(A.Vd) * 2 - i * kFastData) / 16);
-            for (int v = ct; v < nv; v += kFastConsumers) {
-                uint4 q = vp[v];
-                const uint32_t m2 = bmax2_nan(bmax2_nan(q.x, q.y), bmax2_nan(q.z, q.w));
-                float vm = fmax_nan(bf16_lo(m2), bf16_hi(m2));
-                if (vm != vm) {
-                    dflags |= kFlagNaN;
-                    q = make_uint4(bf16x2_nan_to_ninf(q.x), bf16x2_nan_to_ninf(q.y), bf16x2_nan_to_ninf(q.z),
-                                   bf16x2_nan_to_ninf(q.w));
-                    const uint32_t m3 = bmax2_nan(bmax2_nan(q.x, q.y), bmax2_nan(q.z, q.w));
-                    vm = fmaxf(bf16_lo(m3), bf16_hi(m3));
-                }
-                if (vm == INFINITY) dflags |= kFlagPosInf;
-                const float mt = vm * c;
-                if (mt > dm) {
-                    ds = dm == -INFINITY ? 0.f : ds * ex2(dm - mt);
-                    dm = mt;
-                }
-                if (dm > -INFINITY) {
-                    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-                    float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        a0 += ex2(fmaf(bf16_lo(w[e]), c, -dm));
-                        a1 += ex2(fmaf(bf16_hi(w[e]), c, -dm));
-                    }
-                    ds += a0 + a1;
-                }
-            }
-            __syncwarp();
-            if ((ct & 31) == 0) mbar_arrive(&empty[s]);
-        }
-
-        // ---- target row ----
-        float tm = -INFINITY, ts = 0.f;
-        float bv = -INFINITY;
+        float dm = -INFINITY, ds = 0.f, tm = -INFINITY, ts = 0.f, bv = -INFINITY;
         int32_t bx = INT32_MAX;
-        uint32_t tflags = 0;
-        for (uint32_t t = 0; t < u.nt; ++t, ++g) {
-            const uint32_t s = g % kFastStages;
-            if (!timeout && !mbar_wait_bounded(&full[s], (g / kFastStages) & 1u)) timeout = 1;
-            const unsigned char* st = ring + s * kFastStage;
+        uint32_t dflags = 0, tflags = 0;
+        for (int32_t i = 0; i < nw_chunks; ++i, ++gi) {
+            const uint32_t s = gi & 1;
+            if (lane == 0 && i + 1 < nw_chunks) {
+                fence_proxy_async_smem();
+                issue_warp_chunk(A, u, w, i + 1, wst + (s ^ 1) * kFastStage, &wbar[s ^ 1], pol_t, pol_d, plan_ok);
+            }
+            if (!timeout && !mbar_wait_bounded(&wbar[s], (gi >> 1) & 1u)) timeout = 1;
+            const unsigned char* st = wst + s * kFastStage;
             const uint4* vp = reinterpret_cast<const uint4*>(st);
-            const uint16_t* js_st = reinterpret_cast<const uint16_t*>(st + kFastData);
-            const uint32_t off = t * kFastData;
-            const uint32_t nb = min(kFastData, static_cast<uint32_t>(A.V) * 2 - off);
+            const bool is_draft = i < ndw;
+            const int32_t cidx = w + (is_draft ? i : i - ndw) * kFastWarps;
+            const uint32_t off = static_cast<uint32_t>(cidx) * kFastData;
+            const uint32_t nb = min(kFastData, static_cast<uint32_t>(is_draft ? A.Vd : A.V) * 2 - off);
             const int nv = static_cast<int>(nb / 16);
             const int32_t x0 = static_cast<int32_t>(off / 2);
-            int32_t p0a = 0, nstaged = 0;
-            if (u.has_draft) {
-                const int32_t x1 = x0 + static_cast<int32_t>(nb / 2);
-                const int32_t p0 = spref[x0 >> 5];
-                const int32_t w1 = x1 >> 5, b1 = x1 & 31;
-                const int32_t p1 = spref[w1] + (b1 ? __popc(sbits[w1] & ((1u << b1) - 1u)) : 0);
-                p0a = p0 & ~7;
-                nstaged = p1 > p0 ? static_cast<int32_t>(min(kFastJsCap, static_cast<uint32_t>((p1 - p0a) * 2 + 15) & ~15u) / 2) : 0;
-            }
-            for (int v = ct; v < nv; v += kFastConsumers) {
-                uint4 q = vp[v];
-                const int32_t x = x0 + v * 8;
-                const uint32_t m2 = bmax2_nan(bmax2_nan(q.x, q.y), bmax2_nan(q.z, q.w));
-                float vm = fmax_nan(bf16_lo(m2), bf16_hi(m2));
-                if (vm != vm) {
-                    tflags |= kFlagNaN;
-                    q = make_uint4(bf16x2_nan_to_ninf(q.x), bf16x2_nan_to_ninf(q.y), bf16x2_nan_to_ninf(q.z),
-                                   bf16x2_nan_to_ninf(q.w));
-                    const uint32_t m3 = bmax2_nan(bmax2_nan(q.x, q.y), bmax2_nan(q.z, q.w));
-                    vm = fmaxf(bf16_lo(m3), bf16_hi(m3));
-                }
-                const bool up = vm > bv;
-                bv = up ? vm : bv;
-                bx = up ? x : bx;
-                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-                if (u.sampling) {
-                    const float mt = vm * c;
-                    if (mt > tm) {
-                        ts = tm == -INFINITY ? 0.f : ts * ex2(tm - mt);
-                        tm = mt;
-                    }
-                    if (tm > -INFINITY) {
-                        float a0 = 0.f, a1 = 0.f;
+            // all 8 vectors of this lane first (independent loads and max trees), one update of
+            // the running max, then 64 independent exps
+            constexpr int kVL = kChunkElems / 8 / 32;  // vectors per lane per chunk
+            uint4 q[kVL];
+            float vmx[kVL];
+            bool nan_seen = false;
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            a0 += ex2(fmaf(bf16_lo(w[e]), c, -tm));
-                            a1 += ex2(fmaf(bf16_hi(w[e]), c, -tm));
-                        }
-                        ts += a0 + a1;
-                    }
+            for (int e = 0; e < kVL; ++e) {
+                const int v = lane + 32 * e;
+                q[e] = v < nv ? vp[v] : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+                const uint32_t m2 = bmax2_nan(bmax2_nan(q[e].x, q[e].y), bmax2_nan(q[e].z, q[e].w));
+                vmx[e] = fmax_nan(bf16_lo(m2), bf16_hi(m2));
+                nan_seen |= vmx[e] != vmx[e];
+            }
+            if (nan_seen) {  // rare: NaN logits read as -inf
+                (is_draft ? dflags : tflags) |= kFlagNaN;
+#pragma unroll
+                for (int e = 0; e < kVL; ++e) {
+                    q[e] = make_uint4(bf16x2_nan_to_ninf(q[e].x), bf16x2_nan_to_ninf(q[e].y),
+                                      bf16x2_nan_to_ninf(q[e].z), bf16x2_nan_to_ninf(q[e].w));
+                    const uint32_t m3 = bmax2_nan(bmax2_nan(q[e].x, q[e].y), bmax2_nan(q[e].z, q[e].w));
+                    vmx[e] = fmaxf(bf16_lo(m3), bf16_hi(m3));
                 }
-                if (u.has_draft) {
-                    // scatter the support logits of this vector to G[draft id]
-                    const int32_t wi = x >> 5, sh = x & 31;
-                    const uint32_t word = sbits[wi];
-                    uint32_t bits = (word >> sh) & 0xFFu;
-                    if (bits) {
-                        const int32_t base = spref[wi] + (sh ? __popc(word & ((1u << sh) - 1u)) : 0) - p0a;
-                        const uint32_t all = bits;
-                        while (bits) {
-                            const int e = __ffs(bits) - 1;
-                            bits &= bits - 1;
-                            const int32_t li = base + __popc(all & ((1u << e) - 1u));
-                            const int32_t jd = li < nstaged ? js_st[li] : A.plan.js16[p0a + li];
-                            if (jd < A.Vd) G[jd] = static_cast<uint16_t>((e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu));
-                        }
-                    }
-                    if (static_cast<uint32_t>(xj - x) < 8u) {
-                        const int e = xj - x;
-                        zx_shared = (e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1]);
-                    }
+            }
+            float lm = vmx[0];
+#pragma unroll
+            for (int e = 1; e < kVL; ++e) lm = fmaxf(lm, vmx[e]);
+            if (!is_draft) {
+#pragma unroll
+                for (int e = 0; e < kVL; ++e) {  // ascending vector starts: strict > keeps the first
+                    const bool up = vmx[e] > bv;
+                    bv = up ? vmx[e] : bv;
+                    bx = up ? x0 + (lane + 32 * e) * 8 : bx;
                 }
+            } else if (lm == INFINITY) {
+                dflags |= kFlagPosInf;
+            }
+            if (is_draft || u.sampling) {
+                float& rm = is_draft ? dm : tm;
+                float& rs_ = is_draft ? ds : ts;
+                const float mt = lm * c;
+                if (mt > rm) {
+                    rs_ = rm == -INFINITY ? 0.f : rs_ * ex2(rm - mt);
+                    rm = mt;
+                }
+                if (rm > -INFINITY) {
+                    const unsigned long long nm2 = pack2(-rm, -rm);
+                    float acc8[kVL];
+#pragma unroll
+                    for (int e = 0; e < kVL; ++e) acc8[e] = exp_sum8(q[e], c2, nm2);
+#pragma unroll
+                    for (int e = 1; e < kVL; ++e) acc8[0] += acc8[e];
+                    rs_ += acc8[0];
+                }
+            }
+            if (!is_draft && u.has_draft) {
+                // support entries of this chunk: G[draft id] = z at the chunk offset
+                const uint16_t* zs = reinterpret_cast<const uint16_t*>(st);
+                const uint32_t* pr = reinterpret_cast<const uint32_t*>(st + kFastData);
+                const int32_t p0 = plan_ok ? A.plan.chunk[cidx] : 0;
+                const int32_t cnt = plan_ok ? A.plan.chunk[cidx + 1] - p0 : 0;
+                const int32_t base = p0 & 3;
+                const int32_t staged = min(cnt, static_cast<int32_t>(kFastPairCap) - base);
+#pragma unroll 4
+                for (int32_t e = lane; e < staged; e += 32) {
+                    const uint32_t pe = pr[base + e];
+                    G[pe >> 16] = zs[pe & (kChunkElems - 1)];
+                }
+                for (int32_t e = max(staged, 0) + lane; e < cnt; e += 32) {  // beyond the staged entries
+                    const uint32_t pe = A.plan.pairs[p0 + e];
+                    G[pe >> 16] = zs[pe & (kChunkElems - 1)];
+                }
+                if (lane == 0 && xj >= x0 && xj < x0 + static_cast<int32_t>(nb / 2))
+                    zx_shared = __uint_as_float(static_cast<uint32_t>(zs[xj - x0]) << 16);
             }
             __syncwarp();
-            if ((ct & 31) == 0) mbar_arrive(&empty[s]);
+        }
+        // first chunk of this warp's next row, in flight during the reductions below
+        prefetched = false;
+        if (unit + gridDim.x < units) {
+            const FastUnit un = fast_unit(A, unit + gridDim.x);
+            if (warp_chunks(un.nd, w) + warp_chunks(un.nt, w) > 0) {
+                if (lane == 0) {
+                    fence_proxy_async_smem();
+                    issue_warp_chunk(A, un, w, 0, wst + (gi & 1) * kFastStage, &wbar[gi & 1], pol_t, pol_d, plan_ok);
+                }
+                prefetched = true;
+            }
         }
 
-        // ---- reductions over the consumer warps ----
-        cargmax(bv, bx, red_f, red_i);
-        const uint32_t fl_t = cor(tflags, red_u);
-        const uint32_t fl_d = cor(dflags, red_u);
-        int32_t amax = 0;
-        if (bx != INT32_MAX) {
-            amax = bx;
+        // ---- reductions: two exchanges through shared memory ----
+        const float my_bv = bv, my_tm = tm, my_ts = ts, my_dm = dm, my_ds = ds;
+        const int32_t my_bx = bx;
+        uint32_t tfl = tflags | (timeout ? kFlagTimeout : 0u);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int32_t ox = __shfl_xor_sync(0xffffffffu, bx, o);
+            if (ov > bv || (ov == bv && ox < bx)) {
+                bv = ov;
+                bx = ox;
+            }
+            tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
+            dm = fmaxf(dm, __shfl_xor_sync(0xffffffffu, dm, o));
+        }
+        tfl = __reduce_or_sync(0xffffffffu, tfl);
+        dflags = __reduce_or_sync(0xffffffffu, dflags);
+        if (lane == 0) wrec[w] = WarpRec{bv, bx, tfl, dflags, tm, dm};
+        __syncthreads();
+        float BV = wrec[0].bv, M = wrec[0].tm, Mq = wrec[0].dm;
+        int32_t BX = wrec[0].bx;
+        uint32_t FLT = wrec[0].tfl, FLD = wrec[0].dfl;
+        for (int i = 1; i < kFastWarps; ++i) {
+            const WarpRec rec = wrec[i];
+            if (rec.bv > BV || (rec.bv == BV && rec.bx < BX)) {
+                BV = rec.bv;
+                BX = rec.bx;
+            }
+            M = fmaxf(M, rec.tm);
+            Mq = fmaxf(Mq, rec.dm);
+            FLT |= rec.tfl;
+            FLD |= rec.dfl;
+        }
+        // the thread that saw the winning vector finds the first equal element in it
+        if (my_bx == BX && my_bv == BV && BX != INT32_MAX) {
+            int32_t idx = BX;
             for (int e = 0; e < 8; ++e) {
-                const int32_t x = bx + e;
+                const int32_t x = BX + e;
                 if (x >= A.V) break;
-                if (ld_elem<SV_BF16>(u.trow, x) == bv) {
-                    amax = x;
+                if (ld_elem<SV_BF16>(u.trow, x) == BV) {
+                    idx = x;
                     break;
                 }
             }
+            amax_shared = idx;
         }
-        float M = -INFINITY, S = 0.f, Mq = -INFINITY, Sq = 0.f;
-        if (u.sampling) {
-            M = cmax(tm, red_f);
-            const float sc = (tm == -INFINITY || M == -INFINITY) ? 0.f : ex2(tm - M);
-            S = csum(ts * sc, red_f);
+        if (tid == 0 && BX == INT32_MAX) amax_shared = 0;
+        float S = 0.f, Sq = 0.f;
+        {
+            float part_t = 0.f, part_d = 0.f;
+            if (u.sampling && my_tm > -INFINITY && M > -INFINITY) part_t = my_ts * ex2(my_tm - M);
+            if (u.has_draft && my_dm > -INFINITY && Mq > -INFINITY) part_d = my_ds * ex2(my_dm - Mq);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                part_t += __shfl_xor_sync(0xffffffffu, part_t, o);
+                part_d += __shfl_xor_sync(0xffffffffu, part_d, o);
+            }
+            if (lane == 0) {
+                wsum[w][0] = part_t;
+                wsum[w][1] = part_d;
+            }
+            __syncthreads();
+            for (int i = 0; i < kFastWarps; ++i) {
+                S += wsum[i][0];
+                Sq += wsum[i][1];
+            }
         }
-        if (u.has_draft) {
-            Mq = cmax(dm, red_f);
-            const float sc = (dm == -INFINITY || Mq == -INFINITY) ? 0.f : ex2(dm - Mq);
-            Sq = csum(ds * sc, red_f);
-        }
+        if (!u.sampling) M = -INFINITY;
+        if (!u.has_draft) Mq = -INFINITY;
         uint32_t flags = 0;
-        if (fl_t & kFlagNaN) flags |= kFlagNaN;
-        if (bv == INFINITY) flags |= kFlagPosInf;
-        if (bv == -INFINITY) flags |= kFlagAllNegInf;
-        if (u.has_draft && ((fl_d & (kFlagNaN | kFlagPosInf)) || Mq == -INFINITY)) flags |= kFlagDraftBad;
-        if (cor(timeout, red_u)) flags |= kFlagTimeout;
+        if (FLT & kFlagNaN) flags |= kFlagNaN;
+        if (FLT & kFlagTimeout) flags |= kFlagTimeout;
+        if (BV == INFINITY) flags |= kFlagPosInf;
+        if (BV == -INFINITY) flags |= kFlagAllNegInf;
+        if (u.has_draft && ((FLD & (kFlagNaN | kFlagPosInf)) || Mq == -INFINITY)) flags |= kFlagDraftBad;
 
         // ---- TV = sum over the support of max(0, q - p); p(x_j), q(x_j), accept ----
         float tvv = NAN, pj = NAN, qj = NAN;
@@ -1116,54 +1149,98 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
         if (u.has_draft) {
             const float invS = 1.f / S, invSq = 1.f / Sq;
             float a = 0.f;
+            float rbest = 0.f;  // largest residual p - q seen and its draft id
+            int32_t rj = -1;
             const int32_t nv8 = A.Vd / 8;
             const uint4* yv = reinterpret_cast<const uint4*>(u.drow);
             const uint4* gv = reinterpret_cast<const uint4*>(G);
-            for (int32_t v = ct; v < nv8; v += kFastConsumers) {
+            for (int32_t v = tid; v < nv8; v += kFastThreads) {
                 const uint4 gq = gv[v];
-                const uint4 yq = yv[v];
+                const uint4 yq = ld_nc_v4(yv + v);
                 const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
                 const uint32_t yw[4] = {yq.x, yq.y, yq.z, yq.w};
+                float d[8];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float p0 = ex2(fmaf(bf16_lo(gw[e]), c, -M)) * invS;
-                    const float p1 = ex2(fmaf(bf16_hi(gw[e]), c, -M)) * invS;
-                    const float q0 = ex2(fmaf(bf16_lo(yw[e]), c, -Mq)) * invSq;
-                    const float q1 = ex2(fmaf(bf16_hi(yw[e]), c, -Mq)) * invSq;
-                    a += fmaxf(q0 - p0, 0.f) + fmaxf(q1 - p1, 0.f);
+                    d[2 * e] = ex2(fmaf(bf16_lo(yw[e]), c, -Mq)) * invSq - ex2(fmaf(bf16_lo(gw[e]), c, -M)) * invS;
+                    d[2 * e + 1] = ex2(fmaf(bf16_hi(yw[e]), c, -Mq)) * invSq - ex2(fmaf(bf16_hi(gw[e]), c, -M)) * invS;
+                }
+                // d = q - p: TV sums its positive part; the most negative d is the largest residual p - q
+                float dmin = d[0];
+                int emin = 0;
+#pragma unroll
+                for (int e = 1; e < 8; ++e) {
+                    const bool lt = d[e] < dmin;
+                    dmin = lt ? d[e] : dmin;
+                    emin = lt ? e : emin;
+                }
+                if (-dmin > rbest) {
+                    rbest = -dmin;
+                    rj = v * 8 + emin;
+                }
+                a += ((fmaxf(d[0], 0.f) + fmaxf(d[1], 0.f)) + (fmaxf(d[2], 0.f) + fmaxf(d[3], 0.f))) +
+                     ((fmaxf(d[4], 0.f) + fmaxf(d[5], 0.f)) + (fmaxf(d[6], 0.f) + fmaxf(d[7], 0.f)));
+            }
+            for (int32_t jd = nv8 * 8 + tid; jd < A.Vd; jd += kFastThreads) {
+                const float pp = ex2(fmaf(__uint_as_float(static_cast<uint32_t>(G[jd]) << 16), c, -M)) * invS;
+                const float qq = ex2(fmaf(ld_elem<SV_BF16>(u.drow, jd), c, -Mq)) * invSq;
+                a += fmaxf(qq - pp, 0.f);
+            }
+            // one exchange: the TV sum and the largest support residual
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                a += __shfl_xor_sync(0xffffffffu, a, o);
+                const float ov = __shfl_xor_sync(0xffffffffu, rbest, o);
+                const int32_t oj = __shfl_xor_sync(0xffffffffu, rj, o);
+                if (ov > rbest || (ov == rbest && oj < rj)) {
+                    rbest = ov;
+                    rj = oj;
                 }
             }
-            for (int32_t jd = nv8 * 8 + ct; jd < A.Vd; jd += kFastConsumers) {
-                const float p = ex2(fmaf(__uint_as_float(static_cast<uint32_t>(G[jd]) << 16), c, -M)) * invS;
-                const float q = ex2(fmaf(ld_elem<SV_BF16>(u.drow, jd), c, -Mq)) * invSq;
-                a += fmaxf(q - p, 0.f);
+            if (lane == 0) {
+                wtv[w] = a;
+                wrv[w] = rbest;
+                wrj[w] = rj;
             }
-            tvv = csum(a, red_f);
-            if (ct == 0) {
+            __syncthreads();
+            if (tid == 0) {
+                tvv = 0.f;
+                float nrv = 0.f;
+                int32_t nrj = -1;
+                for (int i = 0; i < kFastWarps; ++i) {
+                    tvv += wtv[i];
+                    if (wrv[i] > nrv || (wrv[i] == nrv && wrj[i] < nrj)) {
+                        nrv = wrv[i];
+                        nrj = wrj[i];
+                    }
+                }
+                rx_shared = (plan_ok && nrj >= 0 && nrj < A.Vd && nrv > 0.f) ? A.plan.x_of_j[nrj] : -1;
+                rv_shared = nrv;
                 const bool in_range = xj >= 0 && xj < A.V;
                 float zx = zx_shared;
                 zx = zx != zx ? -INFINITY : zx;
                 pj = in_range ? ex2(fmaf(zx, c, -M)) * invS : 0.f;
                 qj = 0.f;
-                if (in_range && ((sbits[xj >> 5] >> (xj & 31)) & 1u)) {
-                    const int32_t wi = xj >> 5, sh = xj & 31;
-                    const int32_t pos = spref[wi] + (sh ? __popc(sbits[wi] & ((1u << sh) - 1u)) : 0);
-                    const int32_t jd = A.plan.js16[pos];
-                    if (jd < A.Vd) {
+                if (in_range && in_support(A.plan, xj)) {
+                    const int32_t jd = A.plan.js[support_rank(A.plan, xj)];
+                    if (jd >= 0 && jd < A.Vd) {
                         float y = ld_elem<SV_BF16>(u.drow, jd);
                         y = y != y ? -INFINITY : y;
                         qj = ex2(fmaf(y, c, -Mq)) * invSq;
                     }
                 }
                 if (qj > 0.f) {
-                    const uint4 w = philox_block(philox_key(A.seeds[u.r]), 0u, static_cast<uint32_t>(u.j), kTagAccept);
-                    acc = uniform_from_word(w.x) < __fdiv_rn(pj, qj) ? 1 : 0;
+                    const uint4 w4 = philox_block(philox_key(A.seeds[u.r]), 0u, static_cast<uint32_t>(u.j), kTagAccept);
+                    acc = uniform_from_word(w4.x) < __fdiv_rn(pj, qj) ? 1 : 0;
                 } else if (in_range) {
                     flags |= kFlagOffSupport;
                 }
             }
+        } else {
+            __syncthreads();  // amax_shared is visible to thread 0
         }
-        if (ct == 0) {
+        if (tid == 0) {
+            const int32_t amax = amax_shared;
             RowStat rs;
             rs.m = M;
             rs.s = S;
@@ -1175,7 +1252,41 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
             rs.amax = amax;
             rs.flags = flags;
             rs.accept = acc;
-            rs.pad[0] = rs.pad[1] = 0;
+            rs.rx = u.has_draft ? rx_shared : -1;
+            rs.rv = u.has_draft ? rv_shared : 0.f;
+            // a bound for the race on this row, should it be the selected one: the key of
+            // the argmax, and for a residual race also of the largest support residual
+            rs.bkey = INFINITY;
+            rs.bxc = -1;
+            if (u.sampling && !(flags & (kFlagNaN | kFlagPosInf | kFlagAllNegInf | kFlagDraftBad)) && S > 0.f) {
+                const PhiloxKey key = philox_key(A.seeds[u.r]);
+                const bool residual = u.j < A.k;
+                const uint32_t tag = residual ? kTagResidual : kTagBonus;
+                auto key_of = [&](int32_t x, float wt) -> float {
+                    if (!(wt > 0.f)) return INFINITY;
+                    const uint4 w4 = philox_block(key, static_cast<uint32_t>(x >> 2), static_cast<uint32_t>(u.j), tag);
+                    const uint32_t wd = (x & 3) == 0 ? w4.x : ((x & 3) == 1 ? w4.y : ((x & 3) == 2 ? w4.z : w4.w));
+                    return __fdiv_rn(-log1pf(-one_minus_uniform_from_word(wd)), wt);
+                };
+                float wa = ex2(fmaf(BV, c, -M)) * (1.f / S);
+                if (residual && in_support(A.plan, amax)) {
+                    const int32_t jd = A.plan.js[support_rank(A.plan, amax)];
+                    if (jd >= 0 && jd < A.Vd) {
+                        float y = ld_elem<SV_BF16>(u.drow, jd);
+                        y = y != y ? -INFINITY : y;
+                        wa -= ex2(fmaf(y, c, -Mq)) * (1.f / Sq);
+                    }
+                }
+                rs.bkey = key_of(amax, wa);
+                rs.bxc = rs.bkey < INFINITY ? amax : -1;
+                if (residual && rs.rx >= 0) {
+                    const float kr = key_of(rs.rx, rs.rv);
+                    if (kr < rs.bkey) {
+                        rs.bkey = kr;
+                        rs.bxc = rs.rx;
+                    }
+                }
+            }
             A.stats[unit] = rs;
             if (u.j < A.k) {
                 const int64_t o = static_cast<int64_t>(u.r) * A.k + u.j;
@@ -1185,15 +1296,17 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
             }
         }
     }
+    if (timeout && lane == 0) {
+        // give this warp's copies that may still be in flight a bounded chance to land
+        (void)mbar_wait_bounded(&wbar[gi & 1], (gi >> 1) & 1u);
+        (void)mbar_wait_bounded(&wbar[(gi + 1) & 1], ((gi + 1) >> 1) & 1u);
+    }
 }
 
 // ---------------------------------------------------------------------------
 // scan + race + commit
 // ---------------------------------------------------------------------------
 namespace {
-
-// -ln(1 - v) for v = 1 - u in (0, 1), accurate also for tiny v
-__device__ __forceinline__ float neg_log_u(float v) { return -log1pf(-v); }
 
 __device__ __forceinline__ unsigned long long pack_key(float key, int32_t x)
 {
@@ -1202,49 +1315,152 @@ __device__ __forceinline__ unsigned long long pack_key(float key, int32_t x)
 
 }  // namespace
 
-// race over row elements [x0, x1) of one request: returns this thread's best
-// (key, x).  w_x = p(x) - q(x) (residual) or p(x) (bonus); qloc holds q on
-// [x0, x1) for the residual race.
+// E_x = -ln u_x >= -ln(1 - 2^-24) for every uniform of the library, so an
+// element whose weight w satisfies best * w below this cannot have a key
+// E_x / w_x below `best`.  The constant is taken a little low on purpose.
+constexpr float kMinE = 5.9e-8f;
+
 template <int DT>
-__device__ __forceinline__ void race_range(const char* trow, int32_t x0, int32_t x1, float c, float M,
-                                           float invS, const float* qloc, bool residual, PhiloxKey key,
-                                           uint32_t row, uint32_t tag, float& best, int32_t& bx)
+__device__ __forceinline__ void load4(const char* row, int32_t x, bool vec_ok, float* z)
 {
-    // groups of 4 elements share one Philox block (counter x >> 2)
-    const int32_t g0 = x0 >> 2, g1 = (x1 + 3) >> 2;
-    for (int32_t g = g0 + static_cast<int32_t>(threadIdx.x); g < g1; g += kRaceThreads) {
-        const uint4 w4 = philox_block(key, static_cast<uint32_t>(g), row, tag);
-        const uint32_t words[4] = {w4.x, w4.y, w4.z, w4.w};
+    if constexpr (DT == SV_BF16) {
+        if (vec_ok) {
+            const uint2 v = *reinterpret_cast<const uint2*>(row + static_cast<int64_t>(x) * 2);
+            z[0] = bf16_lo(v.x);
+            z[1] = bf16_hi(v.x);
+            z[2] = bf16_lo(v.y);
+            z[3] = bf16_hi(v.y);
+            return;
+        }
+    } else {
+        if (vec_ok) {
+            const float4 v = *reinterpret_cast<const float4*>(row + static_cast<int64_t>(x) * 4);
+            z[0] = v.x;
+            z[1] = v.y;
+            z[2] = v.z;
+            z[3] = v.w;
+            return;
+        }
+    }
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int32_t x = 4 * g + e;
-            if (x < x0 || x >= x1) continue;
-            float z = ld_elem<DT>(trow, x);
-            z = z != z ? -INFINITY : z;
-            float wt = exp2f(fmaf(z, c, -M)) * invS;
-            if (residual) wt = wt - qloc[x - x0];
-            if (!(wt > 0.f)) continue;
-            const float v = one_minus_uniform_from_word(words[e]);
-            if (!(v < best * wt)) continue;  // E >= v, so key >= v / w
-            const float k2 = __fdiv_rn(neg_log_u(v), wt);
-            if (k2 < best || (k2 == best && x < bx)) {
-                best = k2;
-                bx = x;
+    for (int e = 0; e < 4; ++e) z[e] = ld_elem<DT>(row, x + e);
+}
+
+// q(x) of the draft row (0 off the support): the residual weight needs it only for the
+// few elements whose target weight alone could still win the race
+template <int DD>
+__device__ __forceinline__ float draft_q(const SampleArgs& A, const char* drow, int32_t x, float c, float mq,
+                                         float invSq)
+{
+    int32_t jd = x;
+    if (!A.identity) {
+        if (!in_support(A.plan, x)) return 0.f;
+        jd = A.plan.js[support_rank(A.plan, x)];
+    }
+    if (jd < 0 || jd >= A.Vd) return 0.f;
+    float y = ld_elem<DD>(drow, jd);
+    y = y != y ? -INFINITY : y;
+    return ex2(fmaf(y, c, -mq)) * invSq;
+}
+
+// the race over row elements [x0, x1): this thread's best (key, x), starting from the
+// bound `best`.  w_x = p(x) - q(x) (residual) or p(x) (bonus).  Since E_x >= v_x = 1 - u_x
+// and w_x <= p(x), an element with v_x >= best * p(x) cannot win; the row's loads of a
+// batch are issued together, Philox runs only for groups some element of which passes
+// on p, and q is looked up only for elements that pass on p.
+constexpr int kRaceBatch = 8;  // groups of 4 elements per thread in flight
+template <int DT, int DD>
+__device__ __forceinline__ void race_range(const SampleArgs& A, const char* trow, const char* drow, int32_t x0,
+                                           int32_t x1, float c, const RowStat& rs, bool residual, PhiloxKey key,
+                                           uint32_t row, uint32_t tag, bool vec_ok, float& best, int32_t& bx)
+{
+    const int32_t g0 = x0 >> 2, g1 = (x1 + 3) >> 2;
+    const float invS = 1.f / rs.s, invSq = residual ? 1.f / rs.sq : 0.f;
+    for (int32_t gb = g0 + static_cast<int32_t>(threadIdx.x); gb < g1; gb += kRaceBatch * kRaceThreads) {
+        float z[kRaceBatch][4];
+#pragma unroll
+        for (int i = 0; i < kRaceBatch; ++i) {
+            const int32_t g = gb + i * kRaceThreads, xb = 4 * g;
+            if (g < g1 && xb >= x0 && xb + 4 <= x1) {
+                load4<DT>(trow, xb, vec_ok, z[i]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    z[i][e] = (g < g1 && xb + e >= x0 && xb + e < x1) ? ld_elem<DT>(trow, xb + e) : -INFINITY;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kRaceBatch; ++i) {
+            const int32_t g = gb + i * kRaceThreads, xb = 4 * g;
+            float w[4], wmax = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float zz = z[i][e] != z[i][e] ? -INFINITY : z[i][e];
+                w[e] = ex2(fmaf(zz, c, -rs.m)) * invS;
+                wmax = fmaxf(wmax, w[e]);
+            }
+            if (!(best * wmax >= kMinE)) continue;  // no element of the group can beat `best`
+            const uint4 w4 = philox_block(key, static_cast<uint32_t>(g), row, tag);
+            const uint32_t words[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float wt = w[e];
+                if (!(wt > 0.f)) continue;
+                const float v = one_minus_uniform_from_word(words[e]);
+                if (!(v < best * wt)) continue;  // E >= v and w <= p
+                const int32_t x = xb + e;
+                if (residual) {
+                    wt -= draft_q<DD>(A, drow, x, c, rs.mq, invSq);
+                    if (!(wt > 0.f) || !(v < best * wt)) continue;
+                }
+                const float k2 = __fdiv_rn(-log1pf(-v), wt);
+                if (k2 < best || (k2 == best && x < bx)) {
+                    best = k2;
+                    bx = x;
+                }
             }
         }
     }
+}
+
+// the race key of one element (or +inf when its weight is not positive)
+template <int DT, int DD>
+__device__ __forceinline__ float single_key(const SampleArgs& A, const char* trow, const char* drow, int32_t x,
+                                            float c, const RowStat& rs, bool residual, PhiloxKey key, uint32_t row,
+                                            uint32_t tag)
+{
+    float z = ld_elem<DT>(trow, x);
+    z = z != z ? -INFINITY : z;
+    float w = ex2(fmaf(z, c, -rs.m)) * (1.f / rs.s);
+    if (residual) {
+        int32_t jd = -1;
+        if (A.identity) {
+            jd = x;
+        } else if (in_support(A.plan, x)) {
+            jd = A.plan.js[support_rank(A.plan, x)];
+        }
+        if (jd >= 0 && jd < A.Vd) {
+            float y = ld_elem<DD>(drow, jd);
+            y = y != y ? -INFINITY : y;
+            w -= ex2(fmaf(y, c, -rs.mq)) * (1.f / rs.sq);
+        }
+    }
+    if (!(w > 0.f)) return INFINITY;
+    const uint4 w4 = philox_block(key, static_cast<uint32_t>(x >> 2), row, tag);
+    const uint32_t wd = (x & 3) == 0 ? w4.x : ((x & 3) == 1 ? w4.y : ((x & 3) == 2 ? w4.z : w4.w));
+    return __fdiv_rn(-log1pf(-one_minus_uniform_from_word(wd)), w);
 }
 
 template <int DT, int DD>
 __global__ void __launch_bounds__(kRaceThreads) race_commit_kernel(SampleArgs A)
 {
     pdl_wait_primary();
-    __shared__ float qloc[kRaceSeg];
     __shared__ float red_f[kRaceThreads / 32];
     __shared__ int32_t red_i[kRaceThreads / 32];
     __shared__ int last_cta;
     __shared__ int32_t n_shared;
-    const int tid = threadIdx.x;
+    __shared__ uint32_t fl_shared;
+    const int tid = threadIdx.x, lane = tid & 31;
     const int32_t r = static_cast<int32_t>(blockIdx.x / A.race_ctas);
     const int32_t rc = static_cast<int32_t>(blockIdx.x - static_cast<int64_t>(r) * A.race_ctas);
     const int32_t k = A.k;
@@ -1252,25 +1468,33 @@ __global__ void __launch_bounds__(kRaceThreads) race_commit_kernel(SampleArgs A)
     const int32_t* d = A.draft + static_cast<int64_t>(r) * k;
     const float T = A.temp[r];
 
-    // request-level decisions, computed identically by every CTA of the request
-    uint32_t fl = 0;
-    for (int32_t j = tid; j <= k; j += kRaceThreads) fl |= st[j].flags;
-    fl = block_or<kRaceThreads>(fl, reinterpret_cast<uint32_t*>(red_i));
-    const bool bad_rows = (fl & (kFlagNaN | kFlagPosInf | kFlagAllNegInf | kFlagDraftBad)) != 0;
-    const bool greedy = !(T > 0.f) || bad_rows;
-    if (tid == 0) {
+    // request-level decisions (warp 0, ballots), identical in every CTA of the request
+    if (tid < 32) {
+        uint32_t fl = 0;
+        for (int32_t j = lane; j <= k; j += 32) fl |= st[j].flags;
+        fl = __reduce_or_sync(0xffffffffu, fl);
+        const bool bad_rows = (fl & (kFlagNaN | kFlagPosInf | kFlagAllNegInf | kFlagDraftBad)) != 0;
+        const bool greedy = !(T > 0.f) || bad_rows;
         int32_t n = k;
-        for (int32_t j = 0; j < k; ++j) {
-            const bool ok = greedy ? d[j] == st[j].amax : st[j].accept != 0;
-            if (!ok) {
-                n = j;
+        for (int32_t j0 = 0; j0 < k; j0 += 32) {
+            const int32_t j = j0 + lane;
+            const bool fail = j < k && (greedy ? d[j] != st[j].amax : st[j].accept == 0);
+            const unsigned m = __ballot_sync(0xffffffffu, fail);
+            if (m) {
+                n = j0 + __ffs(m) - 1;
                 break;
             }
         }
-        n_shared = n;
+        if (lane == 0) {
+            n_shared = n;
+            fl_shared = fl;
+        }
     }
     __syncthreads();
     const int32_t n = n_shared;
+    const uint32_t fl = fl_shared;
+    const bool bad_rows = (fl & (kFlagNaN | kFlagPosInf | kFlagAllNegInf | kFlagDraftBad)) != 0;
+    const bool greedy = !(T > 0.f) || bad_rows;
     int32_t token = -1;
     uint32_t status = 0;
     if (greedy) {
@@ -1278,41 +1502,22 @@ __global__ void __launch_bounds__(kRaceThreads) race_commit_kernel(SampleArgs A)
         token = st[n].amax;
     } else {
         const bool residual = n < k;
-        const RowStat& rs = st[n];
+        const RowStat rs = st[n];
         const float c = kLog2e / T;
         const int32_t x0 = rc * A.race_seg, x1 = min(A.V, x0 + A.race_seg);
         const char* trow = A.tbase + (static_cast<int64_t>(r) * (k + 1) + n) * A.tstride;
-        if (residual) {
-            for (int32_t i = tid; i < x1 - x0; i += kRaceThreads) qloc[i] = 0.f;
-            __syncthreads();
-            const char* drow = A.dbase + (static_cast<int64_t>(r) * k + n) * A.dstride;
-            const float invSq = 1.f / rs.sq;
-            if (A.identity) {
-                for (int32_t x = x0 + tid; x < x1; x += kRaceThreads) {
-                    float y = ld_elem<DD>(drow, x);
-                    y = y != y ? -INFINITY : y;
-                    qloc[x - x0] = exp2f(fmaf(y, c, -rs.mq)) * invSq;
-                }
-            } else if (x0 < x1) {
-                const int32_t p0 = support_rank(A.plan, x0), p1 = support_rank(A.plan, x1);
-                for (int32_t p = p0 + tid; p < p1; p += kRaceThreads) {
-                    const int32_t x = A.plan.xs[p], jd = A.plan.js[p];
-                    if (x < x0 || x >= x1 || jd < 0 || jd >= A.Vd) continue;
-                    float y = ld_elem<DD>(drow, jd);
-                    y = y != y ? -INFINITY : y;
-                    qloc[x - x0] = exp2f(fmaf(y, c, -rs.mq)) * invSq;
-                }
-            }
-            __syncthreads();
-        }
-        float best = INFINITY;
-        int32_t bx = INT32_MAX;
-        race_range<DT>(trow, x0, x1, c, rs.m, 1.f / rs.s, qloc, residual, philox_key(A.seeds[r]),
-                       static_cast<uint32_t>(n), residual ? kTagResidual : kTagBonus, best, bx);
-        // (key, lowest x) minimum over the CTA
-        float nb = -best;
+        const char* drow = residual ? A.dbase + (static_cast<int64_t>(r) * k + n) * A.dstride : nullptr;
+        const PhiloxKey key = philox_key(A.seeds[r]);
+        const uint32_t tag = residual ? kTagResidual : kTagBonus;
+        // start from the row's precomputed bound; the CTA holding its element keeps it as a candidate
+        const int32_t cand_x = rs.bxc;
+        float best = rs.bkey;
+        int32_t bx = (tid == 0 && cand_x >= x0 && cand_x < x1 && best < INFINITY) ? cand_x : INT32_MAX;
+        race_range<DT, DD>(A, trow, drow, x0, x1, c, rs, residual, key, static_cast<uint32_t>(n), tag,
+                           A.tbulk != 0, best, bx);
+        // (key, lowest x) minimum over the CTA; threads without a candidate carry (inf, INT32_MAX)
+        float nb = bx == INT32_MAX ? -INFINITY : -best;
         int32_t nx = bx;
-        // reuse the argmax reduction on (-key, x): larger -key = smaller key
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             const float ov = __shfl_xor_sync(0xffffffffu, nb, o);
@@ -1322,7 +1527,7 @@ __global__ void __launch_bounds__(kRaceThreads) race_commit_kernel(SampleArgs A)
                 nx = ox;
             }
         }
-        if ((tid & 31) == 0) {
+        if (lane == 0) {
             red_f[tid >> 5] = nb;
             red_i[tid >> 5] = nx;
         }
@@ -1350,9 +1555,9 @@ __global__ void __launch_bounds__(kRaceThreads) race_commit_kernel(SampleArgs A)
             status |= SV_ST_RESIDUAL_ZERO;
             float b2 = INFINITY;
             int32_t x2 = INT32_MAX;
-            race_range<DT>(trow, 0, A.V, c, rs.m, 1.f / rs.s, qloc, false, philox_key(A.seeds[r]),
-                           static_cast<uint32_t>(n), kTagResidual, b2, x2);
-            float nb2 = -b2;
+            race_range<DT, DD>(A, trow, drow, 0, A.V, c, rs, false, key, static_cast<uint32_t>(n), kTagResidual,
+                               A.tbulk != 0, b2, x2);
+            float nb2 = x2 == INT32_MAX ? -INFINITY : -b2;
             block_argmax<kRaceThreads>(nb2, x2, red_f, red_i);
             token = x2 == INT32_MAX ? 0 : x2;
         }
@@ -1390,7 +1595,7 @@ __global__ void __launch_bounds__(kRaceThreads) race_commit_kernel(SampleArgs A)
 namespace {
 
 struct PlanLayout {
-    int64_t header, bitmap, prefix, xs, js, js16, total;
+    int64_t header, bitmap, prefix, xs, js, pairs, chunk, x_of_j, total;
 };
 
 PlanLayout plan_layout(int32_t V, int32_t Vd)
@@ -1408,7 +1613,9 @@ PlanLayout plan_layout(int32_t V, int32_t Vd)
     L.prefix = take((nw + 1) * 4);
     L.xs = take(static_cast<int64_t>(Vd) * 4);
     L.js = take(static_cast<int64_t>(Vd) * 4);
-    L.js16 = take(static_cast<int64_t>(Vd) * 2);
+    L.pairs = take(static_cast<int64_t>(Vd) * 4);
+    L.chunk = take((static_cast<int64_t>(V) / kChunkElems + 2) * 4);
+    L.x_of_j = take(static_cast<int64_t>(Vd) * 4);
     L.total = off;
     return L;
 }
@@ -1423,7 +1630,9 @@ D2tPlan plan_view(void* base, int32_t V, int32_t Vd)
     pl.prefix = reinterpret_cast<int32_t*>(b + L.prefix);
     pl.xs = reinterpret_cast<int32_t*>(b + L.xs);
     pl.js = reinterpret_cast<int32_t*>(b + L.js);
-    pl.js16 = reinterpret_cast<uint16_t*>(b + L.js16);
+    pl.pairs = reinterpret_cast<uint32_t*>(b + L.pairs);
+    pl.chunk = reinterpret_cast<int32_t*>(b + L.chunk);
+    pl.x_of_j = reinterpret_cast<int32_t*>(b + L.x_of_j);
     pl.nw = (V + 31) / 32;
     return pl;
 }
@@ -1461,19 +1670,16 @@ SampleLayout sample_layout(int64_t R, int32_t k, int32_t V, int32_t Vd, int et, 
     return L;
 }
 
-size_t fast_smem_bytes(int32_t V, int32_t Vd)
+size_t fast_smem_bytes(int32_t Vd)
 {
-    const int64_t nw = (V + 31) / 32;
-    return static_cast<size_t>(kFastHeader + kFastStages * static_cast<int64_t>(kFastStage) +
-                               align256(static_cast<int64_t>(Vd) * 2) + nw * 4 + (nw + 1) * 4);
+    return static_cast<size_t>(kFastHeader + 2 * kFastWarps * static_cast<int64_t>(kFastStage) +
+                               align256(static_cast<int64_t>(Vd) * 2));
 }
 
 bool fast_path_ok(const Rows& t, const Rows& d, bool identity)
 {
-    const int32_t nw = (t.width + 31) / 32;
     return !identity && t.dtype == SV_BF16 && d.dtype == SV_BF16 && t.bulk_ok && d.bulk_ok && d.data != nullptr &&
-           t.width % 8 == 0 && d.width % 8 == 0 && d.width <= kFastMaxVd && nw <= kFastMaxWords &&
-           fast_smem_bytes(t.width, d.width) <= 227 * 1024;
+           t.width % 8 == 0 && d.width % 8 == 0 && d.width <= kFastMaxVd && fast_smem_bytes(d.width) <= 227 * 1024;
 }
 
 }  // namespace
@@ -1554,7 +1760,7 @@ static cudaError_t launch_sample_t(const Rows& t, const Rows& d, const int32_t* 
     cfg.attrs = attr;
     cfg.numAttrs = own_plan ? 1 : 0;
     if (fast_path_ok(t, d, identity)) {
-        const size_t smem = fast_smem_bytes(t.width, d.width);
+        const size_t smem = fast_smem_bytes(d.width);
         e = cudaFuncSetAttribute(sample_rows_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem));
         if (e != cudaSuccess) return e;
