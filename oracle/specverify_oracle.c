@@ -39,7 +39,12 @@
  *  - the accept test is the strict comparison u < p/q with u in (0,1).
  *  - the sampler is an exponential race: argmin_x E_x / w_x, E_x = -ln u_x,
  *    u_x a Philox4x32-10 uniform keyed by the request seed and counted by
- *    (x >> 2, row, tag, 0); tags 0 accept, 1 residual, 2 bonus.
+ *    (x >> 2, row, tag, 0); tags 0 accept, 1 residual, 2 bonus.  Over the
+ *    full target vocabulary it is run in two levels: the ids are cut into
+ *    chunks of RACE_CHUNK, the chunk c = argmin E_c / W_c (W_c the chunk's
+ *    weight sum, E_c from tag 3 for the residual, 4 for the bonus, counted by
+ *    c), then the element race inside that chunk; P(x) = w_x / sum w still.
+ *    The per-codebook CFG rows use the one-level race.
  *  - the uniform from a 32-bit word r is (2 * (r >> 9) + 1) * 2^-24.
  *  - NaN logits count as -inf.  A sampling request with a NaN, +inf or
  *    all -inf row is verified greedily and flagged (status bit 2).
@@ -66,7 +71,10 @@ enum {
     OR_ST_BAD_D2T = 32       /* d2t entry out of range or repeated */
 };
 
-enum { TAG_ACCEPT = 0, TAG_RESIDUAL = 1, TAG_BONUS = 2 };
+enum { TAG_ACCEPT = 0, TAG_RESIDUAL = 1, TAG_BONUS = 2, TAG_RESIDUAL_CHUNK = 3, TAG_BONUS_CHUNK = 4 };
+
+/* ids per chunk of the two-level race over the full target vocabulary */
+#define RACE_CHUNK 2048
 
 /* ------------------------------------------------------------------ */
 /* Philox4x32-10, from Salmon, Moraes, Dror, Shaw, "Parallel Random    */
@@ -187,15 +195,16 @@ static void softmax_T(const double* z, int32_t n, double T, double* p)
     for (int32_t x = 0; x < n; ++x) p[x] /= s;
 }
 
-/* exponential race over weights w >= 0: argmin_{w_x > 0} E_x / w_x with
- * E_x = -ln u_x.  Returns -1 if every weight is 0.  *margin receives
- * (key2 - key1) / key1 for the two smallest keys (INFINITY if only one). */
-int32_t or_race(const double* w, int32_t n, uint64_t seed, uint32_t row, uint32_t tag,
-                double* margin)
+/* exponential race over the weights w[x0..x1) >= 0: argmin_{w_x > 0} E_x / w_x
+ * with E_x = -ln u_x, u_x the uniform of the absolute id x.  Returns -1 if
+ * every weight is 0.  *margin receives (key2 - key1) / key1 for the two
+ * smallest keys (INFINITY if only one). */
+static int32_t race_span(const double* w, int32_t x0, int32_t x1, uint64_t seed, uint32_t row,
+                         uint32_t tag, double* margin)
 {
     int32_t arg = -1;
     double best = INFINITY, second = INFINITY;
-    for (int32_t x = 0; x < n; ++x) {
+    for (int32_t x = x0; x < x1; ++x) {
         if (!(w[x] > 0.0)) continue;
         double e = -log(or_uniform(seed, row, tag, (uint32_t)x));
         double key = e / w[x];
@@ -208,6 +217,35 @@ int32_t or_race(const double* w, int32_t n, uint64_t seed, uint32_t row, uint32_
         }
     }
     if (margin) *margin = (arg >= 0 && isfinite(second)) ? (second - best) / best : INFINITY;
+    return arg;
+}
+
+int32_t or_race(const double* w, int32_t n, uint64_t seed, uint32_t row, uint32_t tag,
+                double* margin)
+{
+    return race_span(w, 0, n, seed, row, tag, margin);
+}
+
+/* two-level race: the chunk of `chunk` consecutive ids first, by a race over
+ * the chunk sums W_c with the uniforms of tag_chunk counted by c, then the
+ * element race inside it.  P(chunk c) = W_c / sum W and P(x | c) = w_x / W_c,
+ * so P(x) = w_x / sum w.  *margin = the smaller of the two races' margins. */
+int32_t or_race2(const double* w, int32_t n, int32_t chunk, uint64_t seed, uint32_t row,
+                 uint32_t tag_chunk, uint32_t tag, double* margin)
+{
+    const int32_t nc = (n + chunk - 1) / chunk;
+    double* W = (double*)calloc((size_t)(nc > 0 ? nc : 1), sizeof(double));
+    for (int32_t x = 0; x < n; ++x)
+        if (w[x] > 0.0) W[x / chunk] += w[x];
+    double mc = INFINITY, me = INFINITY;
+    const int32_t c = race_span(W, 0, nc, seed, row, tag_chunk, &mc);
+    free(W);
+    int32_t arg = -1;
+    if (c >= 0) {
+        const int32_t x1 = (c + 1) * chunk < n ? (c + 1) * chunk : n;
+        arg = race_span(w, c * chunk, x1, seed, row, tag, &me);
+    }
+    if (margin) *margin = mc < me ? mc : me;
     return arg;
 }
 
@@ -413,10 +451,10 @@ int or_verify_sample(const void* target, int t_dtype, int64_t t_stride, int32_t 
                 double mg;
                 int32_t tok;
                 if (mass > 0.0) {
-                    tok = or_race(w, V, seeds[r], (uint32_t)j, TAG_RESIDUAL, &mg);
+                    tok = or_race2(w, V, RACE_CHUNK, seeds[r], (uint32_t)j, TAG_RESIDUAL_CHUNK, TAG_RESIDUAL, &mg);
                 } else {
                     st |= OR_ST_RESIDUAL_ZERO;
-                    tok = or_race(p, V, seeds[r], (uint32_t)j, TAG_RESIDUAL, &mg);
+                    tok = or_race2(p, V, RACE_CHUNK, seeds[r], (uint32_t)j, TAG_RESIDUAL_CHUNK, TAG_RESIDUAL, &mg);
                 }
                 out[n] = tok;
                 if (race_margin) race_margin[r] = mg;
@@ -428,7 +466,7 @@ int or_verify_sample(const void* target, int t_dtype, int64_t t_stride, int32_t 
             for (int32_t x = 0; x < V; ++x) z[x] = load_elem(target, t_dtype, trow * t_stride + x);
             softmax_T(z, V, T, p);
             double mg;
-            out[k] = or_race(p, V, seeds[r], (uint32_t)k, TAG_BONUS, &mg);
+            out[k] = or_race2(p, V, RACE_CHUNK, seeds[r], (uint32_t)k, TAG_BONUS_CHUNK, TAG_BONUS, &mg);
             if (race_margin) race_margin[r] = mg;
         }
         for (int32_t j = 0; j < n; ++j) out[j] = d[j];

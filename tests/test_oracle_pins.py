@@ -77,6 +77,44 @@ def test_race_distribution_chi_square():
     assert _chi2_ok(counts, w) > CHI2_ALPHA
 
 
+def test_two_level_race_distribution_chi_square():
+    # chunks of 4 over 23 ids (last chunk ragged), weights spread over every chunk, zeros inside
+    rng = np.random.default_rng(5)
+    w = rng.uniform(0.0, 1.0, 23) ** 3
+    w[[1, 9, 10, 22]] = 0.0
+    n = 60_000
+    counts = np.zeros(len(w))
+    for seed in range(n):
+        counts[oracle.race2(w, 4, seed * 104729 + 3, 5, 3, 1)[0]] += 1
+    assert _chi2_ok(counts, w) > CHI2_ALPHA
+    # the chunk level alone: P(chunk c) = W_c / sum W
+    W = np.add.reduceat(w, np.arange(0, 23, 4))
+    assert _chi2_ok(np.add.reduceat(counts, np.arange(0, 23, 4)), W) > CHI2_ALPHA
+
+
+def test_two_level_race_counter_layout():
+    # the library's convention: the chunk uniform is counted by the chunk index c, the element
+    # uniform by the absolute id x (not the id inside the chunk)
+    w = np.zeros(3 * 2048)
+    w[[4100, 4101, 4102]] = [0.2, 0.5, 0.3]
+    for seed in range(40):
+        keys = [-math.log(oracle.uniform(seed, 9, 1, x)) / w[x] for x in (4100, 4101, 4102)]
+        assert oracle.race2(w, 2048, seed, 9, 3, 1)[0] == 4100 + int(np.argmin(keys))
+
+
+def test_two_level_race_special_cases():
+    w = np.zeros(4100)
+    w[2051] = 1e-30
+    for seed in range(20):
+        assert oracle.race2(w, 2048, seed, 0, 3, 1)[0] == 2051
+    assert oracle.race2(np.zeros(4100), 2048, 7, 0, 3, 1)[0] == -1
+    # one chunk holding every id: the chunk level is a no-op, the element race is the one-level race
+    rng = np.random.default_rng(6)
+    v = rng.uniform(0, 1, 37)
+    for seed in range(200):
+        assert oracle.race2(v, 64, seed, 2, 4, 2)[0] == oracle.race(v, seed, 2, 2)[0]
+
+
 # --------------------------------------------------------------------------
 # worked example of the blog (p = [.5,.3,.2], q = [.4,.4,.2])
 # --------------------------------------------------------------------------
@@ -197,6 +235,45 @@ def test_sampling_output_distribution_chi_square(V, T):
     assert _chi2_ok(np.bincount(out["tokens"][acc, 1], minlength=V), pb) > CHI2_ALPHA
     tv = 0.5 * np.abs(p - q).sum()
     assert abs(acc.mean() - (1 - tv)) < 5 * math.sqrt(tv * (1 - tv) / R)
+
+
+def _binned(tokens, probs, heavy, chunk):
+    """counts and probabilities over bins: each heavy id alone, then the rest of each chunk"""
+    V = probs.size
+    bin_of = np.arange(V) // chunk + len(heavy)
+    bin_of[heavy] = np.arange(len(heavy))
+    nb = len(heavy) + (V + chunk - 1) // chunk
+    return np.bincount(bin_of[tokens], minlength=nb), np.bincount(bin_of, weights=probs, minlength=nb)
+
+
+def test_sampling_distribution_across_race_chunks():
+    # V spans three chunks of the two-level race (the last one ragged); mass sits on a few ids
+    # in different chunks and on the long tail, so both race levels decide
+    V, T, R = 2 * oracle.RACE_CHUNK + 4, 1.0, 8_000
+    rng = np.random.default_rng(11)
+    heavy = np.array([3, 2050, 4099])
+    z0 = rng.normal(0, 0.5, V).astype(np.float32)
+    zb = rng.normal(0, 0.5, V).astype(np.float32)
+    y0 = rng.normal(0, 0.5, V).astype(np.float32)
+    z0[heavy] = [7.0, 6.0, 7.5]
+    zb[heavy] = [6.5, 7.5, 6.0]
+    y0[[3, 1000, 3000]] = [8.0, 7.0, 6.0]
+    p = np.exp(z0.astype(np.float64) / T); p /= p.sum()
+    pb = np.exp(zb.astype(np.float64) / T); pb /= pb.sum()
+    q = np.exp(y0.astype(np.float64) / T); q /= q.sum()
+    x = rng.choice(V, size=R, p=q)
+    target = np.empty((2 * R, V), np.float32)
+    target[0::2] = z0
+    target[1::2] = zb
+    seeds = rng.integers(0, 2 ** 63, size=R, dtype=np.uint64)
+    out = oracle.verify_sample(target, np.tile(y0, (R, 1)), None, R, 1, x.reshape(R, 1).astype(np.int32),
+                               seeds, np.full(R, T, np.float32))
+    first = out["tokens"][:, 0]
+    acc = out["accept_len"] == 1
+    assert _chi2_ok(*_binned(first, p, heavy, oracle.RACE_CHUNK)) > CHI2_ALPHA
+    resid = np.maximum(0.0, p - q)
+    assert _chi2_ok(*_binned(first[~acc], resid, heavy, oracle.RACE_CHUNK)) > CHI2_ALPHA
+    assert _chi2_ok(*_binned(out["tokens"][acc, 1], pb, heavy, oracle.RACE_CHUNK)) > CHI2_ALPHA
 
 
 def test_tokens_per_pass_closed_form():
