@@ -16,12 +16,12 @@
 //                      positions (G[pos]).  A second pass over G and Y gives
 //                      TV over the full vocabulary, p(x_j), q(x_j) and the
 //                      accept test u_j < p/q.
-//   race_commit_kernel RC CTAs per request: the accept-length scan, then the
-//                      exponential race argmin E_x / w_x on the one selected
-//                      row (residual max(0, p - q) at the first rejection, or
-//                      p at the bonus row), Philox uniforms per element, CTA
-//                      results merged with a 64-bit atomicMin; the last CTA
-//                      of the request commits the tokens.
+//   race_chunks_kernel RC CTAs per request: the accept-length scan, then
+//                      the chunk sums of the weights on the one selected row
+//                      (residual max(0, p - q) at the first rejection, or p
+//                      at the bonus row); the last CTA of the request draws
+//                      the chunk and then the id by exponential races with
+//                      Philox uniforms, and commits the tokens.
 // Temperature scaling works in log2 units: with c = log2(e) / T,
 // p(x) = 2^(z_x c - M) / S where M = max_x z_x c and S = sum 2^(z c - M).
 #include <algorithm>
@@ -43,7 +43,6 @@ constexpr int kStages = 4;
 constexpr int kRowHeader = 128;
 constexpr uint32_t kSmemBudget = 220 * 1024;
 constexpr int kRaceThreads = 256;
-constexpr int32_t kRaceSeg = 8192;  // elements of the race row per CTA
 constexpr int32_t kMaxPlanWords = 25600;  // d2t mode supports V <= 819,200
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -56,7 +55,6 @@ struct D2tPlan {
     int32_t* js;       // [Vd] the draft id of xs[pos]
     uint32_t* pairs;   // [Vd] (draft id << 16) | (xs & (kChunkElems - 1)), ascending xs (Vd <= 65535)
     int32_t* chunk;    // [V / kChunkElems + 2] support rank at every multiple of kChunkElems
-    int32_t* x_of_j;   // [Vd] target id of every draft id (a copy of d2t)
     int32_t* header;   // [0] V, [1] Vd the plan was built for, [2] d2t out of range or repeated
     int32_t nw;
 };
@@ -69,15 +67,10 @@ struct RowStat {
     int32_t amax;     // raw argmax of the target row
     uint32_t flags;   // kFlag* of the target and draft rows
     int32_t accept;   // accept decision of position j
-    int32_t rx;       // target id of the largest residual p - q on the support (-1: none)
-    float rv;         // that residual
-    float bkey;       // race key of the candidate bx_c if this row is raced (+inf: no bound)
-    int32_t bxc;      // the candidate (-1: none)
 };
 
 struct RaceSlot {
-    unsigned long long best;  // (key bits << 32) | x, minimum over the race CTAs
-    unsigned int count;       // race CTAs done
+    unsigned int count;  // race CTAs of the request done
     unsigned int pad;
 };
 
@@ -106,8 +99,8 @@ struct SampleArgs {
     char* gslots;        // global-memory Y / G buffers when they do not fit in shared memory
     int64_t gslot_bytes;
     int smem_mode;
+    float* wsum;         // [R][2][chunks] chunk sums of the raced row: W_c, then P_c
     int32_t race_ctas;   // CTAs per request in the race
-    int32_t race_seg;    // elements per race CTA
 };
 
 __host__ __device__ inline int64_t align256(int64_t b) { return (b + 255) / 256 * 256; }
@@ -307,7 +300,6 @@ __global__ void __launch_bounds__(kPlanThreads)
         pl.bitmap[w] = bits[w];
         pl.prefix[w] = pref[w];
     }
-    for (int32_t j = tid; j < Vd; j += kPlanThreads) pl.x_of_j[j] = d2t[j];
     for (int32_t c = tid; c <= (V + kChunkElems - 1) / kChunkElems; c += kPlanThreads) {
         const int32_t x = min(V, c * kChunkElems);
         const int32_t w = x >> 5, b = x & 31;
@@ -407,7 +399,6 @@ __global__ void __launch_bounds__(kRowThreads, 1) sample_rows_kernel(SampleArgs 
         const int32_t xj = has_draft ? A.draft[static_cast<int64_t>(r) * A.k + j] : -1;
 
         if (j == 0 && tid == 0) {
-            A.race[r].best = ~0ull;
             A.race[r].count = 0u;
         }
         // chunk list: draft bulk chunks, then target bulk chunks
@@ -713,10 +704,6 @@ __global__ void __launch_bounds__(kRowThreads, 1) sample_rows_kernel(SampleArgs 
             rs.amax = amax;
             rs.flags = flags;
             rs.accept = acc;
-            rs.rx = -1;
-            rs.rv = 0.f;
-            rs.bkey = INFINITY;
-            rs.bxc = -1;
             A.stats[unit] = rs;
             if (j < A.k) {
                 const int64_t o = static_cast<int64_t>(r) * A.k + j;
@@ -739,24 +726,29 @@ __global__ void __launch_bounds__(kRowThreads, 1) sample_rows_kernel(SampleArgs 
 // ---------------------------------------------------------------------------
 // row pass, fast path: bf16 target and draft rows, d2t vocabulary <= 32768
 // ---------------------------------------------------------------------------
-// Every warp streams its own share of a row: chunks of kChunkElems ids,
-// chunk c going to warp c % kFastWarps, through a private two-stage ring of
-// bulk copies that the warp's lane 0 issues one chunk ahead.  Each stage also
-// receives the chunk's support entries as packed (draft id, offset) pairs,
-// so the warp scatters the support logits to G[draft id] from shared memory.
-// Warps never wait for each other inside a row; only the row's reductions
-// and the TV pass (over G and the L2-resident draft row, in draft-id order)
-// synchronise the CTA, and each warp has already issued its first chunk of
-// the next row before they start.
+// Every warp streams its own share of a row through a private ring of
+// kFastStages bulk-copied stages.  The chunks of a (request, position) unit,
+// draft chunks first and then target chunks, form one sequence; element s of
+// the sequence belongs to warp s % kFastWarps, so warps get equal shares.  The
+// warp's lane 0 keeps all stages in flight: each consumed stage is refilled
+// at once with the warp's next chunk, of this unit or of the CTA's next one,
+// so the row reductions and the TV pass at the end of a unit overlap the
+// first copies of the next.  The support entries of a target chunk, packed
+// (draft id, offset) pairs of the plan, come from L2 into registers while the
+// chunk's maxima and exponentials are taken; the warp then scatters the
+// support logits to G[draft id] from shared memory.
 namespace {
 
 constexpr int kFastWarps = 12;
 constexpr int kFastThreads = 32 * kFastWarps;
+constexpr int kFastStages = 3;                   // per warp: one being read, the others in flight
 constexpr uint32_t kFastData = kChunkElems * 2;  // 4 KB of bf16 per stage
-constexpr uint32_t kFastPairCap = 512;           // staged support entries per stage
-constexpr uint32_t kFastStage = kFastData + kFastPairCap * 4;
-constexpr int kFastHeader = 256;
+constexpr uint32_t kFastStage = kFastData;
+constexpr int kPairRegs = 4;                     // uint4 groups of support entries per lane and chunk
+constexpr int kFastHeader = 512;                 // the stage mbarriers
+static_assert(kFastWarps * kFastStages * 8 <= kFastHeader, "mbarriers fit the header");
 constexpr int32_t kFastMaxVd = 32768;
+constexpr int kVL = kChunkElems / 8 / 32;  // 16-byte vectors per lane and chunk
 
 __device__ __forceinline__ float ex2(float x)
 {
@@ -780,6 +772,12 @@ __device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigne
 {
     unsigned long long r;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b)
+{
+    unsigned long long r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
 __device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b)
@@ -851,57 +849,83 @@ struct FastUnit {
     bool sampling, has_draft;
     const char* trow;
     const char* drow;
-    int32_t nd, nt;  // draft / target chunks of the row
+    int32_t nd, n;  // draft chunks, all chunks (draft then target) of the unit
 };
 
-__device__ __forceinline__ FastUnit fast_unit(const SampleArgs& A, int64_t unit)
+__device__ __forceinline__ FastUnit fast_unit(const SampleArgs& A, int64_t unit, float T)
 {
     FastUnit u;
     u.r = static_cast<int32_t>(unit / (A.k + 1));
     u.j = static_cast<int32_t>(unit - static_cast<int64_t>(u.r) * (A.k + 1));
-    const float T = A.temp[u.r];
     u.sampling = T > 0.f;
     u.has_draft = u.sampling && u.j < A.k;
     u.trow = A.tbase + unit * A.tstride;
     u.drow = u.has_draft ? A.dbase + (static_cast<int64_t>(u.r) * A.k + u.j) * A.dstride : nullptr;
     u.nd = u.has_draft ? (A.Vd + kChunkElems - 1) / kChunkElems : 0;
-    u.nt = (A.V + kChunkElems - 1) / kChunkElems;
+    u.n = u.nd + (A.V + kChunkElems - 1) / kChunkElems;
     return u;
 }
 
-// chunks of warp w in a row: draft chunks w, w + W, ... then target chunks w, w + W, ...
+// chunks of warp w in a unit of n chunks: sequence elements w, w + W, ...
 __device__ __forceinline__ int32_t warp_chunks(int32_t n, int w)
 {
     return n > w ? (n - w + kFastWarps - 1) / kFastWarps : 0;
 }
 
-// issue the i-th chunk of warp w of unit u into `stage` (lane 0 only)
-__device__ __forceinline__ void issue_warp_chunk(const SampleArgs& A, const FastUnit& u, int w, int32_t i,
-                                                 unsigned char* stage, uint64_t* bar, uint64_t pol_t,
-                                                 uint64_t pol_d, bool plan_ok)
+__device__ __forceinline__ float unit_temp(const SampleArgs& A, int64_t unit)
 {
-    const int32_t ndw = warp_chunks(u.nd, w);
-    if (i < ndw) {
-        const int32_t c = w + i * kFastWarps;
-        const uint32_t off = static_cast<uint32_t>(c) * kFastData;
-        const uint32_t nb = min(kFastData, static_cast<uint32_t>(A.Vd) * 2 - off);
-        mbar_arrive_expect_tx(bar, nb);
-        bulk_copy_g2s(stage, u.drow + off, nb, bar, pol_d);
-        return;
+    return A.temp[unit / (A.k + 1)];
+}
+
+// issue sequence element q of unit u into `stage` (lane 0 only)
+__device__ __forceinline__ void issue_seq(const SampleArgs& A, const FastUnit& u, int32_t q, unsigned char* stage,
+                                          uint64_t* bar, uint64_t pol_t, uint64_t pol_d)
+{
+    const bool is_draft = q < u.nd;
+    const uint32_t off = static_cast<uint32_t>(is_draft ? q : q - u.nd) * kFastData;
+    const uint32_t nb = min(kFastData, static_cast<uint32_t>(is_draft ? A.Vd : A.V) * 2 - off);
+    mbar_arrive_expect_tx(bar, nb);
+    bulk_copy_g2s(stage, (is_draft ? u.drow : u.trow) + off, nb, bar, is_draft ? pol_d : pol_t);
+}
+
+// The producer side of a warp's ring: the next chunk to issue (unit, index in
+// the warp's list) and the temperature of the unit after it, loaded a unit
+// ahead.  Every lane keeps the same copy; lane 0 issues.
+struct Producer {
+    int64_t unit;
+    int32_t i, cnt;
+    FastUnit u;
+    float t_next;
+    uint32_t issued;
+};
+
+__device__ __forceinline__ void producer_enter(const SampleArgs& A, Producer& P, int w, int64_t units, float T)
+{
+    while (P.unit < units) {
+        P.u = fast_unit(A, P.unit, T);
+        P.cnt = warp_chunks(P.u.n, w);
+        P.i = 0;
+        const int64_t nx = P.unit + gridDim.x;
+        P.t_next = nx < units ? unit_temp(A, nx) : 0.f;
+        if (P.cnt > 0) return;
+        P.unit = nx;
+        T = P.t_next;
     }
-    const int32_t c = w + (i - ndw) * kFastWarps;
-    const uint32_t off = static_cast<uint32_t>(c) * kFastData;
-    const uint32_t nb = min(kFastData, static_cast<uint32_t>(A.V) * 2 - off);
-    uint32_t pb = 0;
-    int32_t p0a = 0;
-    if (u.has_draft && plan_ok) {
-        const int32_t p0 = A.plan.chunk[c], p1 = A.plan.chunk[c + 1];
-        p0a = p0 & ~3;
-        if (p1 > p0) pb = min(kFastPairCap * 4, static_cast<uint32_t>((p1 - p0a) * 4 + 15) & ~15u);
+}
+
+// issue the warp's next chunk if a stage is free
+__device__ __forceinline__ void producer_step(const SampleArgs& A, Producer& P, uint32_t consumed, int w, int lane,
+                                              int64_t units, unsigned char* wst, uint64_t* wbar, uint64_t pol_t,
+                                              uint64_t pol_d)
+{
+    if (P.unit >= units || P.issued - consumed >= static_cast<uint32_t>(kFastStages)) return;
+    const uint32_t sidx = P.issued % kFastStages;
+    if (lane == 0) issue_seq(A, P.u, w + P.i * kFastWarps, wst + sidx * kFastStage, &wbar[sidx], pol_t, pol_d);
+    ++P.issued;
+    if (++P.i == P.cnt) {
+        P.unit += gridDim.x;
+        producer_enter(A, P, w, units, P.t_next);
     }
-    mbar_arrive_expect_tx(bar, nb + pb);
-    bulk_copy_g2s(stage, u.trow + off, nb, bar, pol_t);
-    if (pb) bulk_copy_g2s(stage + kFastData, A.plan.pairs + p0a, pb, bar, pol_d);
 }
 
 }  // namespace
@@ -909,163 +933,185 @@ __device__ __forceinline__ void issue_warp_chunk(const SampleArgs& A, const Fast
 __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(SampleArgs A)
 {
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // [warp][2]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // [warp][stage]
     unsigned char* ring = smem + kFastHeader;
-    uint16_t* G = reinterpret_cast<uint16_t*>(ring + kFastWarps * 2 * kFastStage);
+    uint16_t* G = reinterpret_cast<uint16_t*>(ring + kFastWarps * kFastStages * kFastStage);
+    int32_t* ctab = reinterpret_cast<int32_t*>(reinterpret_cast<unsigned char*>(G) + align256(A.Vd * 2));
     __shared__ float zx_shared;
-    __shared__ int32_t rx_shared;
-    __shared__ float rv_shared;
+    __shared__ int32_t jdx_shared;  // draft id of the draft token (-1: off the support)
+    __shared__ float qx_shared;     // q at that draft id
     __shared__ WarpRec wrec[kFastWarps];
     __shared__ float wsum[kFastWarps][2];
-    __shared__ float wtv[kFastWarps], wrv[kFastWarps];
-    __shared__ int32_t wrj[kFastWarps];
+    __shared__ float wtv[kFastWarps];
     __shared__ int32_t amax_shared;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int32_t nchunks_t = (A.V + kChunkElems - 1) / kChunkElems;
 
     pdl_wait_primary();  // a plan built in the same call must be complete
     pdl_launch_dependents();
     if (tid == 0) {
-        for (int i = 0; i < 2 * kFastWarps; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < kFastStages * kFastWarps; ++i) mbar_init(&bars[i], 1);
         fence_barrier_init();
     }
-    __syncthreads();
     // a plan for other sizes, or built from a d2t with repeated / out-of-range ids, is not
     // trusted for shared-memory indexing (the race kernel reports SV_ST_BAD_D2T)
     const bool plan_ok = A.plan.header[0] == A.V && A.plan.header[1] == A.Vd && A.plan.header[2] == 0;
+    for (int32_t c = tid; c <= nchunks_t; c += kFastThreads) ctab[c] = plan_ok ? A.plan.chunk[c] : 0;
+    __syncthreads();
     const uint64_t pol_t = l2_policy_evict_first();
     uint64_t pol_d;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_d));
-    unsigned char* wst = ring + w * 2 * kFastStage;  // this warp's two stages
-    uint64_t* wbar = bars + 2 * w;
-    uint32_t gi = 0;  // chunks this warp has consumed so far (stage = gi & 1)
-    uint32_t timeout = 0;
-    bool prefetched = false;
-
+    unsigned char* wst = ring + w * kFastStages * kFastStage;  // this warp's stages
+    uint64_t* wbar = bars + kFastStages * w;
     const int64_t units = static_cast<int64_t>(A.R) * (A.k + 1);
-    for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
-        const FastUnit u = fast_unit(A, unit);
-        const float T = A.temp[u.r];
+    uint32_t consumed = 0;  // chunks this warp has read so far (stage = consumed % kFastStages)
+    uint32_t timeout = 0;
+
+    Producer P;
+    P.unit = blockIdx.x;
+    P.issued = 0;
+    producer_enter(A, P, w, units, P.unit < units ? unit_temp(A, P.unit) : 0.f);
+    for (int i = 0; i < kFastStages; ++i)
+        producer_step(A, P, consumed, w, lane, units, wst, wbar, pol_t, pol_d);
+
+    int64_t unit = blockIdx.x;
+    float T = unit < units ? unit_temp(A, unit) : 0.f;
+    for (; unit < units; unit += gridDim.x) {
+        const FastUnit u = fast_unit(A, unit, T);
+        const int64_t un = unit + gridDim.x;
+        const float T_next = un < units ? unit_temp(A, un) : 0.f;  // for the next unit, loaded early
         const float c = u.sampling ? kLog2e / T : 0.f;
         const unsigned long long c2 = pack2(c, c);
         const int32_t xj = u.has_draft ? A.draft[static_cast<int64_t>(u.r) * A.k + u.j] : -1;
-        const int32_t ndw = warp_chunks(u.nd, w), ntw = warp_chunks(u.nt, w);
-        const int32_t nw_chunks = ndw + ntw;
-        if (u.j == 0 && tid == 0) {
-            A.race[u.r].best = ~0ull;
-            A.race[u.r].count = 0u;
+        const int32_t nw_chunks = warp_chunks(u.n, w);
+        if (u.j == 0 && tid == 0) A.race[u.r].count = 0u;
+        if (tid == 0) {
+            zx_shared = NAN;
+            jdx_shared = -1;
         }
-        if (tid == 0) zx_shared = NAN;
         __syncthreads();  // G, zx and the exchange arrays of the previous row are no longer read
-        if (lane == 0 && !prefetched && nw_chunks > 0)
-            issue_warp_chunk(A, u, w, 0, wst + (gi & 1) * kFastStage, &wbar[gi & 1], pol_t, pol_d, plan_ok);
 
         float dm = -INFINITY, ds = 0.f, tm = -INFINITY, ts = 0.f, bv = -INFINITY;
         int32_t bx = INT32_MAX;
         uint32_t dflags = 0, tflags = 0;
-        for (int32_t i = 0; i < nw_chunks; ++i, ++gi) {
-            const uint32_t s = gi & 1;
-            if (lane == 0 && i + 1 < nw_chunks) {
-                fence_proxy_async_smem();
-                issue_warp_chunk(A, u, w, i + 1, wst + (s ^ 1) * kFastStage, &wbar[s ^ 1], pol_t, pol_d, plan_ok);
-            }
-            if (!timeout && !mbar_wait_bounded(&wbar[s], (gi >> 1) & 1u)) timeout = 1;
-            const unsigned char* st = wst + s * kFastStage;
+        for (int32_t i = 0; i < nw_chunks; ++i) {
+            const uint32_t sidx = consumed % kFastStages;
+            if (!timeout && !mbar_wait_bounded(&wbar[sidx], (consumed / kFastStages) & 1u)) timeout = 1;
+            const unsigned char* st = wst + sidx * kFastStage;
             const uint4* vp = reinterpret_cast<const uint4*>(st);
-            const bool is_draft = i < ndw;
-            const int32_t cidx = w + (is_draft ? i : i - ndw) * kFastWarps;
+            const int32_t q = w + i * kFastWarps;
+            const bool is_draft = q < u.nd;
+            const int32_t cidx = is_draft ? q : q - u.nd;
             const uint32_t off = static_cast<uint32_t>(cidx) * kFastData;
             const uint32_t nb = min(kFastData, static_cast<uint32_t>(is_draft ? A.Vd : A.V) * 2 - off);
             const int nv = static_cast<int>(nb / 16);
             const int32_t x0 = static_cast<int32_t>(off / 2);
-            // all 8 vectors of this lane first (independent loads and max trees), one update of
-            // the running max, then 64 independent exps
-            constexpr int kVL = kChunkElems / 8 / 32;  // vectors per lane per chunk
-            uint4 q[kVL];
-            float vmx[kVL];
-            bool nan_seen = false;
+            // support entries of a target chunk: this lane's groups of four packed pairs, from
+            // L2 while the maxima and exponentials below run
+            const bool scatter = !is_draft && u.has_draft;
+            int32_t p0 = 0, p1 = 0, p0a = 0;
+            uint4 pg[kPairRegs];
+            if (scatter) {
+                p0 = ctab[cidx];
+                p1 = ctab[cidx + 1];
+                p0a = p0 & ~3;
 #pragma unroll
-            for (int e = 0; e < kVL; ++e) {
-                const int v = lane + 32 * e;
-                q[e] = v < nv ? vp[v] : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
-                const uint32_t m2 = bmax2_nan(bmax2_nan(q[e].x, q[e].y), bmax2_nan(q[e].z, q[e].w));
-                vmx[e] = fmax_nan(bf16_lo(m2), bf16_hi(m2));
-                nan_seen |= vmx[e] != vmx[e];
-            }
-            if (nan_seen) {  // rare: NaN logits read as -inf
-                (is_draft ? dflags : tflags) |= kFlagNaN;
-#pragma unroll
-                for (int e = 0; e < kVL; ++e) {
-                    q[e] = make_uint4(bf16x2_nan_to_ninf(q[e].x), bf16x2_nan_to_ninf(q[e].y),
-                                      bf16x2_nan_to_ninf(q[e].z), bf16x2_nan_to_ninf(q[e].w));
-                    const uint32_t m3 = bmax2_nan(bmax2_nan(q[e].x, q[e].y), bmax2_nan(q[e].z, q[e].w));
-                    vmx[e] = fmaxf(bf16_lo(m3), bf16_hi(m3));
+                for (int t = 0; t < kPairRegs; ++t) {
+                    const int32_t g = p0a + 4 * (lane + 32 * t);
+                    pg[t] = g < p1 ? ld_nc_v4(reinterpret_cast<const uint4*>(A.plan.pairs + g)) : make_uint4(0, 0, 0, 0);
                 }
             }
-            float lm = vmx[0];
 #pragma unroll
-            for (int e = 1; e < kVL; ++e) lm = fmaxf(lm, vmx[e]);
-            if (!is_draft) {
+            for (int h = 0; h < 2; ++h) {
+                // half the lane's vectors: independent loads and max trees, one update of the
+                // running max, then the independent exps
+                constexpr int kH = kVL / 2;
+                uint4 qv[kH];
+                float vmx[kH];
+                bool nan_seen = false;
 #pragma unroll
-                for (int e = 0; e < kVL; ++e) {  // ascending vector starts: strict > keeps the first
-                    const bool up = vmx[e] > bv;
-                    bv = up ? vmx[e] : bv;
-                    bx = up ? x0 + (lane + 32 * e) * 8 : bx;
+                for (int e = 0; e < kH; ++e) {
+                    const int v = lane + 32 * (h * kH + e);
+                    qv[e] = v < nv ? vp[v] : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+                    const uint32_t m2 = bmax2_nan(bmax2_nan(qv[e].x, qv[e].y), bmax2_nan(qv[e].z, qv[e].w));
+                    vmx[e] = fmax_nan(bf16_lo(m2), bf16_hi(m2));
+                    nan_seen |= vmx[e] != vmx[e];
                 }
-            } else if (lm == INFINITY) {
-                dflags |= kFlagPosInf;
+                if (nan_seen) {  // rare: NaN logits read as -inf
+                    (is_draft ? dflags : tflags) |= kFlagNaN;
+#pragma unroll
+                    for (int e = 0; e < kH; ++e) {
+                        qv[e] = make_uint4(bf16x2_nan_to_ninf(qv[e].x), bf16x2_nan_to_ninf(qv[e].y),
+                                           bf16x2_nan_to_ninf(qv[e].z), bf16x2_nan_to_ninf(qv[e].w));
+                        const uint32_t m3 = bmax2_nan(bmax2_nan(qv[e].x, qv[e].y), bmax2_nan(qv[e].z, qv[e].w));
+                        vmx[e] = fmaxf(bf16_lo(m3), bf16_hi(m3));
+                    }
+                }
+                float lm = vmx[0];
+#pragma unroll
+                for (int e = 1; e < kH; ++e) lm = fmaxf(lm, vmx[e]);
+                if (!is_draft) {
+                    if (lm > bv) {  // rare after the first chunks: the first vector holding the new max
+#pragma unroll
+                        for (int e = kH - 1; e >= 0; --e)
+                            if (vmx[e] == lm) bx = x0 + (lane + 32 * (h * kH + e)) * 8;
+                        bv = lm;
+                    }
+                } else if (lm == INFINITY) {
+                    dflags |= kFlagPosInf;
+                }
+                if (is_draft || u.sampling) {
+                    float& rm = is_draft ? dm : tm;
+                    float& rs_ = is_draft ? ds : ts;
+                    const float mt = lm * c;
+                    if (mt > rm) {
+                        rs_ = rm == -INFINITY ? 0.f : rs_ * ex2(rm - mt);
+                        rm = mt;
+                    }
+                    if (rm > -INFINITY) {
+                        const unsigned long long nm2 = pack2(-rm, -rm);
+                        float acc[kH];
+#pragma unroll
+                        for (int e = 0; e < kH; ++e) acc[e] = exp_sum8(qv[e], c2, nm2);
+#pragma unroll
+                        for (int e = 1; e < kH; ++e) acc[0] += acc[e];
+                        rs_ += acc[0];
+                    }
+                }
             }
-            if (is_draft || u.sampling) {
-                float& rm = is_draft ? dm : tm;
-                float& rs_ = is_draft ? ds : ts;
-                const float mt = lm * c;
-                if (mt > rm) {
-                    rs_ = rm == -INFINITY ? 0.f : rs_ * ex2(rm - mt);
-                    rm = mt;
-                }
-                if (rm > -INFINITY) {
-                    const unsigned long long nm2 = pack2(-rm, -rm);
-                    float acc8[kVL];
-#pragma unroll
-                    for (int e = 0; e < kVL; ++e) acc8[e] = exp_sum8(q[e], c2, nm2);
-#pragma unroll
-                    for (int e = 1; e < kVL; ++e) acc8[0] += acc8[e];
-                    rs_ += acc8[0];
-                }
-            }
-            if (!is_draft && u.has_draft) {
-                // support entries of this chunk: G[draft id] = z at the chunk offset
+            if (scatter) {
+                // G[draft id] = z at the chunk offset, for the entries [p0, p1) of the plan
                 const uint16_t* zs = reinterpret_cast<const uint16_t*>(st);
-                const uint32_t* pr = reinterpret_cast<const uint32_t*>(st + kFastData);
-                const int32_t p0 = plan_ok ? A.plan.chunk[cidx] : 0;
-                const int32_t cnt = plan_ok ? A.plan.chunk[cidx + 1] - p0 : 0;
-                const int32_t base = p0 & 3;
-                const int32_t staged = min(cnt, static_cast<int32_t>(kFastPairCap) - base);
-#pragma unroll 4
-                for (int32_t e = lane; e < staged; e += 32) {
-                    const uint32_t pe = pr[base + e];
-                    G[pe >> 16] = zs[pe & (kChunkElems - 1)];
+                const bool here = xj >= x0 && xj < x0 + static_cast<int32_t>(nb / 2);
+#pragma unroll
+                for (int t = 0; t < kPairRegs; ++t) {
+                    const int32_t g = p0a + 4 * (lane + 32 * t);
+                    const uint32_t pe[4] = {pg[t].x, pg[t].y, pg[t].z, pg[t].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (g + e >= p0 && g + e < p1) G[pe[e] >> 16] = zs[pe[e] & (kChunkElems - 1)];
                 }
-                for (int32_t e = max(staged, 0) + lane; e < cnt; e += 32) {  // beyond the staged entries
-                    const uint32_t pe = A.plan.pairs[p0 + e];
-                    G[pe >> 16] = zs[pe & (kChunkElems - 1)];
+                // entries beyond this lane's register groups (chunks denser than 512 entries)
+                for (int32_t g = p0a + 4 * 32 * kPairRegs + lane; g < p1; g += 32) {
+                    const uint32_t pe = A.plan.pairs[g];
+                    if (g >= p0) G[pe >> 16] = zs[pe & (kChunkElems - 1)];
                 }
-                if (lane == 0 && xj >= x0 && xj < x0 + static_cast<int32_t>(nb / 2))
-                    zx_shared = __uint_as_float(static_cast<uint32_t>(zs[xj - x0]) << 16);
+                if (here) {  // the draft token: its logit and its draft id
+                    const uint32_t xoff = static_cast<uint32_t>(xj - x0);
+                    if (lane == 0) zx_shared = __uint_as_float(static_cast<uint32_t>(zs[xoff]) << 16);
+                    for (int32_t g = p0 + lane; g < p1; g += 32) {
+                        const uint32_t pe = A.plan.pairs[g];
+                        if ((pe & (kChunkElems - 1)) == xoff) jdx_shared = static_cast<int32_t>(pe >> 16);
+                    }
+                }
             }
+            // the stage is read: refill it with this warp's next chunk
             __syncwarp();
+            ++consumed;
+            if (lane == 0) fence_proxy_async_smem();
+            producer_step(A, P, consumed, w, lane, units, wst, wbar, pol_t, pol_d);
         }
-        // first chunk of this warp's next row, in flight during the reductions below
-        prefetched = false;
-        if (unit + gridDim.x < units) {
-            const FastUnit un = fast_unit(A, unit + gridDim.x);
-            if (warp_chunks(un.nd, w) + warp_chunks(un.nt, w) > 0) {
-                if (lane == 0) {
-                    fence_proxy_async_smem();
-                    issue_warp_chunk(A, un, w, 0, wst + (gi & 1) * kFastStage, &wbar[gi & 1], pol_t, pol_d, plan_ok);
-                }
-                prefetched = true;
-            }
-        }
+        T = T_next;
 
         // ---- reductions: two exchanges through shared memory ----
         const float my_bv = bv, my_tm = tm, my_ts = ts, my_dm = dm, my_ds = ds;
@@ -1144,91 +1190,74 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
         if (u.has_draft && ((FLD & (kFlagNaN | kFlagPosInf)) || Mq == -INFINITY)) flags |= kFlagDraftBad;
 
         // ---- TV = sum over the support of max(0, q - p); p(x_j), q(x_j), accept ----
+        // G (z at every draft id) and the L2-resident draft row, in draft-id order; every
+        // thread issues all of its draft-row loads before the arithmetic
         float tvv = NAN, pj = NAN, qj = NAN;
         int32_t acc = 0;
         if (u.has_draft) {
             const float invS = 1.f / S, invSq = 1.f / Sq;
-            float a = 0.f;
-            float rbest = 0.f;  // largest residual p - q seen and its draft id
-            int32_t rj = -1;
-            const int32_t nv8 = A.Vd / 8;
+            const unsigned long long c2m = pack2(c, c), nM = pack2(-M, -M), nMq = pack2(-Mq, -Mq);
+            const unsigned long long iS = pack2(invS, invS), iSq = pack2(invSq, invSq);
+            const int32_t jdx = jdx_shared;
+            const int32_t nv8 = A.Vd / 8;  // Vd % 8 == 0 on this path
             const uint4* yv = reinterpret_cast<const uint4*>(u.drow);
             const uint4* gv = reinterpret_cast<const uint4*>(G);
-            for (int32_t v = tid; v < nv8; v += kFastThreads) {
-                const uint4 gq = gv[v];
-                const uint4 yq = ld_nc_v4(yv + v);
-                const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
-                const uint32_t yw[4] = {yq.x, yq.y, yq.z, yq.w};
-                float d[8];
+            constexpr int kTvIter = (kFastMaxVd / 8 + kFastThreads - 1) / kFastThreads;
+            constexpr int kTvBatch = (kTvIter + 1) / 2;  // draft-row loads in flight per thread
+            float a = 0.f;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    d[2 * e] = ex2(fmaf(bf16_lo(yw[e]), c, -Mq)) * invSq - ex2(fmaf(bf16_lo(gw[e]), c, -M)) * invS;
-                    d[2 * e + 1] = ex2(fmaf(bf16_hi(yw[e]), c, -Mq)) * invSq - ex2(fmaf(bf16_hi(gw[e]), c, -M)) * invS;
-                }
-                // d = q - p: TV sums its positive part; the most negative d is the largest residual p - q
-                float dmin = d[0];
-                int emin = 0;
+            for (int b0 = 0; b0 < kTvIter; b0 += kTvBatch) {
+                uint4 yq[kTvBatch];
 #pragma unroll
-                for (int e = 1; e < 8; ++e) {
-                    const bool lt = d[e] < dmin;
-                    dmin = lt ? d[e] : dmin;
-                    emin = lt ? e : emin;
+                for (int i = 0; i < kTvBatch; ++i) {
+                    const int32_t v = tid + (b0 + i) * kFastThreads;
+                    if (b0 + i < kTvIter && v < nv8) yq[i] = ld_nc_v4(yv + v);
                 }
-                if (-dmin > rbest) {
-                    rbest = -dmin;
-                    rj = v * 8 + emin;
-                }
-                a += ((fmaxf(d[0], 0.f) + fmaxf(d[1], 0.f)) + (fmaxf(d[2], 0.f) + fmaxf(d[3], 0.f))) +
-                     ((fmaxf(d[4], 0.f) + fmaxf(d[5], 0.f)) + (fmaxf(d[6], 0.f) + fmaxf(d[7], 0.f)));
-            }
-            for (int32_t jd = nv8 * 8 + tid; jd < A.Vd; jd += kFastThreads) {
-                const float pp = ex2(fmaf(__uint_as_float(static_cast<uint32_t>(G[jd]) << 16), c, -M)) * invS;
-                const float qq = ex2(fmaf(ld_elem<SV_BF16>(u.drow, jd), c, -Mq)) * invSq;
-                a += fmaxf(qq - pp, 0.f);
-            }
-            // one exchange: the TV sum and the largest support residual
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                a += __shfl_xor_sync(0xffffffffu, a, o);
-                const float ov = __shfl_xor_sync(0xffffffffu, rbest, o);
-                const int32_t oj = __shfl_xor_sync(0xffffffffu, rj, o);
-                if (ov > rbest || (ov == rbest && oj < rj)) {
-                    rbest = ov;
-                    rj = oj;
+                for (int i = 0; i < kTvBatch; ++i) {
+                    const int32_t v = tid + (b0 + i) * kFastThreads;
+                    if (b0 + i >= kTvIter || v >= nv8) break;
+                    const uint4 gq = gv[v];
+                    const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
+                    const uint32_t yw[4] = {yq[i].x, yq[i].y, yq[i].z, yq[i].w};
+                    float qv[8], dv[8];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        // q and p of two ids at once: 2^(y c - Mq) / Sq and 2^(z c - M) / S
+                        const unsigned long long ty = fma2(bf16x2_to_f32x2(yw[e]), c2m, nMq);
+                        const unsigned long long tz = fma2(bf16x2_to_f32x2(gw[e]), c2m, nM);
+                        float y0, y1, z0, z1;
+                        unpack2(ty, y0, y1);
+                        unpack2(tz, z0, z1);
+                        float q0, q1, p0, p1;
+                        unpack2(mul2(pack2(ex2(y0), ex2(y1)), iSq), q0, q1);
+                        unpack2(mul2(pack2(ex2(z0), ex2(z1)), iS), p0, p1);
+                        qv[2 * e] = q0;
+                        qv[2 * e + 1] = q1;
+                        dv[2 * e] = q0 - p0;
+                        dv[2 * e + 1] = q1 - p1;
+                    }
+                    if (v == (jdx >> 3)) {  // this vector holds the draft token's draft id
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            if (e == (jdx & 7)) qx_shared = qv[e];
+                    }
+                    a += ((fmaxf(dv[0], 0.f) + fmaxf(dv[1], 0.f)) + (fmaxf(dv[2], 0.f) + fmaxf(dv[3], 0.f))) +
+                         ((fmaxf(dv[4], 0.f) + fmaxf(dv[5], 0.f)) + (fmaxf(dv[6], 0.f) + fmaxf(dv[7], 0.f)));
                 }
             }
-            if (lane == 0) {
-                wtv[w] = a;
-                wrv[w] = rbest;
-                wrj[w] = rj;
-            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+            if (lane == 0) wtv[w] = a;
             __syncthreads();
             if (tid == 0) {
                 tvv = 0.f;
-                float nrv = 0.f;
-                int32_t nrj = -1;
-                for (int i = 0; i < kFastWarps; ++i) {
-                    tvv += wtv[i];
-                    if (wrv[i] > nrv || (wrv[i] == nrv && wrj[i] < nrj)) {
-                        nrv = wrv[i];
-                        nrj = wrj[i];
-                    }
-                }
-                rx_shared = (plan_ok && nrj >= 0 && nrj < A.Vd && nrv > 0.f) ? A.plan.x_of_j[nrj] : -1;
-                rv_shared = nrv;
+                for (int i = 0; i < kFastWarps; ++i) tvv += wtv[i];
                 const bool in_range = xj >= 0 && xj < A.V;
                 float zx = zx_shared;
                 zx = zx != zx ? -INFINITY : zx;
                 pj = in_range ? ex2(fmaf(zx, c, -M)) * invS : 0.f;
-                qj = 0.f;
-                if (in_range && in_support(A.plan, xj)) {
-                    const int32_t jd = A.plan.js[support_rank(A.plan, xj)];
-                    if (jd >= 0 && jd < A.Vd) {
-                        float y = ld_elem<SV_BF16>(u.drow, jd);
-                        y = y != y ? -INFINITY : y;
-                        qj = ex2(fmaf(y, c, -Mq)) * invSq;
-                    }
-                }
+                qj = (in_range && jdx >= 0) ? qx_shared : 0.f;
                 if (qj > 0.f) {
                     const uint4 w4 = philox_block(philox_key(A.seeds[u.r]), 0u, static_cast<uint32_t>(u.j), kTagAccept);
                     acc = uniform_from_word(w4.x) < __fdiv_rn(pj, qj) ? 1 : 0;
@@ -1252,41 +1281,6 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
             rs.amax = amax;
             rs.flags = flags;
             rs.accept = acc;
-            rs.rx = u.has_draft ? rx_shared : -1;
-            rs.rv = u.has_draft ? rv_shared : 0.f;
-            // a bound for the race on this row, should it be the selected one: the key of
-            // the argmax, and for a residual race also of the largest support residual
-            rs.bkey = INFINITY;
-            rs.bxc = -1;
-            if (u.sampling && !(flags & (kFlagNaN | kFlagPosInf | kFlagAllNegInf | kFlagDraftBad)) && S > 0.f) {
-                const PhiloxKey key = philox_key(A.seeds[u.r]);
-                const bool residual = u.j < A.k;
-                const uint32_t tag = residual ? kTagResidual : kTagBonus;
-                auto key_of = [&](int32_t x, float wt) -> float {
-                    if (!(wt > 0.f)) return INFINITY;
-                    const uint4 w4 = philox_block(key, static_cast<uint32_t>(x >> 2), static_cast<uint32_t>(u.j), tag);
-                    const uint32_t wd = (x & 3) == 0 ? w4.x : ((x & 3) == 1 ? w4.y : ((x & 3) == 2 ? w4.z : w4.w));
-                    return __fdiv_rn(-log1pf(-one_minus_uniform_from_word(wd)), wt);
-                };
-                float wa = ex2(fmaf(BV, c, -M)) * (1.f / S);
-                if (residual && in_support(A.plan, amax)) {
-                    const int32_t jd = A.plan.js[support_rank(A.plan, amax)];
-                    if (jd >= 0 && jd < A.Vd) {
-                        float y = ld_elem<SV_BF16>(u.drow, jd);
-                        y = y != y ? -INFINITY : y;
-                        wa -= ex2(fmaf(y, c, -Mq)) * (1.f / Sq);
-                    }
-                }
-                rs.bkey = key_of(amax, wa);
-                rs.bxc = rs.bkey < INFINITY ? amax : -1;
-                if (residual && rs.rx >= 0) {
-                    const float kr = key_of(rs.rx, rs.rv);
-                    if (kr < rs.bkey) {
-                        rs.bkey = kr;
-                        rs.bxc = rs.rx;
-                    }
-                }
-            }
             A.stats[unit] = rs;
             if (u.j < A.k) {
                 const int64_t o = static_cast<int64_t>(u.r) * A.k + u.j;
@@ -1298,169 +1292,101 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
     }
     if (timeout && lane == 0) {
         // give this warp's copies that may still be in flight a bounded chance to land
-        (void)mbar_wait_bounded(&wbar[gi & 1], (gi >> 1) & 1u);
-        (void)mbar_wait_bounded(&wbar[(gi + 1) & 1], ((gi + 1) >> 1) & 1u);
+        for (uint32_t g = consumed; g < P.issued; ++g)
+            (void)mbar_wait_bounded(&wbar[g % kFastStages], (g / kFastStages) & 1u);
     }
 }
 
 // ---------------------------------------------------------------------------
-// scan + race + commit
+// scan + two-level race + commit
 // ---------------------------------------------------------------------------
+// The correction token is a draw from w / sum(w), w = max(0, p - q) on the
+// first rejected row (p on the bonus row).  It is taken as an exponential race
+// in two levels: the ids are cut into chunks of kRaceChunk, the chunk is drawn
+// by a race over the chunk sums W_c (uniforms of the chunk tag, counted by c),
+// then the id by a race over that chunk only (uniforms of the element tag,
+// counted by the id).  P(chunk) = W_c / sum W and P(id | chunk) = w / W_c, so
+// the draw is exact, and only one chunk's uniforms are ever generated.
+//
+// race_chunks_kernel: RC CTAs per request, each summing kRaceChunksPerCta
+// chunks of the selected row (W_c and the p sums P_c); the last CTA of the
+// request runs both races and commits the tokens.
 namespace {
 
-__device__ __forceinline__ unsigned long long pack_key(float key, int32_t x)
+constexpr int32_t kRaceChunk = 2048;
+constexpr int kRaceChunksPerCta = 4;
+constexpr int kRaceIdsPerThread = kRaceChunk / kRaceThreads;  // 8
+static_assert(kRaceIdsPerThread == 8, "one 8-id vector per thread and chunk");
+
+// z[0..8) of ids [x, x + 8) of a row (-inf at and beyond x_end; NaN read as -inf)
+template <int DT>
+__device__ __forceinline__ void load8(const char* row, int32_t x, int32_t x_end, bool vec_ok, float* z)
 {
-    return (static_cast<unsigned long long>(__float_as_uint(key)) << 32) | static_cast<uint32_t>(x);
+    if (vec_ok && x + 8 <= x_end) {
+        if constexpr (DT == SV_BF16) {
+            const uint4 v = *reinterpret_cast<const uint4*>(row + static_cast<int64_t>(x) * 2);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                z[2 * e] = bf16_lo(w[e]);
+                z[2 * e + 1] = bf16_hi(w[e]);
+            }
+        } else {
+            const float4 a = *reinterpret_cast<const float4*>(row + static_cast<int64_t>(x) * 4);
+            const float4 b = *reinterpret_cast<const float4*>(row + static_cast<int64_t>(x) * 4 + 16);
+            z[0] = a.x; z[1] = a.y; z[2] = a.z; z[3] = a.w;
+            z[4] = b.x; z[5] = b.y; z[6] = b.z; z[7] = b.w;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) z[e] = x + e < x_end ? ld_elem<DT>(row, x + e) : -INFINITY;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) z[e] = z[e] != z[e] ? -INFINITY : z[e];
+}
+
+// q over target ids [x0, x0 + n) into qs[0..n): 0 off the support.  Every
+// thread of the block takes part; the caller synchronises before reading qs.
+template <int DD>
+__device__ __forceinline__ void fill_q(const SampleArgs& A, const char* drow, int32_t x0, int32_t n, float c,
+                                       float mq, float invSq, float* qs)
+{
+    for (int32_t i = threadIdx.x; i < n; i += kRaceThreads) qs[i] = 0.f;
+    __syncthreads();
+    const int32_t p0 = support_rank(A.plan, x0), p1 = support_rank(A.plan, x0 + n);
+#pragma unroll 4
+    for (int32_t p = p0 + static_cast<int32_t>(threadIdx.x); p < p1; p += kRaceThreads) {
+        const int32_t x = A.plan.xs[p], jd = A.plan.js[p];
+        if (x < x0 || x >= x0 + n || jd < 0 || jd >= A.Vd) continue;
+        float y = ld_elem<DD>(drow, jd);
+        y = y != y ? -INFINITY : y;
+        qs[x - x0] = ex2(fmaf(y, c, -mq)) * invSq;
+    }
+}
+
+// (key, id) minimum over the block, lowest id among equal keys; threads
+// without a candidate pass (+inf, INT32_MAX)
+__device__ __forceinline__ void block_argmin_key(float& key, int32_t& id, float* sf, int32_t* si)
+{
+    float nk = id == INT32_MAX ? -INFINITY : -key;
+    block_argmax<kRaceThreads>(nk, id, sf, si);
+    key = -nk;
 }
 
 }  // namespace
 
-// E_x = -ln u_x >= -ln(1 - 2^-24) for every uniform of the library, so an
-// element whose weight w satisfies best * w below this cannot have a key
-// E_x / w_x below `best`.  The constant is taken a little low on purpose.
-constexpr float kMinE = 5.9e-8f;
-
-template <int DT>
-__device__ __forceinline__ void load4(const char* row, int32_t x, bool vec_ok, float* z)
-{
-    if constexpr (DT == SV_BF16) {
-        if (vec_ok) {
-            const uint2 v = *reinterpret_cast<const uint2*>(row + static_cast<int64_t>(x) * 2);
-            z[0] = bf16_lo(v.x);
-            z[1] = bf16_hi(v.x);
-            z[2] = bf16_lo(v.y);
-            z[3] = bf16_hi(v.y);
-            return;
-        }
-    } else {
-        if (vec_ok) {
-            const float4 v = *reinterpret_cast<const float4*>(row + static_cast<int64_t>(x) * 4);
-            z[0] = v.x;
-            z[1] = v.y;
-            z[2] = v.z;
-            z[3] = v.w;
-            return;
-        }
-    }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) z[e] = ld_elem<DT>(row, x + e);
-}
-
-// q(x) of the draft row (0 off the support): the residual weight needs it only for the
-// few elements whose target weight alone could still win the race
-template <int DD>
-__device__ __forceinline__ float draft_q(const SampleArgs& A, const char* drow, int32_t x, float c, float mq,
-                                         float invSq)
-{
-    int32_t jd = x;
-    if (!A.identity) {
-        if (!in_support(A.plan, x)) return 0.f;
-        jd = A.plan.js[support_rank(A.plan, x)];
-    }
-    if (jd < 0 || jd >= A.Vd) return 0.f;
-    float y = ld_elem<DD>(drow, jd);
-    y = y != y ? -INFINITY : y;
-    return ex2(fmaf(y, c, -mq)) * invSq;
-}
-
-// the race over row elements [x0, x1): this thread's best (key, x), starting from the
-// bound `best`.  w_x = p(x) - q(x) (residual) or p(x) (bonus).  Since E_x >= v_x = 1 - u_x
-// and w_x <= p(x), an element with v_x >= best * p(x) cannot win; the row's loads of a
-// batch are issued together, Philox runs only for groups some element of which passes
-// on p, and q is looked up only for elements that pass on p.
-constexpr int kRaceBatch = 8;  // groups of 4 elements per thread in flight
 template <int DT, int DD>
-__device__ __forceinline__ void race_range(const SampleArgs& A, const char* trow, const char* drow, int32_t x0,
-                                           int32_t x1, float c, const RowStat& rs, bool residual, PhiloxKey key,
-                                           uint32_t row, uint32_t tag, bool vec_ok, float& best, int32_t& bx)
-{
-    const int32_t g0 = x0 >> 2, g1 = (x1 + 3) >> 2;
-    const float invS = 1.f / rs.s, invSq = residual ? 1.f / rs.sq : 0.f;
-    for (int32_t gb = g0 + static_cast<int32_t>(threadIdx.x); gb < g1; gb += kRaceBatch * kRaceThreads) {
-        float z[kRaceBatch][4];
-#pragma unroll
-        for (int i = 0; i < kRaceBatch; ++i) {
-            const int32_t g = gb + i * kRaceThreads, xb = 4 * g;
-            if (g < g1 && xb >= x0 && xb + 4 <= x1) {
-                load4<DT>(trow, xb, vec_ok, z[i]);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    z[i][e] = (g < g1 && xb + e >= x0 && xb + e < x1) ? ld_elem<DT>(trow, xb + e) : -INFINITY;
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < kRaceBatch; ++i) {
-            const int32_t g = gb + i * kRaceThreads, xb = 4 * g;
-            float w[4], wmax = 0.f;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float zz = z[i][e] != z[i][e] ? -INFINITY : z[i][e];
-                w[e] = ex2(fmaf(zz, c, -rs.m)) * invS;
-                wmax = fmaxf(wmax, w[e]);
-            }
-            if (!(best * wmax >= kMinE)) continue;  // no element of the group can beat `best`
-            const uint4 w4 = philox_block(key, static_cast<uint32_t>(g), row, tag);
-            const uint32_t words[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float wt = w[e];
-                if (!(wt > 0.f)) continue;
-                const float v = one_minus_uniform_from_word(words[e]);
-                if (!(v < best * wt)) continue;  // E >= v and w <= p
-                const int32_t x = xb + e;
-                if (residual) {
-                    wt -= draft_q<DD>(A, drow, x, c, rs.mq, invSq);
-                    if (!(wt > 0.f) || !(v < best * wt)) continue;
-                }
-                const float k2 = __fdiv_rn(-log1pf(-v), wt);
-                if (k2 < best || (k2 == best && x < bx)) {
-                    best = k2;
-                    bx = x;
-                }
-            }
-        }
-    }
-}
-
-// the race key of one element (or +inf when its weight is not positive)
-template <int DT, int DD>
-__device__ __forceinline__ float single_key(const SampleArgs& A, const char* trow, const char* drow, int32_t x,
-                                            float c, const RowStat& rs, bool residual, PhiloxKey key, uint32_t row,
-                                            uint32_t tag)
-{
-    float z = ld_elem<DT>(trow, x);
-    z = z != z ? -INFINITY : z;
-    float w = ex2(fmaf(z, c, -rs.m)) * (1.f / rs.s);
-    if (residual) {
-        int32_t jd = -1;
-        if (A.identity) {
-            jd = x;
-        } else if (in_support(A.plan, x)) {
-            jd = A.plan.js[support_rank(A.plan, x)];
-        }
-        if (jd >= 0 && jd < A.Vd) {
-            float y = ld_elem<DD>(drow, jd);
-            y = y != y ? -INFINITY : y;
-            w -= ex2(fmaf(y, c, -rs.mq)) * (1.f / rs.sq);
-        }
-    }
-    if (!(w > 0.f)) return INFINITY;
-    const uint4 w4 = philox_block(key, static_cast<uint32_t>(x >> 2), row, tag);
-    const uint32_t wd = (x & 3) == 0 ? w4.x : ((x & 3) == 1 ? w4.y : ((x & 3) == 2 ? w4.z : w4.w));
-    return __fdiv_rn(-log1pf(-one_minus_uniform_from_word(wd)), w);
-}
-
-template <int DT, int DD>
-__global__ void __launch_bounds__(kRaceThreads) race_commit_kernel(SampleArgs A)
+__global__ void __launch_bounds__(kRaceThreads) race_chunks_kernel(SampleArgs A)
 {
     pdl_wait_primary();
+    __shared__ float qs[kRaceChunksPerCta * kRaceChunk];
     __shared__ float red_f[kRaceThreads / 32];
     __shared__ int32_t red_i[kRaceThreads / 32];
+    __shared__ float part[kRaceThreads / 32][2 * kRaceChunksPerCta];
     __shared__ int last_cta;
     __shared__ int32_t n_shared;
     __shared__ uint32_t fl_shared;
-    const int tid = threadIdx.x, lane = tid & 31;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int32_t r = static_cast<int32_t>(blockIdx.x / A.race_ctas);
     const int32_t rc = static_cast<int32_t>(blockIdx.x - static_cast<int64_t>(r) * A.race_ctas);
     const int32_t k = A.k;
@@ -1503,63 +1429,151 @@ __global__ void __launch_bounds__(kRaceThreads) race_commit_kernel(SampleArgs A)
     } else {
         const bool residual = n < k;
         const RowStat rs = st[n];
-        const float c = kLog2e / T;
-        const int32_t x0 = rc * A.race_seg, x1 = min(A.V, x0 + A.race_seg);
+        const float c = kLog2e / T, invS = 1.f / rs.s, invSq = residual ? 1.f / rs.sq : 0.f;
         const char* trow = A.tbase + (static_cast<int64_t>(r) * (k + 1) + n) * A.tstride;
         const char* drow = residual ? A.dbase + (static_cast<int64_t>(r) * k + n) * A.dstride : nullptr;
-        const PhiloxKey key = philox_key(A.seeds[r]);
-        const uint32_t tag = residual ? kTagResidual : kTagBonus;
-        // start from the row's precomputed bound; the CTA holding its element keeps it as a candidate
-        const int32_t cand_x = rs.bxc;
-        float best = rs.bkey;
-        int32_t bx = (tid == 0 && cand_x >= x0 && cand_x < x1 && best < INFINITY) ? cand_x : INT32_MAX;
-        race_range<DT, DD>(A, trow, drow, x0, x1, c, rs, residual, key, static_cast<uint32_t>(n), tag,
-                           A.tbulk != 0, best, bx);
-        // (key, lowest x) minimum over the CTA; threads without a candidate carry (inf, INT32_MAX)
-        float nb = bx == INT32_MAX ? -INFINITY : -best;
-        int32_t nx = bx;
+        const bool vec_ok = A.tbulk != 0;
+        const bool dvec_ok = A.dbulk != 0;
+        const int32_t nc = (A.V + kRaceChunk - 1) / kRaceChunk;
+        float* Wr = A.wsum + static_cast<int64_t>(r) * 2 * nc;  // [W_0..W_nc) then [P_0..P_nc)
+        float* Pr = Wr + nc;
+
+        // ---- chunk sums of this CTA's chunks ----
+        const int32_t c0 = rc * kRaceChunksPerCta;
+        const int32_t ncta = min(kRaceChunksPerCta, nc - c0);
+        const int32_t x0 = c0 * kRaceChunk, x1 = min(A.V, (c0 + ncta) * kRaceChunk);
+        float z[kRaceChunksPerCta][8];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, nb, o);
-            const int32_t ox = __shfl_xor_sync(0xffffffffu, nx, o);
-            if (ov > nb || (ov == nb && ox < nx)) {
-                nb = ov;
-                nx = ox;
-            }
+        for (int i = 0; i < kRaceChunksPerCta; ++i) {
+            const int32_t x = x0 + i * kRaceChunk + tid * 8;
+            if (i < ncta) load8<DT>(trow, x, x1, vec_ok, z[i]);
         }
-        if (lane == 0) {
-            red_f[tid >> 5] = nb;
-            red_i[tid >> 5] = nx;
+        float y[kRaceChunksPerCta][8];
+        if (residual && A.identity) {
+#pragma unroll
+            for (int i = 0; i < kRaceChunksPerCta; ++i) {
+                const int32_t x = x0 + i * kRaceChunk + tid * 8;
+                if (i < ncta) load8<DD>(drow, x, min(x1, A.Vd), dvec_ok, y[i]);
+            }
+        } else if (residual) {
+            fill_q<DD>(A, drow, x0, x1 - x0, c, rs.mq, invSq, qs);
         }
         __syncthreads();
-        if (tid == 0) {
-            for (int i = 1; i < kRaceThreads / 32; ++i)
-                if (red_f[i] > nb || (red_f[i] == nb && red_i[i] < nx)) {
-                    nb = red_f[i];
-                    nx = red_i[i];
+        float wsum[kRaceChunksPerCta], psum[kRaceChunksPerCta];
+#pragma unroll
+        for (int i = 0; i < kRaceChunksPerCta; ++i) {
+            wsum[i] = 0.f;
+            psum[i] = 0.f;
+            if (i >= ncta) continue;
+            const int32_t xi = x0 + i * kRaceChunk + tid * 8;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if (xi + e >= x1) break;  // beyond the row: qs holds nothing there
+                const float pe = ex2(fmaf(z[i][e], c, -rs.m)) * invS;
+                float we = pe;
+                if (residual) {
+                    const float qe = A.identity ? ex2(fmaf(y[i][e], c, -rs.mq)) * invSq
+                                                : qs[i * kRaceChunk + tid * 8 + e];
+                    we = fmaxf(pe - qe, 0.f);
                 }
-            RaceSlot* slot = A.race + r;
-            if (nx != INT32_MAX) atomicMin(&slot->best, pack_key(-nb, nx));
+                psum[i] += pe;
+                wsum[i] += we;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kRaceChunksPerCta; ++i) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                wsum[i] += __shfl_xor_sync(0xffffffffu, wsum[i], o);
+                psum[i] += __shfl_xor_sync(0xffffffffu, psum[i], o);
+            }
+            if (lane == 0) {
+                part[wid][2 * i] = wsum[i];
+                part[wid][2 * i + 1] = psum[i];
+            }
+        }
+        __syncthreads();
+        if (tid < 2 * ncta) {
+            float t = 0.f;
+            for (int w = 0; w < kRaceThreads / 32; ++w) t += part[w][tid];
+            const int32_t cc = c0 + (tid >> 1);
+            if (tid & 1) Pr[cc] = t;
+            else Wr[cc] = t;
+        }
+        // ---- the last CTA of the request runs the races ----
+        __syncthreads();
+        if (tid == 0) {
             __threadfence();
-            const unsigned prev = atomicAdd(&slot->count, 1u);
+            const unsigned prev = atomicAdd(&A.race[r].count, 1u);
             last_cta = prev == static_cast<unsigned>(A.race_ctas - 1);
         }
         __syncthreads();
         if (!last_cta) return;
         __threadfence();
-        const unsigned long long packed = atomicOr(&A.race[r].best, 0ull);
-        if (packed != ~0ull) {
-            token = static_cast<int32_t>(packed & 0xffffffffull);
-        } else {
-            // no positive residual weight: draw the correction from p (rare)
+
+        // chunk race over W (or over P when the residual has no mass)
+        bool use_p = !residual;
+        float wtot = 0.f;
+        for (int32_t cc = tid; cc < nc; cc += kRaceThreads) wtot += __ldcg(Wr + cc);
+        wtot = block_sum<kRaceThreads>(wtot, red_f);
+        if (residual && !(wtot > 0.f)) {
+            use_p = true;
             status |= SV_ST_RESIDUAL_ZERO;
-            float b2 = INFINITY;
-            int32_t x2 = INT32_MAX;
-            race_range<DT, DD>(A, trow, drow, 0, A.V, c, rs, false, key, static_cast<uint32_t>(n), kTagResidual,
-                               A.tbulk != 0, b2, x2);
-            float nb2 = x2 == INT32_MAX ? -INFINITY : -b2;
-            block_argmax<kRaceThreads>(nb2, x2, red_f, red_i);
-            token = x2 == INT32_MAX ? 0 : x2;
+        }
+        const float* Wsel = use_p ? Pr : Wr;
+        const PhiloxKey key = philox_key(A.seeds[r]);
+        const uint32_t tag_c = residual ? kTagResidualChunk : kTagBonusChunk;
+        const uint32_t tag_x = residual ? kTagResidual : kTagBonus;
+        float best = INFINITY;
+        int32_t bc = INT32_MAX;
+        for (int32_t cc = tid; cc < nc; cc += kRaceThreads) {
+            const float wc = __ldcg(Wsel + cc);
+            if (!(wc > 0.f)) continue;
+            const uint4 w4 = philox_block(key, static_cast<uint32_t>(cc >> 2), static_cast<uint32_t>(n), tag_c);
+            const uint32_t wd = (cc & 3) == 0 ? w4.x : ((cc & 3) == 1 ? w4.y : ((cc & 3) == 2 ? w4.z : w4.w));
+            const float kc = __fdiv_rn(-log1pf(-one_minus_uniform_from_word(wd)), wc);
+            if (kc < best) {  // ascending chunk ids: strict < keeps the lowest
+                best = kc;
+                bc = cc;
+            }
+        }
+        block_argmin_key(best, bc, red_f, red_i);
+        if (bc == INT32_MAX) {
+            token = 0;  // every weight 0 (p itself has no mass): cannot happen for a valid row
+        } else {
+            // element race inside chunk bc
+            const int32_t cx0 = bc * kRaceChunk, cx1 = min(A.V, cx0 + kRaceChunk);
+            const bool wq = residual && !use_p;
+            float ze[8], ye[8];
+            load8<DT>(trow, cx0 + tid * 8, cx1, vec_ok, ze);
+            if (wq && A.identity) load8<DD>(drow, cx0 + tid * 8, min(cx1, A.Vd), dvec_ok, ye);
+            __syncthreads();  // qs of the chunk sums is no longer read
+            if (wq && !A.identity) fill_q<DD>(A, drow, cx0, cx1 - cx0, c, rs.mq, invSq, qs);
+            __syncthreads();
+            float kb = INFINITY;
+            int32_t bx = INT32_MAX;
+            const int32_t xb = cx0 + tid * 8;
+            uint4 w4[2];
+            w4[0] = philox_block(key, static_cast<uint32_t>(xb >> 2), static_cast<uint32_t>(n), tag_x);
+            w4[1] = philox_block(key, static_cast<uint32_t>((xb >> 2) + 1), static_cast<uint32_t>(n), tag_x);
+            const uint32_t words[8] = {w4[0].x, w4[0].y, w4[0].z, w4[0].w, w4[1].x, w4[1].y, w4[1].z, w4[1].w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if (xb + e >= cx1) break;
+                float we = ex2(fmaf(ze[e], c, -rs.m)) * invS;
+                if (wq) {
+                    const float qe = A.identity ? ex2(fmaf(ye[e], c, -rs.mq)) * invSq : qs[tid * 8 + e];
+                    we = fmaxf(we - qe, 0.f);
+                }
+                if (!(we > 0.f)) continue;
+                const float ke = __fdiv_rn(-log1pf(-one_minus_uniform_from_word(words[e])), we);
+                if (ke < kb) {
+                    kb = ke;
+                    bx = xb + e;
+                }
+            }
+            block_argmin_key(kb, bx, red_f, red_i);
+            token = bx == INT32_MAX ? cx0 : bx;
         }
         if (residual && (rs.flags & kFlagOffSupport)) status |= SV_ST_OFF_SUPPORT;
     }
@@ -1595,7 +1609,7 @@ __global__ void __launch_bounds__(kRaceThreads) race_commit_kernel(SampleArgs A)
 namespace {
 
 struct PlanLayout {
-    int64_t header, bitmap, prefix, xs, js, pairs, chunk, x_of_j, total;
+    int64_t header, bitmap, prefix, xs, js, pairs, chunk, total;
 };
 
 PlanLayout plan_layout(int32_t V, int32_t Vd)
@@ -1615,7 +1629,6 @@ PlanLayout plan_layout(int32_t V, int32_t Vd)
     L.js = take(static_cast<int64_t>(Vd) * 4);
     L.pairs = take(static_cast<int64_t>(Vd) * 4);
     L.chunk = take((static_cast<int64_t>(V) / kChunkElems + 2) * 4);
-    L.x_of_j = take(static_cast<int64_t>(Vd) * 4);
     L.total = off;
     return L;
 }
@@ -1632,13 +1645,12 @@ D2tPlan plan_view(void* base, int32_t V, int32_t Vd)
     pl.js = reinterpret_cast<int32_t*>(b + L.js);
     pl.pairs = reinterpret_cast<uint32_t*>(b + L.pairs);
     pl.chunk = reinterpret_cast<int32_t*>(b + L.chunk);
-    pl.x_of_j = reinterpret_cast<int32_t*>(b + L.x_of_j);
     pl.nw = (V + 31) / 32;
     return pl;
 }
 
 struct SampleLayout {
-    int64_t plan, stats, race, gslots;
+    int64_t plan, stats, race, wsum, gslots;
     int64_t gslot_bytes;
     int64_t total;
     int smem_mode;
@@ -1658,6 +1670,7 @@ SampleLayout sample_layout(int64_t R, int32_t k, int32_t V, int32_t Vd, int et, 
     L.plan = take(own_plan ? plan_layout(V, Vd).total : 0);
     L.stats = take(R * (k + 1) * static_cast<int64_t>(sizeof(RowStat)));
     L.race = take(R * static_cast<int64_t>(sizeof(RaceSlot)));
+    L.wsum = take(R * 2 * static_cast<int64_t>((V + kRaceChunk - 1) / kRaceChunk) * 4);
     const int64_t units = R * (k + 1);
     L.grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(units, sms > 0 ? sms : 148)));
     const int64_t resident = align256(static_cast<int64_t>(Vd) * ed) + align256(static_cast<int64_t>(Vd) * et);
@@ -1670,16 +1683,18 @@ SampleLayout sample_layout(int64_t R, int32_t k, int32_t V, int32_t Vd, int et, 
     return L;
 }
 
-size_t fast_smem_bytes(int32_t Vd)
+size_t fast_smem_bytes(int32_t V, int32_t Vd)
 {
-    return static_cast<size_t>(kFastHeader + 2 * kFastWarps * static_cast<int64_t>(kFastStage) +
-                               align256(static_cast<int64_t>(Vd) * 2));
+    return static_cast<size_t>(kFastHeader + kFastWarps * kFastStages * static_cast<int64_t>(kFastStage) +
+                               align256(static_cast<int64_t>(Vd) * 2) +
+                               (static_cast<int64_t>(V + kChunkElems - 1) / kChunkElems + 1) * 4);
 }
 
 bool fast_path_ok(const Rows& t, const Rows& d, bool identity)
 {
     return !identity && t.dtype == SV_BF16 && d.dtype == SV_BF16 && t.bulk_ok && d.bulk_ok && d.data != nullptr &&
-           t.width % 8 == 0 && d.width % 8 == 0 && d.width <= kFastMaxVd && fast_smem_bytes(d.width) <= 227 * 1024;
+           t.width % 8 == 0 && d.width % 8 == 0 && d.width <= kFastMaxVd &&
+           fast_smem_bytes(t.width, d.width) <= 227 * 1024;
 }
 
 }  // namespace
@@ -1745,8 +1760,9 @@ static cudaError_t launch_sample_t(const Rows& t, const Rows& d, const int32_t* 
     A.gslots = ws + L.gslots;
     A.gslot_bytes = L.gslot_bytes;
     A.smem_mode = L.smem_mode;
-    A.race_seg = kRaceSeg;
-    A.race_ctas = (t.width + kRaceSeg - 1) / kRaceSeg;
+    A.wsum = reinterpret_cast<float*>(ws + L.wsum);
+    const int32_t race_chunks = (t.width + kRaceChunk - 1) / kRaceChunk;
+    A.race_ctas = (race_chunks + kRaceChunksPerCta - 1) / kRaceChunksPerCta;
 
     cudaError_t e;
     if (own_plan) {
@@ -1760,7 +1776,7 @@ static cudaError_t launch_sample_t(const Rows& t, const Rows& d, const int32_t* 
     cfg.attrs = attr;
     cfg.numAttrs = own_plan ? 1 : 0;
     if (fast_path_ok(t, d, identity)) {
-        const size_t smem = fast_smem_bytes(d.width);
+        const size_t smem = fast_smem_bytes(t.width, d.width);
         e = cudaFuncSetAttribute(sample_rows_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem));
         if (e != cudaSuccess) return e;
@@ -1785,7 +1801,7 @@ static cudaError_t launch_sample_t(const Rows& t, const Rows& d, const int32_t* 
     cfg2.stream = stream;
     cfg2.attrs = attr;
     cfg2.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg2, race_commit_kernel<DT, DD>, A);
+    return cudaLaunchKernelEx(&cfg2, race_chunks_kernel<DT, DD>, A);
 }
 
 cudaError_t launch_verify_sample(const Rows& target, const Rows& draft_logits, const int32_t* d2t,
