@@ -178,11 +178,16 @@ int sv_verify_greedy_noalloc(sv_rows target, int32_t R, int32_t k, int32_t branc
  * Definition: p_j = softmax(z_j / T), q_j = softmax(y_j / T) pushed through
  * d2t.  Position j is accepted when q_j(x_j) > 0 and u_j < p_j(x_j)/q_j(x_j)
  * with u_j the Philox uniform (counter (0, j, 0, 0), word 0).  n = leading
- * accepts.  n < k: the correction is argmin_{r_x > 0} E_x / r_x over
- * r = max(0, p_n - q_n), E_x = -ln u_x with u_x from counter
- * (x >> 2, n, 1, 0) word x & 3.  n == k: the bonus is argmin E_x / p_k(x)
- * with counter (x >> 2, k, 2, 0).  A uniform from word w is
+ * accepts.  n < k: the correction is drawn from r = max(0, p_n - q_n) (all
+ * of p_n if r has no mass, status bit 8); n == k: the bonus is drawn from
+ * p_k.  The draw is a two-level exponential race: ids are cut into chunks of
+ * 2048; the chunk c = argmin E_c / W_c over the chunk sums W_c of the
+ * weights, E_c = -ln u_c with u_c from counter (c >> 2, row, tag, 0) word
+ * c & 3 (tag 3 correction, 4 bonus); then the id = argmin E_x / w_x over
+ * that chunk, u_x from counter (x >> 2, row, tag, 0) word x & 3 (tag 1
+ * correction, 2 bonus); row is n (or k).  A uniform from word w is
  * (2 * (w >> 9) + 1) * 2^-24.
+ * Limits: V <= 819,200 (SV_ERR_LIMIT above).
  * ---------------------------------------------------------------------- */
 size_t sv_verify_sample_workspace(int32_t R, int32_t k, int32_t V, int32_t Vd);
 int sv_verify_sample(sv_rows target, sv_rows draft_logits, const int32_t* d2t,
@@ -208,7 +213,7 @@ int sv_verify_sample(sv_rows target, sv_rows draft_logits, const int32_t* d2t,
  *               until d2t changes.  A plan whose (V, Vd) differ from the
  *               call's, or a d2t with ids out of range or repeated, makes
  *               sv_verify_sample report SV_ST_BAD_D2T.
- * Limits: V <= 819,200 with a d2t map.
+ * Limits: V <= 819,200.
  * ---------------------------------------------------------------------- */
 size_t sv_d2t_plan_bytes(int32_t V, int32_t Vd);
 int sv_d2t_plan_build(const int32_t* d2t, int32_t Vd, int32_t V, void* plan, size_t plan_bytes,

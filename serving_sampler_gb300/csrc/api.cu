@@ -141,7 +141,7 @@ int sv_verify_sample(sv_rows target, sv_rows draft_logits, const int32_t* d2t, c
     }
     const bool mapped = d2t != nullptr || d2t_plan != nullptr;
     if (!mapped && d.width != t.width) return SV_ERR_SHAPE;
-    if (mapped && t.width > sample_max_plan_width()) return SV_ERR_LIMIT;
+    if (t.width > sample_max_plan_width()) return SV_ERR_LIMIT;  // the race keeps one sum per 2048 ids
     if (int rc = check_workspace(workspace, workspace_bytes,
                                  sample_workspace_bytes(R, k, t.width, d.width)))
         return rc;

@@ -16,12 +16,12 @@
 //                      positions (G[pos]).  A second pass over G and Y gives
 //                      TV over the full vocabulary, p(x_j), q(x_j) and the
 //                      accept test u_j < p/q.
-//   race_chunks_kernel RC CTAs per request: the accept-length scan, then
-//                      the chunk sums of the weights on the one selected row
+//   race_rows_kernel   one CTA per request: the accept-length scan, the
+//                      chunk sums of the weights on the one selected row
 //                      (residual max(0, p - q) at the first rejection, or p
-//                      at the bonus row); the last CTA of the request draws
-//                      the chunk and then the id by exponential races with
-//                      Philox uniforms, and commits the tokens.
+//                      at the bonus row), then the chunk and the id drawn by
+//                      exponential races with Philox uniforms; it commits
+//                      the tokens.
 // Temperature scaling works in log2 units: with c = log2(e) / T,
 // p(x) = 2^(z_x c - M) / S where M = max_x z_x c and S = sum 2^(z c - M).
 #include <algorithm>
@@ -42,8 +42,8 @@ constexpr uint32_t kStageBytes = 16384;
 constexpr int kStages = 4;
 constexpr int kRowHeader = 128;
 constexpr uint32_t kSmemBudget = 220 * 1024;
-constexpr int kRaceThreads = 256;
 constexpr int32_t kMaxPlanWords = 25600;  // d2t mode supports V <= 819,200
+constexpr int32_t kMaxPlanChunks = kMaxPlanWords * 32 / kChunkElems;
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum : uint32_t { kFlagAllNegInf = 8u, kFlagDraftBad = 16u, kFlagOffSupport = 32u };
@@ -53,8 +53,12 @@ struct D2tPlan {
     int32_t* prefix;   // [nw + 1] set bits before each word
     int32_t* xs;       // [Vd] support target ids, ascending
     int32_t* js;       // [Vd] the draft id of xs[pos]
-    uint32_t* pairs;   // [Vd] (draft id << 16) | (xs & (kChunkElems - 1)), ascending xs (Vd <= 65535)
+    uint32_t* pairs;   // per chunk of kChunkElems target ids, from pbase[c]: its support entries
+                       // (draft id << 16) | (x & (kChunkElems - 1)) in ascending x, padded to a
+                       // multiple of 4 with (Vd << 16) (a spare slot of the scatter target)
     int32_t* chunk;    // [V / kChunkElems + 2] support rank at every multiple of kChunkElems
+    int32_t* pbase;    // [V / kChunkElems + 2] start of every chunk's entries in pairs
+    uint16_t* jmap;    // [V] draft id of every target id, 0xFFFF off the support
     int32_t* header;   // [0] V, [1] Vd the plan was built for, [2] d2t out of range or repeated
     int32_t nw;
 };
@@ -67,11 +71,6 @@ struct RowStat {
     int32_t amax;     // raw argmax of the target row
     uint32_t flags;   // kFlag* of the target and draft rows
     int32_t accept;   // accept decision of position j
-};
-
-struct RaceSlot {
-    unsigned int count;  // race CTAs of the request done
-    unsigned int pad;
 };
 
 struct SampleArgs {
@@ -95,12 +94,11 @@ struct SampleArgs {
     int32_t* tokens;
     int32_t* status;
     RowStat* stats;
-    RaceSlot* race;
+    float2* cstat;       // [units][target chunks] (max of z c, sum 2^(z c - max)) per chunk, or NULL
+    int32_t nct;         // target chunks per row
     char* gslots;        // global-memory Y / G buffers when they do not fit in shared memory
     int64_t gslot_bytes;
     int smem_mode;
-    float* wsum;         // [R][2][chunks] chunk sums of the raced row: W_c, then P_c
-    int32_t race_ctas;   // CTAs per request in the race
 };
 
 __host__ __device__ inline int64_t align256(int64_t b) { return (b + 255) / 256 * 256; }
@@ -256,6 +254,8 @@ __global__ void __launch_bounds__(kPlanThreads)
     int32_t* pref = reinterpret_cast<int32_t*>(plan_smem + pl.nw);
     __shared__ int32_t warp_tot[kPlanThreads / 32];
     __shared__ int bad_any;
+    __shared__ int32_t crank[kMaxPlanChunks + 1];  // support rank at every chunk start
+    __shared__ int32_t cbase[kMaxPlanChunks + 1];  // padded start of every chunk's entries
     const int tid = threadIdx.x;
     pdl_launch_dependents();  // the row kernel streams rows while the plan is built
     if (tid == 0) bad_any = 0;
@@ -272,6 +272,7 @@ __global__ void __launch_bounds__(kPlanThreads)
         if (atomicOr(&bits[x >> 5], bit) & bit) bad = 1;
     }
     if (bad) atomicOr(&bad_any, 1);
+    for (int32_t x = tid; x < V; x += kPlanThreads) pl.jmap[x] = 0xFFFFu;
     __syncthreads();
     // exclusive prefix of popcounts, each thread owning a contiguous block of words
     const int32_t per = (pl.nw + kPlanThreads - 1) / kPlanThreads;
@@ -300,10 +301,29 @@ __global__ void __launch_bounds__(kPlanThreads)
         pl.bitmap[w] = bits[w];
         pl.prefix[w] = pref[w];
     }
-    for (int32_t c = tid; c <= (V + kChunkElems - 1) / kChunkElems; c += kPlanThreads) {
+    const int32_t nch = (V + kChunkElems - 1) / kChunkElems;
+    for (int32_t c = tid; c <= nch; c += kPlanThreads) {
         const int32_t x = min(V, c * kChunkElems);
         const int32_t w = x >> 5, b = x & 31;
-        pl.chunk[c] = pref[w] + (b ? __popc(bits[w] & ((1u << b) - 1u)) : 0);
+        const int32_t rk = pref[w] + (b ? __popc(bits[w] & ((1u << b) - 1u)) : 0);
+        pl.chunk[c] = rk;
+        crank[c] = rk;
+    }
+    __syncthreads();
+    if (tid == 0) {  // padded starts: every chunk's entries begin on a 16-byte boundary
+        int32_t run = 0;
+        for (int32_t c = 0; c < nch; ++c) {
+            cbase[c] = run;
+            run += (crank[c + 1] - crank[c] + 3) & ~3;
+        }
+        cbase[nch] = run;
+    }
+    __syncthreads();
+    for (int32_t c = tid; c <= nch; c += kPlanThreads) {
+        pl.pbase[c] = cbase[c];
+        if (c < nch)  // the padding slots of chunk c
+            for (int32_t i = cbase[c] + crank[c + 1] - crank[c]; i < cbase[c + 1]; ++i)
+                pl.pairs[i] = static_cast<uint32_t>(Vd) << 16;
     }
     if (tid == 0) {
         pl.prefix[pl.nw] = pref[pl.nw];
@@ -316,10 +336,13 @@ __global__ void __launch_bounds__(kPlanThreads)
         if (x < 0 || x >= V) continue;
         const int32_t w = x >> 5, b = x & 31;
         const int32_t pos = pref[w] + (b ? __popc(bits[w] & ((1u << b) - 1u)) : 0);
+        pl.jmap[x] = static_cast<uint16_t>(j);
         if (pos >= 0 && pos < Vd) {
             pl.xs[pos] = x;
             pl.js[pos] = j;
-            pl.pairs[pos] = (static_cast<uint32_t>(j) << 16) | static_cast<uint32_t>(x & (kChunkElems - 1));
+            const int32_t c = x / kChunkElems;
+            pl.pairs[cbase[c] + pos - crank[c]] =
+                (static_cast<uint32_t>(j) << 16) | static_cast<uint32_t>(x & (kChunkElems - 1));
         }
     }
 }
@@ -398,9 +421,6 @@ __global__ void __launch_bounds__(kRowThreads, 1) sample_rows_kernel(SampleArgs 
         const char* drow = has_draft ? A.dbase + (static_cast<int64_t>(r) * A.k + j) * A.dstride : nullptr;
         const int32_t xj = has_draft ? A.draft[static_cast<int64_t>(r) * A.k + j] : -1;
 
-        if (j == 0 && tid == 0) {
-            A.race[r].count = 0u;
-        }
         // chunk list: draft bulk chunks, then target bulk chunks
         const uint32_t dbulk = has_draft && A.dbulk ? (static_cast<uint32_t>(A.Vd) * ED) & ~15u : 0u;
         const uint32_t tbulk = A.tbulk ? (static_cast<uint32_t>(A.V) * ET) & ~15u : 0u;
@@ -813,6 +833,14 @@ __device__ __forceinline__ float exp_sum8(uint4 q, unsigned long long c2, unsign
     return lo + hi;
 }
 
+// maximum over the warp (all lanes take part; no NaN among the inputs)
+__device__ __forceinline__ float warp_max(float v)
+{
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
 // 16-byte read-only global load
 __device__ __forceinline__ uint4 ld_nc_v4(const uint4* p)
 {
@@ -936,7 +964,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // [warp][stage]
     unsigned char* ring = smem + kFastHeader;
     uint16_t* G = reinterpret_cast<uint16_t*>(ring + kFastWarps * kFastStages * kFastStage);
-    int32_t* ctab = reinterpret_cast<int32_t*>(reinterpret_cast<unsigned char*>(G) + align256(A.Vd * 2));
+    int32_t* ctab = reinterpret_cast<int32_t*>(reinterpret_cast<unsigned char*>(G) + align256((A.Vd + 8) * 2));
     __shared__ float zx_shared;
     __shared__ int32_t jdx_shared;  // draft id of the draft token (-1: off the support)
     __shared__ float qx_shared;     // q at that draft id
@@ -956,7 +984,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
     // a plan for other sizes, or built from a d2t with repeated / out-of-range ids, is not
     // trusted for shared-memory indexing (the race kernel reports SV_ST_BAD_D2T)
     const bool plan_ok = A.plan.header[0] == A.V && A.plan.header[1] == A.Vd && A.plan.header[2] == 0;
-    for (int32_t c = tid; c <= nchunks_t; c += kFastThreads) ctab[c] = plan_ok ? A.plan.chunk[c] : 0;
+    for (int32_t c = tid; c <= nchunks_t; c += kFastThreads) ctab[c] = plan_ok ? A.plan.pbase[c] : 0;
     __syncthreads();
     const uint64_t pol_t = l2_policy_evict_first();
     uint64_t pol_d;
@@ -984,7 +1012,6 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
         const unsigned long long c2 = pack2(c, c);
         const int32_t xj = u.has_draft ? A.draft[static_cast<int64_t>(u.r) * A.k + u.j] : -1;
         const int32_t nw_chunks = warp_chunks(u.n, w);
-        if (u.j == 0 && tid == 0) A.race[u.r].count = 0u;
         if (tid == 0) {
             zx_shared = NAN;
             jdx_shared = -1;
@@ -1009,16 +1036,17 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
             // support entries of a target chunk: this lane's groups of four packed pairs, from
             // L2 while the maxima and exponentials below run
             const bool scatter = !is_draft && u.has_draft;
-            int32_t p0 = 0, p1 = 0, p0a = 0;
+            float csum = 0.f;  // this lane's share of the chunk's sum, relative to its running max
+            int32_t p0 = 0, p1 = 0;
             uint4 pg[kPairRegs];
             if (scatter) {
-                p0 = ctab[cidx];
+                p0 = ctab[cidx];  // a multiple of 4: the chunk's entries padded to whole groups
                 p1 = ctab[cidx + 1];
-                p0a = p0 & ~3;
 #pragma unroll
                 for (int t = 0; t < kPairRegs; ++t) {
-                    const int32_t g = p0a + 4 * (lane + 32 * t);
-                    pg[t] = g < p1 ? ld_nc_v4(reinterpret_cast<const uint4*>(A.plan.pairs + g)) : make_uint4(0, 0, 0, 0);
+                    const int32_t g = p0 + 4 * (lane + 32 * t);
+                    pg[t] = g < p1 ? ld_nc_v4(reinterpret_cast<const uint4*>(A.plan.pairs + g))
+                                   : make_uint4(0u, 0u, 0u, 0u);
                 }
             }
 #pragma unroll
@@ -1027,45 +1055,49 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                 // running max, then the independent exps
                 constexpr int kH = kVL / 2;
                 uint4 qv[kH];
-                float vmx[kH];
-                bool nan_seen = false;
 #pragma unroll
                 for (int e = 0; e < kH; ++e) {
                     const int v = lane + 32 * (h * kH + e);
                     qv[e] = v < nv ? vp[v] : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
-                    const uint32_t m2 = bmax2_nan(bmax2_nan(qv[e].x, qv[e].y), bmax2_nan(qv[e].z, qv[e].w));
-                    vmx[e] = fmax_nan(bf16_lo(m2), bf16_hi(m2));
-                    nan_seen |= vmx[e] != vmx[e];
                 }
-                if (nan_seen) {  // rare: NaN logits read as -inf
+                // one packed NaN-propagating max tree over the half, widened once
+                uint32_t m2 = bmax2_nan(bmax2_nan(qv[0].x, qv[0].y), bmax2_nan(qv[0].z, qv[0].w));
+#pragma unroll
+                for (int e = 1; e < kH; ++e)
+                    m2 = bmax2_nan(m2, bmax2_nan(bmax2_nan(qv[e].x, qv[e].y), bmax2_nan(qv[e].z, qv[e].w)));
+                float lm = fmax_nan(bf16_lo(m2), bf16_hi(m2));
+                if (lm != lm) {  // rare: NaN logits read as -inf
                     (is_draft ? dflags : tflags) |= kFlagNaN;
+                    lm = -INFINITY;
 #pragma unroll
                     for (int e = 0; e < kH; ++e) {
                         qv[e] = make_uint4(bf16x2_nan_to_ninf(qv[e].x), bf16x2_nan_to_ninf(qv[e].y),
                                            bf16x2_nan_to_ninf(qv[e].z), bf16x2_nan_to_ninf(qv[e].w));
                         const uint32_t m3 = bmax2_nan(bmax2_nan(qv[e].x, qv[e].y), bmax2_nan(qv[e].z, qv[e].w));
-                        vmx[e] = fmaxf(bf16_lo(m3), bf16_hi(m3));
+                        lm = fmaxf(lm, fmaxf(bf16_lo(m3), bf16_hi(m3)));
                     }
                 }
-                float lm = vmx[0];
-#pragma unroll
-                for (int e = 1; e < kH; ++e) lm = fmaxf(lm, vmx[e]);
                 if (!is_draft) {
                     if (lm > bv) {  // rare after the first chunks: the first vector holding the new max
 #pragma unroll
-                        for (int e = kH - 1; e >= 0; --e)
-                            if (vmx[e] == lm) bx = x0 + (lane + 32 * (h * kH + e)) * 8;
+                        for (int e = kH - 1; e >= 0; --e) {
+                            const uint32_t m3 = bmax2_nan(bmax2_nan(qv[e].x, qv[e].y), bmax2_nan(qv[e].z, qv[e].w));
+                            if (fmaxf(bf16_lo(m3), bf16_hi(m3)) == lm) bx = x0 + (lane + 32 * (h * kH + e)) * 8;
+                        }
                         bv = lm;
                     }
                 } else if (lm == INFINITY) {
                     dflags |= kFlagPosInf;
                 }
                 if (is_draft || u.sampling) {
+                    // one running max per warp (the lanes' sums share its reference)
                     float& rm = is_draft ? dm : tm;
                     float& rs_ = is_draft ? ds : ts;
-                    const float mt = lm * c;
+                    const float mt = warp_max(lm) * c;
                     if (mt > rm) {
-                        rs_ = rm == -INFINITY ? 0.f : rs_ * ex2(rm - mt);
+                        const float sc = rm == -INFINITY ? 0.f : ex2(rm - mt);
+                        rs_ *= sc;
+                        csum *= sc;
                         rm = mt;
                     }
                     if (rm > -INFINITY) {
@@ -1076,32 +1108,47 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
 #pragma unroll
                         for (int e = 1; e < kH; ++e) acc[0] += acc[e];
                         rs_ += acc[0];
+                        csum += acc[0];
                     }
                 }
             }
+            if (!is_draft && u.sampling) {
+                // this chunk's (reference max, sum) for the race
+                float cs = csum;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) cs += __shfl_xor_sync(0xffffffffu, cs, o);
+                if (lane == 0) A.cstat[unit * A.nct + cidx] = make_float2(tm, cs);
+            }
             if (scatter) {
-                // G[draft id] = z at the chunk offset, for the entries [p0, p1) of the plan
+                // G[draft id] = z at the chunk offset for every entry of the lane's groups; a
+                // padding entry writes the spare slot G[Vd], which nothing reads
                 const uint16_t* zs = reinterpret_cast<const uint16_t*>(st);
                 const bool here = xj >= x0 && xj < x0 + static_cast<int32_t>(nb / 2);
 #pragma unroll
                 for (int t = 0; t < kPairRegs; ++t) {
-                    const int32_t g = p0a + 4 * (lane + 32 * t);
                     const uint32_t pe[4] = {pg[t].x, pg[t].y, pg[t].z, pg[t].w};
+                    uint16_t zv[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        if (g + e >= p0 && g + e < p1) G[pe[e] >> 16] = zs[pe[e] & (kChunkElems - 1)];
+                    for (int e = 0; e < 4; ++e) zv[e] = zs[pe[e] & (kChunkElems - 1)];
+                    if (p0 + 4 * (lane + 32 * t) < p1) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) G[pe[e] >> 16] = zv[e];
+                    }
                 }
-                // entries beyond this lane's register groups (chunks denser than 512 entries)
-                for (int32_t g = p0a + 4 * 32 * kPairRegs + lane; g < p1; g += 32) {
-                    const uint32_t pe = A.plan.pairs[g];
-                    if (g >= p0) G[pe >> 16] = zs[pe & (kChunkElems - 1)];
+                // groups beyond this lane's registers (chunks denser than 512 entries)
+                for (int32_t g = p0 + 4 * 32 * kPairRegs + 4 * lane; g < p1; g += 4 * 32) {
+                    const uint4 q4 = ld_nc_v4(reinterpret_cast<const uint4*>(A.plan.pairs + g));
+                    const uint32_t pe[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) G[pe[e] >> 16] = zs[pe[e] & (kChunkElems - 1)];
                 }
                 if (here) {  // the draft token: its logit and its draft id
                     const uint32_t xoff = static_cast<uint32_t>(xj - x0);
                     if (lane == 0) zx_shared = __uint_as_float(static_cast<uint32_t>(zs[xoff]) << 16);
                     for (int32_t g = p0 + lane; g < p1; g += 32) {
                         const uint32_t pe = A.plan.pairs[g];
-                        if ((pe & (kChunkElems - 1)) == xoff) jdx_shared = static_cast<int32_t>(pe >> 16);
+                        if ((pe & (kChunkElems - 1)) == xoff && static_cast<int32_t>(pe >> 16) < A.Vd)
+                            jdx_shared = static_cast<int32_t>(pe >> 16);
                     }
                 }
             }
@@ -1112,6 +1159,18 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
             producer_step(A, P, consumed, w, lane, units, wst, wbar, pol_t, pol_d);
         }
         T = T_next;
+
+        // the first batch of draft-row loads of the TV pass, in flight during the reductions
+        constexpr int kTvIter = (kFastMaxVd / 8 + kFastThreads - 1) / kFastThreads;
+        constexpr int kTvBatch = (kTvIter + 1) / 2;  // draft-row loads in flight per thread
+        const int32_t nv8 = u.has_draft ? A.Vd / 8 : 0;  // Vd % 8 == 0 on this path
+        const uint4* yv = reinterpret_cast<const uint4*>(u.drow);
+        uint4 yq0[kTvBatch];
+#pragma unroll
+        for (int i = 0; i < kTvBatch; ++i) {
+            const int32_t v = tid + i * kFastThreads;
+            if (v < nv8) yq0[i] = ld_nc_v4(yv + v);
+        }
 
         // ---- reductions: two exchanges through shared memory ----
         const float my_bv = bv, my_tm = tm, my_ts = ts, my_dm = dm, my_ds = ds;
@@ -1199,11 +1258,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
             const unsigned long long c2m = pack2(c, c), nM = pack2(-M, -M), nMq = pack2(-Mq, -Mq);
             const unsigned long long iS = pack2(invS, invS), iSq = pack2(invSq, invSq);
             const int32_t jdx = jdx_shared;
-            const int32_t nv8 = A.Vd / 8;  // Vd % 8 == 0 on this path
-            const uint4* yv = reinterpret_cast<const uint4*>(u.drow);
             const uint4* gv = reinterpret_cast<const uint4*>(G);
-            constexpr int kTvIter = (kFastMaxVd / 8 + kFastThreads - 1) / kFastThreads;
-            constexpr int kTvBatch = (kTvIter + 1) / 2;  // draft-row loads in flight per thread
             float a = 0.f;
 #pragma unroll
             for (int b0 = 0; b0 < kTvIter; b0 += kTvBatch) {
@@ -1211,7 +1266,8 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
 #pragma unroll
                 for (int i = 0; i < kTvBatch; ++i) {
                     const int32_t v = tid + (b0 + i) * kFastThreads;
-                    if (b0 + i < kTvIter && v < nv8) yq[i] = ld_nc_v4(yv + v);
+                    if (b0 == 0) yq[i] = yq0[i];
+                    else if (b0 + i < kTvIter && v < nv8) yq[i] = ld_nc_v4(yv + v);
                 }
 #pragma unroll
                 for (int i = 0; i < kTvBatch; ++i) {
@@ -1308,15 +1364,22 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
 // counted by the id).  P(chunk) = W_c / sum W and P(id | chunk) = w / W_c, so
 // the draw is exact, and only one chunk's uniforms are ever generated.
 //
-// race_chunks_kernel: RC CTAs per request, each summing kRaceChunksPerCta
-// chunks of the selected row (W_c and the p sums P_c); the last CTA of the
-// request runs both races and commits the tokens.
+// race_rows_kernel: one CTA per request.  The accept-length scan, one pass over
+// the selected row that sums w and p per chunk (each warp's vectors lie in one
+// chunk; q of a support id through the plan's draft-id map from the L1-resident
+// draft row), the chunk race, the element race inside the drawn chunk, commit.
 namespace {
 
 constexpr int32_t kRaceChunk = 2048;
-constexpr int kRaceChunksPerCta = 4;
-constexpr int kRaceIdsPerThread = kRaceChunk / kRaceThreads;  // 8
-static_assert(kRaceIdsPerThread == 8, "one 8-id vector per thread and chunk");
+constexpr int kRaceRowThreads = 1024;
+constexpr int kRaceWarps = kRaceRowThreads / 32;
+constexpr int kRaceInFlight = 4;  // 8-id vectors per thread loaded together
+constexpr int kRaceMaxChunks = kMaxPlanWords * 32 / kRaceChunk;  // V <= 819,200
+constexpr int kWarpsPerChunk = kRaceChunk / 8 / 32;              // 8
+constexpr int kEvalChunks = 8;  // chunks summed together by the bounded chunk race
+constexpr int kEvalVecs = kRaceChunk / 8 / (kRaceRowThreads / kEvalChunks);  // 8-id vectors per thread
+static_assert(kRaceChunk == kChunkElems, "the row pass leaves one (max, sum) per race chunk");
+static_assert(kRaceChunk % (8 * 32) == 0, "a warp's 32 vectors lie in one chunk");
 
 // z[0..8) of ids [x, x + 8) of a row (-inf at and beyond x_end; NaN read as -inf)
 template <int DT>
@@ -1324,7 +1387,7 @@ __device__ __forceinline__ void load8(const char* row, int32_t x, int32_t x_end,
 {
     if (vec_ok && x + 8 <= x_end) {
         if constexpr (DT == SV_BF16) {
-            const uint4 v = *reinterpret_cast<const uint4*>(row + static_cast<int64_t>(x) * 2);
+            const uint4 v = ld_nc_v4(reinterpret_cast<const uint4*>(row + static_cast<int64_t>(x) * 2));
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -1332,10 +1395,12 @@ __device__ __forceinline__ void load8(const char* row, int32_t x, int32_t x_end,
                 z[2 * e + 1] = bf16_hi(w[e]);
             }
         } else {
-            const float4 a = *reinterpret_cast<const float4*>(row + static_cast<int64_t>(x) * 4);
-            const float4 b = *reinterpret_cast<const float4*>(row + static_cast<int64_t>(x) * 4 + 16);
-            z[0] = a.x; z[1] = a.y; z[2] = a.z; z[3] = a.w;
-            z[4] = b.x; z[5] = b.y; z[6] = b.z; z[7] = b.w;
+            const uint4 a = ld_nc_v4(reinterpret_cast<const uint4*>(row + static_cast<int64_t>(x) * 4));
+            const uint4 b = ld_nc_v4(reinterpret_cast<const uint4*>(row + static_cast<int64_t>(x) * 4 + 16));
+            z[0] = __uint_as_float(a.x); z[1] = __uint_as_float(a.y);
+            z[2] = __uint_as_float(a.z); z[3] = __uint_as_float(a.w);
+            z[4] = __uint_as_float(b.x); z[5] = __uint_as_float(b.y);
+            z[6] = __uint_as_float(b.z); z[7] = __uint_as_float(b.w);
         }
     } else {
 #pragma unroll
@@ -1345,23 +1410,38 @@ __device__ __forceinline__ void load8(const char* row, int32_t x, int32_t x_end,
     for (int e = 0; e < 8; ++e) z[e] = z[e] != z[e] ? -INFINITY : z[e];
 }
 
-// q over target ids [x0, x0 + n) into qs[0..n): 0 off the support.  Every
-// thread of the block takes part; the caller synchronises before reading qs.
-template <int DD>
-__device__ __forceinline__ void fill_q(const SampleArgs& A, const char* drow, int32_t x0, int32_t n, float c,
-                                       float mq, float invSq, float* qs)
+// the draft ids of target ids [x, x + 8) (0xFFFF: off the support or beyond V)
+__device__ __forceinline__ void load_jmap8(const D2tPlan& pl, int32_t x, int32_t V, uint32_t* jm)
 {
-    for (int32_t i = threadIdx.x; i < n; i += kRaceThreads) qs[i] = 0.f;
-    __syncthreads();
-    const int32_t p0 = support_rank(A.plan, x0), p1 = support_rank(A.plan, x0 + n);
-#pragma unroll 4
-    for (int32_t p = p0 + static_cast<int32_t>(threadIdx.x); p < p1; p += kRaceThreads) {
-        const int32_t x = A.plan.xs[p], jd = A.plan.js[p];
-        if (x < x0 || x >= x0 + n || jd < 0 || jd >= A.Vd) continue;
-        float y = ld_elem<DD>(drow, jd);
-        y = y != y ? -INFINITY : y;
-        qs[x - x0] = ex2(fmaf(y, c, -mq)) * invSq;
+    if (x + 8 <= V) {
+        const uint4 v = ld_nc_v4(reinterpret_cast<const uint4*>(pl.jmap + x));
+        jm[0] = v.x & 0xFFFFu; jm[1] = v.x >> 16; jm[2] = v.y & 0xFFFFu; jm[3] = v.y >> 16;
+        jm[4] = v.z & 0xFFFFu; jm[5] = v.z >> 16; jm[6] = v.w & 0xFFFFu; jm[7] = v.w >> 16;
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) jm[e] = x + e < V ? pl.jmap[x + e] : 0xFFFFu;
     }
+}
+
+// q at target ids [x, x + 8): 2^(y c - mq) / Sq at the draft id of each, 0 off the support
+template <int DD>
+__device__ __forceinline__ void q8(const SampleArgs& A, const char* drow, int32_t x, int32_t x_end, bool dvec_ok,
+                                   float c, float mq, float invSq, float* q)
+{
+    float y[8];
+    if (A.identity) {
+        load8<DD>(drow, x, min(x_end, A.Vd), dvec_ok, y);
+    } else {
+        uint32_t jm[8];
+        load_jmap8(A.plan, x, A.V, jm);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float v = jm[e] < static_cast<uint32_t>(A.Vd) ? ld_elem<DD>(drow, jm[e]) : -INFINITY;
+            y[e] = v != v ? -INFINITY : v;
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) q[e] = ex2(fmaf(y[e], c, -mq)) * invSq;
 }
 
 // (key, id) minimum over the block, lowest id among equal keys; threads
@@ -1369,32 +1449,36 @@ __device__ __forceinline__ void fill_q(const SampleArgs& A, const char* drow, in
 __device__ __forceinline__ void block_argmin_key(float& key, int32_t& id, float* sf, int32_t* si)
 {
     float nk = id == INT32_MAX ? -INFINITY : -key;
-    block_argmax<kRaceThreads>(nk, id, sf, si);
+    block_argmax<kRaceRowThreads>(nk, id, sf, si);
     key = -nk;
 }
 
 }  // namespace
 
 template <int DT, int DD>
-__global__ void __launch_bounds__(kRaceThreads) race_chunks_kernel(SampleArgs A)
+__global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArgs A)
 {
     pdl_wait_primary();
-    __shared__ float qs[kRaceChunksPerCta * kRaceChunk];
-    __shared__ float red_f[kRaceThreads / 32];
-    __shared__ int32_t red_i[kRaceThreads / 32];
-    __shared__ float part[kRaceThreads / 32][2 * kRaceChunksPerCta];
-    __shared__ int last_cta;
+    __shared__ float wpart[kRaceMaxChunks][kWarpsPerChunk];  // per chunk, per warp: sum of w
+    __shared__ float ppart[kRaceMaxChunks][kWarpsPerChunk];  // and of p
+    __shared__ float lb_s[kRaceMaxChunks];    // lower bounds of the chunk keys
+    __shared__ float ec_s[kRaceMaxChunks];    // E_c of every chunk
+    __shared__ int32_t order_s[kRaceMaxChunks];
+    __shared__ float bpart_s[kRaceWarps];
+    __shared__ float best_s;
+    __shared__ int32_t bc_s;
+    __shared__ float red_f[kRaceWarps];
+    __shared__ int32_t red_i[kRaceWarps];
     __shared__ int32_t n_shared;
     __shared__ uint32_t fl_shared;
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const int32_t r = static_cast<int32_t>(blockIdx.x / A.race_ctas);
-    const int32_t rc = static_cast<int32_t>(blockIdx.x - static_cast<int64_t>(r) * A.race_ctas);
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int32_t r = static_cast<int32_t>(blockIdx.x);
     const int32_t k = A.k;
     const RowStat* st = A.stats + static_cast<int64_t>(r) * (k + 1);
     const int32_t* d = A.draft + static_cast<int64_t>(r) * k;
     const float T = A.temp[r];
 
-    // request-level decisions (warp 0, ballots), identical in every CTA of the request
+    // request-level decisions (warp 0, ballots)
     if (tid < 32) {
         uint32_t fl = 0;
         for (int32_t j = lane; j <= k; j += 32) fl |= st[j].flags;
@@ -1424,7 +1508,6 @@ __global__ void __launch_bounds__(kRaceThreads) race_chunks_kernel(SampleArgs A)
     int32_t token = -1;
     uint32_t status = 0;
     if (greedy) {
-        if (rc != 0) return;
         token = st[n].amax;
     } else {
         const bool residual = n < k;
@@ -1432,102 +1515,128 @@ __global__ void __launch_bounds__(kRaceThreads) race_chunks_kernel(SampleArgs A)
         const float c = kLog2e / T, invS = 1.f / rs.s, invSq = residual ? 1.f / rs.sq : 0.f;
         const char* trow = A.tbase + (static_cast<int64_t>(r) * (k + 1) + n) * A.tstride;
         const char* drow = residual ? A.dbase + (static_cast<int64_t>(r) * k + n) * A.dstride : nullptr;
-        const bool vec_ok = A.tbulk != 0;
-        const bool dvec_ok = A.dbulk != 0;
+        const bool vec_ok = A.tbulk != 0, dvec_ok = A.dbulk != 0;
         const int32_t nc = (A.V + kRaceChunk - 1) / kRaceChunk;
-        float* Wr = A.wsum + static_cast<int64_t>(r) * 2 * nc;  // [W_0..W_nc) then [P_0..P_nc)
-        float* Pr = Wr + nc;
+        const int32_t nvec = (A.V + 7) / 8;
 
-        // ---- chunk sums of this CTA's chunks ----
-        const int32_t c0 = rc * kRaceChunksPerCta;
-        const int32_t ncta = min(kRaceChunksPerCta, nc - c0);
-        const int32_t x0 = c0 * kRaceChunk, x1 = min(A.V, (c0 + ncta) * kRaceChunk);
-        float z[kRaceChunksPerCta][8];
-#pragma unroll
-        for (int i = 0; i < kRaceChunksPerCta; ++i) {
-            const int32_t x = x0 + i * kRaceChunk + tid * 8;
-            if (i < ncta) load8<DT>(trow, x, x1, vec_ok, z[i]);
-        }
-        float y[kRaceChunksPerCta][8];
-        if (residual && A.identity) {
-#pragma unroll
-            for (int i = 0; i < kRaceChunksPerCta; ++i) {
-                const int32_t x = x0 + i * kRaceChunk + tid * 8;
-                if (i < ncta) load8<DD>(drow, x, min(x1, A.Vd), dvec_ok, y[i]);
-            }
-        } else if (residual) {
-            fill_q<DD>(A, drow, x0, x1 - x0, c, rs.mq, invSq, qs);
-        }
-        __syncthreads();
-        float wsum[kRaceChunksPerCta], psum[kRaceChunksPerCta];
-#pragma unroll
-        for (int i = 0; i < kRaceChunksPerCta; ++i) {
-            wsum[i] = 0.f;
-            psum[i] = 0.f;
-            if (i >= ncta) continue;
-            const int32_t xi = x0 + i * kRaceChunk + tid * 8;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                if (xi + e >= x1) break;  // beyond the row: qs holds nothing there
-                const float pe = ex2(fmaf(z[i][e], c, -rs.m)) * invS;
-                float we = pe;
-                if (residual) {
-                    const float qe = A.identity ? ex2(fmaf(y[i][e], c, -rs.mq)) * invSq
-                                                : qs[i * kRaceChunk + tid * 8 + e];
-                    we = fmaxf(pe - qe, 0.f);
-                }
-                psum[i] += pe;
-                wsum[i] += we;
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < kRaceChunksPerCta; ++i) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                wsum[i] += __shfl_xor_sync(0xffffffffu, wsum[i], o);
-                psum[i] += __shfl_xor_sync(0xffffffffu, psum[i], o);
-            }
-            if (lane == 0) {
-                part[wid][2 * i] = wsum[i];
-                part[wid][2 * i + 1] = psum[i];
-            }
-        }
-        __syncthreads();
-        if (tid < 2 * ncta) {
-            float t = 0.f;
-            for (int w = 0; w < kRaceThreads / 32; ++w) t += part[w][tid];
-            const int32_t cc = c0 + (tid >> 1);
-            if (tid & 1) Pr[cc] = t;
-            else Wr[cc] = t;
-        }
-        // ---- the last CTA of the request runs the races ----
-        __syncthreads();
-        if (tid == 0) {
-            __threadfence();
-            const unsigned prev = atomicAdd(&A.race[r].count, 1u);
-            last_cta = prev == static_cast<unsigned>(A.race_ctas - 1);
-        }
-        __syncthreads();
-        if (!last_cta) return;
-        __threadfence();
-
-        // chunk race over W (or over P when the residual has no mass)
+        const PhiloxKey key = philox_key(A.seeds[r]);
+        const uint32_t tag_c = residual ? kTagResidualChunk : kTagBonusChunk;
+        const uint32_t tag_x = residual ? kTagResidual : kTagBonus;
         bool use_p = !residual;
+        int32_t bc = INT32_MAX;
+        if (A.cstat == nullptr) {
+        // ---- chunk sums of w and p: each warp's 32 vectors lie in one chunk ----
+        constexpr int kZW = DT == SV_BF16 ? 1 : 2;  // 16-byte words per 8-id vector
+        // the trip count is uniform across each warp (it depends on the warp's first vector),
+        // so every lane takes part in the shuffles below
+        for (int32_t v0 = tid; v0 - lane < nvec; v0 += kRaceRowThreads * kRaceInFlight) {
+            // raw target words and draft-id words of every vector first, all in flight together
+            uint4 zr[kRaceInFlight][kZW];
+            uint4 jr[kRaceInFlight];
+#pragma unroll
+            for (int b = 0; b < kRaceInFlight; ++b) {
+                const int32_t x = (v0 + b * kRaceRowThreads) * 8;
+                if (vec_ok && x + 8 <= A.V && x >= 0) {
+#pragma unroll
+                    for (int h = 0; h < kZW; ++h)
+                        zr[b][h] = ld_nc_v4(reinterpret_cast<const uint4*>(trow + static_cast<int64_t>(x) * (2 * kZW)) + h);
+                }
+                if (residual && !A.identity && x + 8 <= A.V)
+                    jr[b] = ld_nc_v4(reinterpret_cast<const uint4*>(A.plan.jmap + x));
+            }
+#pragma unroll
+            for (int b = 0; b < kRaceInFlight; ++b) {
+                const int32_t v = v0 + b * kRaceRowThreads;
+                const int32_t vw = v - lane;  // the warp's first vector
+                if (vw >= nvec) break;
+                float ws = 0.f, ps = 0.f;
+                if (v < nvec) {
+                    const int32_t x = v * 8;
+                    float z[8];
+                    if (vec_ok && x + 8 <= A.V) {
+                        if constexpr (DT == SV_BF16) {
+                            const uint32_t wv[4] = {zr[b][0].x, zr[b][0].y, zr[b][0].z, zr[b][0].w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                z[2 * e] = bf16_lo(wv[e]);
+                                z[2 * e + 1] = bf16_hi(wv[e]);
+                            }
+                        } else {
+                            const uint32_t wv[8] = {zr[b][0].x, zr[b][0].y, zr[b][0].z, zr[b][0].w,
+                                                    zr[b][1].x, zr[b][1].y, zr[b][1].z, zr[b][1].w};
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) z[e] = __uint_as_float(wv[e]);
+                        }
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) z[e] = z[e] != z[e] ? -INFINITY : z[e];
+                    } else {
+                        load8<DT>(trow, x, A.V, false, z);
+                    }
+                    float q[8];
+                    if (residual) {
+                        if (A.identity) {
+                            q8<DD>(A, drow, x, A.V, dvec_ok, c, rs.mq, invSq, q);
+                        } else {
+                            uint32_t jm[8];
+                            if (x + 8 <= A.V) {
+                                jm[0] = jr[b].x & 0xFFFFu; jm[1] = jr[b].x >> 16;
+                                jm[2] = jr[b].y & 0xFFFFu; jm[3] = jr[b].y >> 16;
+                                jm[4] = jr[b].z & 0xFFFFu; jm[5] = jr[b].z >> 16;
+                                jm[6] = jr[b].w & 0xFFFFu; jm[7] = jr[b].w >> 16;
+                            } else {
+                                load_jmap8(A.plan, x, A.V, jm);
+                            }
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                float yv = jm[e] < static_cast<uint32_t>(A.Vd) ? ld_elem<DD>(drow, jm[e]) : -INFINITY;
+                                yv = yv != yv ? -INFINITY : yv;
+                                q[e] = ex2(fmaf(yv, c, -rs.mq)) * invSq;
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float pe = x + e < A.V ? ex2(fmaf(z[e], c, -rs.m)) * invS : 0.f;
+                        ps += pe;
+                        ws += residual ? fmaxf(pe - q[e], 0.f) : pe;
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    ws += __shfl_xor_sync(0xffffffffu, ws, o);
+                    ps += __shfl_xor_sync(0xffffffffu, ps, o);
+                }
+                if (lane == 0) {
+                    const int32_t cc = vw * 8 / kRaceChunk;
+                    const int32_t slot = (vw * 8 / 256) % kWarpsPerChunk;
+                    wpart[cc][slot] = ws;
+                    ppart[cc][slot] = ps;
+                }
+            }
+        }
+        __syncthreads();
+        // chunk sums in a fixed order; slots past the row's end hold nothing
         float wtot = 0.f;
-        for (int32_t cc = tid; cc < nc; cc += kRaceThreads) wtot += __ldcg(Wr + cc);
-        wtot = block_sum<kRaceThreads>(wtot, red_f);
+        for (int32_t cc = tid; cc < nc; cc += kRaceRowThreads) {
+            const int32_t nslots = min(kWarpsPerChunk, (min(A.V, (cc + 1) * kRaceChunk) - cc * kRaceChunk + 255) / 256);
+            float wc = 0.f, pc = 0.f;
+            for (int i = 0; i < nslots; ++i) {
+                wc += wpart[cc][i];
+                pc += ppart[cc][i];
+            }
+            wpart[cc][0] = wc;
+            ppart[cc][0] = pc;
+            wtot += wc;
+        }
+        wtot = block_sum<kRaceRowThreads>(wtot, red_f);
         if (residual && !(wtot > 0.f)) {
             use_p = true;
             status |= SV_ST_RESIDUAL_ZERO;
         }
-        const float* Wsel = use_p ? Pr : Wr;
-        const PhiloxKey key = philox_key(A.seeds[r]);
-        const uint32_t tag_c = residual ? kTagResidualChunk : kTagBonusChunk;
-        const uint32_t tag_x = residual ? kTagResidual : kTagBonus;
+        // ---- chunk race ----
         float best = INFINITY;
-        int32_t bc = INT32_MAX;
-        for (int32_t cc = tid; cc < nc; cc += kRaceThreads) {
-            const float wc = __ldcg(Wsel + cc);
+        for (int32_t cc = tid; cc < nc; cc += kRaceRowThreads) {
+            const float wc = use_p ? ppart[cc][0] : wpart[cc][0];
             if (!(wc > 0.f)) continue;
             const uint4 w4 = philox_block(key, static_cast<uint32_t>(cc >> 2), static_cast<uint32_t>(n), tag_c);
             const uint32_t wd = (cc & 3) == 0 ? w4.x : ((cc & 3) == 1 ? w4.y : ((cc & 3) == 2 ? w4.z : w4.w));
@@ -1538,38 +1647,131 @@ __global__ void __launch_bounds__(kRaceThreads) race_chunks_kernel(SampleArgs A)
             }
         }
         block_argmin_key(best, bc, red_f, red_i);
-        if (bc == INT32_MAX) {
-            token = 0;  // every weight 0 (p itself has no mass): cannot happen for a valid row
         } else {
-            // element race inside chunk bc
+            // ---- chunk race with bounds: the row pass left p's sum over every chunk, which
+            // bounds the chunk's weight sum W_c, so E_c / P_c bounds its key from below.
+            // Chunks are summed exactly in the order of these bounds, a batch at a time,
+            // until the next bound exceeds the best exact key. ----
+            const float2* cst = A.cstat + (static_cast<int64_t>(r) * (k + 1) + n) * A.nct;
+            for (int32_t cc = tid; cc < nc; cc += kRaceRowThreads) {
+                const float2 v = cst[cc];
+                const float pc = v.y > 0.f ? v.y * ex2(v.x - rs.m) * invS : 0.f;
+                const uint4 w4 = philox_block(key, static_cast<uint32_t>(cc >> 2), static_cast<uint32_t>(n), tag_c);
+                const uint32_t wd = (cc & 3) == 0 ? w4.x : ((cc & 3) == 1 ? w4.y : ((cc & 3) == 2 ? w4.z : w4.w));
+                const float e = -log1pf(-one_minus_uniform_from_word(wd));
+                ec_s[cc] = e;
+                // the row pass rounds differently from the sums below: widen the bound by 1e-4
+                lb_s[cc] = pc > 0.f ? __fdiv_rn(e, pc * 1.0001f) : INFINITY;
+            }
+            __syncthreads();
+            for (int32_t cc = tid; cc < nc; cc += kRaceRowThreads) {
+                const float l = lb_s[cc];
+                int32_t rk = 0;
+                for (int32_t o = 0; o < nc; ++o) {
+                    const float lo = lb_s[o];
+                    rk += (lo < l || (lo == l && o < cc)) ? 1 : 0;
+                }
+                order_s[rk] = cc;
+            }
+            for (int pass = 0; pass < (residual ? 2 : 1); ++pass) {
+                const bool wp = !residual || pass == 1;  // weights p (bonus, or no residual mass)
+                if (tid == 0) {
+                    best_s = INFINITY;
+                    bc_s = INT32_MAX;
+                }
+                __syncthreads();
+                for (int32_t r0 = 0; r0 < nc; r0 += kEvalChunks) {
+                    if (lb_s[order_s[r0]] > best_s) break;  // block-uniform: read after a barrier
+                    const int slot = tid / (kRaceRowThreads / kEvalChunks);
+                    const int sub = tid % (kRaceRowThreads / kEvalChunks);
+                    float ws = 0.f;
+                    if (r0 + slot < nc) {
+                        const int32_t cc = order_s[r0 + slot];
+                        const int32_t cx1 = min(A.V, (cc + 1) * kRaceChunk);
+#pragma unroll
+                        for (int hv = 0; hv < kEvalVecs; ++hv) {
+                            const int32_t x = cc * kRaceChunk + 8 * (kEvalVecs * sub + hv);
+                            float z[8], q[8];
+                            load8<DT>(trow, x, cx1, vec_ok, z);
+                            if (!wp) q8<DD>(A, drow, x, cx1, dvec_ok, c, rs.mq, invSq, q);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                if (x + e >= cx1) break;
+                                const float pe = ex2(fmaf(z[e], c, -rs.m)) * invS;
+                                ws += wp ? pe : fmaxf(pe - q[e], 0.f);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+                    if (lane == 0) bpart_s[tid >> 5] = ws;
+                    __syncthreads();
+                    if (tid == 0) {
+                        constexpr int kWarpsPerSlot = kRaceWarps / kEvalChunks;
+                        for (int sl = 0; sl < kEvalChunks && r0 + sl < nc; ++sl) {
+                            const int32_t cc = order_s[r0 + sl];
+                            float wc = 0.f;
+                            for (int i = 0; i < kWarpsPerSlot; ++i) wc += bpart_s[sl * kWarpsPerSlot + i];
+                            if (!(wc > 0.f)) continue;
+                            const float kc = __fdiv_rn(ec_s[cc], wc);
+                            if (kc < best_s || (kc == best_s && cc < bc_s)) {
+                                best_s = kc;
+                                bc_s = cc;
+                            }
+                        }
+                    }
+                    __syncthreads();
+                }
+                if (bc_s != INT32_MAX) {
+                    use_p = wp;
+                    break;
+                }
+                if (residual && pass == 0) status |= SV_ST_RESIDUAL_ZERO;
+            }
+            bc = bc_s;
+        }
+        if (bc == INT32_MAX) {
+            token = 0;  // no weight anywhere: cannot happen for a row that is not flagged
+        } else {
+            // ---- element race inside chunk bc: four ids (one Philox block) per thread ----
             const int32_t cx0 = bc * kRaceChunk, cx1 = min(A.V, cx0 + kRaceChunk);
             const bool wq = residual && !use_p;
-            float ze[8], ye[8];
-            load8<DT>(trow, cx0 + tid * 8, cx1, vec_ok, ze);
-            if (wq && A.identity) load8<DD>(drow, cx0 + tid * 8, min(cx1, A.Vd), dvec_ok, ye);
-            __syncthreads();  // qs of the chunk sums is no longer read
-            if (wq && !A.identity) fill_q<DD>(A, drow, cx0, cx1 - cx0, c, rs.mq, invSq, qs);
-            __syncthreads();
             float kb = INFINITY;
             int32_t bx = INT32_MAX;
-            const int32_t xb = cx0 + tid * 8;
-            uint4 w4[2];
-            w4[0] = philox_block(key, static_cast<uint32_t>(xb >> 2), static_cast<uint32_t>(n), tag_x);
-            w4[1] = philox_block(key, static_cast<uint32_t>((xb >> 2) + 1), static_cast<uint32_t>(n), tag_x);
-            const uint32_t words[8] = {w4[0].x, w4[0].y, w4[0].z, w4[0].w, w4[1].x, w4[1].y, w4[1].z, w4[1].w};
+            const int32_t xb = cx0 + 4 * tid;
+            if (tid < kRaceChunk / 4 && xb < cx1) {
+                float ze[4], qe[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                if (xb + e >= cx1) break;
-                float we = ex2(fmaf(ze[e], c, -rs.m)) * invS;
-                if (wq) {
-                    const float qe = A.identity ? ex2(fmaf(ye[e], c, -rs.mq)) * invSq : qs[tid * 8 + e];
-                    we = fmaxf(we - qe, 0.f);
+                for (int e = 0; e < 4; ++e) {
+                    const float v = xb + e < cx1 ? ld_elem<DT>(trow, xb + e) : -INFINITY;
+                    ze[e] = v != v ? -INFINITY : v;
                 }
-                if (!(we > 0.f)) continue;
-                const float ke = __fdiv_rn(-log1pf(-one_minus_uniform_from_word(words[e])), we);
-                if (ke < kb) {
-                    kb = ke;
-                    bx = xb + e;
+                if (wq) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int32_t x = xb + e;
+                        int32_t jd = -1;
+                        if (x < cx1) jd = A.identity ? x : (A.plan.jmap[x] == 0xFFFFu ? -1 : A.plan.jmap[x]);
+                        if (jd >= 0 && jd < A.Vd) {
+                            float y = ld_elem<DD>(drow, jd);
+                            y = y != y ? -INFINITY : y;
+                            qe[e] = ex2(fmaf(y, c, -rs.mq)) * invSq;
+                        }
+                    }
+                }
+                const uint4 w4 = philox_block(key, static_cast<uint32_t>(xb >> 2), static_cast<uint32_t>(n), tag_x);
+                const uint32_t words[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (xb + e >= cx1) break;
+                    float we = ex2(fmaf(ze[e], c, -rs.m)) * invS;
+                    if (wq) we = fmaxf(we - qe[e], 0.f);
+                    if (!(we > 0.f)) continue;
+                    const float ke = __fdiv_rn(-log1pf(-one_minus_uniform_from_word(words[e])), we);
+                    if (ke < kb) {
+                        kb = ke;
+                        bx = xb + e;
+                    }
                 }
             }
             block_argmin_key(kb, bx, red_f, red_i);
@@ -1577,8 +1779,8 @@ __global__ void __launch_bounds__(kRaceThreads) race_chunks_kernel(SampleArgs A)
         }
         if (residual && (rs.flags & kFlagOffSupport)) status |= SV_ST_OFF_SUPPORT;
     }
-    // ---- commit (one CTA per request) ------------------------------------
-    for (int32_t j = tid; j < k; j += kRaceThreads)
+    // ---- commit ------------------------------------------------------------
+    for (int32_t j = tid; j < k; j += kRaceRowThreads)
         if (d[j] < 0 || d[j] >= A.V) status |= SV_ST_TOKEN_RANGE;
     if (fl & kFlagTimeout) status |= SV_ST_TIMEOUT;
     if (bad_rows) status |= SV_ST_BAD_LOGITS;
@@ -1586,17 +1788,17 @@ __global__ void __launch_bounds__(kRaceThreads) race_chunks_kernel(SampleArgs A)
     if (!A.identity && (A.plan.header[2] != 0 || A.plan.header[0] != A.V || A.plan.header[1] != A.Vd))
         status |= SV_ST_BAD_D2T;
     int32_t* out = A.tokens + static_cast<int64_t>(r) * (k + 1);
-    for (int32_t j = tid; j <= k; j += kRaceThreads) out[j] = j < n ? d[j] : (j == n ? token : -1);
+    for (int32_t j = tid; j <= k; j += kRaceRowThreads) out[j] = j < n ? d[j] : (j == n ? token : -1);
     if (greedy) {
         // no sampling statistics for greedily verified requests
-        for (int32_t j = tid; j < k; j += kRaceThreads) {
+        for (int32_t j = tid; j < k; j += kRaceRowThreads) {
             const int64_t o = static_cast<int64_t>(r) * k + j;
             if (A.tv) A.tv[o] = NAN;
             if (A.pd) A.pd[o] = NAN;
             if (A.qd) A.qd[o] = NAN;
         }
     }
-    status = block_or<kRaceThreads>(status, reinterpret_cast<uint32_t*>(red_i));
+    status = block_or<kRaceRowThreads>(status, reinterpret_cast<uint32_t*>(red_i));
     if (tid == 0) {
         A.accept_len[r] = n;
         if (A.status) A.status[r] = static_cast<int32_t>(status);
@@ -1609,7 +1811,7 @@ __global__ void __launch_bounds__(kRaceThreads) race_chunks_kernel(SampleArgs A)
 namespace {
 
 struct PlanLayout {
-    int64_t header, bitmap, prefix, xs, js, pairs, chunk, total;
+    int64_t header, bitmap, prefix, xs, js, pairs, chunk, pbase, jmap, total;
 };
 
 PlanLayout plan_layout(int32_t V, int32_t Vd)
@@ -1627,8 +1829,10 @@ PlanLayout plan_layout(int32_t V, int32_t Vd)
     L.prefix = take((nw + 1) * 4);
     L.xs = take(static_cast<int64_t>(Vd) * 4);
     L.js = take(static_cast<int64_t>(Vd) * 4);
-    L.pairs = take(static_cast<int64_t>(Vd) * 4);
+    L.pairs = take((static_cast<int64_t>(Vd) + 4 * (static_cast<int64_t>(V) / kChunkElems + 2)) * 4);
     L.chunk = take((static_cast<int64_t>(V) / kChunkElems + 2) * 4);
+    L.pbase = take((static_cast<int64_t>(V) / kChunkElems + 2) * 4);
+    L.jmap = take((static_cast<int64_t>(V) + 8) * 2);
     L.total = off;
     return L;
 }
@@ -1645,12 +1849,14 @@ D2tPlan plan_view(void* base, int32_t V, int32_t Vd)
     pl.js = reinterpret_cast<int32_t*>(b + L.js);
     pl.pairs = reinterpret_cast<uint32_t*>(b + L.pairs);
     pl.chunk = reinterpret_cast<int32_t*>(b + L.chunk);
+    pl.pbase = reinterpret_cast<int32_t*>(b + L.pbase);
+    pl.jmap = reinterpret_cast<uint16_t*>(b + L.jmap);
     pl.nw = (V + 31) / 32;
     return pl;
 }
 
 struct SampleLayout {
-    int64_t plan, stats, race, wsum, gslots;
+    int64_t plan, stats, cstat, gslots;
     int64_t gslot_bytes;
     int64_t total;
     int smem_mode;
@@ -1669,8 +1875,7 @@ SampleLayout sample_layout(int64_t R, int32_t k, int32_t V, int32_t Vd, int et, 
     };
     L.plan = take(own_plan ? plan_layout(V, Vd).total : 0);
     L.stats = take(R * (k + 1) * static_cast<int64_t>(sizeof(RowStat)));
-    L.race = take(R * static_cast<int64_t>(sizeof(RaceSlot)));
-    L.wsum = take(R * 2 * static_cast<int64_t>((V + kRaceChunk - 1) / kRaceChunk) * 4);
+    L.cstat = take(R * (k + 1) * ((static_cast<int64_t>(V) + kChunkElems - 1) / kChunkElems) * 8);
     const int64_t units = R * (k + 1);
     L.grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(units, sms > 0 ? sms : 148)));
     const int64_t resident = align256(static_cast<int64_t>(Vd) * ed) + align256(static_cast<int64_t>(Vd) * et);
@@ -1686,7 +1891,7 @@ SampleLayout sample_layout(int64_t R, int32_t k, int32_t V, int32_t Vd, int et, 
 size_t fast_smem_bytes(int32_t V, int32_t Vd)
 {
     return static_cast<size_t>(kFastHeader + kFastWarps * kFastStages * static_cast<int64_t>(kFastStage) +
-                               align256(static_cast<int64_t>(Vd) * 2) +
+                               align256((static_cast<int64_t>(Vd) + 8) * 2) +
                                (static_cast<int64_t>(V + kChunkElems - 1) / kChunkElems + 1) * 4);
 }
 
@@ -1756,13 +1961,13 @@ static cudaError_t launch_sample_t(const Rows& t, const Rows& d, const int32_t* 
     A.tokens = tokens;
     A.status = status;
     A.stats = reinterpret_cast<RowStat*>(ws + L.stats);
-    A.race = reinterpret_cast<RaceSlot*>(ws + L.race);
+    const bool fast = fast_path_ok(t, d, identity);
+    A.cstat = fast ? reinterpret_cast<float2*>(ws + L.cstat) : nullptr;  // the fast row pass leaves chunk sums
+    A.nct = (t.width + kChunkElems - 1) / kChunkElems;
     A.gslots = ws + L.gslots;
     A.gslot_bytes = L.gslot_bytes;
     A.smem_mode = L.smem_mode;
-    A.wsum = reinterpret_cast<float*>(ws + L.wsum);
-    const int32_t race_chunks = (t.width + kRaceChunk - 1) / kRaceChunk;
-    A.race_ctas = (race_chunks + kRaceChunksPerCta - 1) / kRaceChunksPerCta;
+
 
     cudaError_t e;
     if (own_plan) {
@@ -1775,7 +1980,7 @@ static cudaError_t launch_sample_t(const Rows& t, const Rows& d, const int32_t* 
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = own_plan ? 1 : 0;
-    if (fast_path_ok(t, d, identity)) {
+    if (fast) {
         const size_t smem = fast_smem_bytes(t.width, d.width);
         e = cudaFuncSetAttribute(sample_rows_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem));
@@ -1795,13 +2000,13 @@ static cudaError_t launch_sample_t(const Rows& t, const Rows& d, const int32_t* 
     }
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg2 = {};
-    cfg2.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(R) * A.race_ctas));
-    cfg2.blockDim = dim3(kRaceThreads);
+    cfg2.gridDim = dim3(static_cast<unsigned>(R));
+    cfg2.blockDim = dim3(kRaceRowThreads);
     cfg2.dynamicSmemBytes = 0;
     cfg2.stream = stream;
     cfg2.attrs = attr;
     cfg2.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg2, race_chunks_kernel<DT, DD>, A);
+    return cudaLaunchKernelEx(&cfg2, race_rows_kernel<DT, DD>, A);
 }
 
 cudaError_t launch_verify_sample(const Rows& target, const Rows& draft_logits, const int32_t* d2t,
