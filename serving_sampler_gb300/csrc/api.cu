@@ -122,6 +122,7 @@ int sv_verify_sample(sv_rows target, sv_rows draft_logits, const int32_t* d2t, c
 {
     if (R < 0 || k < 0) return SV_ERR_INVALID_ARG;
     if (k > SV_MAX_K) return SV_ERR_LIMIT;
+    if (static_cast<int64_t>(R) * (k + 1) > INT32_MAX) return SV_ERR_LIMIT;
     if (R == 0) return SV_OK;
     if ((k > 0 && draft == nullptr) || seeds == nullptr || temperature == nullptr ||
         accept_len == nullptr || tokens == nullptr)

@@ -849,6 +849,17 @@ __device__ __forceinline__ uint4 ld_nc_v4(const uint4* p)
     return v;
 }
 
+// this lane's register groups of a chunk's padded support entries [p0, p1)
+__device__ __forceinline__ void load_pairs(const SampleArgs& A, int32_t p0, int32_t p1, int lane, uint4* pg)
+{
+#pragma unroll
+    for (int t = 0; t < kPairRegs; ++t) {
+        const int32_t g = p0 + 4 * (lane + 32 * t);
+        pg[t] = g < p1 ? ld_nc_v4(reinterpret_cast<const uint4*>(A.plan.pairs + g)) : make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+
 // order this thread's generic-proxy accesses to shared memory before later
 // bulk copies (async proxy) into the same bytes
 __device__ __forceinline__ void fence_proxy_async_smem()
@@ -866,10 +877,11 @@ __device__ __forceinline__ uint32_t bf16x2_nan_to_ninf(uint32_t w)
 }
 
 struct WarpRec {
-    float bv;
-    int32_t bx;
+    float bv;      // max of the target logits
+    int32_t bx;    // its first id
     uint32_t tfl, dfl;
-    float tm, dm;
+    float tm, dm;  // reference maxima (log2 units) of the target and draft sums
+    float ts, ds;  // the sums
 };
 
 struct FastUnit {
@@ -883,8 +895,9 @@ struct FastUnit {
 __device__ __forceinline__ FastUnit fast_unit(const SampleArgs& A, int64_t unit, float T)
 {
     FastUnit u;
-    u.r = static_cast<int32_t>(unit / (A.k + 1));
-    u.j = static_cast<int32_t>(unit - static_cast<int64_t>(u.r) * (A.k + 1));
+    const int32_t un = static_cast<int32_t>(unit);  // R * (k + 1) < 2^31 (checked by the caller)
+    u.r = un / (A.k + 1);
+    u.j = un - u.r * (A.k + 1);
     u.sampling = T > 0.f;
     u.has_draft = u.sampling && u.j < A.k;
     u.trow = A.tbase + unit * A.tstride;
@@ -902,7 +915,7 @@ __device__ __forceinline__ int32_t warp_chunks(int32_t n, int w)
 
 __device__ __forceinline__ float unit_temp(const SampleArgs& A, int64_t unit)
 {
-    return A.temp[unit / (A.k + 1)];
+    return A.temp[static_cast<int32_t>(unit) / (A.k + 1)];
 }
 
 // issue sequence element q of unit u into `stage` (lane 0 only)
@@ -969,7 +982,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
     __shared__ int32_t jdx_shared;  // draft id of the draft token (-1: off the support)
     __shared__ float qx_shared;     // q at that draft id
     __shared__ WarpRec wrec[kFastWarps];
-    __shared__ float wsum[kFastWarps][2];
+    __shared__ WarpRec merged;
     __shared__ float wtv[kFastWarps];
     __shared__ int32_t amax_shared;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -1021,6 +1034,8 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
         float dm = -INFINITY, ds = 0.f, tm = -INFINITY, ts = 0.f, bv = -INFINITY;
         int32_t bx = INT32_MAX;
         uint32_t dflags = 0, tflags = 0;
+        uint4 pg[kPairRegs];  // support entries of the target chunk pg_for (-1: none)
+        int32_t pg_for = -1;
         for (int32_t i = 0; i < nw_chunks; ++i) {
             const uint32_t sidx = consumed % kFastStages;
             if (!timeout && !mbar_wait_bounded(&wbar[sidx], (consumed / kFastStages) & 1u)) timeout = 1;
@@ -1038,86 +1053,10 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
             const bool scatter = !is_draft && u.has_draft;
             float csum = 0.f;  // this lane's share of the chunk's sum, relative to its running max
             int32_t p0 = 0, p1 = 0;
-            uint4 pg[kPairRegs];
             if (scatter) {
                 p0 = ctab[cidx];  // a multiple of 4: the chunk's entries padded to whole groups
                 p1 = ctab[cidx + 1];
-#pragma unroll
-                for (int t = 0; t < kPairRegs; ++t) {
-                    const int32_t g = p0 + 4 * (lane + 32 * t);
-                    pg[t] = g < p1 ? ld_nc_v4(reinterpret_cast<const uint4*>(A.plan.pairs + g))
-                                   : make_uint4(0u, 0u, 0u, 0u);
-                }
-            }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                // half the lane's vectors: independent loads and max trees, one update of the
-                // running max, then the independent exps
-                constexpr int kH = kVL / 2;
-                uint4 qv[kH];
-#pragma unroll
-                for (int e = 0; e < kH; ++e) {
-                    const int v = lane + 32 * (h * kH + e);
-                    qv[e] = v < nv ? vp[v] : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
-                }
-                // one packed NaN-propagating max tree over the half, widened once
-                uint32_t m2 = bmax2_nan(bmax2_nan(qv[0].x, qv[0].y), bmax2_nan(qv[0].z, qv[0].w));
-#pragma unroll
-                for (int e = 1; e < kH; ++e)
-                    m2 = bmax2_nan(m2, bmax2_nan(bmax2_nan(qv[e].x, qv[e].y), bmax2_nan(qv[e].z, qv[e].w)));
-                float lm = fmax_nan(bf16_lo(m2), bf16_hi(m2));
-                if (lm != lm) {  // rare: NaN logits read as -inf
-                    (is_draft ? dflags : tflags) |= kFlagNaN;
-                    lm = -INFINITY;
-#pragma unroll
-                    for (int e = 0; e < kH; ++e) {
-                        qv[e] = make_uint4(bf16x2_nan_to_ninf(qv[e].x), bf16x2_nan_to_ninf(qv[e].y),
-                                           bf16x2_nan_to_ninf(qv[e].z), bf16x2_nan_to_ninf(qv[e].w));
-                        const uint32_t m3 = bmax2_nan(bmax2_nan(qv[e].x, qv[e].y), bmax2_nan(qv[e].z, qv[e].w));
-                        lm = fmaxf(lm, fmaxf(bf16_lo(m3), bf16_hi(m3)));
-                    }
-                }
-                if (!is_draft) {
-                    if (lm > bv) {  // rare after the first chunks: the first vector holding the new max
-#pragma unroll
-                        for (int e = kH - 1; e >= 0; --e) {
-                            const uint32_t m3 = bmax2_nan(bmax2_nan(qv[e].x, qv[e].y), bmax2_nan(qv[e].z, qv[e].w));
-                            if (fmaxf(bf16_lo(m3), bf16_hi(m3)) == lm) bx = x0 + (lane + 32 * (h * kH + e)) * 8;
-                        }
-                        bv = lm;
-                    }
-                } else if (lm == INFINITY) {
-                    dflags |= kFlagPosInf;
-                }
-                if (is_draft || u.sampling) {
-                    // one running max per warp (the lanes' sums share its reference)
-                    float& rm = is_draft ? dm : tm;
-                    float& rs_ = is_draft ? ds : ts;
-                    const float mt = warp_max(lm) * c;
-                    if (mt > rm) {
-                        const float sc = rm == -INFINITY ? 0.f : ex2(rm - mt);
-                        rs_ *= sc;
-                        csum *= sc;
-                        rm = mt;
-                    }
-                    if (rm > -INFINITY) {
-                        const unsigned long long nm2 = pack2(-rm, -rm);
-                        float acc[kH];
-#pragma unroll
-                        for (int e = 0; e < kH; ++e) acc[e] = exp_sum8(qv[e], c2, nm2);
-#pragma unroll
-                        for (int e = 1; e < kH; ++e) acc[0] += acc[e];
-                        rs_ += acc[0];
-                        csum += acc[0];
-                    }
-                }
-            }
-            if (!is_draft && u.sampling) {
-                // this chunk's (reference max, sum) for the race
-                float cs = csum;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) cs += __shfl_xor_sync(0xffffffffu, cs, o);
-                if (lane == 0) A.cstat[unit * A.nct + cidx] = make_float2(tm, cs);
+                if (pg_for != cidx) load_pairs(A, p0, p1, lane, pg);  // not prefetched
             }
             if (scatter) {
                 // G[draft id] = z at the chunk offset for every entry of the lane's groups; a
@@ -1152,6 +1091,101 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                     }
                 }
             }
+            {
+                // the support entries of this warp's next chunk, if it is a target chunk of this
+                // unit: in flight during this chunk's maxima and exponentials
+                const int32_t qn = q + kFastWarps;
+                pg_for = -1;
+                if (u.has_draft && qn < u.n && qn >= u.nd) {
+                    pg_for = qn - u.nd;
+                    load_pairs(A, ctab[pg_for], ctab[pg_for + 1], lane, pg);
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                // half the lane's vectors: independent loads and max trees, one update of the
+                // running max, then the independent exps
+                constexpr int kH = kVL / 2;
+                uint4 qv[kH];
+#pragma unroll
+                for (int e = 0; e < kH; ++e) {
+                    const int v = lane + 32 * (h * kH + e);
+                    qv[e] = v < nv ? vp[v] : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+                }
+                // one packed NaN-propagating max tree over the half, widened once
+                uint32_t m2 = bmax2_nan(bmax2_nan(qv[0].x, qv[0].y), bmax2_nan(qv[0].z, qv[0].w));
+#pragma unroll
+                for (int e = 1; e < kH; ++e)
+                    m2 = bmax2_nan(m2, bmax2_nan(bmax2_nan(qv[e].x, qv[e].y), bmax2_nan(qv[e].z, qv[e].w)));
+                float lm = fmax_nan(bf16_lo(m2), bf16_hi(m2));
+                if (lm != lm) {  // rare: NaN logits read as -inf
+                    (is_draft ? dflags : tflags) |= kFlagNaN;
+                    lm = -INFINITY;
+#pragma unroll
+                    for (int e = 0; e < kH; ++e) {
+                        qv[e] = make_uint4(bf16x2_nan_to_ninf(qv[e].x), bf16x2_nan_to_ninf(qv[e].y),
+                                           bf16x2_nan_to_ninf(qv[e].z), bf16x2_nan_to_ninf(qv[e].w));
+                        const uint32_t m3 = bmax2_nan(bmax2_nan(qv[e].x, qv[e].y), bmax2_nan(qv[e].z, qv[e].w));
+                        lm = fmaxf(lm, fmaxf(bf16_lo(m3), bf16_hi(m3)));
+                    }
+                }
+                const float wm = warp_max(lm);
+                if (!is_draft) {
+                    if (wm > bv) {  // warp-uniform, rare after the first chunks: the first vector
+                                    // (lowest e, then lowest lane) holding the new maximum
+#pragma unroll
+                        for (int e = 0; e < kH; ++e) {
+                            const uint32_t m3 = bmax2_nan(bmax2_nan(qv[e].x, qv[e].y), bmax2_nan(qv[e].z, qv[e].w));
+                            const unsigned hit = __ballot_sync(0xffffffffu, fmaxf(bf16_lo(m3), bf16_hi(m3)) == wm);
+                            if (hit) {
+                                const int src = __ffs(hit) - 1;
+                                const uint32_t wv[4] = {qv[e].x, qv[e].y, qv[e].z, qv[e].w};
+                                int first = 7;
+#pragma unroll
+                                for (int t = 7; t >= 0; --t) {
+                                    const float zt = (t & 1) ? bf16_hi(wv[t >> 1]) : bf16_lo(wv[t >> 1]);
+                                    if (zt == wm) first = t;
+                                }
+                                first = __shfl_sync(0xffffffffu, first, src);
+                                bx = x0 + (src + 32 * (h * kH + e)) * 8 + first;
+                                break;
+                            }
+                        }
+                        bv = wm;
+                    }
+                } else if (wm == INFINITY) {
+                    dflags |= kFlagPosInf;
+                }
+                if (is_draft || u.sampling) {
+                    // one running max per warp (the lanes' sums share its reference)
+                    float& rm = is_draft ? dm : tm;
+                    float& rs_ = is_draft ? ds : ts;
+                    const float mt = wm * c;
+                    if (mt > rm) {
+                        const float sc = rm == -INFINITY ? 0.f : ex2(rm - mt);
+                        rs_ *= sc;
+                        csum *= sc;
+                        rm = mt;
+                    }
+                    if (rm > -INFINITY) {
+                        const unsigned long long nm2 = pack2(-rm, -rm);
+                        float acc[kH];
+#pragma unroll
+                        for (int e = 0; e < kH; ++e) acc[e] = exp_sum8(qv[e], c2, nm2);
+#pragma unroll
+                        for (int e = 1; e < kH; ++e) acc[0] += acc[e];
+                        rs_ += acc[0];
+                        csum += acc[0];
+                    }
+                }
+            }
+            if (!is_draft && u.sampling) {
+                // this chunk's (reference max, sum) for the race
+                float cs = csum;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) cs += __shfl_xor_sync(0xffffffffu, cs, o);
+                if (lane == 0) A.cstat[unit * A.nct + cidx] = make_float2(tm, cs);
+            }
             // the stage is read: refill it with this warp's next chunk
             __syncwarp();
             ++consumed;
@@ -1172,73 +1206,54 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
             if (v < nv8) yq0[i] = ld_nc_v4(yv + v);
         }
 
-        // ---- reductions: two exchanges through shared memory ----
-        const float my_bv = bv, my_tm = tm, my_ts = ts, my_dm = dm, my_ds = ds;
-        const int32_t my_bx = bx;
-        uint32_t tfl = tflags | (timeout ? kFlagTimeout : 0u);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int32_t ox = __shfl_xor_sync(0xffffffffu, bx, o);
-            if (ov > bv || (ov == bv && ox < bx)) {
-                bv = ov;
-                bx = ox;
-            }
-            tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
-            dm = fmaxf(dm, __shfl_xor_sync(0xffffffffu, dm, o));
-        }
-        tfl = __reduce_or_sync(0xffffffffu, tfl);
-        dflags = __reduce_or_sync(0xffffffffu, dflags);
-        if (lane == 0) wrec[w] = WarpRec{bv, bx, tfl, dflags, tm, dm};
-        __syncthreads();
-        float BV = wrec[0].bv, M = wrec[0].tm, Mq = wrec[0].dm;
-        int32_t BX = wrec[0].bx;
-        uint32_t FLT = wrec[0].tfl, FLD = wrec[0].dfl;
-        for (int i = 1; i < kFastWarps; ++i) {
-            const WarpRec rec = wrec[i];
-            if (rec.bv > BV || (rec.bv == BV && rec.bx < BX)) {
-                BV = rec.bv;
-                BX = rec.bx;
-            }
-            M = fmaxf(M, rec.tm);
-            Mq = fmaxf(Mq, rec.dm);
-            FLT |= rec.tfl;
-            FLD |= rec.dfl;
-        }
-        // the thread that saw the winning vector finds the first equal element in it
-        if (my_bx == BX && my_bv == BV && BX != INT32_MAX) {
-            int32_t idx = BX;
-            for (int e = 0; e < 8; ++e) {
-                const int32_t x = BX + e;
-                if (x >= A.V) break;
-                if (ld_elem<SV_BF16>(u.trow, x) == BV) {
-                    idx = x;
-                    break;
-                }
-            }
-            amax_shared = idx;
-        }
-        if (tid == 0 && BX == INT32_MAX) amax_shared = 0;
-        float S = 0.f, Sq = 0.f;
+        // ---- reductions: max, argmax and reference max are warp-uniform; warp sums, then
+        // warp 0 merges the warps' records ----
         {
-            float part_t = 0.f, part_d = 0.f;
-            if (u.sampling && my_tm > -INFINITY && M > -INFINITY) part_t = my_ts * ex2(my_tm - M);
-            if (u.has_draft && my_dm > -INFINITY && Mq > -INFINITY) part_d = my_ds * ex2(my_dm - Mq);
+            const uint32_t tfl = __reduce_or_sync(0xffffffffu, tflags | (timeout ? kFlagTimeout : 0u));
+            const uint32_t dfl = __reduce_or_sync(0xffffffffu, dflags);
+            float tsw = ts, dsw = ds;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
-                part_t += __shfl_xor_sync(0xffffffffu, part_t, o);
-                part_d += __shfl_xor_sync(0xffffffffu, part_d, o);
+                tsw += __shfl_xor_sync(0xffffffffu, tsw, o);
+                dsw += __shfl_xor_sync(0xffffffffu, dsw, o);
             }
-            if (lane == 0) {
-                wsum[w][0] = part_t;
-                wsum[w][1] = part_d;
-            }
-            __syncthreads();
-            for (int i = 0; i < kFastWarps; ++i) {
-                S += wsum[i][0];
-                Sq += wsum[i][1];
-            }
+            if (lane == 0) wrec[w] = WarpRec{bv, bx, tfl, dfl, tm, dm, tsw, dsw};
         }
+        __syncthreads();
+        if (w == 0) {
+            WarpRec rec = lane < kFastWarps ? wrec[lane]
+                                            : WarpRec{-INFINITY, INT32_MAX, 0u, 0u, -INFINITY, -INFINITY, 0.f, 0.f};
+            float mbv = rec.bv, mtm = rec.tm, mdm = rec.dm;
+            int32_t mbx = rec.bx;
+            uint32_t ftl = rec.tfl, fdl = rec.dfl;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, mbv, o);
+                const int32_t ox = __shfl_xor_sync(0xffffffffu, mbx, o);
+                if (ov > mbv || (ov == mbv && ox < mbx)) {
+                    mbv = ov;
+                    mbx = ox;
+                }
+                mtm = fmaxf(mtm, __shfl_xor_sync(0xffffffffu, mtm, o));
+                mdm = fmaxf(mdm, __shfl_xor_sync(0xffffffffu, mdm, o));
+            }
+            ftl = __reduce_or_sync(0xffffffffu, ftl);
+            fdl = __reduce_or_sync(0xffffffffu, fdl);
+            float st = (rec.tm > -INFINITY && mtm > -INFINITY) ? rec.ts * ex2(rec.tm - mtm) : 0.f;
+            float sd = (rec.dm > -INFINITY && mdm > -INFINITY) ? rec.ds * ex2(rec.dm - mdm) : 0.f;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                st += __shfl_xor_sync(0xffffffffu, st, o);
+                sd += __shfl_xor_sync(0xffffffffu, sd, o);
+            }
+            if (lane == 0) merged = WarpRec{mbv, mbx, ftl, fdl, mtm, mdm, st, sd};
+        }
+        __syncthreads();
+        const float BV = merged.bv;
+        float M = merged.tm, Mq = merged.dm;
+        const float S = merged.ts, Sq = merged.ds;
+        const uint32_t FLT = merged.tfl, FLD = merged.dfl;
+        if (tid == 0) amax_shared = merged.bx == INT32_MAX ? 0 : merged.bx;
         if (!u.sampling) M = -INFINITY;
         if (!u.has_draft) Mq = -INFINITY;
         uint32_t flags = 0;
