@@ -54,8 +54,8 @@ struct D2tPlan {
     int32_t* xs;       // [Vd] support target ids, ascending
     int32_t* js;       // [Vd] the draft id of xs[pos]
     uint32_t* pairs;   // per chunk of kChunkElems target ids, from pbase[c]: its support entries
-                       // (draft id << 16) | (x & (kChunkElems - 1)) in ascending x, padded to a
-                       // multiple of 4 with (Vd << 16) (a spare slot of the scatter target)
+                       // (draft id << 16) | (x & (kChunkElems - 1)) in bank-spread groups of 32
+                       // (see d2t_group_kernel); empty slots hold (Vd << 16), a spare G slot
     int32_t* chunk;    // [V / kChunkElems + 2] support rank at every multiple of kChunkElems
     int32_t* pbase;    // [V / kChunkElems + 2] start of every chunk's entries in pairs
     uint16_t* jmap;    // [V] draft id of every target id, 0xFFFF off the support
@@ -254,8 +254,6 @@ __global__ void __launch_bounds__(kPlanThreads)
     int32_t* pref = reinterpret_cast<int32_t*>(plan_smem + pl.nw);
     __shared__ int32_t warp_tot[kPlanThreads / 32];
     __shared__ int bad_any;
-    __shared__ int32_t crank[kMaxPlanChunks + 1];  // support rank at every chunk start
-    __shared__ int32_t cbase[kMaxPlanChunks + 1];  // padded start of every chunk's entries
     const int tid = threadIdx.x;
     pdl_launch_dependents();  // the row kernel streams rows while the plan is built
     if (tid == 0) bad_any = 0;
@@ -307,24 +305,8 @@ __global__ void __launch_bounds__(kPlanThreads)
         const int32_t w = x >> 5, b = x & 31;
         const int32_t rk = pref[w] + (b ? __popc(bits[w] & ((1u << b) - 1u)) : 0);
         pl.chunk[c] = rk;
-        crank[c] = rk;
     }
     __syncthreads();
-    if (tid == 0) {  // padded starts: every chunk's entries begin on a 16-byte boundary
-        int32_t run = 0;
-        for (int32_t c = 0; c < nch; ++c) {
-            cbase[c] = run;
-            run += (crank[c + 1] - crank[c] + 3) & ~3;
-        }
-        cbase[nch] = run;
-    }
-    __syncthreads();
-    for (int32_t c = tid; c <= nch; c += kPlanThreads) {
-        pl.pbase[c] = cbase[c];
-        if (c < nch)  // the padding slots of chunk c
-            for (int32_t i = cbase[c] + crank[c + 1] - crank[c]; i < cbase[c + 1]; ++i)
-                pl.pairs[i] = static_cast<uint32_t>(Vd) << 16;
-    }
     if (tid == 0) {
         pl.prefix[pl.nw] = pref[pl.nw];
         pl.header[0] = V;
@@ -340,9 +322,95 @@ __global__ void __launch_bounds__(kPlanThreads)
         if (pos >= 0 && pos < Vd) {
             pl.xs[pos] = x;
             pl.js[pos] = j;
-            const int32_t c = x / kChunkElems;
-            pl.pairs[cbase[c] + pos - crank[c]] =
-                (static_cast<uint32_t>(j) << 16) | static_cast<uint32_t>(x & (kChunkElems - 1));
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// support entries of every chunk, grouped for the row pass's scatter
+// ---------------------------------------------------------------------------
+// The row pass moves each support logit z[x] of a chunk (shared-memory stage)
+// to G[draft id] (shared memory) with one 2-byte load and one 2-byte store per
+// entry, 32 entries per warp instruction.  Entries are grouped here so that no
+// bank is hit more than twice by one instruction, neither by the loads
+// (bank (x & 2047) >> 1 mod 32) nor by the stores (bank j >> 1 mod 32): first
+// fit over the chunk's entries in ascending x.  Group g of chunk c occupies
+// slots pbase[c] + 128 (g / 4) + 4 pos + (g % 4), pos = 0..31, which is the
+// layout the row pass reads as one 16-byte word per lane for four groups;
+// slots without an entry hold (Vd << 16).  One warp per chunk, twice: first
+// to count the groups (rounded up to 4), then to write them.
+namespace {
+constexpr int kGroupWarps = 16;
+constexpr int kMaxGroups = 128;  // 128 x 32 slots >= the 2048 entries a chunk can have
+constexpr int kBankCap = 2;
+struct GroupState {
+    uint8_t r[kMaxGroups][32];  // loads per bank
+    uint8_t w[kMaxGroups][32];  // stores per bank
+    uint8_t n[kMaxGroups];      // entries
+};
+}  // namespace
+
+__global__ void __launch_bounds__(kGroupWarps * 32) d2t_group_kernel(int32_t Vd, int32_t V, D2tPlan pl)
+{
+    extern __shared__ __align__(16) unsigned char group_smem[];
+    __shared__ int32_t gcount[kMaxPlanChunks];
+    __shared__ int32_t base_s[kMaxPlanChunks + 1];
+    const int lane = threadIdx.x & 31, wq = threadIdx.x >> 5;
+    GroupState& gs = reinterpret_cast<GroupState*>(group_smem)[wq];
+    const int32_t nch = (V + kChunkElems - 1) / kChunkElems;
+    for (int pass = 0; pass < 2; ++pass) {
+        for (int32_t c = wq; c < nch; c += kGroupWarps) {
+            for (int i = lane; i < kMaxGroups * 32 / 16; i += 32) {
+                reinterpret_cast<uint4*>(gs.r)[i] = make_uint4(0u, 0u, 0u, 0u);
+                reinterpret_cast<uint4*>(gs.w)[i] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            for (int i = lane; i < kMaxGroups; i += 32) gs.n[i] = 0;
+            const int32_t base = pass ? base_s[c] : 0;
+            if (pass)
+                for (int32_t i = lane; i < 32 * gcount[c]; i += 32) pl.pairs[base + i] = static_cast<uint32_t>(Vd) << 16;
+            __syncwarp();
+            const int32_t p0 = min(max(pl.chunk[c], 0), Vd), p1 = min(max(pl.chunk[c + 1], 0), Vd);
+            int32_t ng = 0;
+            for (int32_t p = p0; p < p1; ++p) {
+                const int32_t x = pl.xs[p], j = pl.js[p];
+                if (x < c * kChunkElems || x >= min(V, (c + 1) * kChunkElems) || j < 0 || j >= Vd) continue;
+                const uint32_t xo = static_cast<uint32_t>(x - c * kChunkElems);
+                const int rb = (xo >> 1) & 31, wb = (j >> 1) & 31;
+                int g = -1;
+                for (int s0 = 0; s0 < kMaxGroups && g < 0; s0 += 32) {  // first group with room
+                    const int gg = s0 + lane;
+                    const bool fit = gs.n[gg] < 32 && gs.r[gg][rb] < kBankCap && gs.w[gg][wb] < kBankCap;
+                    const unsigned m = __ballot_sync(0xffffffffu, fit);
+                    if (m) g = s0 + __ffs(m) - 1;
+                }
+                for (int s0 = 0; s0 < kMaxGroups && g < 0; s0 += 32) {  // no bank room: any group with room
+                    const unsigned m = __ballot_sync(0xffffffffu, gs.n[s0 + lane] < 32);
+                    if (m) g = s0 + __ffs(m) - 1;
+                }
+                if (lane == 0) {
+                    const int pos = gs.n[g];
+                    gs.n[g] = static_cast<uint8_t>(pos + 1);
+                    ++gs.r[g][rb];
+                    ++gs.w[g][wb];
+                    if (pass) pl.pairs[base + 128 * (g >> 2) + 4 * pos + (g & 3)] = (static_cast<uint32_t>(j) << 16) | xo;
+                }
+                ng = max(ng, g + 1);
+                __syncwarp();
+            }
+            if (pass == 0 && lane == 0) gcount[c] = (ng + 3) & ~3;
+        }
+        __syncthreads();
+        if (pass == 0) {
+            if (threadIdx.x == 0) {
+                int32_t run = 0;
+                for (int32_t c = 0; c < nch; ++c) {
+                    base_s[c] = run;
+                    run += 32 * gcount[c];
+                }
+                base_s[nch] = run;
+            }
+            __syncthreads();
+            for (int32_t c = threadIdx.x; c <= nch; c += kGroupWarps * 32) pl.pbase[c] = base_s[c];
         }
     }
 }
@@ -1844,7 +1912,8 @@ PlanLayout plan_layout(int32_t V, int32_t Vd)
     L.prefix = take((nw + 1) * 4);
     L.xs = take(static_cast<int64_t>(Vd) * 4);
     L.js = take(static_cast<int64_t>(Vd) * 4);
-    L.pairs = take((static_cast<int64_t>(Vd) + 4 * (static_cast<int64_t>(V) / kChunkElems + 2)) * 4);
+    const int64_t nch = (static_cast<int64_t>(V) + kChunkElems - 1) / kChunkElems;
+    L.pairs = take(nch * kMaxGroups * 32 * 4);
     L.chunk = take((static_cast<int64_t>(V) / kChunkElems + 2) * 4);
     L.pbase = take((static_cast<int64_t>(V) / kChunkElems + 2) * 4);
     L.jmap = take((static_cast<int64_t>(V) + 8) * 2);
@@ -1929,6 +1998,11 @@ cudaError_t launch_d2t_plan_build(const int32_t* d2t, int32_t Vd, int32_t V, voi
                                          static_cast<int>(psmem));
     if (e != cudaSuccess) return e;
     d2t_plan_kernel<<<1, kPlanThreads, psmem, stream>>>(d2t, Vd, V, pl);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const size_t gsmem = kGroupWarps * sizeof(GroupState);
+    e = cudaFuncSetAttribute(d2t_group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(gsmem));
+    if (e != cudaSuccess) return e;
+    d2t_group_kernel<<<1, kGroupWarps * 32, gsmem, stream>>>(Vd, V, pl);
     return cudaGetLastError();
 }
 
