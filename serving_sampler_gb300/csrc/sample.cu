@@ -827,9 +827,9 @@ __global__ void __launch_bounds__(kRowThreads, 1) sample_rows_kernel(SampleArgs 
 // support logits to G[draft id] from shared memory.
 namespace {
 
-constexpr int kFastWarps = 12;
+constexpr int kFastWarps = 16;
 constexpr int kFastThreads = 32 * kFastWarps;
-constexpr int kFastStages = 3;                   // per warp: one being read, the others in flight
+constexpr int kFastStages = 2;                   // per warp: one being read, one in flight
 constexpr uint32_t kFastData = kChunkElems * 2;  // 4 KB of bf16 per stage
 constexpr uint32_t kFastStage = kFastData;
 constexpr int kPairRegs = 4;                     // uint4 groups of support entries per lane and chunk
