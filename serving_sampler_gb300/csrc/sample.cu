@@ -43,7 +43,6 @@ constexpr int kStages = 4;
 constexpr int kRowHeader = 128;
 constexpr uint32_t kSmemBudget = 220 * 1024;
 constexpr int32_t kMaxPlanWords = 25600;  // d2t mode supports V <= 819,200
-constexpr int32_t kMaxPlanChunks = kMaxPlanWords * 32 / kChunkElems;
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum : uint32_t { kFlagAllNegInf = 8u, kFlagDraftBad = 16u, kFlagOffSupport = 32u };
@@ -53,11 +52,11 @@ struct D2tPlan {
     int32_t* prefix;   // [nw + 1] set bits before each word
     int32_t* xs;       // [Vd] support target ids, ascending
     int32_t* js;       // [Vd] the draft id of xs[pos]
-    uint32_t* pairs;   // per chunk of kChunkElems target ids, from pbase[c]: its support entries
+    uint32_t* pairs;   // per chunk c of kChunkElems target ids, from c * 4096: its support entries
                        // (draft id << 16) | (x & (kChunkElems - 1)) in bank-spread groups of 32
                        // (see d2t_group_kernel); empty slots hold (Vd << 16), a spare G slot
     int32_t* chunk;    // [V / kChunkElems + 2] support rank at every multiple of kChunkElems
-    int32_t* pbase;    // [V / kChunkElems + 2] start of every chunk's entries in pairs
+    int32_t* pcount;   // [V / kChunkElems + 2] slots of every chunk in pairs (from c * kMaxGroups * 32)
     uint16_t* jmap;    // [V] draft id of every target id, 0xFFFF off the support
     int32_t* header;   // [0] V, [1] Vd the plan was built for, [2] d2t out of range or repeated
     int32_t nw;
@@ -335,12 +334,11 @@ __global__ void __launch_bounds__(kPlanThreads)
 // bank is hit more than twice by one instruction, neither by the loads
 // (bank (x & 2047) >> 1 mod 32) nor by the stores (bank j >> 1 mod 32): first
 // fit over the chunk's entries in ascending x.  Group g of chunk c occupies
-// slots pbase[c] + 128 (g / 4) + 4 pos + (g % 4), pos = 0..31, which is the
-// layout the row pass reads as one 16-byte word per lane for four groups;
-// slots without an entry hold (Vd << 16).  One warp per chunk, twice: first
-// to count the groups (rounded up to 4), then to write them.
+// slots c * kMaxGroups * 32 + 128 (g / 4) + 4 pos + (g % 4), pos = 0..31,
+// which is the layout the row pass reads as one 16-byte word per lane for four
+// groups; slots without an entry hold (Vd << 16); pcount[c] = 32 x the groups
+// rounded up to 4.  One CTA of one warp per chunk.
 namespace {
-constexpr int kGroupWarps = 16;
 constexpr int kMaxGroups = 128;  // 128 x 32 slots >= the 2048 entries a chunk can have
 constexpr int kBankCap = 2;
 struct GroupState {
@@ -350,69 +348,58 @@ struct GroupState {
 };
 }  // namespace
 
-__global__ void __launch_bounds__(kGroupWarps * 32) d2t_group_kernel(int32_t Vd, int32_t V, D2tPlan pl)
+__global__ void __launch_bounds__(32) d2t_group_kernel(int32_t Vd, int32_t V, D2tPlan pl)
 {
     extern __shared__ __align__(16) unsigned char group_smem[];
-    __shared__ int32_t gcount[kMaxPlanChunks];
-    __shared__ int32_t base_s[kMaxPlanChunks + 1];
-    const int lane = threadIdx.x & 31, wq = threadIdx.x >> 5;
-    GroupState& gs = reinterpret_cast<GroupState*>(group_smem)[wq];
-    const int32_t nch = (V + kChunkElems - 1) / kChunkElems;
-    for (int pass = 0; pass < 2; ++pass) {
-        for (int32_t c = wq; c < nch; c += kGroupWarps) {
-            for (int i = lane; i < kMaxGroups * 32 / 16; i += 32) {
-                reinterpret_cast<uint4*>(gs.r)[i] = make_uint4(0u, 0u, 0u, 0u);
-                reinterpret_cast<uint4*>(gs.w)[i] = make_uint4(0u, 0u, 0u, 0u);
-            }
-            for (int i = lane; i < kMaxGroups; i += 32) gs.n[i] = 0;
-            const int32_t base = pass ? base_s[c] : 0;
-            if (pass)
-                for (int32_t i = lane; i < 32 * gcount[c]; i += 32) pl.pairs[base + i] = static_cast<uint32_t>(Vd) << 16;
-            __syncwarp();
-            const int32_t p0 = min(max(pl.chunk[c], 0), Vd), p1 = min(max(pl.chunk[c + 1], 0), Vd);
-            int32_t ng = 0;
-            for (int32_t p = p0; p < p1; ++p) {
-                const int32_t x = pl.xs[p], j = pl.js[p];
-                if (x < c * kChunkElems || x >= min(V, (c + 1) * kChunkElems) || j < 0 || j >= Vd) continue;
-                const uint32_t xo = static_cast<uint32_t>(x - c * kChunkElems);
-                const int rb = (xo >> 1) & 31, wb = (j >> 1) & 31;
-                int g = -1;
-                for (int s0 = 0; s0 < kMaxGroups && g < 0; s0 += 32) {  // first group with room
-                    const int gg = s0 + lane;
-                    const bool fit = gs.n[gg] < 32 && gs.r[gg][rb] < kBankCap && gs.w[gg][wb] < kBankCap;
-                    const unsigned m = __ballot_sync(0xffffffffu, fit);
-                    if (m) g = s0 + __ffs(m) - 1;
-                }
-                for (int s0 = 0; s0 < kMaxGroups && g < 0; s0 += 32) {  // no bank room: any group with room
-                    const unsigned m = __ballot_sync(0xffffffffu, gs.n[s0 + lane] < 32);
-                    if (m) g = s0 + __ffs(m) - 1;
-                }
-                if (lane == 0) {
-                    const int pos = gs.n[g];
-                    gs.n[g] = static_cast<uint8_t>(pos + 1);
-                    ++gs.r[g][rb];
-                    ++gs.w[g][wb];
-                    if (pass) pl.pairs[base + 128 * (g >> 2) + 4 * pos + (g & 3)] = (static_cast<uint32_t>(j) << 16) | xo;
-                }
-                ng = max(ng, g + 1);
-                __syncwarp();
-            }
-            if (pass == 0 && lane == 0) gcount[c] = (ng + 3) & ~3;
-        }
-        __syncthreads();
-        if (pass == 0) {
-            if (threadIdx.x == 0) {
-                int32_t run = 0;
-                for (int32_t c = 0; c < nch; ++c) {
-                    base_s[c] = run;
-                    run += 32 * gcount[c];
-                }
-                base_s[nch] = run;
-            }
-            __syncthreads();
-            for (int32_t c = threadIdx.x; c <= nch; c += kGroupWarps * 32) pl.pbase[c] = base_s[c];
-        }
+    GroupState& gs = *reinterpret_cast<GroupState*>(group_smem);
+    uint16_t* slot_of = reinterpret_cast<uint16_t*>(group_smem + sizeof(GroupState));  // per entry
+    const int lane = threadIdx.x;
+    const int32_t c = blockIdx.x;
+    for (int i = lane; i < kMaxGroups * 32 / 16; i += 32) {
+        reinterpret_cast<uint4*>(gs.r)[i] = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4*>(gs.w)[i] = make_uint4(0u, 0u, 0u, 0u);
     }
+    for (int i = lane; i < kMaxGroups; i += 32) gs.n[i] = 0;
+    __syncwarp();
+    const int32_t p0 = min(max(pl.chunk[c], 0), Vd), p1 = min(max(pl.chunk[c + 1], p0), min(Vd, p0 + kChunkElems));
+    int32_t ng = 0;
+    for (int32_t p = p0; p < p1; ++p) {
+        const int32_t x = pl.xs[p], j = pl.js[p];
+        if (lane == 0) slot_of[p - p0] = 0xFFFFu;
+        if (x < c * kChunkElems || x >= min(V, (c + 1) * kChunkElems) || j < 0 || j >= Vd) continue;
+        const uint32_t xo = static_cast<uint32_t>(x - c * kChunkElems);
+        const int rb = (xo >> 1) & 31, wb = (j >> 1) & 31;
+        int g = -1;
+        for (int s0 = 0; s0 < kMaxGroups && g < 0; s0 += 32) {  // first group with room
+            const int gg = s0 + lane;
+            const bool fit = gs.n[gg] < 32 && gs.r[gg][rb] < kBankCap && gs.w[gg][wb] < kBankCap;
+            const unsigned m = __ballot_sync(0xffffffffu, fit);
+            if (m) g = s0 + __ffs(m) - 1;
+        }
+        for (int s0 = 0; s0 < kMaxGroups && g < 0; s0 += 32) {  // no bank room: any group with room
+            const unsigned m = __ballot_sync(0xffffffffu, gs.n[s0 + lane] < 32);
+            if (m) g = s0 + __ffs(m) - 1;
+        }
+        if (lane == 0) {
+            const int pos = gs.n[g];
+            gs.n[g] = static_cast<uint8_t>(pos + 1);
+            ++gs.r[g][rb];
+            ++gs.w[g][wb];
+            slot_of[p - p0] = static_cast<uint16_t>(128 * (g >> 2) + 4 * pos + (g & 3));
+        }
+        ng = max(ng, g + 1);
+        __syncwarp();
+    }
+    const int32_t nslots = 32 * ((ng + 3) & ~3);
+    uint32_t* out = pl.pairs + static_cast<int64_t>(c) * kMaxGroups * 32;
+    for (int32_t i = lane; i < nslots; i += 32) out[i] = static_cast<uint32_t>(Vd) << 16;
+    __syncwarp();
+    for (int32_t p = p0 + lane; p < p1; p += 32) {
+        const uint32_t sl = slot_of[p - p0];
+        if (sl != 0xFFFFu)
+            out[sl] = (static_cast<uint32_t>(pl.js[p]) << 16) | static_cast<uint32_t>(pl.xs[p] - c * kChunkElems);
+    }
+    if (lane == 0) pl.pcount[c] = nslots;
 }
 
 // ---------------------------------------------------------------------------
@@ -1065,7 +1052,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
     // a plan for other sizes, or built from a d2t with repeated / out-of-range ids, is not
     // trusted for shared-memory indexing (the race kernel reports SV_ST_BAD_D2T)
     const bool plan_ok = A.plan.header[0] == A.V && A.plan.header[1] == A.Vd && A.plan.header[2] == 0;
-    for (int32_t c = tid; c <= nchunks_t; c += kFastThreads) ctab[c] = plan_ok ? A.plan.pbase[c] : 0;
+    for (int32_t c = tid; c <= nchunks_t; c += kFastThreads) ctab[c] = plan_ok && c < nchunks_t ? A.plan.pcount[c] : 0;
     __syncthreads();
     const uint64_t pol_t = l2_policy_evict_first();
     uint64_t pol_d;
@@ -1122,8 +1109,8 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
             float csum = 0.f;  // this lane's share of the chunk's sum, relative to its running max
             int32_t p0 = 0, p1 = 0;
             if (scatter) {
-                p0 = ctab[cidx];  // a multiple of 4: the chunk's entries padded to whole groups
-                p1 = ctab[cidx + 1];
+                p0 = cidx * (kMaxGroups * 32);  // the chunk's slots: whole groups of four
+                p1 = p0 + ctab[cidx];
                 if (pg_for != cidx) load_pairs(A, p0, p1, lane, pg);  // not prefetched
             }
             if (scatter) {
@@ -1166,7 +1153,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                 pg_for = -1;
                 if (u.has_draft && qn < u.n && qn >= u.nd) {
                     pg_for = qn - u.nd;
-                    load_pairs(A, ctab[pg_for], ctab[pg_for + 1], lane, pg);
+                    load_pairs(A, pg_for * (kMaxGroups * 32), pg_for * (kMaxGroups * 32) + ctab[pg_for], lane, pg);
                 }
             }
 #pragma unroll
@@ -1894,7 +1881,7 @@ __global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArg
 namespace {
 
 struct PlanLayout {
-    int64_t header, bitmap, prefix, xs, js, pairs, chunk, pbase, jmap, total;
+    int64_t header, bitmap, prefix, xs, js, pairs, chunk, pcount, jmap, total;
 };
 
 PlanLayout plan_layout(int32_t V, int32_t Vd)
@@ -1915,7 +1902,7 @@ PlanLayout plan_layout(int32_t V, int32_t Vd)
     const int64_t nch = (static_cast<int64_t>(V) + kChunkElems - 1) / kChunkElems;
     L.pairs = take(nch * kMaxGroups * 32 * 4);
     L.chunk = take((static_cast<int64_t>(V) / kChunkElems + 2) * 4);
-    L.pbase = take((static_cast<int64_t>(V) / kChunkElems + 2) * 4);
+    L.pcount = take((static_cast<int64_t>(V) / kChunkElems + 2) * 4);
     L.jmap = take((static_cast<int64_t>(V) + 8) * 2);
     L.total = off;
     return L;
@@ -1933,7 +1920,7 @@ D2tPlan plan_view(void* base, int32_t V, int32_t Vd)
     pl.js = reinterpret_cast<int32_t*>(b + L.js);
     pl.pairs = reinterpret_cast<uint32_t*>(b + L.pairs);
     pl.chunk = reinterpret_cast<int32_t*>(b + L.chunk);
-    pl.pbase = reinterpret_cast<int32_t*>(b + L.pbase);
+    pl.pcount = reinterpret_cast<int32_t*>(b + L.pcount);
     pl.jmap = reinterpret_cast<uint16_t*>(b + L.jmap);
     pl.nw = (V + 31) / 32;
     return pl;
@@ -1999,10 +1986,9 @@ cudaError_t launch_d2t_plan_build(const int32_t* d2t, int32_t Vd, int32_t V, voi
     if (e != cudaSuccess) return e;
     d2t_plan_kernel<<<1, kPlanThreads, psmem, stream>>>(d2t, Vd, V, pl);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const size_t gsmem = kGroupWarps * sizeof(GroupState);
-    e = cudaFuncSetAttribute(d2t_group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(gsmem));
-    if (e != cudaSuccess) return e;
-    d2t_group_kernel<<<1, kGroupWarps * 32, gsmem, stream>>>(Vd, V, pl);
+    const size_t gsmem = sizeof(GroupState) + kChunkElems * 2;
+    const int32_t nch = (V + kChunkElems - 1) / kChunkElems;
+    d2t_group_kernel<<<nch, 32, gsmem, stream>>>(Vd, V, pl);
     return cudaGetLastError();
 }
 
