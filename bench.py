@@ -40,7 +40,7 @@ def _args():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", choices=["listen", "d2t"], default="listen",
+    ap.add_argument("--workload", choices=["listen", "d2t", "cfg", "sweep"], default="listen",
                     help="listen: greedy verify with a runner-up branch (headline); d2t: speculative sampling")
     ap.add_argument("--sessions", type=int, default=None,
                     help="requests per step (default: the workload's own, 64 listen sessions / 128 d2t requests)")
@@ -193,7 +193,7 @@ class Workload:
             self.desc = (f"listen: {R} sessions x (32 main + 32 runner-up drafts) = 65 rows x 151936 bf16 per "
                          f"session ({self.logit_bytes / 1e9:.3f} GB of logits per step)")
             self.metric = "verify logit GB/s (speculative-listening greedy verify, V=151936 bf16)"
-        else:
+        elif name == "d2t":
             w = workloads.d2t_workload(device=device, R=sessions or 128)
             R, k, V, Vd = w["R"], w["k"], w["V"], w["Vd"]
             self.rows = R * (k + 1)
@@ -209,14 +209,34 @@ class Workload:
             self.ws = torch.empty(sv.verify_sample_workspace(R, k, V, Vd), dtype=torch.uint8, device=device)
             # the d2t map is a constant of the draft model: its device plan is built once, here
             self.plan = sv.d2t_plan(w["d2t"], V)
-            self.launches = 2
-            self.kernel = "sample_rows_kernel<bf16,bf16> + race_commit_kernel"
+            self.launches = sv.LAUNCHES["verify_sample"]
+            self.kernel = "sample_rows_fast_kernel + race_rows_kernel<bf16,bf16>"
             self.kernel_file = "sample.cu"
             self.profile = "sample_rows_d2t.md"
             self.desc = (f"d2t: {R} requests x 7 drafts (+bonus) over V=151936 bf16, draft vocab 32000 bf16 via "
                          f"d2t, T=0.7 ({self.logit_bytes / 1e9:.3f} GB of logits per step; d2t plan built once "
                          f"per draft model, outside the step)")
             self.metric = "verify+sample logit GB/s (speculative sampling, d2t 32000 -> 151936, bf16)"
+        else:  # cfg
+            w = workloads.cfg_workload(device=device, R=sessions or 256)
+            R, k, S, W = w["R"], w["k"], w["S"], w["W"]
+            self.rows = R * (k + 1) * S
+            self.logit_bytes = 2 * R * (k + 1) * S * W * 2 + R * k * S * W * 2
+            self.inputs = {"cond": w["cond"], "uncond": w["uncond"], "draft_logits": w["draft_logits"],
+                           "draft": w["draft"], "seeds": w["seeds"], "temperature": w["temperature"]}
+            self.out = dict(accept_len=torch.empty(R, dtype=torch.int32, device=device),
+                            tokens=torch.empty(R, k + 1, S, dtype=torch.int32, device=device),
+                            status=torch.empty(R, dtype=torch.int32, device=device),
+                            tv=torch.empty(R, k, S, dtype=torch.float32, device=device))
+            self.ws = torch.empty(sv.cfg_merge_sample_workspace(R, k, S, W), dtype=torch.uint8, device=device)
+            self.launches = sv.LAUNCHES["cfg_merge_sample"]
+            self.kernel = "cfg_rows_kernel + cfg_race_kernel"
+            self.kernel_file = "cfg.cu"
+            self.profile = "cfg_rows_cfg.md"
+            self.desc = (f"cfg: {R} requests x {k} drafted frames (+1) x {S} codebooks of {W} bf16 entries, "
+                         f"conditional + unconditional rows merged with w={w['w']}, T=1 "
+                         f"({self.logit_bytes / 1e9:.3f} GB of logits per step)")
+            self.metric = "CFG merge + verify logit GB/s (9 RVQ codebooks x 4096, bf16)"
         self.w = w
         if torch.cuda.is_available():
             torch.cuda.empty_cache()  # drop the generator's fp32 temporaries
@@ -226,6 +246,11 @@ class Workload:
         if self.name == "listen":
             self.sv.verify_greedy(inp["target"], w["R"], w["k"], 2, inp["draft"], out=self.out, workspace=self.ws,
                                   stream=stream)
+        elif self.name == "cfg":
+            self.sv.cfg_merge_sample(inp["cond"], inp["uncond"], w["cb_id_base"], w["cb_data_offset"], w["S"],
+                                     w["W"], w["w"], inp["draft_logits"], w["R"], w["k"], inp["draft"],
+                                     inp["seeds"], inp["temperature"], out=self.out, workspace=self.ws,
+                                     stream=stream)
         else:
             self.sv.verify_sample(inp["target"], inp["draft_logits"], None, w["R"], w["k"], inp["draft"],
                                   inp["seeds"], inp["temperature"], out=self.out, workspace=self.ws, stream=stream,
@@ -239,6 +264,11 @@ class Workload:
             import workloads
 
             w = self.w
+            if self.name == "cfg":
+                self._h = {"cond": workloads.host_rows(w["cond"]), "uncond": workloads.host_rows(w["uncond"]),
+                           "draft_logits": workloads.host_rows(w["draft_logits"]), "draft": w["draft"].cpu().numpy(),
+                           "seeds": w["seeds"].cpu().numpy().view(np.uint64), "T": w["temperature"].cpu().numpy()}
+                return self._h
             h = {"target": workloads.host_rows(w["target"]), "draft": w["draft"].cpu().numpy()}
             if self.name != "listen":
                 h["draft_logits"] = workloads.host_rows(w["draft_logits"])
@@ -259,6 +289,14 @@ class Workload:
             rpr = 2 * k + 1
             oracle.verify_greedy(h["target"][r * rpr:(r + 1) * rpr], 1, k, 2, h["draft"][r:r + 1])
             return rpr * w["V"] * 2, rpr
+        if self.name == "cfg":
+            S, W = w["S"], w["W"]
+            rr = (k + 1) * S
+            oracle.cfg_merge_sample(h["cond"][r * rr:(r + 1) * rr], h["uncond"][r * rr:(r + 1) * rr],
+                                    w["cb_id_base"], w["cb_data_offset"], S, W, w["w"],
+                                    h["draft_logits"][r * k * S:(r + 1) * k * S], 1, k, h["draft"][r:r + 1],
+                                    h["seeds"][r:r + 1], h["T"][r:r + 1])
+            return 2 * rr * W * 2 + k * S * W * 2, rr
         oracle.verify_sample(h["target"][r * (k + 1):(r + 1) * (k + 1)], h["draft_logits"][r * k:(r + 1) * k],
                              h["d2t"], 1, k, h["draft"][r:r + 1], h["seeds"][r:r + 1], h["T"][r:r + 1])
         return (k + 1) * w["V"] * 2 + k * w["Vd"] * 2, k + 1
@@ -306,7 +344,8 @@ def run_reference(a):
 
     oracle.build()
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    wl = Workload(a.workload, dev, a.sessions)
+    # the sweep's oracle leg times the sampling workload's requests (same step definition)
+    wl = Workload("d2t" if a.workload == "sweep" else a.workload, dev, a.sessions)
     # one request per step, timed as it stands
     wl._host()
     for s_ in range(a.warmup):
@@ -450,10 +489,101 @@ def run_native(a):
     return 0
 
 
+def run_sweep(a):
+    """Throughput sweep: batches {1, 8, 64, 256, 1024} x 9 positions (8 drafts + bonus),
+    V = 151,936, bf16 and fp32 logits, half the requests greedy (T = 0) and half sampled
+    (T alternating 0.6 / 1.0) with the d2t draft model of the sampling workload.  Every
+    call is timed alone with CUDA events; L2 is flushed before each call whose inputs
+    fit in four L2s.  Prints one JSON line with a point per (dtype, batch)."""
+    import torch
+
+    import serving_sampler_gb300 as sv
+    import workloads
+    from serving_sampler_gb300 import _build
+
+    world, rank, local = _dist()
+    if rank != 0:
+        return 0
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    _build.build()
+    sv.load()
+    stream = torch.cuda.current_stream(device)
+    peak, peak_kind = _peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    k, V, Vd = 8, workloads.V_QWEN, workloads.VD_DRAFT
+    sigma = list(workloads.D2T_SIGMA) + [workloads.D2T_SIGMA[-1]]
+    steps = max(3, min(a.steps, 50))
+    points = []
+    clocks = Clocks(local)
+    clocks.start()
+    for dt, es in ((torch.bfloat16, 2), (torch.float32, 4)):
+        for B in (1, 8, 64, 256, 1024):
+            T = [0.0 if r % 2 == 0 else (0.6 if (r // 2) % 2 == 0 else 1.0) for r in range(B)]
+            w = workloads.sample_batch(B, k, V, Vd, dt, T=T, sigma_pos=sigma, delta=workloads.D2T_DELTA,
+                                       z_sigma=3.0, seed=1300 + B, seed_base=5000, device=device)
+            plan = sv.d2t_plan(w["d2t"], V)
+            nsamp = sum(1 for t in T if t > 0)
+            nbytes = B * (k + 1) * V * es + nsamp * k * Vd * es
+            out = dict(accept_len=torch.empty(B, dtype=torch.int32, device=device),
+                       tokens=torch.empty(B, k + 1, dtype=torch.int32, device=device),
+                       status=torch.empty(B, dtype=torch.int32, device=device),
+                       tv=torch.empty(B, k, dtype=torch.float32, device=device),
+                       p_draft=torch.empty(B, k, dtype=torch.float32, device=device),
+                       q_draft=torch.empty(B, k, dtype=torch.float32, device=device))
+            ws = torch.empty(sv.verify_sample_workspace(B, k, V, Vd), dtype=torch.uint8, device=device)
+
+            def call():
+                sv.verify_sample(w["target"], w["draft_logits"], None, B, k, w["draft"], w["seeds"],
+                                 w["temperature"], out=out, workspace=ws, stream=stream, plan=plan)
+
+            for _ in range(max(a.warmup, 3)):
+                call()
+            torch.cuda.synchronize()
+            do_flush = nbytes < 4 * (129 << 20)
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+            for e0, e1 in ev:
+                if do_flush:
+                    flush.add_(1)
+                e0.record(stream)
+                call()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / steps
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            points.append({"dtype": "bf16" if es == 2 else "f32", "batch": B, "rows": B * (k + 1),
+                           "sampled_requests": nsamp, "bytes": nbytes, "us_per_call": ms * 1e3, "GB/s": gbs,
+                           "rows_per_s": B * (k + 1) / (ms * 1e-3), "roofline_frac": gbs / peak,
+                           "l2": "flushed before each call" if do_flush else "inputs larger than L2"})
+            del w, plan, out, ws
+            torch.cuda.empty_cache()
+    clock_rows = clocks.stop()
+    best = max(p["GB/s"] for p in points)
+    line = {
+        "metric": "verify+sample logit GB/s sweep (batch x 9 positions, V=151936, 50/50 greedy/sampling)",
+        "value": best, "unit": "GB/s", "n_gpus": 1, "steps": steps, "warmup": max(a.warmup, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16,f32",
+        "data": "synthetic",
+        "config": {"workload": "sweep: batch {1,8,64,256,1024} x (8 drafts + bonus), d2t 32000 -> 151936, "
+                               "T alternating 0 / 0.6 / 0 / 1.0 per request",
+                   "value": "the best point"},
+        "roofline_peak": {"value": peak, "unit": "GB/s",
+                          "source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                          else "fallback 6.8 TB/s"},
+        "points": points,
+        "gpu_launches": len(points) * (steps + max(a.warmup, 3)) * sv.LAUNCHES["verify_sample"],
+        "clocks": Clocks.summarize(clock_rows),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     a = _args()
     if a.impl == "reference":
         return run_reference(a)
+    if a.workload == "sweep":
+        return run_sweep(a)
     return run_native(a)
 
 

@@ -24,7 +24,10 @@ ST_BAD_TEMP, ST_BAD_D2T, ST_TIMEOUT = 16, 32, 64
 MAX_K, MAX_S = 256, 16
 
 # kernels launched by one call of each entry point (reported by the benchmark)
-LAUNCHES = {"verify_greedy": 2, "verify_sample": 3, "cfg_merge_sample": 3, "accept_scan": 1}
+# kernels one call launches: verify_sample with a prebuilt d2t plan (or the identity map)
+# launches 2, and 2 more when it builds the plan itself; d2t_plan launches 2
+LAUNCHES = {"verify_greedy": 2, "verify_sample": 2, "verify_sample_plan_in_call": 4, "d2t_plan": 2,
+            "cfg_merge_sample": 3, "accept_scan": 1}
 
 
 class SpecVerifyError(RuntimeError):

@@ -98,6 +98,21 @@ def test_d2t_shapes(sv, dtype, ddtype, V, Vd, R, k, row_pad):
     compare(_run(sv, w), _oracle(w))
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_sweep_point_mixed_greedy_and_sampling(sv, dtype):
+    """A point of the throughput sweep: 9 positions (8 drafts + bonus), V = 151,936, the d2t
+    draft model, half the requests greedy (T = 0), the others at T = 0.6 or 1.0."""
+    B, k = 6, 8
+    T = [0.0 if r % 2 == 0 else (0.6 if (r // 2) % 2 == 0 else 1.0) for r in range(B)]
+    sigma = list(workloads.D2T_SIGMA) + [workloads.D2T_SIGMA[-1]]
+    w = workloads.sample_batch(B, k, workloads.V_QWEN, workloads.VD_DRAFT, dtype, T=T, sigma_pos=sigma,
+                               delta=workloads.D2T_DELTA, z_sigma=3.0, seed=1308, seed_base=5000)
+    got, want = _run(sv, w), _oracle(w)
+    compare(got, want)
+    greedy = np.array(T) == 0
+    assert np.isnan(got["tv"][greedy]).all() and not np.isnan(got["tv"][~greedy]).any()
+
+
 def test_identity_bf16_shapes(sv):
     w = workloads.sample_batch(12, 6, 5000, None, torch.bfloat16, T=0.9, sigma_pos=0.5, seed=4)
     compare(_run(sv, w), _oracle(w))
