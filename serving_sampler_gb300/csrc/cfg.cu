@@ -5,17 +5,18 @@
 // codebook samples from its own partition of the vocabulary).  Sampling rules
 // follow "speculative decoding for Omni models", section 2.
 //
-// cfg_rows_kernel  one CTA per (request, frame j, codebook s) row.  The row's
-//                  codebook slice of cond and uncond is merged in fp32 as
-//                  fmaf(w, c - u, u) into shared memory; the CTA takes the
-//                  merged row's argmax, max and sum-exp at T, the draft row's
-//                  max and sum-exp, TV = sum max(0, q - p), p and q at the
-//                  drafted id, and the accept test (Philox row j * S + s).
-// cfg_race_kernel  one CTA per (request, codebook): the first frame n with a
-//                  rejected codebook, then for codebook s: its draft if its
-//                  own test passed, else the residual race at frame n (or the
-//                  bonus race at frame k), the merged row rebuilt from the
-//                  inputs.  Codebook 0 also writes accept_len and status.
+// cfg_rows_warp_kernel  one warp per (request, frame j, codebook s) row.  The
+//                  row's codebook slice of cond and uncond is merged in fp32 as
+//                  fmaf(w, c - u, u) (packed fp32 pairs, the same roundings);
+//                  pass 1 takes the merged row's argmax and online max /
+//                  sum-exp at T and the draft row's; pass 2 (the slices again,
+//                  from L2) TV = sum max(0, q - p) and p, q at the drafted id;
+//                  then the accept test (Philox row j * S + s).
+// cfg_race_warp_kernel  one warp per (request, codebook): the first frame n
+//                  with a rejected codebook, then for codebook s its draft if
+//                  its own test passed, else the residual race at frame n (or
+//                  the bonus race at frame k) over the merged row rebuilt from
+//                  the inputs.  Codebook 0 also writes accept_len.
 #include <algorithm>
 #include <cfloat>
 #include <climits>
@@ -27,9 +28,8 @@ namespace sv {
 
 namespace {
 
-constexpr int kCfgThreads = 256;
+constexpr int32_t kCfgMaxW = 16384;  // widest codebook
 constexpr float kLog2eC = 1.4426950408889634f;
-constexpr int32_t kCfgMaxW = 16384;  // two fp32 rows of W in shared memory
 
 enum : uint32_t { kCfgBad = 1u, kCfgOffSupport = 2u };
 
@@ -46,10 +46,9 @@ struct CfgArgs {
     const char* cbase;
     const char* ubase;
     int64_t stride;  // bytes, shared by cond and uncond
-    int esize;
     const char* dbase;
     int64_t dstride;
-    int desize;
+    int cvec, dvec;  // 16-byte loads allowed for cond/uncond slices and for draft rows
     CfgShape shape;
     int32_t R, k;
     const int32_t* draft;
@@ -62,110 +61,84 @@ struct CfgArgs {
     CfgStat* stats;
 };
 
-__device__ __forceinline__ float load_any(const char* p, int64_t e, int esize)
-{
-    if (esize == 2) return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(p)[e]) << 16);
-    return reinterpret_cast<const float*>(p)[e];
-}
 
-// merged logit, fp32: d = c - u (one rounding), fmaf(w, d, u) (one rounding)
-__device__ __forceinline__ float merge_one(float c, float u, float w)
-{
-    return __fmaf_rn(w, __fsub_rn(c, u), u);
-}
 
-template <int NT>
-__device__ __forceinline__ float bsum(float v, float* sc)
+__device__ __forceinline__ float wsum(float v)
 {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) sc[threadIdx.x >> 5] = v;
-    __syncthreads();
-    float t = 0.f;
-    for (int i = 0; i < NT / 32; ++i) t += sc[i];
-    return t;
-}
-
-template <int NT>
-__device__ __forceinline__ float bmax(float v, float* sc)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) sc[threadIdx.x >> 5] = v;
-    __syncthreads();
-    float t = -INFINITY;
-    for (int i = 0; i < NT / 32; ++i) t = fmaxf(t, sc[i]);
-    return t;
-}
-
-template <int NT>
-__device__ __forceinline__ uint32_t bor(uint32_t v, uint32_t* sc)
-{
-    v = __reduce_or_sync(0xffffffffu, v);
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) sc[threadIdx.x >> 5] = v;
-    __syncthreads();
-    uint32_t t = 0;
-    for (int i = 0; i < NT / 32; ++i) t |= sc[i];
-    return t;
-}
-
-// (max value, lowest index) over the block
-template <int NT>
-__device__ __forceinline__ void bargmax(float& v, int32_t& x, float* sv, int32_t* sx)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-        const int32_t ox = __shfl_xor_sync(0xffffffffu, x, o);
-        if (ov > v || (ov == v && ox < x)) {
-            v = ov;
-            x = ox;
-        }
-    }
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) {
-        sv[threadIdx.x >> 5] = v;
-        sx[threadIdx.x >> 5] = x;
-    }
-    __syncthreads();
-    v = sv[0];
-    x = sx[0];
-    for (int i = 1; i < NT / 32; ++i)
-        if (sv[i] > v || (sv[i] == v && sx[i] < x)) {
-            v = sv[i];
-            x = sx[i];
-        }
-}
-
-// merge the codebook slice of one row into m[0..W); returns NaN / +inf flags
-__device__ __forceinline__ uint32_t merge_row(const CfgArgs& A, int64_t row, int32_t s, float* m)
-{
-    const int32_t W = A.shape.W;
-    const char* c = A.cbase + row * A.stride + static_cast<int64_t>(A.shape.data_off[s]) * A.esize;
-    const char* u = A.ubase + row * A.stride + static_cast<int64_t>(A.shape.data_off[s]) * A.esize;
-    uint32_t bad = 0;
-    for (int32_t l = threadIdx.x; l < W; l += kCfgThreads) {
-        const float v = merge_one(load_any(c, l, A.esize), load_any(u, l, A.esize), A.shape.w);
-        if (v != v || v == INFINITY) bad = 1;
-        m[l] = v != v ? -INFINITY : v;
-    }
-    return bad;
+    return v;
 }
 
 }  // namespace
 
-__global__ void __launch_bounds__(kCfgThreads) cfg_rows_kernel(CfgArgs A)
+// One warp per (request, frame j, codebook s) row, four rows per CTA, no block
+// barrier.  Pass 1 streams the row's codebook slices of cond, uncond and the
+// draft row in batches of 32 ids per lane (the next batch's loads in flight
+// while one is reduced): merged logits fmaf(w, c - u, u), argmax, NaN / +inf
+// flags, and online max / sum-exp at T of the merged and the draft row.
+// Pass 2 reads the slices again (from L2) for TV = sum max(0, q - p) and p, q
+// at the drafted id.
+constexpr int kCfgWarpRows = 4;
+
+// one 8-id group of a row as raw 16-byte words (bf16: 1, fp32: 2); -inf beyond W
+template <int DT>
+struct Grp {
+    static constexpr int kWords = DT == SV_BF16 ? 1 : 2;
+    uint4 q[kWords];
+};
+
+template <int DT>
+__device__ __forceinline__ void ld_grp(const char* p, int32_t e0, int32_t W, bool vec, Grp<DT>& g)
 {
-    extern __shared__ __align__(16) float cfg_smem[];
-    __shared__ float rf[kCfgThreads / 32];
-    __shared__ int32_t ri[kCfgThreads / 32];
-    __shared__ uint32_t ru[kCfgThreads / 32];
+    if (vec && e0 + 8 <= W) {
+#pragma unroll
+        for (int h = 0; h < Grp<DT>::kWords; ++h)
+            g.q[h] = ld_nc_v4(reinterpret_cast<const uint4*>(p + static_cast<int64_t>(e0) * (DT == SV_BF16 ? 2 : 4)) + h);
+        return;
+    }
+    uint32_t wv[4 * Grp<DT>::kWords];
+    if constexpr (DT == SV_BF16) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t lo = e0 + 2 * i < W ? reinterpret_cast<const uint16_t*>(p)[e0 + 2 * i] : 0xFF80u;
+            const uint32_t hi = e0 + 2 * i + 1 < W ? reinterpret_cast<const uint16_t*>(p)[e0 + 2 * i + 1] : 0xFF80u;
+            wv[i] = lo | (hi << 16);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            wv[i] = e0 + i < W ? reinterpret_cast<const uint32_t*>(p)[e0 + i] : 0xFF800000u;
+    }
+#pragma unroll
+    for (int h = 0; h < Grp<DT>::kWords; ++h) g.q[h] = make_uint4(wv[4 * h], wv[4 * h + 1], wv[4 * h + 2], wv[4 * h + 3]);
+}
+
+// ids 2h, 2h + 1 of a group as an fp32 pair (h = 0..3)
+template <int DT>
+__device__ __forceinline__ unsigned long long grp_pair(const Grp<DT>& g, int h)
+{
+    if constexpr (DT == SV_BF16) {
+        const uint32_t w = h == 0 ? g.q[0].x : h == 1 ? g.q[0].y : h == 2 ? g.q[0].z : g.q[0].w;
+        return bf16x2_to_f32x2(w);
+    } else {
+        const uint4& q = g.q[h >> 1];
+        return (h & 1) ? pack2(__uint_as_float(q.z), __uint_as_float(q.w))
+                       : pack2(__uint_as_float(q.x), __uint_as_float(q.y));
+    }
+}
+
+template <int DT, int DD>
+__global__ void __launch_bounds__(32 * kCfgWarpRows, 4) cfg_rows_warp_kernel(CfgArgs A)
+{
+    constexpr int kG = 2;      // groups of 8 ids per lane and batch
+    constexpr int kP = 4 * kG; // fp32 pairs per lane and batch
     pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
     const int32_t S = A.shape.S, W = A.shape.W, k = A.k;
-    const int64_t unit = blockIdx.x;  // ((r * (k + 1)) + j) * S + s
+    const int64_t units = static_cast<int64_t>(A.R) * (k + 1) * S;
+    const int64_t unit = static_cast<int64_t>(blockIdx.x) * kCfgWarpRows + (threadIdx.x >> 5);
+    if (unit >= units) return;  // whole warps only
     const int32_t s = static_cast<int32_t>(unit % S);
     const int64_t rj = unit / S;
     const int32_t j = static_cast<int32_t>(rj % (k + 1));
@@ -174,122 +147,277 @@ __global__ void __launch_bounds__(kCfgThreads) cfg_rows_kernel(CfgArgs A)
     const bool sampling = T > 0.f && A.dbase != nullptr;
     const bool has_draft = sampling && j < k;
     const float c = sampling ? kLog2eC / T : 0.f;
-    float* m = cfg_smem;
-    float* y = cfg_smem + W;
+    const unsigned long long w2 = pack2(A.shape.w, A.shape.w), c2 = pack2(c, c);
+    const int64_t off = unit * A.stride + static_cast<int64_t>(A.shape.data_off[s]) * (DT == SV_BF16 ? 2 : 4);
+    const char* cp = A.cbase + off;
+    const char* up = A.ubase + off;
+    const char* dp = has_draft ? A.dbase + ((static_cast<int64_t>(r) * k + j) * S + s) * A.dstride : nullptr;
+    const bool cvec = A.cvec != 0, dvec = A.dvec != 0;
+    const int32_t ngroups = (W + 7) / 8;
+    const int32_t nb = (ngroups + 32 * kG - 1) / (32 * kG);
 
-    uint32_t bad = merge_row(A, unit, s, m);
-    __syncthreads();
-    float bv = -INFINITY;
+    Grp<DT> cg[kG], ug[kG];
+    Grp<DD> yg[kG];
+    auto load = [&](int32_t b) {
+#pragma unroll
+        for (int i = 0; i < kG; ++i) {
+            const int32_t e0 = 8 * (lane + 32 * (kG * b + i));
+            ld_grp<DT>(cp, e0, W, cvec, cg[i]);
+            ld_grp<DT>(up, e0, W, cvec, ug[i]);
+            if (dp) ld_grp<DD>(dp, e0, W, dvec, yg[i]);
+        }
+    };
+    // merged pairs fmaf(w, c - u, u) (the same two roundings as the scalar form); ids at or
+    // beyond W (only in the last batch) read -inf
+    auto merge = [&](int32_t b, unsigned long long* m2) {
+#pragma unroll
+        for (int i = 0; i < kG; ++i)
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const unsigned long long u2 = grp_pair<DT>(ug[i], h);
+                m2[4 * i + h] = fma2(w2, sub2(grp_pair<DT>(cg[i], h), u2), u2);
+            }
+        if (8 * 32 * kG * (b + 1) > W) {  // the tail batch
+#pragma unroll
+            for (int i = 0; i < kG; ++i)
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const int32_t x = 8 * (lane + 32 * (kG * b + i)) + 2 * h;
+                    float lo, hi;
+                    unpack2(m2[4 * i + h], lo, hi);
+                    m2[4 * i + h] = pack2(x < W ? lo : -INFINITY, x + 1 < W ? hi : -INFINITY);
+                }
+        }
+    };
+
+    // ---- pass 1 ----
+    float bv = -INFINITY;  // argmax value (NaN-propagating per batch; a NaN row is flagged)
     int32_t bx = INT32_MAX;
-    float mx = -INFINITY;
-    for (int32_t l = threadIdx.x; l < W; l += kCfgThreads) {
-        const float v = m[l];
-        if (v > bv) {
-            bv = v;
-            bx = l;
+    float ymx = -INFINITY;
+    bool nan_seen = false;
+    float tm = -INFINITY, dm = -INFINITY;                  // running maxima (log2 units)
+    unsigned long long ts2 = 0ull, ds2 = 0ull;             // running sums (pairs)
+    load(0);
+    for (int32_t b = 0; b < nb; ++b) {
+        unsigned long long m2[kP], y2[kP];
+        merge(b, m2);
+#pragma unroll
+        for (int i = 0; i < kG; ++i)
+#pragma unroll
+            for (int h = 0; h < 4; ++h) y2[4 * i + h] = dp ? grp_pair<DD>(yg[i], h) : pack2(-INFINITY, -INFINITY);
+        if (b + 1 < nb) load(b + 1);
+        float lm = -INFINITY, ly = -INFINITY;
+#pragma unroll
+        for (int p = 0; p < kP; ++p) {
+            float lo, hi;
+            unpack2(m2[p], lo, hi);
+            lm = fmax_nan(lm, fmax_nan(lo, hi));
+            unpack2(y2[p], lo, hi);
+            ly = fmax_nan(ly, fmax_nan(lo, hi));
+        }
+        if (lm != lm) {  // rare: NaN logits, which the argmax reads as -inf (the row is flagged)
+            nan_seen = true;
+            lm = -INFINITY;
+#pragma unroll
+            for (int p = 0; p < kP; ++p) {
+                float lo, hi;
+                unpack2(m2[p], lo, hi);
+                lm = fmaxf(lm, fmaxf(lo, hi));
+            }
+        }
+        if (lm > bv) {  // the first id of the batch holding its maximum (ids ascend in the lane)
+#pragma unroll
+            for (int p = kP - 1; p >= 0; --p) {
+                float lo, hi;
+                unpack2(m2[p], lo, hi);
+                const int32_t x = 8 * (lane + 32 * (kG * b + p / 4)) + 2 * (p % 4);
+                if (hi == lm) bx = x + 1;
+                if (lo == lm) bx = x;
+            }
+            bv = lm;
+        }
+        ymx = fmax_nan(ymx, ly);
+        if (sampling && !nan_seen) {
+            const float mt = lm * c;
+            if (mt > tm) {
+                const float sc = tm == -INFINITY ? 0.f : ex2(tm - mt);
+                ts2 = mul2(ts2, pack2(sc, sc));
+                tm = mt;
+            }
+            if (tm > -INFINITY && tm < INFINITY) {
+                const unsigned long long nm2 = pack2(-tm, -tm);
+#pragma unroll
+                for (int p = 0; p < kP; ++p) {
+                    float a0, a1;
+                    unpack2(fma2(m2[p], c2, nm2), a0, a1);
+                    ts2 = add2(ts2, pack2(ex2(a0), ex2(a1)));
+                }
+            }
+        }
+        if (has_draft && !(ly != ly)) {
+            const float yt = ly * c;
+            if (yt > dm) {
+                const float sc = dm == -INFINITY ? 0.f : ex2(dm - yt);
+                ds2 = mul2(ds2, pack2(sc, sc));
+                dm = yt;
+            }
+            if (dm > -INFINITY && dm < INFINITY) {
+                const unsigned long long nd2 = pack2(-dm, -dm);
+#pragma unroll
+                for (int p = 0; p < kP; ++p) {
+                    float a0, a1;
+                    unpack2(fma2(y2[p], c2, nd2), a0, a1);
+                    ds2 = add2(ds2, pack2(ex2(a0), ex2(a1)));
+                }
+            }
         }
     }
-    bargmax<kCfgThreads>(bv, bx, rf, ri);
-    mx = bv;
+    float ts, ds;
+    {
+        float a0, a1;
+        unpack2(ts2, a0, a1);
+        ts = a0 + a1;
+        unpack2(ds2, a0, a1);
+        ds = a0 + a1;
+    }
+    // warp reductions
+    const float my_tm = tm, my_dm = dm;
+    bool bad_l = nan_seen || bv == INFINITY || (has_draft && (ymx != ymx || ymx == INFINITY));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int32_t ox = __shfl_xor_sync(0xffffffffu, bx, o);
+        if (ov > bv || (ov == bv && ox < bx)) {
+            bv = ov;
+            bx = ox;
+        }
+        tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
+        dm = fmaxf(dm, __shfl_xor_sync(0xffffffffu, dm, o));
+        ymx = fmaxf(ymx, __shfl_xor_sync(0xffffffffu, ymx, o));
+    }
+    bool bad = __any_sync(0xffffffffu, bad_l) || bv == -INFINITY;
+    if (has_draft) bad = bad || dm == -INFINITY;
+    float sm = (my_tm > -INFINITY && tm > -INFINITY) ? ts * ex2(my_tm - tm) : 0.f;
+    float sq = (my_dm > -INFINITY && dm > -INFINITY) ? ds * ex2(my_dm - dm) : 0.f;
+    sm = wsum(sm);
+    sq = wsum(sq);
     CfgStat st{};
     st.amax = bx == INT32_MAX ? 0 : bx;
     st.m = -INFINITY;
     st.mq = -INFINITY;
-    if (bv == -INFINITY) bad = 1;
-    if (sampling) {
-        const float M = mx * c;
-        float acc = 0.f;
-        if (M > -INFINITY && M < INFINITY)
-            for (int32_t l = threadIdx.x; l < W; l += kCfgThreads) acc += exp2f(fmaf(m[l], c, -M));
-        st.m = M;
-        st.s = bsum<kCfgThreads>(acc, rf);
-    }
     float tvv = NAN;
-    if (has_draft) {
-        const char* d = A.dbase + (((static_cast<int64_t>(r) * k + j) * S) + s) * A.dstride;
-        float dm = -INFINITY;
-        for (int32_t l = threadIdx.x; l < W; l += kCfgThreads) {
-            float v = load_any(d, l, A.desize);
-            if (v != v || v == INFINITY) bad = 1;
-            v = v != v ? -INFINITY : v;
-            y[l] = v;
-            dm = fmaxf(dm, v);
-        }
-        dm = bmax<kCfgThreads>(dm, rf);
-        const float Mq = dm * c;
-        float acc = 0.f;
-        if (Mq > -INFINITY && Mq < INFINITY)
-            for (int32_t l = threadIdx.x; l < W; l += kCfgThreads) acc += exp2f(fmaf(y[l], c, -Mq));
-        const float Sq = bsum<kCfgThreads>(acc, rf);
-        st.mq = Mq;
-        st.sq = Sq;
-        if (dm == -INFINITY) bad = 1;
-        // TV = sum max(0, q - p) (= 1/2 sum |p - q| since both sum to 1)
-        const float invS = 1.f / st.s, invSq = 1.f / Sq;
-        float a = 0.f;
-        for (int32_t l = threadIdx.x; l < W; l += kCfgThreads) {
-            const float p = exp2f(fmaf(m[l], c, -st.m)) * invS;
-            const float q = exp2f(fmaf(y[l], c, -Mq)) * invSq;
-            a += fmaxf(q - p, 0.f);
-        }
-        tvv = bsum<kCfgThreads>(a, rf);
-        const int32_t xl = A.draft[(static_cast<int64_t>(r) * k + j) * S + s] - A.shape.id_base[s];
-        int32_t acc_ok = 0;
-        uint32_t off = 0;
-        if (xl >= 0 && xl < W) {
-            const float p = exp2f(fmaf(m[xl], c, -st.m)) * invS;
-            const float q = exp2f(fmaf(y[xl], c, -Mq)) * invSq;
-            if (q > 0.f) {
-                const uint4 w = philox_block(philox_key(A.seeds[r]), 0u, static_cast<uint32_t>(j * S + s), kTagAccept);
-                acc_ok = uniform_from_word(w.x) < __fdiv_rn(p, q) ? 1 : 0;
-            } else {
-                off = kCfgOffSupport;
+    if (sampling && !bad) {
+        st.m = tm;
+        st.s = sm;
+        if (has_draft) {
+            st.mq = dm;
+            st.sq = sq;
+            // ---- pass 2: TV and p, q at the drafted id ----
+            const int32_t xl = A.draft[(static_cast<int64_t>(r) * k + j) * S + s] - A.shape.id_base[s];
+            const unsigned long long nm2 = pack2(-tm, -tm), nd2 = pack2(-dm, -dm);
+            const unsigned long long iS2 = pack2(1.f / sm, 1.f / sm), iQ2 = pack2(1.f / sq, 1.f / sq);
+            unsigned long long t2 = 0ull;
+            float pxl = 0.f, qxl = 0.f;
+            load(0);
+            for (int32_t b = 0; b < nb; ++b) {
+                unsigned long long m2[kP], y2[kP];
+                merge(b, m2);
+#pragma unroll
+                for (int i = 0; i < kG; ++i)
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) y2[4 * i + h] = grp_pair<DD>(yg[i], h);
+                if (b + 1 < nb) load(b + 1);
+#pragma unroll
+                for (int p = 0; p < kP; ++p) {
+                    float a0, a1, b0, b1;
+                    unpack2(fma2(m2[p], c2, nm2), a0, a1);
+                    unpack2(fma2(y2[p], c2, nd2), b0, b1);
+                    const unsigned long long p2 = mul2(pack2(ex2(a0), ex2(a1)), iS2);
+                    const unsigned long long q2 = mul2(pack2(ex2(b0), ex2(b1)), iQ2);
+                    float d0, d1;
+                    unpack2(sub2(q2, p2), d0, d1);
+                    const int32_t x = 8 * (lane + 32 * (kG * b + p / 4)) + 2 * (p % 4);
+                    // ids beyond W hold p = 0 and q of a -inf logit = 0
+                    t2 = add2(t2, pack2(fmaxf(d0, 0.f), fmaxf(d1, 0.f)));
+                    if ((xl & ~1) == x) {
+                        float p0, p1, q0, q1;
+                        unpack2(p2, p0, p1);
+                        unpack2(q2, q0, q1);
+                        pxl = (xl & 1) ? p1 : p0;
+                        qxl = (xl & 1) ? q1 : q0;
+                    }
+                }
             }
+            float t;
+            {
+                float a0, a1;
+                unpack2(t2, a0, a1);
+                t = a0 + a1;
+            }
+            t = wsum(t);
+            // the lane that saw xl holds p and q there; the others hold 0
+            pxl = wsum(pxl);
+            qxl = wsum(qxl);
+            tvv = t;
+            int32_t acc_ok = 0;
+            if (xl >= 0 && xl < W) {
+                if (qxl > 0.f) {
+                    const uint4 w4 = philox_block(philox_key(A.seeds[r]), 0u, static_cast<uint32_t>(j * S + s),
+                                                  kTagAccept);
+                    acc_ok = uniform_from_word(w4.x) < __fdiv_rn(pxl, qxl) ? 1 : 0;
+                } else {
+                    st.flags |= kCfgOffSupport;
+                }
+            }
+            st.accept = acc_ok;
         }
-        st.accept = acc_ok;
-        st.flags |= off;
     }
-    bad = bor<kCfgThreads>(bad, ru);
     if (bad) st.flags |= kCfgBad;
-    if (threadIdx.x == 0) {
+    if (lane == 0) {
         A.stats[unit] = st;
         if (A.tv && j < k) A.tv[(static_cast<int64_t>(r) * k + j) * S + s] = tvv;
     }
 }
 
-__global__ void __launch_bounds__(kCfgThreads) cfg_race_kernel(CfgArgs A)
+// One warp per (request, codebook), four per CTA: the first frame n with a rejected
+// codebook (or, greedy, a mismatching one), then codebook s's token at frame n: its
+// draft if its own test passed, else the residual race at frame n (the bonus race
+// at frame k) over the merged row rebuilt from the inputs in batches of 16 ids per
+// lane.  Codebook 0 writes accept_len; the status bits of the codebooks meet in an
+// atomic OR.
+template <int DT, int DD>
+__global__ void __launch_bounds__(32 * kCfgWarpRows, 4) cfg_race_warp_kernel(CfgArgs A)
 {
+    constexpr int kG = 2;
     pdl_wait_primary();
-    extern __shared__ __align__(16) float cfg_smem[];
-    __shared__ float rf[kCfgThreads / 32];
-    __shared__ int32_t ri[kCfgThreads / 32];
-    __shared__ uint32_t ru[kCfgThreads / 32];
+    const int lane = threadIdx.x & 31;
     const int32_t S = A.shape.S, W = A.shape.W, k = A.k;
-    const int32_t r = static_cast<int32_t>(blockIdx.x / S);
-    const int32_t s = static_cast<int32_t>(blockIdx.x - static_cast<int64_t>(r) * S);
+    const int64_t pairs_rs = static_cast<int64_t>(A.R) * S;
+    const int64_t rs_id = static_cast<int64_t>(blockIdx.x) * kCfgWarpRows + (threadIdx.x >> 5);
+    if (rs_id >= pairs_rs) return;  // whole warps only
+    const int32_t r = static_cast<int32_t>(rs_id / S);
+    const int32_t s = static_cast<int32_t>(rs_id - static_cast<int64_t>(r) * S);
     const float T = A.temp[r];
     const CfgStat* st = A.stats + static_cast<int64_t>(r) * (k + 1) * S;
     const int32_t* d = A.draft + static_cast<int64_t>(r) * k * S;
 
+    // ---- the request's decisions ----
     uint32_t fl = 0;
-    for (int32_t i = threadIdx.x; i < (k + 1) * S; i += kCfgThreads) fl |= st[i].flags;
-    fl = bor<kCfgThreads>(fl, ru);
+    for (int32_t i = lane; i < (k + 1) * S; i += 32) fl |= st[i].flags;
+    fl = __reduce_or_sync(0xffffffffu, fl);
     const bool bad = (fl & kCfgBad) != 0;
     const bool greedy = !(T > 0.f) || A.dbase == nullptr || bad;
-    // first frame with a failing codebook
-    int32_t n = k;
-    for (int32_t j = 0; j < k && n == k; ++j) {
-        bool all = true;
-        for (int32_t q = 0; q < S; ++q) {
-            const bool ok = greedy ? (d[j * S + q] - A.shape.id_base[q] == st[j * S + q].amax)
-                                   : st[j * S + q].accept != 0;
-            all = all && ok;
-        }
-        if (!all) n = j;
+    uint32_t nf = static_cast<uint32_t>(k);
+    for (int32_t i = lane; i < k * S; i += 32) {
+        const int32_t q = i % S;
+        const bool ok = greedy ? (d[i] - A.shape.id_base[q] == st[i].amax) : st[i].accept != 0;
+        if (!ok) nf = min(nf, static_cast<uint32_t>(i / S));
     }
-    int32_t tok_local;
+    const int32_t n = static_cast<int32_t>(__reduce_min_sync(0xffffffffu, nf));
+
+    int32_t tok_local = 0;
     uint32_t status = 0;
-    const CfgStat& sn = st[n * S + s];
+    const CfgStat sn = st[n * S + s];
     if (greedy) {
         tok_local = sn.amax;
     } else if (n < k && sn.accept) {
@@ -298,90 +426,111 @@ __global__ void __launch_bounds__(kCfgThreads) cfg_race_kernel(CfgArgs A)
         // race at frame n: residual max(0, p - q) or the bonus p
         const bool residual = n < k;
         const float c = kLog2eC / T;
-        float* m = cfg_smem;
-        float* y = cfg_smem + W;
-        merge_row(A, (static_cast<int64_t>(r) * (k + 1) + n) * S + s, s, m);
-        if (residual) {
-            const char* dr = A.dbase + ((static_cast<int64_t>(r) * k + n) * S + s) * A.dstride;
-            for (int32_t l = threadIdx.x; l < W; l += kCfgThreads) {
-                float v = load_any(dr, l, A.desize);
-                y[l] = v != v ? -INFINITY : v;
-            }
-        }
-        __syncthreads();
-        const float invS = 1.f / sn.s, invSq = residual ? 1.f / sn.sq : 0.f;
+        const unsigned long long w2 = pack2(A.shape.w, A.shape.w), c2 = pack2(c, c);
+        const unsigned long long nm2 = pack2(-sn.m, -sn.m), nd2 = pack2(-sn.mq, -sn.mq);
+        const unsigned long long iS2 = pack2(1.f / sn.s, 1.f / sn.s);
+        const unsigned long long iQ2 = residual ? pack2(1.f / sn.sq, 1.f / sn.sq) : 0ull;
+        const int64_t row = (static_cast<int64_t>(r) * (k + 1) + n) * S + s;
+        const int64_t off = row * A.stride + static_cast<int64_t>(A.shape.data_off[s]) * (DT == SV_BF16 ? 2 : 4);
+        const char* cp = A.cbase + off;
+        const char* up = A.ubase + off;
+        const char* dp = residual ? A.dbase + ((static_cast<int64_t>(r) * k + n) * S + s) * A.dstride : nullptr;
+        const bool cvec = A.cvec != 0, dvec = A.dvec != 0;
+        const int32_t nb = ((W + 7) / 8 + 32 * kG - 1) / (32 * kG);
         const PhiloxKey key = philox_key(A.seeds[r]);
-        const uint32_t row = static_cast<uint32_t>(n * S + s);
+        const uint32_t prow = static_cast<uint32_t>(n * S + s);
         const uint32_t tag = residual ? kTagResidual : kTagBonus;
-        float best = INFINITY;
-        int32_t bx = INT32_MAX;
-        for (int32_t g = threadIdx.x; g < (W + 3) / 4; g += kCfgThreads) {
-            const uint4 w4 = philox_block(key, static_cast<uint32_t>(g), row, tag);
-            const uint32_t words[4] = {w4.x, w4.y, w4.z, w4.w};
+        for (int pass = 0; pass < 2; ++pass) {  // pass 1: no residual mass, draw from p
+            const bool wres = residual && pass == 0;
+            float best = INFINITY;
+            int32_t bx = INT32_MAX;
+            for (int32_t b = 0; b < nb; ++b) {
+                Grp<DT> cg[kG], ug[kG];
+                Grp<DD> yg[kG];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int32_t l = 4 * g + e;
-                if (l >= W) break;
-                float wt = exp2f(fmaf(m[l], c, -sn.m)) * invS;
-                if (residual) wt -= exp2f(fmaf(y[l], c, -sn.mq)) * invSq;
-                if (!(wt > 0.f)) continue;
-                const float v = one_minus_uniform_from_word(words[e]);
-                if (!(v < best * wt)) continue;
-                const float key2 = __fdiv_rn(-log1pf(-v), wt);
-                if (key2 < best) {
-                    best = key2;
-                    bx = l;
+                for (int i = 0; i < kG; ++i) {
+                    const int32_t e0 = 8 * (lane + 32 * (kG * b + i));
+                    ld_grp<DT>(cp, e0, W, cvec, cg[i]);
+                    ld_grp<DT>(up, e0, W, cvec, ug[i]);
+                    if (wres) ld_grp<DD>(dp, e0, W, dvec, yg[i]);
                 }
-            }
-        }
-        float nb = -best;
-        bargmax<kCfgThreads>(nb, bx, rf, ri);
-        if (bx == INT32_MAX) {
-            // no positive residual: draw from p with the same uniforms
-            status |= SV_ST_RESIDUAL_ZERO;
-            best = INFINITY;
-            bx = INT32_MAX;
-            for (int32_t g = threadIdx.x; g < (W + 3) / 4; g += kCfgThreads) {
-                const uint4 w4 = philox_block(key, static_cast<uint32_t>(g), row, tag);
-                const uint32_t words[4] = {w4.x, w4.y, w4.z, w4.w};
-                for (int e = 0; e < 4; ++e) {
-                    const int32_t l = 4 * g + e;
-                    if (l >= W) break;
-                    const float wt = exp2f(fmaf(m[l], c, -sn.m)) * invS;
-                    if (!(wt > 0.f)) continue;
-                    const float key2 = __fdiv_rn(-log1pf(-one_minus_uniform_from_word(words[e])), wt);
-                    if (key2 < best) {
-                        best = key2;
-                        bx = l;
+#pragma unroll
+                for (int i = 0; i < kG; ++i) {
+                    const int32_t e0 = 8 * (lane + 32 * (kG * b + i));
+                    if (e0 >= W) continue;
+                    float wt[8];
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const unsigned long long u2 = grp_pair<DT>(ug[i], h);
+                        const unsigned long long m2 = fma2(w2, sub2(grp_pair<DT>(cg[i], h), u2), u2);
+                        float a0, a1;
+                        unpack2(fma2(m2, c2, nm2), a0, a1);
+                        unsigned long long p2 = mul2(pack2(ex2(a0), ex2(a1)), iS2);
+                        if (wres) {
+                            float b0, b1;
+                            unpack2(fma2(grp_pair<DD>(yg[i], h), c2, nd2), b0, b1);
+                            p2 = sub2(p2, mul2(pack2(ex2(b0), ex2(b1)), iQ2));
+                        }
+                        unpack2(p2, wt[2 * h], wt[2 * h + 1]);
+                    }
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const uint4 w4 = philox_block(key, static_cast<uint32_t>((e0 >> 2) + hh), prow, tag);
+                        const uint32_t words[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int32_t l = e0 + 4 * hh + e;
+                            const float wv = wt[4 * hh + e];
+                            if (l >= W || !(wv > 0.f)) continue;  // NaN merged logits never win
+                            const float v = one_minus_uniform_from_word(words[e]);
+                            if (!(v < best * wv)) continue;  // E = -ln(1 - v) >= v
+                            const float key2 = __fdiv_rn(-log1pf(-v), wv);
+                            if (key2 < best) {  // ascending ids within the lane
+                                best = key2;
+                                bx = l;
+                            }
+                        }
                     }
                 }
             }
-            nb = -best;
-            bargmax<kCfgThreads>(nb, bx, rf, ri);
+            // (key, lowest id) minimum over the warp
+            float nb2 = bx == INT32_MAX ? -INFINITY : -best;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, nb2, o);
+                const int32_t ox = __shfl_xor_sync(0xffffffffu, bx, o);
+                if (ov > nb2 || (ov == nb2 && ox < bx)) {
+                    nb2 = ov;
+                    bx = ox;
+                }
+            }
+            if (bx != INT32_MAX || !residual) {
+                tok_local = bx == INT32_MAX ? 0 : bx;
+                break;
+            }
+            status |= SV_ST_RESIDUAL_ZERO;
         }
-        tok_local = bx == INT32_MAX ? 0 : bx;
         if (residual && (sn.flags & kCfgOffSupport)) status |= SV_ST_OFF_SUPPORT;
     }
     // tokens of codebook s for every frame
     int32_t* out = A.tokens + static_cast<int64_t>(r) * (k + 1) * S;
-    for (int32_t j = threadIdx.x; j <= k; j += kCfgThreads)
+    for (int32_t j = lane; j <= k; j += 32)
         out[j * S + s] = j < n ? d[j * S + s] : (j == n ? A.shape.id_base[s] + tok_local : -1);
     if (greedy && A.tv) {
-        for (int32_t j = threadIdx.x; j < k; j += kCfgThreads) A.tv[(static_cast<int64_t>(r) * k + j) * S + s] = NAN;
+        for (int32_t j = lane; j < k; j += 32) A.tv[(static_cast<int64_t>(r) * k + j) * S + s] = NAN;
     }
-    // request-level status: the OR over codebooks goes through an atomic on status
     uint32_t st_bits = status;
-    for (int32_t j = threadIdx.x; j < k; j += kCfgThreads) {
+    for (int32_t j = lane; j < k; j += 32) {
         const int32_t l = d[j * S + s] - A.shape.id_base[s];
         if (l < 0 || l >= W) st_bits |= SV_ST_TOKEN_RANGE;
     }
-    st_bits = bor<kCfgThreads>(st_bits, ru);
-    if (s == 0) {
-        if (bad) st_bits |= SV_ST_BAD_LOGITS;
-        if (T < 0.f || T != T) st_bits |= SV_ST_BAD_TEMP;
-    }
-    if (threadIdx.x == 0) {
-        if (s == 0) A.accept_len[r] = n;
+    st_bits = __reduce_or_sync(0xffffffffu, st_bits);
+    if (lane == 0) {
+        if (s == 0) {
+            if (bad) st_bits |= SV_ST_BAD_LOGITS;
+            if (T < 0.f || T != T) st_bits |= SV_ST_BAD_TEMP;
+            A.accept_len[r] = n;
+        }
         if (A.status) atomicOr(reinterpret_cast<unsigned int*>(A.status + r), st_bits);
     }
 }
@@ -398,6 +547,27 @@ size_t cfg_workspace_bytes(int64_t R, int32_t k, int32_t S, int32_t W)
     return static_cast<size_t>(R * (k + 1) * S) * sizeof(CfgStat) + 256;
 }
 
+template <int DT, int DD>
+static cudaError_t launch_cfg_t(const CfgArgs& A, int32_t R, int32_t k, cudaStream_t stream)
+{
+    cudaError_t e;
+    const int64_t units = static_cast<int64_t>(R) * (k + 1) * A.shape.S;
+    cfg_rows_warp_kernel<DT, DD>
+        <<<static_cast<unsigned>((units + kCfgWarpRows - 1) / kCfgWarpRows), 32 * kCfgWarpRows, 0, stream>>>(A);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((static_cast<int64_t>(R) * A.shape.S + kCfgWarpRows - 1) / kCfgWarpRows));
+    cfg.blockDim = dim3(32 * kCfgWarpRows);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, cfg_race_warp_kernel<DT, DD>, A);
+}
+
 cudaError_t launch_cfg_merge_sample(const Rows& cond, const Rows& uncond, const CfgShape& shape,
                                     const Rows* draft_logits, int32_t R, int32_t k,
                                     const int32_t* draft, const uint64_t* seeds,
@@ -410,10 +580,13 @@ cudaError_t launch_cfg_merge_sample(const Rows& cond, const Rows& uncond, const 
     A.cbase = cond.data;
     A.ubase = uncond.data;
     A.stride = cond.stride * cond.esize;
-    A.esize = cond.esize;
     A.dbase = draft_logits ? draft_logits->data : nullptr;
     A.dstride = draft_logits ? draft_logits->stride * draft_logits->esize : 0;
-    A.desize = draft_logits ? draft_logits->esize : 4;
+    // 16-byte loads: every slice start and the width in 16-byte units
+    bool cvec = cond.bulk_ok && uncond.bulk_ok && (static_cast<int64_t>(shape.W) * cond.esize) % 16 == 0;
+    for (int q = 0; q < shape.S; ++q) cvec = cvec && (static_cast<int64_t>(shape.data_off[q]) * cond.esize) % 16 == 0;
+    A.cvec = cvec;
+    A.dvec = draft_logits && draft_logits->bulk_ok && (static_cast<int64_t>(shape.W) * draft_logits->esize) % 16 == 0;
     A.shape = shape;
     A.R = R;
     A.k = k;
@@ -425,30 +598,17 @@ cudaError_t launch_cfg_merge_sample(const Rows& cond, const Rows& uncond, const 
     A.tv = tv;
     A.status = status;
     A.stats = static_cast<CfgStat*>(workspace);
-    const size_t smem = static_cast<size_t>(shape.W) * 2 * sizeof(float);
     cudaError_t e;
-    for (const void* f : {reinterpret_cast<const void*>(cfg_rows_kernel), reinterpret_cast<const void*>(cfg_race_kernel)}) {
-        e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-    }
     if (status) {
         cfg_clear_status_kernel<<<static_cast<unsigned>((R + 255) / 256), 256, 0, stream>>>(status, R);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    const int64_t units = static_cast<int64_t>(R) * (k + 1) * shape.S;
-    cfg_rows_kernel<<<static_cast<unsigned>(units), kCfgThreads, smem, stream>>>(A);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(R) * shape.S));
-    cfg.blockDim = dim3(kCfgThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, cfg_race_kernel, A);
+    const bool cb = cond.dtype == SV_BF16;
+    const bool db = draft_logits == nullptr || draft_logits->dtype == SV_BF16;
+    if (cb && db) return launch_cfg_t<SV_BF16, SV_BF16>(A, R, k, stream);
+    if (cb) return launch_cfg_t<SV_BF16, SV_F32>(A, R, k, stream);
+    if (db) return launch_cfg_t<SV_F32, SV_BF16>(A, R, k, stream);
+    return launch_cfg_t<SV_F32, SV_F32>(A, R, k, stream);
 }
 
 int32_t cfg_max_width() { return kCfgMaxW; }

@@ -825,48 +825,8 @@ static_assert(kFastWarps * kFastStages * 8 <= kFastHeader, "mbarriers fit the he
 constexpr int32_t kFastMaxVd = 32768;
 constexpr int kVL = kChunkElems / 8 / 32;  // 16-byte vectors per lane and chunk
 
-__device__ __forceinline__ float ex2(float x)
-{
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
 
-// two fp32 values in one 64-bit register, for the packed f32x2 instructions
-__device__ __forceinline__ unsigned long long pack2(float lo, float hi)
-{
-    unsigned long long r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ void unpack2(unsigned long long v, float& lo, float& hi)
-{
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c)
-{
-    unsigned long long r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b)
-{
-    unsigned long long r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b)
-{
-    unsigned long long r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
 
-// the bf16x2 word w as two fp32 values (exact) in one 64-bit register
-__device__ __forceinline__ unsigned long long bf16x2_to_f32x2(uint32_t w)
-{
-    return pack2(bf16_lo(w), bf16_hi(w));
-}
 
 // sum over the 8 bf16 values z of a vector of 2^(z c - m): packed fp32x2
 // arguments, eight independent MUFU operations, a tree of packed adds
@@ -888,21 +848,7 @@ __device__ __forceinline__ float exp_sum8(uint4 q, unsigned long long c2, unsign
     return lo + hi;
 }
 
-// maximum over the warp (all lanes take part; no NaN among the inputs)
-__device__ __forceinline__ float warp_max(float v)
-{
-    float r;
-    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-    return r;
-}
 
-// 16-byte read-only global load
-__device__ __forceinline__ uint4 ld_nc_v4(const uint4* p)
-{
-    uint4 v;
-    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-    return v;
-}
 
 // this lane's register groups of a chunk's padded support entries [p0, p1)
 __device__ __forceinline__ void load_pairs(const SampleArgs& A, int32_t p0, int32_t p1, int lane, uint4* pg)

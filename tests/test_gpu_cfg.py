@@ -32,6 +32,8 @@ def _oracle(w, greedy=False):
     (5, 2, 3, 1000, torch.float32, 0.8),     # odd codebook width
     (4, 6, 1, 257, torch.bfloat16, 1.5),
     (3, 3, 16, 2048, torch.bfloat16, 0.6),   # the largest S
+    (3, 2, 2, 9000, torch.bfloat16, 1.0),    # wider than 4096: more threads per row
+    (2, 2, 2, 16384, torch.float32, 0.9),    # the widest codebook
 ])
 def test_cfg_sampling(sv, R, k, S, W, dtype, T):
     w = workloads.cfg_batch(R, k, S, W, 3.0, T, dtype, seed=R * 31 + S)
