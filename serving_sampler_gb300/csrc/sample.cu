@@ -1063,16 +1063,17 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                 // G[draft id] = z at the chunk offset for every entry of the lane's groups; a
                 // padding entry writes the spare slot G[Vd], which nothing reads
                 const uint16_t* zs = reinterpret_cast<const uint16_t*>(st);
+                const uint32_t zs_a = smem_addr(st), g_a = smem_addr(G);
                 const bool here = xj >= x0 && xj < x0 + static_cast<int32_t>(nb / 2);
 #pragma unroll
                 for (int t = 0; t < kPairRegs; ++t) {
-                    const uint32_t pe[4] = {pg[t].x, pg[t].y, pg[t].z, pg[t].w};
-                    uint16_t zv[4];
+                    if (p0 + 4 * (lane + 32 * t) < p1) {  // whole groups of four
+                        const uint32_t pe[4] = {pg[t].x, pg[t].y, pg[t].z, pg[t].w};
+                        uint16_t zv[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) zv[e] = zs[pe[e] & (kChunkElems - 1)];
-                    if (p0 + 4 * (lane + 32 * t) < p1) {
+                        for (int e = 0; e < 4; ++e) zv[e] = lds_u16(zs_a + ((pe[e] & (kChunkElems - 1)) << 1));
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) G[pe[e] >> 16] = zv[e];
+                        for (int e = 0; e < 4; ++e) sts_u16(g_a + ((pe[e] >> 15) & ~1u), zv[e]);
                     }
                 }
                 // groups beyond this lane's registers (chunks denser than 512 entries)
@@ -1080,7 +1081,8 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                     const uint4 q4 = ld_nc_v4(reinterpret_cast<const uint4*>(A.plan.pairs + g));
                     const uint32_t pe[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) G[pe[e] >> 16] = zs[pe[e] & (kChunkElems - 1)];
+                    for (int e = 0; e < 4; ++e)
+                        sts_u16(g_a + ((pe[e] >> 15) & ~1u), lds_u16(zs_a + ((pe[e] & (kChunkElems - 1)) << 1)));
                 }
                 if (here) {  // the draft token: its logit and its draft id
                     const uint32_t xoff = static_cast<uint32_t>(xj - x0);
@@ -1272,7 +1274,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
         if (u.has_draft) {
             const float invS = 1.f / S, invSq = 1.f / Sq;
             const unsigned long long c2m = pack2(c, c), nM = pack2(-M, -M), nMq = pack2(-Mq, -Mq);
-            const unsigned long long iS = pack2(invS, invS), iSq = pack2(invSq, invSq);
+            const unsigned long long niS = pack2(-invS, -invS), iSq = pack2(invSq, invSq);
             const int32_t jdx = jdx_shared;
             const uint4* gv = reinterpret_cast<const uint4*>(G);
             float a = 0.f;
@@ -1295,24 +1297,21 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                     float qv[8], dv[8];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        // q and p of two ids at once: 2^(y c - Mq) / Sq and 2^(z c - M) / S
+                        // q and p of two ids at once: q - p = 2^(y c - Mq) / Sq - 2^(z c - M) / S
                         const unsigned long long ty = fma2(bf16x2_to_f32x2(yw[e]), c2m, nMq);
                         const unsigned long long tz = fma2(bf16x2_to_f32x2(gw[e]), c2m, nM);
                         float y0, y1, z0, z1;
                         unpack2(ty, y0, y1);
                         unpack2(tz, z0, z1);
-                        float q0, q1, p0, p1;
-                        unpack2(mul2(pack2(ex2(y0), ex2(y1)), iSq), q0, q1);
-                        unpack2(mul2(pack2(ex2(z0), ex2(z1)), iS), p0, p1);
-                        qv[2 * e] = q0;
-                        qv[2 * e + 1] = q1;
-                        dv[2 * e] = q0 - p0;
-                        dv[2 * e + 1] = q1 - p1;
+                        const unsigned long long eq = pack2(ex2(y0), ex2(y1));
+                        const unsigned long long np = mul2(pack2(ex2(z0), ex2(z1)), niS);
+                        unpack2(eq, qv[2 * e], qv[2 * e + 1]);  // q up to the factor 1 / Sq
+                        unpack2(fma2(eq, iSq, np), dv[2 * e], dv[2 * e + 1]);
                     }
                     if (v == (jdx >> 3)) {  // this vector holds the draft token's draft id
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
-                            if (e == (jdx & 7)) qx_shared = qv[e];
+                            if (e == (jdx & 7)) qx_shared = qv[e] * invSq;
                     }
                     a += ((fmaxf(dv[0], 0.f) + fmaxf(dv[1], 0.f)) + (fmaxf(dv[2], 0.f) + fmaxf(dv[3], 0.f))) +
                          ((fmaxf(dv[4], 0.f) + fmaxf(dv[5], 0.f)) + (fmaxf(dv[6], 0.f) + fmaxf(dv[7], 0.f)));

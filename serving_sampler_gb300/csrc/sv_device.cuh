@@ -179,6 +179,18 @@ __device__ __forceinline__ bool argmax_better(float v, int32_t i, const ArgMax& 
     return v > a.v || (v == a.v && i < a.i);
 }
 
+// ---- shared-memory 16-bit accesses at 32-bit shared addresses ----
+__device__ __forceinline__ uint16_t lds_u16(uint32_t addr)
+{
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ void sts_u16(uint32_t addr, uint16_t v)
+{
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
 // ---- fp32 pairs, exponentials, loads and warp maxima shared by the kernels ----
 __device__ __forceinline__ float ex2(float x)
 {
