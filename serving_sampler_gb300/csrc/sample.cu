@@ -53,8 +53,8 @@ struct D2tPlan {
     int32_t* xs;       // [Vd] support target ids, ascending
     int32_t* js;       // [Vd] the draft id of xs[pos]
     uint32_t* pairs;   // per chunk c of kChunkElems target ids, from c * 4096: its support entries
-                       // (draft id << 16) | (x & (kChunkElems - 1)) in bank-spread groups of 32
-                       // (see d2t_group_kernel); empty slots hold (Vd << 16), a spare G slot
+                       // (2 draft id << 16) | 2 (x & (kChunkElems - 1)) in bank-spread groups of 32
+                       // (see d2t_group_kernel); empty slots hold (2 Vd << 16), a spare G slot
     int32_t* chunk;    // [V / kChunkElems + 2] support rank at every multiple of kChunkElems
     int32_t* pcount;   // [V / kChunkElems + 2] slots of every chunk in pairs (from c * kMaxGroups * 32)
     uint16_t* jmap;    // [V] draft id of every target id, 0xFFFF off the support
@@ -336,8 +336,10 @@ __global__ void __launch_bounds__(kPlanThreads)
 // fit over the chunk's entries in ascending x.  Group g of chunk c occupies
 // slots c * kMaxGroups * 32 + 128 (g / 4) + 4 pos + (g % 4), pos = 0..31,
 // which is the layout the row pass reads as one 16-byte word per lane for four
-// groups; slots without an entry hold (Vd << 16); pcount[c] = 32 x the groups
-// rounded up to 4.  One CTA of one warp per chunk.
+// groups; an entry is (2 j << 16) | 2 (x mod 2048), the byte offsets of the
+// store and of the load (used by the row pass only, where j < 32768); slots
+// without an entry hold (2 Vd << 16); pcount[c] = 32 x the groups rounded up to
+// 4.  One CTA of one warp per chunk.
 namespace {
 constexpr int kMaxGroups = 128;  // 128 x 32 slots >= the 2048 entries a chunk can have
 constexpr int kBankCap = 2;
@@ -392,12 +394,12 @@ __global__ void __launch_bounds__(32) d2t_group_kernel(int32_t Vd, int32_t V, D2
     }
     const int32_t nslots = 32 * ((ng + 3) & ~3);
     uint32_t* out = pl.pairs + static_cast<int64_t>(c) * kMaxGroups * 32;
-    for (int32_t i = lane; i < nslots; i += 32) out[i] = static_cast<uint32_t>(Vd) << 16;
+    for (int32_t i = lane; i < nslots; i += 32) out[i] = static_cast<uint32_t>(2 * Vd) << 16;
     __syncwarp();
     for (int32_t p = p0 + lane; p < p1; p += 32) {
         const uint32_t sl = slot_of[p - p0];
         if (sl != 0xFFFFu)
-            out[sl] = (static_cast<uint32_t>(pl.js[p]) << 16) | static_cast<uint32_t>(pl.xs[p] - c * kChunkElems);
+            out[sl] = (static_cast<uint32_t>(2 * pl.js[p]) << 16) | static_cast<uint32_t>(2 * (pl.xs[p] - c * kChunkElems));
     }
     if (lane == 0) pl.pcount[c] = nslots;
 }
@@ -1059,51 +1061,6 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                 p1 = p0 + ctab[cidx];
                 if (pg_for != cidx) load_pairs(A, p0, p1, lane, pg);  // not prefetched
             }
-            if (scatter) {
-                // G[draft id] = z at the chunk offset for every entry of the lane's groups; a
-                // padding entry writes the spare slot G[Vd], which nothing reads
-                const uint16_t* zs = reinterpret_cast<const uint16_t*>(st);
-                const uint32_t zs_a = smem_addr(st), g_a = smem_addr(G);
-                const bool here = xj >= x0 && xj < x0 + static_cast<int32_t>(nb / 2);
-#pragma unroll
-                for (int t = 0; t < kPairRegs; ++t) {
-                    if (p0 + 4 * (lane + 32 * t) < p1) {  // whole groups of four
-                        const uint32_t pe[4] = {pg[t].x, pg[t].y, pg[t].z, pg[t].w};
-                        uint16_t zv[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) zv[e] = lds_u16(zs_a + ((pe[e] & (kChunkElems - 1)) << 1));
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) sts_u16(g_a + ((pe[e] >> 15) & ~1u), zv[e]);
-                    }
-                }
-                // groups beyond this lane's registers (chunks denser than 512 entries)
-                for (int32_t g = p0 + 4 * 32 * kPairRegs + 4 * lane; g < p1; g += 4 * 32) {
-                    const uint4 q4 = ld_nc_v4(reinterpret_cast<const uint4*>(A.plan.pairs + g));
-                    const uint32_t pe[4] = {q4.x, q4.y, q4.z, q4.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        sts_u16(g_a + ((pe[e] >> 15) & ~1u), lds_u16(zs_a + ((pe[e] & (kChunkElems - 1)) << 1)));
-                }
-                if (here) {  // the draft token: its logit and its draft id
-                    const uint32_t xoff = static_cast<uint32_t>(xj - x0);
-                    if (lane == 0) zx_shared = __uint_as_float(static_cast<uint32_t>(zs[xoff]) << 16);
-                    for (int32_t g = p0 + lane; g < p1; g += 32) {
-                        const uint32_t pe = A.plan.pairs[g];
-                        if ((pe & (kChunkElems - 1)) == xoff && static_cast<int32_t>(pe >> 16) < A.Vd)
-                            jdx_shared = static_cast<int32_t>(pe >> 16);
-                    }
-                }
-            }
-            {
-                // the support entries of this warp's next chunk, if it is a target chunk of this
-                // unit: in flight during this chunk's maxima and exponentials
-                const int32_t qn = q + kFastWarps;
-                pg_for = -1;
-                if (u.has_draft && qn < u.n && qn >= u.nd) {
-                    pg_for = qn - u.nd;
-                    load_pairs(A, pg_for * (kMaxGroups * 32), pg_for * (kMaxGroups * 32) + ctab[pg_for], lane, pg);
-                }
-            }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 // half the lane's vectors: independent loads and max trees, one update of the
@@ -1180,6 +1137,60 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                         rs_ += acc[0];
                         csum += acc[0];
                     }
+                }
+            }
+            if (scatter) {
+                // G[draft id] = z at the chunk offset for every entry of the lane's groups; a
+                // padding entry writes the spare slot G[Vd], which nothing reads
+                const uint16_t* zs = reinterpret_cast<const uint16_t*>(st);
+                const uint32_t zs_a = smem_addr(st), g_a = smem_addr(G);
+                const bool here = xj >= x0 && xj < x0 + static_cast<int32_t>(nb / 2);
+#pragma unroll
+                for (int t = 0; t < kPairRegs; ++t) {
+                    if (p0 + 4 * (lane + 32 * t) < p1) {  // whole groups of four
+                        const uint32_t pe[4] = {pg[t].x, pg[t].y, pg[t].z, pg[t].w};
+                        uint32_t zv[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) zv[e] = lds_u16(zs_a + (pe[e] & 0xFFFFu));
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) sts_u16(g_a + (pe[e] >> 16), zv[e]);
+                    }
+                }
+                // groups beyond this lane's registers (chunks denser than 512 entries)
+                for (int32_t g = p0 + 4 * 32 * kPairRegs + 4 * lane; g < p1; g += 4 * 32) {
+                    const uint4 q4 = ld_nc_v4(reinterpret_cast<const uint4*>(A.plan.pairs + g));
+                    const uint32_t pe[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sts_u16(g_a + (pe[e] >> 16), lds_u16(zs_a + (pe[e] & 0xFFFFu)));
+                }
+                if (here) {  // the draft token: its logit and its draft id (from the registers)
+                    const uint32_t xoff = static_cast<uint32_t>(xj - x0);
+                    if (lane == 0) zx_shared = __uint_as_float(static_cast<uint32_t>(zs[xoff]) << 16);
+#pragma unroll
+                    for (int t = 0; t < kPairRegs; ++t) {
+                        if (p0 + 4 * (lane + 32 * t) < p1) {
+                            const uint32_t pe[4] = {pg[t].x, pg[t].y, pg[t].z, pg[t].w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                if ((pe[e] & 0xFFFFu) == 2 * xoff && static_cast<int32_t>(pe[e] >> 17) < A.Vd)
+                                    jdx_shared = static_cast<int32_t>(pe[e] >> 17);
+                        }
+                    }
+                    for (int32_t g = p0 + 4 * 32 * kPairRegs + lane; g < p1; g += 32) {  // beyond the registers
+                        const uint32_t pe = A.plan.pairs[g];
+                        if ((pe & 0xFFFFu) == 2 * xoff && static_cast<int32_t>(pe >> 17) < A.Vd)
+                            jdx_shared = static_cast<int32_t>(pe >> 17);
+                    }
+                }
+            }
+            {
+                // the support entries of this warp's next chunk, if it is a target chunk of this
+                // unit: in flight until that chunk's scatter
+                const int32_t qn = q + kFastWarps;
+                pg_for = -1;
+                if (u.has_draft && qn < u.n && qn >= u.nd) {
+                    pg_for = qn - u.nd;
+                    load_pairs(A, pg_for * (kMaxGroups * 32), pg_for * (kMaxGroups * 32) + ctab[pg_for], lane, pg);
                 }
             }
             if (!is_draft && u.sampling) {
@@ -1914,7 +1925,7 @@ size_t fast_smem_bytes(int32_t V, int32_t Vd)
 bool fast_path_ok(const Rows& t, const Rows& d, bool identity)
 {
     return !identity && t.dtype == SV_BF16 && d.dtype == SV_BF16 && t.bulk_ok && d.bulk_ok && d.data != nullptr &&
-           t.width % 8 == 0 && d.width % 8 == 0 && d.width <= kFastMaxVd &&
+           t.width % 8 == 0 && d.width % 8 == 0 && d.width < kFastMaxVd &&  // 2 Vd fits 16 bits
            fast_smem_bytes(t.width, d.width) <= 227 * 1024;
 }
 

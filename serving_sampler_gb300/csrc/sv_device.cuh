@@ -179,16 +179,17 @@ __device__ __forceinline__ bool argmax_better(float v, int32_t i, const ArgMax& 
     return v > a.v || (v == a.v && i < a.i);
 }
 
-// ---- shared-memory 16-bit accesses at 32-bit shared addresses ----
-__device__ __forceinline__ uint16_t lds_u16(uint32_t addr)
+// ---- shared-memory 16-bit accesses at 32-bit shared addresses, values in 32-bit registers ----
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr)
 {
-    uint16_t v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    uint32_t v;
+    asm("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr));
     return v;
 }
-__device__ __forceinline__ void sts_u16(uint32_t addr, uint16_t v)
+// no memory clobber: callers order these stores against readers with a barrier
+__device__ __forceinline__ void sts_u16(uint32_t addr, uint32_t v)
 {
-    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "r"(v));
 }
 
 // ---- fp32 pairs, exponentials, loads and warp maxima shared by the kernels ----
