@@ -27,7 +27,7 @@ MAX_K, MAX_S = 256, 16
 # kernels one call launches: verify_sample with a prebuilt d2t plan (or the identity map)
 # launches 2, and 2 more when it builds the plan itself; d2t_plan launches 2
 LAUNCHES = {"verify_greedy": 2, "verify_sample": 2, "verify_sample_plan_in_call": 4, "d2t_plan": 2,
-            "cfg_merge_sample": 3, "accept_scan": 1}
+            "cfg_merge_sample": 2, "accept_scan": 1}
 
 
 class SpecVerifyError(RuntimeError):

@@ -12,11 +12,11 @@
 //                  sum-exp at T and the draft row's; pass 2 (the slices again,
 //                  from L2) TV = sum max(0, q - p) and p, q at the drafted id;
 //                  then the accept test (Philox row j * S + s).
-// cfg_race_warp_kernel  one warp per (request, codebook): the first frame n
-//                  with a rejected codebook, then for codebook s its draft if
-//                  its own test passed, else the residual race at frame n (or
-//                  the bonus race at frame k) over the merged row rebuilt from
-//                  the inputs.  Codebook 0 also writes accept_len.
+// cfg_race_kernel  one CTA of four warps per (request, codebook): the first
+//                  frame n with a rejected codebook, then for codebook s its
+//                  draft if its own test passed, else the residual race at
+//                  frame n (or the bonus race at frame k) over the merged row
+//                  rebuilt from the inputs.  Codebook 0 also writes accept_len.
 #include <algorithm>
 #include <cfloat>
 #include <climits>
@@ -376,44 +376,59 @@ __global__ void __launch_bounds__(32 * kCfgWarpRows, 4) cfg_rows_warp_kernel(Cfg
     if (lane == 0) {
         A.stats[unit] = st;
         if (A.tv && j < k) A.tv[(static_cast<int64_t>(r) * k + j) * S + s] = tvv;
+        if (A.status && j == 0 && s == 0) A.status[r] = 0;  // the race kernel ORs the codebooks' bits
     }
 }
 
-// One warp per (request, codebook), four per CTA: the first frame n with a rejected
-// codebook (or, greedy, a mismatching one), then codebook s's token at frame n: its
-// draft if its own test passed, else the residual race at frame n (the bonus race
-// at frame k) over the merged row rebuilt from the inputs in batches of 16 ids per
-// lane.  Codebook 0 writes accept_len; the status bits of the codebooks meet in an
-// atomic OR.
+// One CTA of four warps per (request, codebook): warp 0 finds the first frame n
+// with a rejected codebook (or, greedy, a mismatching one); then codebook s's token
+// at frame n: its draft if its own test passed, else the residual race at frame n
+// (the bonus race at frame k) over the merged row rebuilt from the inputs, the
+// warps taking alternate batches of 16 ids per lane (the next one in flight);
+// then the codebook's tokens.  Codebook 0 writes accept_len; the codebooks' status
+// bits meet in an atomic OR on a status word the row pass zeroed.
+constexpr int kCfgRaceWarps = 4;
+
 template <int DT, int DD>
-__global__ void __launch_bounds__(32 * kCfgWarpRows, 4) cfg_race_warp_kernel(CfgArgs A)
+__global__ void __launch_bounds__(32 * kCfgRaceWarps, 4) cfg_race_kernel(CfgArgs A)
 {
     constexpr int kG = 2;
     pdl_wait_primary();
-    const int lane = threadIdx.x & 31;
+    __shared__ float red_k[kCfgRaceWarps];
+    __shared__ int32_t red_x[kCfgRaceWarps];
+    __shared__ int32_t n_s;
+    __shared__ uint32_t fl_s;
+    const int lane = threadIdx.x & 31, wq = threadIdx.x >> 5;
     const int32_t S = A.shape.S, W = A.shape.W, k = A.k;
-    const int64_t pairs_rs = static_cast<int64_t>(A.R) * S;
-    const int64_t rs_id = static_cast<int64_t>(blockIdx.x) * kCfgWarpRows + (threadIdx.x >> 5);
-    if (rs_id >= pairs_rs) return;  // whole warps only
-    const int32_t r = static_cast<int32_t>(rs_id / S);
-    const int32_t s = static_cast<int32_t>(rs_id - static_cast<int64_t>(r) * S);
+    const int32_t r = static_cast<int32_t>(blockIdx.x / S);
+    const int32_t s = static_cast<int32_t>(blockIdx.x - static_cast<int64_t>(r) * S);
     const float T = A.temp[r];
     const CfgStat* st = A.stats + static_cast<int64_t>(r) * (k + 1) * S;
     const int32_t* d = A.draft + static_cast<int64_t>(r) * k * S;
 
-    // ---- the request's decisions ----
-    uint32_t fl = 0;
-    for (int32_t i = lane; i < (k + 1) * S; i += 32) fl |= st[i].flags;
-    fl = __reduce_or_sync(0xffffffffu, fl);
-    const bool bad = (fl & kCfgBad) != 0;
-    const bool greedy = !(T > 0.f) || A.dbase == nullptr || bad;
-    uint32_t nf = static_cast<uint32_t>(k);
-    for (int32_t i = lane; i < k * S; i += 32) {
-        const int32_t q = i % S;
-        const bool ok = greedy ? (d[i] - A.shape.id_base[q] == st[i].amax) : st[i].accept != 0;
-        if (!ok) nf = min(nf, static_cast<uint32_t>(i / S));
+    // ---- the request's decisions (warp 0) ----
+    if (wq == 0) {
+        uint32_t fl = 0;
+        for (int32_t i = lane; i < (k + 1) * S; i += 32) fl |= st[i].flags;
+        fl = __reduce_or_sync(0xffffffffu, fl);
+        const bool bad0 = (fl & kCfgBad) != 0;
+        const bool greedy0 = !(T > 0.f) || A.dbase == nullptr || bad0;
+        uint32_t nf = static_cast<uint32_t>(k);
+        for (int32_t i = lane; i < k * S; i += 32) {
+            const int32_t q = i % S;
+            const bool ok = greedy0 ? (d[i] - A.shape.id_base[q] == st[i].amax) : st[i].accept != 0;
+            if (!ok) nf = min(nf, static_cast<uint32_t>(i / S));
+        }
+        nf = __reduce_min_sync(0xffffffffu, nf);
+        if (lane == 0) {
+            n_s = static_cast<int32_t>(nf);
+            fl_s = fl;
+        }
     }
-    const int32_t n = static_cast<int32_t>(__reduce_min_sync(0xffffffffu, nf));
+    __syncthreads();
+    const int32_t n = n_s;
+    const bool bad = (fl_s & kCfgBad) != 0;
+    const bool greedy = !(T > 0.f) || A.dbase == nullptr || bad;
 
     int32_t tok_local = 0;
     uint32_t status = 0;
@@ -444,16 +459,28 @@ __global__ void __launch_bounds__(32 * kCfgWarpRows, 4) cfg_race_warp_kernel(Cfg
             const bool wres = residual && pass == 0;
             float best = INFINITY;
             int32_t bx = INT32_MAX;
-            for (int32_t b = 0; b < nb; ++b) {
+            Grp<DT> ncg[kG], nug[kG];  // the next batch, in flight while one is raced
+            Grp<DD> nyg[kG];
+            auto fetch = [&](int32_t b) {
+#pragma unroll
+                for (int i = 0; i < kG; ++i) {
+                    const int32_t e0 = 8 * (lane + 32 * (kG * b + i));
+                    ld_grp<DT>(cp, e0, W, cvec, ncg[i]);
+                    ld_grp<DT>(up, e0, W, cvec, nug[i]);
+                    if (wres) ld_grp<DD>(dp, e0, W, dvec, nyg[i]);
+                }
+            };
+            if (wq < nb) fetch(wq);
+            for (int32_t b = wq; b < nb; b += kCfgRaceWarps) {
                 Grp<DT> cg[kG], ug[kG];
                 Grp<DD> yg[kG];
 #pragma unroll
                 for (int i = 0; i < kG; ++i) {
-                    const int32_t e0 = 8 * (lane + 32 * (kG * b + i));
-                    ld_grp<DT>(cp, e0, W, cvec, cg[i]);
-                    ld_grp<DT>(up, e0, W, cvec, ug[i]);
-                    if (wres) ld_grp<DD>(dp, e0, W, dvec, yg[i]);
+                    cg[i] = ncg[i];
+                    ug[i] = nug[i];
+                    yg[i] = nyg[i];
                 }
+                if (b + kCfgRaceWarps < nb) fetch(b + kCfgRaceWarps);
 #pragma unroll
                 for (int i = 0; i < kG; ++i) {
                     const int32_t e0 = 8 * (lane + 32 * (kG * b + i));
@@ -493,7 +520,7 @@ __global__ void __launch_bounds__(32 * kCfgWarpRows, 4) cfg_race_warp_kernel(Cfg
                     }
                 }
             }
-            // (key, lowest id) minimum over the warp
+            // (key, lowest id) minimum over the warp, then over the CTA
             float nb2 = bx == INT32_MAX ? -INFINITY : -best;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
@@ -504,6 +531,19 @@ __global__ void __launch_bounds__(32 * kCfgWarpRows, 4) cfg_race_warp_kernel(Cfg
                     bx = ox;
                 }
             }
+            if (lane == 0) {
+                red_k[wq] = nb2;
+                red_x[wq] = bx;
+            }
+            __syncthreads();
+            nb2 = red_k[0];
+            bx = red_x[0];
+            for (int i = 1; i < kCfgRaceWarps; ++i)
+                if (red_k[i] > nb2 || (red_k[i] == nb2 && red_x[i] < bx)) {
+                    nb2 = red_k[i];
+                    bx = red_x[i];
+                }
+            __syncthreads();  // red_* are written again by a second pass
             if (bx != INT32_MAX || !residual) {
                 tok_local = bx == INT32_MAX ? 0 : bx;
                 break;
@@ -512,7 +552,8 @@ __global__ void __launch_bounds__(32 * kCfgWarpRows, 4) cfg_race_warp_kernel(Cfg
         }
         if (residual && (sn.flags & kCfgOffSupport)) status |= SV_ST_OFF_SUPPORT;
     }
-    // tokens of codebook s for every frame
+    if (wq != 0) return;
+    // ---- codebook s's tokens for every frame; status ----
     int32_t* out = A.tokens + static_cast<int64_t>(r) * (k + 1) * S;
     for (int32_t j = lane; j <= k; j += 32)
         out[j * S + s] = j < n ? d[j * S + s] : (j == n ? A.shape.id_base[s] + tok_local : -1);
@@ -531,14 +572,8 @@ __global__ void __launch_bounds__(32 * kCfgWarpRows, 4) cfg_race_warp_kernel(Cfg
             if (T < 0.f || T != T) st_bits |= SV_ST_BAD_TEMP;
             A.accept_len[r] = n;
         }
-        if (A.status) atomicOr(reinterpret_cast<unsigned int*>(A.status + r), st_bits);
+        if (A.status && st_bits) atomicOr(reinterpret_cast<unsigned int*>(A.status + r), st_bits);
     }
-}
-
-__global__ void cfg_clear_status_kernel(int32_t* status, int32_t R)
-{
-    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (i < R) status[i] = 0;
 }
 
 size_t cfg_workspace_bytes(int64_t R, int32_t k, int32_t S, int32_t W)
@@ -559,13 +594,13 @@ static cudaError_t launch_cfg_t(const CfgArgs& A, int32_t R, int32_t k, cudaStre
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>((static_cast<int64_t>(R) * A.shape.S + kCfgWarpRows - 1) / kCfgWarpRows));
-    cfg.blockDim = dim3(32 * kCfgWarpRows);
+    cfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(R) * A.shape.S));
+    cfg.blockDim = dim3(32 * kCfgRaceWarps);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, cfg_race_warp_kernel<DT, DD>, A);
+    return cudaLaunchKernelEx(&cfg, cfg_race_kernel<DT, DD>, A);
 }
 
 cudaError_t launch_cfg_merge_sample(const Rows& cond, const Rows& uncond, const CfgShape& shape,
@@ -598,11 +633,6 @@ cudaError_t launch_cfg_merge_sample(const Rows& cond, const Rows& uncond, const 
     A.tv = tv;
     A.status = status;
     A.stats = static_cast<CfgStat*>(workspace);
-    cudaError_t e;
-    if (status) {
-        cfg_clear_status_kernel<<<static_cast<unsigned>((R + 255) / 256), 256, 0, stream>>>(status, R);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
     const bool cb = cond.dtype == SV_BF16;
     const bool db = draft_logits == nullptr || draft_logits->dtype == SV_BF16;
     if (cb && db) return launch_cfg_t<SV_BF16, SV_BF16>(A, R, k, stream);
