@@ -525,11 +525,11 @@ __global__ void __launch_bounds__(kRowThreads, 1) sample_rows_kernel(SampleArgs 
                     const float mt = mx * c;
                     if (mt > -INFINITY) {
                         if (mt > dl.m) {
-                            dl.s = dl.m == -INFINITY ? 0.f : dl.s * exp2f(dl.m - mt);
+                            dl.s = dl.m == -INFINITY ? 0.f : dl.s * ex2(dl.m - mt);
                             dl.m = mt;
                         }
                         float acc = 0.f;
-                        for (int e = 0; e < n; ++e) acc += exp2f(fmaf(f[e], c, -dl.m));
+                        for (int e = 0; e < n; ++e) acc += ex2(fmaf(f[e], c, -dl.m));
                         dl.s += acc;
                     }
                 }
@@ -551,10 +551,10 @@ __global__ void __launch_bounds__(kRowThreads, 1) sample_rows_kernel(SampleArgs 
                 const float t = f * c;
                 if (t > -INFINITY) {
                     if (t > dl.m) {
-                        dl.s = dl.m == -INFINITY ? 0.f : dl.s * exp2f(dl.m - t);
+                        dl.s = dl.m == -INFINITY ? 0.f : dl.s * ex2(dl.m - t);
                         dl.m = t;
                     }
-                    dl.s += exp2f(t - dl.m);
+                    dl.s += ex2(t - dl.m);
                 }
             }
         }
@@ -595,7 +595,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) sample_rows_kernel(SampleArgs 
                     const float mt = mx * c;
                     if (mt > -INFINITY) {
                         if (mt > tl.m) {
-                            const float sc = tl.m == -INFINITY ? 0.f : exp2f(tl.m - mt);
+                            const float sc = tl.m == -INFINITY ? 0.f : ex2(tl.m - mt);
                             tl.s *= sc;
                             tl.so *= sc;
                             tl.m = mt;
@@ -606,12 +606,12 @@ __global__ void __launch_bounds__(kRowThreads, 1) sample_rows_kernel(SampleArgs 
                             const int32_t x = x0 + v * VT;
                             const uint32_t bits = A.plan.bitmap[x >> 5] >> (x & 31);
                             for (int e = 0; e < n; ++e) {
-                                const float ex = exp2f(fmaf(f[e], c, -tl.m));
+                                const float ex = ex2(fmaf(f[e], c, -tl.m));
                                 acc += ex;
                                 acc_off += ((bits >> e) & 1u) ? 0.f : ex;
                             }
                         } else {
-                            for (int e = 0; e < n; ++e) acc += exp2f(fmaf(f[e], c, -tl.m));
+                            for (int e = 0; e < n; ++e) acc += ex2(fmaf(f[e], c, -tl.m));
                         }
                         tl.s += acc;
                         tl.so += acc_off;
@@ -666,12 +666,12 @@ __global__ void __launch_bounds__(kRowThreads, 1) sample_rows_kernel(SampleArgs 
                 const float t = f * c;
                 if (t > -INFINITY) {
                     if (t > tl.m) {
-                        const float sc = tl.m == -INFINITY ? 0.f : exp2f(tl.m - t);
+                        const float sc = tl.m == -INFINITY ? 0.f : ex2(tl.m - t);
                         tl.s *= sc;
                         tl.so *= sc;
                         tl.m = t;
                     }
-                    const float ex = exp2f(fmaf(f, c, -tl.m));
+                    const float ex = ex2(fmaf(f, c, -tl.m));
                     tl.s += ex;
                     if (track_off && !in_support(A.plan, e)) tl.so += ex;
                 }
@@ -707,13 +707,13 @@ __global__ void __launch_bounds__(kRowThreads, 1) sample_rows_kernel(SampleArgs 
         float s_off = 0.f;  // target mass outside the d2t support, unnormalised
         if (sampling) {
             const float M = block_max<kRowThreads>(tl.m, red_f);
-            const float sc = (tl.m == -INFINITY || M == -INFINITY) ? 0.f : exp2f(tl.m - M);
+            const float sc = (tl.m == -INFINITY || M == -INFINITY) ? 0.f : ex2(tl.m - M);
             T2 = Lse{M, block_sum<kRowThreads>(tl.s * sc, red_f)};
             if (track_off) s_off = block_sum<kRowThreads>(tl.so * sc, red_f);
         }
         if (has_draft) {
             const float M = block_max<kRowThreads>(dl.m, red_f);
-            const float part = dl.m == -INFINITY ? 0.f : dl.s * exp2f(dl.m - M);
+            const float part = dl.m == -INFINITY ? 0.f : dl.s * ex2(dl.m - M);
             D2 = Lse{M, block_sum<kRowThreads>(M == -INFINITY ? 0.f : part, red_f)};
         }
         uint32_t flags = 0;
@@ -738,8 +738,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) sample_rows_kernel(SampleArgs 
                 float y = ld_elem<DD>(Y, jd);
                 z = z != z ? -INFINITY : z;
                 y = y != y ? -INFINITY : y;
-                const float pp = exp2f(fmaf(z, c, -T2.m)) * invS;
-                const float qq = exp2f(fmaf(y, c, -D2.m)) * invSq;
+                const float pp = ex2(fmaf(z, c, -T2.m)) * invS;
+                const float qq = ex2(fmaf(y, c, -D2.m)) * invSq;
                 a_abs += fabsf(pp - qq);
             }
             a_abs = block_sum<kRowThreads>(a_abs, red_f);
@@ -750,14 +750,14 @@ __global__ void __launch_bounds__(kRowThreads, 1) sample_rows_kernel(SampleArgs 
                 const bool in_range = xj >= 0 && xj < A.V;
                 float zx = zx_shared;
                 zx = zx != zx ? -INFINITY : zx;
-                pj = in_range ? exp2f(fmaf(zx, c, -T2.m)) * invS : 0.f;
+                pj = in_range ? ex2(fmaf(zx, c, -T2.m)) * invS : 0.f;
                 qj = 0.f;
                 if (in_range && (A.identity || in_support(A.plan, xj))) {
                     const int32_t jd = A.identity ? xj : A.plan.js[support_rank(A.plan, xj)];
                     if (jd >= 0 && jd < A.Vd) {
                         float y = ld_elem<DD>(Y, jd);
                         y = y != y ? -INFINITY : y;
-                        qj = exp2f(fmaf(y, c, -D2.m)) * invSq;
+                        qj = ex2(fmaf(y, c, -D2.m)) * invSq;
                     }
                 }
                 if (qj > 0.f) {
