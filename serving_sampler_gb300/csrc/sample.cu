@@ -1027,6 +1027,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
         const float c = u.sampling ? kLog2e / T : 0.f;
         const unsigned long long c2 = pack2(c, c);
         const int32_t xj = u.has_draft ? A.draft[static_cast<int64_t>(u.r) * A.k + u.j] : -1;
+        const uint64_t seed = (u.has_draft && tid == 0) ? A.seeds[u.r] : 0ull;  // for the accept test
         const int32_t nw_chunks = warp_chunks(u.n, w);
         if (tid == 0) {
             zx_shared = NAN;
@@ -1341,7 +1342,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                 pj = in_range ? ex2(fmaf(zx, c, -M)) * invS : 0.f;
                 qj = (in_range && jdx >= 0) ? qx_shared : 0.f;
                 if (qj > 0.f) {
-                    const uint4 w4 = philox_block(philox_key(A.seeds[u.r]), 0u, static_cast<uint32_t>(u.j), kTagAccept);
+                    const uint4 w4 = philox_block(philox_key(seed), 0u, static_cast<uint32_t>(u.j), kTagAccept);
                     acc = uniform_from_word(w4.x) < __fdiv_rn(pj, qj) ? 1 : 0;
                 } else if (in_range) {
                     flags |= kFlagOffSupport;

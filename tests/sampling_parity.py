@@ -7,7 +7,7 @@ fp64; those requests are counted.  p(x_j) and q(x_j) must agree within 1e-5
 relative (absolute floor 1e-9, for values near fp32 underflow).  TV must
 agree within 1e-5 relative or 1e-6 absolute: the kernel evaluates every
 probability in fp32 with ~1e-6 relative error (rounding of c = log2(e)/T
-times the logit spread, exp2f's 2 ulp, the normaliser's sum), so a sum of
+times the logit spread, ex2.approx's 2 ulp, the normaliser's sum), so a sum of
 |p - q| carries an absolute error of that order however small TV is.
 """
 import numpy as np
