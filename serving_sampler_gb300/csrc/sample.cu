@@ -1,27 +1,28 @@
 // Speculative sampling with a truncated draft vocabulary ("speculative
 // decoding for Omni models", sections 2 and 4).
 //
-// Three kernels per call:
+// The d2t plan (built once per draft model, or in the call):
 //   d2t_plan_kernel    one CTA: a bitmap of the d2t image over the target
-//                      vocabulary, per-word prefix counts, and the support
-//                      sorted by target id (xs[pos], js[pos]).  Every later
-//                      pass visits the support in row order, so no pass
-//                      gathers at random from a 300 KB target row.
-//   sample_rows_kernel persistent CTAs, one (request, position) unit at a
-//                      time.  The draft row y_j streams through a ring of
-//                      bulk-copied 16 KB stages into a resident buffer Y
-//                      while its max / sum-exp at T are taken; then the
-//                      target row z_j streams through the same ring: max,
-//                      sum-exp, argmax, NaN/inf flags, and z at the support
-//                      positions (G[pos]).  A second pass over G and Y gives
-//                      TV over the full vocabulary, p(x_j), q(x_j) and the
-//                      accept test u_j < p/q.
-//   race_rows_kernel   one CTA per request: the accept-length scan, the
-//                      chunk sums of the weights on the one selected row
-//                      (residual max(0, p - q) at the first rejection, or p
-//                      at the bonus row), then the chunk and the id drawn by
-//                      exponential races with Philox uniforms; it commits
-//                      the tokens.
+//                      vocabulary, per-word prefix counts, the support sorted
+//                      by target id (xs[pos], js[pos]), the target id -> draft
+//                      id map and the support rank at every chunk start.
+//   d2t_group_kernel   one warp per 2048-id chunk: the chunk's support entries
+//                      grouped for the shared-memory scatter of the row pass.
+// Two kernels per call:
+//   sample_rows_fast_kernel (bf16 rows, a d2t map) or sample_rows_kernel (the
+//                      general path): persistent CTAs, one (request, position)
+//                      unit at a time.  The draft and target rows stream
+//                      through bulk-copied shared-memory stages: max, sum-exp
+//                      at T, argmax, NaN/inf flags, z at the support positions
+//                      (G), and on the fast path each target chunk's (max,
+//                      sum) for the race.  A second pass over G and the draft
+//                      row gives TV over the full vocabulary, p(x_j), q(x_j)
+//                      and the accept test u_j < p/q.
+//   race_rows_kernel   one CTA per request: the accept-length scan, then on
+//                      the one selected row (residual max(0, p - q) at the
+//                      first rejection, or p at the bonus row) the chunk and
+//                      the id drawn by exponential races with Philox uniforms;
+//                      it commits the tokens.
 // Temperature scaling works in log2 units: with c = log2(e) / T,
 // p(x) = 2^(z_x c - M) / S where M = max_x z_x c and S = sum 2^(z c - M).
 #include <algorithm>

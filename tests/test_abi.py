@@ -92,6 +92,28 @@ def test_argument_checks_need_no_gpu(lib):
              buf, None, None, ws, 1 << 20, None) == -4
 
 
+def test_sampling_limits_need_no_gpu(lib):
+    P = C.c_void_p
+    buf = P(0x10000)
+    ws = P(0x20000)
+    smp = lib.sv_verify_sample
+
+    def call(target, R, k, d2t=None, plan=None, draft_rows=None):
+        return smp(target, draft_rows or _rows(width=target.width), d2t, plan, R, k, buf, buf, buf, buf, buf,
+                   None, None, None, None, ws, 1 << 30, None)
+
+    # identity map, vocabulary above the race's chunk-table limit (819,200 ids)
+    wide = _rows(width=819208, stride=819208)
+    assert call(wide, 1, 1) == -4
+    # R * (k + 1) must stay below 2^31
+    assert call(_rows(), 1 << 24, 255) == -4
+    # a d2t plan must be 256-byte aligned
+    assert call(_rows(), 1, 1, d2t=buf, plan=P(0x20010), draft_rows=_rows(width=8)) == -6
+    # the plan calls reject impossible sizes before anything runs
+    assert lib.sv_d2t_plan_bytes(0, 5) == 0
+    assert lib.sv_d2t_plan_build(buf, 70000, 151936, ws, 1 << 30, None) == -4
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     import serving_sampler_gb300 as m
 
