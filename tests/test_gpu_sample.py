@@ -170,3 +170,67 @@ def test_bad_and_mismatched_d2t_are_flagged(sv):
                            plan=other)
     torch.cuda.synchronize()
     assert np.all(got["status"].cpu().numpy() & 32)
+
+
+def _with_d2t(w, d2t, seed):
+    """Rebuild the draft rows of a sampling batch for another d2t map (target rows kept)."""
+    R, k, V = w["R"], w["k"], w["V"]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    z = w["target"].float().view(R, k + 1, V)[:, :k]
+    y = (z[:, :, d2t.long()] + torch.randn(R, k, d2t.numel(), generator=g, device="cuda") * 0.8)
+    w = dict(w)
+    w["d2t"] = d2t
+    w["Vd"] = d2t.numel()
+    w["draft_logits"] = y.reshape(R * k, -1).to(w["target"].dtype).contiguous()
+    ids = torch.randint(0, d2t.numel(), (R, k), generator=g, device="cuda")
+    w["draft"] = d2t.long()[ids].to(torch.int32).contiguous()
+    return w
+
+
+def test_dense_support_chunks_use_the_overflow_groups(sv):
+    """A d2t whose image covers whole 2048-id chunks: more support entries per chunk than
+    the row pass holds in registers, so the scatter and the draft-id search take their
+    overflow paths; also a draft vocabulary at the largest width of the row pass."""
+    w = workloads.sample_batch(6, 4, 40960, None, torch.bfloat16, T=0.9, sigma_pos=0.6, seed=21)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(3)
+    dense = torch.cat([torch.arange(0, 6144, device="cuda"),                    # three full chunks
+                       torch.randperm(40960 - 6144, generator=g, device="cuda")[:26616] + 6144]).to(torch.int32)
+    w2 = _with_d2t(w, dense, 4)
+    assert w2["Vd"] == 32760  # the widest draft vocabulary of the bf16 row pass
+    compare(_run(sv, w2), _oracle(w2))
+
+
+def test_zero_residual_mass_on_the_bulk_copy_path(sv):
+    """Positions 0 and 1 of every other request: the target and the draft rows put all their
+    mass on one support id (every other logit -inf), so p = q exactly.  Position 0 drafts
+    that id (p / q = 1: accepted); position 1 drafts an id off the support, rejected
+    (status 4) with no residual mass anywhere, so the correction is drawn from p
+    (status 8), which can only be that id."""
+    R, k, V, Vd = 8, 3, 8192, 4096
+    w = workloads.sample_batch(R, k, V, Vd, torch.bfloat16, T=1.0, sigma_pos=0.5, seed=22)
+    d2t = w["d2t"].long()
+    off = torch.ones(V, dtype=torch.bool, device="cuda")
+    off[d2t] = False
+    t = w["target"].float().view(R, k + 1, V)
+    y = w["draft_logits"].float().view(R, k, Vd)
+    for r in range(0, R, 2):
+        for j in (0, 1):
+            t[r, j] = float("-inf")
+            t[r, j, d2t[100 + r]] = 1.5
+            y[r, j] = float("-inf")
+            y[r, j, 100 + r] = 1.5
+    w["target"] = t.reshape(R * (k + 1), V).to(torch.bfloat16).contiguous()
+    w["draft_logits"] = y.reshape(R * k, Vd).to(torch.bfloat16).contiguous()
+    draft = w["draft"].clone()
+    off_ids = torch.nonzero(off).flatten()
+    draft[::2, 0] = d2t[100 + torch.arange(0, R, 2, device="cuda")].to(torch.int32)  # p/q = 1 at position 0
+    draft[::2, 1] = off_ids[:R // 2].to(torch.int32)
+    w["draft"] = draft
+    got, want = _run(sv, w), _oracle(w)
+    compare(got, want)
+    st = want["status"]
+    assert np.all(st[::2] & 4) and np.all(st[::2] & 8)
+    ids = d2t[100 + torch.arange(0, R, 2, device="cuda")].cpu().numpy()
+    assert np.all(want["accept_len"][::2] == 1) and np.all(want["tokens"][::2, 1] == ids)
