@@ -94,7 +94,7 @@ struct SampleArgs {
     int32_t* tokens;
     int32_t* status;
     RowStat* stats;
-    float2* cstat;       // [units][target chunks] (max of z c, sum 2^(z c - max)) per chunk, or NULL
+    float2* cstat;       // [units][target chunks] (reference r, sum 2^(z c - r)) per chunk, or NULL
     int32_t nct;         // target chunks per row
     char* gslots;        // global-memory Y / G buffers when they do not fit in shared memory
     int64_t gslot_bytes;
@@ -804,27 +804,36 @@ __global__ void __launch_bounds__(kRowThreads, 1) sample_rows_kernel(SampleArgs 
 // ---------------------------------------------------------------------------
 // row pass, fast path: bf16 target and draft rows, d2t vocabulary <= 32768
 // ---------------------------------------------------------------------------
-// Every warp streams its own share of a row through a private ring of
-// kFastStages bulk-copied stages.  The chunks of a (request, position) unit,
-// draft chunks first and then target chunks, form one sequence; element s of
-// the sequence belongs to warp s % kFastWarps, so warps get equal shares.  The
-// warp's lane 0 keeps all stages in flight: each consumed stage is refilled
-// at once with the warp's next chunk, of this unit or of the CTA's next one,
-// so the row reductions and the TV pass at the end of a unit overlap the
-// first copies of the next.  The support entries of a target chunk, packed
-// (draft id, offset) pairs of the plan, come from L2 into registers while the
-// chunk's maxima and exponentials are taken; the warp then scatters the
-// support logits to G[draft id] from shared memory.
+// Two warp roles.  Each stream warp pulls its own share of a row through a
+// private ring of kFastStages bulk-copied stages.  The chunks of a (request,
+// position) unit, draft chunks first and then target chunks, form one
+// sequence; element s of the sequence belongs to stream warp s % kStreamWarps,
+// so the warps get equal shares.  The warp's lane 0 keeps all stages in
+// flight: each consumed stage is refilled at once with the warp's next chunk,
+// of this unit or of the CTA's next one.  The support entries of a target
+// chunk, packed (draft id, offset) pairs of the plan, come from L2 into
+// registers while the chunk's maxima and exponentials are taken; the warp then
+// scatters the support logits to G[draft id] from shared memory.
+//
+// The TV warps finish unit n (merge of the stream warps' records, the TV pass
+// over G and the L2-resident draft row, p and q at the draft token, the accept
+// test) while the stream warps already read unit n + 1: G, the warp records
+// and the draft-token slots are double-buffered by unit parity, and two
+// mbarrier pairs hand a buffer over (full: the stream warps are done with it;
+// freed: the TV warps are).
 namespace {
 
-constexpr int kFastWarps = 16;
+constexpr int kStreamWarps = 12;                 // warps that stream the rows
+constexpr int kTvWarps = 4;                      // warps that finish a unit: reductions, TV, accept test
+constexpr int kFastWarps = kStreamWarps + kTvWarps;
 constexpr int kFastThreads = 32 * kFastWarps;
-constexpr int kFastStages = 2;                   // per warp: one being read, one in flight
+constexpr int kTvThreads = 32 * kTvWarps;
+constexpr int kFastStages = 2;                   // per stream warp: one being read, one in flight
 constexpr uint32_t kFastData = kChunkElems * 2;  // 4 KB of bf16 per stage
 constexpr uint32_t kFastStage = kFastData;
 constexpr int kPairRegs = 4;                     // uint4 groups of support entries per lane and chunk
-constexpr int kFastHeader = 512;                 // the stage mbarriers
-static_assert(kFastWarps * kFastStages * 8 <= kFastHeader, "mbarriers fit the header");
+constexpr int kFastHeader = 512;                 // the stage mbarriers, then the two unit handoffs
+static_assert((kStreamWarps * kFastStages + 4) * 8 <= kFastHeader, "mbarriers fit the header");
 constexpr int32_t kFastMaxVd = 32768;
 constexpr int kVL = kChunkElems / 8 / 32;  // 16-byte vectors per lane and chunk
 
@@ -852,6 +861,34 @@ __device__ __forceinline__ float exp_sum8(uint4 q, unsigned long long c2, unsign
 }
 
 
+
+// offset in the chunk of the first element equal to wm: vectors are numbered
+// lane + 32 e, elements 8 per vector; every lane takes part
+__device__ __forceinline__ uint32_t first_max_offset(const uint4 (&qv)[kVL], float wm, int lane)
+{
+    int ef = kVL;
+#pragma unroll
+    for (int e = kVL - 1; e >= 0; --e) {
+        const uint32_t m3 = bmax2_nan(bmax2_nan(qv[e].x, qv[e].y), bmax2_nan(qv[e].z, qv[e].w));
+        if (fmaxf(bf16_lo(m3), bf16_hi(m3)) == wm) ef = e;
+    }
+    uint32_t key = 0xFFFFFFFFu;
+    if (ef < kVL) {
+        uint4 v = qv[0];
+#pragma unroll
+        for (int e = 1; e < kVL; ++e)
+            if (ef == e) v = qv[e];
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+        int first = 7;
+#pragma unroll
+        for (int t = 7; t >= 0; --t) {
+            const float zt = (t & 1) ? bf16_hi(wv[t >> 1]) : bf16_lo(wv[t >> 1]);
+            if (zt == wm) first = t;
+        }
+        key = static_cast<uint32_t>((lane + 32 * ef) * 8 + first);
+    }
+    return __reduce_min_sync(0xffffffffu, key);
+}
 
 // this lane's register groups of a chunk's padded support entries [p0, p1)
 __device__ __forceinline__ void load_pairs(const SampleArgs& A, int32_t p0, int32_t p1, int lane, uint4* pg)
@@ -911,10 +948,10 @@ __device__ __forceinline__ FastUnit fast_unit(const SampleArgs& A, int64_t unit,
     return u;
 }
 
-// chunks of warp w in a unit of n chunks: sequence elements w, w + W, ...
+// chunks of stream warp w in a unit of n chunks: sequence elements w, w + W, ...
 __device__ __forceinline__ int32_t warp_chunks(int32_t n, int w)
 {
-    return n > w ? (n - w + kFastWarps - 1) / kFastWarps : 0;
+    return n > w ? (n - w + kStreamWarps - 1) / kStreamWarps : 0;
 }
 
 __device__ __forceinline__ float unit_temp(const SampleArgs& A, int64_t unit)
@@ -965,7 +1002,7 @@ __device__ __forceinline__ void producer_step(const SampleArgs& A, Producer& P, 
 {
     if (P.unit >= units || P.issued - consumed >= static_cast<uint32_t>(kFastStages)) return;
     const uint32_t sidx = P.issued % kFastStages;
-    if (lane == 0) issue_seq(A, P.u, w + P.i * kFastWarps, wst + sidx * kFastStage, &wbar[sidx], pol_t, pol_d);
+    if (lane == 0) issue_seq(A, P.u, w + P.i * kStreamWarps, wst + sidx * kFastStage, &wbar[sidx], pol_t, pol_d);
     ++P.issued;
     if (++P.i == P.cnt) {
         P.unit += gridDim.x;
@@ -975,256 +1012,247 @@ __device__ __forceinline__ void producer_step(const SampleArgs& A, Producer& P, 
 
 }  // namespace
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// barrier 1 over the TV warps only
+__device__ __forceinline__ void tv_bar_sync()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kTvThreads) : "memory");
+}
+
 __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(SampleArgs A)
 {
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // [warp][stage]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // [stream warp][stage]
+    uint64_t* full = bars + kStreamWarps * kFastStages;  // [buffer]: records, G and draft-token slots written
+    uint64_t* freed = full + 2;                           // [buffer]: the TV warps are done with them
     unsigned char* ring = smem + kFastHeader;
-    uint16_t* G = reinterpret_cast<uint16_t*>(ring + kFastWarps * kFastStages * kFastStage);
-    int32_t* ctab = reinterpret_cast<int32_t*>(reinterpret_cast<unsigned char*>(G) + align256((A.Vd + 8) * 2));
-    __shared__ float zx_shared;
-    __shared__ int32_t jdx_shared;  // draft id of the draft token (-1: off the support)
-    __shared__ float qx_shared;     // q at that draft id
-    __shared__ WarpRec wrec[kFastWarps];
-    __shared__ WarpRec merged;
-    __shared__ float wtv[kFastWarps];
-    __shared__ int32_t amax_shared;
+    const uint32_t gbytes = static_cast<uint32_t>(align256((static_cast<int64_t>(A.Vd) + 8) * 2));
+    unsigned char* gbase = ring + kStreamWarps * kFastStages * kFastStage;  // G of buffer 0, then of buffer 1
+    int32_t* ctab = reinterpret_cast<int32_t*>(gbase + 2 * gbytes);
+    __shared__ WarpRec wrec[2][kStreamWarps];
+    __shared__ float zx_s[2];      // target logit of the draft token
+    __shared__ int32_t jdx_s[2];   // its draft id (-1: off the support)
+    __shared__ WarpRec merged;     // TV warps: the unit's merged record
+    __shared__ float qx_shared;    // TV warps: q at the draft id
+    __shared__ float wtv[kTvWarps];
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int32_t nchunks_t = (A.V + kChunkElems - 1) / kChunkElems;
 
     pdl_wait_primary();  // a plan built in the same call must be complete
     pdl_launch_dependents();
     if (tid == 0) {
-        for (int i = 0; i < kFastStages * kFastWarps; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < kFastStages * kStreamWarps; ++i) mbar_init(&bars[i], 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&full[b], kStreamWarps * 32);
+            mbar_init(&freed[b], kTvThreads);
+        }
         fence_barrier_init();
+    }
+    if (tid < 2) {
+        zx_s[tid] = NAN;
+        jdx_s[tid] = -1;
     }
     // a plan for other sizes, or built from a d2t with repeated / out-of-range ids, is not
     // trusted for shared-memory indexing (the race kernel reports SV_ST_BAD_D2T)
     const bool plan_ok = A.plan.header[0] == A.V && A.plan.header[1] == A.Vd && A.plan.header[2] == 0;
     for (int32_t c = tid; c <= nchunks_t; c += kFastThreads) ctab[c] = plan_ok && c < nchunks_t ? A.plan.pcount[c] : 0;
     __syncthreads();
-    const uint64_t pol_t = l2_policy_evict_first();
-    uint64_t pol_d;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_d));
-    unsigned char* wst = ring + w * kFastStages * kFastStage;  // this warp's stages
-    uint64_t* wbar = bars + kFastStages * w;
     const int64_t units = static_cast<int64_t>(A.R) * (A.k + 1);
-    uint32_t consumed = 0;  // chunks this warp has read so far (stage = consumed % kFastStages)
-    uint32_t timeout = 0;
 
-    Producer P;
-    P.unit = blockIdx.x;
-    P.issued = 0;
-    producer_enter(A, P, w, units, P.unit < units ? unit_temp(A, P.unit) : 0.f);
-    for (int i = 0; i < kFastStages; ++i)
-        producer_step(A, P, consumed, w, lane, units, wst, wbar, pol_t, pol_d);
+    if (w < kStreamWarps) {
+        // ================= stream warps =================
+        const uint64_t pol_t = l2_policy_evict_first();
+        uint64_t pol_d;
+        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_d));
+        unsigned char* wst = ring + w * kFastStages * kFastStage;  // this warp's stages
+        uint64_t* wbar = bars + kFastStages * w;
+        uint32_t consumed = 0;  // chunks this warp has read so far (stage = consumed % kFastStages)
+        uint32_t timeout = 0;
 
-    int64_t unit = blockIdx.x;
-    float T = unit < units ? unit_temp(A, unit) : 0.f;
-    for (; unit < units; unit += gridDim.x) {
-        const FastUnit u = fast_unit(A, unit, T);
-        const int64_t un = unit + gridDim.x;
-        const float T_next = un < units ? unit_temp(A, un) : 0.f;  // for the next unit, loaded early
-        const float c = u.sampling ? kLog2e / T : 0.f;
-        const unsigned long long c2 = pack2(c, c);
-        const int32_t xj = u.has_draft ? A.draft[static_cast<int64_t>(u.r) * A.k + u.j] : -1;
-        const uint64_t seed = (u.has_draft && tid == 0) ? A.seeds[u.r] : 0ull;  // for the accept test
-        const int32_t nw_chunks = warp_chunks(u.n, w);
-        if (tid == 0) {
-            zx_shared = NAN;
-            jdx_shared = -1;
-        }
-        __syncthreads();  // G, zx and the exchange arrays of the previous row are no longer read
+        Producer P;
+        P.unit = blockIdx.x;
+        P.issued = 0;
+        producer_enter(A, P, w, units, P.unit < units ? unit_temp(A, P.unit) : 0.f);
+        for (int i = 0; i < kFastStages; ++i)
+            producer_step(A, P, consumed, w, lane, units, wst, wbar, pol_t, pol_d);
 
-        float dm = -INFINITY, ds = 0.f, tm = -INFINITY, ts = 0.f, bv = -INFINITY;
-        int32_t bx = INT32_MAX;
-        uint32_t dflags = 0, tflags = 0;
-        uint4 pg[kPairRegs];  // support entries of the target chunk pg_for (-1: none)
-        int32_t pg_for = -1;
-        for (int32_t i = 0; i < nw_chunks; ++i) {
-            const uint32_t sidx = consumed % kFastStages;
-            if (!timeout && !mbar_wait_bounded(&wbar[sidx], (consumed / kFastStages) & 1u)) timeout = 1;
-            const unsigned char* st = wst + sidx * kFastStage;
-            const uint4* vp = reinterpret_cast<const uint4*>(st);
-            const int32_t q = w + i * kFastWarps;
-            const bool is_draft = q < u.nd;
-            const int32_t cidx = is_draft ? q : q - u.nd;
-            const uint32_t off = static_cast<uint32_t>(cidx) * kFastData;
-            const uint32_t nb = min(kFastData, static_cast<uint32_t>(is_draft ? A.Vd : A.V) * 2 - off);
-            const int nv = static_cast<int>(nb / 16);
-            const int32_t x0 = static_cast<int32_t>(off / 2);
-            // support entries of a target chunk: this lane's groups of four packed pairs, from
-            // L2 while the maxima and exponentials below run
-            const bool scatter = !is_draft && u.has_draft;
-            float csum = 0.f;  // this lane's share of the chunk's sum, relative to its running max
-            int32_t p0 = 0, p1 = 0;
-            if (scatter) {
-                p0 = cidx * (kMaxGroups * 32);  // the chunk's slots: whole groups of four
-                p1 = p0 + ctab[cidx];
-                if (pg_for != cidx) load_pairs(A, p0, p1, lane, pg);  // not prefetched
-            }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                // half the lane's vectors: independent loads and max trees, one update of the
-                // running max, then the independent exps
-                constexpr int kH = kVL / 2;
-                uint4 qv[kH];
-#pragma unroll
-                for (int e = 0; e < kH; ++e) {
-                    const int v = lane + 32 * (h * kH + e);
-                    qv[e] = v < nv ? vp[v] : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+        int64_t unit = blockIdx.x;
+        float T = unit < units ? unit_temp(A, unit) : 0.f;
+        for (uint32_t n = 0; unit < units; unit += gridDim.x, ++n) {
+            const uint32_t b = n & 1u;
+            const FastUnit u = fast_unit(A, unit, T);
+            const int64_t un = unit + gridDim.x;
+            const float T_next = un < units ? unit_temp(A, un) : 0.f;  // for the next unit, loaded early
+            const float c = u.sampling ? kLog2e / T : 0.f;
+            const unsigned long long c2 = pack2(c, c);
+            const int32_t xj = u.has_draft ? A.draft[static_cast<int64_t>(u.r) * A.k + u.j] : -1;
+            const int32_t nw_chunks = warp_chunks(u.n, w);
+            uint16_t* G = reinterpret_cast<uint16_t*>(gbase + b * gbytes);
+            // the TV warps are done with this buffer's previous unit
+            if (n >= 2 && !timeout && !mbar_wait_bounded(&freed[b], ((n >> 1) + 1) & 1u)) timeout = 1;
+
+            float dm = -INFINITY, ds = 0.f, tm = -INFINITY, ts = 0.f, bv = -INFINITY;
+            int32_t bx = INT32_MAX;
+            uint32_t dflags = 0, tflags = 0;
+            uint4 pg[kPairRegs];  // support entries of the target chunk pg_for (-1: none)
+            int32_t pg_for = -1;
+            for (int32_t i = 0; i < nw_chunks; ++i) {
+                const uint32_t sidx = consumed % kFastStages;
+                if (!timeout && !mbar_wait_bounded(&wbar[sidx], (consumed / kFastStages) & 1u)) timeout = 1;
+                const unsigned char* st = wst + sidx * kFastStage;
+                const uint4* vp = reinterpret_cast<const uint4*>(st);
+                const int32_t q = w + i * kStreamWarps;
+                const bool is_draft = q < u.nd;
+                const int32_t cidx = is_draft ? q : q - u.nd;
+                const uint32_t off = static_cast<uint32_t>(cidx) * kFastData;
+                const uint32_t nb = min(kFastData, static_cast<uint32_t>(is_draft ? A.Vd : A.V) * 2 - off);
+                const int nv = static_cast<int>(nb / 16);
+                const int32_t x0 = static_cast<int32_t>(off / 2);
+                // support entries of a target chunk: this lane's groups of four packed pairs, from
+                // L2 while the maxima and exponentials below run
+                const bool scatter = !is_draft && u.has_draft;
+                float csum = 0.f;  // this lane's share of the chunk's sum, relative to its running max
+                int32_t p0 = 0, p1 = 0;
+                if (scatter) {
+                    p0 = cidx * (kMaxGroups * 32);  // the chunk's slots: whole groups of four
+                    p1 = p0 + ctab[cidx];
+                    if (pg_for != cidx) load_pairs(A, p0, p1, lane, pg);  // not prefetched
                 }
-                // one packed NaN-propagating max tree over the half, widened once
+                if (nv < kVL * 32) {
+                    // the row's last chunk: -inf beyond its end, so that every lane reads whole
+                    // vectors; the fence orders these writes before the next bulk copy here
+                    for (int v = nv + lane; v < kVL * 32; v += 32)
+                        const_cast<uint4*>(vp)[v] = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                uint4 qv[kVL];
+#pragma unroll
+                for (int e = 0; e < kVL; ++e) qv[e] = vp[lane + 32 * e];
+                // one packed NaN-propagating max tree over the lane's vectors, widened once
                 uint32_t m2 = bmax2_nan(bmax2_nan(qv[0].x, qv[0].y), bmax2_nan(qv[0].z, qv[0].w));
 #pragma unroll
-                for (int e = 1; e < kH; ++e)
+                for (int e = 1; e < kVL; ++e)
                     m2 = bmax2_nan(m2, bmax2_nan(bmax2_nan(qv[e].x, qv[e].y), bmax2_nan(qv[e].z, qv[e].w)));
                 float lm = fmax_nan(bf16_lo(m2), bf16_hi(m2));
                 if (lm != lm) {  // rare: NaN logits read as -inf
                     (is_draft ? dflags : tflags) |= kFlagNaN;
                     lm = -INFINITY;
 #pragma unroll
-                    for (int e = 0; e < kH; ++e) {
+                    for (int e = 0; e < kVL; ++e) {
                         qv[e] = make_uint4(bf16x2_nan_to_ninf(qv[e].x), bf16x2_nan_to_ninf(qv[e].y),
                                            bf16x2_nan_to_ninf(qv[e].z), bf16x2_nan_to_ninf(qv[e].w));
                         const uint32_t m3 = bmax2_nan(bmax2_nan(qv[e].x, qv[e].y), bmax2_nan(qv[e].z, qv[e].w));
                         lm = fmaxf(lm, fmaxf(bf16_lo(m3), bf16_hi(m3)));
                     }
                 }
+                // Each lane sums its exponentials against its own maximum lr, so that they do not wait
+                // for the warp maximum; the lane's sum is then moved to the warp's running reference
+                // rm (the running maximum of z c) with one more exponential.
+                const bool sums = is_draft || u.sampling;
+                float& rm = is_draft ? dm : tm;
+                float& rs_ = is_draft ? ds : ts;
+                const float lr = lm > -INFINITY ? lm * c : 0.f;
+                float acc = 0.f;
+                if (sums) {
+                    const unsigned long long nl2 = pack2(-lr, -lr);
+                    float ae[kVL];
+#pragma unroll
+                    for (int e = 0; e < kVL; ++e) ae[e] = exp_sum8(qv[e], c2, nl2);
+                    acc = ((ae[0] + ae[1]) + (ae[2] + ae[3])) + ((ae[4] + ae[5]) + (ae[6] + ae[7]));
+                }
                 const float wm = warp_max(lm);
                 if (!is_draft) {
-                    if (wm > bv) {  // warp-uniform, rare after the first chunks: the first vector
-                                    // (lowest e, then lowest lane) holding the new maximum
-#pragma unroll
-                        for (int e = 0; e < kH; ++e) {
-                            const uint32_t m3 = bmax2_nan(bmax2_nan(qv[e].x, qv[e].y), bmax2_nan(qv[e].z, qv[e].w));
-                            const unsigned hit = __ballot_sync(0xffffffffu, fmaxf(bf16_lo(m3), bf16_hi(m3)) == wm);
-                            if (hit) {
-                                const int src = __ffs(hit) - 1;
-                                const uint32_t wv[4] = {qv[e].x, qv[e].y, qv[e].z, qv[e].w};
-                                int first = 7;
-#pragma unroll
-                                for (int t = 7; t >= 0; --t) {
-                                    const float zt = (t & 1) ? bf16_hi(wv[t >> 1]) : bf16_lo(wv[t >> 1]);
-                                    if (zt == wm) first = t;
-                                }
-                                first = __shfl_sync(0xffffffffu, first, src);
-                                bx = x0 + (src + 32 * (h * kH + e)) * 8 + first;
-                                break;
-                            }
-                        }
+                    if (wm > bv) {  // warp-uniform, rare after the first chunks
+                        bx = x0 + static_cast<int32_t>(first_max_offset(qv, wm, lane));
                         bv = wm;
                     }
                 } else if (wm == INFINITY) {
                     dflags |= kFlagPosInf;
                 }
-                if (is_draft || u.sampling) {
-                    // one running max per warp (the lanes' sums share its reference)
-                    float& rm = is_draft ? dm : tm;
-                    float& rs_ = is_draft ? ds : ts;
+                if (sums) {
                     const float mt = wm * c;
-                    if (mt > rm) {
-                        const float sc = rm == -INFINITY ? 0.f : ex2(rm - mt);
-                        rs_ *= sc;
-                        csum *= sc;
+                    if (mt > rm) {  // warp-uniform
+                        rs_ *= rm == -INFINITY ? 0.f : ex2(rm - mt);
                         rm = mt;
                     }
-                    if (rm > -INFINITY) {
-                        const unsigned long long nm2 = pack2(-rm, -rm);
-                        float acc[kH];
-#pragma unroll
-                        for (int e = 0; e < kH; ++e) acc[e] = exp_sum8(qv[e], c2, nm2);
-#pragma unroll
-                        for (int e = 1; e < kH; ++e) acc[0] += acc[e];
-                        rs_ += acc[0];
-                        csum += acc[0];
-                    }
+                    csum = lm > -INFINITY ? acc * ex2(lr - rm) : 0.f;
+                    rs_ += csum;
                 }
-            }
-            if (scatter) {
-                // G[draft id] = z at the chunk offset for every entry of the lane's groups; a
-                // padding entry writes the spare slot G[Vd], which nothing reads
-                const uint16_t* zs = reinterpret_cast<const uint16_t*>(st);
-                const uint32_t zs_a = smem_addr(st), g_a = smem_addr(G);
-                const bool here = xj >= x0 && xj < x0 + static_cast<int32_t>(nb / 2);
-#pragma unroll
-                for (int t = 0; t < kPairRegs; ++t) {
-                    if (p0 + 4 * (lane + 32 * t) < p1) {  // whole groups of four
-                        const uint32_t pe[4] = {pg[t].x, pg[t].y, pg[t].z, pg[t].w};
-                        uint32_t zv[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) zv[e] = lds_u16(zs_a + (pe[e] & 0xFFFFu));
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) sts_u16(g_a + (pe[e] >> 16), zv[e]);
-                    }
-                }
-                // groups beyond this lane's registers (chunks denser than 512 entries)
-                for (int32_t g = p0 + 4 * 32 * kPairRegs + 4 * lane; g < p1; g += 4 * 32) {
-                    const uint4 q4 = ld_nc_v4(reinterpret_cast<const uint4*>(A.plan.pairs + g));
-                    const uint32_t pe[4] = {q4.x, q4.y, q4.z, q4.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) sts_u16(g_a + (pe[e] >> 16), lds_u16(zs_a + (pe[e] & 0xFFFFu)));
-                }
-                if (here) {  // the draft token: its logit and its draft id (from the registers)
-                    const uint32_t xoff = static_cast<uint32_t>(xj - x0);
-                    if (lane == 0) zx_shared = __uint_as_float(static_cast<uint32_t>(zs[xoff]) << 16);
+                if (scatter) {
+                    // G[draft id] = z at the chunk offset for every entry of the lane's groups; a
+                    // padding entry writes the spare slot G[Vd], which nothing reads
+                    const uint16_t* zs = reinterpret_cast<const uint16_t*>(st);
+                    const uint32_t zs_a = smem_addr(st), g_a = smem_addr(G);
+                    const bool here = xj >= x0 && xj < x0 + static_cast<int32_t>(nb / 2);
 #pragma unroll
                     for (int t = 0; t < kPairRegs; ++t) {
-                        if (p0 + 4 * (lane + 32 * t) < p1) {
+                        if (p0 + 4 * (lane + 32 * t) < p1) {  // whole groups of four
                             const uint32_t pe[4] = {pg[t].x, pg[t].y, pg[t].z, pg[t].w};
+                            uint32_t zv[4];
 #pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                if ((pe[e] & 0xFFFFu) == 2 * xoff && static_cast<int32_t>(pe[e] >> 17) < A.Vd)
-                                    jdx_shared = static_cast<int32_t>(pe[e] >> 17);
+                            for (int e = 0; e < 4; ++e) zv[e] = lds_u16(zs_a + (pe[e] & 0xFFFFu));
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) sts_u16(g_a + (pe[e] >> 16), zv[e]);
                         }
                     }
-                    for (int32_t g = p0 + 4 * 32 * kPairRegs + lane; g < p1; g += 32) {  // beyond the registers
-                        const uint32_t pe = A.plan.pairs[g];
-                        if ((pe & 0xFFFFu) == 2 * xoff && static_cast<int32_t>(pe >> 17) < A.Vd)
-                            jdx_shared = static_cast<int32_t>(pe >> 17);
+                    // groups beyond this lane's registers (chunks denser than 512 entries)
+                    for (int32_t g = p0 + 4 * 32 * kPairRegs + 4 * lane; g < p1; g += 4 * 32) {
+                        const uint4 q4 = ld_nc_v4(reinterpret_cast<const uint4*>(A.plan.pairs + g));
+                        const uint32_t pe[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) sts_u16(g_a + (pe[e] >> 16), lds_u16(zs_a + (pe[e] & 0xFFFFu)));
+                    }
+                    if (here) {  // the draft token: its logit and its draft id (from the registers)
+                        const uint32_t xoff = static_cast<uint32_t>(xj - x0);
+                        if (lane == 0) zx_s[b] = __uint_as_float(static_cast<uint32_t>(zs[xoff]) << 16);
+#pragma unroll
+                        for (int t = 0; t < kPairRegs; ++t) {
+                            if (p0 + 4 * (lane + 32 * t) < p1) {
+                                const uint32_t pe[4] = {pg[t].x, pg[t].y, pg[t].z, pg[t].w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    if ((pe[e] & 0xFFFFu) == 2 * xoff && static_cast<int32_t>(pe[e] >> 17) < A.Vd)
+                                        jdx_s[b] = static_cast<int32_t>(pe[e] >> 17);
+                            }
+                        }
+                        for (int32_t g = p0 + 4 * 32 * kPairRegs + lane; g < p1; g += 32) {  // beyond the registers
+                            const uint32_t pe = A.plan.pairs[g];
+                            if ((pe & 0xFFFFu) == 2 * xoff && static_cast<int32_t>(pe >> 17) < A.Vd)
+                                jdx_s[b] = static_cast<int32_t>(pe >> 17);
+                        }
                     }
                 }
-            }
-            {
-                // the support entries of this warp's next chunk, if it is a target chunk of this
-                // unit: in flight until that chunk's scatter
-                const int32_t qn = q + kFastWarps;
-                pg_for = -1;
-                if (u.has_draft && qn < u.n && qn >= u.nd) {
-                    pg_for = qn - u.nd;
-                    load_pairs(A, pg_for * (kMaxGroups * 32), pg_for * (kMaxGroups * 32) + ctab[pg_for], lane, pg);
+                {
+                    // the support entries of this warp's next chunk, if it is a target chunk of this
+                    // unit: in flight until that chunk's scatter
+                    const int32_t qn = q + kStreamWarps;
+                    pg_for = -1;
+                    if (u.has_draft && qn < u.n && qn >= u.nd) {
+                        pg_for = qn - u.nd;
+                        load_pairs(A, pg_for * (kMaxGroups * 32), pg_for * (kMaxGroups * 32) + ctab[pg_for], lane, pg);
+                    }
+                }
+                // the stage is read: refill it with this warp's next chunk
+                __syncwarp();
+                ++consumed;
+                if (lane == 0) fence_proxy_async_smem();
+                producer_step(A, P, consumed, w, lane, units, wst, wbar, pol_t, pol_d);
+                if (!is_draft && u.sampling) {
+                    // this chunk's (reference, sum) for the race
+                    float cs = csum;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) cs += __shfl_xor_sync(0xffffffffu, cs, o);
+                    if (lane == 0) A.cstat[unit * A.nct + cidx] = make_float2(tm, cs);
                 }
             }
-            if (!is_draft && u.sampling) {
-                // this chunk's (reference max, sum) for the race
-                float cs = csum;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) cs += __shfl_xor_sync(0xffffffffu, cs, o);
-                if (lane == 0) A.cstat[unit * A.nct + cidx] = make_float2(tm, cs);
-            }
-            // the stage is read: refill it with this warp's next chunk
-            __syncwarp();
-            ++consumed;
-            if (lane == 0) fence_proxy_async_smem();
-            producer_step(A, P, consumed, w, lane, units, wst, wbar, pol_t, pol_d);
-        }
-        T = T_next;
+            T = T_next;
 
-        // the first batch of draft-row loads of the TV pass, in flight during the reductions
-        constexpr int kTvIter = (kFastMaxVd / 8 + kFastThreads - 1) / kFastThreads;
-        constexpr int kTvBatch = (kTvIter + 1) / 2;  // draft-row loads in flight per thread
-        const int32_t nv8 = u.has_draft ? A.Vd / 8 : 0;  // Vd % 8 == 0 on this path
-        const uint4* yv = reinterpret_cast<const uint4*>(u.drow);
-        uint4 yq0[kTvBatch];
-#pragma unroll
-        for (int i = 0; i < kTvBatch; ++i) {
-            const int32_t v = tid + i * kFastThreads;
-            if (v < nv8) yq0[i] = ld_nc_v4(yv + v);
-        }
-
-        // ---- reductions: max, argmax and reference max are warp-uniform; warp sums, then
-        // warp 0 merges the warps' records ----
-        {
+            // this warp's record of the unit; every lane then signals the TV warps
             const uint32_t tfl = __reduce_or_sync(0xffffffffu, tflags | (timeout ? kFlagTimeout : 0u));
             const uint32_t dfl = __reduce_or_sync(0xffffffffu, dflags);
             float tsw = ts, dsw = ds;
@@ -1233,12 +1261,47 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                 tsw += __shfl_xor_sync(0xffffffffu, tsw, o);
                 dsw += __shfl_xor_sync(0xffffffffu, dsw, o);
             }
-            if (lane == 0) wrec[w] = WarpRec{bv, bx, tfl, dfl, tm, dm, tsw, dsw};
+            if (lane == 0) wrec[b][w] = WarpRec{bv, bx, tfl, dfl, tm, dm, tsw, dsw};
+            mbar_arrive(&full[b]);
         }
-        __syncthreads();
-        if (w == 0) {
-            WarpRec rec = lane < kFastWarps ? wrec[lane]
-                                            : WarpRec{-INFINITY, INT32_MAX, 0u, 0u, -INFINITY, -INFINITY, 0.f, 0.f};
+        if (timeout && lane == 0) {
+            // give this warp's copies that may still be in flight a bounded chance to land
+            for (uint32_t g = consumed; g < P.issued; ++g)
+                (void)mbar_wait_bounded(&wbar[g % kFastStages], (g / kFastStages) & 1u);
+        }
+        return;
+    }
+
+    // ================= TV warps =================
+    const int ttid = tid - kStreamWarps * 32, tw = w - kStreamWarps;
+    uint32_t tto = 0;  // a wait of these warps gave up
+    int64_t unit = blockIdx.x;
+    for (uint32_t n = 0; unit < units; unit += gridDim.x, ++n) {
+        const uint32_t b = n & 1u;
+        const float T = unit_temp(A, unit);
+        const FastUnit u = fast_unit(A, unit, T);
+        const float c = u.sampling ? kLog2e / T : 0.f;
+        const int32_t xj = u.has_draft ? A.draft[static_cast<int64_t>(u.r) * A.k + u.j] : -1;
+        const uint64_t seed = (u.has_draft && ttid == 0) ? A.seeds[u.r] : 0ull;  // for the accept test
+        const uint16_t* G = reinterpret_cast<const uint16_t*>(gbase + b * gbytes);
+
+        // the first batch of draft-row loads, in flight while the stream warps finish the unit
+        constexpr int kTvIter = (kFastMaxVd / 8 + kTvThreads - 1) / kTvThreads;
+        constexpr int kTvBatch = 8;  // draft-row loads in flight per thread
+        const int32_t nv8 = u.has_draft ? A.Vd / 8 : 0;  // Vd % 8 == 0 on this path
+        const uint4* yv = reinterpret_cast<const uint4*>(u.drow);
+        uint4 yq[kTvBatch];
+#pragma unroll
+        for (int i = 0; i < kTvBatch; ++i) {
+            const int32_t v = ttid + i * kTvThreads;
+            if (v < nv8) yq[i] = ld_nc_v4(yv + v);
+        }
+        if (!tto && !mbar_wait_bounded(&full[b], (n >> 1) & 1u)) tto = 1;
+
+        // ---- merge the stream warps' records: max, first argmax, reference maxima, sums ----
+        if (tw == 0) {
+            WarpRec rec = lane < kStreamWarps ? wrec[b][lane]
+                                              : WarpRec{-INFINITY, INT32_MAX, 0u, 0u, -INFINITY, -INFINITY, 0.f, 0.f};
             float mbv = rec.bv, mtm = rec.tm, mdm = rec.dm;
             int32_t mbx = rec.bx;
             uint32_t ftl = rec.tfl, fdl = rec.dfl;
@@ -1264,49 +1327,43 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
             }
             if (lane == 0) merged = WarpRec{mbv, mbx, ftl, fdl, mtm, mdm, st, sd};
         }
-        __syncthreads();
+        tv_bar_sync();
         const float BV = merged.bv;
         float M = merged.tm, Mq = merged.dm;
         const float S = merged.ts, Sq = merged.ds;
         const uint32_t FLT = merged.tfl, FLD = merged.dfl;
-        if (tid == 0) amax_shared = merged.bx == INT32_MAX ? 0 : merged.bx;
+        const int32_t amax = merged.bx == INT32_MAX ? 0 : merged.bx;
         if (!u.sampling) M = -INFINITY;
         if (!u.has_draft) Mq = -INFINITY;
         uint32_t flags = 0;
         if (FLT & kFlagNaN) flags |= kFlagNaN;
-        if (FLT & kFlagTimeout) flags |= kFlagTimeout;
+        if ((FLT & kFlagTimeout) || tto) flags |= kFlagTimeout;
         if (BV == INFINITY) flags |= kFlagPosInf;
         if (BV == -INFINITY) flags |= kFlagAllNegInf;
         if (u.has_draft && ((FLD & (kFlagNaN | kFlagPosInf)) || Mq == -INFINITY)) flags |= kFlagDraftBad;
 
         // ---- TV = sum over the support of max(0, q - p); p(x_j), q(x_j), accept ----
         // G (z at every draft id) and the L2-resident draft row, in draft-id order; every
-        // thread issues all of its draft-row loads before the arithmetic
+        // thread issues a batch of draft-row loads before its arithmetic
         float tvv = NAN, pj = NAN, qj = NAN;
         int32_t acc = 0;
+        const float invS = 1.f / S, invSq = 1.f / Sq;
+        const int32_t jdx = jdx_s[b];
         if (u.has_draft) {
-            const float invS = 1.f / S, invSq = 1.f / Sq;
             const unsigned long long c2m = pack2(c, c), nM = pack2(-M, -M), nMq = pack2(-Mq, -Mq);
             const unsigned long long niS = pack2(-invS, -invS), iSq = pack2(invSq, invSq);
-            const int32_t jdx = jdx_shared;
             const uint4* gv = reinterpret_cast<const uint4*>(G);
             float a = 0.f;
-#pragma unroll
-            for (int b0 = 0; b0 < kTvIter; b0 += kTvBatch) {
-                uint4 yq[kTvBatch];
-#pragma unroll
-                for (int i = 0; i < kTvBatch; ++i) {
-                    const int32_t v = tid + (b0 + i) * kFastThreads;
-                    if (b0 == 0) yq[i] = yq0[i];
-                    else if (b0 + i < kTvIter && v < nv8) yq[i] = ld_nc_v4(yv + v);
-                }
+#pragma unroll 1
+            for (int b0 = 0; b0 < kTvIter && b0 * kTvThreads < nv8; b0 += kTvBatch) {
 #pragma unroll
                 for (int i = 0; i < kTvBatch; ++i) {
-                    const int32_t v = tid + (b0 + i) * kFastThreads;
-                    if (b0 + i >= kTvIter || v >= nv8) break;
+                    const int32_t v = ttid + (b0 + i) * kTvThreads;
+                    if (v >= nv8) break;
+                    const uint4 yqi = yq[i];
                     const uint4 gq = gv[v];
                     const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
-                    const uint32_t yw[4] = {yq[i].x, yq[i].y, yq[i].z, yq[i].w};
+                    const uint32_t yw[4] = {yqi.x, yqi.y, yqi.z, yqi.w};
                     float qv[8], dv[8];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -1329,17 +1386,25 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                     a += ((fmaxf(dv[0], 0.f) + fmaxf(dv[1], 0.f)) + (fmaxf(dv[2], 0.f) + fmaxf(dv[3], 0.f))) +
                          ((fmaxf(dv[4], 0.f) + fmaxf(dv[5], 0.f)) + (fmaxf(dv[6], 0.f) + fmaxf(dv[7], 0.f)));
                 }
+                // the next batch of draft-row loads
+#pragma unroll
+                for (int i = 0; i < kTvBatch; ++i) {
+                    const int32_t v = ttid + (b0 + kTvBatch + i) * kTvThreads;
+                    if (v < nv8) yq[i] = ld_nc_v4(yv + v);
+                }
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-            if (lane == 0) wtv[w] = a;
-            __syncthreads();
-            if (tid == 0) {
+            if (lane == 0) wtv[tw] = a;
+        }
+        tv_bar_sync();  // wtv and qx are written; G, jdx and merged are no longer read
+        if (ttid == 0) {
+            const float zraw = zx_s[b];
+            if (u.has_draft) {
                 tvv = 0.f;
-                for (int i = 0; i < kFastWarps; ++i) tvv += wtv[i];
+                for (int i = 0; i < kTvWarps; ++i) tvv += wtv[i];
                 const bool in_range = xj >= 0 && xj < A.V;
-                float zx = zx_shared;
-                zx = zx != zx ? -INFINITY : zx;
+                const float zx = zraw != zraw ? -INFINITY : zraw;
                 pj = in_range ? ex2(fmaf(zx, c, -M)) * invS : 0.f;
                 qj = (in_range && jdx >= 0) ? qx_shared : 0.f;
                 if (qj > 0.f) {
@@ -1349,17 +1414,12 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                     flags |= kFlagOffSupport;
                 }
             }
-        } else {
-            __syncthreads();  // amax_shared is visible to thread 0
-        }
-        if (tid == 0) {
-            const int32_t amax = amax_shared;
             RowStat rs;
             rs.m = M;
             rs.s = S;
             rs.mq = Mq;
             rs.sq = Sq;
-            rs.zx = zx_shared;
+            rs.zx = zraw;
             rs.p = pj;
             rs.q = qj;
             rs.amax = amax;
@@ -1372,16 +1432,12 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                 if (A.pd) A.pd[o] = pj;
                 if (A.qd) A.qd[o] = qj;
             }
+            zx_s[b] = NAN;  // fresh draft-token slots for the buffer's next unit
+            jdx_s[b] = -1;
         }
+        mbar_arrive(&freed[b]);
     }
-    if (timeout && lane == 0) {
-        // give this warp's copies that may still be in flight a bounded chance to land
-        for (uint32_t g = consumed; g < P.issued; ++g)
-            (void)mbar_wait_bounded(&wbar[g % kFastStages], (g / kFastStages) & 1u);
-    }
-}
-
-// ---------------------------------------------------------------------------
+}// ---------------------------------------------------------------------------
 // scan + two-level race + commit
 // ---------------------------------------------------------------------------
 // The correction token is a draw from w / sum(w), w = max(0, p - q) on the
@@ -1917,10 +1973,13 @@ SampleLayout sample_layout(int64_t R, int32_t k, int32_t V, int32_t Vd, int et, 
     return L;
 }
 
+// the opt-in shared memory of a CTA (227 KB) less room for the kernel's static arrays
+constexpr size_t kFastSmemLimit = 227 * 1024 - 1024;
+
 size_t fast_smem_bytes(int32_t V, int32_t Vd)
 {
-    return static_cast<size_t>(kFastHeader + kFastWarps * kFastStages * static_cast<int64_t>(kFastStage) +
-                               align256((static_cast<int64_t>(Vd) + 8) * 2) +
+    return static_cast<size_t>(kFastHeader + kStreamWarps * kFastStages * static_cast<int64_t>(kFastStage) +
+                               2 * align256((static_cast<int64_t>(Vd) + 8) * 2) +
                                (static_cast<int64_t>(V + kChunkElems - 1) / kChunkElems + 1) * 4);
 }
 
@@ -1928,7 +1987,7 @@ bool fast_path_ok(const Rows& t, const Rows& d, bool identity)
 {
     return !identity && t.dtype == SV_BF16 && d.dtype == SV_BF16 && t.bulk_ok && d.bulk_ok && d.data != nullptr &&
            t.width % 8 == 0 && d.width % 8 == 0 && d.width < kFastMaxVd &&  // 2 Vd fits 16 bits
-           fast_smem_bytes(t.width, d.width) <= 227 * 1024;
+           fast_smem_bytes(t.width, d.width) <= kFastSmemLimit;
 }
 
 }  // namespace
