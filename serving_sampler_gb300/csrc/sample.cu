@@ -343,6 +343,7 @@ __global__ void __launch_bounds__(kPlanThreads)
 // 4.  One CTA of one warp per chunk.
 namespace {
 constexpr int kMaxGroups = 128;  // 128 x 32 slots >= the 2048 entries a chunk can have
+constexpr int kPadSlots = 512;   // slots of every chunk that hold an entry or padding (the row pass's registers)
 constexpr int kBankCap = 2;
 struct GroupState {
     uint8_t r[kMaxGroups][32];  // loads per bank
@@ -395,7 +396,7 @@ __global__ void __launch_bounds__(32) d2t_group_kernel(int32_t Vd, int32_t V, D2
     }
     const int32_t nslots = 32 * ((ng + 3) & ~3);
     uint32_t* out = pl.pairs + static_cast<int64_t>(c) * kMaxGroups * 32;
-    for (int32_t i = lane; i < nslots; i += 32) out[i] = static_cast<uint32_t>(2 * Vd) << 16;
+    for (int32_t i = lane; i < max(nslots, kPadSlots); i += 32) out[i] = static_cast<uint32_t>(2 * Vd) << 16;
     __syncwarp();
     for (int32_t p = p0 + lane; p < p1; p += 32) {
         const uint32_t sl = slot_of[p - p0];
@@ -832,6 +833,7 @@ constexpr int kFastStages = 2;                   // per stream warp: one being r
 constexpr uint32_t kFastData = kChunkElems * 2;  // 4 KB of bf16 per stage
 constexpr uint32_t kFastStage = kFastData;
 constexpr int kPairRegs = 4;                     // uint4 groups of support entries per lane and chunk
+static_assert(kPairRegs * 4 * 32 == kPadSlots, "the plan pads every chunk to the slots the registers hold");
 constexpr int kFastHeader = 512;                 // the stage mbarriers, then the two unit handoffs
 static_assert((kStreamWarps * kFastStages + 4) * 8 <= kFastHeader, "mbarriers fit the header");
 constexpr int32_t kFastMaxVd = 32768;
@@ -890,14 +892,11 @@ __device__ __forceinline__ uint32_t first_max_offset(const uint4 (&qv)[kVL], flo
     return __reduce_min_sync(0xffffffffu, key);
 }
 
-// this lane's register groups of a chunk's padded support entries [p0, p1)
-__device__ __forceinline__ void load_pairs(const SampleArgs& A, int32_t p0, int32_t p1, int lane, uint4* pg)
+// this lane's register groups of the first kPadSlots (padded) support entries of a chunk
+__device__ __forceinline__ void load_pairs(const SampleArgs& A, int32_t p0, int lane, uint4* pg)
 {
 #pragma unroll
-    for (int t = 0; t < kPairRegs; ++t) {
-        const int32_t g = p0 + 4 * (lane + 32 * t);
-        pg[t] = g < p1 ? ld_nc_v4(reinterpret_cast<const uint4*>(A.plan.pairs + g)) : make_uint4(0u, 0u, 0u, 0u);
-    }
+    for (int t = 0; t < kPairRegs; ++t) pg[t] = ld_nc_v4(reinterpret_cast<const uint4*>(A.plan.pairs + p0 + 4 * (lane + 32 * t)));
 }
 
 
@@ -1037,7 +1036,6 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
     __shared__ float zx_s[2];      // target logit of the draft token
     __shared__ int32_t jdx_s[2];   // its draft id (-1: off the support)
     __shared__ WarpRec merged;     // TV warps: the unit's merged record
-    __shared__ float qx_shared;    // TV warps: q at the draft id
     __shared__ float wtv[kTvWarps];
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int32_t nchunks_t = (A.V + kChunkElems - 1) / kChunkElems;
@@ -1114,13 +1112,13 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                 const int32_t x0 = static_cast<int32_t>(off / 2);
                 // support entries of a target chunk: this lane's groups of four packed pairs, from
                 // L2 while the maxima and exponentials below run
-                const bool scatter = !is_draft && u.has_draft;
+                const bool scatter = !is_draft && u.has_draft && plan_ok;
                 float csum = 0.f;  // this lane's share of the chunk's sum, relative to its running max
                 int32_t p0 = 0, p1 = 0;
                 if (scatter) {
                     p0 = cidx * (kMaxGroups * 32);  // the chunk's slots: whole groups of four
                     p1 = p0 + ctab[cidx];
-                    if (pg_for != cidx) load_pairs(A, p0, p1, lane, pg);  // not prefetched
+                    if (pg_for != cidx) load_pairs(A, p0, lane, pg);  // not prefetched
                 }
                 if (nv < kVL * 32) {
                     // the row's last chunk: -inf beyond its end, so that every lane reads whole
@@ -1190,15 +1188,13 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                     const uint32_t zs_a = smem_addr(st), g_a = smem_addr(G);
                     const bool here = xj >= x0 && xj < x0 + static_cast<int32_t>(nb / 2);
 #pragma unroll
-                    for (int t = 0; t < kPairRegs; ++t) {
-                        if (p0 + 4 * (lane + 32 * t) < p1) {  // whole groups of four
-                            const uint32_t pe[4] = {pg[t].x, pg[t].y, pg[t].z, pg[t].w};
-                            uint32_t zv[4];
+                    for (int t = 0; t < kPairRegs; ++t) {  // every chunk has kPadSlots entries or padding
+                        const uint32_t pe[4] = {pg[t].x, pg[t].y, pg[t].z, pg[t].w};
+                        uint32_t zv[4];
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) zv[e] = lds_u16(zs_a + (pe[e] & 0xFFFFu));
+                        for (int e = 0; e < 4; ++e) zv[e] = lds_u16(zs_a + (pe[e] & 0xFFFFu));
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) sts_u16(g_a + (pe[e] >> 16), zv[e]);
-                        }
+                        for (int e = 0; e < 4; ++e) sts_u16(g_a + (pe[e] >> 16), zv[e]);
                     }
                     // groups beyond this lane's registers (chunks denser than 512 entries)
                     for (int32_t g = p0 + 4 * 32 * kPairRegs + 4 * lane; g < p1; g += 4 * 32) {
@@ -1212,13 +1208,11 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                         if (lane == 0) zx_s[b] = __uint_as_float(static_cast<uint32_t>(zs[xoff]) << 16);
 #pragma unroll
                         for (int t = 0; t < kPairRegs; ++t) {
-                            if (p0 + 4 * (lane + 32 * t) < p1) {
-                                const uint32_t pe[4] = {pg[t].x, pg[t].y, pg[t].z, pg[t].w};
+                            const uint32_t pe[4] = {pg[t].x, pg[t].y, pg[t].z, pg[t].w};
 #pragma unroll
-                                for (int e = 0; e < 4; ++e)
-                                    if ((pe[e] & 0xFFFFu) == 2 * xoff && static_cast<int32_t>(pe[e] >> 17) < A.Vd)
-                                        jdx_s[b] = static_cast<int32_t>(pe[e] >> 17);
-                            }
+                            for (int e = 0; e < 4; ++e)
+                                if ((pe[e] & 0xFFFFu) == 2 * xoff && static_cast<int32_t>(pe[e] >> 17) < A.Vd)
+                                    jdx_s[b] = static_cast<int32_t>(pe[e] >> 17);
                         }
                         for (int32_t g = p0 + 4 * 32 * kPairRegs + lane; g < p1; g += 32) {  // beyond the registers
                             const uint32_t pe = A.plan.pairs[g];
@@ -1232,9 +1226,9 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                     // unit: in flight until that chunk's scatter
                     const int32_t qn = q + kStreamWarps;
                     pg_for = -1;
-                    if (u.has_draft && qn < u.n && qn >= u.nd) {
+                    if (u.has_draft && plan_ok && qn < u.n && qn >= u.nd) {
                         pg_for = qn - u.nd;
-                        load_pairs(A, pg_for * (kMaxGroups * 32), pg_for * (kMaxGroups * 32) + ctab[pg_for], lane, pg);
+                        load_pairs(A, pg_for * (kMaxGroups * 32), lane, pg);
                     }
                 }
                 // the stage is read: refill it with this warp's next chunk
@@ -1364,7 +1358,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                     const uint4 gq = gv[v];
                     const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
                     const uint32_t yw[4] = {yqi.x, yqi.y, yqi.z, yqi.w};
-                    float qv[8], dv[8];
+                    float dv[8];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         // q and p of two ids at once: q - p = 2^(y c - Mq) / Sq - 2^(z c - M) / S
@@ -1375,13 +1369,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                         unpack2(tz, z0, z1);
                         const unsigned long long eq = pack2(ex2(y0), ex2(y1));
                         const unsigned long long np = mul2(pack2(ex2(z0), ex2(z1)), niS);
-                        unpack2(eq, qv[2 * e], qv[2 * e + 1]);  // q up to the factor 1 / Sq
                         unpack2(fma2(eq, iSq, np), dv[2 * e], dv[2 * e + 1]);
-                    }
-                    if (v == (jdx >> 3)) {  // this vector holds the draft token's draft id
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            if (e == (jdx & 7)) qx_shared = qv[e] * invSq;
                     }
                     a += ((fmaxf(dv[0], 0.f) + fmaxf(dv[1], 0.f)) + (fmaxf(dv[2], 0.f) + fmaxf(dv[3], 0.f))) +
                          ((fmaxf(dv[4], 0.f) + fmaxf(dv[5], 0.f)) + (fmaxf(dv[6], 0.f) + fmaxf(dv[7], 0.f)));
@@ -1397,7 +1385,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
             for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
             if (lane == 0) wtv[tw] = a;
         }
-        tv_bar_sync();  // wtv and qx are written; G, jdx and merged are no longer read
+        tv_bar_sync();  // wtv is written; G, jdx and merged are no longer read
         if (ttid == 0) {
             const float zraw = zx_s[b];
             if (u.has_draft) {
@@ -1406,7 +1394,12 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                 const bool in_range = xj >= 0 && xj < A.V;
                 const float zx = zraw != zraw ? -INFINITY : zraw;
                 pj = in_range ? ex2(fmaf(zx, c, -M)) * invS : 0.f;
-                qj = (in_range && jdx >= 0) ? qx_shared : 0.f;
+                if (in_range && jdx >= 0) {  // q at the draft id, as the TV pass takes it
+                    const uint32_t yb = reinterpret_cast<const uint16_t*>(u.drow)[jdx];
+                    qj = ex2(fmaf(__uint_as_float(yb << 16), c, -Mq)) * invSq;
+                } else {
+                    qj = 0.f;
+                }
                 if (qj > 0.f) {
                     const uint4 w4 = philox_block(philox_key(seed), 0u, static_cast<uint32_t>(u.j), kTagAccept);
                     acc = uniform_from_word(w4.x) < __fdiv_rn(pj, qj) ? 1 : 0;
