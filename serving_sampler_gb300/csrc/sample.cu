@@ -138,51 +138,56 @@ __device__ __forceinline__ bool in_support(const D2tPlan& pl, int32_t x)
     return (pl.bitmap[x >> 5] >> (x & 31)) & 1u;
 }
 
-// ---- block reductions (kRowThreads or kRaceThreads, any multiple of 32) ----
+// ---- block reductions (NT a multiple of 32, at most 1024 threads) ----
+// Each warp reduces with shuffles, lane 0 leaves the warp's value in scratch,
+// and every warp then reduces the NT / 32 values lane-parallel, so all threads
+// return the same result.
 template <int NT>
 __device__ __forceinline__ float block_sum(float v, float* scratch)
 {
+    static_assert(NT % 32 == 0 && NT <= 1024, "block size");
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    const int w = threadIdx.x >> 5;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __syncthreads();
-    if ((threadIdx.x & 31) == 0) scratch[w] = v;
+    if (lane == 0) scratch[w] = v;
     __syncthreads();
-    float t = 0.f;
-    for (int i = 0; i < NT / 32; ++i) t += scratch[i];
+    float t = lane < NT / 32 ? scratch[lane] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
     return t;
 }
 
 template <int NT>
 __device__ __forceinline__ float block_max(float v, float* scratch)
 {
+    static_assert(NT % 32 == 0 && NT <= 1024, "block size");
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    const int w = threadIdx.x >> 5;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __syncthreads();
-    if ((threadIdx.x & 31) == 0) scratch[w] = v;
+    if (lane == 0) scratch[w] = v;
     __syncthreads();
-    float t = -INFINITY;
-    for (int i = 0; i < NT / 32; ++i) t = fmaxf(t, scratch[i]);
+    float t = lane < NT / 32 ? scratch[lane] : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
     return t;
 }
 
 template <int NT>
 __device__ __forceinline__ uint32_t block_or(uint32_t v, uint32_t* scratch)
 {
+    static_assert(NT % 32 == 0 && NT <= 1024, "block size");
     v = __reduce_or_sync(0xffffffffu, v);
-    const int w = threadIdx.x >> 5;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __syncthreads();
-    if ((threadIdx.x & 31) == 0) scratch[w] = v;
+    if (lane == 0) scratch[w] = v;
     __syncthreads();
-    uint32_t t = 0;
-    for (int i = 0; i < NT / 32; ++i) t |= scratch[i];
-    return t;
+    return __reduce_or_sync(0xffffffffu, lane < NT / 32 ? scratch[lane] : 0u);
 }
 
-// (value, first position) maximum over the block
-template <int NT>
-__device__ __forceinline__ void block_argmax(float& v, int32_t& x, float* sv, int32_t* sx)
+// (value, position) pairs: the larger value, the lower position among equal values
+__device__ __forceinline__ void warp_argmax(float& v, int32_t& x)
 {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -193,20 +198,24 @@ __device__ __forceinline__ void block_argmax(float& v, int32_t& x, float* sv, in
             x = ox;
         }
     }
-    const int w = threadIdx.x >> 5;
+}
+
+// (value, first position) maximum over the block
+template <int NT>
+__device__ __forceinline__ void block_argmax(float& v, int32_t& x, float* sv, int32_t* sx)
+{
+    static_assert(NT % 32 == 0 && NT <= 1024, "block size");
+    warp_argmax(v, x);
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __syncthreads();
-    if ((threadIdx.x & 31) == 0) {
+    if (lane == 0) {
         sv[w] = v;
         sx[w] = x;
     }
     __syncthreads();
-    v = sv[0];
-    x = sx[0];
-    for (int i = 1; i < NT / 32; ++i)
-        if (sv[i] > v || (sv[i] == v && sx[i] < x)) {
-            v = sv[i];
-            x = sx[i];
-        }
+    v = lane < NT / 32 ? sv[lane] : -INFINITY;
+    x = lane < NT / 32 ? sx[lane] : INT32_MAX;
+    warp_argmax(v, x);
 }
 
 // ---- online (max, sum 2^(t - max)) over scaled logits t ----------------------
@@ -1457,6 +1466,8 @@ constexpr int kEvalChunks = 8;  // chunks summed together by the bounded chunk r
 constexpr int kEvalVecs = kRaceChunk / 8 / (kRaceRowThreads / kEvalChunks);  // 8-id vectors per thread
 static_assert(kRaceChunk == kChunkElems, "the row pass leaves one (max, sum) per race chunk");
 static_assert(kRaceChunk % (8 * 32) == 0, "a warp's 32 vectors lie in one chunk");
+static_assert(SV_MAX_K < kRaceRowThreads, "one thread per draft position");
+constexpr size_t kRaceWbufBytes = static_cast<size_t>(kEvalChunks) * kRaceChunk * 4;  // the bounded race's weights
 
 // z[0..8) of ids [x, x + 8) of a row (-inf at and beyond x_end; NaN read as -inf)
 template <int DT>
@@ -1536,6 +1547,7 @@ template <int DT, int DD>
 __global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArgs A)
 {
     pdl_wait_primary();
+    extern __shared__ __align__(16) float wbuf[];  // bounded race: [kEvalChunks][kRaceChunk] weights of a round
     __shared__ float wpart[kRaceMaxChunks][kWarpsPerChunk];  // per chunk, per warp: sum of w
     __shared__ float ppart[kRaceMaxChunks][kWarpsPerChunk];  // and of p
     __shared__ float lb_s[kRaceMaxChunks];    // lower bounds of the chunk keys
@@ -1543,29 +1555,50 @@ __global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArg
     __shared__ int32_t order_s[kRaceMaxChunks];
     __shared__ float bpart_s[kRaceWarps];
     __shared__ float best_s;
-    __shared__ int32_t bc_s;
+    __shared__ int32_t bc_s, bslot_s, bround_s;  // best chunk, its slot and round in the bounded race
+    __shared__ RowStat st_s[SV_MAX_K + 1];       // the request's row statistics
+    __shared__ float2 cst_s[kRaceMaxChunks];     // the selected row's chunk sums (bounded race)
     __shared__ float red_f[kRaceWarps];
     __shared__ int32_t red_i[kRaceWarps];
     __shared__ int32_t n_shared;
     __shared__ uint32_t fl_shared;
+    __shared__ __align__(8) uint64_t ybar;  // the bulk copy of the selected draft row (bounded race)
     const int tid = threadIdx.x, lane = tid & 31;
     const int32_t r = static_cast<int32_t>(blockIdx.x);
     const int32_t k = A.k;
     const RowStat* st = A.stats + static_cast<int64_t>(r) * (k + 1);
     const int32_t* d = A.draft + static_cast<int64_t>(r) * k;
     const float T = A.temp[r];
+    const int32_t nc = (A.V + kRaceChunk - 1) / kRaceChunk;
+
+    // everything the scan and the bounded race read, requested at once: the row statistics,
+    // the draft tokens and, when they fit two per thread, the chunk sums of every row
+    if (tid <= k) st_s[tid] = st[tid];
+    const int32_t dj = tid < k ? d[tid] : 0;
+    const float2* cst_r = A.cstat ? A.cstat + static_cast<int64_t>(r) * (k + 1) * A.nct : nullptr;
+    const bool cpre = cst_r != nullptr && (k + 1) * nc <= 2 * kRaceRowThreads;  // A.nct == nc
+    float2 cv0 = make_float2(0.f, 0.f), cv1 = make_float2(0.f, 0.f);
+    if (cpre) {
+        if (tid < (k + 1) * nc) cv0 = cst_r[tid];
+        if (tid + kRaceRowThreads < (k + 1) * nc) cv1 = cst_r[tid + kRaceRowThreads];
+    }
+    if (tid == 0) {
+        mbar_init(&ybar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
 
     // request-level decisions (warp 0, ballots)
     if (tid < 32) {
         uint32_t fl = 0;
-        for (int32_t j = lane; j <= k; j += 32) fl |= st[j].flags;
+        for (int32_t j = lane; j <= k; j += 32) fl |= st_s[j].flags;
         fl = __reduce_or_sync(0xffffffffu, fl);
         const bool bad_rows = (fl & (kFlagNaN | kFlagPosInf | kFlagAllNegInf | kFlagDraftBad)) != 0;
         const bool greedy = !(T > 0.f) || bad_rows;
         int32_t n = k;
         for (int32_t j0 = 0; j0 < k; j0 += 32) {
             const int32_t j = j0 + lane;
-            const bool fail = j < k && (greedy ? d[j] != st[j].amax : st[j].accept == 0);
+            const bool fail = j < k && (greedy ? d[j] != st_s[j].amax : st_s[j].accept == 0);
             const unsigned m = __ballot_sync(0xffffffffu, fail);
             if (m) {
                 n = j0 + __ffs(m) - 1;
@@ -1584,16 +1617,26 @@ __global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArg
     const bool greedy = !(T > 0.f) || bad_rows;
     int32_t token = -1;
     uint32_t status = 0;
+    // bounded race on a rejected row: its draft row into shared memory, one bulk copy that lands
+    // while the chunk bounds are ranked (the bulk-copy path has 16-byte rows and Vd % 8 == 0)
+    const bool ycopy = !greedy && cst_r != nullptr && n < k;
+    uint16_t* ybuf = reinterpret_cast<uint16_t*>(wbuf + kEvalChunks * kRaceChunk);
+    bool ywait = ycopy;  // the copy is still to be waited for
+    if (ycopy && tid == 0) {
+        const uint32_t yb_bytes = static_cast<uint32_t>(A.Vd) * 2;
+        mbar_arrive_expect_tx(&ybar, yb_bytes);
+        bulk_copy_g2s(ybuf, A.dbase + (static_cast<int64_t>(r) * k + n) * A.dstride, yb_bytes, &ybar,
+                      l2_policy_evict_first());
+    }
     if (greedy) {
-        token = st[n].amax;
+        token = st_s[n].amax;
     } else {
         const bool residual = n < k;
-        const RowStat rs = st[n];
+        const RowStat rs = st_s[n];
         const float c = kLog2e / T, invS = 1.f / rs.s, invSq = residual ? 1.f / rs.sq : 0.f;
         const char* trow = A.tbase + (static_cast<int64_t>(r) * (k + 1) + n) * A.tstride;
         const char* drow = residual ? A.dbase + (static_cast<int64_t>(r) * k + n) * A.dstride : nullptr;
         const bool vec_ok = A.tbulk != 0, dvec_ok = A.dbulk != 0;
-        const int32_t nc = (A.V + kRaceChunk - 1) / kRaceChunk;
         const int32_t nvec = (A.V + 7) / 8;
 
         const PhiloxKey key = philox_key(A.seeds[r]);
@@ -1601,6 +1644,7 @@ __global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArg
         const uint32_t tag_x = residual ? kTagResidual : kTagBonus;
         bool use_p = !residual;
         int32_t bc = INT32_MAX;
+        int32_t bslot = -1;  // the slot of wbuf that holds chunk bc's weights, if any
         if (A.cstat == nullptr) {
         // ---- chunk sums of w and p: each warp's 32 vectors lie in one chunk ----
         constexpr int kZW = DT == SV_BF16 ? 1 : 2;  // 16-byte words per 8-id vector
@@ -1729,9 +1773,16 @@ __global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArg
             // bounds the chunk's weight sum W_c, so E_c / P_c bounds its key from below.
             // Chunks are summed exactly in the order of these bounds, a batch at a time,
             // until the next bound exceeds the best exact key. ----
-            const float2* cst = A.cstat + (static_cast<int64_t>(r) * (k + 1) + n) * A.nct;
+            if (cpre) {
+                const int32_t t0 = n * nc;
+                if (tid >= t0 && tid < t0 + nc) cst_s[tid - t0] = cv0;
+                if (tid + kRaceRowThreads >= t0 && tid + kRaceRowThreads < t0 + nc) cst_s[tid + kRaceRowThreads - t0] = cv1;
+            } else {
+                for (int32_t cc = tid; cc < nc; cc += kRaceRowThreads) cst_s[cc] = cst_r[static_cast<int64_t>(n) * A.nct + cc];
+            }
+            __syncthreads();
             for (int32_t cc = tid; cc < nc; cc += kRaceRowThreads) {
-                const float2 v = cst[cc];
+                const float2 v = cst_s[cc];
                 const float pc = v.y > 0.f ? v.y * ex2(v.x - rs.m) * invS : 0.f;
                 const uint4 w4 = philox_block(key, static_cast<uint32_t>(cc >> 2), static_cast<uint32_t>(n), tag_c);
                 const uint32_t wd = (cc & 3) == 0 ? w4.x : ((cc & 3) == 1 ? w4.y : ((cc & 3) == 2 ? w4.z : w4.w));
@@ -1741,41 +1792,105 @@ __global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArg
                 lb_s[cc] = pc > 0.f ? __fdiv_rn(e, pc * 1.0001f) : INFINITY;
             }
             __syncthreads();
-            for (int32_t cc = tid; cc < nc; cc += kRaceRowThreads) {
+            // rank of every bound (ties by chunk id): one warp per chunk, 32 comparisons a ballot
+            for (int32_t cc = tid >> 5; cc < nc; cc += kRaceWarps) {
                 const float l = lb_s[cc];
                 int32_t rk = 0;
-                for (int32_t o = 0; o < nc; ++o) {
-                    const float lo = lb_s[o];
-                    rk += (lo < l || (lo == l && o < cc)) ? 1 : 0;
+                for (int32_t o0 = 0; o0 < nc; o0 += 32) {
+                    const int32_t o = o0 + lane;
+                    const float lo = o < nc ? lb_s[o] : INFINITY;
+                    rk += __popc(__ballot_sync(0xffffffffu, o < nc && (lo < l || (lo == l && o < cc))));
                 }
-                order_s[rk] = cc;
+                if (lane == 0) order_s[rk] = cc;
             }
             for (int pass = 0; pass < (residual ? 2 : 1); ++pass) {
                 const bool wp = !residual || pass == 1;  // weights p (bonus, or no residual mass)
                 if (tid == 0) {
                     best_s = INFINITY;
                     bc_s = INT32_MAX;
+                    bslot_s = -1;
+                    bround_s = -1;
                 }
                 __syncthreads();
+                if (!wp && ywait) {  // the draft row in shared memory
+                    if (!mbar_wait_bounded(&ybar, 0)) status |= SV_ST_TIMEOUT;
+                    ywait = false;
+                }
+                int32_t last_r0 = -1;  // the round whose weights wbuf holds
                 for (int32_t r0 = 0; r0 < nc; r0 += kEvalChunks) {
                     if (lb_s[order_s[r0]] > best_s) break;  // block-uniform: read after a barrier
+                    last_r0 = r0;
                     const int slot = tid / (kRaceRowThreads / kEvalChunks);
                     const int sub = tid % (kRaceRowThreads / kEvalChunks);
                     float ws = 0.f;
                     if (r0 + slot < nc) {
                         const int32_t cc = order_s[r0 + slot];
                         const int32_t cx1 = min(A.V, (cc + 1) * kRaceChunk);
+                        float* wb = wbuf + slot * kRaceChunk;
+                        const bool full = cx1 == (cc + 1) * kRaceChunk && vec_ok && (wp || (dvec_ok && !A.identity));
+                        if (DT == SV_BF16 && DD == SV_BF16 && full) {
+                            // every load of the thread first: the target words and the draft ids of its
+                            // vectors, then the draft-row values of the support ids among them
+                            uint4 tw[kEvalVecs], jw[kEvalVecs];
 #pragma unroll
-                        for (int hv = 0; hv < kEvalVecs; ++hv) {
-                            const int32_t x = cc * kRaceChunk + 8 * (kEvalVecs * sub + hv);
-                            float z[8], q[8];
-                            load8<DT>(trow, x, cx1, vec_ok, z);
-                            if (!wp) q8<DD>(A, drow, x, cx1, dvec_ok, c, rs.mq, invSq, q);
+                            for (int hv = 0; hv < kEvalVecs; ++hv) {
+                                const int32_t x = cc * kRaceChunk + 8 * (kEvalVecs * sub + hv);
+                                tw[hv] = ld_nc_v4(reinterpret_cast<const uint4*>(trow + static_cast<int64_t>(x) * 2));
+                                if (!wp) jw[hv] = ld_nc_v4(reinterpret_cast<const uint4*>(A.plan.jmap + x));
+                            }
+                            uint32_t yb[kEvalVecs][8];
+                            const uint32_t ya = smem_addr(ybuf);
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                if (x + e >= cx1) break;
-                                const float pe = ex2(fmaf(z[e], c, -rs.m)) * invS;
-                                ws += wp ? pe : fmaxf(pe - q[e], 0.f);
+                            for (int hv = 0; hv < kEvalVecs; ++hv) {
+                                const uint32_t jv[4] = {jw[hv].x, jw[hv].y, jw[hv].z, jw[hv].w};
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    const uint32_t jm = (e & 1) ? jv[e >> 1] >> 16 : jv[e >> 1] & 0xFFFFu;
+                                    yb[hv][e] = 0xFF80u;  // -inf: off the support
+                                    if (!wp && jm < static_cast<uint32_t>(A.Vd)) yb[hv][e] = lds_u16(ya + 2 * jm);
+                                }
+                            }
+#pragma unroll
+                            for (int hv = 0; hv < kEvalVecs; ++hv) {
+                                const int32_t xo = 8 * (kEvalVecs * sub + hv);
+                                const uint32_t zv[4] = {tw[hv].x, tw[hv].y, tw[hv].z, tw[hv].w};
+                                float wv[8];
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    float ze = (e & 1) ? bf16_hi(zv[e >> 1]) : bf16_lo(zv[e >> 1]);
+                                    ze = ze != ze ? -INFINITY : ze;
+                                    const float pe = ex2(fmaf(ze, c, -rs.m)) * invS;
+                                    if (wp) {
+                                        wv[e] = pe;
+                                    } else {
+                                        float y = __uint_as_float(yb[hv][e] << 16);
+                                        y = y != y ? -INFINITY : y;
+                                        wv[e] = fmaxf(pe - ex2(fmaf(y, c, -rs.mq)) * invSq, 0.f);
+                                    }
+                                    ws += wv[e];
+                                }
+                                // kept for the element race, should this chunk win
+                                reinterpret_cast<float4*>(wb + xo)[0] = make_float4(wv[0], wv[1], wv[2], wv[3]);
+                                reinterpret_cast<float4*>(wb + xo)[1] = make_float4(wv[4], wv[5], wv[6], wv[7]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int hv = 0; hv < kEvalVecs; ++hv) {
+                                const int32_t xo = 8 * (kEvalVecs * sub + hv);
+                                const int32_t x = cc * kRaceChunk + xo;
+                                float z[8], q[8], wv[8];
+                                load8<DT>(trow, x, cx1, vec_ok, z);
+                                if (!wp) q8<DD>(A, drow, x, cx1, dvec_ok, c, rs.mq, invSq, q);
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    wv[e] = 0.f;
+                                    if (x + e >= cx1) continue;
+                                    const float pe = ex2(fmaf(z[e], c, -rs.m)) * invS;
+                                    wv[e] = wp ? pe : fmaxf(pe - q[e], 0.f);
+                                    ws += wv[e];
+                                }
+                                reinterpret_cast<float4*>(wb + xo)[0] = make_float4(wv[0], wv[1], wv[2], wv[3]);
+                                reinterpret_cast<float4*>(wb + xo)[1] = make_float4(wv[4], wv[5], wv[6], wv[7]);
                             }
                         }
                     }
@@ -1783,17 +1898,32 @@ __global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArg
                     for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
                     if (lane == 0) bpart_s[tid >> 5] = ws;
                     __syncthreads();
-                    if (tid == 0) {
+                    if (tid < 32) {
+                        // lane sl: the key of slot sl's chunk; then the lowest key, lowest chunk id
                         constexpr int kWarpsPerSlot = kRaceWarps / kEvalChunks;
-                        for (int sl = 0; sl < kEvalChunks && r0 + sl < nc; ++sl) {
-                            const int32_t cc = order_s[r0 + sl];
+                        static_assert(kEvalChunks <= 32, "one lane per slot");
+                        float kc = INFINITY;
+                        int32_t ccl = INT32_MAX;
+                        if (lane < kEvalChunks && r0 + lane < nc) {
                             float wc = 0.f;
-                            for (int i = 0; i < kWarpsPerSlot; ++i) wc += bpart_s[sl * kWarpsPerSlot + i];
-                            if (!(wc > 0.f)) continue;
-                            const float kc = __fdiv_rn(ec_s[cc], wc);
-                            if (kc < best_s || (kc == best_s && cc < bc_s)) {
-                                best_s = kc;
-                                bc_s = cc;
+                            for (int i = 0; i < kWarpsPerSlot; ++i) wc += bpart_s[lane * kWarpsPerSlot + i];
+                            if (wc > 0.f) {
+                                ccl = order_s[r0 + lane];
+                                kc = __fdiv_rn(ec_s[ccl], wc);
+                            }
+                        }
+                        float nk = ccl == INT32_MAX ? -INFINITY : -kc;
+                        int32_t cw = ccl;
+                        warp_argmax(nk, cw);
+                        if (lane == 0 && cw != INT32_MAX) {
+                            const float kb2 = -nk;
+                            if (kb2 < best_s || (kb2 == best_s && cw < bc_s)) {
+                                best_s = kb2;
+                                bc_s = cw;
+                                int32_t sl = 0;
+                                while (order_s[r0 + sl] != cw) ++sl;
+                                bslot_s = sl;
+                                bround_s = r0;
                             }
                         }
                     }
@@ -1801,6 +1931,7 @@ __global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArg
                 }
                 if (bc_s != INT32_MAX) {
                     use_p = wp;
+                    if (bround_s == last_r0) bslot = bslot_s;  // no later round overwrote its weights
                     break;
                 }
                 if (residual && pass == 0) status |= SV_ST_RESIDUAL_ZERO;
@@ -1817,23 +1948,37 @@ __global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArg
             int32_t bx = INT32_MAX;
             const int32_t xb = cx0 + 4 * tid;
             if (tid < kRaceChunk / 4 && xb < cx1) {
-                float ze[4], qe[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float v = xb + e < cx1 ? ld_elem<DT>(trow, xb + e) : -INFINITY;
-                    ze[e] = v != v ? -INFINITY : v;
-                }
-                if (wq) {
+                float wgt[4];
+                if (bslot >= 0) {  // the weights the bounded race summed for this chunk
+                    const float4 w4v = reinterpret_cast<const float4*>(wbuf + bslot * kRaceChunk)[tid];
+                    wgt[0] = w4v.x;
+                    wgt[1] = w4v.y;
+                    wgt[2] = w4v.z;
+                    wgt[3] = w4v.w;
+                } else {
+                    float ze[4], qe[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int32_t x = xb + e;
-                        int32_t jd = -1;
-                        if (x < cx1) jd = A.identity ? x : (A.plan.jmap[x] == 0xFFFFu ? -1 : A.plan.jmap[x]);
-                        if (jd >= 0 && jd < A.Vd) {
-                            float y = ld_elem<DD>(drow, jd);
-                            y = y != y ? -INFINITY : y;
-                            qe[e] = ex2(fmaf(y, c, -rs.mq)) * invSq;
+                        const float v = xb + e < cx1 ? ld_elem<DT>(trow, xb + e) : -INFINITY;
+                        ze[e] = v != v ? -INFINITY : v;
+                    }
+                    if (wq) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int32_t x = xb + e;
+                            int32_t jd = -1;
+                            if (x < cx1) jd = A.identity ? x : (A.plan.jmap[x] == 0xFFFFu ? -1 : A.plan.jmap[x]);
+                            if (jd >= 0 && jd < A.Vd) {
+                                float y = ld_elem<DD>(drow, jd);
+                                y = y != y ? -INFINITY : y;
+                                qe[e] = ex2(fmaf(y, c, -rs.mq)) * invSq;
+                            }
                         }
+                    }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        wgt[e] = ex2(fmaf(ze[e], c, -rs.m)) * invS;
+                        if (wq) wgt[e] = fmaxf(wgt[e] - qe[e], 0.f);
                     }
                 }
                 const uint4 w4 = philox_block(key, static_cast<uint32_t>(xb >> 2), static_cast<uint32_t>(n), tag_x);
@@ -1841,8 +1986,7 @@ __global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArg
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     if (xb + e >= cx1) break;
-                    float we = ex2(fmaf(ze[e], c, -rs.m)) * invS;
-                    if (wq) we = fmaxf(we - qe[e], 0.f);
+                    const float we = wgt[e];
                     if (!(we > 0.f)) continue;
                     const float ke = __fdiv_rn(-log1pf(-one_minus_uniform_from_word(words[e])), we);
                     if (ke < kb) {
@@ -1857,15 +2001,14 @@ __global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArg
         if (residual && (rs.flags & kFlagOffSupport)) status |= SV_ST_OFF_SUPPORT;
     }
     // ---- commit ------------------------------------------------------------
-    for (int32_t j = tid; j < k; j += kRaceRowThreads)
-        if (d[j] < 0 || d[j] >= A.V) status |= SV_ST_TOKEN_RANGE;
+    if (tid < k && (dj < 0 || dj >= A.V)) status |= SV_ST_TOKEN_RANGE;  // k <= SV_MAX_K < kRaceRowThreads
     if (fl & kFlagTimeout) status |= SV_ST_TIMEOUT;
     if (bad_rows) status |= SV_ST_BAD_LOGITS;
     if (T < 0.f || T != T) status |= SV_ST_BAD_TEMP;
     if (!A.identity && (A.plan.header[2] != 0 || A.plan.header[0] != A.V || A.plan.header[1] != A.Vd))
         status |= SV_ST_BAD_D2T;
     int32_t* out = A.tokens + static_cast<int64_t>(r) * (k + 1);
-    for (int32_t j = tid; j <= k; j += kRaceRowThreads) out[j] = j < n ? d[j] : (j == n ? token : -1);
+    if (tid <= k) out[tid] = tid < n ? dj : (tid == n ? token : -1);
     if (greedy) {
         // no sampling statistics for greedily verified requests
         for (int32_t j = tid; j < k; j += kRaceRowThreads) {
@@ -1875,6 +2018,7 @@ __global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArg
             if (A.qd) A.qd[o] = NAN;
         }
     }
+    if (ywait && tid == 0) (void)mbar_wait_bounded(&ybar, 0);  // no copy outlives the CTA
     status = block_or<kRaceRowThreads>(status, reinterpret_cast<uint32_t*>(red_i));
     if (tid == 0) {
         A.accept_len[r] = n;
@@ -2084,10 +2228,15 @@ static cudaError_t launch_sample_t(const Rows& t, const Rows& d, const int32_t* 
         e = cudaLaunchKernelEx(&cfg, sample_rows_kernel<DT, DD>, A);
     }
     if (e != cudaSuccess) return e;
+    // the bounded race keeps a round's weights and the selected draft row in shared memory
+    const size_t race_smem = fast ? kRaceWbufBytes + static_cast<size_t>(align256(static_cast<int64_t>(d.width) * 2)) : 0;
+    e = cudaFuncSetAttribute(race_rows_kernel<DT, DD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(race_smem));
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg2 = {};
     cfg2.gridDim = dim3(static_cast<unsigned>(R));
     cfg2.blockDim = dim3(kRaceRowThreads);
-    cfg2.dynamicSmemBytes = 0;
+    cfg2.dynamicSmemBytes = race_smem;
     cfg2.stream = stream;
     cfg2.attrs = attr;
     cfg2.numAttrs = 1;
