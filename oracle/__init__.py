@@ -29,6 +29,7 @@ ST_RESIDUAL_ZERO, ST_BAD_TEMP, ST_BAD_D2T = 8, 16, 32
 TAG_ACCEPT, TAG_RESIDUAL, TAG_BONUS = 0, 1, 2
 TAG_RESIDUAL_CHUNK, TAG_BONUS_CHUNK = 3, 4
 RACE_CHUNK = 2048  # ids per chunk of the two-level race over the full target vocabulary
+CFG_RACE_CHUNK = 256  # ids per chunk of the two-level race over a CFG codebook row
 
 
 def build(force: bool = False) -> str:

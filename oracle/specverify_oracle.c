@@ -44,7 +44,8 @@
  *    chunks of RACE_CHUNK, the chunk c = argmin E_c / W_c (W_c the chunk's
  *    weight sum, E_c from tag 3 for the residual, 4 for the bonus, counted by
  *    c), then the element race inside that chunk; P(x) = w_x / sum w still.
- *    The per-codebook CFG rows use the one-level race.
+ *    The per-codebook CFG rows use the same two-level race with chunks of
+ *    CFG_RACE_CHUNK ids.
  *  - the uniform from a 32-bit word r is (2 * (r >> 9) + 1) * 2^-24.
  *  - NaN logits count as -inf.  A sampling request with a NaN, +inf or
  *    all -inf row is verified greedily and flagged (status bit 2).
@@ -75,6 +76,8 @@ enum { TAG_ACCEPT = 0, TAG_RESIDUAL = 1, TAG_BONUS = 2, TAG_RESIDUAL_CHUNK = 3, 
 
 /* ids per chunk of the two-level race over the full target vocabulary */
 #define RACE_CHUNK 2048
+/* ids per chunk of the two-level race over a CFG codebook row */
+#define CFG_RACE_CHUNK 256
 
 /* ------------------------------------------------------------------ */
 /* Philox4x32-10, from Salmon, Moraes, Dror, Shaw, "Parallel Random    */
@@ -612,7 +615,7 @@ int or_cfg_merge_sample(const void* cond, const void* uncond, int dtype, int64_t
             double mg = INFINITY;
             int32_t tok;
             if (n == k) {
-                tok = or_race(p, W, seeds[r], urow, TAG_BONUS, &mg);
+                tok = or_race2(p, W, CFG_RACE_CHUNK, seeds[r], urow, TAG_BONUS_CHUNK, TAG_BONUS, &mg);
             } else if (acc[n * S + s]) {
                 tok = d[n * S + s] - cb_id_base[s];
             } else {
@@ -629,10 +632,10 @@ int or_cfg_merge_sample(const void* cond, const void* uncond, int dtype, int64_t
                 if (!(ld >= 0 && ld < W && q[ld] > 0.0) && ld >= 0 && ld < W)
                     st |= OR_ST_OFF_SUPPORT;
                 if (mass > 0.0) {
-                    tok = or_race(w, W, seeds[r], urow, TAG_RESIDUAL, &mg);
+                    tok = or_race2(w, W, CFG_RACE_CHUNK, seeds[r], urow, TAG_RESIDUAL_CHUNK, TAG_RESIDUAL, &mg);
                 } else {
                     st |= OR_ST_RESIDUAL_ZERO;
-                    tok = or_race(p, W, seeds[r], urow, TAG_RESIDUAL, &mg);
+                    tok = or_race2(p, W, CFG_RACE_CHUNK, seeds[r], urow, TAG_RESIDUAL_CHUNK, TAG_RESIDUAL, &mg);
                 }
             }
             out[n * S + s] = cb_id_base[s] + tok;

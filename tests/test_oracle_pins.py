@@ -553,6 +553,43 @@ def test_cfg_weight_one_greedy_is_greedy_on_cond():
         assert out["tokens"][r, n].tolist() == (am[r, n] + base).tolist()
 
 
+def test_cfg_sampling_distribution_across_race_chunks():
+    """A codebook row spanning three chunks of the two-level race (the last one ragged), with
+    mass on a few ids in different chunks and on the long tail: the emitted token follows p
+    at the first frame, the residual where the draft was rejected, and p at the bonus frame."""
+    W, T, R, w = 2 * oracle.CFG_RACE_CHUNK + 4, 1.0, 8_000, 2.0
+    rng = np.random.default_rng(24)
+    heavy = np.array([3, 300, 513])
+    cz = rng.normal(0, 0.3, W).astype(np.float32)
+    uz = rng.normal(0, 0.3, W).astype(np.float32)
+    cb = rng.normal(0, 0.3, W).astype(np.float32)
+    cz[heavy] = [3.5, 3.0, 3.8]
+    cb[heavy] = [3.2, 3.8, 3.0]
+    yz = rng.normal(0, 0.5, W).astype(np.float32)
+    yz[[3, 100, 400]] = [8.0, 7.0, 6.0]
+
+    def merged(c):
+        return (np.float32(w) * (c - uz) + uz).astype(np.float64)  # fp32 roundings, widened
+
+    p = np.exp(merged(cz) / T); p /= p.sum()
+    pb = np.exp(merged(cb) / T); pb /= pb.sum()
+    q = np.exp(yz.astype(np.float64) / T); q /= q.sum()
+    x = rng.choice(W, size=R, p=q)
+    cond = np.empty((2 * R, W), np.float32)
+    cond[0::2] = cz
+    cond[1::2] = cb
+    uncond = np.tile(uz, (2 * R, 1))
+    seeds = rng.integers(0, 2 ** 63, size=R, dtype=np.uint64)
+    out = oracle.cfg_merge_sample(cond, uncond, [0], [0], 1, W, w, np.tile(yz, (R, 1)), R, 1,
+                                  x.reshape(R, 1, 1).astype(np.int32), seeds, np.full(R, T, np.float32))
+    first = out["tokens"][:, 0, 0]
+    acc = out["accept_len"] == 1
+    assert _chi2_ok(*_binned(first, p, heavy, oracle.CFG_RACE_CHUNK)) > CHI2_ALPHA
+    resid = np.maximum(0.0, p - q)
+    assert _chi2_ok(*_binned(first[~acc], resid, heavy, oracle.CFG_RACE_CHUNK)) > CHI2_ALPHA
+    assert _chi2_ok(*_binned(out["tokens"][acc, 1, 0], pb, heavy, oracle.CFG_RACE_CHUNK)) > CHI2_ALPHA
+
+
 def test_cfg_codebook_marginals_are_target():
     """Each codebook's emitted token at frame 0 follows its own p (S = 2)."""
     rng = np.random.default_rng(23)
