@@ -1457,17 +1457,53 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
 namespace {
 
 constexpr int32_t kRaceChunk = 2048;
-constexpr int kRaceRowThreads = 1024;
-constexpr int kRaceWarps = kRaceRowThreads / 32;
+constexpr int kRaceMinThreads = 512;  // the race CTA: 1024 threads, or 512 (two per SM) for many requests
 constexpr int kRaceInFlight = 4;  // 8-id vectors per thread loaded together
 constexpr int kRaceMaxChunks = kMaxPlanWords * 32 / kRaceChunk;  // V <= 819,200
 constexpr int kWarpsPerChunk = kRaceChunk / 8 / 32;              // 8
 constexpr int kEvalChunks = 8;  // chunks summed together by the bounded chunk race
-constexpr int kEvalVecs = kRaceChunk / 8 / (kRaceRowThreads / kEvalChunks);  // 8-id vectors per thread
+// 8-id vectors per thread of a round with NT threads
+template <int NT>
+__host__ __device__ constexpr int eval_vecs() { return kRaceChunk / 8 / (NT / kEvalChunks); }
 static_assert(kRaceChunk == kChunkElems, "the row pass leaves one (max, sum) per race chunk");
 static_assert(kRaceChunk % (8 * 32) == 0, "a warp's 32 vectors lie in one chunk");
-static_assert(SV_MAX_K < kRaceRowThreads, "one thread per draft position");
-constexpr size_t kRaceWbufBytes = static_cast<size_t>(kEvalChunks) * kRaceChunk * 4;  // the bounded race's weights
+static_assert(SV_MAX_K < kRaceMinThreads, "one thread per draft position");
+static_assert(eval_vecs<1024>() % 2 == 0 && eval_vecs<kRaceMinThreads>() % 2 == 0, "vectors two at a time");
+static_assert(kRaceChunk / 4 <= kRaceMinThreads, "the element race: four ids per thread");
+constexpr int kWbufSlots = 4;  // chunks of a round (the lowest bounds) whose weights are kept
+
+// Dynamic shared memory of the race kernel, sized by the request's positions and
+// chunks: row statistics, then for the bounded race the selected row's chunk sums,
+// bounds, E_c, bound order, the kept weights and the selected draft row; for the
+// full race the per-warp chunk partials.
+struct RaceSmem {
+    uint32_t st, cst, lb, ec, order, wbuf, ybuf, wpart, ppart, total;
+};
+
+__host__ __device__ inline RaceSmem race_smem_layout(int32_t k, int32_t nc, int32_t Vd, bool bounded)
+{
+    RaceSmem L{};
+    uint32_t off = 0;
+    auto take = [&](uint32_t bytes) {
+        const uint32_t o = off;
+        off += (bytes + 15u) & ~15u;
+        return o;
+    };
+    L.st = take(static_cast<uint32_t>(k + 1) * static_cast<uint32_t>(sizeof(RowStat)));
+    if (bounded) {
+        L.cst = take(static_cast<uint32_t>(nc) * 8u);
+        L.lb = take(static_cast<uint32_t>(nc) * 4u);
+        L.ec = take(static_cast<uint32_t>(nc) * 4u);
+        L.order = take(static_cast<uint32_t>(nc) * 4u);
+        L.wbuf = take(static_cast<uint32_t>(kWbufSlots) * kRaceChunk * 4u);
+        L.ybuf = take(static_cast<uint32_t>(Vd) * 2u);
+    } else {
+        L.wpart = take(static_cast<uint32_t>(nc) * kWarpsPerChunk * 4u);
+        L.ppart = take(static_cast<uint32_t>(nc) * kWarpsPerChunk * 4u);
+    }
+    L.total = off;
+    return L;
+}
 
 // z[0..8) of ids [x, x + 8) of a row (-inf at and beyond x_end; NaN read as -inf)
 template <int DT>
@@ -1534,30 +1570,26 @@ __device__ __forceinline__ void q8(const SampleArgs& A, const char* drow, int32_
 
 // (key, id) minimum over the block, lowest id among equal keys; threads
 // without a candidate pass (+inf, INT32_MAX)
+template <int NT>
 __device__ __forceinline__ void block_argmin_key(float& key, int32_t& id, float* sf, int32_t* si)
 {
     float nk = id == INT32_MAX ? -INFINITY : -key;
-    block_argmax<kRaceRowThreads>(nk, id, sf, si);
+    block_argmax<NT>(nk, id, sf, si);
     key = -nk;
 }
 
 }  // namespace
 
-template <int DT, int DD>
-__global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArgs A)
+template <int DT, int DD, int NT>
+__global__ void __launch_bounds__(NT, 1024 / NT) race_rows_kernel(SampleArgs A)
 {
+    constexpr int kRaceWarps = NT / 32;
+    constexpr int kEvalVecs = eval_vecs<NT>();
     pdl_wait_primary();
-    extern __shared__ __align__(16) float wbuf[];  // bounded race: [kEvalChunks][kRaceChunk] weights of a round
-    __shared__ float wpart[kRaceMaxChunks][kWarpsPerChunk];  // per chunk, per warp: sum of w
-    __shared__ float ppart[kRaceMaxChunks][kWarpsPerChunk];  // and of p
-    __shared__ float lb_s[kRaceMaxChunks];    // lower bounds of the chunk keys
-    __shared__ float ec_s[kRaceMaxChunks];    // E_c of every chunk
-    __shared__ int32_t order_s[kRaceMaxChunks];
+    extern __shared__ __align__(16) unsigned char rsm[];  // laid out by race_smem_layout
     __shared__ float bpart_s[kRaceWarps];
     __shared__ float best_s;
     __shared__ int32_t bc_s, bslot_s, bround_s;  // best chunk, its slot and round in the bounded race
-    __shared__ RowStat st_s[SV_MAX_K + 1];       // the request's row statistics
-    __shared__ float2 cst_s[kRaceMaxChunks];     // the selected row's chunk sums (bounded race)
     __shared__ float red_f[kRaceWarps];
     __shared__ int32_t red_i[kRaceWarps];
     __shared__ int32_t n_shared;
@@ -1570,17 +1602,27 @@ __global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArg
     const int32_t* d = A.draft + static_cast<int64_t>(r) * k;
     const float T = A.temp[r];
     const int32_t nc = (A.V + kRaceChunk - 1) / kRaceChunk;
+    const RaceSmem L = race_smem_layout(k, nc, A.Vd, A.cstat != nullptr);
+    RowStat* st_s = reinterpret_cast<RowStat*>(rsm + L.st);           // the request's row statistics
+    float2* cst_s = reinterpret_cast<float2*>(rsm + L.cst);           // the selected row's chunk sums
+    float* lb_s = reinterpret_cast<float*>(rsm + L.lb);               // lower bounds of the chunk keys
+    float* ec_s = reinterpret_cast<float*>(rsm + L.ec);               // E_c of every chunk
+    int32_t* order_s = reinterpret_cast<int32_t*>(rsm + L.order);     // chunks in bound order
+    float* wbuf = reinterpret_cast<float*>(rsm + L.wbuf);             // [kWbufSlots][kRaceChunk] kept weights
+    uint16_t* ybuf = reinterpret_cast<uint16_t*>(rsm + L.ybuf);       // the selected draft row
+    float* wpart = reinterpret_cast<float*>(rsm + L.wpart);           // full race: [chunk][warp] sums of w
+    float* ppart = reinterpret_cast<float*>(rsm + L.ppart);           // and of p
 
     // everything the scan and the bounded race read, requested at once: the row statistics,
     // the draft tokens and, when they fit two per thread, the chunk sums of every row
     if (tid <= k) st_s[tid] = st[tid];
     const int32_t dj = tid < k ? d[tid] : 0;
     const float2* cst_r = A.cstat ? A.cstat + static_cast<int64_t>(r) * (k + 1) * A.nct : nullptr;
-    const bool cpre = cst_r != nullptr && (k + 1) * nc <= 2 * kRaceRowThreads;  // A.nct == nc
+    const bool cpre = cst_r != nullptr && (k + 1) * nc <= 2 * NT;  // A.nct == nc
     float2 cv0 = make_float2(0.f, 0.f), cv1 = make_float2(0.f, 0.f);
     if (cpre) {
         if (tid < (k + 1) * nc) cv0 = cst_r[tid];
-        if (tid + kRaceRowThreads < (k + 1) * nc) cv1 = cst_r[tid + kRaceRowThreads];
+        if (tid + NT < (k + 1) * nc) cv1 = cst_r[tid + NT];
     }
     if (tid == 0) {
         mbar_init(&ybar, 1);
@@ -1620,7 +1662,6 @@ __global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArg
     // bounded race on a rejected row: its draft row into shared memory, one bulk copy that lands
     // while the chunk bounds are ranked (the bulk-copy path has 16-byte rows and Vd % 8 == 0)
     const bool ycopy = !greedy && cst_r != nullptr && n < k;
-    uint16_t* ybuf = reinterpret_cast<uint16_t*>(wbuf + kEvalChunks * kRaceChunk);
     bool ywait = ycopy;  // the copy is still to be waited for
     if (ycopy && tid == 0) {
         const uint32_t yb_bytes = static_cast<uint32_t>(A.Vd) * 2;
@@ -1650,13 +1691,13 @@ __global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArg
         constexpr int kZW = DT == SV_BF16 ? 1 : 2;  // 16-byte words per 8-id vector
         // the trip count is uniform across each warp (it depends on the warp's first vector),
         // so every lane takes part in the shuffles below
-        for (int32_t v0 = tid; v0 - lane < nvec; v0 += kRaceRowThreads * kRaceInFlight) {
+        for (int32_t v0 = tid; v0 - lane < nvec; v0 += NT * kRaceInFlight) {
             // raw target words and draft-id words of every vector first, all in flight together
             uint4 zr[kRaceInFlight][kZW];
             uint4 jr[kRaceInFlight];
 #pragma unroll
             for (int b = 0; b < kRaceInFlight; ++b) {
-                const int32_t x = (v0 + b * kRaceRowThreads) * 8;
+                const int32_t x = (v0 + b * NT) * 8;
                 if (vec_ok && x + 8 <= A.V && x >= 0) {
 #pragma unroll
                     for (int h = 0; h < kZW; ++h)
@@ -1667,7 +1708,7 @@ __global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArg
             }
 #pragma unroll
             for (int b = 0; b < kRaceInFlight; ++b) {
-                const int32_t v = v0 + b * kRaceRowThreads;
+                const int32_t v = v0 + b * NT;
                 const int32_t vw = v - lane;  // the warp's first vector
                 if (vw >= nvec) break;
                 float ws = 0.f, ps = 0.f;
@@ -1730,34 +1771,34 @@ __global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArg
                 if (lane == 0) {
                     const int32_t cc = vw * 8 / kRaceChunk;
                     const int32_t slot = (vw * 8 / 256) % kWarpsPerChunk;
-                    wpart[cc][slot] = ws;
-                    ppart[cc][slot] = ps;
+                    wpart[cc * kWarpsPerChunk + slot] = ws;
+                    ppart[cc * kWarpsPerChunk + slot] = ps;
                 }
             }
         }
         __syncthreads();
         // chunk sums in a fixed order; slots past the row's end hold nothing
         float wtot = 0.f;
-        for (int32_t cc = tid; cc < nc; cc += kRaceRowThreads) {
+        for (int32_t cc = tid; cc < nc; cc += NT) {
             const int32_t nslots = min(kWarpsPerChunk, (min(A.V, (cc + 1) * kRaceChunk) - cc * kRaceChunk + 255) / 256);
             float wc = 0.f, pc = 0.f;
             for (int i = 0; i < nslots; ++i) {
-                wc += wpart[cc][i];
-                pc += ppart[cc][i];
+                wc += wpart[cc * kWarpsPerChunk + i];
+                pc += ppart[cc * kWarpsPerChunk + i];
             }
-            wpart[cc][0] = wc;
-            ppart[cc][0] = pc;
+            wpart[cc * kWarpsPerChunk] = wc;
+            ppart[cc * kWarpsPerChunk] = pc;
             wtot += wc;
         }
-        wtot = block_sum<kRaceRowThreads>(wtot, red_f);
+        wtot = block_sum<NT>(wtot, red_f);
         if (residual && !(wtot > 0.f)) {
             use_p = true;
             status |= SV_ST_RESIDUAL_ZERO;
         }
         // ---- chunk race ----
         float best = INFINITY;
-        for (int32_t cc = tid; cc < nc; cc += kRaceRowThreads) {
-            const float wc = use_p ? ppart[cc][0] : wpart[cc][0];
+        for (int32_t cc = tid; cc < nc; cc += NT) {
+            const float wc = use_p ? ppart[cc * kWarpsPerChunk] : wpart[cc * kWarpsPerChunk];
             if (!(wc > 0.f)) continue;
             const uint4 w4 = philox_block(key, static_cast<uint32_t>(cc >> 2), static_cast<uint32_t>(n), tag_c);
             const uint32_t wd = (cc & 3) == 0 ? w4.x : ((cc & 3) == 1 ? w4.y : ((cc & 3) == 2 ? w4.z : w4.w));
@@ -1767,7 +1808,7 @@ __global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArg
                 bc = cc;
             }
         }
-        block_argmin_key(best, bc, red_f, red_i);
+        block_argmin_key<NT>(best, bc, red_f, red_i);
         } else {
             // ---- chunk race with bounds: the row pass left p's sum over every chunk, which
             // bounds the chunk's weight sum W_c, so E_c / P_c bounds its key from below.
@@ -1776,12 +1817,12 @@ __global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArg
             if (cpre) {
                 const int32_t t0 = n * nc;
                 if (tid >= t0 && tid < t0 + nc) cst_s[tid - t0] = cv0;
-                if (tid + kRaceRowThreads >= t0 && tid + kRaceRowThreads < t0 + nc) cst_s[tid + kRaceRowThreads - t0] = cv1;
+                if (tid + NT >= t0 && tid + NT < t0 + nc) cst_s[tid + NT - t0] = cv1;
             } else {
-                for (int32_t cc = tid; cc < nc; cc += kRaceRowThreads) cst_s[cc] = cst_r[static_cast<int64_t>(n) * A.nct + cc];
+                for (int32_t cc = tid; cc < nc; cc += NT) cst_s[cc] = cst_r[static_cast<int64_t>(n) * A.nct + cc];
             }
             __syncthreads();
-            for (int32_t cc = tid; cc < nc; cc += kRaceRowThreads) {
+            for (int32_t cc = tid; cc < nc; cc += NT) {
                 const float2 v = cst_s[cc];
                 const float pc = v.y > 0.f ? v.y * ex2(v.x - rs.m) * invS : 0.f;
                 const uint4 w4 = philox_block(key, static_cast<uint32_t>(cc >> 2), static_cast<uint32_t>(n), tag_c);
@@ -1820,58 +1861,64 @@ __global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArg
                 for (int32_t r0 = 0; r0 < nc; r0 += kEvalChunks) {
                     if (lb_s[order_s[r0]] > best_s) break;  // block-uniform: read after a barrier
                     last_r0 = r0;
-                    const int slot = tid / (kRaceRowThreads / kEvalChunks);
-                    const int sub = tid % (kRaceRowThreads / kEvalChunks);
+                    const int slot = tid / (NT / kEvalChunks);
+                    const int sub = tid % (NT / kEvalChunks);
                     float ws = 0.f;
                     if (r0 + slot < nc) {
                         const int32_t cc = order_s[r0 + slot];
                         const int32_t cx1 = min(A.V, (cc + 1) * kRaceChunk);
-                        float* wb = wbuf + slot * kRaceChunk;
+                        // the weights of the round's first kWbufSlots chunks (lowest bounds) are kept
+                        // for the element race, should one of them win
+                        float* wb = slot < kWbufSlots ? wbuf + slot * kRaceChunk : nullptr;
                         const bool full = cx1 == (cc + 1) * kRaceChunk && vec_ok && (wp || (dvec_ok && !A.identity));
                         if (DT == SV_BF16 && DD == SV_BF16 && full) {
-                            // every load of the thread first: the target words and the draft ids of its
-                            // vectors, then the draft-row values of the support ids among them
-                            uint4 tw[kEvalVecs], jw[kEvalVecs];
 #pragma unroll
-                            for (int hv = 0; hv < kEvalVecs; ++hv) {
-                                const int32_t x = cc * kRaceChunk + 8 * (kEvalVecs * sub + hv);
-                                tw[hv] = ld_nc_v4(reinterpret_cast<const uint4*>(trow + static_cast<int64_t>(x) * 2));
-                                if (!wp) jw[hv] = ld_nc_v4(reinterpret_cast<const uint4*>(A.plan.jmap + x));
-                            }
-                            uint32_t yb[kEvalVecs][8];
-                            const uint32_t ya = smem_addr(ybuf);
+                            for (int hv0 = 0; hv0 < kEvalVecs; hv0 += 2) {
+                                // every load of two vectors first: the target words and the draft ids,
+                                // then the draft-row values of the support ids among them
+                                uint4 tw[2], jw[2];
 #pragma unroll
-                            for (int hv = 0; hv < kEvalVecs; ++hv) {
-                                const uint32_t jv[4] = {jw[hv].x, jw[hv].y, jw[hv].z, jw[hv].w};
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) {
-                                    const uint32_t jm = (e & 1) ? jv[e >> 1] >> 16 : jv[e >> 1] & 0xFFFFu;
-                                    yb[hv][e] = 0xFF80u;  // -inf: off the support
-                                    if (!wp && jm < static_cast<uint32_t>(A.Vd)) yb[hv][e] = lds_u16(ya + 2 * jm);
+                                for (int hv = 0; hv < 2; ++hv) {
+                                    const int32_t x = cc * kRaceChunk + 8 * (kEvalVecs * sub + hv0 + hv);
+                                    tw[hv] = ld_nc_v4(reinterpret_cast<const uint4*>(trow + static_cast<int64_t>(x) * 2));
+                                    if (!wp) jw[hv] = ld_nc_v4(reinterpret_cast<const uint4*>(A.plan.jmap + x));
                                 }
-                            }
+                                uint32_t yb[2][8];
+                                const uint32_t ya = smem_addr(ybuf);
 #pragma unroll
-                            for (int hv = 0; hv < kEvalVecs; ++hv) {
-                                const int32_t xo = 8 * (kEvalVecs * sub + hv);
-                                const uint32_t zv[4] = {tw[hv].x, tw[hv].y, tw[hv].z, tw[hv].w};
-                                float wv[8];
+                                for (int hv = 0; hv < 2; ++hv) {
+                                    const uint32_t jv[4] = {jw[hv].x, jw[hv].y, jw[hv].z, jw[hv].w};
 #pragma unroll
-                                for (int e = 0; e < 8; ++e) {
-                                    float ze = (e & 1) ? bf16_hi(zv[e >> 1]) : bf16_lo(zv[e >> 1]);
-                                    ze = ze != ze ? -INFINITY : ze;
-                                    const float pe = ex2(fmaf(ze, c, -rs.m)) * invS;
-                                    if (wp) {
-                                        wv[e] = pe;
-                                    } else {
-                                        float y = __uint_as_float(yb[hv][e] << 16);
-                                        y = y != y ? -INFINITY : y;
-                                        wv[e] = fmaxf(pe - ex2(fmaf(y, c, -rs.mq)) * invSq, 0.f);
+                                    for (int e = 0; e < 8; ++e) {
+                                        const uint32_t jm = (e & 1) ? jv[e >> 1] >> 16 : jv[e >> 1] & 0xFFFFu;
+                                        yb[hv][e] = 0xFF80u;  // -inf: off the support
+                                        if (!wp && jm < static_cast<uint32_t>(A.Vd)) yb[hv][e] = lds_u16(ya + 2 * jm);
                                     }
-                                    ws += wv[e];
                                 }
-                                // kept for the element race, should this chunk win
-                                reinterpret_cast<float4*>(wb + xo)[0] = make_float4(wv[0], wv[1], wv[2], wv[3]);
-                                reinterpret_cast<float4*>(wb + xo)[1] = make_float4(wv[4], wv[5], wv[6], wv[7]);
+#pragma unroll
+                                for (int hv = 0; hv < 2; ++hv) {
+                                    const int32_t xo = 8 * (kEvalVecs * sub + hv0 + hv);
+                                    const uint32_t zv[4] = {tw[hv].x, tw[hv].y, tw[hv].z, tw[hv].w};
+                                    float wv[8];
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e) {
+                                        float ze = (e & 1) ? bf16_hi(zv[e >> 1]) : bf16_lo(zv[e >> 1]);
+                                        ze = ze != ze ? -INFINITY : ze;
+                                        const float pe = ex2(fmaf(ze, c, -rs.m)) * invS;
+                                        if (wp) {
+                                            wv[e] = pe;
+                                        } else {
+                                            float y = __uint_as_float(yb[hv][e] << 16);
+                                            y = y != y ? -INFINITY : y;
+                                            wv[e] = fmaxf(pe - ex2(fmaf(y, c, -rs.mq)) * invSq, 0.f);
+                                        }
+                                        ws += wv[e];
+                                    }
+                                    if (wb) {
+                                        reinterpret_cast<float4*>(wb + xo)[0] = make_float4(wv[0], wv[1], wv[2], wv[3]);
+                                        reinterpret_cast<float4*>(wb + xo)[1] = make_float4(wv[4], wv[5], wv[6], wv[7]);
+                                    }
+                                }
                             }
                         } else {
 #pragma unroll
@@ -1889,8 +1936,10 @@ __global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArg
                                     wv[e] = wp ? pe : fmaxf(pe - q[e], 0.f);
                                     ws += wv[e];
                                 }
-                                reinterpret_cast<float4*>(wb + xo)[0] = make_float4(wv[0], wv[1], wv[2], wv[3]);
-                                reinterpret_cast<float4*>(wb + xo)[1] = make_float4(wv[4], wv[5], wv[6], wv[7]);
+                                if (wb) {
+                                    reinterpret_cast<float4*>(wb + xo)[0] = make_float4(wv[0], wv[1], wv[2], wv[3]);
+                                    reinterpret_cast<float4*>(wb + xo)[1] = make_float4(wv[4], wv[5], wv[6], wv[7]);
+                                }
                             }
                         }
                     }
@@ -1931,7 +1980,8 @@ __global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArg
                 }
                 if (bc_s != INT32_MAX) {
                     use_p = wp;
-                    if (bround_s == last_r0) bslot = bslot_s;  // no later round overwrote its weights
+                    // the kept weights, if the chunk was among the kept ones of the last round
+                    if (bround_s == last_r0 && bslot_s < kWbufSlots) bslot = bslot_s;
                     break;
                 }
                 if (residual && pass == 0) status |= SV_ST_RESIDUAL_ZERO;
@@ -1995,13 +2045,13 @@ __global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArg
                     }
                 }
             }
-            block_argmin_key(kb, bx, red_f, red_i);
+            block_argmin_key<NT>(kb, bx, red_f, red_i);
             token = bx == INT32_MAX ? cx0 : bx;
         }
         if (residual && (rs.flags & kFlagOffSupport)) status |= SV_ST_OFF_SUPPORT;
     }
     // ---- commit ------------------------------------------------------------
-    if (tid < k && (dj < 0 || dj >= A.V)) status |= SV_ST_TOKEN_RANGE;  // k <= SV_MAX_K < kRaceRowThreads
+    if (tid < k && (dj < 0 || dj >= A.V)) status |= SV_ST_TOKEN_RANGE;  // k <= SV_MAX_K < NT
     if (fl & kFlagTimeout) status |= SV_ST_TIMEOUT;
     if (bad_rows) status |= SV_ST_BAD_LOGITS;
     if (T < 0.f || T != T) status |= SV_ST_BAD_TEMP;
@@ -2011,7 +2061,7 @@ __global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArg
     if (tid <= k) out[tid] = tid < n ? dj : (tid == n ? token : -1);
     if (greedy) {
         // no sampling statistics for greedily verified requests
-        for (int32_t j = tid; j < k; j += kRaceRowThreads) {
+        for (int32_t j = tid; j < k; j += NT) {
             const int64_t o = static_cast<int64_t>(r) * k + j;
             if (A.tv) A.tv[o] = NAN;
             if (A.pd) A.pd[o] = NAN;
@@ -2019,7 +2069,7 @@ __global__ void __launch_bounds__(kRaceRowThreads, 1) race_rows_kernel(SampleArg
         }
     }
     if (ywait && tid == 0) (void)mbar_wait_bounded(&ybar, 0);  // no copy outlives the CTA
-    status = block_or<kRaceRowThreads>(status, reinterpret_cast<uint32_t*>(red_i));
+    status = block_or<NT>(status, reinterpret_cast<uint32_t*>(red_i));
     if (tid == 0) {
         A.accept_len[r] = n;
         if (A.status) A.status[r] = static_cast<int32_t>(status);
@@ -2228,19 +2278,20 @@ static cudaError_t launch_sample_t(const Rows& t, const Rows& d, const int32_t* 
         e = cudaLaunchKernelEx(&cfg, sample_rows_kernel<DT, DD>, A);
     }
     if (e != cudaSuccess) return e;
-    // the bounded race keeps a round's weights and the selected draft row in shared memory
-    const size_t race_smem = fast ? kRaceWbufBytes + static_cast<size_t>(align256(static_cast<int64_t>(d.width) * 2)) : 0;
-    e = cudaFuncSetAttribute(race_rows_kernel<DT, DD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(race_smem));
+    // one CTA per request: 1024 threads while the requests fit one CTA per SM, else 512 (two per SM)
+    const bool wide = R <= (sms > 0 ? sms : 148);
+    const size_t race_smem = race_smem_layout(k, A.nct, d.width, fast).total;
+    auto* race = wide ? race_rows_kernel<DT, DD, 1024> : race_rows_kernel<DT, DD, kRaceMinThreads>;
+    e = cudaFuncSetAttribute(race, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(race_smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg2 = {};
     cfg2.gridDim = dim3(static_cast<unsigned>(R));
-    cfg2.blockDim = dim3(kRaceRowThreads);
+    cfg2.blockDim = dim3(wide ? 1024 : kRaceMinThreads);
     cfg2.dynamicSmemBytes = race_smem;
     cfg2.stream = stream;
     cfg2.attrs = attr;
     cfg2.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg2, race_rows_kernel<DT, DD>, A);
+    return cudaLaunchKernelEx(&cfg2, race, A);
 }
 
 cudaError_t launch_verify_sample(const Rows& target, const Rows& draft_logits, const int32_t* d2t,

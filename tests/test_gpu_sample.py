@@ -98,6 +98,16 @@ def test_d2t_shapes(sv, dtype, ddtype, V, Vd, R, k, row_pad):
     compare(_run(sv, w), _oracle(w))
 
 
+@pytest.mark.parametrize("dtype,V,Vd", [(torch.bfloat16, 20000, 4096), (torch.float32, 6000, 1500)])
+def test_more_requests_than_sms(sv, dtype, V, Vd):
+    """More requests than SMs: the race runs as 512-thread CTAs, two per SM (bulk-copy and
+    general row paths)."""
+    R, k = 200, 3
+    T = [(0.7, 1.0, 0.0, 0.45)[i % 4] for i in range(R)]
+    w = workloads.sample_batch(R, k, V, Vd, dtype, T=T, sigma_pos=0.8, delta=2.7, seed=V + 7)
+    compare(_run(sv, w), _oracle(w))
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_sweep_point_mixed_greedy_and_sampling(sv, dtype):
     """A point of the throughput sweep: 9 positions (8 drafts + bonus), V = 151,936, the d2t
