@@ -243,7 +243,8 @@ int sv_d2t_plan_build(const int32_t* d2t, int32_t Vd, int32_t V, void* plan, siz
  * fmaf(w, d, u).  A frame is accepted when all S codebooks pass; at the
  * first rejected frame n each codebook keeps its draft if its own test
  * passed, else takes its residual sample (Philox row n * S + s); uniforms of
- * (frame j, codebook s) use Philox row j * S + s.
+ * (frame j, codebook s) use Philox row j * S + s.  The residual and bonus
+ * draws are the two-level race of sv_verify_sample with 256-id chunks.
  * ---------------------------------------------------------------------- */
 size_t sv_cfg_merge_sample_workspace(int32_t R, int32_t k, int32_t S, int32_t W);
 int sv_cfg_merge_sample(sv_rows cond, sv_rows uncond, const int32_t* cb_id_base,
