@@ -814,20 +814,21 @@ __global__ void __launch_bounds__(kRowThreads, 1) sample_rows_kernel(SampleArgs 
 // ---------------------------------------------------------------------------
 // row pass, fast path: bf16 target and draft rows, d2t vocabulary <= 32768
 // ---------------------------------------------------------------------------
-// Two warp roles.  Each stream warp pulls its own share of a row through a
-// private ring of kFastStages bulk-copied stages.  The chunks of a (request,
-// position) unit, draft chunks first and then target chunks, form one
-// sequence; element s of the sequence belongs to stream warp s % kStreamWarps,
-// so the warps get equal shares.  The warp's lane 0 keeps all stages in
+// Two warp roles.  Each stream warp pulls its own share of a target row
+// through a private ring of kFastStages bulk-copied stages: chunk s of a
+// (request, position) unit belongs to stream warp s % kStreamWarps, so the
+// warps get equal shares.  The warp's lane 0 keeps all stages in
 // flight: each consumed stage is refilled at once with the warp's next chunk,
 // of this unit or of the CTA's next one.  The support entries of a target
 // chunk, packed (draft id, offset) pairs of the plan, come from L2 into
 // registers while the chunk's maxima and exponentials are taken; the warp then
 // scatters the support logits to G[draft id] from shared memory.
 //
-// The TV warps finish unit n (merge of the stream warps' records, the TV pass
-// over G and the L2-resident draft row, p and q at the draft token, the accept
-// test) while the stream warps already read unit n + 1: G, the warp records
+// The TV warps read the draft row of unit n themselves (its maximum, sum and
+// flags) while the stream warps read the target row, then finish unit n (merge
+// of the stream warps' records, the TV pass over G and the L2-resident draft
+// row, p and q at the draft token, the accept test) while the stream warps
+// already read unit n + 1: G, the warp records
 // and the draft-token slots are double-buffered by unit parity, and two
 // mbarrier pairs hand a buffer over (full: the stream warps are done with it;
 // freed: the TV warps are).
@@ -909,6 +910,16 @@ __device__ __forceinline__ void load_pairs(const SampleArgs& A, int32_t p0, int 
 }
 
 
+// 16-byte read-only global load with an L2 cache policy
+__device__ __forceinline__ uint4 ld_nc_v4_hint(const uint4* p, uint64_t pol)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+
 // order this thread's generic-proxy accesses to shared memory before later
 // bulk copies (async proxy) into the same bytes
 __device__ __forceinline__ void fence_proxy_async_smem()
@@ -926,11 +937,16 @@ __device__ __forceinline__ uint32_t bf16x2_nan_to_ninf(uint32_t w)
 }
 
 struct WarpRec {
-    float bv;      // max of the target logits
-    int32_t bx;    // its first id
-    uint32_t tfl, dfl;
-    float tm, dm;  // reference maxima (log2 units) of the target and draft sums
-    float ts, ds;  // the sums
+    float bv;     // max of the target logits
+    int32_t bx;   // its first id
+    uint32_t tfl; // flags of the target row
+    float tm;     // reference maximum (log2 units) of the target sum
+    float ts;     // the sum
+};
+
+struct DraftRec {  // a TV warp's share of the draft row
+    float m, s;    // reference maximum (log2 units) and sum
+    uint32_t fl;   // flags
 };
 
 struct FastUnit {
@@ -938,7 +954,7 @@ struct FastUnit {
     bool sampling, has_draft;
     const char* trow;
     const char* drow;
-    int32_t nd, n;  // draft chunks, all chunks (draft then target) of the unit
+    int32_t n;      // target chunks of the unit
 };
 
 __device__ __forceinline__ FastUnit fast_unit(const SampleArgs& A, int64_t unit, float T)
@@ -951,8 +967,7 @@ __device__ __forceinline__ FastUnit fast_unit(const SampleArgs& A, int64_t unit,
     u.has_draft = u.sampling && u.j < A.k;
     u.trow = A.tbase + unit * A.tstride;
     u.drow = u.has_draft ? A.dbase + (static_cast<int64_t>(u.r) * A.k + u.j) * A.dstride : nullptr;
-    u.nd = u.has_draft ? (A.Vd + kChunkElems - 1) / kChunkElems : 0;
-    u.n = u.nd + (A.V + kChunkElems - 1) / kChunkElems;
+    u.n = (A.V + kChunkElems - 1) / kChunkElems;
     return u;
 }
 
@@ -969,13 +984,12 @@ __device__ __forceinline__ float unit_temp(const SampleArgs& A, int64_t unit)
 
 // issue sequence element q of unit u into `stage` (lane 0 only)
 __device__ __forceinline__ void issue_seq(const SampleArgs& A, const FastUnit& u, int32_t q, unsigned char* stage,
-                                          uint64_t* bar, uint64_t pol_t, uint64_t pol_d)
+                                          uint64_t* bar, uint64_t pol_t)
 {
-    const bool is_draft = q < u.nd;
-    const uint32_t off = static_cast<uint32_t>(is_draft ? q : q - u.nd) * kFastData;
-    const uint32_t nb = min(kFastData, static_cast<uint32_t>(is_draft ? A.Vd : A.V) * 2 - off);
+    const uint32_t off = static_cast<uint32_t>(q) * kFastData;
+    const uint32_t nb = min(kFastData, static_cast<uint32_t>(A.V) * 2 - off);
     mbar_arrive_expect_tx(bar, nb);
-    bulk_copy_g2s(stage, (is_draft ? u.drow : u.trow) + off, nb, bar, is_draft ? pol_d : pol_t);
+    bulk_copy_g2s(stage, u.trow + off, nb, bar, pol_t);
 }
 
 // The producer side of a warp's ring: the next chunk to issue (unit, index in
@@ -1005,12 +1019,11 @@ __device__ __forceinline__ void producer_enter(const SampleArgs& A, Producer& P,
 
 // issue the warp's next chunk if a stage is free
 __device__ __forceinline__ void producer_step(const SampleArgs& A, Producer& P, uint32_t consumed, int w, int lane,
-                                              int64_t units, unsigned char* wst, uint64_t* wbar, uint64_t pol_t,
-                                              uint64_t pol_d)
+                                              int64_t units, unsigned char* wst, uint64_t* wbar, uint64_t pol_t)
 {
     if (P.unit >= units || P.issued - consumed >= static_cast<uint32_t>(kFastStages)) return;
     const uint32_t sidx = P.issued % kFastStages;
-    if (lane == 0) issue_seq(A, P.u, w + P.i * kStreamWarps, wst + sidx * kFastStage, &wbar[sidx], pol_t, pol_d);
+    if (lane == 0) issue_seq(A, P.u, w + P.i * kStreamWarps, wst + sidx * kFastStage, &wbar[sidx], pol_t);
     ++P.issued;
     if (++P.i == P.cnt) {
         P.unit += gridDim.x;
@@ -1045,6 +1058,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
     __shared__ float zx_s[2];      // target logit of the draft token
     __shared__ int32_t jdx_s[2];   // its draft id (-1: off the support)
     __shared__ WarpRec merged;     // TV warps: the unit's merged record
+    __shared__ DraftRec drec[kTvWarps];  // TV warps: their shares of the draft row
     __shared__ float wtv[kTvWarps];
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int32_t nchunks_t = (A.V + kChunkElems - 1) / kChunkElems;
@@ -1073,8 +1087,6 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
     if (w < kStreamWarps) {
         // ================= stream warps =================
         const uint64_t pol_t = l2_policy_evict_first();
-        uint64_t pol_d;
-        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_d));
         unsigned char* wst = ring + w * kFastStages * kFastStage;  // this warp's stages
         uint64_t* wbar = bars + kFastStages * w;
         uint32_t consumed = 0;  // chunks this warp has read so far (stage = consumed % kFastStages)
@@ -1085,7 +1097,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
         P.issued = 0;
         producer_enter(A, P, w, units, P.unit < units ? unit_temp(A, P.unit) : 0.f);
         for (int i = 0; i < kFastStages; ++i)
-            producer_step(A, P, consumed, w, lane, units, wst, wbar, pol_t, pol_d);
+            producer_step(A, P, consumed, w, lane, units, wst, wbar, pol_t);
 
         int64_t unit = blockIdx.x;
         float T = unit < units ? unit_temp(A, unit) : 0.f;
@@ -1102,9 +1114,9 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
             // the TV warps are done with this buffer's previous unit
             if (n >= 2 && !timeout && !mbar_wait_bounded(&freed[b], ((n >> 1) + 1) & 1u)) timeout = 1;
 
-            float dm = -INFINITY, ds = 0.f, tm = -INFINITY, ts = 0.f, bv = -INFINITY;
+            float tm = -INFINITY, ts = 0.f, bv = -INFINITY;
             int32_t bx = INT32_MAX;
-            uint32_t dflags = 0, tflags = 0;
+            uint32_t tflags = 0;
             uint4 pg[kPairRegs];  // support entries of the target chunk pg_for (-1: none)
             int32_t pg_for = -1;
             for (int32_t i = 0; i < nw_chunks; ++i) {
@@ -1113,15 +1125,14 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                 const unsigned char* st = wst + sidx * kFastStage;
                 const uint4* vp = reinterpret_cast<const uint4*>(st);
                 const int32_t q = w + i * kStreamWarps;
-                const bool is_draft = q < u.nd;
-                const int32_t cidx = is_draft ? q : q - u.nd;
+                const int32_t cidx = q;  // target chunk
                 const uint32_t off = static_cast<uint32_t>(cidx) * kFastData;
-                const uint32_t nb = min(kFastData, static_cast<uint32_t>(is_draft ? A.Vd : A.V) * 2 - off);
+                const uint32_t nb = min(kFastData, static_cast<uint32_t>(A.V) * 2 - off);
                 const int nv = static_cast<int>(nb / 16);
                 const int32_t x0 = static_cast<int32_t>(off / 2);
                 // support entries of a target chunk: this lane's groups of four packed pairs, from
                 // L2 while the maxima and exponentials below run
-                const bool scatter = !is_draft && u.has_draft && plan_ok;
+                const bool scatter = u.has_draft && plan_ok;
                 float csum = 0.f;  // this lane's share of the chunk's sum, relative to its running max
                 int32_t p0 = 0, p1 = 0;
                 if (scatter) {
@@ -1147,7 +1158,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                     m2 = bmax2_nan(m2, bmax2_nan(bmax2_nan(qv[e].x, qv[e].y), bmax2_nan(qv[e].z, qv[e].w)));
                 float lm = fmax_nan(bf16_lo(m2), bf16_hi(m2));
                 if (lm != lm) {  // rare: NaN logits read as -inf
-                    (is_draft ? dflags : tflags) |= kFlagNaN;
+                    tflags |= kFlagNaN;
                     lm = -INFINITY;
 #pragma unroll
                     for (int e = 0; e < kVL; ++e) {
@@ -1160,9 +1171,9 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                 // Each lane sums its exponentials against its own maximum lr, so that they do not wait
                 // for the warp maximum; the lane's sum is then moved to the warp's running reference
                 // rm (the running maximum of z c) with one more exponential.
-                const bool sums = is_draft || u.sampling;
-                float& rm = is_draft ? dm : tm;
-                float& rs_ = is_draft ? ds : ts;
+                const bool sums = u.sampling;
+                float& rm = tm;
+                float& rs_ = ts;
                 const float lr = lm > -INFINITY ? lm * c : 0.f;
                 float acc = 0.f;
                 if (sums) {
@@ -1173,13 +1184,9 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                     acc = ((ae[0] + ae[1]) + (ae[2] + ae[3])) + ((ae[4] + ae[5]) + (ae[6] + ae[7]));
                 }
                 const float wm = warp_max(lm);
-                if (!is_draft) {
-                    if (wm > bv) {  // warp-uniform, rare after the first chunks
-                        bx = x0 + static_cast<int32_t>(first_max_offset(qv, wm, lane));
-                        bv = wm;
-                    }
-                } else if (wm == INFINITY) {
-                    dflags |= kFlagPosInf;
+                if (wm > bv) {  // warp-uniform, rare after the first chunks
+                    bx = x0 + static_cast<int32_t>(first_max_offset(qv, wm, lane));
+                    bv = wm;
                 }
                 if (sums) {
                     const float mt = wm * c;
@@ -1235,8 +1242,8 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                     // unit: in flight until that chunk's scatter
                     const int32_t qn = q + kStreamWarps;
                     pg_for = -1;
-                    if (u.has_draft && plan_ok && qn < u.n && qn >= u.nd) {
-                        pg_for = qn - u.nd;
+                    if (u.has_draft && plan_ok && qn < u.n) {
+                        pg_for = qn;
                         load_pairs(A, pg_for * (kMaxGroups * 32), lane, pg);
                     }
                 }
@@ -1244,8 +1251,8 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                 __syncwarp();
                 ++consumed;
                 if (lane == 0) fence_proxy_async_smem();
-                producer_step(A, P, consumed, w, lane, units, wst, wbar, pol_t, pol_d);
-                if (!is_draft && u.sampling) {
+                producer_step(A, P, consumed, w, lane, units, wst, wbar, pol_t);
+                if (u.sampling) {
                     // this chunk's (reference, sum) for the race
                     float cs = csum;
 #pragma unroll
@@ -1257,14 +1264,10 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
 
             // this warp's record of the unit; every lane then signals the TV warps
             const uint32_t tfl = __reduce_or_sync(0xffffffffu, tflags | (timeout ? kFlagTimeout : 0u));
-            const uint32_t dfl = __reduce_or_sync(0xffffffffu, dflags);
-            float tsw = ts, dsw = ds;
+            float tsw = ts;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                tsw += __shfl_xor_sync(0xffffffffu, tsw, o);
-                dsw += __shfl_xor_sync(0xffffffffu, dsw, o);
-            }
-            if (lane == 0) wrec[b][w] = WarpRec{bv, bx, tfl, dfl, tm, dm, tsw, dsw};
+            for (int o = 16; o > 0; o >>= 1) tsw += __shfl_xor_sync(0xffffffffu, tsw, o);
+            if (lane == 0) wrec[b][w] = WarpRec{bv, bx, tfl, tm, tsw};
             mbar_arrive(&full[b]);
         }
         if (timeout && lane == 0) {
@@ -1278,6 +1281,8 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
     // ================= TV warps =================
     const int ttid = tid - kStreamWarps * 32, tw = w - kStreamWarps;
     uint32_t tto = 0;  // a wait of these warps gave up
+    uint64_t pol_keep;  // the draft rows stay in L2 between the two passes over them
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_keep));
     int64_t unit = blockIdx.x;
     for (uint32_t n = 0; unit < units; unit += gridDim.x, ++n) {
         const uint32_t b = n & 1u;
@@ -1288,11 +1293,71 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
         const uint64_t seed = (u.has_draft && ttid == 0) ? A.seeds[u.r] : 0ull;  // for the accept test
         const uint16_t* G = reinterpret_cast<const uint16_t*>(gbase + b * gbytes);
 
-        // the first batch of draft-row loads, in flight while the stream warps finish the unit
-        constexpr int kTvIter = (kFastMaxVd / 8 + kTvThreads - 1) / kTvThreads;
-        constexpr int kTvBatch = 8;  // draft-row loads in flight per thread
         const int32_t nv8 = u.has_draft ? A.Vd / 8 : 0;  // Vd % 8 == 0 on this path
         const uint4* yv = reinterpret_cast<const uint4*>(u.drow);
+        {
+            // ---- the draft row, read by these warps (from HBM, kept in L2 for the TV pass)
+            // while the stream warps read the target row: maximum, sum at T, flags.  Each
+            // thread sums a batch against the batch maximum and moves it to its running
+            // reference. ----
+            constexpr int kDraftBatch = 8;
+            const unsigned long long c2 = pack2(c, c);
+            float rm = -INFINITY, rs = 0.f;
+            uint32_t fl = 0;
+#pragma unroll 1
+            for (int32_t v0 = ttid; v0 < nv8; v0 += kTvThreads * kDraftBatch) {
+                uint4 yb[kDraftBatch];
+#pragma unroll
+                for (int i = 0; i < kDraftBatch; ++i) {
+                    const int32_t v = v0 + i * kTvThreads;
+                    yb[i] = v < nv8 ? ld_nc_v4_hint(yv + v, pol_keep)
+                                    : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+                }
+                uint32_t m2 = bmax2_nan(bmax2_nan(yb[0].x, yb[0].y), bmax2_nan(yb[0].z, yb[0].w));
+#pragma unroll
+                for (int i = 1; i < kDraftBatch; ++i)
+                    m2 = bmax2_nan(m2, bmax2_nan(bmax2_nan(yb[i].x, yb[i].y), bmax2_nan(yb[i].z, yb[i].w)));
+                float lm = fmax_nan(bf16_lo(m2), bf16_hi(m2));
+                if (lm != lm) {  // rare: NaN logits, flagged (the request is verified greedily)
+                    fl |= kFlagNaN;
+                    lm = -INFINITY;
+#pragma unroll
+                    for (int i = 0; i < kDraftBatch; ++i) {
+                        yb[i] = make_uint4(bf16x2_nan_to_ninf(yb[i].x), bf16x2_nan_to_ninf(yb[i].y),
+                                           bf16x2_nan_to_ninf(yb[i].z), bf16x2_nan_to_ninf(yb[i].w));
+                        const uint32_t m3 = bmax2_nan(bmax2_nan(yb[i].x, yb[i].y), bmax2_nan(yb[i].z, yb[i].w));
+                        lm = fmaxf(lm, fmaxf(bf16_lo(m3), bf16_hi(m3)));
+                    }
+                }
+                if (lm == INFINITY) fl |= kFlagPosInf;
+                if (lm > -INFINITY && lm < INFINITY) {
+                    const float lr = lm * c;
+                    const unsigned long long nl2 = pack2(-lr, -lr);
+                    float ae[kDraftBatch];
+#pragma unroll
+                    for (int i = 0; i < kDraftBatch; ++i) ae[i] = exp_sum8(yb[i], c2, nl2);
+                    const float acc = ((ae[0] + ae[1]) + (ae[2] + ae[3])) + ((ae[4] + ae[5]) + (ae[6] + ae[7]));
+                    if (lr > rm) {
+                        rs *= rm == -INFINITY ? 0.f : ex2(rm - lr);
+                        rm = lr;
+                    }
+                    rs += acc * ex2(lr - rm);
+                }
+            }
+            float wm = rm;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+            float ws = rm > -INFINITY ? rs * ex2(rm - wm) : 0.f;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+            fl = __reduce_or_sync(0xffffffffu, fl);
+            if (lane == 0) drec[tw] = DraftRec{wm, ws, fl};
+        }
+
+        // the first batch of the TV pass's draft-row loads, in flight while the stream warps
+        // finish the unit
+        constexpr int kTvIter = (kFastMaxVd / 8 + kTvThreads - 1) / kTvThreads;
+        constexpr int kTvBatch = 8;  // draft-row loads in flight per thread
         uint4 yq[kTvBatch];
 #pragma unroll
         for (int i = 0; i < kTvBatch; ++i) {
@@ -1303,11 +1368,10 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
 
         // ---- merge the stream warps' records: max, first argmax, reference maxima, sums ----
         if (tw == 0) {
-            WarpRec rec = lane < kStreamWarps ? wrec[b][lane]
-                                              : WarpRec{-INFINITY, INT32_MAX, 0u, 0u, -INFINITY, -INFINITY, 0.f, 0.f};
-            float mbv = rec.bv, mtm = rec.tm, mdm = rec.dm;
+            WarpRec rec = lane < kStreamWarps ? wrec[b][lane] : WarpRec{-INFINITY, INT32_MAX, 0u, -INFINITY, 0.f};
+            float mbv = rec.bv, mtm = rec.tm;
             int32_t mbx = rec.bx;
-            uint32_t ftl = rec.tfl, fdl = rec.dfl;
+            uint32_t ftl = rec.tfl;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
                 const float ov = __shfl_xor_sync(0xffffffffu, mbv, o);
@@ -1317,24 +1381,28 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                     mbx = ox;
                 }
                 mtm = fmaxf(mtm, __shfl_xor_sync(0xffffffffu, mtm, o));
-                mdm = fmaxf(mdm, __shfl_xor_sync(0xffffffffu, mdm, o));
             }
             ftl = __reduce_or_sync(0xffffffffu, ftl);
-            fdl = __reduce_or_sync(0xffffffffu, fdl);
             float st = (rec.tm > -INFINITY && mtm > -INFINITY) ? rec.ts * ex2(rec.tm - mtm) : 0.f;
-            float sd = (rec.dm > -INFINITY && mdm > -INFINITY) ? rec.ds * ex2(rec.dm - mdm) : 0.f;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                st += __shfl_xor_sync(0xffffffffu, st, o);
-                sd += __shfl_xor_sync(0xffffffffu, sd, o);
-            }
-            if (lane == 0) merged = WarpRec{mbv, mbx, ftl, fdl, mtm, mdm, st, sd};
+            for (int o = 16; o > 0; o >>= 1) st += __shfl_xor_sync(0xffffffffu, st, o);
+            if (lane == 0) merged = WarpRec{mbv, mbx, ftl, mtm, st};
         }
-        tv_bar_sync();
+        tv_bar_sync();  // merged and the TV warps' draft shares are written
         const float BV = merged.bv;
-        float M = merged.tm, Mq = merged.dm;
-        const float S = merged.ts, Sq = merged.ds;
-        const uint32_t FLT = merged.tfl, FLD = merged.dfl;
+        float M = merged.tm;
+        const float S = merged.ts;
+        const uint32_t FLT = merged.tfl;
+        float Mq = -INFINITY, Sq = 0.f;
+        uint32_t FLD = 0;
+#pragma unroll
+        for (int i = 0; i < kTvWarps; ++i) {
+            Mq = fmaxf(Mq, drec[i].m);
+            FLD |= drec[i].fl;
+        }
+#pragma unroll
+        for (int i = 0; i < kTvWarps; ++i)
+            if (drec[i].m > -INFINITY) Sq += drec[i].s * ex2(drec[i].m - Mq);
         const int32_t amax = merged.bx == INT32_MAX ? 0 : merged.bx;
         if (!u.sampling) M = -INFINITY;
         if (!u.has_draft) Mq = -INFINITY;
@@ -1459,7 +1527,6 @@ namespace {
 constexpr int32_t kRaceChunk = 2048;
 constexpr int kRaceMinThreads = 512;  // the race CTA: 1024 threads, or 512 (two per SM) for many requests
 constexpr int kRaceInFlight = 4;  // 8-id vectors per thread loaded together
-constexpr int kRaceMaxChunks = kMaxPlanWords * 32 / kRaceChunk;  // V <= 819,200
 constexpr int kWarpsPerChunk = kRaceChunk / 8 / 32;              // 8
 constexpr int kEvalChunks = 8;  // chunks summed together by the bounded chunk race
 // 8-id vectors per thread of a round with NT threads
