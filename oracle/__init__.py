@@ -64,6 +64,8 @@ def _load():
             lib.or_accept_scan.restype = C.c_int
             lib.or_verify_greedy.argtypes = [P, C.c_int, i64, i32, i32, i32, i32, P, P, P, P, P]
             lib.or_verify_greedy.restype = C.c_int
+            lib.or_top2_rows.argtypes = [P, C.c_int, i64, i64, i32, P]
+            lib.or_top2_rows.restype = C.c_int
             lib.or_verify_sample.argtypes = [P, C.c_int, i64, i32, P, C.c_int, i64, i32, P, i32, i32,
                                              P, P, P, P, P, P, P, P, P, P, P]
             lib.or_verify_sample.restype = C.c_int
@@ -159,6 +161,17 @@ def verify_greedy(target, R: int, k: int, branches: int, draft):
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments ({rc})")
     return dict(accept_len=acc_len, tokens=tokens, branch=branch, status=status)
+
+
+def top2_rows(rows):
+    """[n, 2] int32: per row the argmax and the runner-up id (value descending, then id
+    ascending; NaN read as -inf; -1 for one-id rows)."""
+    t, code, stride, V = _rows(rows, "rows")
+    out = np.zeros((t.shape[0], 2), np.int32)
+    rc = _load().or_top2_rows(_ptr(t), code, stride, t.shape[0], V, _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments ({rc})")
+    return out
 
 
 def verify_sample(target, draft_logits, d2t, R: int, k: int, draft, seeds, temperature):

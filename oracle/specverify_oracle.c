@@ -180,6 +180,43 @@ static int32_t argmax_row(const double* z, int32_t n)
     return best;
 }
 
+/* the two ids ranked first when ids are ordered by value (descending), then
+ * by id (ascending), NaN read as -inf: the argmax and the runner-up of a row
+ * ([SL] "method steps", step 2: the runner-up branch starts from the second-best
+ * token of the verified row).  second = -1 for a one-id row. */
+static void top2_row(const double* z, int32_t n, int32_t* first, int32_t* second)
+{
+    int32_t a = -1, b = -1;
+    double av = -INFINITY, bv = -INFINITY;
+    for (int32_t x = 0; x < n; ++x) {  /* ascending ids: an equal value never displaces */
+        double v = isnan(z[x]) ? -INFINITY : z[x];
+        if (a < 0 || v > av) {
+            b = a;
+            bv = av;
+            a = x;
+            av = v;
+        } else if (b < 0 || v > bv) {
+            b = x;
+            bv = v;
+        }
+    }
+    *first = a < 0 ? 0 : a;
+    *second = b;
+}
+
+int or_top2_rows(const void* rows, int dtype, int64_t row_stride, int64_t nrows, int32_t V,
+                 int32_t* top2)
+{
+    if (V < 1 || nrows < 0) return -1;
+    double* z = (double*)malloc(sizeof(double) * (size_t)V);
+    for (int64_t r = 0; r < nrows; ++r) {
+        for (int32_t x = 0; x < V; ++x) z[x] = load_elem(rows, dtype, r * row_stride + x);
+        top2_row(z, V, &top2[2 * r], &top2[2 * r + 1]);
+    }
+    free(z);
+    return 0;
+}
+
 /* p = softmax(z / T) in fp64; NaN read as -inf.  Caller ensures the row
  * is not bad. */
 static void softmax_T(const double* z, int32_t n, double T, double* p)

@@ -471,6 +471,41 @@ def test_greedy_ties_nan_inf_and_ranges():
     assert res["tokens"][0].tolist() == [4] and res["status"][0] & oracle.ST_BAD_LOGITS
 
 
+def _top2_by_sort(rows):
+    """the first two ids of each row under a stable sort by value, descending (NaN as -inf)"""
+    v = np.where(np.isnan(rows), -np.inf, rows.astype(np.float64))
+    order = np.argsort(-v, axis=1, kind="stable")
+    return order[:, :2]
+
+
+def test_top2_matches_a_stable_sort():
+    rng = np.random.default_rng(31)
+    rows = rng.integers(-3, 4, (400, 37)).astype(np.float32)  # many ties
+    rows[rng.random(rows.shape) < 0.05] = np.nan
+    rows[rng.random(rows.shape) < 0.05] = -np.inf
+    rows[::7, 5] = np.inf
+    got = oracle.top2_rows(rows)
+    assert np.array_equal(got, _top2_by_sort(rows))
+    bits = (rng.normal(0, 2, (50, 300)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    widened = (bits.astype(np.uint32) << 16).view(np.float32)
+    assert np.array_equal(oracle.top2_rows(bits), _top2_by_sort(widened))
+
+
+def test_top2_special_cases_and_greedy_argmax():
+    rows = np.array([[1, 3, 3, 0, 3, 2],                       # tied maximum: its first two ids
+                     [np.nan, 0, 7, np.nan, 5, 1],             # NaN reads as -inf
+                     [-np.inf] * 6,                            # all -inf: ids 0 and 1
+                     [2, -np.inf, -np.inf, -np.inf, -np.inf, -np.inf]], np.float32)
+    assert oracle.top2_rows(rows).tolist() == [[1, 2], [2, 4], [0, 1], [0, 1]]
+    assert oracle.top2_rows(np.array([[4.0], [np.nan]], np.float32)).tolist() == [[0, -1], [0, -1]]
+    # the first id is the argmax of greedy verification
+    rng = np.random.default_rng(32)
+    z = rng.normal(0, 1, (9, 50)).astype(np.float32)
+    z[:, 10] = z[:, 20] = z.max(axis=1) + 1.0
+    res = oracle.verify_greedy(z, 1, 8, 1, np.full((1, 8), -1, np.int32))
+    assert res["tokens"][0, 0] == oracle.top2_rows(z)[0, 0] == 10
+
+
 def test_bf16_rows_are_widened_exactly():
     rng = np.random.default_rng(3)
     V = 33
