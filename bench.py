@@ -40,7 +40,7 @@ def _args():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", choices=["listen", "d2t", "cfg", "sweep"], default="listen",
+    ap.add_argument("--workload", choices=["listen", "listen_top2", "d2t", "cfg", "sweep"], default="listen",
                     help="listen: greedy verify with a runner-up branch (headline); d2t: speculative sampling")
     ap.add_argument("--sessions", type=int, default=None,
                     help="requests per step (default: the workload's own, 64 listen sessions / 128 d2t requests)")
@@ -175,7 +175,7 @@ class Workload:
 
         self.name = name
         self.sv = sv
-        if name == "listen":
+        if name in ("listen", "listen_top2"):
             w = workloads.listen(device=device, R=sessions or 64)
             R, k = w["R"], w["k"]
             self.rows = R * (2 * k + 1)
@@ -193,6 +193,16 @@ class Workload:
             self.desc = (f"listen: {R} sessions x (32 main + 32 runner-up drafts) = 65 rows x 151936 bf16 per "
                          f"session ({self.logit_bytes / 1e9:.3f} GB of logits per step)")
             self.metric = "verify logit GB/s (speculative-listening greedy verify, V=151936 bf16)"
+            if name == "listen_top2":
+                # the same verification, also returning every row's argmax and runner-up id
+                self.out["top2"] = torch.empty(self.rows, 2, dtype=torch.int32, device=device)
+                self.ws = torch.empty(sv.verify_greedy_top2_workspace(R, k, 2, w["V"]), dtype=torch.uint8,
+                                      device=device)
+                self.launches = sv.LAUNCHES["verify_greedy_top2"]
+                self.kernel = "argmax_segments_kernel<bf16, top-2>"
+                self.profile = "argmax_segments_listen_top2.md"
+                self.desc = self.desc.replace("listen:", "listen with every row's argmax and runner-up:")
+                self.metric = "verify + top-2 logit GB/s (speculative-listening greedy verify, V=151936 bf16)"
         elif name == "d2t":
             w = workloads.d2t_workload(device=device, R=sessions or 128)
             R, k, V, Vd = w["R"], w["k"], w["V"], w["Vd"]
@@ -246,6 +256,9 @@ class Workload:
         if self.name == "listen":
             self.sv.verify_greedy(inp["target"], w["R"], w["k"], 2, inp["draft"], out=self.out, workspace=self.ws,
                                   stream=stream)
+        elif self.name == "listen_top2":
+            self.sv.verify_greedy_top2(inp["target"], w["R"], w["k"], 2, inp["draft"], out=self.out,
+                                       workspace=self.ws, stream=stream)
         elif self.name == "cfg":
             self.sv.cfg_merge_sample(inp["cond"], inp["uncond"], w["cb_id_base"], w["cb_data_offset"], w["S"],
                                      w["W"], w["w"], inp["draft_logits"], w["R"], w["k"], inp["draft"],
@@ -270,7 +283,7 @@ class Workload:
                            "seeds": w["seeds"].cpu().numpy().view(np.uint64), "T": w["temperature"].cpu().numpy()}
                 return self._h
             h = {"target": workloads.host_rows(w["target"]), "draft": w["draft"].cpu().numpy()}
-            if self.name != "listen":
+            if self.name not in ("listen", "listen_top2"):
                 h["draft_logits"] = workloads.host_rows(w["draft_logits"])
                 h["d2t"] = w["d2t"].cpu().numpy()
                 h["seeds"] = w["seeds"].cpu().numpy().view(np.uint64)
@@ -285,9 +298,11 @@ class Workload:
         w, h = self.w, self._host()
         k = w["k"]
         r = r % w["R"]
-        if self.name == "listen":
+        if self.name in ("listen", "listen_top2"):
             rpr = 2 * k + 1
             oracle.verify_greedy(h["target"][r * rpr:(r + 1) * rpr], 1, k, 2, h["draft"][r:r + 1])
+            if self.name == "listen_top2":
+                oracle.top2_rows(h["target"][r * rpr:(r + 1) * rpr])
             return rpr * w["V"] * 2, rpr
         if self.name == "cfg":
             S, W = w["S"], w["W"]

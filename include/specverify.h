@@ -128,6 +128,25 @@ int sv_verify_greedy(sv_rows target, int32_t R, int32_t k, int32_t branches,
                      size_t workspace_bytes, sv_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * sv_verify_greedy_top2 -- sv_verify_greedy that also returns, fused into the
+ * same pass over the rows, the argmax and the runner-up id of every row.
+ * Source: "Decode Before You Hear ..." method step 2: the runner-up branch
+ * starts from the second-best token of the verified row.
+ *
+ *   top2        int32 [R * rows_per_request, 2] out: per row, in row order,
+ *               the first two ids when ids are ordered by logit (descending),
+ *               then by id (ascending), NaN read as -inf; the first equals the
+ *               argmax of sv_verify_greedy; the second is -1 when V == 1.
+ * Every other argument, output and limit is that of sv_verify_greedy; the
+ * workspace is sized by sv_verify_greedy_top2_workspace.
+ * ---------------------------------------------------------------------- */
+size_t sv_verify_greedy_top2_workspace(int32_t R, int32_t k, int32_t branches, int32_t V);
+int sv_verify_greedy_top2(sv_rows target, int32_t R, int32_t k, int32_t branches,
+                          const int32_t* draft, int32_t* accept_len, int32_t* tokens,
+                          int32_t* branch, int32_t* status, int32_t* top2, void* workspace,
+                          size_t workspace_bytes, sv_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * sv_verify_greedy_noalloc -- sv_verify_greedy without a workspace argument.
  * The source pages have no counterpart; this is a convenience for callers
  * that cannot allocate device memory: a plugin whose host framework owns all

@@ -26,7 +26,7 @@ MAX_K, MAX_S = 256, 16
 # kernels launched by one call of each entry point (reported by the benchmark)
 # kernels one call launches: verify_sample with a prebuilt d2t plan (or the identity map)
 # launches 2, and 2 more when it builds the plan itself; d2t_plan launches 2
-LAUNCHES = {"verify_greedy": 2, "verify_sample": 2, "verify_sample_plan_in_call": 4, "d2t_plan": 2,
+LAUNCHES = {"verify_greedy": 2, "verify_greedy_top2": 2, "verify_sample": 2, "verify_sample_plan_in_call": 4, "d2t_plan": 2,
             "cfg_merge_sample": 2, "accept_scan": 1}
 
 
@@ -61,6 +61,10 @@ def load(path: str | None = None):
     lib.sv_verify_greedy_workspace.restype = sz
     lib.sv_verify_greedy.argtypes = [SvRows, i32, i32, i32, P, P, P, P, P, P, sz, P]
     lib.sv_verify_greedy.restype = C.c_int
+    lib.sv_verify_greedy_top2_workspace.argtypes = [i32, i32, i32, i32]
+    lib.sv_verify_greedy_top2_workspace.restype = sz
+    lib.sv_verify_greedy_top2.argtypes = [SvRows, i32, i32, i32, P, P, P, P, P, P, P, sz, P]
+    lib.sv_verify_greedy_top2.restype = C.c_int
     lib.sv_verify_sample_workspace.argtypes = [i32, i32, i32, i32]
     lib.sv_verify_sample_workspace.restype = sz
     lib.sv_verify_sample.argtypes = [SvRows, SvRows, P, P, i32, i32, P, P, P, P, P, P, P, P, P, P, sz, P]
@@ -156,6 +160,30 @@ def verify_greedy(target, R: int, k: int, branches: int, draft, out: dict | None
     _check(lib.sv_verify_greedy(rows_of(target), R, k, branches, _ptr(draft), _ptr(out["accept_len"]),
                                 _ptr(out["tokens"]), _ptr(out.get("branch")), _ptr(out.get("status")), _ptr(ws),
                                 _nbytes(ws), _stream(stream)))
+    return out
+
+
+def verify_greedy_top2_workspace(R: int, k: int, branches: int, V: int) -> int:
+    return int(load().sv_verify_greedy_top2_workspace(R, k, branches, V))
+
+
+def verify_greedy_top2(target, R: int, k: int, branches: int, draft, out: dict | None = None, workspace=None,
+                       stream=None) -> dict:
+    """verify_greedy plus top2 [rows, 2]: per row the argmax and the runner-up id
+    (logit descending, then id ascending; -1 when V == 1), from the same pass."""
+    import torch
+
+    lib = load()
+    dev = target.device
+    rows = target.shape[0] if R == 0 else R * (k + 1 if branches == 1 else 2 * k + 1)
+    if out is None:
+        out = dict(accept_len=_empty(R, torch.int32, dev), tokens=_empty((R, k + 1), torch.int32, dev),
+                   branch=_empty(R, torch.int32, dev), status=_empty(R, torch.int32, dev),
+                   top2=_empty((rows, 2), torch.int32, dev))
+    ws = _workspace(lib.sv_verify_greedy_top2_workspace(R, k, branches, target.shape[1]), dev, workspace)
+    _check(lib.sv_verify_greedy_top2(rows_of(target), R, k, branches, _ptr(draft), _ptr(out["accept_len"]),
+                                     _ptr(out["tokens"]), _ptr(out.get("branch")), _ptr(out.get("status")),
+                                     _ptr(out["top2"]), _ptr(ws), _nbytes(ws), _stream(stream)))
     return out
 
 

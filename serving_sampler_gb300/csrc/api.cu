@@ -108,6 +108,39 @@ int sv_verify_greedy(sv_rows target, int32_t R, int32_t k, int32_t branches, con
                                          status, workspace, stream));
 }
 
+size_t sv_verify_greedy_top2_workspace(int32_t R, int32_t k, int32_t branches, int32_t V)
+{
+    if (R < 0 || k < 0 || V < 1 || (branches != 1 && branches != 2)) return 0;
+    return greedy_workspace_bytes(R, k, branches, V, true);
+}
+
+int sv_verify_greedy_top2(sv_rows target, int32_t R, int32_t k, int32_t branches, const int32_t* draft,
+                          int32_t* accept_len, int32_t* tokens, int32_t* branch, int32_t* status,
+                          int32_t* top2, void* workspace, size_t workspace_bytes, sv_stream_t stream)
+{
+    if (R < 0 || k < 0) return SV_ERR_INVALID_ARG;
+    if (branches != 1 && branches != 2) return SV_ERR_INVALID_ARG;
+    if (branches == 2 && k < 1) return SV_ERR_INVALID_ARG;
+    if (k > SV_MAX_K) return SV_ERR_LIMIT;
+    if (R == 0) return SV_OK;
+    if ((k > 0 && draft == nullptr) || accept_len == nullptr || tokens == nullptr || top2 == nullptr)
+        return SV_ERR_INVALID_ARG;
+    if (!aligned(draft, 4) || !aligned(accept_len, 4) || !aligned(tokens, 4) ||
+        !aligned(branch, 4) || !aligned(status, 4) || !aligned(top2, 4))
+        return SV_ERR_ALIGN;
+    const int64_t rows = static_cast<int64_t>(R) * (branches == 2 ? 2 * k + 1 : k + 1);
+    Rows t{};
+    if (int rc = check_rows(target, rows, target.width, &t)) return rc;
+    const SegPlan plan = plan_segments(rows, t.width, t.esize);
+    if (rows * plan.nseg > INT32_MAX) return SV_ERR_LIMIT;
+    if (int rc = check_workspace(workspace, workspace_bytes,
+                                 greedy_workspace_bytes(R, k, branches, t.width, true)))
+        return rc;
+    if (!have_device()) return SV_ERR_DEVICE;
+    return launched(launch_verify_greedy(t, R, k, branches, draft, accept_len, tokens, branch,
+                                         status, workspace, stream, top2));
+}
+
 size_t sv_verify_sample_workspace(int32_t R, int32_t k, int32_t V, int32_t Vd)
 {
     if (R < 0 || k < 0 || V < 1 || Vd < 1) return 0;

@@ -927,15 +927,6 @@ __device__ __forceinline__ void fence_proxy_async_smem()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// replace NaN halves of a bf16x2 word by -inf
-__device__ __forceinline__ uint32_t bf16x2_nan_to_ninf(uint32_t w)
-{
-    uint32_t lo = w & 0xFFFFu, hi = w >> 16;
-    if ((lo & 0x7FFFu) > 0x7F80u) lo = 0xFF80u;
-    if ((hi & 0x7FFFu) > 0x7F80u) hi = 0xFF80u;
-    return lo | (hi << 16);
-}
-
 struct WarpRec {
     float bv;     // max of the target logits
     int32_t bx;   // its first id

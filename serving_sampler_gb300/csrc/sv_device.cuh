@@ -113,6 +113,15 @@ __device__ __forceinline__ float fmax_nan(float a, float b)
     asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
     return d;
 }
+// replace NaN halves of a bf16x2 word by -inf
+__device__ __forceinline__ uint32_t bf16x2_nan_to_ninf(uint32_t w)
+{
+    uint32_t lo = w & 0xFFFFu, hi = w >> 16;
+    if ((lo & 0x7FFFu) > 0x7F80u) lo = 0xFF80u;
+    if ((hi & 0x7FFFu) > 0x7F80u) hi = 0xFF80u;
+    return lo | (hi << 16);
+}
+
 // the two bf16 halves of a 32-bit word, widened exactly to fp32
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }

@@ -35,11 +35,22 @@ struct ArgPartial {
     uint32_t pad;
 };
 
-size_t greedy_workspace_bytes(int64_t R, int32_t k, int32_t branches, int32_t V);
+// a segment's two first ids (value descending, id ascending; INT32_MAX: none)
+struct Top2Partial {
+    float v1;
+    int32_t i1;
+    float v2;
+    int32_t i2;
+    uint32_t flags;
+    uint32_t pad[3];
+};
+
+size_t greedy_workspace_bytes(int64_t R, int32_t k, int32_t branches, int32_t V, bool top2 = false);
+// top2 != NULL: also the argmax and runner-up id of every row ([rows, 2])
 cudaError_t launch_verify_greedy(const Rows& target, int32_t R, int32_t k, int32_t branches,
                                  const int32_t* draft, int32_t* accept_len, int32_t* tokens,
                                  int32_t* branch, int32_t* status, void* workspace,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream, int32_t* top2 = nullptr);
 
 cudaError_t launch_accept_scan(const uint8_t* accept, const int32_t* draft, const int32_t* fix,
                                int32_t R, int32_t k, int32_t* accept_len, int32_t* tokens,

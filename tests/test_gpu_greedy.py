@@ -120,3 +120,76 @@ def test_accept_scan_matches_oracle(sv):
         want = oracle.accept_scan(acc, draft, fix)
         np.testing.assert_array_equal(got["accept_len"].cpu().numpy(), want["accept_len"])
         np.testing.assert_array_equal(got["tokens"].cpu().numpy(), want["tokens"])
+
+
+# --------------------------------------------------------------------------
+# argmax and runner-up of every row, fused into the greedy pass
+# --------------------------------------------------------------------------
+def _check_top2(sv, target, R, k, branches, draft):
+    got = sv.verify_greedy_top2(target, R, k, branches, draft)
+    torch.cuda.synchronize()
+    host = workloads.host_rows(target)
+    want = oracle.verify_greedy(host, R, k, branches, draft.cpu().numpy())
+    for key in ("accept_len", "tokens", "branch", "status"):
+        np.testing.assert_array_equal(got[key].cpu().numpy(), want[key], err_msg=key)
+    np.testing.assert_array_equal(got["top2"].cpu().numpy(), oracle.top2_rows(host), err_msg="top2")
+    return got
+
+
+@pytest.mark.parametrize(
+    "R,k,branches,V,dtype,row_pad",
+    [
+        (5, 8, 1, 4096, torch.bfloat16, 0),
+        (7, 3, 2, 4099, torch.bfloat16, 0),     # plain-load path
+        (6, 5, 1, 4100, torch.bfloat16, 4),     # sub-16-byte tail
+        (3, 4, 1, 151936, torch.float32, 0),
+        (2, 7, 2, 151936, torch.bfloat16, 0),   # several segments per row
+        (9, 2, 1, 17, torch.float32, 3),        # tiny vocabulary
+        (4, 1, 1, 7, torch.bfloat16, 1),        # fewer ids than a vector
+        (40, 6, 2, 65536, torch.bfloat16, 0),
+    ],
+)
+def test_top2_random_shapes(sv, R, k, branches, V, dtype, row_pad):
+    w = workloads.greedy_batch(R, k, V, dtype, branches=branches, p_full=0.5, p_first=0.5, seed=R * 77 + k,
+                               row_pad=row_pad)
+    _check_top2(sv, w["target"], R, k, branches, w["draft"])
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_top2_ties_nan_and_inf(sv, dtype):
+    """Values from a small set (ties everywhere), NaN, +inf, all -inf and all-NaN rows."""
+    g = torch.Generator(device="cuda").manual_seed(9)
+    R, k, V = 6, 5, 3001
+    z = torch.randint(-2, 3, (R * (k + 1), V), generator=g, device="cuda").to(dtype)
+    z[0, 5] = float("nan")
+    z[1, ::3] = float("nan")
+    z[2, 77] = float("inf")
+    z[3, 100] = float("inf")
+    z[3, 2000] = float("inf")                # tied +inf
+    z[4, :] = float("-inf")
+    z[5, :] = float("nan")
+    z[6, :] = float("-inf")
+    z[6, 2999] = 1.0                         # one finite value, the rest -inf
+    z[7, :] = 2.0                            # a constant row
+    z[8, 1] = 50.0                           # a unique maximum, the runner-up tied many times
+    d = torch.zeros(R, 1, k, dtype=torch.int32, device="cuda")
+    _check_top2(sv, z, R, k, 1, d)
+
+
+def test_top2_one_id_rows(sv):
+    z = torch.tensor([[3.0], [float("nan")], [-1.0]], device="cuda", dtype=torch.float32)
+    got = _check_top2(sv, z, 3, 0, 1, torch.zeros(3, 1, 0, dtype=torch.int32, device="cuda"))
+    assert got["top2"][:, 1].tolist() == [-1, -1, -1]
+
+
+def test_top2_listen_runner_up(sv):
+    """On the listen workload a runner-up branch whose main branch starts with the argmax of
+    row 0 starts from the second-best id of row 0."""
+    w = workloads.listen()
+    got = _check_top2(sv, w["target"], w["R"], w["k"], 2, w["draft"])
+    rows_per = 2 * w["k"] + 1
+    first0 = got["top2"].view(w["R"], rows_per, 2)[:, 0, 0]
+    second0 = got["top2"].view(w["R"], rows_per, 2)[:, 0, 1]
+    main = w["draft"][:, 0, 0] == first0
+    assert main.sum() > w["R"] // 2
+    assert torch.equal(second0[main], w["draft"][main, 1, 0])
