@@ -812,26 +812,27 @@ __global__ void __launch_bounds__(kRowThreads, 1) sample_rows_kernel(SampleArgs 
 }
 
 // ---------------------------------------------------------------------------
-// row pass, fast path: bf16 target and draft rows, d2t vocabulary <= 32768
+// row pass, fast path: bf16 or fp32 target and draft rows, d2t vocabulary < 32768
 // ---------------------------------------------------------------------------
 // Two warp roles.  Each stream warp pulls its own share of a target row
-// through a private ring of kFastStages bulk-copied stages: chunk s of a
-// (request, position) unit belongs to stream warp s % kStreamWarps, so the
-// warps get equal shares.  The warp's lane 0 keeps all stages in
-// flight: each consumed stage is refilled at once with the warp's next chunk,
-// of this unit or of the CTA's next one.  The support entries of a target
-// chunk, packed (draft id, offset) pairs of the plan, come from L2 into
-// registers while the chunk's maxima and exponentials are taken; the warp then
-// scatters the support logits to G[draft id] from shared memory.
+// through a private ring of bulk-copied stages, one 2048-id chunk per stage:
+// chunk s of a (request, position) unit belongs to stream warp s % kStreamWarps,
+// so the warps get equal shares.  The warp's lane 0 refills a stage the moment
+// it is read, with the warp's next chunk of this unit or of the CTA's next one.
+// The support entries of a target chunk, packed (draft id, offset) pairs of the
+// plan, come from L2 into registers while the chunk's maxima and exponentials
+// are taken; the warp then scatters the support logits to G[draft id] from
+// shared memory.
 //
 // The TV warps read the draft row of unit n themselves (its maximum, sum and
 // flags) while the stream warps read the target row, then finish unit n (merge
 // of the stream warps' records, the TV pass over G and the L2-resident draft
-// row, p and q at the draft token, the accept test) while the stream warps
-// already read unit n + 1: G, the warp records
-// and the draft-token slots are double-buffered by unit parity, and two
-// mbarrier pairs hand a buffer over (full: the stream warps are done with it;
-// freed: the TV warps are).
+// row, p and q at the draft token, the accept test).  G, the warp records and
+// the draft-token slots live in kNG buffers taken by unit in turn, handed over
+// by two mbarriers per buffer (full: the stream warps are done with it; freed:
+// the TV warps are).  bf16: two stages of 4 KB per stream warp and two buffers,
+// so the TV warps finish unit n while the stream warps read unit n + 1.  fp32:
+// one 8 KB stage per stream warp and one buffer (the 128 KB support image).
 namespace {
 
 constexpr int kStreamWarps = 12;                 // warps that stream the rows
@@ -839,67 +840,179 @@ constexpr int kTvWarps = 4;                      // warps that finish a unit: re
 constexpr int kFastWarps = kStreamWarps + kTvWarps;
 constexpr int kFastThreads = 32 * kFastWarps;
 constexpr int kTvThreads = 32 * kTvWarps;
-constexpr int kFastStages = 2;                   // per stream warp: one being read, one in flight
-constexpr uint32_t kFastData = kChunkElems * 2;  // 4 KB of bf16 per stage
-constexpr uint32_t kFastStage = kFastData;
 constexpr int kPairRegs = 4;                     // uint4 groups of support entries per lane and chunk
 static_assert(kPairRegs * 4 * 32 == kPadSlots, "the plan pads every chunk to the slots the registers hold");
-constexpr int kFastHeader = 512;                 // the stage mbarriers, then the two unit handoffs
-static_assert((kStreamWarps * kFastStages + 4) * 8 <= kFastHeader, "mbarriers fit the header");
+constexpr int kFastHeader = 512;                 // the stage mbarriers, then the unit handoffs
 constexpr int32_t kFastMaxVd = 32768;
-constexpr int kVL = kChunkElems / 8 / 32;  // 16-byte vectors per lane and chunk
+constexpr int kHV = 8;                           // 16-byte vectors per lane taken together
 
+template <int DT>
+struct FastCfg {
+    static constexpr int kElem = DT == SV_BF16 ? 2 : 4;
+    static constexpr int kStages = DT == SV_BF16 ? 2 : 1;       // per stream warp
+    static constexpr int kNG = DT == SV_BF16 ? 2 : 1;           // unit buffers
+    static constexpr uint32_t kStageBytes = kChunkElems * kElem;
+    static constexpr int kEPV = 16 / kElem;                     // elements per 16-byte vector
+    static constexpr int kVPL = kChunkElems / kEPV / 32;        // vectors per lane and chunk
+    static constexpr int kHalves = kVPL / kHV;
+    static_assert((kStreamWarps * kStages + 2 * kNG) * 8 <= kFastHeader, "mbarriers fit the header");
+};
 
-
-
-// sum over the 8 bf16 values z of a vector of 2^(z c - m): packed fp32x2
-// arguments, eight independent MUFU operations, a tree of packed adds
-__device__ __forceinline__ float exp_sum8(uint4 q, unsigned long long c2, unsigned long long nm2)
+__device__ __forceinline__ uint4 ninf_vec(int elem)
 {
-    const unsigned long long t0 = fma2(bf16x2_to_f32x2(q.x), c2, nm2);
-    const unsigned long long t1 = fma2(bf16x2_to_f32x2(q.y), c2, nm2);
-    const unsigned long long t2 = fma2(bf16x2_to_f32x2(q.z), c2, nm2);
-    const unsigned long long t3 = fma2(bf16x2_to_f32x2(q.w), c2, nm2);
-    float a0, a1, a2, a3, a4, a5, a6, a7;
-    unpack2(t0, a0, a1);
-    unpack2(t1, a2, a3);
-    unpack2(t2, a4, a5);
-    unpack2(t3, a6, a7);
-    const unsigned long long e0 = pack2(ex2(a0), ex2(a1)), e1 = pack2(ex2(a2), ex2(a3));
-    const unsigned long long e2 = pack2(ex2(a4), ex2(a5)), e3 = pack2(ex2(a6), ex2(a7));
+    return elem == 2 ? make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u)
+                     : make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
+}
+
+// NaN-propagating maximum of one vector
+template <int DT>
+__device__ __forceinline__ float vec_max(uint4 q)
+{
+    if constexpr (DT == SV_BF16) {
+        const uint32_t m = bmax2_nan(bmax2_nan(q.x, q.y), bmax2_nan(q.z, q.w));
+        return fmax_nan(bf16_lo(m), bf16_hi(m));
+    } else {
+        return fmax_nan(fmax_nan(__uint_as_float(q.x), __uint_as_float(q.y)),
+                        fmax_nan(__uint_as_float(q.z), __uint_as_float(q.w)));
+    }
+}
+
+// NaN-propagating maximum of kHV vectors (bf16: one packed tree, widened once)
+template <int DT>
+__device__ __forceinline__ float group_max(const uint4 (&qv)[kHV])
+{
+    if constexpr (DT == SV_BF16) {
+        uint32_t m2 = bmax2_nan(bmax2_nan(qv[0].x, qv[0].y), bmax2_nan(qv[0].z, qv[0].w));
+#pragma unroll
+        for (int e = 1; e < kHV; ++e)
+            m2 = bmax2_nan(m2, bmax2_nan(bmax2_nan(qv[e].x, qv[e].y), bmax2_nan(qv[e].z, qv[e].w)));
+        return fmax_nan(bf16_lo(m2), bf16_hi(m2));
+    } else {
+        float m = vec_max<DT>(qv[0]);
+#pragma unroll
+        for (int e = 1; e < kHV; ++e) m = fmax_nan(m, vec_max<DT>(qv[e]));
+        return m;
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ uint4 nan_to_ninf(uint4 q)
+{
+    if constexpr (DT == SV_BF16) {
+        return make_uint4(bf16x2_nan_to_ninf(q.x), bf16x2_nan_to_ninf(q.y), bf16x2_nan_to_ninf(q.z),
+                          bf16x2_nan_to_ninf(q.w));
+    } else {
+        auto f = [](uint32_t w) { return __uint_as_float(w) != __uint_as_float(w) ? 0xFF800000u : w; };
+        return make_uint4(f(q.x), f(q.y), f(q.z), f(q.w));
+    }
+}
+
+// the elements 2h and 2h + 1 of a vector as an fp32 pair (h < kEPV / 2), exact
+template <int DT>
+__device__ __forceinline__ unsigned long long vec_pair(uint4 q, int h)
+{
+    if constexpr (DT == SV_BF16) {
+        return bf16x2_to_f32x2(h == 0 ? q.x : h == 1 ? q.y : h == 2 ? q.z : q.w);
+    } else {
+        return h == 0 ? pack2(__uint_as_float(q.x), __uint_as_float(q.y))
+                      : pack2(__uint_as_float(q.z), __uint_as_float(q.w));
+    }
+}
+
+// element t of a vector (t < kEPV)
+template <int DT>
+__device__ __forceinline__ float vec_elem(uint4 q, int t)
+{
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    if constexpr (DT == SV_BF16) return (t & 1) ? bf16_hi(w[t >> 1]) : bf16_lo(w[t >> 1]);
+    else return __uint_as_float(w[t]);
+}
+
+// sum over the elements z of a vector of 2^(z c - m): packed fp32x2 arguments,
+// independent MUFU operations, a tree of packed adds
+template <int DT>
+__device__ __forceinline__ float exp_sum_vec(uint4 q, unsigned long long c2, unsigned long long nm2)
+{
+    constexpr int kP = FastCfg<DT>::kEPV / 2;
+    unsigned long long e[kP];
+#pragma unroll
+    for (int h = 0; h < kP; ++h) {
+        float a0, a1;
+        unpack2(fma2(vec_pair<DT>(q, h), c2, nm2), a0, a1);
+        e[h] = pack2(ex2(a0), ex2(a1));
+    }
+    unsigned long long s2 = e[0];
+#pragma unroll
+    for (int h = 1; h < kP; ++h) s2 = add2(s2, e[h]);
     float lo, hi;
-    unpack2(add2(add2(e0, e1), add2(e2, e3)), lo, hi);
+    unpack2(s2, lo, hi);
     return lo + hi;
 }
 
-
-
-// offset in the chunk of the first element equal to wm: vectors are numbered
-// lane + 32 e, elements 8 per vector; every lane takes part
-__device__ __forceinline__ uint32_t first_max_offset(const uint4 (&qv)[kVL], float wm, int lane)
+// offset among the lane's kHV vectors (numbered lane + 32 e, kEPV elements each) of the
+// first element equal to wm; every lane takes part
+template <int DT>
+__device__ __forceinline__ uint32_t first_max_offset(const uint4 (&qv)[kHV], float wm, int lane)
 {
-    int ef = kVL;
+    constexpr int kEPV = FastCfg<DT>::kEPV;
+    int ef = kHV;
 #pragma unroll
-    for (int e = kVL - 1; e >= 0; --e) {
-        const uint32_t m3 = bmax2_nan(bmax2_nan(qv[e].x, qv[e].y), bmax2_nan(qv[e].z, qv[e].w));
-        if (fmaxf(bf16_lo(m3), bf16_hi(m3)) == wm) ef = e;
-    }
+    for (int e = kHV - 1; e >= 0; --e)
+        if (vec_max<DT>(qv[e]) == wm) ef = e;
     uint32_t key = 0xFFFFFFFFu;
-    if (ef < kVL) {
+    if (ef < kHV) {
         uint4 v = qv[0];
 #pragma unroll
-        for (int e = 1; e < kVL; ++e)
+        for (int e = 1; e < kHV; ++e)
             if (ef == e) v = qv[e];
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-        int first = 7;
+        int first = kEPV - 1;
 #pragma unroll
-        for (int t = 7; t >= 0; --t) {
-            const float zt = (t & 1) ? bf16_hi(wv[t >> 1]) : bf16_lo(wv[t >> 1]);
-            if (zt == wm) first = t;
-        }
-        key = static_cast<uint32_t>((lane + 32 * ef) * 8 + first);
+        for (int t = kEPV - 1; t >= 0; --t)
+            if (vec_elem<DT>(v, t) == wm) first = t;
+        key = static_cast<uint32_t>((lane + 32 * ef) * kEPV + first);
     }
     return __reduce_min_sync(0xffffffffu, key);
+}
+
+// shared-memory 32-bit accesses at 32-bit shared addresses
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ void sts_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v));
+}
+
+// G[draft id] = the chunk's logit at an entry's offset; a pair holds (2 draft id, 2 offset)
+template <int DT>
+__device__ __forceinline__ void scatter4(uint32_t zs_a, uint32_t g_a, uint4 pq)
+{
+    const uint32_t pe[4] = {pq.x, pq.y, pq.z, pq.w};
+    uint32_t zv[4];
+    if constexpr (DT == SV_BF16) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) zv[e] = lds_u16(zs_a + (pe[e] & 0xFFFFu));
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sts_u16(g_a + (pe[e] >> 16), zv[e]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) zv[e] = lds_u32(zs_a + 2 * (pe[e] & 0xFFFFu));
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sts_u32(g_a + ((pe[e] >> 15) & ~3u), zv[e]);
+    }
+}
+
+// element e of a row held in bytes (global or shared)
+template <int DT>
+__device__ __forceinline__ float row_elem(const void* row, int32_t e)
+{
+    if constexpr (DT == SV_BF16)
+        return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(row)[e]) << 16);
+    else
+        return reinterpret_cast<const float*>(row)[e];
 }
 
 // this lane's register groups of the first kPadSlots (padded) support entries of a chunk
@@ -908,7 +1021,6 @@ __device__ __forceinline__ void load_pairs(const SampleArgs& A, int32_t p0, int 
 #pragma unroll
     for (int t = 0; t < kPairRegs; ++t) pg[t] = ld_nc_v4(reinterpret_cast<const uint4*>(A.plan.pairs + p0 + 4 * (lane + 32 * t)));
 }
-
 
 // 16-byte read-only global load with an L2 cache policy
 __device__ __forceinline__ uint4 ld_nc_v4_hint(const uint4* p, uint64_t pol)
@@ -973,12 +1085,14 @@ __device__ __forceinline__ float unit_temp(const SampleArgs& A, int64_t unit)
     return A.temp[static_cast<int32_t>(unit) / (A.k + 1)];
 }
 
-// issue sequence element q of unit u into `stage` (lane 0 only)
+// issue chunk q of unit u into `stage` (lane 0 only)
+template <int DT>
 __device__ __forceinline__ void issue_seq(const SampleArgs& A, const FastUnit& u, int32_t q, unsigned char* stage,
                                           uint64_t* bar, uint64_t pol_t)
 {
-    const uint32_t off = static_cast<uint32_t>(q) * kFastData;
-    const uint32_t nb = min(kFastData, static_cast<uint32_t>(A.V) * 2 - off);
+    constexpr uint32_t kSB = FastCfg<DT>::kStageBytes;
+    const uint32_t off = static_cast<uint32_t>(q) * kSB;
+    const uint32_t nb = min(kSB, static_cast<uint32_t>(A.V) * FastCfg<DT>::kElem - off);
     mbar_arrive_expect_tx(bar, nb);
     bulk_copy_g2s(stage, u.trow + off, nb, bar, pol_t);
 }
@@ -1009,12 +1123,14 @@ __device__ __forceinline__ void producer_enter(const SampleArgs& A, Producer& P,
 }
 
 // issue the warp's next chunk if a stage is free
+template <int DT>
 __device__ __forceinline__ void producer_step(const SampleArgs& A, Producer& P, uint32_t consumed, int w, int lane,
                                               int64_t units, unsigned char* wst, uint64_t* wbar, uint64_t pol_t)
 {
-    if (P.unit >= units || P.issued - consumed >= static_cast<uint32_t>(kFastStages)) return;
-    const uint32_t sidx = P.issued % kFastStages;
-    if (lane == 0) issue_seq(A, P.u, w + P.i * kStreamWarps, wst + sidx * kFastStage, &wbar[sidx], pol_t);
+    constexpr uint32_t kS = FastCfg<DT>::kStages;
+    if (P.unit >= units || P.issued - consumed >= kS) return;
+    const uint32_t sidx = P.issued % kS;
+    if (lane == 0) issue_seq<DT>(A, P.u, w + P.i * kStreamWarps, wst + sidx * FastCfg<DT>::kStageBytes, &wbar[sidx], pol_t);
     ++P.issued;
     if (++P.i == P.cnt) {
         P.unit += gridDim.x;
@@ -1035,19 +1151,23 @@ __device__ __forceinline__ void tv_bar_sync()
     asm volatile("bar.sync 1, %0;" ::"n"(kTvThreads) : "memory");
 }
 
+template <int DT>
 __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(SampleArgs A)
 {
+    using Cfg = FastCfg<DT>;
+    constexpr int kNG = Cfg::kNG, kS = Cfg::kStages, kE = Cfg::kElem, kEPV = Cfg::kEPV, kVPL = Cfg::kVPL;
+    constexpr uint32_t kSB = Cfg::kStageBytes;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // [stream warp][stage]
-    uint64_t* full = bars + kStreamWarps * kFastStages;  // [buffer]: records, G and draft-token slots written
-    uint64_t* freed = full + 2;                           // [buffer]: the TV warps are done with them
+    uint64_t* full = bars + kStreamWarps * kS;           // [buffer]: records, G and draft-token slots written
+    uint64_t* freed = full + kNG;                         // [buffer]: the TV warps are done with them
     unsigned char* ring = smem + kFastHeader;
-    const uint32_t gbytes = static_cast<uint32_t>(align256((static_cast<int64_t>(A.Vd) + 8) * 2));
-    unsigned char* gbase = ring + kStreamWarps * kFastStages * kFastStage;  // G of buffer 0, then of buffer 1
-    int32_t* ctab = reinterpret_cast<int32_t*>(gbase + 2 * gbytes);
-    __shared__ WarpRec wrec[2][kStreamWarps];
-    __shared__ float zx_s[2];      // target logit of the draft token
-    __shared__ int32_t jdx_s[2];   // its draft id (-1: off the support)
+    const uint32_t gbytes = static_cast<uint32_t>(align256((static_cast<int64_t>(A.Vd) + 8) * kE));
+    unsigned char* gbase = ring + kStreamWarps * kS * kSB;  // G of buffer 0 (then of buffer 1)
+    int32_t* ctab = reinterpret_cast<int32_t*>(gbase + kNG * gbytes);
+    __shared__ WarpRec wrec[kNG][kStreamWarps];
+    __shared__ float zx_s[kNG];      // target logit of the draft token
+    __shared__ int32_t jdx_s[kNG];   // its draft id (-1: off the support)
     __shared__ WarpRec merged;     // TV warps: the unit's merged record
     __shared__ DraftRec drec[kTvWarps];  // TV warps: their shares of the draft row
     __shared__ float wtv[kTvWarps];
@@ -1057,14 +1177,14 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
     pdl_wait_primary();  // a plan built in the same call must be complete
     pdl_launch_dependents();
     if (tid == 0) {
-        for (int i = 0; i < kFastStages * kStreamWarps; ++i) mbar_init(&bars[i], 1);
-        for (int b = 0; b < 2; ++b) {
+        for (int i = 0; i < kS * kStreamWarps; ++i) mbar_init(&bars[i], 1);
+        for (int b = 0; b < kNG; ++b) {
             mbar_init(&full[b], kStreamWarps * 32);
             mbar_init(&freed[b], kTvThreads);
         }
         fence_barrier_init();
     }
-    if (tid < 2) {
+    if (tid < kNG) {
         zx_s[tid] = NAN;
         jdx_s[tid] = -1;
     }
@@ -1078,22 +1198,22 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
     if (w < kStreamWarps) {
         // ================= stream warps =================
         const uint64_t pol_t = l2_policy_evict_first();
-        unsigned char* wst = ring + w * kFastStages * kFastStage;  // this warp's stages
-        uint64_t* wbar = bars + kFastStages * w;
-        uint32_t consumed = 0;  // chunks this warp has read so far (stage = consumed % kFastStages)
+        unsigned char* wst = ring + w * kS * kSB;  // this warp's stages
+        uint64_t* wbar = bars + kS * w;
+        uint32_t consumed = 0;  // chunks this warp has read so far (stage = consumed % kS)
         uint32_t timeout = 0;
 
         Producer P;
         P.unit = blockIdx.x;
         P.issued = 0;
         producer_enter(A, P, w, units, P.unit < units ? unit_temp(A, P.unit) : 0.f);
-        for (int i = 0; i < kFastStages; ++i)
-            producer_step(A, P, consumed, w, lane, units, wst, wbar, pol_t);
+        for (int i = 0; i < kS; ++i)
+            producer_step<DT>(A, P, consumed, w, lane, units, wst, wbar, pol_t);
 
         int64_t unit = blockIdx.x;
         float T = unit < units ? unit_temp(A, unit) : 0.f;
         for (uint32_t n = 0; unit < units; unit += gridDim.x, ++n) {
-            const uint32_t b = n & 1u;
+            const uint32_t b = n % kNG;
             const FastUnit u = fast_unit(A, unit, T);
             const int64_t un = unit + gridDim.x;
             const float T_next = un < units ? unit_temp(A, un) : 0.f;  // for the next unit, loaded early
@@ -1101,9 +1221,9 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
             const unsigned long long c2 = pack2(c, c);
             const int32_t xj = u.has_draft ? A.draft[static_cast<int64_t>(u.r) * A.k + u.j] : -1;
             const int32_t nw_chunks = warp_chunks(u.n, w);
-            uint16_t* G = reinterpret_cast<uint16_t*>(gbase + b * gbytes);
+            unsigned char* G = gbase + b * gbytes;
             // the TV warps are done with this buffer's previous unit
-            if (n >= 2 && !timeout && !mbar_wait_bounded(&freed[b], ((n >> 1) + 1) & 1u)) timeout = 1;
+            if (n >= kNG && !timeout && !mbar_wait_bounded(&freed[b], ((n / kNG) + 1) & 1u)) timeout = 1;
 
             float tm = -INFINITY, ts = 0.f, bv = -INFINITY;
             int32_t bx = INT32_MAX;
@@ -1111,16 +1231,16 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
             uint4 pg[kPairRegs];  // support entries of the target chunk pg_for (-1: none)
             int32_t pg_for = -1;
             for (int32_t i = 0; i < nw_chunks; ++i) {
-                const uint32_t sidx = consumed % kFastStages;
-                if (!timeout && !mbar_wait_bounded(&wbar[sidx], (consumed / kFastStages) & 1u)) timeout = 1;
-                const unsigned char* st = wst + sidx * kFastStage;
+                const uint32_t sidx = consumed % kS;
+                if (!timeout && !mbar_wait_bounded(&wbar[sidx], (consumed / kS) & 1u)) timeout = 1;
+                const unsigned char* st = wst + sidx * kSB;
                 const uint4* vp = reinterpret_cast<const uint4*>(st);
                 const int32_t q = w + i * kStreamWarps;
                 const int32_t cidx = q;  // target chunk
-                const uint32_t off = static_cast<uint32_t>(cidx) * kFastData;
-                const uint32_t nb = min(kFastData, static_cast<uint32_t>(A.V) * 2 - off);
+                const uint32_t off = static_cast<uint32_t>(cidx) * kSB;
+                const uint32_t nb = min(kSB, static_cast<uint32_t>(A.V) * kE - off);
                 const int nv = static_cast<int>(nb / 16);
-                const int32_t x0 = static_cast<int32_t>(off / 2);
+                const int32_t x0 = static_cast<int32_t>(off / kE);
                 // support entries of a target chunk: this lane's groups of four packed pairs, from
                 // L2 while the maxima and exponentials below run
                 const bool scatter = u.has_draft && plan_ok;
@@ -1131,88 +1251,73 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                     p1 = p0 + ctab[cidx];
                     if (pg_for != cidx) load_pairs(A, p0, lane, pg);  // not prefetched
                 }
-                if (nv < kVL * 32) {
+                if (nv < kVPL * 32) {
                     // the row's last chunk: -inf beyond its end, so that every lane reads whole
                     // vectors; the fence orders these writes before the next bulk copy here
-                    for (int v = nv + lane; v < kVL * 32; v += 32)
-                        const_cast<uint4*>(vp)[v] = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+                    for (int v = nv + lane; v < kVPL * 32; v += 32) const_cast<uint4*>(vp)[v] = ninf_vec(kE);
                     fence_proxy_async_smem();
                     __syncwarp();
                 }
-                uint4 qv[kVL];
 #pragma unroll
-                for (int e = 0; e < kVL; ++e) qv[e] = vp[lane + 32 * e];
-                // one packed NaN-propagating max tree over the lane's vectors, widened once
-                uint32_t m2 = bmax2_nan(bmax2_nan(qv[0].x, qv[0].y), bmax2_nan(qv[0].z, qv[0].w));
+                for (int h = 0; h < Cfg::kHalves; ++h) {
+                    uint4 qv[kHV];
 #pragma unroll
-                for (int e = 1; e < kVL; ++e)
-                    m2 = bmax2_nan(m2, bmax2_nan(bmax2_nan(qv[e].x, qv[e].y), bmax2_nan(qv[e].z, qv[e].w)));
-                float lm = fmax_nan(bf16_lo(m2), bf16_hi(m2));
-                if (lm != lm) {  // rare: NaN logits read as -inf
-                    tflags |= kFlagNaN;
-                    lm = -INFINITY;
+                    for (int e = 0; e < kHV; ++e) qv[e] = vp[lane + 32 * (kHV * h + e)];
+                    // one NaN-propagating max tree over the lane's vectors
+                    float lm = group_max<DT>(qv);
+                    if (lm != lm) {  // rare: NaN logits read as -inf
+                        tflags |= kFlagNaN;
+                        lm = -INFINITY;
 #pragma unroll
-                    for (int e = 0; e < kVL; ++e) {
-                        qv[e] = make_uint4(bf16x2_nan_to_ninf(qv[e].x), bf16x2_nan_to_ninf(qv[e].y),
-                                           bf16x2_nan_to_ninf(qv[e].z), bf16x2_nan_to_ninf(qv[e].w));
-                        const uint32_t m3 = bmax2_nan(bmax2_nan(qv[e].x, qv[e].y), bmax2_nan(qv[e].z, qv[e].w));
-                        lm = fmaxf(lm, fmaxf(bf16_lo(m3), bf16_hi(m3)));
+                        for (int e = 0; e < kHV; ++e) {
+                            qv[e] = nan_to_ninf<DT>(qv[e]);
+                            lm = fmaxf(lm, vec_max<DT>(qv[e]));
+                        }
                     }
-                }
-                // Each lane sums its exponentials against its own maximum lr, so that they do not wait
-                // for the warp maximum; the lane's sum is then moved to the warp's running reference
-                // rm (the running maximum of z c) with one more exponential.
-                const bool sums = u.sampling;
-                float& rm = tm;
-                float& rs_ = ts;
-                const float lr = lm > -INFINITY ? lm * c : 0.f;
-                float acc = 0.f;
-                if (sums) {
-                    const unsigned long long nl2 = pack2(-lr, -lr);
-                    float ae[kVL];
+                    // Each lane sums its exponentials against its own maximum lr, so that they do
+                    // not wait for the warp maximum; the lane's sum is then moved to the warp's
+                    // running reference tm (the running maximum of z c) with one more exponential.
+                    const float lr = lm > -INFINITY ? lm * c : 0.f;
+                    float acc = 0.f;
+                    if (u.sampling) {
+                        const unsigned long long nl2 = pack2(-lr, -lr);
+                        float ae[kHV];
 #pragma unroll
-                    for (int e = 0; e < kVL; ++e) ae[e] = exp_sum8(qv[e], c2, nl2);
-                    acc = ((ae[0] + ae[1]) + (ae[2] + ae[3])) + ((ae[4] + ae[5]) + (ae[6] + ae[7]));
-                }
-                const float wm = warp_max(lm);
-                if (wm > bv) {  // warp-uniform, rare after the first chunks
-                    bx = x0 + static_cast<int32_t>(first_max_offset(qv, wm, lane));
-                    bv = wm;
-                }
-                if (sums) {
-                    const float mt = wm * c;
-                    if (mt > rm) {  // warp-uniform
-                        rs_ *= rm == -INFINITY ? 0.f : ex2(rm - mt);
-                        rm = mt;
+                        for (int e = 0; e < kHV; ++e) ae[e] = exp_sum_vec<DT>(qv[e], c2, nl2);
+                        acc = ((ae[0] + ae[1]) + (ae[2] + ae[3])) + ((ae[4] + ae[5]) + (ae[6] + ae[7]));
                     }
-                    csum = lm > -INFINITY ? acc * ex2(lr - rm) : 0.f;
-                    rs_ += csum;
+                    const float wm = warp_max(lm);
+                    if (wm > bv) {  // warp-uniform, rare after the first chunks
+                        bx = x0 + kHV * 32 * kEPV * h + static_cast<int32_t>(first_max_offset<DT>(qv, wm, lane));
+                        bv = wm;
+                    }
+                    if (u.sampling) {
+                        const float mt = wm * c;
+                        if (mt > tm) {  // warp-uniform
+                            const float sc = tm == -INFINITY ? 0.f : ex2(tm - mt);
+                            ts *= sc;
+                            csum *= sc;
+                            tm = mt;
+                        }
+                        const float add = lm > -INFINITY ? acc * ex2(lr - tm) : 0.f;
+                        csum += add;
+                        ts += add;
+                    }
                 }
                 if (scatter) {
                     // G[draft id] = z at the chunk offset for every entry of the lane's groups; a
                     // padding entry writes the spare slot G[Vd], which nothing reads
-                    const uint16_t* zs = reinterpret_cast<const uint16_t*>(st);
                     const uint32_t zs_a = smem_addr(st), g_a = smem_addr(G);
-                    const bool here = xj >= x0 && xj < x0 + static_cast<int32_t>(nb / 2);
+                    const bool here = xj >= x0 && xj < x0 + static_cast<int32_t>(nb / kE);
 #pragma unroll
-                    for (int t = 0; t < kPairRegs; ++t) {  // every chunk has kPadSlots entries or padding
-                        const uint32_t pe[4] = {pg[t].x, pg[t].y, pg[t].z, pg[t].w};
-                        uint32_t zv[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) zv[e] = lds_u16(zs_a + (pe[e] & 0xFFFFu));
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) sts_u16(g_a + (pe[e] >> 16), zv[e]);
-                    }
+                    for (int t = 0; t < kPairRegs; ++t)  // every chunk has kPadSlots entries or padding
+                        scatter4<DT>(zs_a, g_a, pg[t]);
                     // groups beyond this lane's registers (chunks denser than 512 entries)
-                    for (int32_t g = p0 + 4 * 32 * kPairRegs + 4 * lane; g < p1; g += 4 * 32) {
-                        const uint4 q4 = ld_nc_v4(reinterpret_cast<const uint4*>(A.plan.pairs + g));
-                        const uint32_t pe[4] = {q4.x, q4.y, q4.z, q4.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) sts_u16(g_a + (pe[e] >> 16), lds_u16(zs_a + (pe[e] & 0xFFFFu)));
-                    }
+                    for (int32_t g = p0 + 4 * 32 * kPairRegs + 4 * lane; g < p1; g += 4 * 32)
+                        scatter4<DT>(zs_a, g_a, ld_nc_v4(reinterpret_cast<const uint4*>(A.plan.pairs + g)));
                     if (here) {  // the draft token: its logit and its draft id (from the registers)
                         const uint32_t xoff = static_cast<uint32_t>(xj - x0);
-                        if (lane == 0) zx_s[b] = __uint_as_float(static_cast<uint32_t>(zs[xoff]) << 16);
+                        if (lane == 0) zx_s[b] = row_elem<DT>(st, static_cast<int32_t>(xoff));
 #pragma unroll
                         for (int t = 0; t < kPairRegs; ++t) {
                             const uint32_t pe[4] = {pg[t].x, pg[t].y, pg[t].z, pg[t].w};
@@ -1242,7 +1347,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                 __syncwarp();
                 ++consumed;
                 if (lane == 0) fence_proxy_async_smem();
-                producer_step(A, P, consumed, w, lane, units, wst, wbar, pol_t);
+                producer_step<DT>(A, P, consumed, w, lane, units, wst, wbar, pol_t);
                 if (u.sampling) {
                     // this chunk's (reference, sum) for the race
                     float cs = csum;
@@ -1264,7 +1369,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
         if (timeout && lane == 0) {
             // give this warp's copies that may still be in flight a bounded chance to land
             for (uint32_t g = consumed; g < P.issued; ++g)
-                (void)mbar_wait_bounded(&wbar[g % kFastStages], (g / kFastStages) & 1u);
+                (void)mbar_wait_bounded(&wbar[g % kS], (g / kS) & 1u);
         }
         return;
     }
@@ -1276,22 +1381,22 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_keep));
     int64_t unit = blockIdx.x;
     for (uint32_t n = 0; unit < units; unit += gridDim.x, ++n) {
-        const uint32_t b = n & 1u;
+        const uint32_t b = n % kNG;
         const float T = unit_temp(A, unit);
         const FastUnit u = fast_unit(A, unit, T);
         const float c = u.sampling ? kLog2e / T : 0.f;
         const int32_t xj = u.has_draft ? A.draft[static_cast<int64_t>(u.r) * A.k + u.j] : -1;
         const uint64_t seed = (u.has_draft && ttid == 0) ? A.seeds[u.r] : 0ull;  // for the accept test
-        const uint16_t* G = reinterpret_cast<const uint16_t*>(gbase + b * gbytes);
+        const unsigned char* G = gbase + b * gbytes;
 
-        const int32_t nv8 = u.has_draft ? A.Vd / 8 : 0;  // Vd % 8 == 0 on this path
+        const int32_t nv8 = u.has_draft ? A.Vd / kEPV : 0;  // draft-row vectors (Vd % 8 == 0 on this path)
         const uint4* yv = reinterpret_cast<const uint4*>(u.drow);
         {
             // ---- the draft row, read by these warps (from HBM, kept in L2 for the TV pass)
             // while the stream warps read the target row: maximum, sum at T, flags.  Each
             // thread sums a batch against the batch maximum and moves it to its running
             // reference. ----
-            constexpr int kDraftBatch = 8;
+            constexpr int kDraftBatch = kHV;
             const unsigned long long c2 = pack2(c, c);
             float rm = -INFINITY, rs = 0.f;
             uint32_t fl = 0;
@@ -1301,23 +1406,16 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
 #pragma unroll
                 for (int i = 0; i < kDraftBatch; ++i) {
                     const int32_t v = v0 + i * kTvThreads;
-                    yb[i] = v < nv8 ? ld_nc_v4_hint(yv + v, pol_keep)
-                                    : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+                    yb[i] = v < nv8 ? ld_nc_v4_hint(yv + v, pol_keep) : ninf_vec(kE);
                 }
-                uint32_t m2 = bmax2_nan(bmax2_nan(yb[0].x, yb[0].y), bmax2_nan(yb[0].z, yb[0].w));
-#pragma unroll
-                for (int i = 1; i < kDraftBatch; ++i)
-                    m2 = bmax2_nan(m2, bmax2_nan(bmax2_nan(yb[i].x, yb[i].y), bmax2_nan(yb[i].z, yb[i].w)));
-                float lm = fmax_nan(bf16_lo(m2), bf16_hi(m2));
+                float lm = group_max<DT>(yb);
                 if (lm != lm) {  // rare: NaN logits, flagged (the request is verified greedily)
                     fl |= kFlagNaN;
                     lm = -INFINITY;
 #pragma unroll
                     for (int i = 0; i < kDraftBatch; ++i) {
-                        yb[i] = make_uint4(bf16x2_nan_to_ninf(yb[i].x), bf16x2_nan_to_ninf(yb[i].y),
-                                           bf16x2_nan_to_ninf(yb[i].z), bf16x2_nan_to_ninf(yb[i].w));
-                        const uint32_t m3 = bmax2_nan(bmax2_nan(yb[i].x, yb[i].y), bmax2_nan(yb[i].z, yb[i].w));
-                        lm = fmaxf(lm, fmaxf(bf16_lo(m3), bf16_hi(m3)));
+                        yb[i] = nan_to_ninf<DT>(yb[i]);
+                        lm = fmaxf(lm, vec_max<DT>(yb[i]));
                     }
                 }
                 if (lm == INFINITY) fl |= kFlagPosInf;
@@ -1326,7 +1424,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                     const unsigned long long nl2 = pack2(-lr, -lr);
                     float ae[kDraftBatch];
 #pragma unroll
-                    for (int i = 0; i < kDraftBatch; ++i) ae[i] = exp_sum8(yb[i], c2, nl2);
+                    for (int i = 0; i < kDraftBatch; ++i) ae[i] = exp_sum_vec<DT>(yb[i], c2, nl2);
                     const float acc = ((ae[0] + ae[1]) + (ae[2] + ae[3])) + ((ae[4] + ae[5]) + (ae[6] + ae[7]));
                     if (lr > rm) {
                         rs *= rm == -INFINITY ? 0.f : ex2(rm - lr);
@@ -1347,7 +1445,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
 
         // the first batch of the TV pass's draft-row loads, in flight while the stream warps
         // finish the unit
-        constexpr int kTvIter = (kFastMaxVd / 8 + kTvThreads - 1) / kTvThreads;
+        constexpr int kTvIter = (kFastMaxVd / kEPV + kTvThreads - 1) / kTvThreads;
         constexpr int kTvBatch = 8;  // draft-row loads in flight per thread
         uint4 yq[kTvBatch];
 #pragma unroll
@@ -1355,7 +1453,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
             const int32_t v = ttid + i * kTvThreads;
             if (v < nv8) yq[i] = ld_nc_v4(yv + v);
         }
-        if (!tto && !mbar_wait_bounded(&full[b], (n >> 1) & 1u)) tto = 1;
+        if (!tto && !mbar_wait_bounded(&full[b], (n / kNG) & 1u)) tto = 1;
 
         // ---- merge the stream warps' records: max, first argmax, reference maxima, sums ----
         if (tw == 0) {
@@ -1424,14 +1522,12 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                     if (v >= nv8) break;
                     const uint4 yqi = yq[i];
                     const uint4 gq = gv[v];
-                    const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
-                    const uint32_t yw[4] = {yqi.x, yqi.y, yqi.z, yqi.w};
-                    float dv[8];
+                    float dv[kEPV];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
+                    for (int e = 0; e < kEPV / 2; ++e) {
                         // q and p of two ids at once: q - p = 2^(y c - Mq) / Sq - 2^(z c - M) / S
-                        const unsigned long long ty = fma2(bf16x2_to_f32x2(yw[e]), c2m, nMq);
-                        const unsigned long long tz = fma2(bf16x2_to_f32x2(gw[e]), c2m, nM);
+                        const unsigned long long ty = fma2(vec_pair<DT>(yqi, e), c2m, nMq);
+                        const unsigned long long tz = fma2(vec_pair<DT>(gq, e), c2m, nM);
                         float y0, y1, z0, z1;
                         unpack2(ty, y0, y1);
                         unpack2(tz, z0, z1);
@@ -1439,8 +1535,13 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                         const unsigned long long np = mul2(pack2(ex2(z0), ex2(z1)), niS);
                         unpack2(fma2(eq, iSq, np), dv[2 * e], dv[2 * e + 1]);
                     }
-                    a += ((fmaxf(dv[0], 0.f) + fmaxf(dv[1], 0.f)) + (fmaxf(dv[2], 0.f) + fmaxf(dv[3], 0.f))) +
-                         ((fmaxf(dv[4], 0.f) + fmaxf(dv[5], 0.f)) + (fmaxf(dv[6], 0.f) + fmaxf(dv[7], 0.f)));
+                    float pv[kEPV];
+#pragma unroll
+                    for (int e = 0; e < kEPV; ++e) pv[e] = fmaxf(dv[e], 0.f);
+                    if constexpr (kEPV == 8)
+                        a += ((pv[0] + pv[1]) + (pv[2] + pv[3])) + ((pv[4] + pv[5]) + (pv[6] + pv[7]));
+                    else
+                        a += (pv[0] + pv[1]) + (pv[2] + pv[3]);
                 }
                 // the next batch of draft-row loads
 #pragma unroll
@@ -1463,8 +1564,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                 const float zx = zraw != zraw ? -INFINITY : zraw;
                 pj = in_range ? ex2(fmaf(zx, c, -M)) * invS : 0.f;
                 if (in_range && jdx >= 0) {  // q at the draft id, as the TV pass takes it
-                    const uint32_t yb = reinterpret_cast<const uint16_t*>(u.drow)[jdx];
-                    qj = ex2(fmaf(__uint_as_float(yb << 16), c, -Mq)) * invSq;
+                    qj = ex2(fmaf(row_elem<DT>(u.drow, jdx), c, -Mq)) * invSq;
                 } else {
                     qj = 0.f;
                 }
@@ -1719,7 +1819,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) race_rows_kernel(SampleArgs A)
     uint32_t status = 0;
     // bounded race on a rejected row: its draft row into shared memory, one bulk copy that lands
     // while the chunk bounds are ranked (the bulk-copy path has 16-byte rows and Vd % 8 == 0)
-    const bool ycopy = !greedy && cst_r != nullptr && n < k;
+    const bool ycopy = DD == SV_BF16 && !greedy && cst_r != nullptr && n < k;
     bool ywait = ycopy;  // the copy is still to be waited for
     if (ycopy && tid == 0) {
         const uint32_t yb_bytes = static_cast<uint32_t>(A.Vd) * 2;
@@ -2221,18 +2321,26 @@ SampleLayout sample_layout(int64_t R, int32_t k, int32_t V, int32_t Vd, int et, 
 // the opt-in shared memory of a CTA (227 KB) less room for the kernel's static arrays
 constexpr size_t kFastSmemLimit = 227 * 1024 - 1024;
 
+template <int DT>
 size_t fast_smem_bytes(int32_t V, int32_t Vd)
 {
-    return static_cast<size_t>(kFastHeader + kStreamWarps * kFastStages * static_cast<int64_t>(kFastStage) +
-                               2 * align256((static_cast<int64_t>(Vd) + 8) * 2) +
+    using Cfg = FastCfg<DT>;
+    return static_cast<size_t>(kFastHeader + kStreamWarps * Cfg::kStages * static_cast<int64_t>(Cfg::kStageBytes) +
+                               Cfg::kNG * align256((static_cast<int64_t>(Vd) + 8) * Cfg::kElem) +
                                (static_cast<int64_t>(V + kChunkElems - 1) / kChunkElems + 1) * 4);
 }
 
+size_t fast_smem_bytes(const Rows& t, const Rows& d)
+{
+    return t.dtype == SV_BF16 ? fast_smem_bytes<SV_BF16>(t.width, d.width) : fast_smem_bytes<SV_F32>(t.width, d.width);
+}
+
+// the fast row pass: bf16 target and draft rows, or fp32 target and draft rows, with a d2t map
 bool fast_path_ok(const Rows& t, const Rows& d, bool identity)
 {
-    return !identity && t.dtype == SV_BF16 && d.dtype == SV_BF16 && t.bulk_ok && d.bulk_ok && d.data != nullptr &&
-           t.width % 8 == 0 && d.width % 8 == 0 && d.width < kFastMaxVd &&  // 2 Vd fits 16 bits
-           fast_smem_bytes(t.width, d.width) <= kFastSmemLimit;
+    return !identity && t.dtype == d.dtype && t.bulk_ok && d.bulk_ok && d.data != nullptr && t.width % 8 == 0 &&
+           d.width % 8 == 0 && d.width < kFastMaxVd &&  // 2 Vd fits 16 bits
+           fast_smem_bytes(t, d) <= kFastSmemLimit;
 }
 
 }  // namespace
@@ -2318,14 +2426,14 @@ static cudaError_t launch_sample_t(const Rows& t, const Rows& d, const int32_t* 
     cfg.attrs = attr;
     cfg.numAttrs = own_plan ? 1 : 0;
     if (fast) {
-        const size_t smem = fast_smem_bytes(t.width, d.width);
-        e = cudaFuncSetAttribute(sample_rows_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem));
+        const size_t smem = fast_smem_bytes(t, d);
+        auto* kern = t.dtype == SV_BF16 ? sample_rows_fast_kernel<SV_BF16> : sample_rows_fast_kernel<SV_F32>;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         cfg.gridDim = dim3(static_cast<unsigned>(L.grid));
         cfg.blockDim = dim3(kFastThreads);
         cfg.dynamicSmemBytes = smem;
-        e = cudaLaunchKernelEx(&cfg, sample_rows_fast_kernel, A);
+        e = cudaLaunchKernelEx(&cfg, kern, A);
     } else {
         e = cudaFuncSetAttribute(sample_rows_kernel<DT, DD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(L.smem_bytes));

@@ -198,28 +198,30 @@ def _with_d2t(w, d2t, seed):
     return w
 
 
-def test_dense_support_chunks_use_the_overflow_groups(sv):
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_dense_support_chunks_use_the_overflow_groups(sv, dtype):
     """A d2t whose image covers whole 2048-id chunks: more support entries per chunk than
     the row pass holds in registers, so the scatter and the draft-id search take their
     overflow paths; also a draft vocabulary at the largest width of the row pass."""
-    w = workloads.sample_batch(6, 4, 40960, None, torch.bfloat16, T=0.9, sigma_pos=0.6, seed=21)
+    w = workloads.sample_batch(6, 4, 40960, None, dtype, T=0.9, sigma_pos=0.6, seed=21)
     g = torch.Generator(device="cuda")
     g.manual_seed(3)
     dense = torch.cat([torch.arange(0, 6144, device="cuda"),                    # three full chunks
                        torch.randperm(40960 - 6144, generator=g, device="cuda")[:26616] + 6144]).to(torch.int32)
     w2 = _with_d2t(w, dense, 4)
-    assert w2["Vd"] == 32760  # the widest draft vocabulary of the bf16 row pass
+    assert w2["Vd"] == 32760  # the widest draft vocabulary of the row pass
     compare(_run(sv, w2), _oracle(w2))
 
 
-def test_zero_residual_mass_on_the_bulk_copy_path(sv):
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_zero_residual_mass_on_the_bulk_copy_path(sv, dtype):
     """Positions 0 and 1 of every other request: the target and the draft rows put all their
     mass on one support id (every other logit -inf), so p = q exactly.  Position 0 drafts
     that id (p / q = 1: accepted); position 1 drafts an id off the support, rejected
     (status 4) with no residual mass anywhere, so the correction is drawn from p
     (status 8), which can only be that id."""
     R, k, V, Vd = 8, 3, 8192, 4096
-    w = workloads.sample_batch(R, k, V, Vd, torch.bfloat16, T=1.0, sigma_pos=0.5, seed=22)
+    w = workloads.sample_batch(R, k, V, Vd, dtype, T=1.0, sigma_pos=0.5, seed=22)
     d2t = w["d2t"].long()
     off = torch.ones(V, dtype=torch.bool, device="cuda")
     off[d2t] = False
@@ -231,8 +233,8 @@ def test_zero_residual_mass_on_the_bulk_copy_path(sv):
             t[r, j, d2t[100 + r]] = 1.5
             y[r, j] = float("-inf")
             y[r, j, 100 + r] = 1.5
-    w["target"] = t.reshape(R * (k + 1), V).to(torch.bfloat16).contiguous()
-    w["draft_logits"] = y.reshape(R * k, Vd).to(torch.bfloat16).contiguous()
+    w["target"] = t.reshape(R * (k + 1), V).to(dtype).contiguous()
+    w["draft_logits"] = y.reshape(R * k, Vd).to(dtype).contiguous()
     draft = w["draft"].clone()
     off_ids = torch.nonzero(off).flatten()
     draft[::2, 0] = d2t[100 + torch.arange(0, R, 2, device="cuda")].to(torch.int32)  # p/q = 1 at position 0
