@@ -66,6 +66,8 @@ def _load():
             lib.or_verify_greedy.restype = C.c_int
             lib.or_top2_rows.argtypes = [P, C.c_int, i64, i64, i32, P]
             lib.or_top2_rows.restype = C.c_int
+            lib.or_infer_modality.argtypes = [P, C.c_int, i64, i64, i32, P, i32, P, P, P, P]
+            lib.or_infer_modality.restype = C.c_int
             lib.or_verify_sample.argtypes = [P, C.c_int, i64, i32, P, C.c_int, i64, i32, P, i32, i32,
                                              P, P, P, P, P, P, P, P, P, P, P]
             lib.or_verify_sample.restype = C.c_int
@@ -169,6 +171,20 @@ def top2_rows(rows):
     t, code, stride, V = _rows(rows, "rows")
     out = np.zeros((t.shape[0], 2), np.int32)
     rc = _load().or_top2_rows(_ptr(t), code, stride, t.shape[0], V, _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments ({rc})")
+    return out
+
+
+def infer_modality(rows, part_start):
+    """Per row of full-vocabulary logits: argmax, the partition holding it (-1: none) and
+    that partition's id range [lo, hi) (0, 0 when none)."""
+    t, code, stride, V = _rows(rows, "rows")
+    ps = _i32(part_start)
+    n = t.shape[0]
+    out = {key: np.zeros(n, np.int32) for key in ("amax", "part", "mask_lo", "mask_hi")}
+    rc = _load().or_infer_modality(_ptr(t), code, stride, n, V, _ptr(ps), ps.size - 1, _ptr(out["amax"]),
+                                   _ptr(out["part"]), _ptr(out["mask_lo"]), _ptr(out["mask_hi"]))
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments ({rc})")
     return out

@@ -217,6 +217,40 @@ int or_top2_rows(const void* rows, int dtype, int64_t row_stride, int64_t nrows,
     return 0;
 }
 
+/* modality of a row of the full vocabulary ("An Efficient vLLM-Based
+ * Inference Pipeline ..." phase management: the vocabulary is split into a
+ * text part and S audio sub-vocabularies, and the current modality is the
+ * partition holding the maximum of the unmasked distribution): per row the
+ * argmax (NaN read as -inf, lowest id), the partition p with
+ * part_start[p] <= argmax < part_start[p + 1] (-1 when none), and that
+ * partition's id range [lo, hi) as the phase mask of the next step (0, 0
+ * when none).  part_start holds P + 1 ascending ids. */
+int or_infer_modality(const void* rows, int dtype, int64_t row_stride, int64_t nrows, int32_t V,
+                      const int32_t* part_start, int32_t P, int32_t* amax, int32_t* part,
+                      int32_t* mask_lo, int32_t* mask_hi)
+{
+    if (V < 1 || nrows < 0 || P < 1) return -1;
+    for (int32_t p = 0; p < P; ++p)
+        if (part_start[p] > part_start[p + 1]) return -1;
+    double* z = (double*)malloc(sizeof(double) * (size_t)V);
+    for (int64_t r = 0; r < nrows; ++r) {
+        for (int32_t x = 0; x < V; ++x) z[x] = load_elem(rows, dtype, r * row_stride + x);
+        const int32_t a = argmax_row(z, V);
+        int32_t pi = -1;
+        for (int32_t p = 0; p < P; ++p)
+            if (part_start[p] <= a && a < part_start[p + 1]) {
+                pi = p;
+                break;
+            }
+        amax[r] = a;
+        part[r] = pi;
+        mask_lo[r] = pi < 0 ? 0 : part_start[pi];
+        mask_hi[r] = pi < 0 ? 0 : part_start[pi + 1];
+    }
+    free(z);
+    return 0;
+}
+
 /* p = softmax(z / T) in fp64; NaN read as -inf.  Caller ensures the row
  * is not bad. */
 static void softmax_T(const double* z, int32_t n, double T, double* p)

@@ -506,6 +506,29 @@ def test_top2_special_cases_and_greedy_argmax():
     assert res["tokens"][0, 0] == oracle.top2_rows(z)[0, 0] == 10
 
 
+def test_modality_is_the_partition_of_the_unmasked_argmax():
+    """Text part [0, 100), codebooks [100, 164), [164, 228), a gap [228, 240) in no partition."""
+    rng = np.random.default_rng(33)
+    V, starts = 240, np.array([0, 100, 164, 228], np.int32)
+    rows = rng.normal(0, 1, (60, V)).astype(np.float32)
+    planted = rng.integers(0, V, 60)
+    rows[np.arange(60), planted] = 9.0
+    rows[0, 99] = rows[0, 100] = 20.0          # tie across a boundary: the lower id, text
+    rows[1, :] = np.nan                       # all NaN: argmax 0
+    rows[2, 230] = 30.0                       # in the gap: no partition
+    out = oracle.infer_modality(rows, starts)
+    amax = _top2_by_sort(rows)[:, 0]
+    assert np.array_equal(out["amax"], amax)
+    want = np.searchsorted(starts, amax, side="right") - 1
+    want[amax >= starts[-1]] = -1
+    assert np.array_equal(out["part"], want)
+    ok = want >= 0
+    assert np.array_equal(out["mask_lo"][ok], starts[want[ok]])
+    assert np.array_equal(out["mask_hi"][ok], starts[want[ok] + 1])
+    assert np.all(out["mask_lo"][~ok] == 0) and np.all(out["mask_hi"][~ok] == 0)
+    assert out["part"][:3].tolist() == [0, 0, -1]
+
+
 def test_bf16_rows_are_widened_exactly():
     rng = np.random.default_rng(3)
     V = 33
