@@ -81,6 +81,7 @@ enum {
 /* limits */
 #define SV_MAX_K 256       /* drafts per request (per branch) */
 #define SV_MAX_S 16        /* codebooks per CFG frame */
+#define SV_MAX_PARTS 64    /* vocabulary partitions of sv_infer_modality */
 #define SV_MAX_WIDTH (1 << 30)
 
 /* A matrix of logit rows: row i, entry x is at data + (i * row_stride + x)
@@ -145,6 +146,34 @@ int sv_verify_greedy_top2(sv_rows target, int32_t R, int32_t k, int32_t branches
                           const int32_t* draft, int32_t* accept_len, int32_t* tokens,
                           int32_t* branch, int32_t* status, int32_t* top2, void* workspace,
                           size_t workspace_bytes, sv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * sv_infer_modality -- the modality of each row of full-vocabulary logits and
+ * the phase mask of its next step.
+ * Source: "An Efficient vLLM-Based Inference Pipeline ..." phase management and
+ * Figure 1 text: the vocabulary is split into a text part and S audio
+ * sub-vocabularies; since continuous batching flattens the requests' tokens,
+ * the current modality is inferred from the partition that holds the maximum
+ * of the unmasked output distribution.
+ *
+ *   logits      N rows of raw logits over the full vocabulary, width V.
+ *   part_start  HOST int32 [P + 1], ascending: partition p is the id range
+ *               [part_start[p], part_start[p + 1]) (e.g. the text part, then
+ *               the S codebooks); ids outside every range belong to none.
+ *   P           partitions, 1 <= P <= SV_MAX_PARTS.
+ *   amax        int32 [N] out or NULL: argmax of the row (NaN read as -inf,
+ *               lowest id among equal maxima).
+ *   part        int32 [N] out: the partition holding the argmax, -1 for none.
+ *   mask_lo, mask_hi  int32 [N] out or NULL: that partition's id range, the
+ *               vocabulary mask of the row's next step (0, 0 for none).
+ *   status      int32 [N] out or NULL: SV_ST_BAD_LOGITS for NaN or +-inf maxima.
+ * The workspace is sized by sv_infer_modality_workspace(N, V).
+ * ---------------------------------------------------------------------- */
+size_t sv_infer_modality_workspace(int32_t N, int32_t V);
+int sv_infer_modality(sv_rows logits, int32_t N, const int32_t* part_start, int32_t P,
+                      int32_t* amax, int32_t* part, int32_t* mask_lo, int32_t* mask_hi,
+                      int32_t* status, void* workspace, size_t workspace_bytes,
+                      sv_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * sv_verify_greedy_noalloc -- sv_verify_greedy without a workspace argument.

@@ -26,7 +26,7 @@ MAX_K, MAX_S = 256, 16
 # kernels launched by one call of each entry point (reported by the benchmark)
 # kernels one call launches: verify_sample with a prebuilt d2t plan (or the identity map)
 # launches 2, and 2 more when it builds the plan itself; d2t_plan launches 2
-LAUNCHES = {"verify_greedy": 2, "verify_greedy_top2": 2, "verify_sample": 2, "verify_sample_plan_in_call": 4, "d2t_plan": 2,
+LAUNCHES = {"verify_greedy": 2, "verify_greedy_top2": 2, "infer_modality": 2, "verify_sample": 2, "verify_sample_plan_in_call": 4, "d2t_plan": 2,
             "cfg_merge_sample": 2, "accept_scan": 1}
 
 
@@ -65,6 +65,10 @@ def load(path: str | None = None):
     lib.sv_verify_greedy_top2_workspace.restype = sz
     lib.sv_verify_greedy_top2.argtypes = [SvRows, i32, i32, i32, P, P, P, P, P, P, P, sz, P]
     lib.sv_verify_greedy_top2.restype = C.c_int
+    lib.sv_infer_modality_workspace.argtypes = [i32, i32]
+    lib.sv_infer_modality_workspace.restype = sz
+    lib.sv_infer_modality.argtypes = [SvRows, i32, P, i32, P, P, P, P, P, P, sz, P]
+    lib.sv_infer_modality.restype = C.c_int
     lib.sv_verify_sample_workspace.argtypes = [i32, i32, i32, i32]
     lib.sv_verify_sample_workspace.restype = sz
     lib.sv_verify_sample.argtypes = [SvRows, SvRows, P, P, i32, i32, P, P, P, P, P, P, P, P, P, P, sz, P]
@@ -184,6 +188,26 @@ def verify_greedy_top2(target, R: int, k: int, branches: int, draft, out: dict |
     _check(lib.sv_verify_greedy_top2(rows_of(target), R, k, branches, _ptr(draft), _ptr(out["accept_len"]),
                                      _ptr(out["tokens"]), _ptr(out.get("branch")), _ptr(out.get("status")),
                                      _ptr(out["top2"]), _ptr(ws), _nbytes(ws), _stream(stream)))
+    return out
+
+
+def infer_modality(logits, part_start, out: dict | None = None, workspace=None, stream=None) -> dict:
+    """Per row of full-vocabulary logits [N, V]: amax, the partition holding it (part, -1 for
+    none) and its id range (mask_lo, mask_hi), with status bits.  part_start: host ints,
+    ascending, P + 1 of them."""
+    import numpy as np
+    import torch
+
+    lib = load()
+    dev = logits.device
+    N = logits.shape[0]
+    ps = np.ascontiguousarray(np.asarray(part_start, dtype=np.int32))
+    if out is None:
+        out = {key: _empty(N, torch.int32, dev) for key in ("amax", "part", "mask_lo", "mask_hi", "status")}
+    ws = _workspace(lib.sv_infer_modality_workspace(N, logits.shape[1]), dev, workspace)
+    _check(lib.sv_infer_modality(rows_of(logits), N, ps.ctypes.data, ps.size - 1, _ptr(out.get("amax")),
+                                 _ptr(out["part"]), _ptr(out.get("mask_lo")), _ptr(out.get("mask_hi")),
+                                 _ptr(out.get("status")), _ptr(ws), _nbytes(ws), _stream(stream)))
     return out
 
 

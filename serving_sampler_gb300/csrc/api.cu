@@ -141,6 +141,37 @@ int sv_verify_greedy_top2(sv_rows target, int32_t R, int32_t k, int32_t branches
                                          status, workspace, stream, top2));
 }
 
+size_t sv_infer_modality_workspace(int32_t N, int32_t V)
+{
+    if (N < 0 || V < 1) return 0;
+    return modality_workspace_bytes(N, V);
+}
+
+int sv_infer_modality(sv_rows logits, int32_t N, const int32_t* part_start, int32_t P, int32_t* amax,
+                      int32_t* part, int32_t* mask_lo, int32_t* mask_hi, int32_t* status, void* workspace,
+                      size_t workspace_bytes, sv_stream_t stream)
+{
+    if (N < 0 || P < 1 || part_start == nullptr) return SV_ERR_INVALID_ARG;
+    if (P > kMaxParts) return SV_ERR_LIMIT;
+    for (int32_t p = 0; p < P; ++p)
+        if (part_start[p] > part_start[p + 1]) return SV_ERR_INVALID_ARG;
+    if (N == 0) return SV_OK;
+    if (part == nullptr) return SV_ERR_INVALID_ARG;
+    if (!aligned(amax, 4) || !aligned(part, 4) || !aligned(mask_lo, 4) || !aligned(mask_hi, 4) ||
+        !aligned(status, 4))
+        return SV_ERR_ALIGN;
+    Rows t{};
+    if (int rc = check_rows(logits, N, logits.width, &t)) return rc;
+    const SegPlan plan = plan_segments(N, t.width, t.esize);
+    if (static_cast<int64_t>(N) * plan.nseg > INT32_MAX) return SV_ERR_LIMIT;
+    if (int rc = check_workspace(workspace, workspace_bytes, modality_workspace_bytes(N, t.width))) return rc;
+    if (!have_device()) return SV_ERR_DEVICE;
+    PartTable pt{};
+    pt.P = P;
+    for (int32_t p = 0; p <= P; ++p) pt.start[p] = part_start[p];
+    return launched(launch_infer_modality(t, N, pt, amax, part, mask_lo, mask_hi, status, workspace, stream));
+}
+
 size_t sv_verify_sample_workspace(int32_t R, int32_t k, int32_t V, int32_t Vd)
 {
     if (R < 0 || k < 0 || V < 1 || Vd < 1) return 0;

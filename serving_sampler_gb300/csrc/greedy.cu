@@ -527,6 +527,45 @@ __global__ void __launch_bounds__(kFinThreads)
     }
 }
 
+// One thread per row: the row's argmax from its segment results, then the
+// partition holding it (the text part or an audio codebook) and that
+// partition's id range, the phase mask of the next step.
+__global__ void __launch_bounds__(kFinThreads)
+    modality_finalize_kernel(const ArgPartial* __restrict__ part, int32_t nseg, int64_t rows, PartTable pt,
+                             int32_t* __restrict__ amax, int32_t* __restrict__ part_out,
+                             int32_t* __restrict__ mask_lo, int32_t* __restrict__ mask_hi,
+                             int32_t* __restrict__ status)
+{
+    pdl_wait_primary();
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * kFinThreads + threadIdx.x;
+    if (row >= rows) return;
+    const ArgPartial* p = part + row * nseg;
+    ArgMax best{-INFINITY, INT32_MAX};
+    uint32_t fl = 0;
+    for (int32_t s = 0; s < nseg; ++s) {
+        const ArgPartial q = p[s];
+        fl |= q.flags;
+        if (argmax_better(q.v, q.i, best)) best = ArgMax{q.v, q.i};
+    }
+    const int32_t a = best.i == INT32_MAX ? 0 : best.i;
+    int32_t pi = -1;
+    for (int32_t q = 0; q < pt.P; ++q)  // ascending starts: the first range holding a
+        if (pt.start[q] <= a && a < pt.start[q + 1]) {
+            pi = q;
+            break;
+        }
+    if (amax) amax[row] = a;
+    part_out[row] = pi;
+    if (mask_lo) mask_lo[row] = pi < 0 ? 0 : pt.start[pi];
+    if (mask_hi) mask_hi[row] = pi < 0 ? 0 : pt.start[pi + 1];
+    if (status) {
+        uint32_t st = 0;
+        if ((fl & kFlagNaN) || isinf(best.v)) st |= SV_ST_BAD_LOGITS;
+        if (fl & kFlagTimeout) st |= SV_ST_TIMEOUT;
+        status[row] = static_cast<int32_t>(st);
+    }
+}
+
 size_t greedy_workspace_bytes(int64_t R, int32_t k, int32_t branches, int32_t V, bool top2)
 {
     const int64_t rows = R * (branches == 2 ? 2 * (int64_t)k + 1 : (int64_t)k + 1);
@@ -580,6 +619,34 @@ cudaError_t launch_verify_greedy(const Rows& target, int32_t R, int32_t k, int32
                                   R, k, branches, target.width, draft, accept_len, tokens, branch, status, top2);
     return cudaLaunchKernelEx(&cfg, greedy_finalize_kernel<false>, static_cast<const void*>(part), plan.nseg, R,
                               k, branches, target.width, draft, accept_len, tokens, branch, status, top2);
+}
+
+size_t modality_workspace_bytes(int64_t rows, int32_t V)
+{
+    int64_t nseg = 1;
+    for (int es : {2, 4}) nseg = std::max<int64_t>(nseg, plan_segments(rows, V, es).nseg);
+    return static_cast<size_t>(rows * nseg) * sizeof(ArgPartial) + 256;
+}
+
+cudaError_t launch_infer_modality(const Rows& rows, int64_t nrows, const PartTable& pt, int32_t* amax,
+                                  int32_t* part, int32_t* mask_lo, int32_t* mask_hi, int32_t* status,
+                                  void* workspace, cudaStream_t stream)
+{
+    const SegPlan plan = plan_segments(nrows, rows.width, rows.esize);
+    cudaError_t e = rows.dtype == SV_BF16 ? launch_argmax<SV_BF16, false>(rows, nrows, plan, workspace, stream)
+                                          : launch_argmax<SV_F32, false>(rows, nrows, plan, workspace, stream);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((nrows + kFinThreads - 1) / kFinThreads));
+    cfg.blockDim = dim3(kFinThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, modality_finalize_kernel, static_cast<const ArgPartial*>(workspace), plan.nseg,
+                              nrows, pt, amax, part, mask_lo, mask_hi, status);
 }
 
 }  // namespace sv

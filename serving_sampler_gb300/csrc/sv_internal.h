@@ -46,6 +46,17 @@ struct Top2Partial {
 };
 
 size_t greedy_workspace_bytes(int64_t R, int32_t k, int32_t branches, int32_t V, bool top2 = false);
+// vocabulary partitions: [start[p], start[p + 1]) for p < P
+constexpr int kMaxParts = SV_MAX_PARTS;
+struct PartTable {
+    int32_t P;
+    int32_t start[kMaxParts + 1];
+};
+size_t modality_workspace_bytes(int64_t rows, int32_t V);
+cudaError_t launch_infer_modality(const Rows& rows, int64_t nrows, const PartTable& pt, int32_t* amax,
+                                  int32_t* part, int32_t* mask_lo, int32_t* mask_hi, int32_t* status,
+                                  void* workspace, cudaStream_t stream);
+
 // top2 != NULL: also the argmax and runner-up id of every row ([rows, 2])
 cudaError_t launch_verify_greedy(const Rows& target, int32_t R, int32_t k, int32_t branches,
                                  const int32_t* draft, int32_t* accept_len, int32_t* tokens,

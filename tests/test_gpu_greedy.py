@@ -193,3 +193,40 @@ def test_top2_listen_runner_up(sv):
     main = w["draft"][:, 0, 0] == first0
     assert main.sum() > w["R"] // 2
     assert torch.equal(second0[main], w["draft"][main, 1, 0])
+
+
+# --------------------------------------------------------------------------
+# modality of a row: the vocabulary partition of its unmasked argmax
+# --------------------------------------------------------------------------
+def _va_partitions(V=151936, S=9, W=4096):
+    text = V - S * W
+    return [0, text] + [text + W * (s + 1) for s in range(S)]
+
+
+@pytest.mark.parametrize("dtype,N,V,starts", [
+    (torch.bfloat16, 300, 151936, _va_partitions()),       # the text part, then 9 codebooks of 4096
+    (torch.float32, 70, 151936, _va_partitions()),
+    (torch.bfloat16, 40, 5003, [0, 1000, 1000, 2500, 4096]),  # an empty partition, ids past the last
+    (torch.float32, 9, 17, [3, 9]),                        # ids before the first partition
+])
+def test_infer_modality_matches_oracle(sv, dtype, N, V, starts):
+    g = torch.Generator(device="cuda").manual_seed(N + V)
+    z = torch.randn(N, V, generator=g, device="cuda") * 3.0
+    # plant the maximum in a random partition (or none) for most rows
+    pick = torch.randint(0, V, (N,), generator=g, device="cuda")
+    z[torch.arange(N, device="cuda"), pick] = 40.0
+    z = z.to(dtype)
+    z[0, :] = float("nan")                                 # argmax 0, flagged
+    if V > 2000:
+        b = starts[1]
+        z[1, b - 1] = z[1, b] = 60.0                       # a tie across a partition boundary
+        z[2, 7] = float("inf")                             # +inf maximum, flagged
+    got = sv.infer_modality(z, starts)
+    torch.cuda.synchronize()
+    want = oracle.infer_modality(workloads.host_rows(z), np.array(starts, np.int32))
+    for key in ("amax", "part", "mask_lo", "mask_hi"):
+        np.testing.assert_array_equal(got[key].cpu().numpy(), want[key], err_msg=key)
+    st = got["status"].cpu().numpy()
+    assert st[0] & oracle.ST_BAD_LOGITS
+    if V > 2000:
+        assert st[2] & oracle.ST_BAD_LOGITS and not (st[3:] & oracle.ST_BAD_LOGITS).any()
