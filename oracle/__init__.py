@@ -150,7 +150,7 @@ def accept_scan(accept, draft, fix):
 
 def verify_greedy(target, R: int, k: int, branches: int, draft):
     t, code, stride, V = _rows(target, "target")
-    rows_per_req = k + 1 if branches == 1 else 2 * k + 1
+    rows_per_req = 1 + branches * k
     if t.shape[0] < R * rows_per_req:
         raise ValueError("target has too few rows")
     draft = _i32(draft).reshape(R, branches, k) if k else np.zeros((R, branches, 0), np.int32)

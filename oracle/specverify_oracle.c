@@ -344,8 +344,10 @@ int or_accept_scan(const uint8_t* accept, const int32_t* draft, const int32_t* f
 
 /* ------------------------------------------------------------------ */
 /* greedy verification ([P1] step 4, with the step-2 runner-up branch)  */
-/* target rows per request: branches == 1: k + 1 rows p_1..p_{k+1};    */
-/* branches == 2: 2k + 1 rows [p_1 | main p_2..p_{k+1} | runner p_2..]  */
+/* target rows per request: 1 + branches * k: p_1 shared, then each    */
+/* branch's p_2..p_{k+1} ([p_1 | main | runner | ...]; branches == 1:   */
+/* k + 1 rows).  More than two branches are tree drafts whose first    */
+/* tokens differ.                                                      */
 /* ------------------------------------------------------------------ */
 static int64_t branch_row(int32_t b, int32_t j, int32_t k)
 {
@@ -356,8 +358,8 @@ int or_verify_greedy(const void* target, int dtype, int64_t row_stride, int32_t 
                      int32_t k, int32_t branches, const int32_t* draft, int32_t* accept_len,
                      int32_t* tokens, int32_t* branch_out, int32_t* status)
 {
-    if (branches < 1 || branches > 2 || k < 0 || (branches == 2 && k < 1)) return -1;
-    const int32_t rows_per_req = branches == 1 ? k + 1 : 2 * k + 1;
+    if (branches < 1 || branches > 8 || k < 0 || (branches >= 2 && k < 1)) return -1;
+    const int32_t rows_per_req = 1 + branches * k;
     double* z = (double*)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
     int32_t* amax = (int32_t*)malloc(sizeof(int32_t) * (size_t)rows_per_req);
     for (int32_t r = 0; r < R; ++r) {

@@ -382,7 +382,7 @@ def _ar_greedy(ctx, L, V):
     return out
 
 
-@pytest.mark.parametrize("branches", [1, 2])
+@pytest.mark.parametrize("branches", [1, 2, 4])
 def test_greedy_verification_equals_autoregressive(branches):
     V, k, L = 50, 6, 120
     rng = np.random.default_rng(branches)
@@ -401,10 +401,11 @@ def test_greedy_verification_equals_autoregressive(branches):
             main.append(t)
         rows = [_toy_logits(base + tuple(main[:j]), V) for j in range(k + 1)]
         drafts = [main]
-        if branches == 2:
-            row0 = rows[0].astype(np.float64)
-            order = np.argsort(-row0, kind="stable")
-            first = int(order[0]) if int(order[0]) != main[0] else int(order[1])
+        # further branches (a tree of first tokens): the best ids of row 0 other than the main
+        # draft's first token, each continued greedily
+        row0 = rows[0].astype(np.float64)
+        firsts = [int(t) for t in np.argsort(-row0, kind="stable") if int(t) != main[0]][:branches - 1]
+        for first in firsts:
             runner = [first]
             for _ in range(k - 1):
                 runner.append(int(np.argmax(_toy_logits(base + tuple(runner), V))))
@@ -447,6 +448,31 @@ def test_greedy_branch_selection_rules():
     res = oracle.verify_greedy(rows, 1, k, 2, np.array([[1, 3, 4], [0, 6, 7]], np.int32))
     assert res["branch"][0] == 0 and res["accept_len"][0] == 0
     assert res["tokens"][0].tolist() == [2, -1, -1, -1]
+
+
+def test_tree_branch_selection_rules():
+    """Four branches sharing row 0: the viable branch with the longest accepted prefix wins,
+    ties go to the lowest branch; rows are [p1 | b0 p2..p4 | b1 .. | b2 .. | b3 ..]."""
+    V, k, B = 10, 3, 4
+    ams = [2, 3, 4, 5, 6, 7, 1, 8, 9, 0, 3, 4, 5]  # argmax of row 0, then three rows per branch
+    rows = np.zeros((1 + B * k, V), np.float32)
+    for i, a in enumerate(ams):
+        rows[i, a] = 5.0
+    # accepted prefixes 2, 3, 3 and a branch that is not viable: branch 1 (the first of the longest)
+    drafts = np.array([[2, 3, 0], [2, 6, 7], [2, 8, 9], [1, 3, 4]], np.int32)
+    res = oracle.verify_greedy(rows, 1, k, B, drafts)
+    assert res["accept_len"][0] == 3 and res["branch"][0] == 1
+    assert res["tokens"][0].tolist() == [2, 6, 7, 1]
+    # accepted prefixes 2, 1, 1, 1: branch 0, its correction from its own row
+    drafts = np.array([[2, 3, 0], [2, 5, 6], [2, 1, 8], [2, 0, 3]], np.int32)
+    res = oracle.verify_greedy(rows, 1, k, B, drafts)
+    assert res["accept_len"][0] == 2 and res["branch"][0] == 0
+    assert res["tokens"][0].tolist() == [2, 3, 4, -1]
+    # only the last branch is viable
+    drafts = np.array([[1, 3, 4], [0, 6, 7], [9, 8, 9], [2, 3, 4]], np.int32)
+    res = oracle.verify_greedy(rows, 1, k, B, drafts)
+    assert res["accept_len"][0] == 3 and res["branch"][0] == 3
+    assert res["tokens"][0].tolist() == [2, 3, 4, 5]
 
 
 def test_greedy_ties_nan_inf_and_ranges():
