@@ -82,6 +82,7 @@ enum {
 #define SV_MAX_K 256       /* drafts per request (per branch) */
 #define SV_MAX_S 16        /* codebooks per CFG frame */
 #define SV_MAX_PARTS 64    /* vocabulary partitions of sv_infer_modality */
+#define SV_MAX_BRANCHES 8  /* draft branches sharing the first row (sv_verify_greedy) */
 #define SV_MAX_WIDTH (1 << 30)
 
 /* A matrix of logit rows: row i, entry x is at data + (i * row_stride + x)
@@ -100,18 +101,20 @@ typedef struct sv_rows {
 const char* sv_status_string(int code);
 
 /* ------------------------------------------------------------------------
- * sv_verify_greedy -- greedy verification with an optional runner-up branch.
- * Source: "Decode Before You Hear ..." method steps 2 and 4.
+ * sv_verify_greedy -- greedy verification with optional further branches.
+ * Source: "Decode Before You Hear ..." method steps 2 and 4 (a runner-up
+ * branch beside the main draft); more branches are tree drafts whose first
+ * tokens differ.
  *
- *   target      rows of raw target logits, width V.  branches == 1: k + 1 rows
- *               per request (positions 1..k and the row after the last
- *               draft); branches == 2: 2k + 1 rows per request laid out as
- *               [p_1 | main p_2..p_{k+1} | runner p_2..p_{k+1}] (row p_1 is
- *               shared by both branches).  Request r's rows start at row
- *               r * rows_per_request.
+ *   target      rows of raw target logits, width V: 1 + branches * k rows per
+ *               request laid out as [p_1 | branch 0 p_2..p_{k+1} | branch 1
+ *               p_2..p_{k+1} | ...] (row p_1 is shared by every branch; with
+ *               one branch, the k + 1 rows of positions 1..k and the row after
+ *               the last draft; with two, [p_1 | main | runner]).  Request r's
+ *               rows start at row r * rows_per_request.
  *   R           requests (>= 0; 0 is a no-op).
- *   k           drafts per branch, 0 <= k <= SV_MAX_K (k >= 1 with 2 branches).
- *   branches    1 or 2.
+ *   k           drafts per branch, 0 <= k <= SV_MAX_K (k >= 1 with 2+ branches).
+ *   branches    1 <= branches <= SV_MAX_BRANCHES.
  *   draft       int32 [R, branches, k] target ids.
  *   accept_len  int32 [R] out: accepted drafts n in [0, k].
  *   tokens      int32 [R, k + 1] out: the n accepted drafts then the
@@ -120,7 +123,8 @@ const char* sv_status_string(int code);
  *   status      int32 [R] out or NULL: SV_ST_* bits.
  * argmax is over raw logits (temperature cannot change it).  A branch is
  * viable when its first draft equals argmax p_1; among viable branches the
- * longer accepted prefix wins, ties to branch 0; with none viable n = 0.
+ * longer accepted prefix wins, ties to the lower branch; with none viable
+ * n = 0 and branch 0.
  * ---------------------------------------------------------------------- */
 size_t sv_verify_greedy_workspace(int32_t R, int32_t k, int32_t branches, int32_t V);
 int sv_verify_greedy(sv_rows target, int32_t R, int32_t k, int32_t branches,

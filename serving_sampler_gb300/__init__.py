@@ -179,7 +179,7 @@ def verify_greedy_top2(target, R: int, k: int, branches: int, draft, out: dict |
 
     lib = load()
     dev = target.device
-    rows = target.shape[0] if R == 0 else R * (k + 1 if branches == 1 else 2 * k + 1)
+    rows = target.shape[0] if R == 0 else R * (1 + branches * k)
     if out is None:
         out = dict(accept_len=_empty(R, torch.int32, dev), tokens=_empty((R, k + 1), torch.int32, dev),
                    branch=_empty(R, torch.int32, dev), status=_empty(R, torch.int32, dev),

@@ -77,7 +77,7 @@ const char* sv_status_string(int code)
 
 size_t sv_verify_greedy_workspace(int32_t R, int32_t k, int32_t branches, int32_t V)
 {
-    if (R < 0 || k < 0 || V < 1 || (branches != 1 && branches != 2)) return 0;
+    if (R < 0 || k < 0 || V < 1 || branches < 1 || branches > SV_MAX_BRANCHES) return 0;
     return greedy_workspace_bytes(R, k, branches, V);
 }
 
@@ -86,8 +86,8 @@ int sv_verify_greedy(sv_rows target, int32_t R, int32_t k, int32_t branches, con
                      void* workspace, size_t workspace_bytes, sv_stream_t stream)
 {
     if (R < 0 || k < 0) return SV_ERR_INVALID_ARG;
-    if (branches != 1 && branches != 2) return SV_ERR_INVALID_ARG;
-    if (branches == 2 && k < 1) return SV_ERR_INVALID_ARG;
+    if (branches < 1 || (branches >= 2 && k < 1)) return SV_ERR_INVALID_ARG;
+    if (branches > SV_MAX_BRANCHES) return SV_ERR_LIMIT;
     if (k > SV_MAX_K) return SV_ERR_LIMIT;
     if (R == 0) return SV_OK;
     if ((k > 0 && draft == nullptr) || accept_len == nullptr || tokens == nullptr)
@@ -95,7 +95,7 @@ int sv_verify_greedy(sv_rows target, int32_t R, int32_t k, int32_t branches, con
     if (!aligned(draft, 4) || !aligned(accept_len, 4) || !aligned(tokens, 4) ||
         !aligned(branch, 4) || !aligned(status, 4))
         return SV_ERR_ALIGN;
-    const int64_t rows = static_cast<int64_t>(R) * (branches == 2 ? 2 * k + 1 : k + 1);
+    const int64_t rows = static_cast<int64_t>(R) * (1 + static_cast<int64_t>(branches) * k);
     Rows t{};
     if (int rc = check_rows(target, rows, target.width, &t)) return rc;
     const SegPlan plan = plan_segments(rows, t.width, t.esize);
@@ -110,7 +110,7 @@ int sv_verify_greedy(sv_rows target, int32_t R, int32_t k, int32_t branches, con
 
 size_t sv_verify_greedy_top2_workspace(int32_t R, int32_t k, int32_t branches, int32_t V)
 {
-    if (R < 0 || k < 0 || V < 1 || (branches != 1 && branches != 2)) return 0;
+    if (R < 0 || k < 0 || V < 1 || branches < 1 || branches > SV_MAX_BRANCHES) return 0;
     return greedy_workspace_bytes(R, k, branches, V, true);
 }
 
@@ -119,8 +119,8 @@ int sv_verify_greedy_top2(sv_rows target, int32_t R, int32_t k, int32_t branches
                           int32_t* top2, void* workspace, size_t workspace_bytes, sv_stream_t stream)
 {
     if (R < 0 || k < 0) return SV_ERR_INVALID_ARG;
-    if (branches != 1 && branches != 2) return SV_ERR_INVALID_ARG;
-    if (branches == 2 && k < 1) return SV_ERR_INVALID_ARG;
+    if (branches < 1 || (branches >= 2 && k < 1)) return SV_ERR_INVALID_ARG;
+    if (branches > SV_MAX_BRANCHES) return SV_ERR_LIMIT;
     if (k > SV_MAX_K) return SV_ERR_LIMIT;
     if (R == 0) return SV_OK;
     if ((k > 0 && draft == nullptr) || accept_len == nullptr || tokens == nullptr || top2 == nullptr)
@@ -128,7 +128,7 @@ int sv_verify_greedy_top2(sv_rows target, int32_t R, int32_t k, int32_t branches
     if (!aligned(draft, 4) || !aligned(accept_len, 4) || !aligned(tokens, 4) ||
         !aligned(branch, 4) || !aligned(status, 4) || !aligned(top2, 4))
         return SV_ERR_ALIGN;
-    const int64_t rows = static_cast<int64_t>(R) * (branches == 2 ? 2 * k + 1 : k + 1);
+    const int64_t rows = static_cast<int64_t>(R) * (1 + static_cast<int64_t>(branches) * k);
     Rows t{};
     if (int rc = check_rows(target, rows, target.width, &t)) return rc;
     const SegPlan plan = plan_segments(rows, t.width, t.esize);

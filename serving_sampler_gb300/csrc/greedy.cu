@@ -451,7 +451,7 @@ __global__ void __launch_bounds__(kFinThreads)
     extern __shared__ int32_t fin_amax[];
     __shared__ uint32_t st_shared;
     const int64_t r = blockIdx.x;
-    const int32_t rpr = branches == 1 ? k + 1 : 2 * k + 1;
+    const int32_t rpr = 1 + branches * k;
     if (threadIdx.x == 0) st_shared = 0;
     __syncthreads();
     uint32_t st = 0;
@@ -568,7 +568,7 @@ __global__ void __launch_bounds__(kFinThreads)
 
 size_t greedy_workspace_bytes(int64_t R, int32_t k, int32_t branches, int32_t V, bool top2)
 {
-    const int64_t rows = R * (branches == 2 ? 2 * (int64_t)k + 1 : (int64_t)k + 1);
+    const int64_t rows = R * (1 + static_cast<int64_t>(branches) * k);
     int64_t nseg = 1;
     for (int es : {2, 4}) nseg = std::max<int64_t>(nseg, plan_segments(rows, V, es).nseg);
     return static_cast<size_t>(rows * nseg) * (top2 ? sizeof(Top2Partial) : sizeof(ArgPartial)) + 256;
@@ -593,7 +593,7 @@ cudaError_t launch_verify_greedy(const Rows& target, int32_t R, int32_t k, int32
                                  int32_t* branch, int32_t* status, void* workspace,
                                  cudaStream_t stream, int32_t* top2)
 {
-    const int64_t rows = static_cast<int64_t>(R) * (branches == 2 ? 2 * k + 1 : k + 1);
+    const int64_t rows = static_cast<int64_t>(R) * (1 + static_cast<int64_t>(branches) * k);
     const SegPlan plan = plan_segments(rows, target.width, target.esize);
     void* part = workspace;
     const bool bf = target.dtype == SV_BF16;
@@ -603,7 +603,7 @@ cudaError_t launch_verify_greedy(const Rows& target, int32_t R, int32_t k, int32
                                : launch_argmax<SV_F32, false>(target, rows, plan, part, stream));
     if (e != cudaSuccess) return e;
 
-    const int32_t rpr = branches == 2 ? 2 * k + 1 : k + 1;
+    const int32_t rpr = 1 + branches * k;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(R));
     cfg.blockDim = dim3(kFinThreads);

@@ -53,7 +53,7 @@ extern "C" int sv_verify_greedy_noalloc(sv_rows target, int32_t R, int32_t k, in
                                         const int32_t* draft, int32_t* accept_len, int32_t* tokens,
                                         int32_t* branch, int32_t* status, sv_stream_t stream)
 {
-    if (R < 0 || k < 0 || (branches != 1 && branches != 2) || (branches == 2 && k < 1) ||
+    if (R < 0 || k < 0 || branches < 1 || branches > SV_MAX_BRANCHES || (branches >= 2 && k < 1) ||
         target.width < 1)
         return SV_ERR_INVALID_ARG;
     if (k > SV_MAX_K) return SV_ERR_LIMIT;

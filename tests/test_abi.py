@@ -51,7 +51,9 @@ def test_status_strings(lib):
 def test_workspace_sizes(lib):
     assert lib.sv_verify_greedy_workspace(64, 32, 2, 151936) >= 64 * 65 * 16
     assert lib.sv_verify_greedy_workspace(-1, 2, 1, 10) == 0
-    assert lib.sv_verify_greedy_workspace(1, 2, 3, 10) == 0
+    assert lib.sv_verify_greedy_workspace(1, 2, 9, 10) == 0  # more branches than SV_MAX_BRANCHES
+    assert lib.sv_verify_greedy_workspace(1, 2, 0, 10) == 0
+    assert lib.sv_verify_greedy_workspace(1, 2, 8, 10) > 0  # eight branches: 1 + 8 * 2 rows
     assert lib.sv_verify_sample_workspace(128, 7, 151936, 32000) > 0
     assert lib.sv_cfg_merge_sample_workspace(256, 4, 9, 4096) > 0
     assert lib.sv_cfg_merge_sample_workspace(1, 1, 17, 4096) == 0
@@ -71,7 +73,8 @@ def test_argument_checks_need_no_gpu(lib):
     # R == 0 is a no-op
     assert g(_rows(), 0, 2, 1, buf, buf, buf, None, None, ws, 1 << 20, None) == 0
     assert g(_rows(), -1, 2, 1, buf, buf, buf, None, None, ws, 1 << 20, None) == -1
-    assert g(_rows(), 1, 2, 3, buf, buf, buf, None, None, ws, 1 << 20, None) == -1
+    assert g(_rows(), 1, 2, 0, buf, buf, buf, None, None, ws, 1 << 20, None) == -1
+    assert g(_rows(), 1, 2, 9, buf, buf, buf, None, None, ws, 1 << 20, None) == -4  # SV_ERR_LIMIT
     assert g(_rows(), 1, 0, 2, buf, buf, buf, None, None, ws, 1 << 20, None) == -1
     assert g(_rows(), 1, 257, 1, buf, buf, buf, None, None, ws, 1 << 20, None) == -4
     assert g(_rows(dtype=7), 1, 2, 1, buf, buf, buf, None, None, ws, 1 << 20, None) == -2

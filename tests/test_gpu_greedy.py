@@ -48,6 +48,19 @@ def test_random_shapes(sv, R, k, branches, V, dtype, row_pad):
     _check(sv, w["target"], R, k, branches, w["draft"])
 
 
+@pytest.mark.parametrize("R,k,branches,V,dtype", [
+    (9, 5, 4, 4096, torch.bfloat16),
+    (6, 3, 8, 151936, torch.bfloat16),
+    (5, 7, 3, 3001, torch.float32),     # plain-load path
+])
+def test_tree_drafts(sv, R, k, branches, V, dtype):
+    """More than two branches sharing the first row (tree drafts), also with the top-2 output."""
+    w = workloads.greedy_batch(R, k, V, dtype, branches=branches, p_full=0.5, p_first=0.5, seed=R * 31 + branches)
+    got, want = _check(sv, w["target"], R, k, branches, w["draft"])
+    assert len(set(want["branch"].tolist())) > 1  # the winning branch varies
+    _check_top2(sv, w["target"], R, k, branches, w["draft"])
+
+
 def test_ties_go_to_lowest_index(sv):
     g = torch.Generator(device="cuda").manual_seed(5)
     R, k, V = 6, 5, 3000

@@ -86,7 +86,7 @@ def greedy_batch(R: int, k: int, V: int, dtype=torch.bfloat16, sigma: float = 3.
     planted [R, rows_per_request] argmax ids).
     """
     g = _gen(seed, device)
-    rpr = k + 1 if branches == 1 else 2 * k + 1
+    rpr = 1 + branches * k
     rows = R * rpr
     z = torch.randn(rows, V + row_pad, generator=g, device=device, dtype=torch.float32) * sigma
     top = torch.randint(0, V, (rows,), generator=g, device=device)
@@ -118,6 +118,18 @@ def greedy_batch(R: int, k: int, V: int, dtype=torch.bfloat16, sigma: float = 3.
         runner[:, 0] = torch.where(main[:, 0] == top[:, 0], second, top[:, 0])
         runner[:, 1:] = top[:, k + 1:2 * k]
         drafts.append(runner)
+    for b in range(1, branches) if branches > 2 else ():
+        # tree drafts: branch b starts with the argmax of row 0 (viable) or another id, then
+        # follows its own rows' argmaxes with one corrupted position w.p. 1/2
+        br = top[:, b * k:b * k + k].clone()
+        br[:, 0] = torch.where(torch.rand(R, generator=g, device=device) < 0.5, top[:, 0],
+                               _rand_other(g, top[:, 0], V))
+        if k > 1:
+            pos = torch.randint(1, k, (R,), generator=g, device=device)
+            bad = torch.rand(R, generator=g, device=device) < 0.5
+            wrong = _rand_other(g, br.gather(1, pos.view(-1, 1)).view(-1), V)
+            br[bad, pos[bad]] = wrong[bad]
+        drafts.append(br)
     draft = torch.stack(drafts, dim=1).to(torch.int32).contiguous()
     return dict(target=target, draft=draft, R=R, k=k, branches=branches, V=V, planted=top)
 
