@@ -68,6 +68,10 @@ def _load():
             lib.or_top2_rows.restype = C.c_int
             lib.or_infer_modality.argtypes = [P, C.c_int, i64, i64, i32, P, i32, P, P, P, P]
             lib.or_infer_modality.restype = C.c_int
+            lib.or_pool_append.argtypes = [P, P, i32, P, i32, i32, P]
+            lib.or_pool_append.restype = C.c_int
+            lib.or_pool_lookup.argtypes = [P, P, i32, P, i32, i32, i32, P, P]
+            lib.or_pool_lookup.restype = C.c_int
             lib.or_verify_sample.argtypes = [P, C.c_int, i64, i32, P, C.c_int, i64, i32, P, i32, i32,
                                              P, P, P, P, P, P, P, P, P, P, P]
             lib.or_verify_sample.restype = C.c_int
@@ -188,6 +192,39 @@ def infer_modality(rows, part_start):
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments ({rc})")
     return out
+
+
+def pool_append(pool, pool_len, drafts):
+    """Insert drafts int32 [R, k] (a negative id ends a draft early) into the pools
+    int32 [R, Lp] with used lengths pool_len int32 [R].  Returns the new pool,
+    pool_len and status (128 where a draft did not fit)."""
+    pool = _i32(pool).copy()
+    pool_len = _i32(pool_len).copy()
+    drafts = _i32(drafts)
+    R, Lp = pool.shape
+    status = np.zeros(R, np.int32)
+    rc = _load().or_pool_append(_ptr(pool), _ptr(pool_len), Lp, _ptr(drafts), drafts.shape[1], R, _ptr(status))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments ({rc})")
+    return dict(pool=pool, pool_len=pool_len, status=status)
+
+
+def pool_lookup(pool, pool_len, suffix, gamma: int):
+    """pool int32 [R, Lp] with used lengths pool_len int32 [R]; suffix int32 [R, N]
+    (the last N emitted tokens, -1 where shorter).  Returns match_len [R] and
+    cont [R, gamma]."""
+    pool = _i32(pool)
+    pool_len = _i32(pool_len)
+    suffix = _i32(suffix)
+    R, Lp = pool.shape
+    N = suffix.shape[1]
+    match_len = np.zeros(R, np.int32)
+    cont = np.zeros((R, gamma), np.int32)
+    rc = _load().or_pool_lookup(_ptr(pool), _ptr(pool_len), Lp, _ptr(suffix), N, R, gamma, _ptr(match_len),
+                                _ptr(cont))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments ({rc})")
+    return dict(match_len=match_len, cont=cont)
 
 
 def verify_sample(target, draft_logits, d2t, R: int, k: int, draft, seeds, temperature):

@@ -324,6 +324,80 @@ int32_t or_race2(const double* w, int32_t n, int32_t chunk, uint64_t seed, uint3
 }
 
 /* ------------------------------------------------------------------ */
+/* hypothesis pool ([SL] "method steps" 3 and 5: every draft of the      */
+/* session goes into a pool indexed by n-grams; while the output         */
+/* continues, the longest n-gram of the pool matching the emitted suffix */
+/* supplies its continuation as the next drafts).                        */
+/* A request's pool is int32 [Lp]: its drafts in insertion order, each   */
+/* followed by -1; pool_len[r] entries are in use.                       */
+/* ------------------------------------------------------------------ */
+
+/* append: draft r is drafts[r, 0 .. L) with L the first index holding a */
+/* negative id (k if none).  L == 0 inserts nothing.  When pool_len + L  */
+/* + 1 exceeds Lp (or pool_len is outside [0, Lp]) nothing is inserted   */
+/* and status bit 128 is set.                                            */
+int or_pool_append(int32_t* pool, int32_t* pool_len, int32_t Lp, const int32_t* drafts, int32_t k,
+                   int32_t R, int32_t* status)
+{
+    if (Lp < 0 || k < 0 || R < 0) return -1;
+    for (int32_t r = 0; r < R; ++r) {
+        const int32_t* D = drafts + (int64_t)r * k;
+        int32_t L = 0;
+        while (L < k && D[L] >= 0) ++L;
+        status[r] = 0;
+        if (L == 0) continue;
+        const int32_t used = pool_len[r];
+        if (used < 0 || used > Lp || (int64_t)used + L + 1 > Lp) {
+            status[r] = 128;
+            continue;
+        }
+        int32_t* P = pool + (int64_t)r * Lp;
+        for (int32_t i = 0; i < L; ++i) P[used + i] = D[i];
+        P[used + L] = -1;
+        pool_len[r] = used + L + 1;
+    }
+    return 0;
+}
+
+/* lookup: suffix [R, N] holds the last N emitted tokens, -1 where the   */
+/* output is shorter (left side).  A match of length n >= 1 ends at pool */
+/* position p when pool[p - n + 1 .. p] equals the last n suffix tokens  */
+/* (all >= 0, so inside one draft) and pool[p + 1] >= 0 (a continuation */
+/* exists), with p + 1 < len, len = pool_len[r] clamped to [0, Lp].  The */
+/* longest match wins, the latest p among equal lengths; the             */
+/* continuation is pool[p + 1 ..] up to gamma tokens or the draft's end, */
+/* -1 padded.  match_len 0: no continuation.                             */
+int or_pool_lookup(const int32_t* pool, const int32_t* pool_len, int32_t Lp, const int32_t* suffix,
+                   int32_t N, int32_t R, int32_t gamma, int32_t* match_len, int32_t* cont)
+{
+    if (Lp < 0 || N < 0 || R < 0 || gamma < 0) return -1;
+    for (int32_t r = 0; r < R; ++r) {
+        const int32_t* P = pool + (int64_t)r * Lp;
+        const int32_t* S = suffix + (int64_t)r * N;
+        int32_t len = pool_len[r];
+        if (len < 0) len = 0;
+        if (len > Lp) len = Lp;
+        int32_t best_n = 0, best_p = -1;
+        for (int32_t p = 0; p + 1 < len; ++p) {
+            if (P[p + 1] < 0) continue;  /* no continuation after p */
+            int32_t n = 0;
+            while (n < N && p - n >= 0 && P[p - n] >= 0 && S[N - 1 - n] >= 0 && P[p - n] == S[N - 1 - n]) ++n;
+            if (n > 0 && n >= best_n) {  /* ascending p: the latest among equal lengths */
+                best_n = n;
+                best_p = p;
+            }
+        }
+        match_len[r] = best_n;
+        int32_t* out = cont + (int64_t)r * gamma;
+        int32_t i = 0;
+        if (best_p >= 0)
+            for (; i < gamma && best_p + 1 + i < len && P[best_p + 1 + i] >= 0; ++i) out[i] = P[best_p + 1 + i];
+        for (; i < gamma; ++i) out[i] = -1;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
 /* accept-length scan over caller-given accept flags ([P1] step 4,      */
 /* [P3] section 3: draft i counts only if drafts 0..i-1 were accepted)  */
 /* ------------------------------------------------------------------ */

@@ -694,3 +694,145 @@ def test_cfg_codebook_marginals_are_target():
                                   draft.astype(np.int32), seeds, np.ones(R, np.float32))
     for s in range(S):
         assert _chi2_ok(np.bincount(out["tokens"][:, 0, s], minlength=W), p[s]) > CHI2_ALPHA
+
+
+# --------------------------------------------------------------------------
+# hypothesis pool ("Decode Before You Hear ...", method steps 3 and 5; the
+# tool-call case study of Figure 6 (b))
+# --------------------------------------------------------------------------
+# token ids of the tool-call case study: "ok" (listen), "sure", "<call>", "find",
+# "(", "TYO", ",", "Fri", ")", "</call>"
+OK, SURE, CALL, FIND, LP, TYO, COMMA, FRI, RP, ENDCALL = 20, 21, 10, 11, 12, 13, 14, 15, 16, 17
+CASE_DRAFTS = [
+    [OK],                                             # chunk 1: listen
+    [SURE, CALL, FIND, LP, TYO, COMMA, FRI, RP, ENDCALL],  # chunk 2: the call, drafted under silence
+    [CALL, FIND, LP, TYO],                            # chunk 3: cut off by the window
+    [OK],                                             # chunk 3: runner-up branch
+]
+CASE_POOL = [OK, -1, SURE, CALL, FIND, LP, TYO, COMMA, FRI, RP, ENDCALL, -1, CALL, FIND, LP, TYO, -1, OK, -1]
+
+
+def _append_all(drafts, Lp, width=10):
+    pool = np.full((1, Lp), -7, np.int32)  # contents beyond pool_len never matter
+    plen = np.zeros(1, np.int32)
+    statuses = []
+    for d in drafts:
+        row = np.full((1, width), -1, np.int32)
+        row[0, :len(d)] = d
+        out = oracle.pool_append(pool, plen, row)
+        pool, plen = out["pool"], out["pool_len"]
+        statuses.append(int(out["status"][0]))
+    return pool, plen, statuses
+
+
+def test_pool_append_case_study():
+    pool, plen, st = _append_all(CASE_DRAFTS, len(CASE_POOL))
+    assert plen[0] == len(CASE_POOL) and st == [0, 0, 0, 0]
+    assert pool[0].tolist() == CASE_POOL
+    # one slot short: the last draft does not fit and nothing of it is written
+    pool, plen, st = _append_all(CASE_DRAFTS, len(CASE_POOL) - 1)
+    assert st == [0, 0, 0, 128] and plen[0] == len(CASE_POOL) - 2
+    assert pool[0, :plen[0]].tolist() == CASE_POOL[:-2] and pool[0, -1] == -7
+    # an empty draft inserts nothing; a negative id ends a draft early
+    pool, plen, st = _append_all([[], [5, 6, -1, 7]], 8)
+    assert st == [0, 0] and plen[0] == 3 and pool[0, :3].tolist() == [5, 6, -1]
+
+
+@pytest.mark.parametrize(
+    "suffix, n, cont",
+    [
+        # "sure <call> find (": the whole suffix matches chunk 2's draft, whose rest is the call
+        ([SURE, CALL, FIND, LP], 4, [TYO, COMMA, FRI, RP, ENDCALL]),
+        # a shorter output: "<call> find (" matches both drafts; the later one (chunk 3) wins
+        ([-1, CALL, FIND, LP], 3, [TYO]),
+        # "find ( TYO": chunk 3's occurrence ends its draft, so only chunk 2 continues
+        ([99, FIND, LP, TYO], 3, [COMMA, FRI, RP, ENDCALL]),
+        # a mismatch at the oldest suffix token: only the two newest count
+        ([99, 98, LP, TYO], 2, [COMMA, FRI, RP, ENDCALL]),
+        # "</call>" and "ok" end their drafts: nothing follows them
+        ([FRI, RP, ENDCALL, ENDCALL], 0, []),
+        ([SURE, CALL, FIND, OK], 0, []),
+        ([99, 99, 99, 99], 0, []),
+        ([-1, -1, -1, -1], 0, []),
+    ],
+)
+def test_pool_lookup_case_study(suffix, n, cont):
+    gamma = 8
+    out = oracle.pool_lookup(np.array([CASE_POOL], np.int32), np.array([len(CASE_POOL)], np.int32),
+                             np.array([suffix], np.int32), gamma)
+    assert out["match_len"][0] == n
+    assert out["cont"][0].tolist() == cont + [-1] * (gamma - len(cont))
+    # gamma caps the continuation; gamma 0 still reports the match
+    out = oracle.pool_lookup(np.array([CASE_POOL], np.int32), np.array([len(CASE_POOL)], np.int32),
+                             np.array([suffix], np.int32), 2)
+    assert out["cont"][0].tolist() == (cont + [-1, -1])[:2]
+    out = oracle.pool_lookup(np.array([CASE_POOL], np.int32), np.array([len(CASE_POOL)], np.int32),
+                             np.array([suffix], np.int32), 0)
+    assert out["match_len"][0] == n and out["cont"].shape == (1, 0)
+
+
+def _ngram_index(drafts, N):
+    """An n-gram index built the way the pages describe the pool: every n-gram
+    (1 <= n <= N) of every draft that has a next token maps to (insertion rank,
+    position of that next token); later insertions overwrite earlier ones."""
+    index = {}
+    rank = 0
+    for d in drafts:
+        for end in range(len(d) - 1):  # d[end + 1] exists
+            for n in range(1, min(N, end + 1) + 1):
+                index[tuple(d[end - n + 1:end + 1])] = (rank, d, end + 1)
+            rank += 1
+    return index
+
+
+def test_pool_lookup_equals_an_ngram_index():
+    rng = np.random.default_rng(11)
+    for trial in range(300):
+        vocab = int(rng.integers(2, 6))
+        drafts = [rng.integers(0, vocab, int(rng.integers(0, 9))).tolist() for _ in range(int(rng.integers(0, 7)))]
+        N = int(rng.integers(1, 6))
+        gamma = int(rng.integers(0, 7))
+        Lp = sum(len(d) + 1 for d in drafts if d) + int(rng.integers(0, 3))
+        pool, plen, st = _append_all(drafts, max(Lp, 1), width=9)
+        assert not any(st)
+        out_len = int(rng.integers(0, N + 1))
+        suffix = [-1] * (N - out_len) + rng.integers(0, vocab, out_len).tolist()
+        got = oracle.pool_lookup(pool, plen, np.array([suffix], np.int32), gamma)
+        index = _ngram_index([d for d in drafts if d], N)
+        want_n, want = 0, []
+        for n in range(out_len, 0, -1):
+            hit = index.get(tuple(suffix[N - n:]))
+            if hit is not None:
+                _, d, start = hit
+                want_n, want = n, d[start:start + gamma]
+                break
+        assert got["match_len"][0] == want_n, (trial, drafts, suffix)
+        assert got["cont"][0].tolist() == want + [-1] * (gamma - len(want)), (trial, drafts, suffix)
+
+
+def test_pool_lookup_continues_a_draft_the_output_follows():
+    # Step 5: when the emitted output runs along a stored draft, the lookup hands
+    # back the rest of that draft, so later forwards only pay for uncovered tokens.
+    rng = np.random.default_rng(12)
+    for _ in range(100):
+        # distinct ids in every draft and no id shared between drafts: the match is unique
+        drafts = [(2000 * j + rng.permutation(2000)[:int(rng.integers(2, 40))]).tolist() for j in range(5)]
+        pool, plen, _ = _append_all(drafts, 256, width=40)
+        j = int(rng.integers(0, 5))
+        d = drafts[j]
+        cut = int(rng.integers(1, len(d)))
+        N = 6
+        emitted = [10_001, 10_002] + d[:cut]  # tokens no draft holds, then the draft's prefix
+        got = oracle.pool_lookup(pool, plen, np.array([emitted[-N:]], np.int32), 64)
+        rest = d[cut:]
+        assert got["match_len"][0] == min(cut, N)
+        assert got["cont"][0].tolist() == rest + [-1] * (64 - len(rest))
+
+
+def test_pool_lookup_pool_len_is_clamped():
+    pool = np.array([[5, 6, 7, -1]], np.int32)
+    for plen, n in [(-3, 0), (0, 0), (1, 0), (2, 1), (4, 1), (99, 1)]:
+        got = oracle.pool_lookup(pool, np.array([plen], np.int32), np.array([[5]], np.int32), 4)
+        assert got["match_len"][0] == n
+        want = [6, 7][: max(0, min(plen, 4) - 1)] if n else []
+        assert got["cont"][0].tolist() == want + [-1] * (4 - len(want))
