@@ -40,7 +40,7 @@ def _args():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", choices=["listen", "listen_top2", "d2t", "cfg", "sweep"], default="listen",
+    ap.add_argument("--workload", choices=["listen", "listen_top2", "d2t", "cfg", "sweep", "pool"], default="listen",
                     help="listen: greedy verify with a runner-up branch (headline); d2t: speculative sampling")
     ap.add_argument("--sessions", type=int, default=None,
                     help="requests per step (default: the workload's own, 64 listen sessions / 128 d2t requests)")
@@ -358,6 +358,8 @@ def run_reference(a):
     import oracle
 
     oracle.build()
+    if a.workload == "pool":
+        return _reference_pool(a, world)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     # the sweep's oracle leg times the sampling workload's requests (same step definition)
     wl = Workload("d2t" if a.workload == "sweep" else a.workload, dev, a.sessions)
@@ -385,6 +387,49 @@ def run_reference(a):
                          "sample": f"{done} requests of the {a.workload} workload, one per step"},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "rows_per_s": nrows / el,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _reference_pool(a, world):
+    """Reference arm of the pool workload: the oracle's lookup over the 4096-session
+    pools of the native arm's headline point, a bounded slice of 64 sessions per step."""
+    import numpy as np
+
+    import oracle
+    import workloads
+
+    R = 4096
+    w = workloads.pool_session(R=R, seed=900 + R)
+    pool = np.full((R, w["Lp"]), -1, np.int32)
+    plen = np.zeros(R, np.int32)
+    for d in w["drafts"][:-2]:
+        o = oracle.pool_append(pool, plen, d)
+        pool, plen = o["pool"], o["pool_len"]
+    per = 64
+
+    def one(s_):
+        lo = (s_ * per) % R
+        oracle.pool_lookup(pool[lo:lo + per], plen[lo:lo + per], w["suffix"][lo:lo + per], w["gamma"])
+
+    for s_ in range(a.warmup):
+        one(s_)
+    t0 = time.perf_counter()
+    for s_ in range(a.steps):
+        one(a.warmup + s_)
+    el = time.perf_counter() - t0
+    v = a.steps * per / el
+    line = {
+        "impl": "reference", "metric": "hypothesis-pool lookups/s (longest 8-gram match, 32-token continuation)",
+        "value": v, "unit": "lookups/s", "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": el / a.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int32", "data": "synthetic",
+        "config": {"workload": "pool: the 4096-session pools, 64 sessions per step through the CPU oracle",
+                   "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": v, "unit": "lookups/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{a.steps * per} lookups, 64 per step"},
+        "e2e": {"value": v, "unit": "lookups/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -593,12 +638,119 @@ def run_sweep(a):
     return 0
 
 
+def run_pool(a):
+    """Hypothesis pool: sessions of 21 chunks, each inserting a main draft and a
+    runner-up branch of up to 32 tokens (about 720 pool entries per session),
+    then one lookup of the longest n-gram (N = 8) matching the emitted suffix
+    with a 32-token continuation.  Per batch of sessions, the lookup call and the
+    append call of one chunk are timed alone with CUDA events after an L2 flush.
+    Prints one JSON line with a point per batch; bytes are the pool entries in
+    use (int32) plus suffixes and continuations."""
+    import torch
+
+    import oracle
+    import serving_sampler_gb300 as sv
+    import workloads
+    from serving_sampler_gb300 import _build
+
+    world, rank, local = _dist()
+    if rank != 0:
+        return 0
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    _build.build()
+    sv.load()
+    stream = torch.cuda.current_stream(device)
+    peak, peak_kind = _peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    steps = max(3, min(a.steps, 50))
+    points = []
+    cpu = None
+    clocks = Clocks(local)
+    clocks.start()
+    for R in (1, 64, 1024, 4096):
+        w = workloads.pool_session(R=R, seed=900 + R)
+        Lp, N, gamma = w["Lp"], w["N"], w["gamma"]
+        pool = torch.full((R, Lp), -1, dtype=torch.int32, device=device)
+        plen = torch.zeros(R, dtype=torch.int32, device=device)
+        drafts = [torch.from_numpy(d).to(device) for d in w["drafts"]]
+        for d in drafts[:-2]:
+            sv.pool_append(pool, plen, d)
+        suffix = torch.from_numpy(w["suffix"]).to(device)
+        out = dict(match_len=torch.empty(R, dtype=torch.int32, device=device),
+                   cont=torch.empty(R, gamma, dtype=torch.int32, device=device))
+        used = int(plen.sum().item())
+        look_bytes = 4 * (used + R + R * N + R + R * gamma)
+
+        def timed(fn):
+            for _ in range(max(a.warmup, 3)):
+                fn()
+            torch.cuda.synchronize()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+            for e0, e1 in ev:
+                flush.add_(1)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            return sum(e0.elapsed_time(e1) for e0, e1 in ev) / steps
+
+        ms_look = timed(lambda: sv.pool_lookup(pool, plen, suffix, gamma, out=out, stream=stream))
+        # append: the last chunk's main draft, undone after every call so the pool stays the same
+        saved = plen.clone()
+
+        def append():
+            sv.pool_append(pool, plen, drafts[-2], stream=stream)
+            plen.copy_(saved)
+
+        ms_app = timed(append)
+        gbs = look_bytes / (ms_look * 1e-3) / 1e9
+        points.append({"sessions": R, "pool_entries": used, "lookup_us": ms_look * 1e3,
+                       "lookups_per_s": R / (ms_look * 1e-3), "lookup_GB/s": gbs, "roofline_frac": gbs / peak,
+                       "append_us_incl_restore_copy": ms_app * 1e3,
+                       "matches": int((out["match_len"] > 0).sum().item())})
+        if R == 64 and not a.no_cpu_baseline:
+            pool_h, plen_h, suf_h = pool.cpu().numpy(), plen.cpu().numpy(), suffix.cpu().numpy()
+            t0 = time.perf_counter()
+            done = 0
+            while time.perf_counter() - t0 < min(a.cpu_seconds, 5.0):
+                oracle.pool_lookup(pool_h, plen_h, suf_h, gamma)
+                done += R
+            el = time.perf_counter() - t0
+            cpu = {"value": done / el, "unit": "lookups/s", "cores": 1, "kind": "oracle",
+                   "sample": f"{done} lookups of the 64-session pool, {el:.1f} s, single-threaded C"}
+        del w, pool, plen, drafts, suffix, out
+        torch.cuda.empty_cache()
+    clock_rows = clocks.stop()
+    big = points[-1]
+    line = {
+        "metric": "hypothesis-pool lookups/s (longest 8-gram match, 32-token continuation)",
+        "value": big["lookups_per_s"], "unit": "lookups/s", "n_gpus": 1, "steps": steps,
+        "warmup": max(a.warmup, 3), "ms_per_step": big["lookup_us"] * 1e-3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+        "config": {"workload": "pool: sessions of 21 chunks x (main draft + runner-up), up to 32 tokens each, "
+                               "N = 8, gamma = 32; value = the 4096-session point",
+                   "l2": "flushed before each call"},
+        "roofline_peak": {"value": peak, "unit": "GB/s",
+                          "source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                          else "fallback 6.8 TB/s"},
+        "points": points,
+        "cpu_baseline": cpu,
+        "gpu_launches": len(points) * 2 * (steps + max(a.warmup, 3)),
+        "clocks": Clocks.summarize(clock_rows),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     a = _args()
     if a.impl == "reference":
         return run_reference(a)
     if a.workload == "sweep":
         return run_sweep(a)
+    if a.workload == "pool":
+        return run_pool(a)
     return run_native(a)
 
 

@@ -75,7 +75,8 @@ enum {
     SV_ST_RESIDUAL_ZERO = 8,  /* max(0, p - q) had no mass: the correction was drawn from p */
     SV_ST_BAD_TEMP = 16,      /* temperature negative or NaN: greedy verification used */
     SV_ST_BAD_D2T = 32,       /* d2t holds an id outside [0, V) or a repeated id */
-    SV_ST_TIMEOUT = 64        /* a bounded device wait gave up; the request's outputs are invalid */
+    SV_ST_TIMEOUT = 64,       /* a bounded device wait gave up; the request's outputs are invalid */
+    SV_ST_POOL_FULL = 128     /* sv_pool_append: the draft did not fit in the pool; nothing inserted */
 };
 
 /* limits */
@@ -83,6 +84,8 @@ enum {
 #define SV_MAX_S 16        /* codebooks per CFG frame */
 #define SV_MAX_PARTS 64    /* vocabulary partitions of sv_infer_modality */
 #define SV_MAX_BRANCHES 8  /* draft branches sharing the first row (sv_verify_greedy) */
+#define SV_MAX_NGRAM 64     /* emitted-suffix tokens matched by sv_pool_lookup */
+#define SV_MAX_POOL (1 << 24) /* pool capacity per request (tokens and separators) */
 #define SV_MAX_WIDTH (1 << 30)
 
 /* A matrix of logit rows: row i, entry x is at data + (i * row_stride + x)
@@ -305,6 +308,48 @@ int sv_cfg_merge_sample(sv_rows cond, sv_rows uncond, const int32_t* cb_id_base,
                         const uint64_t* seeds, const float* temperature,
                         int32_t* accept_len, int32_t* tokens, float* tv, int32_t* status,
                         void* workspace, size_t workspace_bytes, sv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * sv_pool_append / sv_pool_lookup -- the hypothesis pool.
+ * Source: "Decode Before You Hear ..." method steps 3 and 5 and the tool-call
+ * case study (Figure 6 (b)): every draft of the session enters a pool indexed
+ * by n-grams; while the output is unfinished, each later forward first takes
+ * the longest n-gram of the pool that matches the emitted suffix and feeds
+ * its continuation in as drafts.
+ *
+ * Pool layout, kept on the device by the caller:
+ *   pool        int32 [R, Lp]: request r's drafts in insertion order, each
+ *               followed by -1.  Entries at or beyond pool_len[r] are unused
+ *               and never read.
+ *   pool_len    int32 [R]: entries in use (start a session with 0).  Values
+ *               outside [0, Lp] read as a full pool (append) or are clamped
+ *               to [0, Lp] (lookup).
+ *   Lp          capacity per request, 0 <= Lp <= SV_MAX_POOL.
+ *
+ * sv_pool_append inserts drafts int32 [R, k] (k <= SV_MAX_K; a negative id
+ * ends a draft early, an empty draft inserts nothing).  A draft of L tokens
+ * needs L + 1 free entries; when they are not there nothing of it is written
+ * and status[r] (int32 [R] out or NULL) gets SV_ST_POOL_FULL.  drafts must
+ * not overlap the pool.  Call it once per branch to insert several drafts.
+ *
+ * sv_pool_lookup:
+ *   suffix      int32 [R, N]: the last N emitted tokens, oldest first,
+ *               right-aligned; -1 on the left where the output is shorter.
+ *               0 <= N <= SV_MAX_NGRAM.
+ *   gamma       continuation tokens wanted, 0 <= gamma <= SV_MAX_K.
+ *   match_len   int32 [R] out: length n of the match, 0 for none.
+ *   cont        int32 [R, gamma] out: the continuation, -1 padded.
+ * A match of length n >= 1 ends at pool position p when pool[p-n+1 .. p]
+ * equals the last n suffix tokens (none negative, so it lies inside one
+ * draft) and pool[p+1] is a token (not a separator).  The longest match
+ * wins, then the latest p (the most recently inserted draft).  The
+ * continuation is pool[p+1 ..] up to gamma tokens or that draft's end.
+ * ---------------------------------------------------------------------- */
+int sv_pool_append(int32_t* pool, int32_t* pool_len, int32_t Lp, const int32_t* drafts, int32_t k,
+                   int32_t R, int32_t* status, sv_stream_t stream);
+int sv_pool_lookup(const int32_t* pool, const int32_t* pool_len, int32_t Lp, const int32_t* suffix,
+                   int32_t N, int32_t R, int32_t gamma, int32_t* match_len, int32_t* cont,
+                   sv_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * sv_accept_scan -- accept length and commit from caller-given accept flags.

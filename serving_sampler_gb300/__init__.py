@@ -20,13 +20,13 @@ LIB_PATH = _build.LIB
 
 SV_BF16, SV_F32 = 0, 1
 ST_TOKEN_RANGE, ST_BAD_LOGITS, ST_OFF_SUPPORT, ST_RESIDUAL_ZERO = 1, 2, 4, 8
-ST_BAD_TEMP, ST_BAD_D2T, ST_TIMEOUT = 16, 32, 64
-MAX_K, MAX_S = 256, 16
+ST_BAD_TEMP, ST_BAD_D2T, ST_TIMEOUT, ST_POOL_FULL = 16, 32, 64, 128
+MAX_K, MAX_S, MAX_NGRAM, MAX_POOL = 256, 16, 64, 1 << 24
 
 # kernels launched by one call of each entry point (reported by the benchmark)
 # kernels one call launches: verify_sample with a prebuilt d2t plan (or the identity map)
 # launches 2, and 2 more when it builds the plan itself; d2t_plan launches 2
-LAUNCHES = {"verify_greedy": 2, "verify_greedy_top2": 2, "infer_modality": 2, "verify_sample": 2, "verify_sample_plan_in_call": 4, "d2t_plan": 2,
+LAUNCHES = {"verify_greedy": 2, "verify_greedy_top2": 2, "infer_modality": 2, "pool_append": 1, "pool_lookup": 1, "verify_sample": 2, "verify_sample_plan_in_call": 4, "d2t_plan": 2,
             "cfg_merge_sample": 2, "accept_scan": 1}
 
 
@@ -82,6 +82,8 @@ def load(path: str | None = None):
     lib.sv_cfg_merge_sample.argtypes = [SvRows, SvRows, P, P, i32, f32, SvRows, i32, i32, P, P, P, P, P, P,
                                         P, P, sz, P]
     lib.sv_cfg_merge_sample.restype = C.c_int
+    lib.sv_pool_append.argtypes = [P, P, i32, P, i32, i32, P, P]
+    lib.sv_pool_lookup.argtypes = [P, P, i32, P, i32, i32, i32, P, P, P]
     lib.sv_accept_scan.argtypes = [P, P, P, i32, i32, P, P, P]
     lib.sv_accept_scan.restype = C.c_int
     _lib = lib
@@ -286,6 +288,34 @@ def cfg_merge_sample(cond, uncond, cb_id_base, cb_data_offset, S: int, W: int, w
                                    rows_of(draft_logits, W), R, k, _ptr(draft), _ptr(seeds), _ptr(temperature),
                                    _ptr(out["accept_len"]), _ptr(out["tokens"]), _ptr(out.get("tv")),
                                    _ptr(out.get("status")), _ptr(ws), _nbytes(ws), _stream(stream)))
+    return out
+
+
+def pool_append(pool, pool_len, drafts, status=None, stream=None):
+    """Insert drafts int32 [R, k] (a negative id ends a draft early) into the pools
+    int32 [R, Lp] whose used lengths are pool_len int32 [R]; both are updated in
+    place.  status int32 [R] (optional) gets SV_ST_POOL_FULL where a draft did not fit."""
+    lib = load()
+    R, Lp = pool.shape
+    k = drafts.shape[1]
+    _check(lib.sv_pool_append(_ptr(pool), _ptr(pool_len), Lp, _ptr(drafts), k, R, _ptr(status), _stream(stream)))
+    return status
+
+
+def pool_lookup(pool, pool_len, suffix, gamma: int, out: dict | None = None, stream=None) -> dict:
+    """Longest n-gram of the pools int32 [R, Lp] (used lengths pool_len int32 [R])
+    matching the emitted suffix int32 [R, N] (-1 padded on the left); returns
+    match_len int32 [R] and the continuation cont int32 [R, gamma] (-1 padded)."""
+    import torch
+
+    lib = load()
+    R, Lp = pool.shape
+    N = suffix.shape[1]
+    dev = pool.device
+    if out is None:
+        out = dict(match_len=_empty(R, torch.int32, dev), cont=_empty((R, gamma), torch.int32, dev))
+    _check(lib.sv_pool_lookup(_ptr(pool), _ptr(pool_len), Lp, _ptr(suffix), N, R, gamma, _ptr(out["match_len"]),
+                              _ptr(out["cont"]), _stream(stream)))
     return out
 
 

@@ -288,6 +288,37 @@ int sv_cfg_merge_sample(sv_rows cond, sv_rows uncond, const int32_t* cb_id_base,
                                             accept_len, tokens, tv, status, workspace, stream));
 }
 
+int sv_pool_append(int32_t* pool, int32_t* pool_len, int32_t Lp, const int32_t* drafts, int32_t k,
+                   int32_t R, int32_t* status, sv_stream_t stream)
+{
+    if (R < 0 || k < 0 || Lp < 0) return SV_ERR_INVALID_ARG;
+    if (k > SV_MAX_K || Lp > SV_MAX_POOL) return SV_ERR_LIMIT;
+    if (R == 0) return SV_OK;
+    if (pool_len == nullptr || (k > 0 && drafts == nullptr) || (Lp > 0 && pool == nullptr))
+        return SV_ERR_INVALID_ARG;
+    if (!aligned(pool, 4) || !aligned(pool_len, 4) || !aligned(drafts, 4) || !aligned(status, 4))
+        return SV_ERR_ALIGN;
+    if (!have_device()) return SV_ERR_DEVICE;
+    return launched(launch_pool_append(pool, pool_len, Lp, drafts, k, R, status, stream));
+}
+
+int sv_pool_lookup(const int32_t* pool, const int32_t* pool_len, int32_t Lp, const int32_t* suffix,
+                   int32_t N, int32_t R, int32_t gamma, int32_t* match_len, int32_t* cont,
+                   sv_stream_t stream)
+{
+    if (R < 0 || N < 0 || gamma < 0 || Lp < 0) return SV_ERR_INVALID_ARG;
+    if (N > SV_MAX_NGRAM || gamma > SV_MAX_K || Lp > SV_MAX_POOL) return SV_ERR_LIMIT;
+    if (R == 0) return SV_OK;
+    if (pool_len == nullptr || match_len == nullptr || (Lp > 0 && pool == nullptr) ||
+        (N > 0 && suffix == nullptr) || (gamma > 0 && cont == nullptr))
+        return SV_ERR_INVALID_ARG;
+    if (!aligned(pool, 4) || !aligned(pool_len, 4) || !aligned(suffix, 4) || !aligned(match_len, 4) ||
+        !aligned(cont, 4))
+        return SV_ERR_ALIGN;
+    if (!have_device()) return SV_ERR_DEVICE;
+    return launched(launch_pool_lookup(pool, pool_len, Lp, suffix, N, R, gamma, match_len, cont, stream));
+}
+
 int sv_accept_scan(const uint8_t* accept, const int32_t* draft, const int32_t* fix, int32_t R,
                    int32_t k, int32_t* accept_len, int32_t* tokens, sv_stream_t stream)
 {

@@ -63,6 +63,12 @@ cudaError_t launch_verify_greedy(const Rows& target, int32_t R, int32_t k, int32
                                  int32_t* branch, int32_t* status, void* workspace,
                                  cudaStream_t stream, int32_t* top2 = nullptr);
 
+cudaError_t launch_pool_append(int32_t* pool, int32_t* pool_len, int32_t Lp, const int32_t* drafts,
+                               int32_t k, int32_t R, int32_t* status, cudaStream_t stream);
+cudaError_t launch_pool_lookup(const int32_t* pool, const int32_t* pool_len, int32_t Lp, const int32_t* suffix,
+                               int32_t N, int32_t R, int32_t gamma, int32_t* match_len, int32_t* cont,
+                               cudaStream_t stream);
+
 cudaError_t launch_accept_scan(const uint8_t* accept, const int32_t* draft, const int32_t* fix,
                                int32_t R, int32_t k, int32_t* accept_len, int32_t* tokens,
                                cudaStream_t stream);

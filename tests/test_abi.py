@@ -87,6 +87,19 @@ def test_argument_checks_need_no_gpu(lib):
     assert s(buf, buf, buf, -2, 3, buf, buf, None) == -1
     assert s(buf, buf, buf, 0, 3, buf, buf, None) == 0
     assert s(buf, buf, None, 2, 3, buf, buf, None) == -1
+    pa, pl = lib.sv_pool_append, lib.sv_pool_lookup
+    assert pa(buf, buf, 64, buf, 4, 0, None, None) == 0
+    assert pa(buf, buf, 64, buf, 4, -1, None, None) == -1
+    assert pa(buf, buf, 64, buf, 257, 1, None, None) == -4
+    assert pa(buf, buf, (1 << 24) + 1, buf, 4, 1, None, None) == -4
+    assert pa(buf, None, 64, buf, 4, 1, None, None) == -1
+    assert pa(P(0x10002), buf, 64, buf, 4, 1, None, None) == -7
+    assert pl(buf, buf, 64, buf, 4, 0, 8, buf, buf, None) == 0
+    assert pl(buf, buf, 64, buf, 65, 1, 8, buf, buf, None) == -4  # N above SV_MAX_NGRAM
+    assert pl(buf, buf, 64, buf, 4, 1, 257, buf, buf, None) == -4
+    assert pl(buf, buf, 64, None, 4, 1, 8, buf, buf, None) == -1
+    assert pl(buf, buf, 64, buf, 4, 1, 8, buf, None, None) == -1
+    assert pl(buf, buf, 64, buf, 4, 1, -1, buf, buf, None) == -1
     c = lib.sv_cfg_merge_sample
     base = (C.c_int32 * 2)(0, 16)
     assert c(_rows(), _rows(width=8), C.cast(base, P), None, 2, 3.0, _rows(data=None), 1, 1, buf, buf, buf, buf,

@@ -26,6 +26,11 @@ Workloads (names used by tests and the benchmark):
             32,000 with a seeded random injective d2t, T = 0.7.
   cfg       256 requests, 9 codebooks x 4096 entries, 4 drafted frames (+1),
             bf16 cond / uncond rows, w = 3, T = 1, flat distributions.
+  pool      sessions of chunks whose drafts (a main draft of up to 32 tokens
+            and a runner-up branch) are noisy windows of the session's final
+            response, as in the tool-call case study: later chunks redraft
+            what earlier ones already held; the emitted output is a prefix of
+            the response, V = 151,936 token ids.
   sweep     batch x 9 rows (k = 8), V = 151,936, bf16 or fp32 ~ N(0, 3^2),
             requests alternating greedy (T = 0) and sampling (T in {0.6, 1.0})
             with d2t-truncated draft logits.
@@ -278,3 +283,40 @@ def cfg_batch(R: int, k: int, S: int, W: int, w: float = 3.0, T=1.0, dtype=torch
 def cfg_workload(device="cuda", R: int = 256):
     """256 requests, 9 codebooks x 4096 entries, 4 drafted frames (+1), bf16, w = 3, T = 1."""
     return cfg_batch(R, 4, 9, 4096, 3.0, 1.0, torch.bfloat16, seed=1238, seed_base=1234 + 3, device=device)
+
+
+def pool_session(R: int = 64, chunks: int = 21, gamma: int = 32, N: int = 8, V: int = 151936, seed: int = 77,
+                 noise: float = 0.05):
+    """Hypothesis-pool inputs: per chunk a main draft and a runner-up branch per
+    session (int32 [R, gamma], -1 padded), and the emitted suffix int32 [R, N].
+
+    Session r has a final response of 4 * gamma tokens.  Chunk c's main draft is
+    a window of it that starts near the response's beginning and grows with c,
+    cut to a random length, with each token replaced by a random id w.p.
+    `noise`; the runner-up branch is random ids of random length.  The emitted
+    output is a random prefix of the response (at least one token)."""
+    rng = np.random.default_rng(seed)
+    L = 4 * gamma
+    resp = rng.integers(0, V, (R, L), dtype=np.int64)
+    drafts = []
+    for c in range(chunks):
+        for branch in range(2):
+            d = np.full((R, gamma), -1, np.int64)
+            for r in range(R):
+                n = int(rng.integers(1, gamma + 1))
+                if branch == 0:
+                    start = int(rng.integers(0, min(L - n, 2 * c + 1) + 1))
+                    tok = resp[r, start:start + n].copy()
+                    flip = rng.random(n) < noise
+                    tok[flip] = rng.integers(0, V, int(flip.sum()))
+                else:
+                    tok = rng.integers(0, V, n)
+                d[r, :n] = tok
+            drafts.append(d.astype(np.int32))
+    emitted = rng.integers(1, L, R)
+    suffix = np.full((R, N), -1, np.int32)
+    for r in range(R):
+        tail = resp[r, max(0, emitted[r] - N):emitted[r]]
+        suffix[r, N - len(tail):] = tail
+    Lp = chunks * 2 * (gamma + 1)
+    return dict(drafts=drafts, suffix=suffix, Lp=Lp, R=R, N=N, gamma=gamma)
