@@ -58,6 +58,10 @@ def _peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# GB300 HBM3e nominal bandwidth (the measured copy peak is the roofline denominator)
+NOMINAL_HBM_GBS = 7900.0
+
+
 def _dist():
     import torch
 
@@ -512,6 +516,7 @@ def run_native(a):
     peak, peak_kind = _peaks()
     achieved = wl.logit_bytes / (ms_local * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
                 "traffic": _traffic_from_profile(wl.kernel_file, wl.profile),
                 "kernel": f"{wl.kernel} (all kernels of one call inside the same events)",
                 "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
@@ -522,7 +527,7 @@ def run_native(a):
         gbs, rps, done, el = wl.oracle_sample(a.cpu_seconds)
         cpu = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": f"{done} requests of the {a.workload} workload, {el:.1f} s, single-threaded fp64 C",
-               "rows_per_s": rps}
+               "rows_per_s": rps, "host_cores": os.cpu_count()}
 
     if rank == 0:
         line = {
