@@ -816,8 +816,10 @@ __global__ void __launch_bounds__(kRowThreads, 1) sample_rows_kernel(SampleArgs 
 // ---------------------------------------------------------------------------
 // Two warp roles.  Each stream warp pulls its own share of a target row
 // through a private ring of bulk-copied stages, one 2048-id chunk per stage:
-// chunk s of a (request, position) unit belongs to stream warp s % kStreamWarps,
-// so the warps get equal shares.  The warp's lane 0 refills a stage the moment
+// chunk s of (request, position) unit u belongs to stream warp (s + u) % kStreamWarps:
+// a row's chunk count is rarely a multiple of the warp count, and rotating which
+// warps take the extra chunks by unit evens the warps' shares over a CTA's units
+// (the assignment depends on the unit alone, not on the launch geometry).  The warp's lane 0 refills a stage the moment
 // it is read, with the warp's next chunk of this unit or of the CTA's next one.
 // The support entries of a target chunk, packed (draft id, offset) pairs of the
 // plan, come from L2 into registers while the chunk's maxima and exponentials
@@ -1074,10 +1076,16 @@ __device__ __forceinline__ FastUnit fast_unit(const SampleArgs& A, int64_t unit,
     return u;
 }
 
-// chunks of stream warp w in a unit of n chunks: sequence elements w, w + W, ...
-__device__ __forceinline__ int32_t warp_chunks(int32_t n, int w)
+// the first chunk of stream warp w in unit u: chunk s goes to warp (s + u) mod W
+__device__ __forceinline__ int32_t warp_first(int64_t unit, int w)
 {
-    return n > w ? (n - w + kStreamWarps - 1) / kStreamWarps : 0;
+    return (w + kStreamWarps - static_cast<int32_t>(unit % kStreamWarps)) % kStreamWarps;
+}
+
+// chunks of a stream warp whose first chunk is q0 in a unit of n chunks: q0, q0 + W, ...
+__device__ __forceinline__ int32_t warp_chunks(int32_t n, int32_t q0)
+{
+    return n > q0 ? (n - q0 + kStreamWarps - 1) / kStreamWarps : 0;
 }
 
 __device__ __forceinline__ float unit_temp(const SampleArgs& A, int64_t unit)
@@ -1102,7 +1110,7 @@ __device__ __forceinline__ void issue_seq(const SampleArgs& A, const FastUnit& u
 // ahead.  Every lane keeps the same copy; lane 0 issues.
 struct Producer {
     int64_t unit;
-    int32_t i, cnt;
+    int32_t i, cnt, q0;
     FastUnit u;
     float t_next;
     uint32_t issued;
@@ -1112,7 +1120,8 @@ __device__ __forceinline__ void producer_enter(const SampleArgs& A, Producer& P,
 {
     while (P.unit < units) {
         P.u = fast_unit(A, P.unit, T);
-        P.cnt = warp_chunks(P.u.n, w);
+        P.q0 = warp_first(P.unit, w);
+        P.cnt = warp_chunks(P.u.n, P.q0);
         P.i = 0;
         const int64_t nx = P.unit + gridDim.x;
         P.t_next = nx < units ? unit_temp(A, nx) : 0.f;
@@ -1130,7 +1139,7 @@ __device__ __forceinline__ void producer_step(const SampleArgs& A, Producer& P, 
     constexpr uint32_t kS = FastCfg<DT>::kStages;
     if (P.unit >= units || P.issued - consumed >= kS) return;
     const uint32_t sidx = P.issued % kS;
-    if (lane == 0) issue_seq<DT>(A, P.u, w + P.i * kStreamWarps, wst + sidx * FastCfg<DT>::kStageBytes, &wbar[sidx], pol_t);
+    if (lane == 0) issue_seq<DT>(A, P.u, P.q0 + P.i * kStreamWarps, wst + sidx * FastCfg<DT>::kStageBytes, &wbar[sidx], pol_t);
     ++P.issued;
     if (++P.i == P.cnt) {
         P.unit += gridDim.x;
@@ -1220,7 +1229,8 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
             const float c = u.sampling ? kLog2e / T : 0.f;
             const unsigned long long c2 = pack2(c, c);
             const int32_t xj = u.has_draft ? A.draft[static_cast<int64_t>(u.r) * A.k + u.j] : -1;
-            const int32_t nw_chunks = warp_chunks(u.n, w);
+            const int32_t q0 = warp_first(unit, w);
+            const int32_t nw_chunks = warp_chunks(u.n, q0);
             unsigned char* G = gbase + b * gbytes;
             // the TV warps are done with this buffer's previous unit
             if (n >= kNG && !timeout && !mbar_wait_bounded(&freed[b], ((n / kNG) + 1) & 1u)) timeout = 1;
@@ -1235,7 +1245,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                 if (!timeout && !mbar_wait_bounded(&wbar[sidx], (consumed / kS) & 1u)) timeout = 1;
                 const unsigned char* st = wst + sidx * kSB;
                 const uint4* vp = reinterpret_cast<const uint4*>(st);
-                const int32_t q = w + i * kStreamWarps;
+                const int32_t q = q0 + i * kStreamWarps;
                 const int32_t cidx = q;  // target chunk
                 const uint32_t off = static_cast<uint32_t>(cidx) * kSB;
                 const uint32_t nb = min(kSB, static_cast<uint32_t>(A.V) * kE - off);
