@@ -816,10 +816,12 @@ __global__ void __launch_bounds__(kRowThreads, 1) sample_rows_kernel(SampleArgs 
 // ---------------------------------------------------------------------------
 // Two warp roles.  Each stream warp pulls its own share of a target row
 // through a private ring of bulk-copied stages, one 2048-id chunk per stage:
-// chunk s of (request, position) unit u belongs to stream warp (s + u) % kStreamWarps:
-// a row's chunk count is rarely a multiple of the warp count, and rotating which
-// warps take the extra chunks by unit evens the warps' shares over a CTA's units
-// (the assignment depends on the unit alone, not on the launch geometry).  The warp's lane 0 refills a stage the moment
+// chunk s of a (request, position) unit belongs to stream warp (s + rot) % kStreamWarps,
+// rot a hash of the request's seed and the position: a row's chunk count is rarely a
+// multiple of the warp count, and varying which warps take the extra chunks evens the
+// warps' shares over a CTA's units.  rot depends on the request's own inputs only, so
+// the summation order, and with it every output bit of the row pass, does not depend on
+// the request's place in the batch or on the launch geometry.  The warp's lane 0 refills a stage the moment
 // it is read, with the warp's next chunk of this unit or of the CTA's next one.
 // The support entries of a target chunk, packed (draft id, offset) pairs of the
 // plan, come from L2 into registers while the chunk's maxima and exponentials
@@ -1056,6 +1058,7 @@ struct DraftRec {  // a TV warp's share of the draft row
 
 struct FastUnit {
     int32_t r, j;
+    int32_t rot;    // chunk s goes to stream warp (s + rot) mod kStreamWarps
     bool sampling, has_draft;
     const char* trow;
     const char* drow;
@@ -1073,13 +1076,16 @@ __device__ __forceinline__ FastUnit fast_unit(const SampleArgs& A, int64_t unit,
     u.trow = A.tbase + unit * A.tstride;
     u.drow = u.has_draft ? A.dbase + (static_cast<int64_t>(u.r) * A.k + u.j) * A.dstride : nullptr;
     u.n = (A.V + kChunkElems - 1) / kChunkElems;
+    const uint64_t sd = A.seeds[u.r];
+    u.rot = static_cast<int32_t>(((static_cast<uint32_t>(sd) ^ static_cast<uint32_t>(sd >> 32)) * 0x9E3779B1u >> 16) %
+                                 kStreamWarps + u.j) % kStreamWarps;
     return u;
 }
 
-// the first chunk of stream warp w in unit u: chunk s goes to warp (s + u) mod W
-__device__ __forceinline__ int32_t warp_first(int64_t unit, int w)
+// the first chunk of stream warp w in a unit whose chunk s goes to warp (s + rot) mod W
+__device__ __forceinline__ int32_t warp_first(int32_t rot, int w)
 {
-    return (w + kStreamWarps - static_cast<int32_t>(unit % kStreamWarps)) % kStreamWarps;
+    return (w + kStreamWarps - rot) % kStreamWarps;
 }
 
 // chunks of a stream warp whose first chunk is q0 in a unit of n chunks: q0, q0 + W, ...
@@ -1120,7 +1126,7 @@ __device__ __forceinline__ void producer_enter(const SampleArgs& A, Producer& P,
 {
     while (P.unit < units) {
         P.u = fast_unit(A, P.unit, T);
-        P.q0 = warp_first(P.unit, w);
+        P.q0 = warp_first(P.u.rot, w);
         P.cnt = warp_chunks(P.u.n, P.q0);
         P.i = 0;
         const int64_t nx = P.unit + gridDim.x;
@@ -1229,7 +1235,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
             const float c = u.sampling ? kLog2e / T : 0.f;
             const unsigned long long c2 = pack2(c, c);
             const int32_t xj = u.has_draft ? A.draft[static_cast<int64_t>(u.r) * A.k + u.j] : -1;
-            const int32_t q0 = warp_first(unit, w);
+            const int32_t q0 = warp_first(u.rot, w);
             const int32_t nw_chunks = warp_chunks(u.n, q0);
             unsigned char* G = gbase + b * gbytes;
             // the TV warps are done with this buffer's previous unit

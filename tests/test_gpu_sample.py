@@ -155,6 +155,38 @@ def test_d2t_workload_full_size(sv):
         assert np.array_equal(np.nan_to_num(again[key]), np.nan_to_num(got[key]))
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_results_do_not_depend_on_the_place_in_the_batch(sv, dtype):
+    # every output bit (TV, p, q included) is a function of the request's own inputs: the
+    # batch reversed, and a request run alone, give the same bits
+    R, k = 24, 7
+    T = [0.7 if r % 3 else 0.0 for r in range(R)]
+    w = workloads.sample_batch(R, k, workloads.V_QWEN, workloads.VD_DRAFT, dtype, T=T, sigma_pos=0.8, delta=2.7,
+                               seed=31, seed_base=77)
+    a = _run(sv, w)
+    perm = torch.arange(R - 1, -1, -1, device=w["target"].device)
+    rows_t = (perm[:, None] * (k + 1) + torch.arange(k + 1, device=perm.device)).reshape(-1)
+    rows_d = (perm[:, None] * k + torch.arange(k, device=perm.device)).reshape(-1)
+    wp = dict(w, target=w["target"][rows_t].contiguous(), draft_logits=w["draft_logits"][rows_d].contiguous(),
+              draft=w["draft"][perm].contiguous(), seeds=w["seeds"][perm].contiguous(),
+              temperature=w["temperature"][perm].contiguous())
+    b = _run(sv, wp)
+    inv = perm.cpu().numpy()  # reversal is its own inverse
+    for key in a:
+        np.testing.assert_array_equal(a[key].view(np.uint32) if a[key].dtype == np.float32 else a[key],
+                                      b[key][inv].view(np.uint32) if b[key].dtype == np.float32 else b[key][inv],
+                                      err_msg=key)
+    r = 5
+    wa = dict(w, R=1, target=w["target"][r * (k + 1):(r + 1) * (k + 1)], draft_logits=w["draft_logits"][r * k:(r + 1) * k],
+              draft=w["draft"][r:r + 1], seeds=w["seeds"][r:r + 1], temperature=w["temperature"][r:r + 1])
+    c = _run(sv, wa)
+    for key in a:
+        x, y = a[key][r:r + 1], c[key]
+        if x.dtype == np.float32:
+            x, y = x.view(np.uint32), y.view(np.uint32)
+        np.testing.assert_array_equal(x, y, err_msg=key)
+
+
 def test_prebuilt_plan_matches_in_call_plan(sv):
     w = workloads.d2t_workload(R=24)
     plan = sv.d2t_plan(w["d2t"], w["V"])
