@@ -28,15 +28,10 @@
  *    the launch status only; per-request data problems are reported in the
  *    device-written `status` array (bits SV_ST_*), never by a trap.
  *  - Results are a pure function of the inputs: they do not depend on the
- *    position of a request in the batch or on the launch geometry.  Random
- *    draws come from Philox4x32-10 keyed by the request's seed, so a call
- *    repeated on the same inputs gives the same bits.  One exception in
- *    sv_verify_sample: its race kernel uses 1024-thread CTAs while the
- *    batch has at most as many requests as the GPU has SMs and 512-thread
- *    CTAs above that, and the chunk sums of the race are added in an order
- *    that follows the CTA size; a correction or bonus token can therefore
- *    differ between a small and a large batch when two chunk keys of the
- *    race tie to within fp32 rounding.  Accept lengths, TV, p and q do not.
+ *    batch size, the position of a request in the batch or the launch
+ *    geometry (every sum is taken in an order fixed by the request's own
+ *    inputs).  Random draws come from Philox4x32-10 keyed by the request's
+ *    seed, so a call repeated on the same inputs gives the same bits.
  *  - Ties in an argmax or in the sampler go to the lowest index.  NaN logits
  *    read as -inf.
  *  - Workspace: calls that take one need at least the number of bytes the

@@ -1758,10 +1758,15 @@ template <int DT, int DD, int NT>
 __global__ void __launch_bounds__(NT, 1024 / NT) race_rows_kernel(SampleArgs A)
 {
     constexpr int kRaceWarps = NT / 32;
-    constexpr int kEvalVecs = eval_vecs<NT>();
+    // The bounded race sums a round's chunks in the layout of a 1024-thread CTA whatever NT
+    // is (a 512-thread CTA takes two passes of virtual threads), so the sums, and the tokens
+    // they decide, do not depend on the CTA size.
+    constexpr int kVT = 1024;
+    constexpr int kVPass = kVT / NT;
+    constexpr int kEvalVecs = eval_vecs<kVT>();
     pdl_wait_primary();
     extern __shared__ __align__(16) unsigned char rsm[];  // laid out by race_smem_layout
-    __shared__ float bpart_s[kRaceWarps];
+    __shared__ float bpart_s[kVT / 32];
     __shared__ float best_s;
     __shared__ int32_t bc_s, bslot_s, bround_s;  // best chunk, its slot and round in the bounded race
     __shared__ float red_f[kRaceWarps];
@@ -2035,8 +2040,11 @@ __global__ void __launch_bounds__(NT, 1024 / NT) race_rows_kernel(SampleArgs A)
                 for (int32_t r0 = 0; r0 < nc; r0 += kEvalChunks) {
                     if (lb_s[order_s[r0]] > best_s) break;  // block-uniform: read after a barrier
                     last_r0 = r0;
-                    const int slot = tid / (NT / kEvalChunks);
-                    const int sub = tid % (NT / kEvalChunks);
+#pragma unroll 1
+                    for (int vp = 0; vp < kVPass; ++vp) {
+                    const int vtid = tid + vp * NT;  // the virtual thread
+                    const int slot = vtid / (kVT / kEvalChunks);
+                    const int sub = vtid % (kVT / kEvalChunks);
                     float ws = 0.f;
                     if (r0 + slot < nc) {
                         const int32_t cc = order_s[r0 + slot];
@@ -2119,11 +2127,12 @@ __global__ void __launch_bounds__(NT, 1024 / NT) race_rows_kernel(SampleArgs A)
                     }
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
-                    if (lane == 0) bpart_s[tid >> 5] = ws;
+                    if (lane == 0) bpart_s[vtid >> 5] = ws;
+                    }
                     __syncthreads();
                     if (tid < 32) {
                         // lane sl: the key of slot sl's chunk; then the lowest key, lowest chunk id
-                        constexpr int kWarpsPerSlot = kRaceWarps / kEvalChunks;
+                        constexpr int kWarpsPerSlot = kVT / 32 / kEvalChunks;
                         static_assert(kEvalChunks <= 32, "one lane per slot");
                         float kc = INFINITY;
                         int32_t ccl = INT32_MAX;

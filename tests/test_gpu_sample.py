@@ -187,6 +187,24 @@ def test_results_do_not_depend_on_the_place_in_the_batch(sv, dtype):
         np.testing.assert_array_equal(x, y, err_msg=key)
 
 
+def test_results_do_not_depend_on_the_batch_size(sv):
+    # a batch larger than the SM count runs the race in 512-thread CTAs, a small one in
+    # 1024-thread CTAs; the race's sums follow one fixed layout, so the bits agree
+    R, k = 160, 7
+    w = workloads.sample_batch(R, k, workloads.V_QWEN, workloads.VD_DRAFT, torch.bfloat16, T=0.7, sigma_pos=0.9,
+                               delta=2.7, seed=41, seed_base=91)
+    big = _run(sv, w)
+    n = 24
+    small = _run(sv, dict(w, R=n, target=w["target"][:n * (k + 1)], draft_logits=w["draft_logits"][:n * k],
+                          draft=w["draft"][:n], seeds=w["seeds"][:n], temperature=w["temperature"][:n]))
+    for key in small:
+        x, y = big[key][:n], small[key]
+        if x.dtype == np.float32:
+            x, y = x.view(np.uint32), y.view(np.uint32)
+        np.testing.assert_array_equal(x, y, err_msg=key)
+    assert (big["accept_len"][:n] < k).sum() >= 12  # the residual race ran on most of them
+
+
 def test_prebuilt_plan_matches_in_call_plan(sv):
     w = workloads.d2t_workload(R=24)
     plan = sv.d2t_plan(w["d2t"], w["V"])
