@@ -15,7 +15,10 @@
  *       correction argmax p_{n+1} is committed, so every pass commits >= 1
  *       token.  Step 2: a runner-up branch whose first token is the best
  *       token other than the main draft's first token, verified in the same
- *       forward pass.
+ *       forward pass.  Steps 3 and 5: every draft of the session goes into a
+ *       pool indexed by n-grams; while the output continues, the longest
+ *       n-gram of the pool matching the emitted suffix supplies its
+ *       continuation (the tool-call case study, Figure 6 (b)).
  *  [P3] "speculative decoding for Omni models" (blog), section 2 "why it is
  *       lossless": accept draft x_i with probability min(1, p(x_i)/q(x_i));
  *       on rejection resample from norm(max(0, p - q)) and drop the rest;
@@ -55,6 +58,9 @@
  *  - a CFG frame is accepted when all S codebooks are accepted; at the first
  *    rejected frame each codebook keeps its draft if its own test passed,
  *    else draws its own residual sample.
+ *  - hypothesis pool: drafts are stored in insertion order with -1
+ *    separators; a match lies inside one draft and must have a token after
+ *    it; the longest match wins, then the most recently inserted.
  */
 #include <math.h>
 #include <stdint.h>
