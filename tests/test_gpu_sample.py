@@ -155,6 +155,18 @@ def test_d2t_workload_full_size(sv):
         assert np.array_equal(np.nan_to_num(again[key]), np.nan_to_num(got[key]))
 
 
+@pytest.mark.parametrize("V,Vd,R,k", [
+    (151936, 40000, 3, 2),    # a draft vocabulary above the fast path's 32,767 ids: the general row kernel
+    (819200, None, 1, 1),     # identity map at the race's vocabulary limit
+    (4096, 1024, 1, 256),     # the most drafts per request
+])
+def test_size_limits(sv, V, Vd, R, k):
+    T = [0.9] * R
+    w = workloads.sample_batch(R, k, V, Vd, torch.bfloat16, T=T, sigma_pos=0.6, delta=2.0 if Vd else 0.0,
+                               seed=V % 977 + k)
+    compare(_run(sv, w), _oracle(w))
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_results_do_not_depend_on_the_place_in_the_batch(sv, dtype):
     # every output bit (TV, p, q included) is a function of the request's own inputs: the
