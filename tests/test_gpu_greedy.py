@@ -221,6 +221,7 @@ def _va_partitions(V=151936, S=9, W=4096):
     (torch.float32, 70, 151936, _va_partitions()),
     (torch.bfloat16, 40, 5003, [0, 1000, 1000, 2500, 4096]),  # an empty partition, ids past the last
     (torch.float32, 9, 17, [3, 9]),                        # ids before the first partition
+    (torch.bfloat16, 50, 65536, list(range(0, 65537, 1024))),  # the most partitions (64)
 ])
 def test_infer_modality_matches_oracle(sv, dtype, N, V, starts):
     g = torch.Generator(device="cuda").manual_seed(N + V)
