@@ -542,6 +542,7 @@ def test_modality_is_the_partition_of_the_unmasked_argmax():
     rows[0, 99] = rows[0, 100] = 20.0          # tie across a boundary: the lower id, text
     rows[1, :] = np.nan                       # all NaN: argmax 0
     rows[2, 230] = 30.0                       # in the gap: no partition
+    rows[3, 164] = rows[4, 100] = rows[5, 227] = 30.0  # the first and the last id of a partition
     out = oracle.infer_modality(rows, starts)
     amax = _top2_by_sort(rows)[:, 0]
     assert np.array_equal(out["amax"], amax)
@@ -552,7 +553,7 @@ def test_modality_is_the_partition_of_the_unmasked_argmax():
     assert np.array_equal(out["mask_lo"][ok], starts[want[ok]])
     assert np.array_equal(out["mask_hi"][ok], starts[want[ok] + 1])
     assert np.all(out["mask_lo"][~ok] == 0) and np.all(out["mask_hi"][~ok] == 0)
-    assert out["part"][:3].tolist() == [0, 0, -1]
+    assert out["part"][:6].tolist() == [0, 0, -1, 2, 1, 2]
 
 
 def test_bf16_rows_are_widened_exactly():
