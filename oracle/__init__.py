@@ -72,6 +72,8 @@ def _load():
             lib.or_pool_append.restype = C.c_int
             lib.or_pool_lookup.argtypes = [P, P, i32, P, i32, i32, i32, P, P]
             lib.or_pool_lookup.restype = C.c_int
+            lib.or_suffix_append.argtypes = [P, i32, i32, P, P, i32]
+            lib.or_suffix_append.restype = C.c_int
             lib.or_verify_sample.argtypes = [P, C.c_int, i64, i32, P, C.c_int, i64, i32, P, i32, i32,
                                              P, P, P, P, P, P, P, P, P, P, P]
             lib.or_verify_sample.restype = C.c_int
@@ -225,6 +227,19 @@ def pool_lookup(pool, pool_len, suffix, gamma: int):
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments ({rc})")
     return dict(match_len=match_len, cont=cont)
+
+
+def suffix_append(suffix, tokens, accept_len):
+    """The emitted suffix int32 [R, N] after a step that committed tokens[r, 0..n],
+    n = accept_len[r] (tokens int32 [R, k + 1]).  Returns the new suffix."""
+    suffix = _i32(suffix).copy()
+    tokens = _i32(tokens)
+    accept_len = _i32(accept_len)
+    R, N = suffix.shape
+    rc = _load().or_suffix_append(_ptr(suffix), N, R, _ptr(tokens), _ptr(accept_len), tokens.shape[1] - 1)
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments ({rc})")
+    return suffix
 
 
 def verify_sample(target, draft_logits, d2t, R: int, k: int, draft, seeds, temperature):

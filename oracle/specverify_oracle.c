@@ -403,6 +403,29 @@ int or_pool_lookup(const int32_t* pool, const int32_t* pool_len, int32_t Lp, con
     return 0;
 }
 
+/* suffix update after a verify step: the tokens a step commits are its  */
+/* n accepted drafts and the correction, tokens[r, 0 .. n] with n =      */
+/* accept_len[r] (clamped to [0, k]); the emitted suffix [R, N] (oldest  */
+/* first, -1 on the left where the output is shorter) becomes the last N */
+/* tokens of the old suffix followed by them.                            */
+int or_suffix_append(int32_t* suffix, int32_t N, int32_t R, const int32_t* tokens, const int32_t* accept_len,
+                     int32_t k)
+{
+    if (N < 0 || R < 0 || k < 0) return -1;
+    int32_t* all = (int32_t*)malloc(sizeof(int32_t) * (size_t)(N + k + 1));
+    for (int32_t r = 0; r < R; ++r) {
+        int32_t n = accept_len[r];
+        if (n < 0) n = 0;
+        if (n > k) n = k;
+        int32_t m = 0;
+        for (int32_t i = 0; i < N; ++i) all[m++] = suffix[(int64_t)r * N + i];
+        for (int32_t j = 0; j <= n; ++j) all[m++] = tokens[(int64_t)r * (k + 1) + j];
+        for (int32_t i = 0; i < N; ++i) suffix[(int64_t)r * N + i] = all[m - N + i];
+    }
+    free(all);
+    return 0;
+}
+
 /* ------------------------------------------------------------------ */
 /* accept-length scan over caller-given accept flags ([P1] step 4,      */
 /* [P3] section 3: draft i counts only if drafts 0..i-1 were accepted)  */

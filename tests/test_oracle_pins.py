@@ -837,3 +837,44 @@ def test_pool_lookup_pool_len_is_clamped():
         assert got["match_len"][0] == n
         want = [6, 7][: max(0, min(plen, 4) - 1)] if n else []
         assert got["cont"][0].tolist() == want + [-1] * (4 - len(want))
+
+
+def test_suffix_append_shifts_in_the_committed_tokens():
+    # a step commits its n accepted drafts and the correction: tokens[0 .. n]
+    suffix = np.array([[-1, -1, 5, 6], [1, 2, 3, 4], [9, 9, 9, 9]], np.int32)
+    tokens = np.array([[7, 8, 9, -1], [10, -1, -1, -1], [20, 21, 22, 23]], np.int32)
+    out = oracle.suffix_append(suffix, tokens, np.array([2, 0, 3], np.int32))
+    assert out.tolist() == [[6, 7, 8, 9], [2, 3, 4, 10], [20, 21, 22, 23]]
+    # accept lengths outside [0, k] are clamped; a longer commit than N keeps its last N tokens
+    out = oracle.suffix_append(suffix[:1], np.array([[1, 2, 3, 4, 5, 6]], np.int32), np.array([99], np.int32))
+    assert out.tolist() == [[3, 4, 5, 6]]
+    out = oracle.suffix_append(suffix[:1], tokens[:1], np.array([-4], np.int32))
+    assert out.tolist() == [[-1, 5, 6, 7]]
+
+
+def test_verify_then_lookup_walks_along_a_stored_draft():
+    # Steps 4 and 5 in a loop: each verify step commits a prefix of the pool's draft plus the
+    # next token as its correction; the suffix update and the lookup then hand back the rest
+    # of the draft after the committed tokens, until the draft is used up.
+    rng = np.random.default_rng(14)
+    for _ in range(50):
+        drafts = [(3000 * j + rng.permutation(3000)[:int(rng.integers(10, 60))]).tolist() for j in range(4)]
+        pool, plen, _ = _append_all(drafts, 512, width=60)
+        d = drafts[int(rng.integers(0, 4))]
+        N, k = 8, 6
+        suffix = np.full((1, N), -1, np.int32)
+        suffix[0, -1] = d[0]  # the output so far ends with the draft's first token
+        pos = 1               # tokens of d emitted
+        while True:
+            got = oracle.pool_lookup(pool, plen, suffix, k)
+            rest = d[pos:pos + k]
+            assert got["cont"][0, :len(rest)].tolist() == rest
+            if not rest:
+                assert got["match_len"][0] == 0
+                break
+            n = int(rng.integers(0, len(rest)))  # drafts accepted; the next token is the correction
+            tokens = np.full((1, k + 1), -1, np.int32)
+            tokens[0, :n + 1] = d[pos:pos + n + 1]
+            suffix = oracle.suffix_append(suffix, tokens, np.array([n], np.int32))
+            pos += n + 1
+            assert suffix[0, -1] == d[pos - 1]
