@@ -352,6 +352,17 @@ int sv_pool_lookup(const int32_t* pool, const int32_t* pool_len, int32_t Lp, con
                    int32_t N, int32_t R, int32_t gamma, int32_t* match_len, int32_t* cont,
                    sv_stream_t stream);
 
+/* sv_suffix_append: the emitted suffix after a verify step, on the device.
+ *   suffix      int32 [R, N] in/out, as sv_pool_lookup takes it (oldest first,
+ *               -1 on the left where the output is shorter), 0 <= N <= SV_MAX_NGRAM.
+ *   tokens      int32 [R, k + 1]: a verify call's tokens; the step committed
+ *               tokens[r, 0 .. n], n = accept_len[r] clamped to [0, k].
+ *   accept_len  int32 [R].
+ * The new suffix is the last N tokens of the old suffix followed by the committed
+ * tokens.  tokens and accept_len must not overlap suffix. */
+int sv_suffix_append(int32_t* suffix, int32_t N, int32_t R, const int32_t* tokens, const int32_t* accept_len,
+                     int32_t k, sv_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * sv_accept_scan -- accept length and commit from caller-given accept flags.
  * Source: "Decode Before You Hear ..." step 4 (the accepted prefix stops at

@@ -26,7 +26,7 @@ MAX_K, MAX_S, MAX_NGRAM, MAX_POOL = 256, 16, 64, 1 << 24
 # kernels launched by one call of each entry point (reported by the benchmark)
 # kernels one call launches: verify_sample with a prebuilt d2t plan (or the identity map)
 # launches 2, and 2 more when it builds the plan itself; d2t_plan launches 2
-LAUNCHES = {"verify_greedy": 2, "verify_greedy_top2": 2, "infer_modality": 2, "pool_append": 1, "pool_lookup": 1, "verify_sample": 2, "verify_sample_plan_in_call": 4, "d2t_plan": 2,
+LAUNCHES = {"verify_greedy": 2, "verify_greedy_top2": 2, "infer_modality": 2, "pool_append": 1, "pool_lookup": 1, "suffix_append": 1, "verify_sample": 2, "verify_sample_plan_in_call": 4, "d2t_plan": 2,
             "cfg_merge_sample": 2, "accept_scan": 1}
 
 
@@ -84,6 +84,7 @@ def load(path: str | None = None):
     lib.sv_cfg_merge_sample.restype = C.c_int
     lib.sv_pool_append.argtypes = [P, P, i32, P, i32, i32, P, P]
     lib.sv_pool_lookup.argtypes = [P, P, i32, P, i32, i32, i32, P, P, P]
+    lib.sv_suffix_append.argtypes = [P, i32, i32, P, P, i32, P]
     lib.sv_accept_scan.argtypes = [P, P, P, i32, i32, P, P, P]
     lib.sv_accept_scan.restype = C.c_int
     _lib = lib
@@ -317,6 +318,16 @@ def pool_lookup(pool, pool_len, suffix, gamma: int, out: dict | None = None, str
     _check(lib.sv_pool_lookup(_ptr(pool), _ptr(pool_len), Lp, _ptr(suffix), N, R, gamma, _ptr(out["match_len"]),
                               _ptr(out["cont"]), _stream(stream)))
     return out
+
+
+def suffix_append(suffix, tokens, accept_len, stream=None):
+    """Shift a verify step's committed tokens (tokens int32 [R, k + 1], entries 0..n with
+    n = accept_len[r]) into the emitted suffix int32 [R, N], in place."""
+    lib = load()
+    R, N = suffix.shape
+    k = tokens.shape[1] - 1
+    _check(lib.sv_suffix_append(_ptr(suffix), N, R, _ptr(tokens), _ptr(accept_len), k, _stream(stream)))
+    return suffix
 
 
 def accept_scan(accept, draft, fix, out: dict | None = None, stream=None) -> dict:

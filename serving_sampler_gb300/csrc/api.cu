@@ -319,6 +319,18 @@ int sv_pool_lookup(const int32_t* pool, const int32_t* pool_len, int32_t Lp, con
     return launched(launch_pool_lookup(pool, pool_len, Lp, suffix, N, R, gamma, match_len, cont, stream));
 }
 
+int sv_suffix_append(int32_t* suffix, int32_t N, int32_t R, const int32_t* tokens, const int32_t* accept_len,
+                     int32_t k, sv_stream_t stream)
+{
+    if (R < 0 || N < 0 || k < 0) return SV_ERR_INVALID_ARG;
+    if (N > SV_MAX_NGRAM || k > SV_MAX_K) return SV_ERR_LIMIT;
+    if (R == 0 || N == 0) return SV_OK;
+    if (suffix == nullptr || tokens == nullptr || accept_len == nullptr) return SV_ERR_INVALID_ARG;
+    if (!aligned(suffix, 4) || !aligned(tokens, 4) || !aligned(accept_len, 4)) return SV_ERR_ALIGN;
+    if (!have_device()) return SV_ERR_DEVICE;
+    return launched(launch_suffix_append(suffix, N, R, tokens, accept_len, k, stream));
+}
+
 int sv_accept_scan(const uint8_t* accept, const int32_t* draft, const int32_t* fix, int32_t R,
                    int32_t k, int32_t* accept_len, int32_t* tokens, sv_stream_t stream)
 {

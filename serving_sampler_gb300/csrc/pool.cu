@@ -99,6 +99,46 @@ __global__ void __launch_bounds__(kPoolThreads)
     if (threadIdx.x == 0) match_len[r] = n;
 }
 
+// The emitted suffix after a verify step: one warp per request reads the old
+// suffix and the step's committed tokens (its n accepted drafts and the
+// correction) into registers, then writes the last N of the concatenation.
+constexpr int kSuffixWarps = 8;
+
+__global__ void __launch_bounds__(kSuffixWarps * 32)
+    suffix_append_kernel(int32_t* __restrict__ suffix, int32_t N, int32_t R, const int32_t* __restrict__ tokens,
+                         const int32_t* __restrict__ accept_len, int32_t k)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * kSuffixWarps + (threadIdx.x >> 5);
+    if (r >= R) return;
+    const int32_t n = min(max(accept_len[r], 0), k);
+    const int32_t shift = n + 1;  // tokens committed by the step
+    int32_t* S = suffix + r * N;
+    const int32_t* tk = tokens + r * (k + 1);
+    // new[i] = old[i + shift] while that lies in the old suffix, else tokens[i + shift - N]
+    int32_t val[SV_MAX_NGRAM / 32];
+#pragma unroll
+    for (int h = 0; h < SV_MAX_NGRAM / 32; ++h) {
+        const int32_t i = lane + 32 * h;
+        const int32_t src = i + shift;
+        val[h] = i < N ? (src < N ? S[src] : tk[src - N]) : 0;
+    }
+    __syncwarp();  // every lane has read the old suffix before any lane overwrites it
+#pragma unroll
+    for (int h = 0; h < SV_MAX_NGRAM / 32; ++h) {
+        const int32_t i = lane + 32 * h;
+        if (i < N) S[i] = val[h];
+    }
+}
+
+cudaError_t launch_suffix_append(int32_t* suffix, int32_t N, int32_t R, const int32_t* tokens,
+                                 const int32_t* accept_len, int32_t k, cudaStream_t stream)
+{
+    const unsigned blocks = static_cast<unsigned>((R + kSuffixWarps - 1) / kSuffixWarps);
+    suffix_append_kernel<<<blocks, kSuffixWarps * 32, 0, stream>>>(suffix, N, R, tokens, accept_len, k);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_pool_append(int32_t* pool, int32_t* pool_len, int32_t Lp, const int32_t* drafts,
                                int32_t k, int32_t R, int32_t* status, cudaStream_t stream)
 {

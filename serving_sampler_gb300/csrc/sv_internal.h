@@ -69,6 +69,9 @@ cudaError_t launch_pool_lookup(const int32_t* pool, const int32_t* pool_len, int
                                int32_t N, int32_t R, int32_t gamma, int32_t* match_len, int32_t* cont,
                                cudaStream_t stream);
 
+cudaError_t launch_suffix_append(int32_t* suffix, int32_t N, int32_t R, const int32_t* tokens,
+                                 const int32_t* accept_len, int32_t k, cudaStream_t stream);
+
 cudaError_t launch_accept_scan(const uint8_t* accept, const int32_t* draft, const int32_t* fix,
                                int32_t R, int32_t k, int32_t* accept_len, int32_t* tokens,
                                cudaStream_t stream);

@@ -100,6 +100,13 @@ def test_argument_checks_need_no_gpu(lib):
     assert pl(buf, buf, 64, None, 4, 1, 8, buf, buf, None) == -1
     assert pl(buf, buf, 64, buf, 4, 1, 8, buf, None, None) == -1
     assert pl(buf, buf, 64, buf, 4, 1, -1, buf, buf, None) == -1
+    sa = lib.sv_suffix_append
+    assert sa(buf, 8, 0, buf, buf, 4, None) == 0
+    assert sa(buf, 0, 3, buf, buf, 4, None) == 0
+    assert sa(buf, 65, 1, buf, buf, 4, None) == -4
+    assert sa(buf, 8, 1, buf, buf, 257, None) == -4
+    assert sa(buf, 8, 1, None, buf, 4, None) == -1
+    assert sa(buf, -1, 1, buf, buf, 4, None) == -1
     c = lib.sv_cfg_merge_sample
     base = (C.c_int32 * 2)(0, 16)
     assert c(_rows(), _rows(width=8), C.cast(base, P), None, 2, 3.0, _rows(data=None), 1, 1, buf, buf, buf, buf,

@@ -134,3 +134,45 @@ def test_empty_batch(sv):
     sv.pool_append(pool, plen, torch.zeros((0, 4), dtype=torch.int32, device="cuda"))
     torch.cuda.synchronize()
     assert out["match_len"].numel() == 0
+
+
+@pytest.mark.parametrize("R,N,k", [(300, 8, 7), (5, 64, 256), (9, 1, 0), (7, 40, 33)])
+def test_suffix_append(sv, R, N, k):
+    rng = np.random.default_rng(R + N + k)
+    suffix = rng.integers(0, 1000, (R, N)).astype(np.int32)
+    suffix[::3, : N // 2] = -1  # shorter outputs
+    tokens = rng.integers(0, 1000, (R, k + 1)).astype(np.int32)
+    acc = rng.integers(-2, k + 3, R).astype(np.int32)  # also outside [0, k]: clamped
+    for r in range(R):
+        tokens[r, max(0, min(acc[r], k)) + 1:] = -1
+    s_d = _dev(suffix)
+    sv.suffix_append(s_d, _dev(tokens), _dev(acc))
+    want = oracle.suffix_append(suffix, tokens, acc)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(s_d.cpu().numpy(), want)
+
+
+def test_verify_suffix_lookup_loop_on_the_device(sv):
+    # the device-resident loop of the pages' steps 3-5: greedy verification of drafts taken
+    # from the pool, the suffix update from its outputs, the next lookup, all on the GPU
+    import workloads as wl
+
+    w = wl.greedy_batch(16, 6, 4096, torch.bfloat16, branches=1, p_full=0.5, p_first=0.2, seed=5)
+    R, k = w["R"], w["k"]
+    drafts = w["draft"].view(R, k)
+    pool_h = np.zeros((R, 64), np.int32)
+    plen_h = np.zeros(R, np.int32)
+    pool_d, plen_d = _dev(pool_h), _dev(plen_h)
+    pool_h, plen_h = _append_both(sv, pool_d, plen_d, pool_h, plen_h, drafts.cpu().numpy())
+    out = sv.verify_greedy(w["target"], R, k, 1, w["draft"])
+    suffix_h = np.full((R, 8), -1, np.int32)
+    s_d = _dev(suffix_h)
+    sv.suffix_append(s_d, out["tokens"], out["accept_len"])
+    got = sv.pool_lookup(pool_d, plen_d, s_d, k)
+    torch.cuda.synchronize()
+    tok, acc = out["tokens"].cpu().numpy(), out["accept_len"].cpu().numpy()
+    suffix_w = oracle.suffix_append(suffix_h, tok, acc)
+    np.testing.assert_array_equal(s_d.cpu().numpy(), suffix_w)
+    want = oracle.pool_lookup(pool_h, plen_h, suffix_w, k)
+    np.testing.assert_array_equal(got["match_len"].cpu().numpy(), want["match_len"])
+    np.testing.assert_array_equal(got["cont"].cpu().numpy(), want["cont"])
