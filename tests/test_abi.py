@@ -41,6 +41,19 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, name), f"{name} declared in specverify.h but not exported"
 
 
+def test_every_exported_entry_point_is_declared(lib):
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    import serving_sampler_gb300 as m
+    import subprocess
+
+    out = subprocess.run([nm, "-D", "--defined-only", m.LIB_PATH], capture_output=True, text=True, check=True)
+    exported = sorted({line.split()[-1] for line in out.stdout.splitlines()
+                       if line.split()[-1].startswith("sv_") and " T " in line})
+    assert exported == _declared()
+
+
 def test_status_strings(lib):
     for code in range(0, -9, -1):
         s = lib.sv_status_string(code)
