@@ -31,8 +31,28 @@ def close(got, want, name=""):
                              f"(rel {abs(g[i] - w[i]) / max(abs(w[i]), 1e-300):.3g}) at flat index {i}")
 
 
+def commits_at_least_one_token(accept_len, tokens):
+    """The pass-level invariant of the pages: every pass commits its n accepted drafts and
+    one more token (n + 1 >= 1 valid ids per request, frames of S ids for CFG), so a
+    speculative pass never does worse than one autoregressive step; -1 after them."""
+    R = len(accept_len)
+    t = np.asarray(tokens).reshape(R, -1)
+    k1 = t.shape[1]
+    n = np.asarray(accept_len)
+    per = 1
+    if tokens.ndim == 3:  # [R, k + 1, S]
+        k1, per = tokens.shape[1], tokens.shape[2]
+    assert np.all((n >= 0) & (n <= k1 - 1)), "accept length outside [0, k]"
+    idx = np.arange(k1 * per)[None, :] // per
+    committed = idx <= n[:, None]
+    assert np.all(t[committed] >= 0), "a committed token is not a vocabulary id"
+    assert np.all(t[~committed] == -1), "padding after the committed tokens is not -1"
+
+
 def compare(got: dict, want: dict, stats=True):
     """got: CUDA outputs (numpy); want: oracle outputs.  Returns the exempt count."""
+    commits_at_least_one_token(got["accept_len"], got["tokens"])
+    commits_at_least_one_token(want["accept_len"], want["tokens"])
     am = want["accept_margin"]
     am = am.reshape(am.shape[0], -1) if am.size else np.full((len(want["accept_len"]), 1), np.inf)
     margin = np.minimum(am.min(axis=1), want["race_margin"].reshape(len(want["accept_len"]), -1).min(axis=1))

@@ -7,6 +7,7 @@ import torch
 
 import oracle
 import workloads
+from tests.sampling_parity import commits_at_least_one_token
 
 pytestmark = pytest.mark.gpu
 
@@ -17,6 +18,7 @@ def _check(sv, target, R, k, branches, draft, out=None):
     want = oracle.verify_greedy(workloads.host_rows(target), R, k, branches, draft.cpu().numpy())
     for key in ("accept_len", "tokens", "branch", "status"):
         np.testing.assert_array_equal(got[key].cpu().numpy(), want[key], err_msg=key)
+    commits_at_least_one_token(want["accept_len"], want["tokens"])
     return got, want
 
 
