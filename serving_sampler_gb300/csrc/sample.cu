@@ -9,8 +9,9 @@
 //   d2t_group_kernel   one warp per 2048-id chunk: the chunk's support entries
 //                      grouped for the shared-memory scatter of the row pass.
 // Two kernels per call:
-//   sample_rows_fast_kernel (bf16 rows, a d2t map) or sample_rows_kernel (the
-//                      general path): persistent CTAs, one (request, position)
+//   sample_rows_fast_kernel (target and draft rows of one dtype, bf16 or fp32,
+//                      with a d2t map) or sample_rows_kernel (the general
+//                      path): persistent CTAs, one (request, position)
 //                      unit at a time.  The draft and target rows stream
 //                      through bulk-copied shared-memory stages: max, sum-exp
 //                      at T, argmax, NaN/inf flags, z at the support positions
@@ -37,7 +38,7 @@ namespace sv {
 namespace {
 
 constexpr int kPlanThreads = 1024;
-constexpr int32_t kChunkElems = 2048;  // ids per bulk-copied chunk of the bf16 fast path (4 KB)
+constexpr int32_t kChunkElems = 2048;  // ids per bulk-copied chunk of the fast path (4 KB bf16, 8 KB fp32)
 constexpr int kRowThreads = 512;
 constexpr uint32_t kStageBytes = 16384;
 constexpr int kStages = 4;
