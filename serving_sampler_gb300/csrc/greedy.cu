@@ -11,8 +11,14 @@
 // the first index inside the winning vector is found once per segment.  Only
 // a vector holding a NaN leaves the straight-line path.
 // Kernel 2 (greedy_finalize_kernel) merges the segment results of each row
-// and runs the per-request scan, one CTA per request; it is launched as a
-// programmatic dependent of kernel 1 so its launch overlaps kernel 1.
+// and runs the per-request scan and branch choice (one main branch, or up to
+// eight branches sharing the first row), one CTA per request; it is launched
+// as a programmatic dependent of kernel 1 so its launch overlaps kernel 1.
+// With the top-2 output, kernel 1 also keeps each thread's two first
+// (value, position) pairs and kernel 2 merges them into every row's argmax and
+// runner-up id.  Modality inference reuses kernel 1 on full-vocabulary rows,
+// then maps each row's argmax to its vocabulary partition
+// (modality_finalize_kernel).
 #include <algorithm>
 #include <cfloat>
 #include <climits>
