@@ -60,6 +60,9 @@ def _peaks():
 
 # GB300 HBM3e nominal bandwidth (the measured copy peak is the roofline denominator)
 NOMINAL_HBM_GBS = 7900.0
+# GB300 L2 capacity, and the buffer written to flush it
+L2_BYTES = 129 << 20
+L2_FLUSH_BYTES = 256 << 20
 
 
 def _dist():
@@ -463,18 +466,33 @@ def run_native(a):
     torch.cuda.synchronize()
     clocks = Clocks(local)
     clocks.start()
+    # Inputs below four L2s get an L2 flush before every step, outside the events: the row
+    # pass keeps the draft rows in L2 on purpose (for its TV pass), and back-to-back steps
+    # would otherwise find them there.  Larger inputs run back to back.
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device) if wl.logit_bytes < 4 * L2_BYTES else None
     _barrier(world)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(a.steps):
-        wl.call(wl.inputs, stream)
-    e1.record(stream)
-    e1.synchronize()
+    if flush is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(a.steps):
+            wl.call(wl.inputs, stream)
+        e1.record(stream)
+        e1.synchronize()
+        ms_local = e0.elapsed_time(e1) / a.steps
+    else:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+        for f0_, f1_ in ev:
+            flush.add_(1)
+            f0_.record(stream)
+            wl.call(wl.inputs, stream)
+            f1_.record(stream)
+        ev[-1][1].synchronize()
+        ms_local = sum(f0_.elapsed_time(f1_) for f0_, f1_ in ev) / a.steps
     _barrier(world)
     torch.cuda.synchronize()
     clock_rows = clocks.stop()
-    ms_local = e0.elapsed_time(e1) / a.steps
+    del flush
     ms = _max_over_ranks(ms_local, world, device)
     value = world * wl.logit_bytes / (ms * 1e-3) / 1e9
     rows_per_s = world * wl.rows / (ms * 1e-3)
@@ -536,7 +554,10 @@ def run_native(a):
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
             "config": {"workload": wl.desc,
-                       "l2": f"inputs ({wl.logit_bytes / 1e9:.3f} GB) larger than L2 (129 MB); no flush",
+                       "l2": (f"inputs ({wl.logit_bytes / 1e9:.3f} GB) larger than 4 x L2 (129 MB); no flush"
+                              if wl.logit_bytes >= 4 * L2_BYTES else
+                              f"inputs ({wl.logit_bytes / 1e9:.3f} GB) below 4 x L2: L2 flushed before every "
+                              f"step, outside the timed events"),
                        "parallelism": f"replicas x{world}"},
             "rows_per_s": rows_per_s,
             "roofline": roofline,
@@ -558,8 +579,8 @@ def run_sweep(a):
     """Throughput sweep: batches {1, 8, 64, 256, 1024} x 9 positions (8 drafts + bonus),
     V = 151,936, bf16 and fp32 logits, half the requests greedy (T = 0) and half sampled
     (T alternating 0.6 / 1.0) with the d2t draft model of the sampling workload.  Every
-    call is timed alone with CUDA events; L2 is flushed before each call whose inputs
-    fit in four L2s.  Prints one JSON line with a point per (dtype, batch)."""
+    call is timed alone with CUDA events after an L2 flush.  Prints one JSON line with a
+    point per (dtype, batch)."""
     import torch
 
     import serving_sampler_gb300 as sv
@@ -605,11 +626,11 @@ def run_sweep(a):
             for _ in range(max(a.warmup, 3)):
                 call()
             torch.cuda.synchronize()
-            do_flush = nbytes < 4 * (129 << 20)
+            # every call follows an L2 flush: the row pass keeps draft rows in L2 for its TV pass,
+            # and without the flush a call could find the previous call's there
             ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
             for e0, e1 in ev:
-                if do_flush:
-                    flush.add_(1)
+                flush.add_(1)
                 e0.record(stream)
                 call()
                 e1.record(stream)
@@ -619,7 +640,7 @@ def run_sweep(a):
             points.append({"dtype": "bf16" if es == 2 else "f32", "batch": B, "rows": B * (k + 1),
                            "sampled_requests": nsamp, "bytes": nbytes, "us_per_call": ms * 1e3, "GB/s": gbs,
                            "rows_per_s": B * (k + 1) / (ms * 1e-3), "roofline_frac": gbs / peak,
-                           "l2": "flushed before each call" if do_flush else "inputs larger than L2"})
+                           "l2": "flushed before each call"})
             del w, plan, out, ws
             torch.cuda.empty_cache()
     clock_rows = clocks.stop()
