@@ -30,6 +30,21 @@ def lib():
     return m.load()
 
 
+def test_binding_constants_match_the_header():
+    import serving_sampler_gb300 as m
+
+    text = open(HEADER).read()
+    st = dict(re.findall(r"SV_(ST_[A-Z_0-9]+)\s*=\s*(\d+)", text))
+    for name, v in st.items():
+        assert getattr(m, name) == int(v), name
+    limits = {}
+    for name, v in re.findall(r"#define SV_(MAX_[A-Z]+)\s+(\(?[0-9 <]+\)?)", text):
+        a, _, b = v.strip("() ").partition("<<")
+        limits[name] = int(a) << int(b) if b else int(a)
+    for name in ("MAX_K", "MAX_S", "MAX_NGRAM", "MAX_POOL"):
+        assert getattr(m, name) == limits[name], name
+
+
 def test_header_declares_the_four_calls():
     names = _declared()
     for n in ["sv_verify_greedy", "sv_verify_sample", "sv_cfg_merge_sample", "sv_accept_scan"]:
