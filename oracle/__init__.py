@@ -27,9 +27,6 @@ BF16, F32 = 0, 1
 ST_TOKEN_RANGE, ST_BAD_LOGITS, ST_OFF_SUPPORT = 1, 2, 4
 ST_RESIDUAL_ZERO, ST_BAD_TEMP, ST_BAD_D2T = 8, 16, 32
 TAG_ACCEPT, TAG_RESIDUAL, TAG_BONUS = 0, 1, 2
-TAG_RESIDUAL_CHUNK, TAG_BONUS_CHUNK = 3, 4
-RACE_CHUNK = 2048  # ids per chunk of the two-level race over the full target vocabulary
-CFG_RACE_CHUNK = 256  # ids per chunk of the two-level race over a CFG codebook row
 
 
 def build(force: bool = False) -> str:
@@ -58,8 +55,6 @@ def _load():
             lib.or_uniform_from_word.restype = C.c_double
             lib.or_race.argtypes = [P, i32, u64, u32, u32, P]
             lib.or_race.restype = i32
-            lib.or_race2.argtypes = [P, i32, i32, u64, u32, u32, u32, P]
-            lib.or_race2.restype = i32
             lib.or_accept_scan.argtypes = [P, P, P, i32, i32, P, P]
             lib.or_accept_scan.restype = C.c_int
             lib.or_verify_greedy.argtypes = [P, C.c_int, i64, i32, i32, i32, i32, P, P, P, P, P]
@@ -133,14 +128,6 @@ def race(w, seed: int, row: int, tag: int):
     w = np.ascontiguousarray(np.asarray(w, dtype=np.float64))
     m = C.c_double(0.0)
     idx = _load().or_race(_ptr(w), w.size, seed, row, tag, C.byref(m))
-    return int(idx), float(m.value)
-
-
-def race2(w, chunk: int, seed: int, row: int, tag_chunk: int, tag: int):
-    """(index, margin) of the two-level race: chunk of ``chunk`` ids first, then the element."""
-    w = np.ascontiguousarray(np.asarray(w, dtype=np.float64))
-    m = C.c_double(0.0)
-    idx = _load().or_race2(_ptr(w), w.size, chunk, seed, row, tag_chunk, tag, C.byref(m))
     return int(idx), float(m.value)
 
 

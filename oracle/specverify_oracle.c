@@ -40,15 +40,13 @@
  *  - T <= 0 (or NaN) selects greedy verification for that request.
  *  - argmax and the sampler break ties toward the lowest index.
  *  - the accept test is the strict comparison u < p/q with u in (0,1).
- *  - the sampler is an exponential race: argmin_x E_x / w_x, E_x = -ln u_x,
- *    u_x a Philox4x32-10 uniform keyed by the request seed and counted by
- *    (x >> 2, row, tag, 0); tags 0 accept, 1 residual, 2 bonus.  Over the
- *    full target vocabulary it is run in two levels: the ids are cut into
- *    chunks of RACE_CHUNK, the chunk c = argmin E_c / W_c (W_c the chunk's
- *    weight sum, E_c from tag 3 for the residual, 4 for the bonus, counted by
- *    c), then the element race inside that chunk; P(x) = w_x / sum w still.
- *    The per-codebook CFG rows use the same two-level race with chunks of
- *    CFG_RACE_CHUNK ids.
+ *  - the sampler is an exponential race over the whole row: the token is
+ *    argmin_x E_x / w_x over the ids with w_x > 0, E_x = -ln u_x, u_x the
+ *    Philox4x32-10 uniform of id x keyed by the request seed and counted by
+ *    (x >> 2, row, tag, 0), word x & 3; tags 0 accept, 1 residual, 2 bonus.
+ *    P(argmin = x) = w_x / sum w, which is the draw from norm(w) the blog
+ *    asks for.  The same race serves the full target vocabulary and the CFG
+ *    codebook rows.
  *  - the uniform from a 32-bit word r is (2 * (r >> 9) + 1) * 2^-24.
  *  - NaN logits count as -inf.  A sampling request with a NaN, +inf or
  *    all -inf row is verified greedily and flagged (status bit 2).
@@ -78,12 +76,7 @@ enum {
     OR_ST_BAD_D2T = 32       /* d2t entry out of range or repeated */
 };
 
-enum { TAG_ACCEPT = 0, TAG_RESIDUAL = 1, TAG_BONUS = 2, TAG_RESIDUAL_CHUNK = 3, TAG_BONUS_CHUNK = 4 };
-
-/* ids per chunk of the two-level race over the full target vocabulary */
-#define RACE_CHUNK 2048
-/* ids per chunk of the two-level race over a CFG codebook row */
-#define CFG_RACE_CHUNK 256
+enum { TAG_ACCEPT = 0, TAG_RESIDUAL = 1, TAG_BONUS = 2 };
 
 /* ------------------------------------------------------------------ */
 /* Philox4x32-10, from Salmon, Moraes, Dror, Shaw, "Parallel Random    */
@@ -304,29 +297,6 @@ int32_t or_race(const double* w, int32_t n, uint64_t seed, uint32_t row, uint32_
                 double* margin)
 {
     return race_span(w, 0, n, seed, row, tag, margin);
-}
-
-/* two-level race: the chunk of `chunk` consecutive ids first, by a race over
- * the chunk sums W_c with the uniforms of tag_chunk counted by c, then the
- * element race inside it.  P(chunk c) = W_c / sum W and P(x | c) = w_x / W_c,
- * so P(x) = w_x / sum w.  *margin = the smaller of the two races' margins. */
-int32_t or_race2(const double* w, int32_t n, int32_t chunk, uint64_t seed, uint32_t row,
-                 uint32_t tag_chunk, uint32_t tag, double* margin)
-{
-    const int32_t nc = (n + chunk - 1) / chunk;
-    double* W = (double*)calloc((size_t)(nc > 0 ? nc : 1), sizeof(double));
-    for (int32_t x = 0; x < n; ++x)
-        if (w[x] > 0.0) W[x / chunk] += w[x];
-    double mc = INFINITY, me = INFINITY;
-    const int32_t c = race_span(W, 0, nc, seed, row, tag_chunk, &mc);
-    free(W);
-    int32_t arg = -1;
-    if (c >= 0) {
-        const int32_t x1 = (c + 1) * chunk < n ? (c + 1) * chunk : n;
-        arg = race_span(w, c * chunk, x1, seed, row, tag, &me);
-    }
-    if (margin) *margin = mc < me ? mc : me;
-    return arg;
 }
 
 /* ------------------------------------------------------------------ */
@@ -630,10 +600,10 @@ int or_verify_sample(const void* target, int t_dtype, int64_t t_stride, int32_t 
                 double mg;
                 int32_t tok;
                 if (mass > 0.0) {
-                    tok = or_race2(w, V, RACE_CHUNK, seeds[r], (uint32_t)j, TAG_RESIDUAL_CHUNK, TAG_RESIDUAL, &mg);
+                    tok = or_race(w, V, seeds[r], (uint32_t)j, TAG_RESIDUAL, &mg);
                 } else {
                     st |= OR_ST_RESIDUAL_ZERO;
-                    tok = or_race2(p, V, RACE_CHUNK, seeds[r], (uint32_t)j, TAG_RESIDUAL_CHUNK, TAG_RESIDUAL, &mg);
+                    tok = or_race(p, V, seeds[r], (uint32_t)j, TAG_RESIDUAL, &mg);
                 }
                 out[n] = tok;
                 if (race_margin) race_margin[r] = mg;
@@ -645,7 +615,7 @@ int or_verify_sample(const void* target, int t_dtype, int64_t t_stride, int32_t 
             for (int32_t x = 0; x < V; ++x) z[x] = load_elem(target, t_dtype, trow * t_stride + x);
             softmax_T(z, V, T, p);
             double mg;
-            out[k] = or_race2(p, V, RACE_CHUNK, seeds[r], (uint32_t)k, TAG_BONUS_CHUNK, TAG_BONUS, &mg);
+            out[k] = or_race(p, V, seeds[r], (uint32_t)k, TAG_BONUS, &mg);
             if (race_margin) race_margin[r] = mg;
         }
         for (int32_t j = 0; j < n; ++j) out[j] = d[j];
@@ -791,7 +761,7 @@ int or_cfg_merge_sample(const void* cond, const void* uncond, int dtype, int64_t
             double mg = INFINITY;
             int32_t tok;
             if (n == k) {
-                tok = or_race2(p, W, CFG_RACE_CHUNK, seeds[r], urow, TAG_BONUS_CHUNK, TAG_BONUS, &mg);
+                tok = or_race(p, W, seeds[r], urow, TAG_BONUS, &mg);
             } else if (acc[n * S + s]) {
                 tok = d[n * S + s] - cb_id_base[s];
             } else {
@@ -808,10 +778,10 @@ int or_cfg_merge_sample(const void* cond, const void* uncond, int dtype, int64_t
                 if (!(ld >= 0 && ld < W && q[ld] > 0.0) && ld >= 0 && ld < W)
                     st |= OR_ST_OFF_SUPPORT;
                 if (mass > 0.0) {
-                    tok = or_race2(w, W, CFG_RACE_CHUNK, seeds[r], urow, TAG_RESIDUAL_CHUNK, TAG_RESIDUAL, &mg);
+                    tok = or_race(w, W, seeds[r], urow, TAG_RESIDUAL, &mg);
                 } else {
                     st |= OR_ST_RESIDUAL_ZERO;
-                    tok = or_race2(p, W, CFG_RACE_CHUNK, seeds[r], urow, TAG_RESIDUAL_CHUNK, TAG_RESIDUAL, &mg);
+                    tok = or_race(p, W, seeds[r], urow, TAG_RESIDUAL, &mg);
                 }
             }
             out[n * S + s] = cb_id_base[s] + tok;

@@ -77,42 +77,35 @@ def test_race_distribution_chi_square():
     assert _chi2_ok(counts, w) > CHI2_ALPHA
 
 
-def test_two_level_race_distribution_chi_square():
-    # chunks of 4 over 23 ids (last chunk ragged), weights spread over every chunk, zeros inside
+def test_race_distribution_ragged_row_with_zeros():
+    # 23 ids (not a multiple of the four uniforms a Philox block gives), zeros inside
     rng = np.random.default_rng(5)
     w = rng.uniform(0.0, 1.0, 23) ** 3
     w[[1, 9, 10, 22]] = 0.0
     n = 60_000
     counts = np.zeros(len(w))
     for seed in range(n):
-        counts[oracle.race2(w, 4, seed * 104729 + 3, 5, 3, 1)[0]] += 1
+        counts[oracle.race(w, seed * 104729 + 3, 5, 1)[0]] += 1
     assert _chi2_ok(counts, w) > CHI2_ALPHA
-    # the chunk level alone: P(chunk c) = W_c / sum W
-    W = np.add.reduceat(w, np.arange(0, 23, 4))
-    assert _chi2_ok(np.add.reduceat(counts, np.arange(0, 23, 4)), W) > CHI2_ALPHA
 
 
-def test_two_level_race_counter_layout():
-    # the library's convention: the chunk uniform is counted by the chunk index c, the element
-    # uniform by the absolute id x (not the id inside the chunk)
-    w = np.zeros(3 * 2048)
-    w[[4100, 4101, 4102]] = [0.2, 0.5, 0.3]
+def test_race_counter_layout_and_margin():
+    # the uniform of a candidate is counted by its absolute id x (block x >> 2, word x & 3), the
+    # row and the tag; the margin is the relative gap between the two smallest keys
+    V = 151_936
+    ids = np.array([4100, 4101, 4102, 77_777, V - 1])
+    w = np.zeros(V)
+    w[ids] = [0.2, 0.5, 0.3, 0.25, 0.4]
     for seed in range(40):
-        keys = [-math.log(oracle.uniform(seed, 9, 1, x)) / w[x] for x in (4100, 4101, 4102)]
-        assert oracle.race2(w, 2048, seed, 9, 3, 1)[0] == 4100 + int(np.argmin(keys))
-
-
-def test_two_level_race_special_cases():
-    w = np.zeros(4100)
-    w[2051] = 1e-30
-    for seed in range(20):
-        assert oracle.race2(w, 2048, seed, 0, 3, 1)[0] == 2051
-    assert oracle.race2(np.zeros(4100), 2048, 7, 0, 3, 1)[0] == -1
-    # one chunk holding every id: the chunk level is a no-op, the element race is the one-level race
-    rng = np.random.default_rng(6)
-    v = rng.uniform(0, 1, 37)
-    for seed in range(200):
-        assert oracle.race2(v, 64, seed, 2, 4, 2)[0] == oracle.race(v, seed, 2, 2)[0]
+        keys = np.array([-math.log(oracle.uniform(seed, 9, 1, int(x))) / w[x] for x in ids])
+        got, margin = oracle.race(w, seed, 9, 1)
+        assert got == ids[int(np.argmin(keys))]
+        ks = np.sort(keys)
+        assert margin == pytest.approx((ks[1] - ks[0]) / ks[0], rel=1e-12)
+    # another row or tag draws other uniforms, so the winners differ for some seeds
+    same_row = [oracle.race(w, s, 9, 1)[0] for s in range(40)]
+    assert same_row != [oracle.race(w, s, 8, 1)[0] for s in range(40)]
+    assert same_row != [oracle.race(w, s, 9, 2)[0] for s in range(40)]
 
 
 # --------------------------------------------------------------------------
@@ -246,10 +239,12 @@ def _binned(tokens, probs, heavy, chunk):
     return np.bincount(bin_of[tokens], minlength=nb), np.bincount(bin_of, weights=probs, minlength=nb)
 
 
-def test_sampling_distribution_across_race_chunks():
-    # V spans three chunks of the two-level race (the last one ragged); mass sits on a few ids
-    # in different chunks and on the long tail, so both race levels decide
-    V, T, R = 2 * oracle.RACE_CHUNK + 4, 1.0, 8_000
+TAIL_BIN = 2048  # ids per bin of the long tail in the binned chi-square tests
+
+
+def test_sampling_distribution_long_row():
+    # a row of 4100 ids with mass on a few ids far apart and on the long tail (binned in 2048s)
+    V, T, R = 2 * TAIL_BIN + 4, 1.0, 8_000
     rng = np.random.default_rng(11)
     heavy = np.array([3, 2050, 4099])
     z0 = rng.normal(0, 0.5, V).astype(np.float32)
@@ -270,10 +265,10 @@ def test_sampling_distribution_across_race_chunks():
                                seeds, np.full(R, T, np.float32))
     first = out["tokens"][:, 0]
     acc = out["accept_len"] == 1
-    assert _chi2_ok(*_binned(first, p, heavy, oracle.RACE_CHUNK)) > CHI2_ALPHA
+    assert _chi2_ok(*_binned(first, p, heavy, TAIL_BIN)) > CHI2_ALPHA
     resid = np.maximum(0.0, p - q)
-    assert _chi2_ok(*_binned(first[~acc], resid, heavy, oracle.RACE_CHUNK)) > CHI2_ALPHA
-    assert _chi2_ok(*_binned(out["tokens"][acc, 1], pb, heavy, oracle.RACE_CHUNK)) > CHI2_ALPHA
+    assert _chi2_ok(*_binned(first[~acc], resid, heavy, TAIL_BIN)) > CHI2_ALPHA
+    assert _chi2_ok(*_binned(out["tokens"][acc, 1], pb, heavy, TAIL_BIN)) > CHI2_ALPHA
 
 
 def test_tokens_per_pass_closed_form():
@@ -315,6 +310,39 @@ def test_dspark_arithmetic():
 def _toy_logits(ctx, V, scale=1.0, salt=0):
     h = abs(hash((salt,) + tuple(int(c) for c in ctx))) % (2 ** 32)
     return (np.random.default_rng(h).normal(0, scale, V)).astype(np.float32)
+
+
+def test_sampling_stream_convention():
+    """Which uniforms decide: position j's accept test takes element 0 of (row j, tag 0); the
+    residual race at the first rejection n takes (row n, tag 1); the bonus race (row k, tag 2).
+    The expected tokens are rebuilt here from p and q in numpy and the library-independent
+    race/uniform pins above, so a swapped tag or row in the verify path fails."""
+    V, k, T, R = 6, 2, 0.8, 300
+    rng = np.random.default_rng(31)
+    z = rng.normal(0, 1.0, (R * (k + 1), V)).astype(np.float32)
+    y = rng.normal(0, 1.0, (R * k, V)).astype(np.float32)
+    draft = rng.integers(0, V, size=(R, k)).astype(np.int32)
+    seeds = rng.integers(0, 2 ** 63, size=R, dtype=np.uint64)
+    out = oracle.verify_sample(z, y, None, R, k, draft, seeds, np.full(R, T, np.float32))
+
+    def sm(v):
+        e = np.exp(v.astype(np.float64) / T - (v.astype(np.float64) / T).max())
+        return e / e.sum()
+
+    for r in range(R):
+        sd = int(seeds[r])
+        n = k
+        for j in range(k):
+            p, q = sm(z[r * (k + 1) + j]), sm(y[r * k + j])
+            x = draft[r, j]
+            if not oracle.uniform(sd, j, 0, 0) < p[x] / q[x]:
+                n = j
+                want = oracle.race(np.maximum(p - q, 0.0), sd, j, 1)[0]
+                break
+        if n == k:
+            want = oracle.race(sm(z[r * (k + 1) + k]), sd, k, 2)[0]
+        assert out["accept_len"][r] == n
+        assert out["tokens"][r, n] == want
 
 
 def test_sampling_matches_autoregressive_pairs():
@@ -638,11 +666,14 @@ def test_cfg_weight_one_greedy_is_greedy_on_cond():
         assert out["tokens"][r, n].tolist() == (am[r, n] + base).tolist()
 
 
-def test_cfg_sampling_distribution_across_race_chunks():
-    """A codebook row spanning three chunks of the two-level race (the last one ragged), with
-    mass on a few ids in different chunks and on the long tail: the emitted token follows p
-    at the first frame, the residual where the draft was rejected, and p at the bonus frame."""
-    W, T, R, w = 2 * oracle.CFG_RACE_CHUNK + 4, 1.0, 8_000, 2.0
+CFG_TAIL_BIN = 256  # ids per tail bin of the codebook-row chi-square test
+
+
+def test_cfg_sampling_distribution_long_codebook_row():
+    """A codebook row of 516 ids with mass on a few ids far apart and on the long tail: the
+    emitted token follows p at the first frame, the residual where the draft was rejected,
+    and p at the bonus frame."""
+    W, T, R, w = 2 * CFG_TAIL_BIN + 4, 1.0, 8_000, 2.0
     rng = np.random.default_rng(24)
     heavy = np.array([3, 300, 513])
     cz = rng.normal(0, 0.3, W).astype(np.float32)
@@ -669,10 +700,10 @@ def test_cfg_sampling_distribution_across_race_chunks():
                                   x.reshape(R, 1, 1).astype(np.int32), seeds, np.full(R, T, np.float32))
     first = out["tokens"][:, 0, 0]
     acc = out["accept_len"] == 1
-    assert _chi2_ok(*_binned(first, p, heavy, oracle.CFG_RACE_CHUNK)) > CHI2_ALPHA
+    assert _chi2_ok(*_binned(first, p, heavy, CFG_TAIL_BIN)) > CHI2_ALPHA
     resid = np.maximum(0.0, p - q)
-    assert _chi2_ok(*_binned(first[~acc], resid, heavy, oracle.CFG_RACE_CHUNK)) > CHI2_ALPHA
-    assert _chi2_ok(*_binned(out["tokens"][acc, 1, 0], pb, heavy, oracle.CFG_RACE_CHUNK)) > CHI2_ALPHA
+    assert _chi2_ok(*_binned(first[~acc], resid, heavy, CFG_TAIL_BIN)) > CHI2_ALPHA
+    assert _chi2_ok(*_binned(out["tokens"][acc, 1, 0], pb, heavy, CFG_TAIL_BIN)) > CHI2_ALPHA
 
 
 def test_cfg_codebook_marginals_are_target():
