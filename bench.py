@@ -28,6 +28,8 @@ import sys
 import tempfile
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -45,7 +47,11 @@ def _args():
     ap.add_argument("--sessions", type=int, default=None,
                     help="requests per step (default: the workload's own, 64 listen sessions / 128 d2t requests)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
+    ap.add_argument("--no-sub", action="store_true",
+                    help="listen only: skip the d2t, CFG and sweep sub-records of the same line")
+    ap.add_argument("--sub-steps", type=int, default=100, help="timed calls per sub-record")
+    ap.add_argument("--cpu-seconds", type=float, default=16.0, help="CPU-baseline sample budget (two halves: "
+                    "single-threaded, then all host threads)")
     return ap.parse_args()
 
 
@@ -170,173 +176,266 @@ class Clocks:
 # ---------------------------------------------------------------------------
 # workloads
 # ---------------------------------------------------------------------------
-class Workload:
-    """Inputs resident on the device, the library call of one step, and the
-    algorithmic bytes it must read."""
+SAMPLING = ("d2t", "cfg")  # sampling workloads besides the sweep points
 
-    def __init__(self, name, device, sessions):
-        import torch
 
-        import serving_sampler_gb300 as sv
+class Spec:
+    """The inputs of one workload (seeded, synthetic, generated with torch on `device`),
+    the algorithmic bytes one call must read, and its description.  Holds no library
+    object, so the reference arm can use it without loading the CUDA library."""
+
+    def __init__(self, name, device, sessions=None):
         import workloads
 
         self.name = name
-        self.sv = sv
+        self.sweep = name.startswith("sweep_")
         if name in ("listen", "listen_top2"):
             w = workloads.listen(device=device, R=sessions or 64)
             R, k = w["R"], w["k"]
             self.rows = R * (2 * k + 1)
             self.logit_bytes = self.rows * w["V"] * 2
             self.inputs = {"target": w["target"], "draft": w["draft"]}
-            self.out = dict(accept_len=torch.empty(R, dtype=torch.int32, device=device),
-                            tokens=torch.empty(R, k + 1, dtype=torch.int32, device=device),
-                            branch=torch.empty(R, dtype=torch.int32, device=device),
-                            status=torch.empty(R, dtype=torch.int32, device=device))
-            self.ws = torch.empty(sv.verify_greedy_workspace(R, k, 2, w["V"]), dtype=torch.uint8, device=device)
-            self.launches = sv.LAUNCHES["verify_greedy"]
-            self.kernel = "argmax_segments_kernel<bf16>"
-            self.kernel_file = "greedy.cu"
-            self.profile = "argmax_segments_listen.md"
+            self.dtype = "bf16"
             self.desc = (f"listen: {R} sessions x (32 main + 32 runner-up drafts) = 65 rows x 151936 bf16 per "
                          f"session ({self.logit_bytes / 1e9:.3f} GB of logits per step)")
             self.metric = "verify logit GB/s (speculative-listening greedy verify, V=151936 bf16)"
             if name == "listen_top2":
-                # the same verification, also returning every row's argmax and runner-up id
-                self.out["top2"] = torch.empty(self.rows, 2, dtype=torch.int32, device=device)
-                self.ws = torch.empty(sv.verify_greedy_top2_workspace(R, k, 2, w["V"]), dtype=torch.uint8,
-                                      device=device)
-                self.launches = sv.LAUNCHES["verify_greedy_top2"]
-                self.kernel = "argmax_segments_kernel<bf16, top-2>"
-                self.profile = "argmax_segments_listen_top2.md"
                 self.desc = self.desc.replace("listen:", "listen with every row's argmax and runner-up:")
                 self.metric = "verify + top-2 logit GB/s (speculative-listening greedy verify, V=151936 bf16)"
-        elif name == "d2t":
-            w = workloads.d2t_workload(device=device, R=sessions or 128)
+        elif name == "d2t" or self.sweep:
+            if self.sweep:  # sweep_<bf16|f32>_b<B>
+                _, dt, b = name.split("_")
+                import torch
+
+                w = workloads.sweep_batch(int(b[1:]), torch.bfloat16 if dt == "bf16" else torch.float32,
+                                          device=device)
+                self.dtype = dt
+            else:
+                w = workloads.d2t_workload(device=device, R=sessions or 128)
+                self.dtype = "bf16"
             R, k, V, Vd = w["R"], w["k"], w["V"], w["Vd"]
+            es = w["target"].element_size()
+            self.sampled = int((w["temperature"] > 0).sum().item())
             self.rows = R * (k + 1)
-            self.logit_bytes = R * (k + 1) * V * 2 + R * k * Vd * 2 + Vd * 4
+            self.logit_bytes = R * (k + 1) * V * es + self.sampled * k * Vd * es + Vd * 4
             self.inputs = {"target": w["target"], "draft_logits": w["draft_logits"], "d2t": w["d2t"],
                            "draft": w["draft"], "seeds": w["seeds"], "temperature": w["temperature"]}
-            self.out = dict(accept_len=torch.empty(R, dtype=torch.int32, device=device),
-                            tokens=torch.empty(R, k + 1, dtype=torch.int32, device=device),
-                            status=torch.empty(R, dtype=torch.int32, device=device),
-                            tv=torch.empty(R, k, dtype=torch.float32, device=device),
-                            p_draft=torch.empty(R, k, dtype=torch.float32, device=device),
-                            q_draft=torch.empty(R, k, dtype=torch.float32, device=device))
-            self.ws = torch.empty(sv.verify_sample_workspace(R, k, V, Vd), dtype=torch.uint8, device=device)
-            # the d2t map is a constant of the draft model: its device plan is built once, here
-            self.plan = sv.d2t_plan(w["d2t"], V)
-            self.launches = sv.LAUNCHES["verify_sample"]
-            self.kernel = "sample_rows_fast_kernel + race_rows_kernel<bf16,bf16>"
-            self.kernel_file = "sample.cu"
-            self.profile = "sample_rows_d2t.md"
-            self.desc = (f"d2t: {R} requests x 7 drafts (+bonus) over V=151936 bf16, draft vocab 32000 bf16 via "
-                         f"d2t, T=0.7 ({self.logit_bytes / 1e9:.3f} GB of logits per step; d2t plan built once "
-                         f"per draft model, outside the step)")
-            self.metric = "verify+sample logit GB/s (speculative sampling, d2t 32000 -> 151936, bf16)"
-        else:  # cfg
+            if self.sweep:
+                self.desc = (f"sweep point: {R} requests x (8 drafts + bonus) over V=151936 {dt}, half greedy, half "
+                             f"sampled at T 0.6 / 1.0 with the d2t draft model (32000 ids) "
+                             f"({self.logit_bytes / 1e9:.3f} GB of logits per call)")
+                self.metric = f"verify+sample logit GB/s (sweep, {dt}, batch {R})"
+            else:
+                self.desc = (f"d2t: {R} requests x 7 drafts (+bonus) over V=151936 bf16, draft vocab 32000 bf16 "
+                             f"via d2t, T=0.7 ({self.logit_bytes / 1e9:.3f} GB of logits per step; d2t plan built "
+                             f"once per draft model, outside the step)")
+                self.metric = "verify+sample logit GB/s (speculative sampling, d2t 32000 -> 151936, bf16)"
+        elif name == "cfg":
             w = workloads.cfg_workload(device=device, R=sessions or 256)
             R, k, S, W = w["R"], w["k"], w["S"], w["W"]
             self.rows = R * (k + 1) * S
             self.logit_bytes = 2 * R * (k + 1) * S * W * 2 + R * k * S * W * 2
             self.inputs = {"cond": w["cond"], "uncond": w["uncond"], "draft_logits": w["draft_logits"],
                            "draft": w["draft"], "seeds": w["seeds"], "temperature": w["temperature"]}
-            self.out = dict(accept_len=torch.empty(R, dtype=torch.int32, device=device),
-                            tokens=torch.empty(R, k + 1, S, dtype=torch.int32, device=device),
-                            status=torch.empty(R, dtype=torch.int32, device=device),
-                            tv=torch.empty(R, k, S, dtype=torch.float32, device=device))
-            self.ws = torch.empty(sv.cfg_merge_sample_workspace(R, k, S, W), dtype=torch.uint8, device=device)
-            self.launches = sv.LAUNCHES["cfg_merge_sample"]
-            self.kernel = "cfg_rows_kernel + cfg_race_kernel"
-            self.kernel_file = "cfg.cu"
-            self.profile = "cfg_rows_cfg.md"
+            self.dtype = "bf16"
             self.desc = (f"cfg: {R} requests x {k} drafted frames (+1) x {S} codebooks of {W} bf16 entries, "
                          f"conditional + unconditional rows merged with w={w['w']}, T=1 "
                          f"({self.logit_bytes / 1e9:.3f} GB of logits per step)")
             self.metric = "CFG merge + verify logit GB/s (9 RVQ codebooks x 4096, bf16)"
-        self.w = w
-        if torch.cuda.is_available():
-            torch.cuda.empty_cache()  # drop the generator's fp32 temporaries
-
-    def call(self, inp, stream):
-        w = self.w
-        if self.name == "listen":
-            self.sv.verify_greedy(inp["target"], w["R"], w["k"], 2, inp["draft"], out=self.out, workspace=self.ws,
-                                  stream=stream)
-        elif self.name == "listen_top2":
-            self.sv.verify_greedy_top2(inp["target"], w["R"], w["k"], 2, inp["draft"], out=self.out,
-                                       workspace=self.ws, stream=stream)
-        elif self.name == "cfg":
-            self.sv.cfg_merge_sample(inp["cond"], inp["uncond"], w["cb_id_base"], w["cb_data_offset"], w["S"],
-                                     w["W"], w["w"], inp["draft_logits"], w["R"], w["k"], inp["draft"],
-                                     inp["seeds"], inp["temperature"], out=self.out, workspace=self.ws,
-                                     stream=stream)
         else:
-            self.sv.verify_sample(inp["target"], inp["draft_logits"], None, w["R"], w["k"], inp["draft"],
-                                  inp["seeds"], inp["temperature"], out=self.out, workspace=self.ws, stream=stream,
-                                  plan=self.plan)
+            raise ValueError(name)
+        self.w = w
+        self._h = None
 
-    def _host(self):
-        """CPU copies of the inputs for the oracle (made once)."""
-        if getattr(self, "_h", None) is None:
+    # ---- the oracle side (host copies made once) ----
+    def host(self):
+        if self._h is None:
             import numpy as np
 
             import workloads
 
             w = self.w
             if self.name == "cfg":
-                self._h = {"cond": workloads.host_rows(w["cond"]), "uncond": workloads.host_rows(w["uncond"]),
-                           "draft_logits": workloads.host_rows(w["draft_logits"]), "draft": w["draft"].cpu().numpy(),
-                           "seeds": w["seeds"].cpu().numpy().view(np.uint64), "T": w["temperature"].cpu().numpy()}
-                return self._h
-            h = {"target": workloads.host_rows(w["target"]), "draft": w["draft"].cpu().numpy()}
-            if self.name not in ("listen", "listen_top2"):
-                h["draft_logits"] = workloads.host_rows(w["draft_logits"])
-                h["d2t"] = w["d2t"].cpu().numpy()
+                h = {"cond": workloads.host_rows(w["cond"]), "uncond": workloads.host_rows(w["uncond"]),
+                     "draft_logits": workloads.host_rows(w["draft_logits"])}
+            else:
+                h = {"target": workloads.host_rows(w["target"])}
+                if self.name not in ("listen", "listen_top2"):
+                    h["draft_logits"] = workloads.host_rows(w["draft_logits"])
+                    h["d2t"] = w["d2t"].cpu().numpy()
+            h["draft"] = w["draft"].cpu().numpy()
+            if "seeds" in w:
                 h["seeds"] = w["seeds"].cpu().numpy().view(np.uint64)
                 h["T"] = w["temperature"].cpu().numpy()
             self._h = h
         return self._h
 
     def oracle_one(self, r):
-        """Run the oracle on request r; returns (logit bytes, rows) it covered."""
+        """The oracle on request r: (its outputs, logit bytes, rows)."""
         import oracle
 
-        w, h = self.w, self._host()
+        w, h = self.w, self.host()
         k = w["k"]
         r = r % w["R"]
         if self.name in ("listen", "listen_top2"):
             rpr = 2 * k + 1
-            oracle.verify_greedy(h["target"][r * rpr:(r + 1) * rpr], 1, k, 2, h["draft"][r:r + 1])
+            out = oracle.verify_greedy(h["target"][r * rpr:(r + 1) * rpr], 1, k, 2, h["draft"][r:r + 1])
             if self.name == "listen_top2":
                 oracle.top2_rows(h["target"][r * rpr:(r + 1) * rpr])
-            return rpr * w["V"] * 2, rpr
+            return out, rpr * w["V"] * 2, rpr
         if self.name == "cfg":
             S, W = w["S"], w["W"]
             rr = (k + 1) * S
-            oracle.cfg_merge_sample(h["cond"][r * rr:(r + 1) * rr], h["uncond"][r * rr:(r + 1) * rr],
-                                    w["cb_id_base"], w["cb_data_offset"], S, W, w["w"],
-                                    h["draft_logits"][r * k * S:(r + 1) * k * S], 1, k, h["draft"][r:r + 1],
-                                    h["seeds"][r:r + 1], h["T"][r:r + 1])
-            return 2 * rr * W * 2 + k * S * W * 2, rr
-        oracle.verify_sample(h["target"][r * (k + 1):(r + 1) * (k + 1)], h["draft_logits"][r * k:(r + 1) * k],
-                             h["d2t"], 1, k, h["draft"][r:r + 1], h["seeds"][r:r + 1], h["T"][r:r + 1])
-        return (k + 1) * w["V"] * 2 + k * w["Vd"] * 2, k + 1
+            out = oracle.cfg_merge_sample(h["cond"][r * rr:(r + 1) * rr], h["uncond"][r * rr:(r + 1) * rr],
+                                          w["cb_id_base"], w["cb_data_offset"], S, W, w["w"],
+                                          h["draft_logits"][r * k * S:(r + 1) * k * S], 1, k, h["draft"][r:r + 1],
+                                          h["seeds"][r:r + 1], h["T"][r:r + 1])
+            return out, 2 * rr * W * 2 + k * S * W * 2, rr
+        es = h["target"].itemsize
+        out = oracle.verify_sample(h["target"][r * (k + 1):(r + 1) * (k + 1)], h["draft_logits"][r * k:(r + 1) * k],
+                                   h["d2t"], 1, k, h["draft"][r:r + 1], h["seeds"][r:r + 1], h["T"][r:r + 1])
+        sampled = h["T"][r] > 0
+        return out, (k + 1) * w["V"] * es + (k * w["Vd"] * es if sampled else 0), k + 1
 
-    def oracle_sample(self, seconds):
-        """(GB/s, rows/s, requests, seconds) of the oracle over about `seconds` of requests."""
-        self._host()
-        done = nbytes = nrows = 0
+    def oracle_requests(self, requests, threads):
+        """The oracle over the given requests on `threads` host threads (the oracle is C called
+        through ctypes, which releases the GIL): outputs concatenated in request order, bytes,
+        rows, seconds."""
+        import concurrent.futures as cf
+
+        import numpy as np
+
+        self.host()
+        if not requests:
+            return {}, 0, 0, 0.0
         t0 = time.perf_counter()
-        while True:
-            b, rr = self.oracle_one(done)
-            done += 1
+        if threads > 1:
+            with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+                res = list(ex.map(self.oracle_one, requests))
+        else:
+            res = [self.oracle_one(r) for r in requests]
+        el = time.perf_counter() - t0
+        outs = {key: np.concatenate([o[key] for o, _, _ in res]) for key in res[0][0]}
+        return outs, sum(b for _, b, _ in res), sum(n for _, _, n in res), el
+
+    def oracle_sample(self, seconds, threads):
+        """(GB/s, rows/s, requests, seconds) of the oracle over about `seconds` of requests,
+        processed in rounds of `threads` requests at once."""
+        self.host()
+        done = nbytes = nrows = 0
+        el = 0.0
+        while el < seconds:
+            _, b, n, t = self.oracle_requests(list(range(done, done + threads)), threads)
+            done += threads
             nbytes += b
-            nrows += rr
-            el = time.perf_counter() - t0
-            if el >= seconds:
-                break
+            nrows += n
+            el += t
         return nbytes / el / 1e9, nrows / el, done, el
+
+
+class Native:
+    """The library call of one step on a Spec's device inputs: outputs, workspace, plan."""
+
+    def __init__(self, spec, sv, device):
+        import torch
+
+        self.spec, self.sv = spec, sv
+        w = spec.w
+        R, k = w["R"], w["k"]
+        i32 = dict(dtype=torch.int32, device=device)
+        self.plan = None
+        self.kernel_file, self.profile = None, None
+        if spec.name in ("listen", "listen_top2"):
+            self.out = dict(accept_len=torch.empty(R, **i32), tokens=torch.empty(R, k + 1, **i32),
+                            branch=torch.empty(R, **i32), status=torch.empty(R, **i32))
+            if spec.name == "listen":
+                self.ws = torch.empty(sv.verify_greedy_workspace(R, k, 2, w["V"]), dtype=torch.uint8, device=device)
+                self.launches = sv.LAUNCHES["verify_greedy"]
+                self.kernel, self.profile = "argmax_segments_kernel<bf16>", "argmax_segments_listen.md"
+            else:
+                self.out["top2"] = torch.empty(spec.rows, 2, **i32)
+                self.ws = torch.empty(sv.verify_greedy_top2_workspace(R, k, 2, w["V"]), dtype=torch.uint8,
+                                      device=device)
+                self.launches = sv.LAUNCHES["verify_greedy_top2"]
+                self.kernel, self.profile = "argmax_segments_kernel<bf16, top-2>", "argmax_segments_listen_top2.md"
+            self.kernel_file = "greedy.cu"
+        elif spec.name == "cfg":
+            S, W = w["S"], w["W"]
+            self.out = dict(accept_len=torch.empty(R, **i32), tokens=torch.empty(R, k + 1, S, **i32),
+                            status=torch.empty(R, **i32),
+                            tv=torch.empty(R, k, S, dtype=torch.float32, device=device))
+            self.ws = torch.empty(sv.cfg_merge_sample_workspace(R, k, S, W), dtype=torch.uint8, device=device)
+            self.launches = sv.LAUNCHES["cfg_merge_sample"]
+            self.kernel, self.kernel_file, self.profile = "cfg_rows_warp_kernel + cfg_race_kernel", "cfg.cu", \
+                "cfg_rows_cfg.md"
+        else:
+            f32 = dict(dtype=torch.float32, device=device)
+            self.out = dict(accept_len=torch.empty(R, **i32), tokens=torch.empty(R, k + 1, **i32),
+                            status=torch.empty(R, **i32), tv=torch.empty(R, k, **f32),
+                            p_draft=torch.empty(R, k, **f32), q_draft=torch.empty(R, k, **f32))
+            self.ws = torch.empty(sv.verify_sample_workspace(R, k, w["V"], w["Vd"]), dtype=torch.uint8,
+                                  device=device)
+            # the d2t map is a constant of the draft model: its device plan is built once, here
+            self.plan = sv.d2t_plan(w["d2t"], w["V"])
+            self.launches = sv.LAUNCHES["verify_sample"]
+            self.kernel, self.kernel_file = "sample_rows_fast_kernel + race_flat_kernel", "sample.cu"
+            self.profile = "sample_rows_d2t.md" if spec.name == "d2t" else None
+
+    def call(self, inp, stream):
+        w, sv = self.spec.w, self.sv
+        name = self.spec.name
+        if name == "listen":
+            sv.verify_greedy(inp["target"], w["R"], w["k"], 2, inp["draft"], out=self.out, workspace=self.ws,
+                             stream=stream)
+        elif name == "listen_top2":
+            sv.verify_greedy_top2(inp["target"], w["R"], w["k"], 2, inp["draft"], out=self.out, workspace=self.ws,
+                                  stream=stream)
+        elif name == "cfg":
+            sv.cfg_merge_sample(inp["cond"], inp["uncond"], w["cb_id_base"], w["cb_data_offset"], w["S"], w["W"],
+                                w["w"], inp["draft_logits"], w["R"], w["k"], inp["draft"], inp["seeds"],
+                                inp["temperature"], out=self.out, workspace=self.ws, stream=stream)
+        else:
+            sv.verify_sample(inp["target"], inp["draft_logits"], None, w["R"], w["k"], inp["draft"], inp["seeds"],
+                             inp["temperature"], out=self.out, workspace=self.ws, stream=stream, plan=self.plan)
+
+
+def _timed_calls(fn, steps, stream, flush):
+    """Mean ms per call over `steps` calls on `stream`, each in its own CUDA events; with
+    `flush`, an L2 flush (a write larger than L2) precedes every call outside its events;
+    without, the calls run back to back inside one pair of events."""
+    import torch
+
+    if flush is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for f0_, f1_ in ev:
+        flush.add_(1)
+        f0_.record(stream)
+        fn()
+        f1_.record(stream)
+    ev[-1][1].synchronize()
+    return sum(f0_.elapsed_time(f1_) for f0_, f1_ in ev) / steps
+
+
+def _sampling_stats(spec, out):
+    """The pages' acceptance metrics of one call's outputs: per-position acceptance 1 - TV
+    averaged over the sampled requests (raw_tv's complement; for CFG averaged over the
+    codebooks too) and the mean accept length (drafts accepted per call)."""
+    import numpy as np
+
+    tv = out["tv"].float().cpu().numpy()
+    n = out["accept_len"].cpu().numpy()
+    T = spec.w["temperature"].cpu().numpy()
+    s = T > 0
+    tvs = tv[s].reshape(int(s.sum()), spec.w["k"], -1)
+    return {"alpha_per_position": [round(float(a), 4) for a in 1.0 - tvs.mean(axis=(0, 2))],
+            "mean_accept_len": float(n[s].mean()), "sampled_requests": int(s.sum())}
 
 
 def _traffic_from_profile(kernel_file, profile):
@@ -355,8 +454,14 @@ def _traffic_from_profile(kernel_file, profile):
     return None
 
 
+def _oracle_threads():
+    return max(1, os.cpu_count() or 1)
+
+
 def run_reference(a):
-    """Reference arm: the fp64 CPU oracle as it stands, one request per step."""
+    """Reference arm: the fp64 CPU oracle as it stands, on the host cores.  It loads the
+    oracle only: the inputs come from the seeded generator (torch), never from the CUDA
+    library."""
     world, rank = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
@@ -367,31 +472,33 @@ def run_reference(a):
     oracle.build()
     if a.workload == "pool":
         return _reference_pool(a, world)
-    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    dev = "cuda" if torch.cuda.is_available() else "cpu"  # the generator's device: the native arm's bytes
     # the sweep's oracle leg times the sampling workload's requests (same step definition)
-    wl = Workload("d2t" if a.workload == "sweep" else a.workload, dev, a.sessions)
-    # one request per step, timed as it stands
-    wl._host()
-    for s_ in range(a.warmup):
-        wl.oracle_one(s_)
+    spec = Spec("d2t" if a.workload == "sweep" else a.workload, dev, a.sessions)
+    spec.host()
+    threads = _oracle_threads()
+    # one step = one round of `threads` requests, one per host thread
+    spec.oracle_requests(list(range(threads * a.warmup)), threads)
     nbytes = nrows = 0
-    t0 = time.perf_counter()
+    el = 0.0
     for s_ in range(a.steps):
-        b, rr = wl.oracle_one(a.warmup + s_)
+        lo = threads * (a.warmup + s_)
+        _, b, n, t = spec.oracle_requests(list(range(lo, lo + threads)), threads)
         nbytes += b
-        nrows += rr
-    el = time.perf_counter() - t0
+        nrows += n
+        el += t
     gbs = nbytes / el / 1e9
-    done = a.steps
+    done = a.steps * threads
     line = {
-        "impl": "reference", "metric": wl.metric,
+        "impl": "reference", "metric": spec.metric,
         "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
         "ms_per_step": el / a.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.desc, "step": "one request of the workload through the CPU oracle",
+        "config": {"workload": spec.desc,
+                   "step": f"{threads} requests of the workload through the CPU oracle, one per host thread",
                    "l2": "n/a (CPU)"},
-        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{done} requests of the {a.workload} workload, one per step"},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{done} requests of the {a.workload} workload, {threads} per step"},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "rows_per_s": nrows / el,
     }
@@ -442,6 +549,57 @@ def _reference_pool(a, world):
     return 0
 
 
+SUB_WORKLOADS = ("d2t", "cfg", "sweep_bf16_b1024", "sweep_bf16_b256")
+
+
+def _roofline(spec, nat, ms, peak, peak_kind):
+    achieved = spec.logit_bytes / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
+            "traffic": _traffic_from_profile(nat.kernel_file, nat.profile) if nat.profile else None,
+            "kernel": f"{nat.kernel} (all kernels of one call inside the same events)",
+            "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+            else "fallback 6.8 TB/s"}
+
+
+def _sub_record(name, sv, device, stream, steps, warmup, peak, peak_kind, flush, threads):
+    """One sub-workload: timed calls (an L2 flush before every call), its roofline, the pages'
+    acceptance metrics, and the oracle over every request for the exempt-row count."""
+    import torch
+
+    import oracle
+
+    spec = Spec(name, device)
+    nat = Native(spec, sv, device)
+    fn = lambda: nat.call(spec.inputs, stream)  # noqa: E731
+    for _ in range(max(warmup, 3)):
+        fn()
+    torch.cuda.synchronize()
+    ms = _timed_calls(fn, steps, stream, flush)
+    rec = {"metric": spec.metric, "value": spec.logit_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s",
+           "us_per_call": ms * 1e3, "rows_per_s": spec.rows / (ms * 1e-3), "steps": steps,
+           "workload": spec.desc, "l2": "flushed before every call, outside the timed events",
+           "roofline": _roofline(spec, nat, ms, peak, peak_kind), "gpu_launches": steps * nat.launches}
+    rec.update(_sampling_stats(spec, nat.out))
+    # the oracle over the sampled requests: parity of tokens / accept lengths / status and the
+    # rows whose decision margin is below 1e-6 (exempt from exact parity)
+    T = spec.w["temperature"].cpu().numpy()
+    req = [r for r in range(spec.w["R"]) if T[r] > 0]
+    want, _, _, el = spec.oracle_requests(req, threads)
+    got = {key: v.cpu().numpy()[req] for key, v in nat.out.items()}
+    ex = oracle.exempt_rows(want)
+    diff = (got["accept_len"] != want["accept_len"]) | np.any(
+        got["tokens"].reshape(len(req), -1) != want["tokens"].reshape(len(req), -1), axis=1) | (
+        got["status"] != want["status"])
+    rec.update({"rows_checked": int(ex.size), "exempt_rows": int(ex.sum()),
+                "requests_checked": len(req), "requests_differing": int(diff.sum()),
+                "requests_differing_not_exempt": int((diff & ~ex.any(axis=1)).sum()),
+                "oracle_seconds": round(el, 2), "oracle_threads": threads})
+    del nat, spec
+    torch.cuda.empty_cache()
+    return rec
+
+
 def run_native(a):
     import torch
 
@@ -458,60 +616,60 @@ def run_native(a):
     _barrier(world)
     sv.load()
 
-    wl = Workload(a.workload, device, a.sessions)
+    spec = Spec(a.workload, device, a.sessions)
+    nat = Native(spec, sv, device)
+    if torch.cuda.is_available():
+        torch.cuda.empty_cache()  # drop the generator's fp32 temporaries
     stream = torch.cuda.current_stream(device)
 
     for _ in range(max(a.warmup, 3)):
-        wl.call(wl.inputs, stream)
+        nat.call(spec.inputs, stream)
     torch.cuda.synchronize()
     clocks = Clocks(local)
     clocks.start()
     # Inputs below four L2s get an L2 flush before every step, outside the events: the row
     # pass keeps the draft rows in L2 on purpose (for its TV pass), and back-to-back steps
     # would otherwise find them there.  Larger inputs run back to back.
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device) if wl.logit_bytes < 4 * L2_BYTES else None
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     _barrier(world)
     torch.cuda.synchronize()
-    if flush is None:
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(a.steps):
-            wl.call(wl.inputs, stream)
-        e1.record(stream)
-        e1.synchronize()
-        ms_local = e0.elapsed_time(e1) / a.steps
-    else:
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
-        for f0_, f1_ in ev:
-            flush.add_(1)
-            f0_.record(stream)
-            wl.call(wl.inputs, stream)
-            f1_.record(stream)
-        ev[-1][1].synchronize()
-        ms_local = sum(f0_.elapsed_time(f1_) for f0_, f1_ in ev) / a.steps
+    ms_local = _timed_calls(lambda: nat.call(spec.inputs, stream), a.steps, stream,
+                            flush if spec.logit_bytes < 4 * L2_BYTES else None)
     _barrier(world)
     torch.cuda.synchronize()
+    ms = _max_over_ranks(ms_local, world, device)
+    value = world * spec.logit_bytes / (ms * 1e-3) / 1e9
+    rows_per_s = world * spec.rows / (ms * 1e-3)
+    peak, peak_kind = _peaks()
+    roofline = _roofline(spec, nat, ms_local, peak, peak_kind)
+    threads = _oracle_threads()
+
+    # the sampling half of the metric: sub-records on the same box, in the same clock record
+    subs = {}
+    if rank == 0 and a.workload == "listen" and not a.no_sub:
+        for name in SUB_WORKLOADS:
+            subs[name] = _sub_record(name, sv, device, stream, max(3, min(a.steps, a.sub_steps)), a.warmup, peak,
+                                     peak_kind, flush, threads)
     clock_rows = clocks.stop()
     del flush
-    ms = _max_over_ranks(ms_local, world, device)
-    value = world * wl.logit_bytes / (ms * 1e-3) / 1e9
-    rows_per_s = world * wl.rows / (ms * 1e-3)
 
     # end to end: pinned host inputs in, results out, every step
     e2e_steps = max(3, min(a.steps, 20))
     h_in = {}
-    for key, t in wl.inputs.items():
+    for key, t in spec.inputs.items():
+        if t is None:
+            continue
         h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
         h.copy_(t)
         h_in[key] = h
-    d_in = {key: torch.empty_like(t) for key, t in wl.inputs.items()}
-    h_out = {key: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for key, v in wl.out.items()}
+    d_in = {key: torch.empty_like(t) for key, t in h_in.items()}
+    h_out = {key: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for key, v in nat.out.items()}
 
     def e2e_step():
         for key in d_in:
             d_in[key].copy_(h_in[key], non_blocking=True)
-        wl.call(d_in, stream)
-        for key, v in wl.out.items():
+        nat.call(d_in, stream)
+        for key, v in nat.out.items():
             h_out[key].copy_(v, non_blocking=True)
 
     for _ in range(2):
@@ -528,35 +686,30 @@ def run_native(a):
     e2e_ms = _max_over_ranks(f0.elapsed_time(f1) / e2e_steps, world, device)
     h2d = sum(h.numel() * h.element_size() for h in h_in.values())
     d2h = sum(v.numel() * v.element_size() for v in h_out.values())
-    e2e_value = world * wl.logit_bytes / (e2e_ms * 1e-3) / 1e9
+    e2e_value = world * spec.logit_bytes / (e2e_ms * 1e-3) / 1e9
     del h_in, d_in
-
-    peak, peak_kind = _peaks()
-    achieved = wl.logit_bytes / (ms_local * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
-                "traffic": _traffic_from_profile(wl.kernel_file, wl.profile),
-                "kernel": f"{wl.kernel} (all kernels of one call inside the same events)",
-                "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-                else "fallback 6.8 TB/s"}
 
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
-        gbs, rps, done, el = wl.oracle_sample(a.cpu_seconds)
-        cpu = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"{done} requests of the {a.workload} workload, {el:.1f} s, single-threaded fp64 C",
-               "rows_per_s": rps, "host_cores": os.cpu_count()}
+        g1, r1, d1, e1 = spec.oracle_sample(a.cpu_seconds / 2, 1)
+        gn, rn, dn, en = spec.oracle_sample(a.cpu_seconds / 2, threads)
+        cpu = {"value": gn, "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"{dn} requests of the {a.workload} workload in {en:.1f} s on {threads} host threads "
+                         f"(one request per thread at a time), fp64 C as it stands",
+               "rows_per_s": rn, "host_cores": os.cpu_count(),
+               "single_thread": {"value": g1, "unit": "GB/s", "cores": 1, "rows_per_s": r1,
+                                 "sample": f"{d1} requests in {e1:.1f} s"}}
 
     if rank == 0:
         line = {
-            "metric": wl.metric,
+            "metric": spec.metric,
             "value": value, "unit": "GB/s", "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": wl.desc,
-                       "l2": (f"inputs ({wl.logit_bytes / 1e9:.3f} GB) larger than 4 x L2 (129 MB); no flush"
-                              if wl.logit_bytes >= 4 * L2_BYTES else
-                              f"inputs ({wl.logit_bytes / 1e9:.3f} GB) below 4 x L2: L2 flushed before every "
+            "dtype": spec.dtype, "data": "synthetic",
+            "config": {"workload": spec.desc,
+                       "l2": (f"inputs ({spec.logit_bytes / 1e9:.3f} GB) larger than 4 x L2 (129 MB); no flush"
+                              if spec.logit_bytes >= 4 * L2_BYTES else
+                              f"inputs ({spec.logit_bytes / 1e9:.3f} GB) below 4 x L2: L2 flushed before every "
                               f"step, outside the timed events"),
                        "parallelism": f"replicas x{world}"},
             "rows_per_s": rows_per_s,
@@ -564,9 +717,12 @@ def run_native(a):
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps},
-            "gpu_launches": a.steps * wl.launches,
+            "gpu_launches": a.steps * nat.launches,
             "clocks": Clocks.summarize(clock_rows),
         }
+        if subs:
+            line["sub"] = subs
+            line["gpu_launches_sub"] = sum(r["gpu_launches"] for r in subs.values())
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -598,18 +754,15 @@ def run_sweep(a):
     peak, peak_kind = _peaks()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
     k, V, Vd = 8, workloads.V_QWEN, workloads.VD_DRAFT
-    sigma = list(workloads.D2T_SIGMA) + [workloads.D2T_SIGMA[-1]]
     steps = max(3, min(a.steps, 50))
     points = []
     clocks = Clocks(local)
     clocks.start()
     for dt, es in ((torch.bfloat16, 2), (torch.float32, 4)):
-        for B in (1, 8, 64, 256, 1024):
-            T = [0.0 if r % 2 == 0 else (0.6 if (r // 2) % 2 == 0 else 1.0) for r in range(B)]
-            w = workloads.sample_batch(B, k, V, Vd, dt, T=T, sigma_pos=sigma, delta=workloads.D2T_DELTA,
-                                       z_sigma=3.0, seed=1300 + B, seed_base=5000, device=device)
+        for B in workloads.SWEEP_BATCHES:
+            w = workloads.sweep_batch(B, dt, device=device)
             plan = sv.d2t_plan(w["d2t"], V)
-            nsamp = sum(1 for t in T if t > 0)
+            nsamp = int((w["temperature"] > 0).sum().item())
             nbytes = B * (k + 1) * V * es + nsamp * k * Vd * es
             out = dict(accept_len=torch.empty(B, dtype=torch.int32, device=device),
                        tokens=torch.empty(B, k + 1, dtype=torch.int32, device=device),

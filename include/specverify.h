@@ -193,11 +193,13 @@ int sv_infer_modality(sv_rows logits, int32_t N, const int32_t* part_start, int3
  * Arguments, outputs and results are those of sv_verify_greedy.  The scratch
  * lives in a fixed device array of SV_NOALLOC_SCRATCH_BYTES compiled into the
  * library; every GPU that loads the library keeps it until the process exits.
- *  - Batches whose workspace (sv_verify_greedy_workspace) exceeds that size
- *    are rejected with SV_ERR_LIMIT before anything is launched.
- *  - The first call on a device looks up the array's device address for that
- *    device (cudaGetSymbolAddress with the device current); make that first
- *    call before any stream capture.
+ *  - Argument errors are those of sv_verify_greedy, checked in its order.
+ *    Batches whose workspace (sv_verify_greedy_workspace) exceeds that size
+ *    are then rejected with SV_ERR_LIMIT before anything is launched.
+ *  - Every call looks up the array's device address on the current device
+ *    (cudaGetSymbolAddress with that device current).  The first call on a
+ *    device may also load the library's device code: make that first call
+ *    before any stream capture.
  *  - All calls share the one array.  Calls that overlap on the GPU (other
  *    streams, other host threads) race on it and give wrong results;
  *    serialise them.  The array keeps the last call's contents, which no

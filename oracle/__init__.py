@@ -281,3 +281,24 @@ def cfg_merge_sample(cond, uncond, cb_id_base, cb_data_offset, S: int, W: int, w
         raise ValueError(f"oracle rejected the arguments ({rc})")
     return dict(accept_len=acc_len, tokens=tokens, tv=tv, status=status, accept_margin=am,
                 race_margin=rm)
+
+
+MARGIN = 1e-6  # decision margin below which a row is exempt from exact parity
+
+
+def exempt_rows(out: dict) -> np.ndarray:
+    """Boolean [R, rows per request] mask of the rows of a verify_sample / cfg_merge_sample
+    result whose decision margin is below MARGIN: tested positions with |u - p/q| < MARGIN,
+    and the row the race ran on (the first rejected position, or the bonus row: index
+    accept_len) when its two smallest keys are within MARGIN (relative).  CFG results
+    ([R, k + 1, S] tokens) give one row per (frame, codebook)."""
+    n = np.asarray(out["accept_len"])
+    R = len(n)
+    tok = np.asarray(out["tokens"])
+    k1 = tok.shape[1]
+    S = tok.shape[2] if tok.ndim == 3 else 1
+    mask = np.zeros((R, k1, S), bool)
+    if k1 > 1:
+        mask[:, : k1 - 1] |= np.asarray(out["accept_margin"]).reshape(R, k1 - 1, S) < MARGIN
+    mask[np.arange(R), n] |= np.asarray(out["race_margin"]).reshape(R, S) < MARGIN
+    return mask.reshape(R, -1)

@@ -10,16 +10,14 @@
 //                  fmaf(w, c - u, u) (packed fp32 pairs, the same roundings);
 //                  pass 1 takes the merged row's argmax and online max /
 //                  sum-exp at T and the draft row's; pass 2 (the slices again,
-//                  from L2) TV = sum max(0, q - p), p, q at the drafted id and
-//                  the residual weight of every 256-id race chunk; then the
-//                  accept test (Philox row j * S + s).
-// cfg_race_kernel  one warp per (request, codebook): the first
-//                  frame n with a rejected codebook, then for codebook s its
-//                  draft if its own test passed, else the two-level residual
-//                  race at frame n (or the bonus race at frame k): the chunk
-//                  from the chunk sums, then the id inside that chunk, its
-//                  weights rebuilt from the inputs.  Codebook 0 also writes
-//                  accept_len.
+//                  from L2) TV = sum max(0, q - p) and p, q at the drafted id;
+//                  then the accept test (Philox row j * S + s).
+// cfg_race_kernel  one CTA per (request, codebook): the first frame n with a
+//                  rejected codebook, then for codebook s its draft if its own
+//                  test passed, else the exponential race over the codebook's
+//                  ids of the residual at frame n (or of p at the bonus frame
+//                  k), its weights rebuilt from the inputs.  Codebook 0 also
+//                  writes accept_len.
 #include <algorithm>
 #include <cfloat>
 #include <climits>
@@ -32,9 +30,6 @@ namespace sv {
 namespace {
 
 constexpr int32_t kCfgMaxW = 16384;  // widest codebook
-constexpr int32_t kCfgChunk = 256;   // ids per chunk of the two-level race (one 8-id group per lane of a warp)
-constexpr int32_t kCfgMaxChunks = kCfgMaxW / kCfgChunk;
-static_assert(kCfgChunk == 8 * 32, "a race chunk is one 8-id group of every lane of a warp");
 constexpr float kLog2eC = 1.4426950408889634f;
 
 enum : uint32_t { kCfgBad = 1u, kCfgOffSupport = 2u };
@@ -65,8 +60,6 @@ struct CfgArgs {
     float* tv;
     int32_t* status;
     CfgStat* stats;
-    float* wchunk;    // [units][nchunk]: sum of max(0, p - q) per race chunk of each drafted row
-    int32_t nchunk;   // race chunks per row
 };
 
 
@@ -335,9 +328,6 @@ __global__ void __launch_bounds__(32 * kCfgWarpRows, 4) cfg_rows_warp_kernel(Cfg
 #pragma unroll
                     for (int h = 0; h < 4; ++h) y2[4 * i + h] = grp_pair<DD>(yg[i], h);
                 if (b + 1 < nb) load(b + 1);
-                unsigned long long r2[kG];  // per group (one race chunk): sum of max(0, p - q)
-#pragma unroll
-                for (int i = 0; i < kG; ++i) r2[i] = 0ull;
 #pragma unroll
                 for (int p = 0; p < kP; ++p) {
                     float a0, a1, b0, b1;
@@ -350,7 +340,6 @@ __global__ void __launch_bounds__(32 * kCfgWarpRows, 4) cfg_rows_warp_kernel(Cfg
                     const int32_t x = 8 * (lane + 32 * (kG * b + p / 4)) + 2 * (p % 4);
                     // ids beyond W hold p = 0 and q of a -inf logit = 0
                     t2 = add2(t2, pack2(fmaxf(d0, 0.f), fmaxf(d1, 0.f)));
-                    r2[p / 4] = add2(r2[p / 4], pack2(fmaxf(-d0, 0.f), fmaxf(-d1, 0.f)));
                     if ((xl & ~1) == x) {
                         float p0, p1, q0, q1;
                         unpack2(p2, p0, p1);
@@ -358,15 +347,6 @@ __global__ void __launch_bounds__(32 * kCfgWarpRows, 4) cfg_rows_warp_kernel(Cfg
                         pxl = (xl & 1) ? p1 : p0;
                         qxl = (xl & 1) ? q1 : q0;
                     }
-                }
-                // the residual weight of each race chunk of the batch, for the race kernel
-#pragma unroll
-                for (int i = 0; i < kG; ++i) {
-                    float a0, a1;
-                    unpack2(r2[i], a0, a1);
-                    const float wc = wsum(a0 + a1);
-                    const int32_t ch = kG * b + i;
-                    if (lane == 0 && ch < A.nchunk) A.wchunk[unit * A.nchunk + ch] = wc;
                 }
             }
             float t;
@@ -401,25 +381,32 @@ __global__ void __launch_bounds__(32 * kCfgWarpRows, 4) cfg_rows_warp_kernel(Cfg
     }
 }
 
-// One warp per (request, codebook), sixteen resident per SM: it finds the first frame n
-// with a rejected codebook (or, greedy, a mismatching one); then codebook s's token
-// at frame n: its draft if its own test passed, else the two-level residual race at
-// frame n (the bonus race at frame k).  The chunk weights of the residual come from
-// the row pass; p's chunk sums (bonus, or no residual mass) are taken here, one
-// 256-id chunk at a time.  Then the chunk race and the element race inside the
-// drawn chunk, its weights rebuilt from the inputs; then the codebook's tokens.  Codebook 0 writes accept_len; the codebooks' status bits meet in an
-// atomic OR on a status word the row pass zeroed.
-constexpr int kCfgRaceWarps = 1;
+// One CTA of kCfgRaceThreads per (request, codebook): warp 0 finds the first frame
+// n with a rejected codebook (or, greedy, a mismatching one); then codebook s's
+// token at frame n: its draft if its own test passed, else the exponential race
+// over the codebook's W ids of the residual max(0, p - q) at frame n (p at the
+// bonus frame k).  The weights are rebuilt from the inputs into shared memory;
+// the key of the heaviest id bounds the minimum key B, so a Philox block is
+// generated only when one of its ids has B w >= 2^-24 and a logarithm is taken
+// only when 1 - u <= B w (both widened against fp32 rounding).  Codebook 0
+// writes accept_len; the codebooks' status bits meet in an atomic OR on a
+// status word the row pass zeroed.
+constexpr int kCfgRaceThreads = 128;
+constexpr float kCfgRaceSlack = 1.0f + 1.0f / 1024.0f;
+constexpr float kCfgRaceMinGap = 5.9604645e-8f;  // 2^-24: the smallest 1 - u
 
 template <int DT, int DD>
-__global__ void __launch_bounds__(32 * kCfgRaceWarps, 16) cfg_race_kernel(CfgArgs A)
+__global__ void __launch_bounds__(kCfgRaceThreads) cfg_race_kernel(CfgArgs A)
 {
     pdl_wait_primary();
-    __shared__ float wc_s[kCfgMaxChunks];  // the race chunks' weight sums
-    __shared__ int32_t tok_s;
+    extern __shared__ __align__(16) float wbuf[];  // the race weights, W rounded up to 8
+    __shared__ float hv_s[kCfgRaceThreads / 32];
+    __shared__ int32_t hx_s[kCfgRaceThreads / 32];
+    __shared__ unsigned long long kb_s[kCfgRaceThreads / 32];
+    __shared__ float bound_s;
     __shared__ int32_t n_s;
     __shared__ uint32_t fl_s;
-    const int lane = threadIdx.x & 31, wq = threadIdx.x >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, wq = tid >> 5;
     const int32_t S = A.shape.S, W = A.shape.W, k = A.k;
     const int32_t r = static_cast<int32_t>(blockIdx.x / S);
     const int32_t s = static_cast<int32_t>(blockIdx.x - static_cast<int64_t>(r) * S);
@@ -459,9 +446,6 @@ __global__ void __launch_bounds__(32 * kCfgRaceWarps, 16) cfg_race_kernel(CfgArg
     } else if (n < k && sn.accept) {
         tok_local = d[n * S + s] - A.shape.id_base[s];
     } else {
-        // two-level race at frame n over the residual max(0, p - q) or the bonus p: the chunk
-        // by a race over the chunk sums (uniforms of the chunk tag counted by the chunk), then
-        // the id by a race inside that chunk (uniforms of the id tag counted by the id)
         const bool residual = n < k;
         const float c = kLog2eC / T;
         const unsigned long long w2 = pack2(A.shape.w, A.shape.w), c2 = pack2(c, c);
@@ -474,119 +458,127 @@ __global__ void __launch_bounds__(32 * kCfgRaceWarps, 16) cfg_race_kernel(CfgArg
         const char* up = A.ubase + off;
         const char* dp = residual ? A.dbase + ((static_cast<int64_t>(r) * k + n) * S + s) * A.dstride : nullptr;
         const bool cvec = A.cvec != 0, dvec = A.dvec != 0;
-        const int32_t nch = A.nchunk;
         const PhiloxKey key = philox_key(A.seeds[r]);
         const uint32_t prow = static_cast<uint32_t>(n * S + s);
-        // weights of ids [e0, e0 + 8): p, or max(0, p - q) with wres (0 at and beyond W)
-        auto weights8 = [&](int32_t e0, bool wres, float* wt) {
-            Grp<DT> cg, ug;
-            Grp<DD> yg;
-            ld_grp<DT>(cp, e0, W, cvec, cg);
-            ld_grp<DT>(up, e0, W, cvec, ug);
-            if (wres) ld_grp<DD>(dp, e0, W, dvec, yg);
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const unsigned long long u2 = grp_pair<DT>(ug, h);
-                const unsigned long long m2 = fma2(w2, sub2(grp_pair<DT>(cg, h), u2), u2);
-                float a0, a1;
-                unpack2(fma2(m2, c2, nm2), a0, a1);
-                unsigned long long p2 = mul2(pack2(ex2(a0), ex2(a1)), iS2);
-                if (wres) {
-                    float b0, b1;
-                    unpack2(fma2(grp_pair<DD>(yg, h), c2, nd2), b0, b1);
-                    p2 = sub2(p2, mul2(pack2(ex2(b0), ex2(b1)), iQ2));
-                }
-                unpack2(p2, wt[2 * h], wt[2 * h + 1]);
-            }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) wt[e] = (e0 + e < W && wt[e] > 0.f) ? wt[e] : 0.f;  // NaN never wins
-        };
+        const uint32_t tag = residual ? kTagResidual : kTagBonus;
+        const int32_t ngroups = (W + 7) / 8;
         for (int pass = 0; pass < 2; ++pass) {  // pass 1: no residual mass, draw from p
             const bool wres = residual && pass == 0;
-            // ---- chunk weights: the row pass left the residual's; p's are summed here ----
-            if (wres) {
-                for (int32_t ch = threadIdx.x; ch < nch; ch += 32 * kCfgRaceWarps) wc_s[ch] = A.wchunk[row * nch + ch];
-            } else {
-                for (int32_t ch = wq; ch < nch; ch += kCfgRaceWarps) {
-                    float wt[8];
-                    weights8(ch * kCfgChunk + 8 * lane, false, wt);
-                    const float v = wsum(((wt[0] + wt[1]) + (wt[2] + wt[3])) + ((wt[4] + wt[5]) + (wt[6] + wt[7])));
-                    if (lane == 0) wc_s[ch] = v;
-                }
-            }
-            __syncthreads();
-            if (wq == 0) {
-                // ---- chunk race (warp 0): lowest E_c / W_c, lowest chunk among equal keys ----
-                const uint32_t tag_c = residual ? kTagResidualChunk : kTagBonusChunk;
-                float nk = -INFINITY;
-                int32_t cb = INT32_MAX;
-                for (int32_t ch = lane; ch < nch; ch += 32) {
-                    const float wc = wc_s[ch];
-                    if (!(wc > 0.f)) continue;
-                    const uint4 w4 = philox_block(key, static_cast<uint32_t>(ch >> 2), prow, tag_c);
-                    const uint32_t wd = (ch & 3) == 0 ? w4.x : ((ch & 3) == 1 ? w4.y : ((ch & 3) == 2 ? w4.z : w4.w));
-                    const float kc = __fdiv_rn(-log1pf(-one_minus_uniform_from_word(wd)), wc);
-                    if (-kc > nk) {  // ascending chunks within the lane
-                        nk = -kc;
-                        cb = ch;
+            // ---- weights into shared memory; every thread's heaviest id ----
+            float hw = 0.f;
+            int32_t hx = INT32_MAX;
+            for (int32_t g = tid; g < ngroups; g += kCfgRaceThreads) {
+                const int32_t e0 = 8 * g;
+                Grp<DT> cg, ug;
+                Grp<DD> yg;
+                ld_grp<DT>(cp, e0, W, cvec, cg);
+                ld_grp<DT>(up, e0, W, cvec, ug);
+                if (wres) ld_grp<DD>(dp, e0, W, dvec, yg);
+                float wt[8];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const unsigned long long u2 = grp_pair<DT>(ug, h);
+                    const unsigned long long m2 = fma2(w2, sub2(grp_pair<DT>(cg, h), u2), u2);
+                    float a0, a1;
+                    unpack2(fma2(m2, c2, nm2), a0, a1);
+                    unsigned long long p2 = mul2(pack2(ex2(a0), ex2(a1)), iS2);
+                    if (wres) {
+                        float b0, b1;
+                        unpack2(fma2(grp_pair<DD>(yg, h), c2, nd2), b0, b1);
+                        p2 = sub2(p2, mul2(pack2(ex2(b0), ex2(b1)), iQ2));
                     }
+                    unpack2(p2, wt[2 * h], wt[2 * h + 1]);
                 }
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const float ov = __shfl_xor_sync(0xffffffffu, nk, o);
-                    const int32_t ox = __shfl_xor_sync(0xffffffffu, cb, o);
-                    if (ov > nk || (ov == nk && ox < cb)) {
-                        nk = ov;
-                        cb = ox;
+                for (int e = 0; e < 8; ++e) {
+                    wt[e] = (e0 + e < W && wt[e] > 0.f) ? wt[e] : 0.f;  // NaN never wins
+                    if (wt[e] > hw) {  // ascending ids within the thread
+                        hw = wt[e];
+                        hx = e0 + e;
                     }
                 }
+                reinterpret_cast<float4*>(wbuf + e0)[0] = make_float4(wt[0], wt[1], wt[2], wt[3]);
+                reinterpret_cast<float4*>(wbuf + e0)[1] = make_float4(wt[4], wt[5], wt[6], wt[7]);
+            }
+            // ---- the heaviest id of the row and its key: the bound B ----
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, hw, o);
+                const int32_t ox = __shfl_xor_sync(0xffffffffu, hx, o);
+                if (ov > hw || (ov == hw && ox < hx)) {
+                    hw = ov;
+                    hx = ox;
+                }
+            }
+            if (lane == 0) {
+                hv_s[wq] = hw;
+                hx_s[wq] = hx;
+            }
+            __syncthreads();
+            if (tid == 0) {
+                float bw = 0.f;
                 int32_t bx = INT32_MAX;
-                if (cb != INT32_MAX) {
-                    // ---- element race inside chunk cb: eight ids (two Philox blocks) per lane ----
-                    const uint32_t tag = residual ? kTagResidual : kTagBonus;
-                    const int32_t e0 = cb * kCfgChunk + 8 * lane;
-                    float wt[8];
-                    weights8(e0, wres, wt);
-                    float best = INFINITY;
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const uint4 w4 = philox_block(key, static_cast<uint32_t>((e0 >> 2) + hh), prow, tag);
-                        const uint32_t words[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float wv = wt[4 * hh + e];
-                            if (!(wv > 0.f)) continue;
-                            const float v = one_minus_uniform_from_word(words[e]);
-                            if (!(v < best * wv)) continue;  // E = -ln(1 - v) >= v
-                            const float key2 = __fdiv_rn(-log1pf(-v), wv);
-                            if (key2 < best) {  // ascending ids within the lane
-                                best = key2;
-                                bx = e0 + 4 * hh + e;
-                            }
-                        }
+                for (int i = 0; i < kCfgRaceThreads / 32; ++i)
+                    if (hv_s[i] > bw || (hv_s[i] == bw && hx_s[i] < bx)) {
+                        bw = hv_s[i];
+                        bx = hx_s[i];
                     }
-                    float nb2 = bx == INT32_MAX ? -INFINITY : -best;
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        const float ov = __shfl_xor_sync(0xffffffffu, nb2, o);
-                        const int32_t ox = __shfl_xor_sync(0xffffffffu, bx, o);
-                        if (ov > nb2 || (ov == nb2 && ox < bx)) {
-                            nb2 = ov;
-                            bx = ox;
-                        }
-                    }
-                    if (bx == INT32_MAX) bx = cb * kCfgChunk;  // no weight left after rounding
+                float b = INFINITY;
+                if (bw > 0.f && bx != INT32_MAX) {
+                    const uint4 w4 = philox_block(key, static_cast<uint32_t>(bx) >> 2, prow, tag);
+                    const uint32_t wd = (bx & 3) == 0 ? w4.x : (bx & 3) == 1 ? w4.y : (bx & 3) == 2 ? w4.z : w4.w;
+                    b = __fdiv_rn(-log1pf(-one_minus_uniform_from_word(wd)), bw);
                 }
-                if (lane == 0) tok_s = bx;
+                bound_s = b;
             }
             __syncthreads();
-            const int32_t bx = tok_s;
-            __syncthreads();  // wc_s and tok_s are written again by a second pass
-            if (bx != INT32_MAX || !residual) {
-                tok_local = bx == INT32_MAX ? 0 : bx;
-                break;
+            const float B = bound_s;
+            if (!(B < INFINITY)) {  // no weight anywhere (block-uniform)
+                if (!residual || pass == 1) break;
+                status |= SV_ST_RESIDUAL_ZERO;
+                __syncthreads();  // wbuf and the shared arrays are written again
+                continue;
             }
-            status |= SV_ST_RESIDUAL_ZERO;
+            // ---- the race: blocks of four ids, one Philox block each when one of them can win ----
+            const float bs = B * kCfgRaceSlack;
+            float best = INFINITY;
+            int32_t bx = INT32_MAX;
+            for (int32_t b4 = tid; 4 * b4 < W; b4 += kCfgRaceThreads) {
+                const float4 wv = reinterpret_cast<const float4*>(wbuf)[b4];
+                const float w4v[4] = {wv.x, wv.y, wv.z, wv.w};
+                bool need = false;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) need |= w4v[e] * bs >= kCfgRaceMinGap;
+                if (!need) continue;
+                const uint4 u4 = philox_block(key, static_cast<uint32_t>(b4), prow, tag);
+                const uint32_t words[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float w = w4v[e];
+                    if (!(w > 0.f)) continue;
+                    const float om = one_minus_uniform_from_word(words[e]);
+                    if (!(om <= w * bs)) continue;
+                    const float kx = __fdiv_rn(-log1pf(-om), w);
+                    if (kx < best) {  // ascending ids within the thread
+                        best = kx;
+                        bx = 4 * b4 + e;
+                    }
+                }
+            }
+            unsigned long long pk = bx == INT32_MAX ? ~0ull
+                                                     : (static_cast<unsigned long long>(__float_as_uint(best)) << 32) |
+                                                           static_cast<uint32_t>(bx);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const unsigned long long ov = __shfl_xor_sync(0xffffffffu, pk, o);
+                pk = ov < pk ? ov : pk;
+            }
+            if (lane == 0) kb_s[wq] = pk;
+            __syncthreads();
+            unsigned long long m = ~0ull;
+            for (int i = 0; i < kCfgRaceThreads / 32; ++i) m = kb_s[i] < m ? kb_s[i] : m;
+            tok_local = m == ~0ull ? 0 : static_cast<int32_t>(m & 0xFFFFFFFFu);
+            break;
         }
         if (residual && (sn.flags & kCfgOffSupport)) status |= SV_ST_OFF_SUPPORT;
     }
@@ -621,8 +613,8 @@ static int64_t cfg_stats_bytes(int64_t R, int32_t k, int32_t S)
 
 size_t cfg_workspace_bytes(int64_t R, int32_t k, int32_t S, int32_t W)
 {
-    const int64_t nchunk = (static_cast<int64_t>(W) + kCfgChunk - 1) / kCfgChunk;
-    return static_cast<size_t>(cfg_stats_bytes(R, k, S) + R * (k + 1) * S * nchunk * 4 + 256);
+    (void)W;
+    return static_cast<size_t>(cfg_stats_bytes(R, k, S) + 256);
 }
 
 template <int DT, int DD>
@@ -637,9 +629,13 @@ static cudaError_t launch_cfg_t(const CfgArgs& A, int32_t R, int32_t k, cudaStre
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
+    const size_t wsmem = static_cast<size_t>((A.shape.W + 7) / 8) * 8 * sizeof(float);
+    e = cudaFuncSetAttribute(cfg_race_kernel<DT, DD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(wsmem));
+    if (e != cudaSuccess) return e;
     cfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(R) * A.shape.S));
-    cfg.blockDim = dim3(32 * kCfgRaceWarps);
-    cfg.dynamicSmemBytes = 0;
+    cfg.blockDim = dim3(kCfgRaceThreads);
+    cfg.dynamicSmemBytes = wsmem;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -676,8 +672,6 @@ cudaError_t launch_cfg_merge_sample(const Rows& cond, const Rows& uncond, const 
     A.tv = tv;
     A.status = status;
     A.stats = static_cast<CfgStat*>(workspace);
-    A.nchunk = (shape.W + kCfgChunk - 1) / kCfgChunk;
-    A.wchunk = reinterpret_cast<float*>(static_cast<char*>(workspace) + cfg_stats_bytes(R, k, shape.S));
     const bool cb = cond.dtype == SV_BF16;
     const bool db = draft_logits == nullptr || draft_logits->dtype == SV_BF16;
     if (cb && db) return launch_cfg_t<SV_BF16, SV_BF16>(A, R, k, stream);

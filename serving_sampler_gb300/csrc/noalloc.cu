@@ -11,39 +11,32 @@
 //
 // The array is a file-scope __device__ object: every GPU that loads the
 // library holds SV_NOALLOC_SCRATCH_BYTES of it until the process exits.  In
-// host code its name is only a stand-in, so the device address is fetched
-// with cudaGetSymbolAddress once per device (on the first call made with that
-// device current) and that address is what the kernels receive.
-#include <mutex>
-
+// host code its name is only a stand-in, so every call looks up the array's
+// device address on the current device with cudaGetSymbolAddress (no
+// allocation, and no address kept across calls that a device reset could
+// invalidate) and hands that address to the kernels.
 #include <cuda_runtime.h>
 
 #include "specverify.h"
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-
 static __device__ __align__(256) unsigned char g_greedy_scratch[SV_NOALLOC_SCRATCH_BYTES];
-
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
 
 // device address of the scratch array on the current device
 int scratch_address(void** out)
 {
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SV_ERR_DEVICE;
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_addr[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_greedy_scratch) != cudaSuccess || p == nullptr) {
-            (void)cudaGetLastError();  // leave no sticky launch error behind
-            return SV_ERR_DEVICE;
-        }
-        g_scratch_addr[dev] = p;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+        (void)cudaGetLastError();
+        return SV_ERR_DEVICE;
     }
-    *out = g_scratch_addr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_greedy_scratch) != cudaSuccess || p == nullptr) {
+        (void)cudaGetLastError();  // leave no sticky launch error behind
+        return SV_ERR_DEVICE;
+    }
+    *out = p;
     return SV_OK;
 }
 
@@ -53,11 +46,11 @@ extern "C" int sv_verify_greedy_noalloc(sv_rows target, int32_t R, int32_t k, in
                                         const int32_t* draft, int32_t* accept_len, int32_t* tokens,
                                         int32_t* branch, int32_t* status, sv_stream_t stream)
 {
-    if (R < 0 || k < 0 || branches < 1 || branches > SV_MAX_BRANCHES || (branches >= 2 && k < 1) ||
-        target.width < 1)
-        return SV_ERR_INVALID_ARG;
-    if (k > SV_MAX_K) return SV_ERR_LIMIT;
-    if (R == 0) return SV_OK;
+    // sv_verify_greedy's own argument checks, in its order: without a workspace it stops at
+    // the workspace check, after every argument check and before anything is launched
+    const int pre = sv_verify_greedy(target, R, k, branches, draft, accept_len, tokens, branch, status,
+                                     nullptr, 0, stream);
+    if (pre != SV_ERR_WORKSPACE) return pre;  // an argument error, or SV_OK for R == 0
     const size_t need = sv_verify_greedy_workspace(R, k, branches, target.width);
     if (need == 0) return SV_ERR_INVALID_ARG;
     if (need > SV_NOALLOC_SCRATCH_BYTES) return SV_ERR_LIMIT;  // batch too large for the fixed array

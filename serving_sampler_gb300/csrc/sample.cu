@@ -14,16 +14,16 @@
 //                      path): persistent CTAs, one (request, position)
 //                      unit at a time.  The draft and target rows stream
 //                      through bulk-copied shared-memory stages: max, sum-exp
-//                      at T, argmax, NaN/inf flags, z at the support positions
-//                      (G), and on the fast path each target chunk's (max,
-//                      sum) for the race.  A second pass over G and the draft
+//                      at T, argmax, NaN/inf flags and z at the support
+//                      positions (G).  A second pass over G and the draft
 //                      row gives TV over the full vocabulary, p(x_j), q(x_j)
 //                      and the accept test u_j < p/q.
-//   race_rows_kernel   one CTA per request: the accept-length scan, then on
-//                      the one selected row (residual max(0, p - q) at the
-//                      first rejection, or p at the bonus row) the chunk and
-//                      the id drawn by exponential races with Philox uniforms;
-//                      it commits the tokens.
+//   race_flat_kernel   work items of (request, 4096-id slice): the
+//                      accept-length scan, then on the one selected row
+//                      (residual max(0, p - q) at the first rejection, or p at
+//                      the bonus row) the exponential race over every id with
+//                      Philox uniforms, pruned by a bound shared by the
+//                      request's items; the last item commits the tokens.
 // Temperature scaling works in log2 units: with c = log2(e) / T,
 // p(x) = 2^(z_x c - M) / S where M = max_x z_x c and S = sum 2^(z c - M).
 #include <algorithm>
@@ -95,14 +95,28 @@ struct SampleArgs {
     int32_t* tokens;
     int32_t* status;
     RowStat* stats;
-    float2* cstat;       // [units][target chunks] (reference r, sum 2^(z c - r)) per chunk, or NULL
-    int32_t nct;         // target chunks per row
+    // per request, reset by the row pass: the race's bound (fp32 bits), its packed (key, id)
+    // minimum and the count of finished work items
+    unsigned int* race_bound;
+    unsigned long long* race_best;
+    unsigned int* race_done;
     char* gslots;        // global-memory Y / G buffers when they do not fit in shared memory
     int64_t gslot_bytes;
     int smem_mode;
 };
 
 __host__ __device__ inline int64_t align256(int64_t b) { return (b + 255) / 256 * 256; }
+
+// the race's per-request board for this call: the row pass resets it, the race
+// kernel (launched after the row pass has completed) uses it
+__device__ __forceinline__ void reset_race_board(const SampleArgs& A)
+{
+    for (int32_t r = blockIdx.x * blockDim.x + threadIdx.x; r < A.R; r += gridDim.x * blockDim.x) {
+        A.race_bound[r] = 0x7F800000u;  // +inf
+        A.race_best[r] = ~0ull;
+        A.race_done[r] = 0u;
+    }
+}
 
 template <int DT>
 __device__ __forceinline__ float ld_elem(const char* p, int64_t e)
@@ -454,6 +468,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) sample_rows_kernel(SampleArgs 
     const int tid = threadIdx.x;
 
     pdl_launch_dependents();
+    reset_race_board(A);
 
     // resident buffers of the draft row (Y, draft dtype) and of the target
     // logits at the support positions (G, target dtype)
@@ -1192,6 +1207,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
 
     pdl_wait_primary();  // a plan built in the same call must be complete
     pdl_launch_dependents();
+    reset_race_board(A);
     if (tid == 0) {
         for (int i = 0; i < kS * kStreamWarps; ++i) mbar_init(&bars[i], 1);
         for (int b = 0; b < kNG; ++b) {
@@ -1261,7 +1277,6 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                 // support entries of a target chunk: this lane's groups of four packed pairs, from
                 // L2 while the maxima and exponentials below run
                 const bool scatter = u.has_draft && plan_ok;
-                float csum = 0.f;  // this lane's share of the chunk's sum, relative to its running max
                 int32_t p0 = 0, p1 = 0;
                 if (scatter) {
                     p0 = cidx * (kMaxGroups * 32);  // the chunk's slots: whole groups of four
@@ -1313,12 +1328,9 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                         if (mt > tm) {  // warp-uniform
                             const float sc = tm == -INFINITY ? 0.f : ex2(tm - mt);
                             ts *= sc;
-                            csum *= sc;
                             tm = mt;
                         }
-                        const float add = lm > -INFINITY ? acc * ex2(lr - tm) : 0.f;
-                        csum += add;
-                        ts += add;
+                        ts += lm > -INFINITY ? acc * ex2(lr - tm) : 0.f;
                     }
                 }
                 if (scatter) {
@@ -1365,13 +1377,6 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                 ++consumed;
                 if (lane == 0) fence_proxy_async_smem();
                 producer_step<DT>(A, P, consumed, w, lane, units, wst, wbar, pol_t);
-                if (u.sampling) {
-                    // this chunk's (reference, sum) for the race
-                    float cs = csum;
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) cs += __shfl_xor_sync(0xffffffffu, cs, o);
-                    if (lane == 0) A.cstat[unit * A.nct + cidx] = make_float2(tm, cs);
-                }
             }
             T = T_next;
 
@@ -1615,70 +1620,35 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
         }
         mbar_arrive(&freed[b]);
     }
-}// ---------------------------------------------------------------------------
-// scan + two-level race + commit
+}
+// ---------------------------------------------------------------------------
+// scan + race + commit
 // ---------------------------------------------------------------------------
 // The correction token is a draw from w / sum(w), w = max(0, p - q) on the
-// first rejected row (p on the bonus row).  It is taken as an exponential race
-// in two levels: the ids are cut into chunks of kRaceChunk, the chunk is drawn
-// by a race over the chunk sums W_c (uniforms of the chunk tag, counted by c),
-// then the id by a race over that chunk only (uniforms of the element tag,
-// counted by the id).  P(chunk) = W_c / sum W and P(id | chunk) = w / W_c, so
-// the draw is exact, and only one chunk's uniforms are ever generated.
+// first rejected row (p on the bonus row), taken as one exponential race over
+// the whole row: argmin over the ids with w_x > 0 of E_x / w_x, E_x = -ln u_x,
+// u_x the Philox uniform of id x (counter (x >> 2, row, tag, 0), word x & 3).
 //
-// race_rows_kernel: one CTA per request.  The accept-length scan, one pass over
-// the selected row that sums w and p per chunk (each warp's vectors lie in one
-// chunk; q of a support id through the plan's draft-id map from the L1-resident
-// draft row), the chunk race, the element race inside the drawn chunk, commit.
+// race_flat_kernel: work items (request, slice of kRaceSlice ids), a grid-stride
+// loop of CTAs of kRaceThreads.  Every item scans the request's accept flags for
+// n (greedy requests are committed by their slice 0); a sampled request's item
+// computes the weights of its slice in registers, takes the exact keys of its
+// warps' heaviest ids, and publishes the smallest as a bound B of the row's
+// minimum key (atomicMin over the request's items).  A key E_x / w_x <= B needs
+// 1 - u_x <= E_x <= B w_x, so a Philox block is generated only when one of its
+// four ids has B w_x >= 2^-24 (the smallest 1 - u there is), and a logarithm is
+// taken only for ids with 1 - u_x <= B w_x; both tests are widened by
+// kRaceSlack against fp32 rounding, so no id that can win is skipped and the
+// winner does not depend on which bound an item saw.  Each item's (key, id)
+// minimum goes into the request's packed 64-bit minimum (lowest key, then
+// lowest id); the item that finishes last commits the tokens.
 namespace {
 
-constexpr int32_t kRaceChunk = 2048;
-constexpr int kRaceMinThreads = 512;  // the race CTA: 1024 threads, or 512 (two per SM) for many requests
-constexpr int kRaceInFlight = 4;  // 8-id vectors per thread loaded together
-constexpr int kWarpsPerChunk = kRaceChunk / 8 / 32;              // 8
-constexpr int kEvalChunks = 8;  // chunks summed together by the bounded chunk race
-// 8-id vectors per thread of a round with NT threads
-template <int NT>
-__host__ __device__ constexpr int eval_vecs() { return kRaceChunk / 8 / (NT / kEvalChunks); }
-static_assert(kRaceChunk == kChunkElems, "the row pass leaves one (max, sum) per race chunk");
-static_assert(kRaceChunk % (8 * 32) == 0, "a warp's 32 vectors lie in one chunk");
-static_assert(SV_MAX_K < kRaceMinThreads, "one thread per draft position");
-static_assert(eval_vecs<1024>() % 2 == 0 && eval_vecs<kRaceMinThreads>() % 2 == 0, "vectors two at a time");
-static_assert(kRaceChunk / 4 <= kRaceMinThreads, "the element race: four ids per thread");
-constexpr int kWbufSlots = 4;  // chunks of a round (the lowest bounds) whose weights are kept
-
-// Dynamic shared memory of the race kernel, sized by the request's positions and
-// chunks: row statistics, then for the bounded race the selected row's chunk sums,
-// bounds, E_c, bound order, the kept weights and the selected draft row; for the
-// full race the per-warp chunk partials.
-struct RaceSmem {
-    uint32_t st, cst, lb, ec, order, wbuf, ybuf, wpart, ppart, total;
-};
-
-__host__ __device__ inline RaceSmem race_smem_layout(int32_t k, int32_t nc, int32_t Vd, bool bounded)
-{
-    RaceSmem L{};
-    uint32_t off = 0;
-    auto take = [&](uint32_t bytes) {
-        const uint32_t o = off;
-        off += (bytes + 15u) & ~15u;
-        return o;
-    };
-    L.st = take(static_cast<uint32_t>(k + 1) * static_cast<uint32_t>(sizeof(RowStat)));
-    if (bounded) {
-        L.cst = take(static_cast<uint32_t>(nc) * 8u);
-        L.lb = take(static_cast<uint32_t>(nc) * 4u);
-        L.ec = take(static_cast<uint32_t>(nc) * 4u);
-        L.order = take(static_cast<uint32_t>(nc) * 4u);
-        L.wbuf = take(static_cast<uint32_t>(kWbufSlots) * kRaceChunk * 4u);
-        L.ybuf = take(static_cast<uint32_t>(Vd) * 2u);
-    } else {
-        L.wpart = take(static_cast<uint32_t>(nc) * kWarpsPerChunk * 4u);
-        L.ppart = take(static_cast<uint32_t>(nc) * kWarpsPerChunk * 4u);
-    }
-    L.total = off;
-    return L;
-}
+constexpr int kRaceThreads = 256;
+constexpr int kRaceVecs = 2;                                      // 8-id vectors per thread
+constexpr int32_t kRaceSlice = kRaceThreads * kRaceVecs * 8;      // 4096 ids per work item
+constexpr float kRaceSlack = 1.0f + 1.0f / 1024.0f;
+constexpr float kRaceMinGap = 5.9604645e-8f;                      // 2^-24: the smallest 1 - u
 
 // z[0..8) of ids [x, x + 8) of a row (-inf at and beyond x_end; NaN read as -inf)
 template <int DT>
@@ -1724,12 +1694,12 @@ __device__ __forceinline__ void load_jmap8(const D2tPlan& pl, int32_t x, int32_t
 
 // q at target ids [x, x + 8): 2^(y c - mq) / Sq at the draft id of each, 0 off the support
 template <int DD>
-__device__ __forceinline__ void q8(const SampleArgs& A, const char* drow, int32_t x, int32_t x_end, bool dvec_ok,
-                                   float c, float mq, float invSq, float* q)
+__device__ __forceinline__ void q8(const SampleArgs& A, const char* drow, int32_t x, bool dvec_ok, float c,
+                                   float mq, float invSq, float* q)
 {
     float y[8];
     if (A.identity) {
-        load8<DD>(drow, x, min(x_end, A.Vd), dvec_ok, y);
+        load8<DD>(drow, x, A.Vd, dvec_ok, y);
     } else {
         uint32_t jm[8];
         load_jmap8(A.plan, x, A.V, jm);
@@ -1743,520 +1713,261 @@ __device__ __forceinline__ void q8(const SampleArgs& A, const char* drow, int32_
     for (int e = 0; e < 8; ++e) q[e] = ex2(fmaf(y[e], c, -mq)) * invSq;
 }
 
-// (key, id) minimum over the block, lowest id among equal keys; threads
-// without a candidate pass (+inf, INT32_MAX)
-template <int NT>
-__device__ __forceinline__ void block_argmin_key(float& key, int32_t& id, float* sf, int32_t* si)
+// the uniform's complement 1 - u_x and the key E_x / w of id x
+__device__ __forceinline__ float race_key(float om, float w) { return __fdiv_rn(-log1pf(-om), w); }
+
+// (key bits, id) packed so that the unsigned minimum is the lowest key, then the lowest id;
+// keys are positive, so their bits order like the keys
+__device__ __forceinline__ unsigned long long pack_key(float key, int32_t id)
 {
-    float nk = id == INT32_MAX ? -INFINITY : -key;
-    block_argmax<NT>(nk, id, sf, si);
-    key = -nk;
+    return (static_cast<unsigned long long>(__float_as_uint(key)) << 32) | static_cast<uint32_t>(id);
+}
+constexpr unsigned long long kNoKey = ~0ull;
+
+__device__ __forceinline__ unsigned long long warp_min_u64(unsigned long long v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long ov = __shfl_xor_sync(0xffffffffu, v, o);
+        v = ov < v ? ov : v;
+    }
+    return v;
+}
+
+// What a race over one row needs.
+struct RaceRow {
+    const char* trow;
+    const char* drow;   // the draft row (residual weights only)
+    float c, m, invS, mq, invSq;
+    PhiloxKey key;
+    uint32_t row, tag;
+};
+
+// the CTA's shared scratch of race_slice
+struct RaceShared {
+    float wkey[kRaceThreads / 32];                 // key of each warp's heaviest id
+    unsigned long long best[kRaceThreads / 32];    // each warp's (key, id) minimum
+    float bound;
+};
+
+// One slice [x0, x0 + kRaceSlice) of the race: the weights (residual max(0, p - q) when
+// `resid`, else p), a bound from the warps' heaviest ids (lowered to *bound_g when given,
+// which also receives this slice's bound), then the pruned race.  Returns the slice's
+// packed (key, id) minimum to every thread.
+template <int DT, int DD>
+__device__ unsigned long long race_slice(const SampleArgs& A, const RaceRow& Rr, int32_t x0, bool resid,
+                                         unsigned int* bound_g, float bound_in, RaceShared& sh)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool vec_ok = A.tbulk != 0, dvec_ok = A.dbulk != 0;
+    float wv[kRaceVecs][8];
+    float hw = 0.f;  // this thread's heaviest weight and its id
+    int32_t hx = INT32_MAX;
+#pragma unroll
+    for (int v = 0; v < kRaceVecs; ++v) {
+        const int32_t x = x0 + 8 * (tid + kRaceThreads * v);
+        float z[8], q[8];
+        load8<DT>(Rr.trow, x, A.V, vec_ok, z);
+        if (resid) q8<DD>(A, Rr.drow, x, dvec_ok, Rr.c, Rr.mq, Rr.invSq, q);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float p = ex2(fmaf(z[e], Rr.c, -Rr.m)) * Rr.invS;
+            float w = resid ? fmaxf(p - q[e], 0.f) : p;
+            w = x + e < A.V ? w : 0.f;
+            wv[v][e] = w;
+            if (w > hw) {  // ascending ids: the first of equal weights
+                hw = w;
+                hx = x + e;
+            }
+        }
+    }
+    // the key of the warp's heaviest id
+    float nw = hw;
+    int32_t nx = hx;
+    warp_argmax(nw, nx);
+    if (lane == 0) {
+        float kh = INFINITY;
+        if (nw > 0.f && nx != INT32_MAX) {
+            const uint4 w4 = philox_block(Rr.key, static_cast<uint32_t>(nx) >> 2, Rr.row, Rr.tag);
+            const uint32_t wd = (nx & 3) == 0 ? w4.x : (nx & 3) == 1 ? w4.y : (nx & 3) == 2 ? w4.z : w4.w;
+            kh = race_key(one_minus_uniform_from_word(wd), nw);
+        }
+        sh.wkey[warp] = kh;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        float b = bound_in;
+        for (int i = 0; i < kRaceThreads / 32; ++i) b = fminf(b, sh.wkey[i]);
+        if (bound_g != nullptr && b < INFINITY) {
+            const unsigned int old = atomicMin(bound_g, __float_as_uint(b));
+            b = fminf(b, __uint_as_float(old));
+        }
+        sh.bound = b;
+    }
+    __syncthreads();
+    const float bs = sh.bound * kRaceSlack;
+    float best = INFINITY;
+    int32_t bx = INT32_MAX;
+#pragma unroll
+    for (int v = 0; v < kRaceVecs; ++v) {
+        const int32_t x = x0 + 8 * (tid + kRaceThreads * v);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            bool need = false;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) need |= wv[v][4 * h + e] * bs >= kRaceMinGap;
+            if (!need) continue;
+            const uint4 w4 = philox_block(Rr.key, static_cast<uint32_t>(x >> 2) + h, Rr.row, Rr.tag);
+            const uint32_t words[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float w = wv[v][4 * h + e];
+                if (!(w > 0.f)) continue;
+                const float om = one_minus_uniform_from_word(words[e]);
+                if (!(om <= w * bs)) continue;
+                const float kx = race_key(om, w);
+                if (kx < best) {  // ascending ids within the thread
+                    best = kx;
+                    bx = x + 4 * h + e;
+                }
+            }
+        }
+    }
+    unsigned long long pk = bx == INT32_MAX ? kNoKey : pack_key(best, bx);
+    pk = warp_min_u64(pk);
+    if (lane == 0) sh.best[warp] = pk;
+    __syncthreads();
+    unsigned long long out = kNoKey;
+#pragma unroll
+    for (int i = 0; i < kRaceThreads / 32; ++i) out = sh.best[i] < out ? sh.best[i] : out;
+    __syncthreads();  // the shared arrays are written again by the next slice
+    return out;
 }
 
 }  // namespace
 
-template <int DT, int DD, int NT>
-__global__ void __launch_bounds__(NT, 1024 / NT) race_rows_kernel(SampleArgs A)
+template <int DT, int DD>
+__global__ void __launch_bounds__(kRaceThreads) race_flat_kernel(SampleArgs A)
 {
-    constexpr int kRaceWarps = NT / 32;
-    // The bounded race sums a round's chunks in the layout of a 1024-thread CTA whatever NT
-    // is (a 512-thread CTA takes two passes of virtual threads), so the sums, and the tokens
-    // they decide, do not depend on the CTA size.
-    constexpr int kVT = 1024;
-    constexpr int kVPass = kVT / NT;
-    constexpr int kEvalVecs = eval_vecs<kVT>();
-    pdl_wait_primary();
-    extern __shared__ __align__(16) unsigned char rsm[];  // laid out by race_smem_layout
-    __shared__ float bpart_s[kVT / 32];
-    __shared__ float best_s;
-    __shared__ int32_t bc_s, bslot_s, bround_s;  // best chunk, its slot and round in the bounded race
-    __shared__ float red_f[kRaceWarps];
-    __shared__ int32_t red_i[kRaceWarps];
-    __shared__ int32_t n_shared;
-    __shared__ uint32_t fl_shared;
-    __shared__ __align__(8) uint64_t ybar;  // the bulk copy of the selected draft row (bounded race)
+    __shared__ int32_t n_s, last_s;
+    __shared__ uint32_t fl_s;
+    __shared__ unsigned long long best_s;
+    __shared__ RaceShared sh;
+    __shared__ uint32_t red_u[kRaceThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31;
-    const int32_t r = static_cast<int32_t>(blockIdx.x);
     const int32_t k = A.k;
-    const RowStat* st = A.stats + static_cast<int64_t>(r) * (k + 1);
-    const int32_t* d = A.draft + static_cast<int64_t>(r) * k;
-    const float T = A.temp[r];
-    const int32_t nc = (A.V + kRaceChunk - 1) / kRaceChunk;
-    const RaceSmem L = race_smem_layout(k, nc, A.Vd, A.cstat != nullptr);
-    RowStat* st_s = reinterpret_cast<RowStat*>(rsm + L.st);           // the request's row statistics
-    float2* cst_s = reinterpret_cast<float2*>(rsm + L.cst);           // the selected row's chunk sums
-    float* lb_s = reinterpret_cast<float*>(rsm + L.lb);               // lower bounds of the chunk keys
-    float* ec_s = reinterpret_cast<float*>(rsm + L.ec);               // E_c of every chunk
-    int32_t* order_s = reinterpret_cast<int32_t*>(rsm + L.order);     // chunks in bound order
-    float* wbuf = reinterpret_cast<float*>(rsm + L.wbuf);             // [kWbufSlots][kRaceChunk] kept weights
-    uint16_t* ybuf = reinterpret_cast<uint16_t*>(rsm + L.ybuf);       // the selected draft row
-    float* wpart = reinterpret_cast<float*>(rsm + L.wpart);           // full race: [chunk][warp] sums of w
-    float* ppart = reinterpret_cast<float*>(rsm + L.ppart);           // and of p
-
-    // everything the scan and the bounded race read, requested at once: the row statistics,
-    // the draft tokens and, when they fit two per thread, the chunk sums of every row
-    if (tid <= k) st_s[tid] = st[tid];
-    const int32_t dj = tid < k ? d[tid] : 0;
-    const float2* cst_r = A.cstat ? A.cstat + static_cast<int64_t>(r) * (k + 1) * A.nct : nullptr;
-    const bool cpre = cst_r != nullptr && (k + 1) * nc <= 2 * NT;  // A.nct == nc
-    float2 cv0 = make_float2(0.f, 0.f), cv1 = make_float2(0.f, 0.f);
-    if (cpre) {
-        if (tid < (k + 1) * nc) cv0 = cst_r[tid];
-        if (tid + NT < (k + 1) * nc) cv1 = cst_r[tid + NT];
-    }
-    if (tid == 0) {
-        mbar_init(&ybar, 1);
-        fence_barrier_init();
-    }
-    __syncthreads();
-
-    // request-level decisions (warp 0, ballots)
-    if (tid < 32) {
-        uint32_t fl = 0;
-        for (int32_t j = lane; j <= k; j += 32) fl |= st_s[j].flags;
-        fl = __reduce_or_sync(0xffffffffu, fl);
-        const bool bad_rows = (fl & (kFlagNaN | kFlagPosInf | kFlagAllNegInf | kFlagDraftBad)) != 0;
-        const bool greedy = !(T > 0.f) || bad_rows;
-        int32_t n = k;
-        for (int32_t j0 = 0; j0 < k; j0 += 32) {
-            const int32_t j = j0 + lane;
-            const bool fail = j < k && (greedy ? d[j] != st_s[j].amax : st_s[j].accept == 0);
-            const unsigned m = __ballot_sync(0xffffffffu, fail);
-            if (m) {
-                n = j0 + __ffs(m) - 1;
-                break;
+    const int32_t nsl = (A.V + kRaceSlice - 1) / kRaceSlice;
+    const int64_t items = static_cast<int64_t>(A.R) * nsl;
+    pdl_wait_primary();
+    for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+        const int32_t r = static_cast<int32_t>(it / nsl);
+        const int32_t sl = static_cast<int32_t>(it - static_cast<int64_t>(r) * nsl);
+        const RowStat* st = A.stats + static_cast<int64_t>(r) * (k + 1);
+        const int32_t* d = A.draft + static_cast<int64_t>(r) * k;
+        const float T = A.temp[r];
+        // ---- the request's decisions (warp 0, ballots) ----
+        if (tid < 32) {
+            uint32_t fl = 0;
+            for (int32_t j = lane; j <= k; j += 32) fl |= st[j].flags;
+            fl = __reduce_or_sync(0xffffffffu, fl);
+            const bool bad_rows = (fl & (kFlagNaN | kFlagPosInf | kFlagAllNegInf | kFlagDraftBad)) != 0;
+            const bool greedy = !(T > 0.f) || bad_rows;
+            int32_t n = k;
+            for (int32_t j0 = 0; j0 < k; j0 += 32) {
+                const int32_t j = j0 + lane;
+                const bool fail = j < k && (greedy ? d[j] != st[j].amax : st[j].accept == 0);
+                const unsigned m = __ballot_sync(0xffffffffu, fail);
+                if (m) {
+                    n = j0 + __ffs(m) - 1;
+                    break;
+                }
             }
-        }
-        if (lane == 0) {
-            n_shared = n;
-            fl_shared = fl;
-        }
-    }
-    __syncthreads();
-    const int32_t n = n_shared;
-    const uint32_t fl = fl_shared;
-    const bool bad_rows = (fl & (kFlagNaN | kFlagPosInf | kFlagAllNegInf | kFlagDraftBad)) != 0;
-    const bool greedy = !(T > 0.f) || bad_rows;
-    int32_t token = -1;
-    uint32_t status = 0;
-    // bounded race on a rejected row: its draft row into shared memory, one bulk copy that lands
-    // while the chunk bounds are ranked (the bulk-copy path has 16-byte rows and Vd % 8 == 0)
-    const bool ycopy = DD == SV_BF16 && !greedy && cst_r != nullptr && n < k;
-    bool ywait = ycopy;  // the copy is still to be waited for
-    if (ycopy && tid == 0) {
-        const uint32_t yb_bytes = static_cast<uint32_t>(A.Vd) * 2;
-        mbar_arrive_expect_tx(&ybar, yb_bytes);
-        bulk_copy_g2s(ybuf, A.dbase + (static_cast<int64_t>(r) * k + n) * A.dstride, yb_bytes, &ybar,
-                      l2_policy_evict_first());
-    }
-    if (greedy) {
-        token = st_s[n].amax;
-    } else {
-        const bool residual = n < k;
-        const RowStat rs = st_s[n];
-        const float c = kLog2e / T, invS = 1.f / rs.s, invSq = residual ? 1.f / rs.sq : 0.f;
-        const char* trow = A.tbase + (static_cast<int64_t>(r) * (k + 1) + n) * A.tstride;
-        const char* drow = residual ? A.dbase + (static_cast<int64_t>(r) * k + n) * A.dstride : nullptr;
-        const bool vec_ok = A.tbulk != 0, dvec_ok = A.dbulk != 0;
-        const int32_t nvec = (A.V + 7) / 8;
-
-        const PhiloxKey key = philox_key(A.seeds[r]);
-        const uint32_t tag_c = residual ? kTagResidualChunk : kTagBonusChunk;
-        const uint32_t tag_x = residual ? kTagResidual : kTagBonus;
-        bool use_p = !residual;
-        int32_t bc = INT32_MAX;
-        int32_t bslot = -1;  // the slot of wbuf that holds chunk bc's weights, if any
-        if (A.cstat == nullptr) {
-        // ---- chunk sums of w and p: each warp's 32 vectors lie in one chunk ----
-        constexpr int kZW = DT == SV_BF16 ? 1 : 2;  // 16-byte words per 8-id vector
-        // the trip count is uniform across each warp (it depends on the warp's first vector),
-        // so every lane takes part in the shuffles below
-        for (int32_t v0 = tid; v0 - lane < nvec; v0 += NT * kRaceInFlight) {
-            // raw target words and draft-id words of every vector first, all in flight together
-            uint4 zr[kRaceInFlight][kZW];
-            uint4 jr[kRaceInFlight];
-#pragma unroll
-            for (int b = 0; b < kRaceInFlight; ++b) {
-                const int32_t x = (v0 + b * NT) * 8;
-                if (vec_ok && x + 8 <= A.V && x >= 0) {
-#pragma unroll
-                    for (int h = 0; h < kZW; ++h)
-                        zr[b][h] = ld_nc_v4(reinterpret_cast<const uint4*>(trow + static_cast<int64_t>(x) * (2 * kZW)) + h);
-                }
-                if (residual && !A.identity && x + 8 <= A.V)
-                    jr[b] = ld_nc_v4(reinterpret_cast<const uint4*>(A.plan.jmap + x));
-            }
-#pragma unroll
-            for (int b = 0; b < kRaceInFlight; ++b) {
-                const int32_t v = v0 + b * NT;
-                const int32_t vw = v - lane;  // the warp's first vector
-                if (vw >= nvec) break;
-                float ws = 0.f, ps = 0.f;
-                if (v < nvec) {
-                    const int32_t x = v * 8;
-                    float z[8];
-                    if (vec_ok && x + 8 <= A.V) {
-                        if constexpr (DT == SV_BF16) {
-                            const uint32_t wv[4] = {zr[b][0].x, zr[b][0].y, zr[b][0].z, zr[b][0].w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                z[2 * e] = bf16_lo(wv[e]);
-                                z[2 * e + 1] = bf16_hi(wv[e]);
-                            }
-                        } else {
-                            const uint32_t wv[8] = {zr[b][0].x, zr[b][0].y, zr[b][0].z, zr[b][0].w,
-                                                    zr[b][1].x, zr[b][1].y, zr[b][1].z, zr[b][1].w};
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) z[e] = __uint_as_float(wv[e]);
-                        }
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) z[e] = z[e] != z[e] ? -INFINITY : z[e];
-                    } else {
-                        load8<DT>(trow, x, A.V, false, z);
-                    }
-                    float q[8];
-                    if (residual) {
-                        if (A.identity) {
-                            q8<DD>(A, drow, x, A.V, dvec_ok, c, rs.mq, invSq, q);
-                        } else {
-                            uint32_t jm[8];
-                            if (x + 8 <= A.V) {
-                                jm[0] = jr[b].x & 0xFFFFu; jm[1] = jr[b].x >> 16;
-                                jm[2] = jr[b].y & 0xFFFFu; jm[3] = jr[b].y >> 16;
-                                jm[4] = jr[b].z & 0xFFFFu; jm[5] = jr[b].z >> 16;
-                                jm[6] = jr[b].w & 0xFFFFu; jm[7] = jr[b].w >> 16;
-                            } else {
-                                load_jmap8(A.plan, x, A.V, jm);
-                            }
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                float yv = jm[e] < static_cast<uint32_t>(A.Vd) ? ld_elem<DD>(drow, jm[e]) : -INFINITY;
-                                yv = yv != yv ? -INFINITY : yv;
-                                q[e] = ex2(fmaf(yv, c, -rs.mq)) * invSq;
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float pe = x + e < A.V ? ex2(fmaf(z[e], c, -rs.m)) * invS : 0.f;
-                        ps += pe;
-                        ws += residual ? fmaxf(pe - q[e], 0.f) : pe;
-                    }
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    ws += __shfl_xor_sync(0xffffffffu, ws, o);
-                    ps += __shfl_xor_sync(0xffffffffu, ps, o);
-                }
-                if (lane == 0) {
-                    const int32_t cc = vw * 8 / kRaceChunk;
-                    const int32_t slot = (vw * 8 / 256) % kWarpsPerChunk;
-                    wpart[cc * kWarpsPerChunk + slot] = ws;
-                    ppart[cc * kWarpsPerChunk + slot] = ps;
-                }
+            if (lane == 0) {
+                n_s = n;
+                fl_s = fl;
             }
         }
         __syncthreads();
-        // chunk sums in a fixed order; slots past the row's end hold nothing
-        float wtot = 0.f;
-        for (int32_t cc = tid; cc < nc; cc += NT) {
-            const int32_t nslots = min(kWarpsPerChunk, (min(A.V, (cc + 1) * kRaceChunk) - cc * kRaceChunk + 255) / 256);
-            float wc = 0.f, pc = 0.f;
-            for (int i = 0; i < nslots; ++i) {
-                wc += wpart[cc * kWarpsPerChunk + i];
-                pc += ppart[cc * kWarpsPerChunk + i];
-            }
-            wpart[cc * kWarpsPerChunk] = wc;
-            ppart[cc * kWarpsPerChunk] = pc;
-            wtot += wc;
-        }
-        wtot = block_sum<NT>(wtot, red_f);
-        if (residual && !(wtot > 0.f)) {
-            use_p = true;
-            status |= SV_ST_RESIDUAL_ZERO;
-        }
-        // ---- chunk race ----
-        float best = INFINITY;
-        for (int32_t cc = tid; cc < nc; cc += NT) {
-            const float wc = use_p ? ppart[cc * kWarpsPerChunk] : wpart[cc * kWarpsPerChunk];
-            if (!(wc > 0.f)) continue;
-            const uint4 w4 = philox_block(key, static_cast<uint32_t>(cc >> 2), static_cast<uint32_t>(n), tag_c);
-            const uint32_t wd = (cc & 3) == 0 ? w4.x : ((cc & 3) == 1 ? w4.y : ((cc & 3) == 2 ? w4.z : w4.w));
-            const float kc = __fdiv_rn(-log1pf(-one_minus_uniform_from_word(wd)), wc);
-            if (kc < best) {  // ascending chunk ids: strict < keeps the lowest
-                best = kc;
-                bc = cc;
-            }
-        }
-        block_argmin_key<NT>(best, bc, red_f, red_i);
+        const int32_t n = n_s;
+        const uint32_t fl = fl_s;
+        __syncthreads();  // n_s and fl_s are written again by the next item
+        const bool bad_rows = (fl & (kFlagNaN | kFlagPosInf | kFlagAllNegInf | kFlagDraftBad)) != 0;
+        const bool greedy = !(T > 0.f) || bad_rows;
+        const bool residual = n < k;
+        uint32_t status = 0;
+        int32_t token = -1;
+        if (greedy) {
+            if (sl != 0) continue;  // block-uniform
+            token = st[n].amax;
         } else {
-            // ---- chunk race with bounds: the row pass left p's sum over every chunk, which
-            // bounds the chunk's weight sum W_c, so E_c / P_c bounds its key from below.
-            // Chunks are summed exactly in the order of these bounds, a batch at a time,
-            // until the next bound exceeds the best exact key. ----
-            if (cpre) {
-                const int32_t t0 = n * nc;
-                if (tid >= t0 && tid < t0 + nc) cst_s[tid - t0] = cv0;
-                if (tid + NT >= t0 && tid + NT < t0 + nc) cst_s[tid + NT - t0] = cv1;
-            } else {
-                for (int32_t cc = tid; cc < nc; cc += NT) cst_s[cc] = cst_r[static_cast<int64_t>(n) * A.nct + cc];
+            const RowStat rs = st[n];
+            RaceRow Rr;
+            Rr.trow = A.tbase + (static_cast<int64_t>(r) * (k + 1) + n) * A.tstride;
+            Rr.drow = residual ? A.dbase + (static_cast<int64_t>(r) * k + n) * A.dstride : nullptr;
+            Rr.c = kLog2e / T;
+            Rr.m = rs.m;
+            Rr.invS = 1.f / rs.s;
+            Rr.mq = rs.mq;
+            Rr.invSq = residual ? 1.f / rs.sq : 0.f;
+            Rr.key = philox_key(A.seeds[r]);
+            Rr.row = static_cast<uint32_t>(n);
+            Rr.tag = residual ? kTagResidual : kTagBonus;
+            const unsigned long long mine =
+                race_slice<DT, DD>(A, Rr, sl * kRaceSlice, residual, A.race_bound + r, INFINITY, sh);
+            if (tid == 0) {
+                if (mine != kNoKey) atomicMin(A.race_best + r, mine);
+                __threadfence();
+                const unsigned int done = atomicAdd(A.race_done + r, 1u);
+                last_s = done == static_cast<unsigned int>(nsl - 1);
+                if (last_s) {
+                    __threadfence();
+                    best_s = atomicOr(A.race_best + r, 0ull);
+                }
             }
             __syncthreads();
-            for (int32_t cc = tid; cc < nc; cc += NT) {
-                const float2 v = cst_s[cc];
-                const float pc = v.y > 0.f ? v.y * ex2(v.x - rs.m) * invS : 0.f;
-                const uint4 w4 = philox_block(key, static_cast<uint32_t>(cc >> 2), static_cast<uint32_t>(n), tag_c);
-                const uint32_t wd = (cc & 3) == 0 ? w4.x : ((cc & 3) == 1 ? w4.y : ((cc & 3) == 2 ? w4.z : w4.w));
-                const float e = -log1pf(-one_minus_uniform_from_word(wd));
-                ec_s[cc] = e;
-                // the row pass rounds differently from the sums below: widen the bound by 1e-4
-                lb_s[cc] = pc > 0.f ? __fdiv_rn(e, pc * 1.0001f) : INFINITY;
+            const bool last = last_s != 0;
+            unsigned long long best = best_s;
+            __syncthreads();  // last_s and best_s are written again by the next item
+            if (!last) continue;  // block-uniform
+            if (best == kNoKey && residual) {
+                // no residual mass anywhere: the correction is drawn from p (same row and tag),
+                // by this item alone, slice by slice
+                status |= SV_ST_RESIDUAL_ZERO;
+                float bnd = INFINITY;
+                for (int32_t s2 = 0; s2 < nsl; ++s2) {
+                    const unsigned long long b2 = race_slice<DT, DD>(A, Rr, s2 * kRaceSlice, false, nullptr, bnd, sh);
+                    if (b2 < best) best = b2;
+                    if (best != kNoKey) bnd = __uint_as_float(static_cast<uint32_t>(best >> 32));
+                }
             }
-            __syncthreads();
-            // rank of every bound (ties by chunk id): one warp per chunk, 32 comparisons a ballot
-            for (int32_t cc = tid >> 5; cc < nc; cc += kRaceWarps) {
-                const float l = lb_s[cc];
-                int32_t rk = 0;
-                for (int32_t o0 = 0; o0 < nc; o0 += 32) {
-                    const int32_t o = o0 + lane;
-                    const float lo = o < nc ? lb_s[o] : INFINITY;
-                    rk += __popc(__ballot_sync(0xffffffffu, o < nc && (lo < l || (lo == l && o < cc))));
-                }
-                if (lane == 0) order_s[rk] = cc;
-            }
-            for (int pass = 0; pass < (residual ? 2 : 1); ++pass) {
-                const bool wp = !residual || pass == 1;  // weights p (bonus, or no residual mass)
-                if (tid == 0) {
-                    best_s = INFINITY;
-                    bc_s = INT32_MAX;
-                    bslot_s = -1;
-                    bround_s = -1;
-                }
-                __syncthreads();
-                if (!wp && ywait) {  // the draft row in shared memory
-                    if (!mbar_wait_bounded(&ybar, 0)) status |= SV_ST_TIMEOUT;
-                    ywait = false;
-                }
-                int32_t last_r0 = -1;  // the round whose weights wbuf holds
-                for (int32_t r0 = 0; r0 < nc; r0 += kEvalChunks) {
-                    if (lb_s[order_s[r0]] > best_s) break;  // block-uniform: read after a barrier
-                    last_r0 = r0;
-#pragma unroll 1
-                    for (int vp = 0; vp < kVPass; ++vp) {
-                    const int vtid = tid + vp * NT;  // the virtual thread
-                    const int slot = vtid / (kVT / kEvalChunks);
-                    const int sub = vtid % (kVT / kEvalChunks);
-                    float ws = 0.f;
-                    if (r0 + slot < nc) {
-                        const int32_t cc = order_s[r0 + slot];
-                        const int32_t cx1 = min(A.V, (cc + 1) * kRaceChunk);
-                        // the weights of the round's first kWbufSlots chunks (lowest bounds) are kept
-                        // for the element race, should one of them win
-                        float* wb = slot < kWbufSlots ? wbuf + slot * kRaceChunk : nullptr;
-                        const bool full = cx1 == (cc + 1) * kRaceChunk && vec_ok && (wp || (dvec_ok && !A.identity));
-                        if (DT == SV_BF16 && DD == SV_BF16 && full) {
-#pragma unroll
-                            for (int hv0 = 0; hv0 < kEvalVecs; hv0 += 2) {
-                                // every load of two vectors first: the target words and the draft ids,
-                                // then the draft-row values of the support ids among them
-                                uint4 tw[2], jw[2];
-#pragma unroll
-                                for (int hv = 0; hv < 2; ++hv) {
-                                    const int32_t x = cc * kRaceChunk + 8 * (kEvalVecs * sub + hv0 + hv);
-                                    tw[hv] = ld_nc_v4(reinterpret_cast<const uint4*>(trow + static_cast<int64_t>(x) * 2));
-                                    if (!wp) jw[hv] = ld_nc_v4(reinterpret_cast<const uint4*>(A.plan.jmap + x));
-                                }
-                                uint32_t yb[2][8];
-                                const uint32_t ya = smem_addr(ybuf);
-#pragma unroll
-                                for (int hv = 0; hv < 2; ++hv) {
-                                    const uint32_t jv[4] = {jw[hv].x, jw[hv].y, jw[hv].z, jw[hv].w};
-#pragma unroll
-                                    for (int e = 0; e < 8; ++e) {
-                                        const uint32_t jm = (e & 1) ? jv[e >> 1] >> 16 : jv[e >> 1] & 0xFFFFu;
-                                        yb[hv][e] = 0xFF80u;  // -inf: off the support
-                                        if (!wp && jm < static_cast<uint32_t>(A.Vd)) yb[hv][e] = lds_u16(ya + 2 * jm);
-                                    }
-                                }
-#pragma unroll
-                                for (int hv = 0; hv < 2; ++hv) {
-                                    const int32_t xo = 8 * (kEvalVecs * sub + hv0 + hv);
-                                    const uint32_t zv[4] = {tw[hv].x, tw[hv].y, tw[hv].z, tw[hv].w};
-                                    float wv[8];
-#pragma unroll
-                                    for (int e = 0; e < 8; ++e) {
-                                        float ze = (e & 1) ? bf16_hi(zv[e >> 1]) : bf16_lo(zv[e >> 1]);
-                                        ze = ze != ze ? -INFINITY : ze;
-                                        const float pe = ex2(fmaf(ze, c, -rs.m)) * invS;
-                                        if (wp) {
-                                            wv[e] = pe;
-                                        } else {
-                                            float y = __uint_as_float(yb[hv][e] << 16);
-                                            y = y != y ? -INFINITY : y;
-                                            wv[e] = fmaxf(pe - ex2(fmaf(y, c, -rs.mq)) * invSq, 0.f);
-                                        }
-                                        ws += wv[e];
-                                    }
-                                    if (wb) {
-                                        reinterpret_cast<float4*>(wb + xo)[0] = make_float4(wv[0], wv[1], wv[2], wv[3]);
-                                        reinterpret_cast<float4*>(wb + xo)[1] = make_float4(wv[4], wv[5], wv[6], wv[7]);
-                                    }
-                                }
-                            }
-                        } else {
-#pragma unroll
-                            for (int hv = 0; hv < kEvalVecs; ++hv) {
-                                const int32_t xo = 8 * (kEvalVecs * sub + hv);
-                                const int32_t x = cc * kRaceChunk + xo;
-                                float z[8], q[8], wv[8];
-                                load8<DT>(trow, x, cx1, vec_ok, z);
-                                if (!wp) q8<DD>(A, drow, x, cx1, dvec_ok, c, rs.mq, invSq, q);
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) {
-                                    wv[e] = 0.f;
-                                    if (x + e >= cx1) continue;
-                                    const float pe = ex2(fmaf(z[e], c, -rs.m)) * invS;
-                                    wv[e] = wp ? pe : fmaxf(pe - q[e], 0.f);
-                                    ws += wv[e];
-                                }
-                                if (wb) {
-                                    reinterpret_cast<float4*>(wb + xo)[0] = make_float4(wv[0], wv[1], wv[2], wv[3]);
-                                    reinterpret_cast<float4*>(wb + xo)[1] = make_float4(wv[4], wv[5], wv[6], wv[7]);
-                                }
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
-                    if (lane == 0) bpart_s[vtid >> 5] = ws;
-                    }
-                    __syncthreads();
-                    if (tid < 32) {
-                        // lane sl: the key of slot sl's chunk; then the lowest key, lowest chunk id
-                        constexpr int kWarpsPerSlot = kVT / 32 / kEvalChunks;
-                        static_assert(kEvalChunks <= 32, "one lane per slot");
-                        float kc = INFINITY;
-                        int32_t ccl = INT32_MAX;
-                        if (lane < kEvalChunks && r0 + lane < nc) {
-                            float wc = 0.f;
-                            for (int i = 0; i < kWarpsPerSlot; ++i) wc += bpart_s[lane * kWarpsPerSlot + i];
-                            if (wc > 0.f) {
-                                ccl = order_s[r0 + lane];
-                                kc = __fdiv_rn(ec_s[ccl], wc);
-                            }
-                        }
-                        float nk = ccl == INT32_MAX ? -INFINITY : -kc;
-                        int32_t cw = ccl;
-                        warp_argmax(nk, cw);
-                        if (lane == 0 && cw != INT32_MAX) {
-                            const float kb2 = -nk;
-                            if (kb2 < best_s || (kb2 == best_s && cw < bc_s)) {
-                                best_s = kb2;
-                                bc_s = cw;
-                                int32_t sl = 0;
-                                while (order_s[r0 + sl] != cw) ++sl;
-                                bslot_s = sl;
-                                bround_s = r0;
-                            }
-                        }
-                    }
-                    __syncthreads();
-                }
-                if (bc_s != INT32_MAX) {
-                    use_p = wp;
-                    // the kept weights, if the chunk was among the kept ones of the last round
-                    if (bround_s == last_r0 && bslot_s < kWbufSlots) bslot = bslot_s;
-                    break;
-                }
-                if (residual && pass == 0) status |= SV_ST_RESIDUAL_ZERO;
-            }
-            bc = bc_s;
+            token = best == kNoKey ? 0 : static_cast<int32_t>(best & 0xFFFFFFFFu);
+            if (residual && (rs.flags & kFlagOffSupport)) status |= SV_ST_OFF_SUPPORT;
         }
-        if (bc == INT32_MAX) {
-            token = 0;  // no weight anywhere: cannot happen for a row that is not flagged
-        } else {
-            // ---- element race inside chunk bc: four ids (one Philox block) per thread ----
-            const int32_t cx0 = bc * kRaceChunk, cx1 = min(A.V, cx0 + kRaceChunk);
-            const bool wq = residual && !use_p;
-            float kb = INFINITY;
-            int32_t bx = INT32_MAX;
-            const int32_t xb = cx0 + 4 * tid;
-            if (tid < kRaceChunk / 4 && xb < cx1) {
-                float wgt[4];
-                if (bslot >= 0) {  // the weights the bounded race summed for this chunk
-                    const float4 w4v = reinterpret_cast<const float4*>(wbuf + bslot * kRaceChunk)[tid];
-                    wgt[0] = w4v.x;
-                    wgt[1] = w4v.y;
-                    wgt[2] = w4v.z;
-                    wgt[3] = w4v.w;
-                } else {
-                    float ze[4], qe[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float v = xb + e < cx1 ? ld_elem<DT>(trow, xb + e) : -INFINITY;
-                        ze[e] = v != v ? -INFINITY : v;
-                    }
-                    if (wq) {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int32_t x = xb + e;
-                            int32_t jd = -1;
-                            if (x < cx1) jd = A.identity ? x : (A.plan.jmap[x] == 0xFFFFu ? -1 : A.plan.jmap[x]);
-                            if (jd >= 0 && jd < A.Vd) {
-                                float y = ld_elem<DD>(drow, jd);
-                                y = y != y ? -INFINITY : y;
-                                qe[e] = ex2(fmaf(y, c, -rs.mq)) * invSq;
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        wgt[e] = ex2(fmaf(ze[e], c, -rs.m)) * invS;
-                        if (wq) wgt[e] = fmaxf(wgt[e] - qe[e], 0.f);
-                    }
-                }
-                const uint4 w4 = philox_block(key, static_cast<uint32_t>(xb >> 2), static_cast<uint32_t>(n), tag_x);
-                const uint32_t words[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    if (xb + e >= cx1) break;
-                    const float we = wgt[e];
-                    if (!(we > 0.f)) continue;
-                    const float ke = __fdiv_rn(-log1pf(-one_minus_uniform_from_word(words[e])), we);
-                    if (ke < kb) {
-                        kb = ke;
-                        bx = xb + e;
-                    }
-                }
+        // ---- commit (one item per request) ----
+        for (int32_t j = tid; j < k; j += kRaceThreads)
+            if (d[j] < 0 || d[j] >= A.V) status |= SV_ST_TOKEN_RANGE;
+        if (fl & kFlagTimeout) status |= SV_ST_TIMEOUT;
+        if (bad_rows) status |= SV_ST_BAD_LOGITS;
+        if (T < 0.f || T != T) status |= SV_ST_BAD_TEMP;
+        if (!A.identity && (A.plan.header[2] != 0 || A.plan.header[0] != A.V || A.plan.header[1] != A.Vd))
+            status |= SV_ST_BAD_D2T;
+        int32_t* out = A.tokens + static_cast<int64_t>(r) * (k + 1);
+        for (int32_t j = tid; j <= k; j += kRaceThreads) out[j] = j < n ? d[j] : (j == n ? token : -1);
+        if (greedy) {
+            // no sampling statistics for greedily verified requests
+            for (int32_t j = tid; j < k; j += kRaceThreads) {
+                const int64_t o = static_cast<int64_t>(r) * k + j;
+                if (A.tv) A.tv[o] = NAN;
+                if (A.pd) A.pd[o] = NAN;
+                if (A.qd) A.qd[o] = NAN;
             }
-            block_argmin_key<NT>(kb, bx, red_f, red_i);
-            token = bx == INT32_MAX ? cx0 : bx;
         }
-        if (residual && (rs.flags & kFlagOffSupport)) status |= SV_ST_OFF_SUPPORT;
-    }
-    // ---- commit ------------------------------------------------------------
-    if (tid < k && (dj < 0 || dj >= A.V)) status |= SV_ST_TOKEN_RANGE;  // k <= SV_MAX_K < NT
-    if (fl & kFlagTimeout) status |= SV_ST_TIMEOUT;
-    if (bad_rows) status |= SV_ST_BAD_LOGITS;
-    if (T < 0.f || T != T) status |= SV_ST_BAD_TEMP;
-    if (!A.identity && (A.plan.header[2] != 0 || A.plan.header[0] != A.V || A.plan.header[1] != A.Vd))
-        status |= SV_ST_BAD_D2T;
-    int32_t* out = A.tokens + static_cast<int64_t>(r) * (k + 1);
-    if (tid <= k) out[tid] = tid < n ? dj : (tid == n ? token : -1);
-    if (greedy) {
-        // no sampling statistics for greedily verified requests
-        for (int32_t j = tid; j < k; j += NT) {
-            const int64_t o = static_cast<int64_t>(r) * k + j;
-            if (A.tv) A.tv[o] = NAN;
-            if (A.pd) A.pd[o] = NAN;
-            if (A.qd) A.qd[o] = NAN;
+        status = block_or<kRaceThreads>(status, red_u);
+        if (tid == 0) {
+            A.accept_len[r] = n;
+            if (A.status) A.status[r] = static_cast<int32_t>(status);
         }
-    }
-    if (ywait && tid == 0) (void)mbar_wait_bounded(&ybar, 0);  // no copy outlives the CTA
-    status = block_or<NT>(status, reinterpret_cast<uint32_t*>(red_i));
-    if (tid == 0) {
-        A.accept_len[r] = n;
-        if (A.status) A.status[r] = static_cast<int32_t>(status);
+        __syncthreads();  // red_u is written again by the next item
     }
 }
 
@@ -2312,7 +2023,7 @@ D2tPlan plan_view(void* base, int32_t V, int32_t Vd)
 }
 
 struct SampleLayout {
-    int64_t plan, stats, cstat, gslots;
+    int64_t plan, stats, rbound, rbest, rdone, gslots;
     int64_t gslot_bytes;
     int64_t total;
     int smem_mode;
@@ -2331,7 +2042,9 @@ SampleLayout sample_layout(int64_t R, int32_t k, int32_t V, int32_t Vd, int et, 
     };
     L.plan = take(own_plan ? plan_layout(V, Vd).total : 0);
     L.stats = take(R * (k + 1) * static_cast<int64_t>(sizeof(RowStat)));
-    L.cstat = take(R * (k + 1) * ((static_cast<int64_t>(V) + kChunkElems - 1) / kChunkElems) * 8);
+    L.rbound = take(R * 4);
+    L.rbest = take(R * 8);
+    L.rdone = take(R * 4);
     const int64_t units = R * (k + 1);
     L.grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(units, sms > 0 ? sms : 148)));
     const int64_t resident = align256(static_cast<int64_t>(Vd) * ed) + align256(static_cast<int64_t>(Vd) * et);
@@ -2433,8 +2146,9 @@ static cudaError_t launch_sample_t(const Rows& t, const Rows& d, const int32_t* 
     A.status = status;
     A.stats = reinterpret_cast<RowStat*>(ws + L.stats);
     const bool fast = fast_path_ok(t, d, identity);
-    A.cstat = fast ? reinterpret_cast<float2*>(ws + L.cstat) : nullptr;  // the fast row pass leaves chunk sums
-    A.nct = (t.width + kChunkElems - 1) / kChunkElems;
+    A.race_bound = reinterpret_cast<unsigned int*>(ws + L.rbound);
+    A.race_best = reinterpret_cast<unsigned long long*>(ws + L.rbest);
+    A.race_done = reinterpret_cast<unsigned int*>(ws + L.rdone);
     A.gslots = ws + L.gslots;
     A.gslot_bytes = L.gslot_bytes;
     A.smem_mode = L.smem_mode;
@@ -2470,16 +2184,20 @@ static cudaError_t launch_sample_t(const Rows& t, const Rows& d, const int32_t* 
         e = cudaLaunchKernelEx(&cfg, sample_rows_kernel<DT, DD>, A);
     }
     if (e != cudaSuccess) return e;
-    // one CTA per request: 1024 threads while the requests fit one CTA per SM, else 512 (two per SM)
-    const bool wide = R <= (sms > 0 ? sms : 148);
-    const size_t race_smem = race_smem_layout(k, A.nct, d.width, fast).total;
-    auto* race = wide ? race_rows_kernel<DT, DD, 1024> : race_rows_kernel<DT, DD, kRaceMinThreads>;
-    e = cudaFuncSetAttribute(race, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(race_smem));
-    if (e != cudaSuccess) return e;
+    // the race: work items of (request, slice), CTAs resident at once on every SM
+    auto* race = race_flat_kernel<DT, DD>;
+    static int race_per_sm = 0;  // per (DT, DD) instance
+    if (race_per_sm == 0) {
+        int b = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, race, kRaceThreads, 0) != cudaSuccess || b < 1) b = 1;
+        race_per_sm = b;
+    }
+    const int64_t items = static_cast<int64_t>(R) * ((t.width + kRaceSlice - 1) / kRaceSlice);
+    const int64_t rgrid = std::max<int64_t>(1, std::min<int64_t>(items, static_cast<int64_t>(sms > 0 ? sms : 148) * race_per_sm));
     cudaLaunchConfig_t cfg2 = {};
-    cfg2.gridDim = dim3(static_cast<unsigned>(R));
-    cfg2.blockDim = dim3(wide ? 1024 : kRaceMinThreads);
-    cfg2.dynamicSmemBytes = race_smem;
+    cfg2.gridDim = dim3(static_cast<unsigned>(rgrid));
+    cfg2.blockDim = dim3(kRaceThreads);
+    cfg2.dynamicSmemBytes = 0;
     cfg2.stream = stream;
     cfg2.attrs = attr;
     cfg2.numAttrs = 1;

@@ -169,8 +169,8 @@ __device__ __forceinline__ float one_minus_uniform_from_word(uint32_t w)
 }
 
 // counter layout of the library: (x >> 2, row, tag, 0), word x & 3
-// uniform tags: accept test, element races, and the chunk level of the two-level race
-enum : uint32_t { kTagAccept = 0, kTagResidual = 1, kTagBonus = 2, kTagResidualChunk = 3, kTagBonusChunk = 4 };
+// uniform tags: the accept test, the residual race and the bonus race
+enum : uint32_t { kTagAccept = 0, kTagResidual = 1, kTagBonus = 2 };
 
 __device__ __forceinline__ uint4 philox_block(PhiloxKey key, uint32_t x4, uint32_t row, uint32_t tag)
 {

@@ -32,3 +32,21 @@ def sv():
 
     m.load()
     return m
+
+
+def pytest_terminal_summary(terminalreporter):
+    """The exempt-row counts of every sampling comparison (decision margin below 1e-6)."""
+    try:
+        from tests.sampling_parity import EXEMPT_LOG
+    except Exception:
+        return
+    if not EXEMPT_LOG:
+        return
+    ex = sum(e for _, e, _, _ in EXEMPT_LOG)
+    rows = sum(n for _, _, n, _ in EXEMPT_LOG)
+    diff = sum(d for _, _, _, d in EXEMPT_LOG)
+    worst = max(EXEMPT_LOG, key=lambda t: t[1] / max(t[2], 1))
+    terminalreporter.write_line(
+        f"exempt rows (decision margin < 1e-6): {ex} of {rows} rows in {len(EXEMPT_LOG)} comparisons "
+        f"(rate {ex / max(rows, 1):.2e}); requests differing from the oracle: {diff}; "
+        f"highest rate: {worst[0]} {worst[1]}/{worst[2]}")

@@ -186,3 +186,31 @@ def test_valid_call_without_device_reports_no_device(lib):
     buf = P(0x10000)
     rc = lib.sv_verify_greedy(_rows(), 1, 2, 1, buf, buf, buf, None, None, P(0x20000), 1 << 20, None)
     assert rc == -8
+
+
+def test_noalloc_argument_errors_match_the_workspace_entry(lib):
+    """sv_verify_greedy_noalloc answers every argument error with sv_verify_greedy's code, in
+    sv_verify_greedy's order (no GPU is touched before the arguments pass)."""
+    P = C.c_void_p
+    buf = P(0x10000)
+    ws = P(0x20000)
+    g, na = lib.sv_verify_greedy, lib.sv_verify_greedy_noalloc
+    cases = [
+        (_rows(), 0, 2, 1, buf),            # R == 0: a no-op
+        (_rows(), -1, 2, 1, buf),
+        (_rows(), 1, 2, 0, buf),
+        (_rows(), 1, 2, 9, buf),            # more branches than SV_MAX_BRANCHES: SV_ERR_LIMIT
+        (_rows(), 1, 0, 2, buf),
+        (_rows(), 1, 257, 1, buf),
+        (_rows(), -1, 2, 9, buf),           # two errors: the first check decides
+        (_rows(dtype=7), 1, 257, 1, buf),
+        (_rows(dtype=7), 1, 2, 1, buf),
+        (_rows(stride=8), 1, 2, 1, buf),
+        (_rows(data=0x1001), 1, 2, 1, buf),
+        (_rows(), 1, 2, 1, None),           # no draft tokens
+        (_rows(), 1, 2, 1, P(0x10002)),     # misaligned draft tokens
+    ]
+    for t, R, k, br, d in cases:
+        want = g(t, R, k, br, d, buf, buf, None, None, ws, 1 << 30, None)
+        assert want != 0 or R == 0
+        assert na(t, R, k, br, d, buf, buf, None, None, None) == want, (R, k, br)

@@ -43,3 +43,17 @@ def test_native_arm_needs_a_gpu():
     r = _run("--steps", "1", "--warmup", "1")
     assert r.returncode != 0
     assert "GPU" in (r.stderr + r.stdout)
+
+
+def test_reference_arm_loads_only_the_oracle():
+    """The reference arm builds its inputs with the seeded generator and runs the oracle: the
+    CUDA library's package is never imported and its shared object never loaded."""
+    code = ("import sys; sys.argv = ['bench.py', '--impl', 'reference', '--steps', '1', '--warmup', '0', "
+            "'--sessions', '1', '--workload', 'd2t']; import bench; bench.main(); "
+            "maps = open('/proc/self/maps').read(); "
+            "assert 'serving_sampler_gb300' not in sys.modules; assert 'libspecverify' not in maps; "
+            "assert 'liboracle' in maps; print('ONLY_ORACLE')")
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, cwd=ROOT, env=env, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert "ONLY_ORACLE" in r.stdout

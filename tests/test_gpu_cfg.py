@@ -58,10 +58,9 @@ def test_cfg_greedy_and_partition_offsets(sv):
 
 
 def test_cfg_workload_full_size(sv):
+    """256 requests x 5 frames x 9 codebooks (11,520 codebook rows): fewer than 1e-5 of the
+    rows may be exempt, so none.  Flat codebooks: most frames are rejected early."""
     w = workloads.cfg_workload()
     got, want = _run(sv, w), _oracle(w)
-    exempt = compare(got, want)
-    assert exempt <= 1
-    p_top = None  # flat codebooks: most frames are rejected early, acceptance well below text
+    compare(got, want)
     assert want["accept_len"].mean() < 2.0
-    del p_top

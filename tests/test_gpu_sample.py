@@ -80,8 +80,7 @@ def test_worked_example_distribution_and_parity(sv):
     assert stats.chisquare(counts, exp).pvalue > 1e-3
     acc = got["accept_len"] == 1
     assert abs(acc.mean() - g["alpha"]) < 5 * math.sqrt(0.09 / R)
-    exempt = compare(got, _oracle(w), stats=False)
-    assert exempt <= 2
+    compare(got, _oracle(w), stats=False)  # 400,000 rows: fewer than 4 may be exempt
 
 
 @pytest.mark.parametrize("dtype,ddtype,V,Vd,R,k,row_pad", [
@@ -100,8 +99,8 @@ def test_d2t_shapes(sv, dtype, ddtype, V, Vd, R, k, row_pad):
 
 @pytest.mark.parametrize("dtype,V,Vd", [(torch.bfloat16, 20000, 4096), (torch.float32, 6000, 1500)])
 def test_more_requests_than_sms(sv, dtype, V, Vd):
-    """More requests than SMs: the race runs as 512-thread CTAs, two per SM (bulk-copy and
-    general row paths)."""
+    """More requests than SMs: the row pass's persistent CTAs take several units each and the
+    race's CTAs several work items each (bulk-copy and general row paths)."""
     R, k = 200, 3
     T = [(0.7, 1.0, 0.0, 0.45)[i % 4] for i in range(R)]
     w = workloads.sample_batch(R, k, V, Vd, dtype, T=T, sigma_pos=0.8, delta=2.7, seed=V + 7)
@@ -145,8 +144,7 @@ def test_d2t_workload_full_size(sv):
     w = workloads.d2t_workload()
     got = _run(sv, w)
     want = _oracle(w)
-    exempt = compare(got, want)
-    assert exempt <= 1
+    compare(got, want)  # 1,024 rows: none may be exempt
     # acceptance profile of the stand-in drafter: falls from ~0.7 toward ~0.4
     alpha = 1 - want["tv"].mean(axis=0)
     assert alpha[0] > alpha[-1]
@@ -200,8 +198,8 @@ def test_results_do_not_depend_on_the_place_in_the_batch(sv, dtype):
 
 
 def test_results_do_not_depend_on_the_batch_size(sv):
-    # a batch larger than the SM count runs the race in 512-thread CTAs, a small one in
-    # 1024-thread CTAs; the race's sums follow one fixed layout, so the bits agree
+    # a batch larger than the SM count gives every persistent CTA of the row pass and of the
+    # race several work items, a small one at most one; the bits agree
     R, k = 160, 7
     w = workloads.sample_batch(R, k, workloads.V_QWEN, workloads.VD_DRAFT, torch.bfloat16, T=0.7, sigma_pos=0.9,
                                delta=2.7, seed=41, seed_base=91)

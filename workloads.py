@@ -235,6 +235,19 @@ def d2t_workload(device="cuda", R: int = 128):
                         delta=D2T_DELTA, z_sigma=3.0, seed=1237, seed_base=1234, device=device)
 
 
+SWEEP_BATCHES = (1, 8, 64, 256, 1024)
+
+
+def sweep_batch(B: int, dtype=torch.bfloat16, device="cuda"):
+    """A point of the throughput sweep: B requests x (8 drafts + bonus), V = 151,936, the d2t
+    draft model of the sampling workload, requests alternating greedy (T = 0) and sampled
+    (T alternating 0.6 / 1.0)."""
+    T = [0.0 if r % 2 == 0 else (0.6 if (r // 2) % 2 == 0 else 1.0) for r in range(B)]
+    sigma = list(D2T_SIGMA) + [D2T_SIGMA[-1]]
+    return sample_batch(B, 8, V_QWEN, VD_DRAFT, dtype, T=T, sigma_pos=sigma, delta=D2T_DELTA, z_sigma=3.0,
+                        seed=1300 + B, seed_base=5000, device=device)
+
+
 # ---------------------------------------------------------------------------
 # CFG workload
 # ---------------------------------------------------------------------------
