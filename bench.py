@@ -662,7 +662,7 @@ def run_native(a):
         h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
         h.copy_(t)
         h_in[key] = h
-    d_in = {key: torch.empty_like(t) for key, t in h_in.items()}
+    d_in = {key: torch.empty_like(spec.inputs[key]) for key in h_in}  # device buffers
     h_out = {key: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for key, v in nat.out.items()}
 
     def e2e_step():

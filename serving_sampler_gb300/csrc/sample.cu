@@ -18,12 +18,12 @@
 //                      positions (G).  A second pass over G and the draft
 //                      row gives TV over the full vocabulary, p(x_j), q(x_j)
 //                      and the accept test u_j < p/q.
-//   race_flat_kernel   work items of (request, 4096-id slice): the
-//                      accept-length scan, then on the one selected row
-//                      (residual max(0, p - q) at the first rejection, or p at
-//                      the bonus row) the exponential race over every id with
-//                      Philox uniforms, pruned by a bound shared by the
-//                      request's items; the last item commits the tokens.
+//   race_rows_kernel   one CTA per request (or per part of its row for small
+//                      batches): the accept-length scan, then on the one
+//                      selected row (residual max(0, p - q) at the first
+//                      rejection, or p at the bonus row) the exponential race
+//                      over every id with Philox uniforms, pruned by a bound on
+//                      the row's minimum key; then the commit.
 // Temperature scaling works in log2 units: with c = log2(e) / T,
 // p(x) = 2^(z_x c - M) / S where M = max_x z_x c and S = sum 2^(z c - M).
 #include <algorithm>
@@ -1629,92 +1629,29 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
 // the whole row: argmin over the ids with w_x > 0 of E_x / w_x, E_x = -ln u_x,
 // u_x the Philox uniform of id x (counter (x >> 2, row, tag, 0), word x & 3).
 //
-// race_flat_kernel: work items (request, slice of kRaceSlice ids), a grid-stride
-// loop of CTAs of kRaceThreads.  Every item scans the request's accept flags for
-// n (greedy requests are committed by their slice 0); a sampled request's item
-// computes the weights of its slice in registers, takes the exact keys of its
-// warps' heaviest ids, and publishes the smallest as a bound B of the row's
-// minimum key (atomicMin over the request's items).  A key E_x / w_x <= B needs
-// 1 - u_x <= E_x <= B w_x, so a Philox block is generated only when one of its
-// four ids has B w_x >= 2^-24 (the smallest 1 - u there is), and a logarithm is
-// taken only for ids with 1 - u_x <= B w_x; both tests are widened by
-// kRaceSlack against fp32 rounding, so no id that can win is skipped and the
-// winner does not depend on which bound an item saw.  Each item's (key, id)
-// minimum goes into the request's packed 64-bit minimum (lowest key, then
-// lowest id); the item that finishes last commits the tokens.
+// race_rows_kernel: one CTA per request, or per part of its row when the batch
+// has fewer requests than the GPU has CTA slots (then the parts meet in a
+// packed 64-bit per-request minimum and the part that finishes last commits).
+// Warp 0 scans the accept flags for n.  Each warp streams 256-id steps of the
+// selected row (the next step's loads in flight) and keeps a running minimum
+// key; a bound B of the row's minimum key is shared through shared memory
+// (seeded with the key of the row's argmax).  An id can win only if
+// 1 - u <= E <= B w (E = -ln u >= 1 - u) and 1 - u >= 2^-24, so it needs
+// p B >= 2^-24: ids whose scaled logit t = z c - m is below
+// lg2(S) - 24 - lg2(B) are skipped without an exponential, a Philox block is
+// generated only when one of its four ids has B w >= 2^-24, and a logarithm
+// is taken only when 1 - u <= B w.  Every test is widened by kRaceSlack
+// against fp32 rounding, so no id that can win is skipped and the winner
+// does not depend on which bound a warp saw.
 namespace {
 
-constexpr int kRaceThreads = 256;
-constexpr int kRaceVecs = 2;                                      // 8-id vectors per thread
-constexpr int32_t kRaceSlice = kRaceThreads * kRaceVecs * 8;      // 4096 ids per work item
+constexpr int kRaceThreads = 512;
+constexpr int kRaceWarps = kRaceThreads / 32;
+constexpr int32_t kRaceStep = 256;                // ids per warp step, eight per lane
+constexpr uint32_t kRaceSmemRow = 96 * 1024;      // draft rows up to this size are staged in shared memory
 constexpr float kRaceSlack = 1.0f + 1.0f / 1024.0f;
-constexpr float kRaceMinGap = 5.9604645e-8f;                      // 2^-24: the smallest 1 - u
-
-// z[0..8) of ids [x, x + 8) of a row (-inf at and beyond x_end; NaN read as -inf)
-template <int DT>
-__device__ __forceinline__ void load8(const char* row, int32_t x, int32_t x_end, bool vec_ok, float* z)
-{
-    if (vec_ok && x + 8 <= x_end) {
-        if constexpr (DT == SV_BF16) {
-            const uint4 v = ld_nc_v4(reinterpret_cast<const uint4*>(row + static_cast<int64_t>(x) * 2));
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                z[2 * e] = bf16_lo(w[e]);
-                z[2 * e + 1] = bf16_hi(w[e]);
-            }
-        } else {
-            const uint4 a = ld_nc_v4(reinterpret_cast<const uint4*>(row + static_cast<int64_t>(x) * 4));
-            const uint4 b = ld_nc_v4(reinterpret_cast<const uint4*>(row + static_cast<int64_t>(x) * 4 + 16));
-            z[0] = __uint_as_float(a.x); z[1] = __uint_as_float(a.y);
-            z[2] = __uint_as_float(a.z); z[3] = __uint_as_float(a.w);
-            z[4] = __uint_as_float(b.x); z[5] = __uint_as_float(b.y);
-            z[6] = __uint_as_float(b.z); z[7] = __uint_as_float(b.w);
-        }
-    } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) z[e] = x + e < x_end ? ld_elem<DT>(row, x + e) : -INFINITY;
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) z[e] = z[e] != z[e] ? -INFINITY : z[e];
-}
-
-// the draft ids of target ids [x, x + 8) (0xFFFF: off the support or beyond V)
-__device__ __forceinline__ void load_jmap8(const D2tPlan& pl, int32_t x, int32_t V, uint32_t* jm)
-{
-    if (x + 8 <= V) {
-        const uint4 v = ld_nc_v4(reinterpret_cast<const uint4*>(pl.jmap + x));
-        jm[0] = v.x & 0xFFFFu; jm[1] = v.x >> 16; jm[2] = v.y & 0xFFFFu; jm[3] = v.y >> 16;
-        jm[4] = v.z & 0xFFFFu; jm[5] = v.z >> 16; jm[6] = v.w & 0xFFFFu; jm[7] = v.w >> 16;
-    } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) jm[e] = x + e < V ? pl.jmap[x + e] : 0xFFFFu;
-    }
-}
-
-// q at target ids [x, x + 8): 2^(y c - mq) / Sq at the draft id of each, 0 off the support
-template <int DD>
-__device__ __forceinline__ void q8(const SampleArgs& A, const char* drow, int32_t x, bool dvec_ok, float c,
-                                   float mq, float invSq, float* q)
-{
-    float y[8];
-    if (A.identity) {
-        load8<DD>(drow, x, A.Vd, dvec_ok, y);
-    } else {
-        uint32_t jm[8];
-        load_jmap8(A.plan, x, A.V, jm);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float v = jm[e] < static_cast<uint32_t>(A.Vd) ? ld_elem<DD>(drow, jm[e]) : -INFINITY;
-            y[e] = v != v ? -INFINITY : v;
-        }
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) q[e] = ex2(fmaf(y[e], c, -mq)) * invSq;
-}
-
-// the uniform's complement 1 - u_x and the key E_x / w of id x
-__device__ __forceinline__ float race_key(float om, float w) { return __fdiv_rn(-log1pf(-om), w); }
+constexpr float kRaceMinGap = 5.9604645e-8f;      // 2^-24: the smallest 1 - u
+constexpr unsigned long long kNoKey = ~0ull;
 
 // (key bits, id) packed so that the unsigned minimum is the lowest key, then the lowest id;
 // keys are positive, so their bits order like the keys
@@ -1722,7 +1659,6 @@ __device__ __forceinline__ unsigned long long pack_key(float key, int32_t id)
 {
     return (static_cast<unsigned long long>(__float_as_uint(key)) << 32) | static_cast<uint32_t>(id);
 }
-constexpr unsigned long long kNoKey = ~0ull;
 
 __device__ __forceinline__ unsigned long long warp_min_u64(unsigned long long v)
 {
@@ -1734,134 +1670,341 @@ __device__ __forceinline__ unsigned long long warp_min_u64(unsigned long long v)
     return v;
 }
 
+// the key E_x / w of an id from its uniform's complement 1 - u
+__device__ __forceinline__ float race_key(float om, float w) { return __fdiv_rn(-log1pf(-om), w); }
+
+__device__ __forceinline__ uint32_t word_of(uint4 w4, int e)
+{
+    return e == 0 ? w4.x : e == 1 ? w4.y : e == 2 ? w4.z : w4.w;
+}
+
+// the lowest scaled logit t = z c - m an id can have and still win against bound B
+__device__ __forceinline__ float race_t_floor(float B, float S)
+{
+    if (!(B < INFINITY)) return -INFINITY;
+    return __log2f(S) - 24.0f - __log2f(B * kRaceSlack) - 1e-3f;
+}
+
 // What a race over one row needs.
 struct RaceRow {
     const char* trow;
-    const char* drow;   // the draft row (residual weights only)
-    float c, m, invS, mq, invSq;
+    const char* drow;     // the draft row (residual weights only)
+    const uint16_t* ysm;  // the draft row in shared memory (bf16), or NULL
+    const float* ysmf;    // the draft row in shared memory (fp32), or NULL
+    float c, m, S, invS, mq, invSq;
     PhiloxKey key;
     uint32_t row, tag;
+    unsigned int* bound_g;  // the request's bound shared by the CTAs of its parts (fp32 bits), or NULL
 };
 
-// the CTA's shared scratch of race_slice
-struct RaceShared {
-    float wkey[kRaceThreads / 32];                 // key of each warp's heaviest id
-    unsigned long long best[kRaceThreads / 32];    // each warp's (key, id) minimum
-    float bound;
-};
-
-// One slice [x0, x0 + kRaceSlice) of the race: the weights (residual max(0, p - q) when
-// `resid`, else p), a bound from the warps' heaviest ids (lowered to *bound_g when given,
-// which also receives this slice's bound), then the pruned race.  Returns the slice's
-// packed (key, id) minimum to every thread.
-template <int DT, int DD>
-__device__ unsigned long long race_slice(const SampleArgs& A, const RaceRow& Rr, int32_t x0, bool resid,
-                                         unsigned int* bound_g, float bound_in, RaceShared& sh)
+// the largest of four target logits (NaN ignored), from their raw 16-byte words
+template <int DT>
+__device__ __forceinline__ float max4(const uint4* zq, int h)
 {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const bool vec_ok = A.tbulk != 0, dvec_ok = A.dbulk != 0;
-    float wv[kRaceVecs][8];
-    float hw = 0.f;  // this thread's heaviest weight and its id
-    int32_t hx = INT32_MAX;
+    if constexpr (DT == SV_BF16) {
+        const uint32_t a = h == 0 ? zq[0].x : zq[0].z, b = h == 0 ? zq[0].y : zq[0].w;
+        uint32_t m;
+        asm("max.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(a), "r"(b));
+        return fmaxf(bf16_lo(m), bf16_hi(m));
+    } else {
+        const uint4 q = zq[h];
+        return fmaxf(fmaxf(__uint_as_float(q.x), __uint_as_float(q.y)), fmaxf(__uint_as_float(q.z), __uint_as_float(q.w)));
+    }
+}
+
+// the raw words of the eight target logits of ids [x, x + 8) (-inf at and past x_end, plain loads
+// at a ragged or unaligned end).  Read-only loads the compiler may batch and hoist.
+template <int DT>
+__device__ __forceinline__ void load_z8(const SampleArgs& A, const RaceRow& Rr, int32_t x, int32_t x_end, uint4* zq)
+{
+    constexpr int ZW = DT == SV_BF16 ? 1 : 2;
+    if (x + 8 <= x_end && A.tbulk) {
 #pragma unroll
-    for (int v = 0; v < kRaceVecs; ++v) {
-        const int32_t x = x0 + 8 * (tid + kRaceThreads * v);
-        float z[8], q[8];
-        load8<DT>(Rr.trow, x, A.V, vec_ok, z);
-        if (resid) q8<DD>(A, Rr.drow, x, dvec_ok, Rr.c, Rr.mq, Rr.invSq, q);
+        for (int h = 0; h < ZW; ++h)
+            zq[h] = __ldg(reinterpret_cast<const uint4*>(Rr.trow + static_cast<int64_t>(x) * (2 * ZW)) + h);
+        return;
+    }
+    uint32_t wv[4 * ZW];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float p = ex2(fmaf(z[e], Rr.c, -Rr.m)) * Rr.invS;
-            float w = resid ? fmaxf(p - q[e], 0.f) : p;
-            w = x + e < A.V ? w : 0.f;
-            wv[v][e] = w;
-            if (w > hw) {  // ascending ids: the first of equal weights
-                hw = w;
-                hx = x + e;
+    for (int e = 0; e < 8; ++e) {
+        const bool ok = x + e < x_end;
+        if constexpr (DT == SV_BF16) {
+            const uint32_t h16 = ok ? __ldg(reinterpret_cast<const uint16_t*>(Rr.trow) + x + e) : 0xFF80u;
+            if (e & 1) wv[e >> 1] |= h16 << 16;
+            else wv[e >> 1] = h16;
+        } else {
+            wv[e] = ok ? __ldg(reinterpret_cast<const uint32_t*>(Rr.trow) + x + e) : 0xFF800000u;
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < ZW; ++h) zq[h] = make_uint4(wv[4 * h], wv[4 * h + 1], wv[4 * h + 2], wv[4 * h + 3]);
+}
+
+// the draft ids of target ids [x, x + 8) as four words of two 16-bit ids (0xFFFF off the support)
+__device__ __forceinline__ uint4 load_j8(const SampleArgs& A, int32_t x)
+{
+    if (x + 8 <= A.V) return __ldg(reinterpret_cast<const uint4*>(A.plan.jmap + x));
+    uint32_t jm[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) jm[e] = x + e < A.V ? A.plan.jmap[x + e] : 0xFFFFu;
+    return make_uint4(jm[0] | (jm[1] << 16), jm[2] | (jm[3] << 16), jm[4] | (jm[5] << 16), jm[6] | (jm[7] << 16));
+}
+
+template <int DT>
+__device__ __forceinline__ float z_of(const uint4* zq, int e)
+{
+    if constexpr (DT == SV_BF16) {
+        const uint32_t ww = (e >> 1) == 0 ? zq[0].x : (e >> 1) == 1 ? zq[0].y : (e >> 1) == 2 ? zq[0].z : zq[0].w;
+        return (e & 1) ? bf16_hi(ww) : bf16_lo(ww);
+    } else {
+        const uint4 q = zq[e >> 2];
+        const int t = e & 3;
+        return __uint_as_float(t == 0 ? q.x : t == 1 ? q.y : t == 2 ? q.z : q.w);
+    }
+}
+
+// where the residual weights read the draft row: the identity map (draft logit x of the draft
+// row), the d2t map through a copy of the row in shared memory, or the d2t map from global memory
+enum { kYIdentity = 0, kYShared = 1, kYGlobal = 2 };
+
+// q at target id x (residual weights); jm is its draft id (0xFFFF: off the support).  The rows
+// a race runs on hold no NaN (a request with one is verified greedily).
+template <int DD, int YM>
+__device__ __forceinline__ float q_at(const SampleArgs& A, const RaceRow& Rr, int32_t x, uint32_t jm)
+{
+    float v;
+    if constexpr (YM == kYIdentity) {
+        v = x < A.Vd ? ld_elem<DD>(Rr.drow, x) : -INFINITY;
+    } else {
+        const bool on = jm < static_cast<uint32_t>(A.Vd);
+        const uint32_t j = on ? jm : 0u;
+        if constexpr (YM == kYShared) {
+            if constexpr (DD == SV_BF16) v = __uint_as_float(static_cast<uint32_t>(Rr.ysm[j]) << 16);
+            else v = Rr.ysmf[j];
+        } else {
+            v = ld_elem<DD>(Rr.drow, j);
+        }
+        v = on ? v : -INFINITY;
+    }
+    return ex2(fmaf(v, Rr.c, -Rr.mq)) * Rr.invSq;
+}
+
+// the weight of id x: p, or max(0, p - q) with resid
+template <int DT, int DD, int YM>
+__device__ __forceinline__ float weight_at(const SampleArgs& A, const RaceRow& Rr, int32_t x, bool resid)
+{
+    const float z = ld_elem<DT>(Rr.trow, x);
+    float w = ex2(fmaf(z, Rr.c, -Rr.m)) * Rr.invS;
+    if (resid) {
+        const uint32_t jm = YM == kYIdentity ? 0u : A.plan.jmap[x];
+        w = fmaxf(w - q_at<DD, YM>(A, Rr, x, jm), 0.f);
+    }
+    return w;
+}
+
+// the key of id x with weight w; +inf when w is not positive
+__device__ __forceinline__ float key_of(const RaceRow& Rr, int32_t x, float w)
+{
+    if (!(w > 0.f)) return INFINITY;
+    const uint4 w4 = philox_block(Rr.key, static_cast<uint32_t>(x) >> 2, Rr.row, Rr.tag);
+    return race_key(one_minus_uniform_from_word(word_of(w4, x & 3)), w);
+}
+
+// Pass 1 of the race over ids [x_lo, x_hi), one warp (steps warp, warp + nwarps, ...): every lane
+// finds the id of its largest target logit (packed maxima, no exponential) and takes that id's
+// exact key; the warp's smallest lowers the CTA's shared bound (fp32 bits in *bound_s).
+template <int DT, int DD, int YM>
+__device__ void race_seed_pass(const SampleArgs& A, const RaceRow& Rr, int32_t x_lo, int32_t x_hi, bool resid,
+                               unsigned int* bound_s, int warp, int nwarps)
+{
+    constexpr int ZW = DT == SV_BF16 ? 1 : 2;
+    constexpr int kBatch = 4;  // steps whose loads are in flight together
+    const int lane = threadIdx.x & 31;
+    float zb = -INFINITY;
+    int32_t xb = -1;
+    const int32_t step = kRaceStep * nwarps;
+    for (int32_t x0 = x_lo + kRaceStep * warp; x0 < x_hi; x0 += kBatch * step) {
+        uint4 zq[kBatch][ZW];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) load_z8<DT>(A, Rr, x0 + b * step + 8 * lane, x_hi, zq[b]);
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const float m = fmaxf(max4<DT>(zq[b], 0), max4<DT>(zq[b], 1));
+            if (m > zb) {  // ids ascend within the lane: the first of equal maxima
+                zb = m;
+                const int32_t x = x0 + b * step + 8 * lane;
+#pragma unroll
+                for (int e = 7; e >= 0; --e)
+                    if (z_of<DT>(zq[b], e) == m) xb = x + e;
             }
         }
     }
-    // the key of the warp's heaviest id
-    float nw = hw;
-    int32_t nx = hx;
-    warp_argmax(nw, nx);
-    if (lane == 0) {
-        float kh = INFINITY;
-        if (nw > 0.f && nx != INT32_MAX) {
-            const uint4 w4 = philox_block(Rr.key, static_cast<uint32_t>(nx) >> 2, Rr.row, Rr.tag);
-            const uint32_t wd = (nx & 3) == 0 ? w4.x : (nx & 3) == 1 ? w4.y : (nx & 3) == 2 ? w4.z : w4.w;
-            kh = race_key(one_minus_uniform_from_word(wd), nw);
-        }
-        sh.wkey[warp] = kh;
+    float kb = xb >= 0 ? key_of(Rr, xb, weight_at<DT, DD, YM>(A, Rr, xb, resid)) : INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) kb = fminf(kb, __shfl_xor_sync(0xffffffffu, kb, o));
+    if (lane == 0 && kb < INFINITY) {
+        atomicMin(bound_s, __float_as_uint(kb));
+        if (Rr.bound_g) atomicMin(Rr.bound_g, __float_as_uint(kb));
     }
-    __syncthreads();
-    if (tid == 0) {
-        float b = bound_in;
-        for (int i = 0; i < kRaceThreads / 32; ++i) b = fminf(b, sh.wkey[i]);
-        if (bound_g != nullptr && b < INFINITY) {
-            const unsigned int old = atomicMin(bound_g, __float_as_uint(b));
-            b = fminf(b, __uint_as_float(old));
+}
+
+// A queued block of four ids of pass 2: its first id, its raw target logits and draft ids.
+struct RaceQ {
+    int32_t x[2 * 32];
+    uint4 z[2 * 32];   // bf16: the first 8 bytes; fp32: all 16
+    uint2 j[2 * 32];   // four 16-bit draft ids (d2t)
+};
+
+// the full test of one queued block: weights, the Philox block when one of its ids can win,
+// keys where 1 - u <= B w (w = 0 never passes); updates the lane's running minimum (blocks
+// reach a lane out of id order, so equal keys compare ids)
+template <int DT, int DD, int YM>
+__device__ __forceinline__ void race_block(const SampleArgs& A, const RaceRow& Rr, bool resid, int32_t x,
+                                           uint4 zq, uint2 jq, float tfl, float bs, float& best, int32_t& bx)
+{
+    float w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        float z;
+        if constexpr (DT == SV_BF16) {
+            const uint32_t ww = e < 2 ? zq.x : zq.y;
+            z = (e & 1) ? bf16_hi(ww) : bf16_lo(ww);
+        } else {
+            z = __uint_as_float(e == 0 ? zq.x : e == 1 ? zq.y : e == 2 ? zq.z : zq.w);
         }
-        sh.bound = b;
+        const float t = fmaf(z, Rr.c, -Rr.m);
+        w[e] = t >= tfl ? ex2(t) * Rr.invS : 0.f;
     }
-    __syncthreads();
-    const float bs = sh.bound * kRaceSlack;
-    float best = INFINITY;
+    if (resid) {
+        const uint32_t jm[4] = {jq.x & 0xFFFFu, jq.x >> 16, jq.y & 0xFFFFu, jq.y >> 16};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w[e] = fmaxf(w[e] - q_at<DD, YM>(A, Rr, x + e, jm[e]), 0.f);
+    }
+    const float wmax = fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3]));
+    if (!(wmax * bs >= kRaceMinGap)) return;
+    const uint4 w4 = philox_block(Rr.key, static_cast<uint32_t>(x) >> 2, Rr.row, Rr.tag);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float om = one_minus_uniform_from_word(word_of(w4, e));
+        if (om <= w[e] * bs) {  // rare
+            const float kx = race_key(om, w[e]);
+            if (kx < best || (kx == best && x + e < bx)) {
+                best = kx;
+                bx = x + e;
+            }
+        }
+    }
+}
+
+// Pass 2: the race over ids [x_lo, x_hi) by one warp, against the shared bound; returns the warp's
+// packed (key, id) minimum to every lane.  Each lane tests its two blocks of four ids per step on
+// their largest raw logit alone; the blocks that pass go to the warp's queue in shared memory,
+// which the warp works off 32 blocks at a time, one per lane, so that the exponentials and the
+// Philox rounds run with every lane busy.
+template <int DT, int DD, int YM>
+__device__ unsigned long long race_pass(const SampleArgs& A, const RaceRow& Rr, int32_t x_lo, int32_t x_hi,
+                                        bool resid, unsigned int* bound_s, RaceQ& q, int warp, int nwarps)
+{
+    const int lane = threadIdx.x & 31;
+    const unsigned lt = (1u << lane) - 1u;
+    float best = INFINITY;  // this lane's running minimum and its id
     int32_t bx = INT32_MAX;
+    float B = __uint_as_float(*reinterpret_cast<volatile unsigned int*>(bound_s));
+    float tfl = race_t_floor(B, Rr.S);
+    float zfl = tfl > -INFINITY ? (tfl + Rr.m) / Rr.c : -INFINITY;  // the same floor on raw logits
+    uint32_t qh = 0, qn = 0;  // the queue's head and length (warp-uniform)
+    constexpr int ZW = DT == SV_BF16 ? 1 : 2;
+    constexpr int kBatch = 2;  // steps whose loads are in flight together
+    const int32_t step = kRaceStep * nwarps;
+    for (int32_t xb0 = x_lo + kRaceStep * warp; xb0 < x_hi; xb0 += kBatch * step) {
+        uint4 zb[kBatch][ZW], jb[kBatch];
 #pragma unroll
-    for (int v = 0; v < kRaceVecs; ++v) {
-        const int32_t x = x0 + 8 * (tid + kRaceThreads * v);
+        for (int b = 0; b < kBatch; ++b) {
+            const int32_t x = xb0 + b * step + 8 * lane;
+            load_z8<DT>(A, Rr, x, x_hi, zb[b]);
+            jb[b] = resid && YM != kYIdentity ? load_j8(A, x) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        // the bound the request's other parts have reached (read now, used at the batch's end)
+        const unsigned int gb = Rr.bound_g ? *reinterpret_cast<volatile unsigned int*>(Rr.bound_g) : 0x7F800000u;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            bool need = false;
+        for (int b = 0; b < kBatch; ++b) {
+            const int32_t x = xb0 + b * step + 8 * lane;
+            // the blocks that can hold a winner join the queue (at most 31 + 32 entries at a time)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) need |= wv[v][4 * h + e] * bs >= kRaceMinGap;
-            if (!need) continue;
-            const uint4 w4 = philox_block(Rr.key, static_cast<uint32_t>(x >> 2) + h, Rr.row, Rr.tag);
-            const uint32_t words[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float w = wv[v][4 * h + e];
-                if (!(w > 0.f)) continue;
-                const float om = one_minus_uniform_from_word(words[e]);
-                if (!(om <= w * bs)) continue;
-                const float kx = race_key(om, w);
-                if (kx < best) {  // ascending ids within the thread
-                    best = kx;
-                    bx = x + 4 * h + e;
+            for (int h = 0; h < 2; ++h) {
+                const bool pass = max4<DT>(zb[b], h) >= zfl;  // false past the end (-inf)
+                const unsigned bal = __ballot_sync(0xffffffffu, pass);
+                if (pass) {
+                    const uint32_t s = (qh + qn + __popc(bal & lt)) & 63u;
+                    q.x[s] = x + 4 * h;
+                    if constexpr (DT == SV_BF16)
+                        q.z[s] = h == 0 ? make_uint4(zb[b][0].x, zb[b][0].y, 0u, 0u)
+                                        : make_uint4(zb[b][0].z, zb[b][0].w, 0u, 0u);
+                    else
+                        q.z[s] = zb[b][h];
+                    q.j[s] = h == 0 ? make_uint2(jb[b].x, jb[b].y) : make_uint2(jb[b].z, jb[b].w);
+                }
+                qn += __popc(bal);
+                __syncwarp();
+                if (qn >= 32) {  // warp-uniform
+                    const uint32_t s = (qh + lane) & 63u;
+                    race_block<DT, DD, YM>(A, Rr, resid, q.x[s], q.z[s], q.j[s], tfl, B * kRaceSlack, best, bx);
+                    qh = (qh + 32) & 63u;
+                    qn -= 32;
+                    __syncwarp();
                 }
             }
         }
+        // a lower key lowers this lane's bound and the shared ones; the shared bounds lower this lane's
+        const float sb = fminf(__uint_as_float(*reinterpret_cast<volatile unsigned int*>(bound_s)), __uint_as_float(gb));
+        if (best < sb) {
+            atomicMin(bound_s, __float_as_uint(best));
+            if (Rr.bound_g) atomicMin(Rr.bound_g, __float_as_uint(best));
+        }
+        const float nb = fminf(fminf(best, sb), B);
+        if (nb < B) {
+            B = nb;
+            tfl = race_t_floor(B, Rr.S);
+            zfl = tfl > -INFINITY ? (tfl + Rr.m) / Rr.c : -INFINITY;
+        }
     }
-    unsigned long long pk = bx == INT32_MAX ? kNoKey : pack_key(best, bx);
-    pk = warp_min_u64(pk);
-    if (lane == 0) sh.best[warp] = pk;
-    __syncthreads();
-    unsigned long long out = kNoKey;
-#pragma unroll
-    for (int i = 0; i < kRaceThreads / 32; ++i) out = sh.best[i] < out ? sh.best[i] : out;
-    __syncthreads();  // the shared arrays are written again by the next slice
-    return out;
+    if (lane < qn) {  // the queue's rest
+        const uint32_t s = (qh + lane) & 63u;
+        race_block<DT, DD, YM>(A, Rr, resid, q.x[s], q.z[s], q.j[s], tfl, B * kRaceSlack, best, bx);
+    }
+    __syncwarp();
+    return warp_min_u64(bx == INT32_MAX ? kNoKey : pack_key(best, bx));
 }
 
 }  // namespace
 
-template <int DT, int DD>
-__global__ void __launch_bounds__(kRaceThreads) race_flat_kernel(SampleArgs A)
+template <int DT, int DD, int YM>
+__global__ void __launch_bounds__(kRaceThreads, 2) race_rows_kernel(SampleArgs A, int64_t share)
 {
+    extern __shared__ __align__(16) unsigned char ysm_raw[];  // the selected draft row (d2t residual rows)
     __shared__ int32_t n_s, last_s;
     __shared__ uint32_t fl_s;
+    __shared__ unsigned int bound_s;
+    __shared__ unsigned long long wbest_s[kRaceWarps];
     __shared__ unsigned long long best_s;
-    __shared__ RaceShared sh;
-    __shared__ uint32_t red_u[kRaceThreads / 32];
-    const int tid = threadIdx.x, lane = tid & 31;
+    __shared__ uint32_t red_u[kRaceWarps];
+    __shared__ RaceQ queue_s[kRaceWarps];  // every warp's queue of blocks for pass 2
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int32_t k = A.k;
-    const int32_t nsl = (A.V + kRaceSlice - 1) / kRaceSlice;
-    const int64_t items = static_cast<int64_t>(A.R) * nsl;
+    // The rows, padded to whole 256-id steps, laid end to end: this CTA takes [g_lo, g_hi).
+    const int64_t Vp = (static_cast<int64_t>(A.V) + kRaceStep - 1) / kRaceStep * kRaceStep;
+    const int64_t total = static_cast<int64_t>(A.R) * Vp;
+    const int64_t g_lo = static_cast<int64_t>(blockIdx.x) * share, g_hi = min(total, g_lo + share);
     pdl_wait_primary();
-    for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
-        const int32_t r = static_cast<int32_t>(it / nsl);
-        const int32_t sl = static_cast<int32_t>(it - static_cast<int64_t>(r) * nsl);
+    for (int64_t g = g_lo; g < g_hi;) {
+        const int32_t r = static_cast<int32_t>(g / Vp);
+        const int64_t rbase = static_cast<int64_t>(r) * Vp;
+        const int32_t x_lo = static_cast<int32_t>(g - rbase);
+        const int32_t x_hi = static_cast<int32_t>(min(Vp, g_hi - rbase));
+        g = rbase + x_hi;
+        // the CTAs that share request r's row, and whether this one holds its first part
+        const int32_t parts = static_cast<int32_t>((rbase + Vp - 1) / share - rbase / share + 1);
+        const bool first = x_lo == 0;
         const RowStat* st = A.stats + static_cast<int64_t>(r) * (k + 1);
         const int32_t* d = A.draft + static_cast<int64_t>(r) * k;
         const float T = A.temp[r];
@@ -1885,89 +2028,128 @@ __global__ void __launch_bounds__(kRaceThreads) race_flat_kernel(SampleArgs A)
             if (lane == 0) {
                 n_s = n;
                 fl_s = fl;
+                bound_s = 0x7F800000u;  // +inf
             }
         }
         __syncthreads();
         const int32_t n = n_s;
         const uint32_t fl = fl_s;
-        __syncthreads();  // n_s and fl_s are written again by the next item
         const bool bad_rows = (fl & (kFlagNaN | kFlagPosInf | kFlagAllNegInf | kFlagDraftBad)) != 0;
         const bool greedy = !(T > 0.f) || bad_rows;
         const bool residual = n < k;
         uint32_t status = 0;
         int32_t token = -1;
+        bool commit = true;
         if (greedy) {
-            if (sl != 0) continue;  // block-uniform
+            commit = first;  // block-uniform
             token = st[n].amax;
         } else {
             const RowStat rs = st[n];
             RaceRow Rr;
             Rr.trow = A.tbase + (static_cast<int64_t>(r) * (k + 1) + n) * A.tstride;
             Rr.drow = residual ? A.dbase + (static_cast<int64_t>(r) * k + n) * A.dstride : nullptr;
+            Rr.ysm = nullptr;
+            Rr.ysmf = nullptr;
             Rr.c = kLog2e / T;
             Rr.m = rs.m;
+            Rr.S = rs.s;
             Rr.invS = 1.f / rs.s;
             Rr.mq = rs.mq;
             Rr.invSq = residual ? 1.f / rs.sq : 0.f;
             Rr.key = philox_key(A.seeds[r]);
             Rr.row = static_cast<uint32_t>(n);
             Rr.tag = residual ? kTagResidual : kTagBonus;
-            const unsigned long long mine =
-                race_slice<DT, DD>(A, Rr, sl * kRaceSlice, residual, A.race_bound + r, INFINITY, sh);
-            if (tid == 0) {
-                if (mine != kNoKey) atomicMin(A.race_best + r, mine);
-                __threadfence();
-                const unsigned int done = atomicAdd(A.race_done + r, 1u);
-                last_s = done == static_cast<unsigned int>(nsl - 1);
-                if (last_s) {
-                    __threadfence();
-                    best_s = atomicOr(A.race_best + r, 0ull);
+            Rr.bound_g = parts > 1 ? A.race_bound + r : nullptr;
+            constexpr int ED = DD == SV_BF16 ? 2 : 4;
+            // the selected draft row into shared memory, for the d2t gathers of the residual weights
+            const uint32_t ybytes = static_cast<uint32_t>(A.Vd) * ED;
+            if (YM == kYShared && residual) {  // the launch checked that the row fits, aligned
+                const uint4* src = reinterpret_cast<const uint4*>(Rr.drow);
+                uint4* dst = reinterpret_cast<uint4*>(ysm_raw);
+                constexpr int kY = 4;  // loads in flight per thread
+                for (uint32_t i0 = tid; i0 < ybytes / 16; i0 += kY * kRaceThreads) {
+                    uint4 v[kY];
+#pragma unroll
+                    for (int b = 0; b < kY; ++b)
+                        if (i0 + b * kRaceThreads < ybytes / 16) v[b] = __ldg(src + i0 + b * kRaceThreads);
+#pragma unroll
+                    for (int b = 0; b < kY; ++b)
+                        if (i0 + b * kRaceThreads < ybytes / 16) dst[i0 + b * kRaceThreads] = v[b];
                 }
+                if (DD == SV_BF16) Rr.ysm = reinterpret_cast<const uint16_t*>(ysm_raw);
+                else Rr.ysmf = reinterpret_cast<const float*>(ysm_raw);
             }
             __syncthreads();
-            const bool last = last_s != 0;
-            unsigned long long best = best_s;
-            __syncthreads();  // last_s and best_s are written again by the next item
-            if (!last) continue;  // block-uniform
-            if (best == kNoKey && residual) {
-                // no residual mass anywhere: the correction is drawn from p (same row and tag),
-                // by this item alone, slice by slice
-                status |= SV_ST_RESIDUAL_ZERO;
-                float bnd = INFINITY;
-                for (int32_t s2 = 0; s2 < nsl; ++s2) {
-                    const unsigned long long b2 = race_slice<DT, DD>(A, Rr, s2 * kRaceSlice, false, nullptr, bnd, sh);
-                    if (b2 < best) best = b2;
-                    if (best != kNoKey) bnd = __uint_as_float(static_cast<uint32_t>(best >> 32));
+            const int32_t xe = min(x_hi, A.V);
+            // pass 1 sets the bound from every lane's largest logit; pass 2 is the pruned race
+            race_seed_pass<DT, DD, YM>(A, Rr, x_lo, xe, residual, &bound_s, warp, kRaceWarps);
+            __syncthreads();
+            unsigned long long mine =
+                race_pass<DT, DD, YM>(A, Rr, x_lo, xe, residual, &bound_s, queue_s[warp], warp, kRaceWarps);
+            if (lane == 0) wbest_s[warp] = mine;
+            __syncthreads();
+            if (tid == 0) {
+                unsigned long long b = kNoKey;
+                for (int i = 0; i < kRaceWarps; ++i) b = wbest_s[i] < b ? wbest_s[i] : b;
+                last_s = 1;
+                if (parts > 1) {
+                    if (b != kNoKey) atomicMin(A.race_best + r, b);
+                    __threadfence();
+                    last_s = atomicAdd(A.race_done + r, 1u) == static_cast<unsigned int>(parts - 1);
+                    if (last_s) {
+                        __threadfence();
+                        b = atomicOr(A.race_best + r, 0ull);
+                    }
                 }
+                best_s = b;
+            }
+            __syncthreads();
+            commit = last_s != 0;  // block-uniform
+            unsigned long long best = best_s;
+            if (commit && best == kNoKey && residual) {
+                // no residual mass anywhere: the correction is drawn from p (same row and tag)
+                status |= SV_ST_RESIDUAL_ZERO;
+                __syncthreads();
+                if (tid == 0) bound_s = 0x7F800000u;
+                __syncthreads();
+                Rr.bound_g = nullptr;  // the bound of the residual race says nothing about p's
+                race_seed_pass<DT, DD, YM>(A, Rr, 0, A.V, false, &bound_s, warp, kRaceWarps);
+                __syncthreads();
+                mine = race_pass<DT, DD, YM>(A, Rr, 0, A.V, false, &bound_s, queue_s[warp], warp, kRaceWarps);
+                if (lane == 0) wbest_s[warp] = mine;
+                __syncthreads();
+                for (int i = 0; i < kRaceWarps; ++i) best = wbest_s[i] < best ? wbest_s[i] : best;
             }
             token = best == kNoKey ? 0 : static_cast<int32_t>(best & 0xFFFFFFFFu);
             if (residual && (rs.flags & kFlagOffSupport)) status |= SV_ST_OFF_SUPPORT;
         }
-        // ---- commit (one item per request) ----
-        for (int32_t j = tid; j < k; j += kRaceThreads)
-            if (d[j] < 0 || d[j] >= A.V) status |= SV_ST_TOKEN_RANGE;
-        if (fl & kFlagTimeout) status |= SV_ST_TIMEOUT;
-        if (bad_rows) status |= SV_ST_BAD_LOGITS;
-        if (T < 0.f || T != T) status |= SV_ST_BAD_TEMP;
-        if (!A.identity && (A.plan.header[2] != 0 || A.plan.header[0] != A.V || A.plan.header[1] != A.Vd))
-            status |= SV_ST_BAD_D2T;
-        int32_t* out = A.tokens + static_cast<int64_t>(r) * (k + 1);
-        for (int32_t j = tid; j <= k; j += kRaceThreads) out[j] = j < n ? d[j] : (j == n ? token : -1);
-        if (greedy) {
-            // no sampling statistics for greedily verified requests
-            for (int32_t j = tid; j < k; j += kRaceThreads) {
-                const int64_t o = static_cast<int64_t>(r) * k + j;
-                if (A.tv) A.tv[o] = NAN;
-                if (A.pd) A.pd[o] = NAN;
-                if (A.qd) A.qd[o] = NAN;
+        if (commit) {
+            // ---- commit (one CTA per request) ----
+            for (int32_t j = tid; j < k; j += kRaceThreads)
+                if (d[j] < 0 || d[j] >= A.V) status |= SV_ST_TOKEN_RANGE;
+            if (fl & kFlagTimeout) status |= SV_ST_TIMEOUT;
+            if (bad_rows) status |= SV_ST_BAD_LOGITS;
+            if (T < 0.f || T != T) status |= SV_ST_BAD_TEMP;
+            if (!A.identity && (A.plan.header[2] != 0 || A.plan.header[0] != A.V || A.plan.header[1] != A.Vd))
+                status |= SV_ST_BAD_D2T;
+            int32_t* out = A.tokens + static_cast<int64_t>(r) * (k + 1);
+            for (int32_t j = tid; j <= k; j += kRaceThreads) out[j] = j < n ? d[j] : (j == n ? token : -1);
+            if (greedy) {
+                // no sampling statistics for greedily verified requests
+                for (int32_t j = tid; j < k; j += kRaceThreads) {
+                    const int64_t o = static_cast<int64_t>(r) * k + j;
+                    if (A.tv) A.tv[o] = NAN;
+                    if (A.pd) A.pd[o] = NAN;
+                    if (A.qd) A.qd[o] = NAN;
+                }
+            }
+            status = block_or<kRaceThreads>(status, red_u);
+            if (tid == 0) {
+                A.accept_len[r] = n;
+                if (A.status) A.status[r] = static_cast<int32_t>(status);
             }
         }
-        status = block_or<kRaceThreads>(status, red_u);
-        if (tid == 0) {
-            A.accept_len[r] = n;
-            if (A.status) A.status[r] = static_cast<int32_t>(status);
-        }
-        __syncthreads();  // red_u is written again by the next item
+        __syncthreads();  // the shared state is written again by the next part
     }
 }
 
@@ -2184,24 +2366,32 @@ static cudaError_t launch_sample_t(const Rows& t, const Rows& d, const int32_t* 
         e = cudaLaunchKernelEx(&cfg, sample_rows_kernel<DT, DD>, A);
     }
     if (e != cudaSuccess) return e;
-    // the race: work items of (request, slice), CTAs resident at once on every SM
-    auto* race = race_flat_kernel<DT, DD>;
-    static int race_per_sm = 0;  // per (DT, DD) instance
-    if (race_per_sm == 0) {
-        int b = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, race, kRaceThreads, 0) != cudaSuccess || b < 1) b = 1;
-        race_per_sm = b;
-    }
-    const int64_t items = static_cast<int64_t>(R) * ((t.width + kRaceSlice - 1) / kRaceSlice);
-    const int64_t rgrid = std::max<int64_t>(1, std::min<int64_t>(items, static_cast<int64_t>(sms > 0 ? sms : 148) * race_per_sm));
+    // the race: one CTA per request; a request's row is split over several CTAs while the batch
+    // leaves CTA slots (two per SM) idle
+    // the race: the rows, padded to whole 256-id steps and laid end to end, in equal shares over one
+    // wave of CTAs (two per SM), each share at least two steps per warp
+    const int64_t slots = 2LL * (sms > 0 ? sms : 148);
+    const int64_t Vp = (static_cast<int64_t>(t.width) + kRaceStep - 1) / kRaceStep * kRaceStep;
+    const int64_t total_ids = static_cast<int64_t>(R) * Vp;
+    const int64_t min_share = 2LL * kRaceWarps * kRaceStep;
+    int64_t share = std::max<int64_t>(min_share, (total_ids + slots - 1) / slots);
+    share = (share + kRaceStep - 1) / kRaceStep * kRaceStep;
+    const int64_t rgrid = (total_ids + share - 1) / share;
+    const uint32_t ybytes = static_cast<uint32_t>(d.width) * d.esize;
+    const bool yshared = !identity && A.dbulk && ybytes <= kRaceSmemRow && ybytes % 16 == 0;
+    const size_t race_smem = yshared ? ybytes : 0;
+    auto* race = identity ? race_rows_kernel<DT, DD, kYIdentity>
+                          : (yshared ? race_rows_kernel<DT, DD, kYShared> : race_rows_kernel<DT, DD, kYGlobal>);
+    e = cudaFuncSetAttribute(race, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(race_smem));
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg2 = {};
     cfg2.gridDim = dim3(static_cast<unsigned>(rgrid));
     cfg2.blockDim = dim3(kRaceThreads);
-    cfg2.dynamicSmemBytes = 0;
+    cfg2.dynamicSmemBytes = race_smem;
     cfg2.stream = stream;
     cfg2.attrs = attr;
     cfg2.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg2, race, A);
+    return cudaLaunchKernelEx(&cfg2, race, A, share);
 }
 
 cudaError_t launch_verify_sample(const Rows& target, const Rows& draft_logits, const int32_t* d2t,

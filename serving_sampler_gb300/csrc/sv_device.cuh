@@ -145,11 +145,11 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, PhiloxKey key)
             k0 += 0x9E3779B9u;
             k1 += 0xBB67AE85u;
         }
-        const uint32_t hi_a = __umulhi(0xD2511F53u, c.x);
-        const uint32_t lo_a = 0xD2511F53u * c.x;
-        const uint32_t hi_b = __umulhi(0xCD9E8D57u, c.z);
-        const uint32_t lo_b = 0xCD9E8D57u * c.z;
-        c = make_uint4(hi_b ^ c.y ^ k0, lo_b, hi_a ^ c.w ^ k1, lo_a);
+        // one 32 x 32 -> 64-bit product each: high and low halves from the same multiply
+        const uint64_t pa = static_cast<uint64_t>(0xD2511F53u) * c.x;
+        const uint64_t pb = static_cast<uint64_t>(0xCD9E8D57u) * c.z;
+        c = make_uint4(static_cast<uint32_t>(pb >> 32) ^ c.y ^ k0, static_cast<uint32_t>(pb),
+                       static_cast<uint32_t>(pa >> 32) ^ c.w ^ k1, static_cast<uint32_t>(pa));
     }
     return c;
 }

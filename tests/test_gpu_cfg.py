@@ -7,7 +7,7 @@ import torch
 
 import oracle
 import workloads
-from tests.sampling_parity import compare
+from tests.sampling_parity import assert_pooled_rate, by_request, compare
 
 pytestmark = pytest.mark.gpu
 
@@ -57,10 +57,34 @@ def test_cfg_greedy_and_partition_offsets(sv):
     compare(_run(sv, w2), _oracle(w2))
 
 
+def _oracle_par(w):
+    """The oracle over every request of a batch, on the host threads."""
+    k, S = w["k"], w["S"]
+    c, u, y = (workloads.host_rows(w[key]) for key in ("cond", "uncond", "draft_logits"))
+    draft = w["draft"].cpu().numpy()
+    seeds = w["seeds"].cpu().numpy().view(np.uint64)
+    T = w["temperature"].cpu().numpy()
+    rr = (k + 1) * S
+    return by_request(lambda lo, hi: oracle.cfg_merge_sample(
+        c[lo * rr:hi * rr], u[lo * rr:hi * rr], w["cb_id_base"], w["cb_data_offset"], S, w["W"], w["w"],
+        y[lo * k * S:hi * k * S], hi - lo, k, draft[lo:hi], seeds[lo:hi], T[lo:hi]), w["R"])
+
+
 def test_cfg_workload_full_size(sv):
-    """256 requests x 5 frames x 9 codebooks (11,520 codebook rows): fewer than 1e-5 of the
-    rows may be exempt, so none.  Flat codebooks: most frames are rejected early."""
-    w = workloads.cfg_workload()
-    got, want = _run(sv, w), _oracle(w)
-    compare(got, want)
-    assert want["accept_len"].mean() < 2.0
+    """The full-size CFG configuration (256 requests x 5 frames x 9 codebooks of 4096) against the
+    oracle, then further seeded batches of it until more than 10^5 codebook rows are compared:
+    fewer than 1e-5 of the pooled rows may be exempt.  Flat codebooks: most frames are
+    rejected early."""
+    rows = exempt = b = 0
+    while rows < 100_000:
+        w = workloads.cfg_workload(batch=b)
+        got, want = _run(sv, w), _oracle_par(w)
+        exempt += compare(got, want, stats=b % 4 == 0, pooled=True, label=f"cfg batch {b}")
+        if b == 0:
+            assert want["accept_len"].mean() < 2.0
+            ref = _oracle(w)  # the threaded oracle gives the single-threaded oracle's bits
+            for key in ("accept_len", "tokens", "status", "tv"):
+                np.testing.assert_array_equal(np.nan_to_num(want[key]), np.nan_to_num(ref[key]), err_msg=key)
+        rows += w["R"] * (w["k"] + 1) * w["S"]
+        b += 1
+    assert_pooled_rate(exempt, rows)

@@ -60,3 +60,28 @@ def test_compare_rules():
     big = {key: np.concatenate([v, clean[key]]) for key, v in want.items()}   # 160,000 rows: one may be exempt
     gbig = {key: np.concatenate([v, clean[key]]) for key, v in got.items()}
     assert compare(gbig, big, stats=False, label="rate ok", log=False) == 1
+
+
+def test_threaded_oracle_equals_one_call():
+    """The GPU tests run the oracle on request ranges in host threads; the concatenated outputs
+    equal one call over the whole batch, bit for bit."""
+    import torch
+
+    import oracle
+    import workloads
+    from tests.sampling_parity import by_request
+
+    w = workloads.sample_batch(37, 3, 3000, 700, torch.bfloat16, T=[(0.7, 0.0, 1.1)[r % 3] for r in range(37)],
+                               sigma_pos=0.8, delta=2.0,
+                               seed=3, device="cpu")
+    R, k = w["R"], w["k"]
+    t, d = workloads.host_rows(w["target"]), workloads.host_rows(w["draft_logits"])
+    d2t, draft = w["d2t"].numpy(), w["draft"].numpy()
+    seeds, T = w["seeds"].numpy().view(np.uint64), w["temperature"].numpy()
+    one = oracle.verify_sample(t, d, d2t, R, k, draft, seeds, T)
+    par = by_request(lambda lo, hi: oracle.verify_sample(t[lo * (k + 1):hi * (k + 1)], d[lo * k:hi * k], d2t,
+                                                         hi - lo, k, draft[lo:hi], seeds[lo:hi], T[lo:hi]), R,
+                     threads=4)
+    assert set(one) == set(par)
+    for key in one:
+        np.testing.assert_array_equal(np.nan_to_num(one[key]), np.nan_to_num(par[key]), err_msg=key)

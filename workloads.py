@@ -228,11 +228,14 @@ def tiny_sample(device="cuda"):
                         seed_base=0, device=device)
 
 
-def d2t_workload(device="cuda", R: int = 128):
+def d2t_workload(device="cuda", R: int = 128, batch: int = 0):
     """128 requests x 7 drafts (+ bonus), V = 151,936 bf16, draft vocabulary 32,000 via a seeded
-    random injective d2t, T = 0.7, per-request seeds splitmix64(1234 + r)."""
+    random injective d2t, T = 0.7, per-request seeds splitmix64(1234 + r).  `batch` > 0 draws
+    another batch of the same configuration (other logits, drafts and request seeds; the same
+    d2t map, a constant of the draft model)."""
     return sample_batch(R, 7, V_QWEN, VD_DRAFT, torch.bfloat16, T=0.7, sigma_pos=D2T_SIGMA,
-                        delta=D2T_DELTA, z_sigma=3.0, seed=1237, seed_base=1234, device=device)
+                        delta=D2T_DELTA, z_sigma=3.0, seed=1237 + 7919 * batch,
+                        seed_base=1234 + 1_000_003 * batch, device=device, d2t_seed=1244)
 
 
 SWEEP_BATCHES = (1, 8, 64, 256, 1024)
@@ -293,9 +296,11 @@ def cfg_batch(R: int, k: int, S: int, W: int, w: float = 3.0, T=1.0, dtype=torch
                 seeds=seeds_tensor(seed_base, R, device), temperature=Tt)
 
 
-def cfg_workload(device="cuda", R: int = 256):
-    """256 requests, 9 codebooks x 4096 entries, 4 drafted frames (+1), bf16, w = 3, T = 1."""
-    return cfg_batch(R, 4, 9, 4096, 3.0, 1.0, torch.bfloat16, seed=1238, seed_base=1234 + 3, device=device)
+def cfg_workload(device="cuda", R: int = 256, batch: int = 0):
+    """256 requests, 9 codebooks x 4096 entries, 4 drafted frames (+1), bf16, w = 3, T = 1;
+    `batch` > 0 draws another batch of the same configuration."""
+    return cfg_batch(R, 4, 9, 4096, 3.0, 1.0, torch.bfloat16, seed=1238 + 7919 * batch,
+                     seed_base=1234 + 3 + 1_000_003 * batch, device=device)
 
 
 def pool_session(R: int = 64, chunks: int = 21, gamma: int = 32, N: int = 8, V: int = 151936, seed: int = 77,
