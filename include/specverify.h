@@ -380,6 +380,23 @@ int sv_suffix_append(int32_t* suffix, int32_t N, int32_t R, const int32_t* token
 int sv_accept_scan(const uint8_t* accept, const int32_t* draft, const int32_t* fix, int32_t R,
                    int32_t k, int32_t* accept_len, int32_t* tokens, sv_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * sv_selftest_wait_timeout -- a self-test of the library's bounded waits; the
+ * source pages have no counterpart.  Every wait of the library on a
+ * shared-memory barrier gives up after a time limit and reports
+ * SV_ST_TIMEOUT instead of hanging; this call makes one such wait run out on
+ * purpose, with the same wait routine and a caller-chosen limit, so a test can
+ * check that the timeout path works without any fault.
+ *
+ *   src16         16 readable, 16-byte aligned device bytes (copied once).
+ *   status        int32 [2] out (device): [0] SV_ST_TIMEOUT when the wait
+ *                 that cannot complete gave up (the expected result); [1] 1
+ *                 when the copy that was issued landed intact.
+ *   limit_cycles  the wait's limit in SM cycles (>= 1).
+ * Launches one warp on `stream`; nothing is in flight when it exits.
+ * ---------------------------------------------------------------------- */
+int sv_selftest_wait_timeout(const void* src16, int32_t* status, int64_t limit_cycles, sv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

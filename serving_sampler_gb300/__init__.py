@@ -87,6 +87,8 @@ def load(path: str | None = None):
     lib.sv_suffix_append.argtypes = [P, i32, i32, P, P, i32, P]
     lib.sv_accept_scan.argtypes = [P, P, P, i32, i32, P, P, P]
     lib.sv_accept_scan.restype = C.c_int
+    lib.sv_selftest_wait_timeout.argtypes = [P, P, C.c_int64, P]
+    lib.sv_selftest_wait_timeout.restype = C.c_int
     _lib = lib
     return lib
 
@@ -342,3 +344,14 @@ def accept_scan(accept, draft, fix, out: dict | None = None, stream=None) -> dic
     _check(lib.sv_accept_scan(_ptr(accept), _ptr(draft), _ptr(fix), R, k, _ptr(out["accept_len"]),
                               _ptr(out["tokens"]), _stream(stream)))
     return out
+
+
+def selftest_wait_timeout(limit_cycles: int, stream=None):
+    """Make one bounded barrier wait of the library run out on purpose (sv_selftest_wait_timeout);
+    returns the int32 [2] device status: [0] the timeout bit, [1] whether the real copy landed."""
+    import torch
+
+    src = torch.arange(4, dtype=torch.int32, device="cuda") + 0x5A5A0000
+    status = torch.full((2,), -1, dtype=torch.int32, device="cuda")
+    _check(load().sv_selftest_wait_timeout(_ptr(src), _ptr(status), limit_cycles, _stream(stream)))
+    return status

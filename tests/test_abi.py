@@ -135,6 +135,10 @@ def test_argument_checks_need_no_gpu(lib):
     assert sa(buf, 8, 1, buf, buf, 257, None) == -4
     assert sa(buf, 8, 1, None, buf, 4, None) == -1
     assert sa(buf, -1, 1, buf, buf, 4, None) == -1
+    st = lib.sv_selftest_wait_timeout
+    st.argtypes = [P, P, C.c_int64, P]
+    assert st(buf, buf, 0, None) == -1          # the wait's limit must be positive
+    assert st(P(0x10004), buf, 10, None) == -7  # the copy source must be 16-byte aligned
     c = lib.sv_cfg_merge_sample
     base = (C.c_int32 * 2)(0, 16)
     assert c(_rows(), _rows(width=8), C.cast(base, P), None, 2, 3.0, _rows(data=None), 1, 1, buf, buf, buf, buf,
