@@ -27,6 +27,7 @@
 // Temperature scaling works in log2 units: with c = log2(e) / T,
 // p(x) = 2^(z_x c - M) / S where M = max_x z_x c and S = sum 2^(z c - M).
 #include <algorithm>
+#include <numeric>
 #include <cfloat>
 #include <climits>
 
@@ -106,6 +107,18 @@ struct SampleArgs {
 };
 
 __host__ __device__ inline int64_t align256(int64_t b) { return (b + 255) / 256 * 256; }
+
+// The row passes take their units (request r, position j) in position-major order, L = j R + r;
+// a persistent CTA takes L, L + grid, ...  Position-major order ends with the cheaper bonus rows
+// (measured faster on the d2t workload, 85 against 93 us), and the host picks a grid coprime to
+// 6, so that a CTA's requests change parity and residue mod 3 from unit to unit (batches that
+// alternate greedy and sampled requests would otherwise split into greedy-only and sampled-only
+// CTAs).
+__device__ __forceinline__ void unit_rj(const SampleArgs& A, int64_t L, int32_t& r, int32_t& j)
+{
+    j = static_cast<int32_t>(L / A.R);
+    r = static_cast<int32_t>(L - static_cast<int64_t>(j) * A.R);
+}
 
 // the race's per-request board for this call: the row pass resets it, the race
 // kernel (launched after the row pass has completed) uses it
@@ -494,9 +507,10 @@ __global__ void __launch_bounds__(kRowThreads, 1) sample_rows_kernel(SampleArgs 
     uint32_t timeout = 0;
 
     const int64_t units = static_cast<int64_t>(A.R) * (A.k + 1);
-    for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
-        const int32_t r = static_cast<int32_t>(unit / (A.k + 1));
-        const int32_t j = static_cast<int32_t>(unit - static_cast<int64_t>(r) * (A.k + 1));
+    for (int64_t L = blockIdx.x; L < units; L += gridDim.x) {
+        int32_t r, j;
+        unit_rj(A, L, r, j);
+        const int64_t unit = static_cast<int64_t>(r) * (A.k + 1) + j;  // the row of (r, j)
         const float T = A.temp[r];
         const bool sampling = T > 0.f;
         const bool has_draft = sampling && j < A.k;
@@ -1074,6 +1088,7 @@ struct DraftRec {  // a TV warp's share of the draft row
 
 struct FastUnit {
     int32_t r, j;
+    int64_t row;    // r (k + 1) + j, the unit's row of the statistics
     int32_t rot;    // chunk s goes to stream warp (s + rot) mod kStreamWarps
     bool sampling, has_draft;
     const char* trow;
@@ -1084,12 +1099,11 @@ struct FastUnit {
 __device__ __forceinline__ FastUnit fast_unit(const SampleArgs& A, int64_t unit, float T)
 {
     FastUnit u;
-    const int32_t un = static_cast<int32_t>(unit);  // R * (k + 1) < 2^31 (checked by the caller)
-    u.r = un / (A.k + 1);
-    u.j = un - u.r * (A.k + 1);
+    unit_rj(A, unit, u.r, u.j);  // R * (k + 1) < 2^31 (checked by the caller)
+    u.row = static_cast<int64_t>(u.r) * (A.k + 1) + u.j;
     u.sampling = T > 0.f;
     u.has_draft = u.sampling && u.j < A.k;
-    u.trow = A.tbase + unit * A.tstride;
+    u.trow = A.tbase + u.row * A.tstride;
     u.drow = u.has_draft ? A.dbase + (static_cast<int64_t>(u.r) * A.k + u.j) * A.dstride : nullptr;
     u.n = (A.V + kChunkElems - 1) / kChunkElems;
     const uint64_t sd = A.seeds[u.r];
@@ -1112,7 +1126,7 @@ __device__ __forceinline__ int32_t warp_chunks(int32_t n, int32_t q0)
 
 __device__ __forceinline__ float unit_temp(const SampleArgs& A, int64_t unit)
 {
-    return A.temp[static_cast<int32_t>(unit) / (A.k + 1)];
+    return A.temp[static_cast<int32_t>(unit % A.R)];
 }
 
 // issue chunk q of unit u into `stage` (lane 0 only)
@@ -1608,7 +1622,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
             rs.amax = amax;
             rs.flags = flags;
             rs.accept = acc;
-            A.stats[unit] = rs;
+            A.stats[u.row] = rs;
             if (u.j < A.k) {
                 const int64_t o = static_cast<int64_t>(u.r) * A.k + u.j;
                 if (A.tv) A.tv[o] = tvv;
@@ -2228,7 +2242,12 @@ SampleLayout sample_layout(int64_t R, int32_t k, int32_t V, int32_t Vd, int et, 
     L.rbest = take(R * 8);
     L.rdone = take(R * 4);
     const int64_t units = R * (k + 1);
-    L.grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(units, sms > 0 ? sms : 148)));
+    // one CTA per unit while they fit one per SM; else the largest grid within one CTA per SM that
+    // is coprime to 6 (see unit_rj)
+    int64_t g = std::max<int64_t>(1, std::min<int64_t>(units, sms > 0 ? sms : 148));
+    if (g < units)
+        while (g > 1 && std::gcd<int64_t>(g, 6) != 1) --g;
+    L.grid = static_cast<int>(g);
     const int64_t resident = align256(static_cast<int64_t>(Vd) * ed) + align256(static_cast<int64_t>(Vd) * et);
     const size_t ring = kRowHeader + static_cast<size_t>(kStages) * kStageBytes;
     L.smem_mode = ring + resident <= kSmemBudget ? 1 : 0;
