@@ -88,3 +88,17 @@ def test_cfg_workload_full_size(sv):
         rows += w["R"] * (w["k"] + 1) * w["S"]
         b += 1
     assert_pooled_rate(exempt, rows)
+
+
+def test_near_tie_codebook_races_outside_the_margin(sv):
+    """CFG codebook races whose two smallest keys are within 2e-6 .. 1e-4 (relative): outside the
+    exempt margin, so the kernel must pick exactly the oracle's token."""
+    R, k, S, W = 40_000, 1, 4, 64
+    w = workloads.cfg_batch(R, k, S, W, 2.0, 1.0, torch.float32, sigma_h=0.6, bump=1.0, seed=88)
+    got, want = _run(sv, w), _oracle_par(w)
+    compare(got, want, stats=False)
+    rm = want["race_margin"]
+    near = ((rm > 2e-6) & (rm < 1e-4)).any(axis=1)
+    assert near.sum() >= 5, near.sum()
+    for key in ("accept_len", "tokens"):
+        np.testing.assert_array_equal(got[key][near], want[key][near], err_msg=key)

@@ -325,3 +325,19 @@ def test_zero_residual_mass_on_the_bulk_copy_path(sv, dtype):
     assert np.all(st[::2] & 4) and np.all(st[::2] & 8)
     ids = d2t[100 + torch.arange(0, R, 2, device="cuda")].cpu().numpy()
     assert np.all(want["accept_len"][::2] == 1) and np.all(want["tokens"][::2, 1] == ids)
+
+
+def test_near_tie_races_outside_the_margin(sv):
+    """Races whose two smallest keys are within 2e-6 .. 1e-4 of each other (relative): close, but
+    outside the exempt margin, so the kernel's pruned race must pick exactly the oracle's token.
+    600,000 requests of 64 ids (fp32, k = 1) hold several dozen such races."""
+    R, k, V = 600_000, 1, 64
+    w = workloads.sample_batch(R, k, V, None, torch.float32, T=1.0, sigma_pos=0.3, z_sigma=1.0, seed=77,
+                               seed_base=99)
+    got, want = _run(sv, w), _oracle_par(w)
+    compare(got, want, stats=False)
+    rm = want["race_margin"]
+    near = (rm > 2e-6) & (rm < 1e-4) & (want["accept_margin"][:, 0] > 1e-6)
+    assert near.sum() >= 30, near.sum()
+    for key in ("accept_len", "tokens"):
+        np.testing.assert_array_equal(got[key][near], want[key][near], err_msg=key)
