@@ -378,7 +378,7 @@ class Native:
             # the d2t map is a constant of the draft model: its device plan is built once, here
             self.plan = sv.d2t_plan(w["d2t"], w["V"])
             self.launches = sv.LAUNCHES["verify_sample"]
-            self.kernel, self.kernel_file = "sample_rows_fast_kernel + race_flat_kernel", "sample.cu"
+            self.kernel, self.kernel_file = "sample_rows_fast_kernel + race_rows_kernel", "sample.cu"
             self.profile = "sample_rows_d2t.md" if spec.name == "d2t" else None
 
     def call(self, inp, stream):
