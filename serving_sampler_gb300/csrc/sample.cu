@@ -101,6 +101,10 @@ struct SampleArgs {
     unsigned int* race_bound;
     unsigned long long* race_best;
     unsigned int* race_done;
+    // per target row and group of the fast row pass (2048 bf16 or 1024 fp32 ids): the first
+    // lane holding the group's largest logit, whose ids seed the race's bound; NULL without it
+    uint8_t* clane;
+    int32_t ngroups;
     char* gslots;        // global-memory Y / G buffers when they do not fit in shared memory
     int64_t gslot_bytes;
     int smem_mode;
@@ -1333,6 +1337,11 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
                         acc = ((ae[0] + ae[1]) + (ae[2] + ae[3])) + ((ae[4] + ae[5]) + (ae[6] + ae[7]));
                     }
                     const float wm = warp_max(lm);
+                    if (u.sampling && A.clane) {  // the first lane holding the group's maximum
+                        const unsigned hold = __ballot_sync(0xffffffffu, lm == wm);
+                        if (lane == 0)
+                            A.clane[u.row * A.ngroups + cidx * Cfg::kHalves + h] = static_cast<uint8_t>(__ffs(hold) - 1);
+                    }
                     if (wm > bv) {  // warp-uniform, rare after the first chunks
                         bx = x0 + kHV * 32 * kEPV * h + static_cast<int32_t>(first_max_offset<DT>(qv, wm, lane));
                         bv = wm;
@@ -1862,6 +1871,51 @@ __device__ void race_seed_pass(const SampleArgs& A, const RaceRow& Rr, int32_t x
     }
 }
 
+// Pass 1 from the row pass's group records (fast row pass only): the groups that overlap the part,
+// one per lane; each reads the eight 16-byte vectors of the lane that held its largest logit (the
+// group may reach past the part: any id's key bounds the row's minimum) and takes the exact key
+// of their first id of the largest value; the warp's smallest lowers the CTA's bound and the
+// request's.
+template <int DT, int DD, int YM>
+__device__ void race_seed_groups(const SampleArgs& A, const RaceRow& Rr, int64_t srow, int32_t x_lo, int32_t x_hi,
+                                 bool resid, unsigned int* bound_s, int warp, int nwarps)
+{
+    constexpr int kEPV = FastCfg<DT>::kEPV, kE = FastCfg<DT>::kElem;
+    constexpr int32_t kG = kHV * 32 * kEPV;  // ids per group
+    const int lane = threadIdx.x & 31;
+    const int32_t g1 = (x_hi + kG - 1) / kG;
+    float kb = INFINITY;
+    for (int32_t g = x_lo / kG + 32 * warp + lane; g < g1; g += 32 * nwarps) {
+        const int32_t L = A.clane[srow * A.ngroups + g];
+        const int32_t xg = g * kG + kEPV * L;  // the lane's first id; its vectors follow every 32 kEPV ids
+        uint4 v[kHV];
+#pragma unroll
+        for (int e = 0; e < kHV; ++e) {
+            const int32_t x = xg + 32 * kEPV * e;
+            v[e] = x < A.V ? __ldg(reinterpret_cast<const uint4*>(Rr.trow + static_cast<int64_t>(x) * kE)) : ninf_vec(kE);
+        }
+        float zb = -INFINITY;
+        int32_t xb = -1;
+#pragma unroll
+        for (int e = 0; e < kHV; ++e)
+#pragma unroll
+            for (int t = 0; t < kEPV; ++t) {
+                const float z = vec_elem<DT>(v[e], t);
+                if (z > zb) {  // ids ascend: the first of equal maxima
+                    zb = z;
+                    xb = xg + 32 * kEPV * e + t;
+                }
+            }
+        if (xb >= 0) kb = fminf(kb, key_of(Rr, xb, weight_at<DT, DD, YM>(A, Rr, xb, resid)));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) kb = fminf(kb, __shfl_xor_sync(0xffffffffu, kb, o));
+    if (lane == 0 && kb < INFINITY) {
+        atomicMin(bound_s, __float_as_uint(kb));
+        if (Rr.bound_g) atomicMin(Rr.bound_g, __float_as_uint(kb));
+    }
+}
+
 // A queued block of four ids of pass 2: its first id, its raw target logits and draft ids.
 struct RaceQ {
     int32_t x[2 * 32];
@@ -2095,8 +2149,23 @@ __global__ void __launch_bounds__(kRaceThreads, 2) race_rows_kernel(SampleArgs A
             }
             __syncthreads();
             const int32_t xe = min(x_hi, A.V);
-            // pass 1 sets the bound from every lane's largest logit; pass 2 is the pruned race
-            race_seed_pass<DT, DD, YM>(A, Rr, x_lo, xe, residual, &bound_s, warp, kRaceWarps);
+            // pass 1 sets the bound from the keys of the groups' largest logits (the lanes the fast
+            // row pass recorded; else from every lane's largest logit over the part); pass 2 is
+            // the pruned race
+            if (A.clane) {
+                if (tid == 0 && A.tbulk) {  // the part's ids into L2 while the seeds are taken
+                    constexpr int ET = DT == SV_BF16 ? 2 : 4;
+                    for (int32_t x = x_lo; x < xe; x += 16384) {
+                        const uint32_t pb = static_cast<uint32_t>((min(xe, x + 16384) - x) * ET) & ~15u;
+                        const char* pa = Rr.trow + static_cast<int64_t>(x) * ET;
+                        if (pb) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(pa), "r"(pb) : "memory");
+                    }
+                }
+                race_seed_groups<DT, DD, YM>(A, Rr, static_cast<int64_t>(r) * (k + 1) + n, x_lo, xe, residual,
+                                             &bound_s, warp, kRaceWarps);
+            } else {
+                race_seed_pass<DT, DD, YM>(A, Rr, x_lo, xe, residual, &bound_s, warp, kRaceWarps);
+            }
             __syncthreads();
             unsigned long long mine =
                 race_pass<DT, DD, YM>(A, Rr, x_lo, xe, residual, &bound_s, queue_s[warp], warp, kRaceWarps);
@@ -2219,7 +2288,7 @@ D2tPlan plan_view(void* base, int32_t V, int32_t Vd)
 }
 
 struct SampleLayout {
-    int64_t plan, stats, rbound, rbest, rdone, gslots;
+    int64_t plan, stats, rbound, rbest, rdone, clane, gslots;
     int64_t gslot_bytes;
     int64_t total;
     int smem_mode;
@@ -2241,6 +2310,8 @@ SampleLayout sample_layout(int64_t R, int32_t k, int32_t V, int32_t Vd, int et, 
     L.rbound = take(R * 4);
     L.rbest = take(R * 8);
     L.rdone = take(R * 4);
+    // the fast row pass's group records: one byte per group of 2048 (bf16) or 1024 (fp32) ids
+    L.clane = take(R * (k + 1) * ((static_cast<int64_t>(V) + kChunkElems - 1) / kChunkElems) * 2);
     const int64_t units = R * (k + 1);
     // one CTA per unit while they fit one per SM; else the largest grid within one CTA per SM that
     // is coprime to 6 (see unit_rj)
@@ -2350,6 +2421,11 @@ static cudaError_t launch_sample_t(const Rows& t, const Rows& d, const int32_t* 
     A.race_bound = reinterpret_cast<unsigned int*>(ws + L.rbound);
     A.race_best = reinterpret_cast<unsigned long long*>(ws + L.rbest);
     A.race_done = reinterpret_cast<unsigned int*>(ws + L.rdone);
+    if (fast) {
+        A.clane = reinterpret_cast<uint8_t*>(ws + L.clane);
+        A.ngroups = ((t.width + kChunkElems - 1) / kChunkElems) * (t.dtype == SV_BF16 ? FastCfg<SV_BF16>::kHalves
+                                                                                    : FastCfg<SV_F32>::kHalves);
+    }
     A.gslots = ws + L.gslots;
     A.gslot_bytes = L.gslot_bytes;
     A.smem_mode = L.smem_mode;
