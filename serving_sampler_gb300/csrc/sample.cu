@@ -1671,6 +1671,9 @@ namespace {
 constexpr int kRaceThreads = 512;
 constexpr int kRaceWarps = kRaceThreads / 32;
 constexpr int32_t kRaceStep = 256;                // ids per warp step, eight per lane
+// a part's fixed cost (decisions, seeds, setup) in ids of its race, measured on the sampling
+// workload: parts are cut so that every CTA carries the same ids plus this cost per part
+constexpr int64_t kRacePartIds = 16384;
 constexpr uint32_t kRaceSmemRow = 96 * 1024;      // draft rows up to this size are staged in shared memory
 constexpr float kRaceSlack = 1.0f + 1.0f / 1024.0f;
 constexpr float kRaceMinGap = 5.9604645e-8f;      // 2^-24: the smallest 1 - u
@@ -2061,17 +2064,20 @@ __global__ void __launch_bounds__(kRaceThreads, 2) race_rows_kernel(SampleArgs A
     const int32_t k = A.k;
     // The rows, padded to whole 256-id steps, laid end to end: this CTA takes [g_lo, g_hi).
     const int64_t Vp = (static_cast<int64_t>(A.V) + kRaceStep - 1) / kRaceStep * kRaceStep;
-    const int64_t total = static_cast<int64_t>(A.R) * Vp;
+    // the partition line: every row is its part cost, then its ids padded to whole steps
+    const int64_t Vv = kRacePartIds + Vp;
+    const int64_t total = static_cast<int64_t>(A.R) * Vv;
     const int64_t g_lo = static_cast<int64_t>(blockIdx.x) * share, g_hi = min(total, g_lo + share);
     pdl_wait_primary();
     for (int64_t g = g_lo; g < g_hi;) {
-        const int32_t r = static_cast<int32_t>(g / Vp);
-        const int64_t rbase = static_cast<int64_t>(r) * Vp;
-        const int32_t x_lo = static_cast<int32_t>(g - rbase);
-        const int32_t x_hi = static_cast<int32_t>(min(Vp, g_hi - rbase));
-        g = rbase + x_hi;
+        const int32_t r = static_cast<int32_t>(g / Vv);
+        const int64_t ids0 = static_cast<int64_t>(r) * Vv + kRacePartIds;  // where the row's ids start
+        const int32_t x_lo = static_cast<int32_t>(g > ids0 ? g - ids0 : 0);
+        const int32_t x_hi = static_cast<int32_t>(min(Vp, g_hi - ids0));
+        g = ids0 + Vp;
+        if (x_hi <= x_lo) continue;  // this share holds only the row's part cost (block-uniform)
         // the CTAs that share request r's row, and whether this one holds its first part
-        const int32_t parts = static_cast<int32_t>((rbase + Vp - 1) / share - rbase / share + 1);
+        const int32_t parts = static_cast<int32_t>((ids0 + Vp - 1) / share - ids0 / share + 1);
         const bool first = x_lo == 0;
         const RowStat* st = A.stats + static_cast<int64_t>(r) * (k + 1);
         const int32_t* d = A.draft + static_cast<int64_t>(r) * k;
@@ -2461,13 +2467,12 @@ static cudaError_t launch_sample_t(const Rows& t, const Rows& d, const int32_t* 
         e = cudaLaunchKernelEx(&cfg, sample_rows_kernel<DT, DD>, A);
     }
     if (e != cudaSuccess) return e;
-    // the race: one CTA per request; a request's row is split over several CTAs while the batch
-    // leaves CTA slots (two per SM) idle
-    // the race: the rows, padded to whole 256-id steps and laid end to end, in equal shares over one
-    // wave of CTAs (two per SM), each share at least two steps per warp
+    // the race: the rows, each its part cost then its ids padded to whole 256-id steps, laid end to
+    // end and cut in equal shares over one wave of CTAs (two per SM), each share at least two steps
+    // per warp; a request's row is split over several CTAs
     const int64_t slots = 2LL * (sms > 0 ? sms : 148);
     const int64_t Vp = (static_cast<int64_t>(t.width) + kRaceStep - 1) / kRaceStep * kRaceStep;
-    const int64_t total_ids = static_cast<int64_t>(R) * Vp;
+    const int64_t total_ids = static_cast<int64_t>(R) * (kRacePartIds + Vp);  // the partition line
     const int64_t min_share = 2LL * kRaceWarps * kRaceStep;
     int64_t share = std::max<int64_t>(min_share, (total_ids + slots - 1) / slots);
     share = (share + kRaceStep - 1) / kRaceStep * kRaceStep;
