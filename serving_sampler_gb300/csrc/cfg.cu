@@ -129,6 +129,16 @@ __device__ __forceinline__ unsigned long long grp_pair(const Grp<DT>& g, int h)
     }
 }
 
+// element e of a row, widened exactly to fp32
+template <int DT>
+__device__ __forceinline__ float row_value(const char* p, int32_t e)
+{
+    if constexpr (DT == SV_BF16)
+        return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(p)[e]) << 16);
+    else
+        return reinterpret_cast<const float*>(p)[e];
+}
+
 template <int DT, int DD>
 __global__ void __launch_bounds__(32 * kCfgWarpRows, 4) cfg_rows_warp_kernel(CfgArgs A)
 {
@@ -318,7 +328,6 @@ __global__ void __launch_bounds__(32 * kCfgWarpRows, 4) cfg_rows_warp_kernel(Cfg
             const unsigned long long nm2 = pack2(-tm, -tm), nd2 = pack2(-dm, -dm);
             const unsigned long long iS2 = pack2(1.f / sm, 1.f / sm), iQ2 = pack2(1.f / sq, 1.f / sq);
             unsigned long long t2 = 0ull;
-            float pxl = 0.f, qxl = 0.f;
             load(0);
             for (int32_t b = 0; b < nb; ++b) {
                 unsigned long long m2[kP], y2[kP];
@@ -337,16 +346,8 @@ __global__ void __launch_bounds__(32 * kCfgWarpRows, 4) cfg_rows_warp_kernel(Cfg
                     const unsigned long long q2 = mul2(pack2(ex2(b0), ex2(b1)), iQ2);
                     float d0, d1;
                     unpack2(sub2(q2, p2), d0, d1);
-                    const int32_t x = 8 * (lane + 32 * (kG * b + p / 4)) + 2 * (p % 4);
                     // ids beyond W hold p = 0 and q of a -inf logit = 0
                     t2 = add2(t2, pack2(fmaxf(d0, 0.f), fmaxf(d1, 0.f)));
-                    if ((xl & ~1) == x) {
-                        float p0, p1, q0, q1;
-                        unpack2(p2, p0, p1);
-                        unpack2(q2, q0, q1);
-                        pxl = (xl & 1) ? p1 : p0;
-                        qxl = (xl & 1) ? q1 : q0;
-                    }
                 }
             }
             float t;
@@ -356,9 +357,14 @@ __global__ void __launch_bounds__(32 * kCfgWarpRows, 4) cfg_rows_warp_kernel(Cfg
                 t = a0 + a1;
             }
             t = wsum(t);
-            // the lane that saw xl holds p and q there; the others hold 0
-            pxl = wsum(pxl);
-            qxl = wsum(qxl);
+            // p and q at the drafted id, with the pass's own operations on that id's inputs
+            float pxl = 0.f, qxl = 0.f;
+            if (xl >= 0 && xl < W) {
+                const float cx = row_value<DT>(cp, xl), ux = row_value<DT>(up, xl), yx = row_value<DD>(dp, xl);
+                const float mx = fmaf(A.shape.w, cx - ux, ux);
+                pxl = ex2(fmaf(mx, c, -tm)) * (1.f / sm);
+                qxl = ex2(fmaf(yx, c, -dm)) * (1.f / sq);
+            }
             tvv = t;
             int32_t acc_ok = 0;
             if (xl >= 0 && xl < W) {
