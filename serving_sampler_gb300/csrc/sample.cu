@@ -1766,16 +1766,6 @@ __device__ __forceinline__ void load_z8(const SampleArgs& A, const RaceRow& Rr, 
     for (int h = 0; h < ZW; ++h) zq[h] = make_uint4(wv[4 * h], wv[4 * h + 1], wv[4 * h + 2], wv[4 * h + 3]);
 }
 
-// the draft ids of target ids [x, x + 8) as four words of two 16-bit ids (0xFFFF off the support)
-__device__ __forceinline__ uint4 load_j8(const SampleArgs& A, int32_t x)
-{
-    if (x + 8 <= A.V) return __ldg(reinterpret_cast<const uint4*>(A.plan.jmap + x));
-    uint32_t jm[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) jm[e] = x + e < A.V ? A.plan.jmap[x + e] : 0xFFFFu;
-    return make_uint4(jm[0] | (jm[1] << 16), jm[2] | (jm[3] << 16), jm[4] | (jm[5] << 16), jm[6] | (jm[7] << 16));
-}
-
 template <int DT>
 __device__ __forceinline__ float z_of(const uint4* zq, int e)
 {
@@ -1919,20 +1909,24 @@ __device__ void race_seed_groups(const SampleArgs& A, const RaceRow& Rr, int64_t
     }
 }
 
-// A queued block of four ids of pass 2: its first id, its raw target logits and draft ids.
+// A queued block of four ids of pass 2: its first id and its raw target logits.
 struct RaceQ {
     int32_t x[2 * 32];
     uint4 z[2 * 32];   // bf16: the first 8 bytes; fp32: all 16
-    uint2 j[2 * 32];   // four 16-bit draft ids (d2t)
 };
 
-// the full test of one queued block: weights, the Philox block when one of its ids can win,
-// keys where 1 - u <= B w (w = 0 never passes); updates the lane's running minimum (blocks
-// reach a lane out of id order, so equal keys compare ids)
+// the full test of one queued block: weights (the block's draft ids read here, for the blocks
+// that reach the queue only), the Philox block when one of its ids can win, keys where
+// 1 - u <= B w (w = 0 never passes); updates the lane's running minimum (blocks reach a lane out
+// of id order, so equal keys compare ids)
 template <int DT, int DD, int YM>
 __device__ __forceinline__ void race_block(const SampleArgs& A, const RaceRow& Rr, bool resid, int32_t x,
-                                           uint4 zq, uint2 jq, float tfl, float bs, float& best, int32_t& bx)
+                                           uint4 zq, float tfl, float bs, float& best, int32_t& bx)
 {
+    uint2 jq = make_uint2(0u, 0u);  // four 16-bit draft ids (x is a multiple of four)
+    if constexpr (YM != kYIdentity) {
+        if (resid) jq = __ldg(reinterpret_cast<const uint2*>(A.plan.jmap + x));
+    }
     float w[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -1988,13 +1982,9 @@ __device__ unsigned long long race_pass(const SampleArgs& A, const RaceRow& Rr, 
     constexpr int kBatch = 2;  // steps whose loads are in flight together
     const int32_t step = kRaceStep * nwarps;
     for (int32_t xb0 = x_lo + kRaceStep * warp; xb0 < x_hi; xb0 += kBatch * step) {
-        uint4 zb[kBatch][ZW], jb[kBatch];
+        uint4 zb[kBatch][ZW];
 #pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-            const int32_t x = xb0 + b * step + 8 * lane;
-            load_z8<DT>(A, Rr, x, x_hi, zb[b]);
-            jb[b] = resid && YM != kYIdentity ? load_j8(A, x) : make_uint4(0u, 0u, 0u, 0u);
-        }
+        for (int b = 0; b < kBatch; ++b) load_z8<DT>(A, Rr, xb0 + b * step + 8 * lane, x_hi, zb[b]);
         // the bound the request's other parts have reached (read now, used at the batch's end)
         const unsigned int gb = Rr.bound_g ? *reinterpret_cast<volatile unsigned int*>(Rr.bound_g) : 0x7F800000u;
 #pragma unroll
@@ -2013,13 +2003,12 @@ __device__ unsigned long long race_pass(const SampleArgs& A, const RaceRow& Rr, 
                                         : make_uint4(zb[b][0].z, zb[b][0].w, 0u, 0u);
                     else
                         q.z[s] = zb[b][h];
-                    q.j[s] = h == 0 ? make_uint2(jb[b].x, jb[b].y) : make_uint2(jb[b].z, jb[b].w);
                 }
                 qn += __popc(bal);
                 __syncwarp();
                 if (qn >= 32) {  // warp-uniform
                     const uint32_t s = (qh + lane) & 63u;
-                    race_block<DT, DD, YM>(A, Rr, resid, q.x[s], q.z[s], q.j[s], tfl, B * kRaceSlack, best, bx);
+                    race_block<DT, DD, YM>(A, Rr, resid, q.x[s], q.z[s], tfl, B * kRaceSlack, best, bx);
                     qh = (qh + 32) & 63u;
                     qn -= 32;
                     __syncwarp();
@@ -2041,7 +2030,7 @@ __device__ unsigned long long race_pass(const SampleArgs& A, const RaceRow& Rr, 
     }
     if (lane < qn) {  // the queue's rest
         const uint32_t s = (qh + lane) & 63u;
-        race_block<DT, DD, YM>(A, Rr, resid, q.x[s], q.z[s], q.j[s], tfl, B * kRaceSlack, best, bx);
+        race_block<DT, DD, YM>(A, Rr, resid, q.x[s], q.z[s], tfl, B * kRaceSlack, best, bx);
     }
     __syncwarp();
     return warp_min_u64(bx == INT32_MAX ? kNoKey : pack_key(best, bx));
