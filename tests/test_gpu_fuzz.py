@@ -1,0 +1,59 @@
+"""Speculative sampling on seeded random configurations against the oracle: both dtypes and their
+mixes, vocabulary sizes that are and are not multiples of the 16-byte vector, the identity map
+and d2t maps of every density, k from 0 to 9, batches from 1 to 12 with greedy, sampled and
+invalid temperatures mixed.  Together they reach the bulk-copy row pass and the general one, and
+race partitions that cut rows at odd places.  Every case is compared element by element under
+the parity rules (tokens, accept lengths and status exact outside the decision margin; TV, p
+and q within 1e-5 relative)."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from tests.sampling_parity import compare
+from tests.test_gpu_sample import _oracle, _run
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = (torch.bfloat16, torch.float32)
+TEMPS = (0.0, 0.3, 0.7, 1.0, 1.6, -0.5)  # a negative temperature: verified greedily, flagged
+
+
+def case(i: int):
+    """The i-th configuration (a pure function of i)."""
+    rng = np.random.default_rng(9100 + i)
+    dt = DTYPES[rng.integers(2)]
+    dd = DTYPES[rng.integers(2)] if rng.random() < 0.3 else dt
+    V = int(rng.choice([int(rng.integers(9, 600)), int(rng.integers(600, 20000))]))
+    Vd = None if rng.random() < 0.3 else int(rng.integers(1, min(V, 4000) + 1))
+    if rng.random() < 0.5:  # widths in whole 16-byte vectors (the bulk-copy path when the map is given)
+        V = max(8, V // 8 * 8)
+        Vd = None if Vd is None else max(8, min(V, Vd) // 8 * 8)
+    k = int(rng.integers(0, 10))
+    R = int(rng.integers(1, 13))
+    T = [float(TEMPS[j]) for j in rng.integers(0, len(TEMPS), R)]
+    return dict(R=R, k=k, V=V, Vd=Vd, dtype=dt, draft_dtype=dd, T=T,
+                sigma_pos=float(rng.uniform(0.2, 1.5)), delta=float(rng.uniform(0, 3)) if Vd else 0.0,
+                z_sigma=float(rng.uniform(0.5, 4)), seed=int(rng.integers(1 << 30)),
+                seed_base=int(rng.integers(1 << 30)))
+
+
+@pytest.mark.parametrize("i", range(32))
+def test_random_configuration(sv, i):
+    c = case(i)
+    w = workloads.sample_batch(c["R"], c["k"], c["V"], c["Vd"], c["dtype"], c["draft_dtype"], T=c["T"],
+                               sigma_pos=c["sigma_pos"], delta=c["delta"], z_sigma=c["z_sigma"], seed=c["seed"],
+                               seed_base=c["seed_base"])
+    compare(_run(sv, w), _oracle(w), label=f"fuzz {i}")
+
+
+def test_cases_cover_both_row_passes():
+    """The configurations reach the bulk-copy row pass (matched dtypes, a d2t map, widths that are
+    multiples of eight) and the general one (identity, mixed dtypes, odd widths)."""
+    fast = general = 0
+    for i in range(32):
+        c = case(i)
+        ok = c["Vd"] is not None and c["dtype"] == c["draft_dtype"] and c["V"] % 8 == 0 and c["Vd"] % 8 == 0
+        fast += ok
+        general += not ok
+    assert fast >= 4 and general >= 4, (fast, general)
