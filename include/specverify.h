@@ -291,7 +291,9 @@ int sv_d2t_plan_build(const int32_t* d2t, int32_t Vd, int32_t V, void* plan, siz
  *                   s inside its row; offset + W <= row_stride.
  *   S               codebooks, 1 <= S <= SV_MAX_S;  w  CFG weight;  W <= 16384.
  *   draft_logits    draft rows, width W, row (r * k + j) * S + s; data == NULL
- *                   selects greedy verification on the merged logits.
+ *                   selects greedy verification on the merged logits when k > 0
+ *                   (with k = 0 there are no draft rows: a request with T > 0
+ *                   draws its bonus from p, as in sv_verify_sample).
  *   draft           int32 [R, k, S] absolute ids.
  *   seeds, temperature  as in sv_verify_sample.
  *   accept_len      int32 [R] out: accepted FRAMES.

@@ -632,7 +632,7 @@ int or_verify_sample(const void* target, int t_dtype, int64_t t_stride, int32_t 
 /* cond / uncond; its codebook slice starts at element cb_data_offset[s]*/
 /* and has W entries; local id l is absolute id cb_id_base[s] + l.      */
 /* Draft logit rows: (r * k + j) * S + s, W entries from element 0.     */
-/* draft_logits == NULL or T <= 0: greedy on the merged logits.         */
+/* T <= 0, or draft_logits == NULL with k > 0: greedy on the merged logits. */
 /* Optional: tv [R,k,S], accept_margin [R,k,S], race_margin [R,S].      */
 /* ------------------------------------------------------------------ */
 static void merged_row(const void* cond, const void* uncond, int dtype, int64_t stride,
@@ -667,7 +667,9 @@ int or_cfg_merge_sample(const void* cond, const void* uncond, int dtype, int64_t
     for (int32_t r = 0; r < R; ++r) {
         int32_t st = 0;
         const double T = (double)temperature[r];
-        int greedy = !(T > 0.0) || draft_logits == NULL;
+        /* NULL draft logits select greedy verification when there are draft rows; with k = 0
+           the bonus follows the temperature alone (drawn from p when T > 0) */
+        int greedy = !(T > 0.0) || (draft_logits == NULL && k > 0);
         if (T < 0.0 || isnan(T)) st |= OR_ST_BAD_TEMP;
         const int32_t* d = draft + (int64_t)r * k * S;
         int32_t* out = tokens + (int64_t)r * (k + 1) * S;

@@ -155,7 +155,9 @@ __global__ void __launch_bounds__(32 * kCfgWarpRows, 4) cfg_rows_warp_kernel(Cfg
     const int32_t j = static_cast<int32_t>(rj % (k + 1));
     const int32_t r = static_cast<int32_t>(rj / (k + 1));
     const float T = A.temp[r];
-    const bool sampling = T > 0.f && A.dbase != nullptr;
+    // NULL draft rows select greedy verification when there are drafts; with k = 0 the bonus
+    // follows the temperature alone
+    const bool sampling = T > 0.f && (A.dbase != nullptr || k == 0);
     const bool has_draft = sampling && j < k;
     const float c = sampling ? kLog2eC / T : 0.f;
     const unsigned long long w2 = pack2(A.shape.w, A.shape.w), c2 = pack2(c, c);
@@ -426,7 +428,7 @@ __global__ void __launch_bounds__(kCfgRaceThreads) cfg_race_kernel(CfgArgs A)
         for (int32_t i = lane; i < (k + 1) * S; i += 32) fl |= st[i].flags;
         fl = __reduce_or_sync(0xffffffffu, fl);
         const bool bad0 = (fl & kCfgBad) != 0;
-        const bool greedy0 = !(T > 0.f) || A.dbase == nullptr || bad0;
+        const bool greedy0 = !(T > 0.f) || (A.dbase == nullptr && k > 0) || bad0;
         uint32_t nf = static_cast<uint32_t>(k);
         for (int32_t i = lane; i < k * S; i += 32) {
             const int32_t q = i % S;
@@ -442,7 +444,7 @@ __global__ void __launch_bounds__(kCfgRaceThreads) cfg_race_kernel(CfgArgs A)
     __syncthreads();
     const int32_t n = n_s;
     const bool bad = (fl_s & kCfgBad) != 0;
-    const bool greedy = !(T > 0.f) || A.dbase == nullptr || bad;
+    const bool greedy = !(T > 0.f) || (A.dbase == nullptr && k > 0) || bad;
 
     int32_t tok_local = 0;
     uint32_t status = 0;

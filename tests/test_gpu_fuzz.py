@@ -1,16 +1,18 @@
-"""Speculative sampling on seeded random configurations against the oracle: both dtypes and their
-mixes, vocabulary sizes that are and are not multiples of the 16-byte vector, the identity map
-and d2t maps of every density, k from 0 to 9, batches from 1 to 12 with greedy, sampled and
-invalid temperatures mixed.  Together they reach the bulk-copy row pass and the general one, and
-race partitions that cut rows at odd places.  Every case is compared element by element under
-the parity rules (tokens, accept lengths and status exact outside the decision margin; TV, p
-and q within 1e-5 relative)."""
+"""Speculative sampling and CFG sampling on seeded random configurations against the oracle:
+both dtypes and their mixes, widths that are and are not multiples of the 16-byte vector, the
+identity map and d2t maps of every density, codebook counts and widths, k from 0 to 9, batches
+of 1 to 12 requests with greedy, sampled and invalid temperatures mixed.  Together they reach the
+bulk-copy row pass and the general one, and race partitions that cut rows at odd places.  Every
+case is compared element by element under the parity rules (tokens, accept lengths and status
+exact outside the decision margin; TV, p and q within 1e-5 relative)."""
 import numpy as np
 import pytest
 import torch
 
 import workloads
 from tests.sampling_parity import compare
+from tests.test_gpu_cfg import _oracle as _cfg_oracle
+from tests.test_gpu_cfg import _run as _cfg_run
 from tests.test_gpu_sample import _oracle, _run
 
 pytestmark = pytest.mark.gpu
@@ -57,3 +59,26 @@ def test_cases_cover_both_row_passes():
         fast += ok
         general += not ok
     assert fast >= 4 and general >= 4, (fast, general)
+
+
+def cfg_case(i: int):
+    """The i-th CFG configuration (a pure function of i)."""
+    rng = np.random.default_rng(9300 + i)
+    dt = DTYPES[rng.integers(2)]
+    dd = DTYPES[rng.integers(2)] if rng.random() < 0.3 else dt
+    R, k, S = int(rng.integers(1, 11)), int(rng.integers(0, 7)), int(rng.integers(1, 17))
+    W = int(rng.choice([int(rng.integers(1, 300)), int(rng.integers(300, 6000))]))
+    T = [float(TEMPS[j]) for j in rng.integers(0, len(TEMPS), R)]
+    return dict(R=R, k=k, S=S, W=W, w=float(rng.uniform(1.0, 5.0)), T=T, dtype=dt, draft_dtype=dd,
+                sigma_h=float(rng.uniform(0.2, 1.0)), bump=float(rng.uniform(0.0, 8.0)),
+                sigma_d=float(rng.uniform(0.3, 1.5)), greedy_drafts=float(rng.uniform(0, 0.5)),
+                seed=int(rng.integers(1 << 30)), seed_base=int(rng.integers(1 << 30)))
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_random_cfg_configuration(sv, i):
+    c = cfg_case(i)
+    w = workloads.cfg_batch(c["R"], c["k"], c["S"], c["W"], c["w"], c["T"], c["dtype"], c["draft_dtype"],
+                            sigma_h=c["sigma_h"], bump=c["bump"], sigma_d=c["sigma_d"], seed=c["seed"],
+                            seed_base=c["seed_base"], greedy_drafts=c["greedy_drafts"])
+    compare(_cfg_run(sv, w), _cfg_oracle(w), label=f"cfg fuzz {i}")

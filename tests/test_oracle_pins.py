@@ -648,6 +648,28 @@ def test_cfg_weight_zero_is_plain_sampling_of_uncond():
     assert np.allclose(a["tv"][:, :, 0], b["tv"], atol=1e-15)
 
 
+def test_cfg_without_drafts_draws_the_bonus_like_sampling():
+    """k = 0: no draft rows, so the bonus follows the temperature alone, whether the draft
+    logits are absent or empty.  With w = 0 (merged = u) and one codebook it is the sampling
+    path's bonus on u: the same race, counter row 0, tag 2 (speculative decoding for Omni
+    models, section 2: the bonus token is drawn from p)."""
+    rng = np.random.default_rng(23)
+    R, W = 300, 24
+    c = rng.normal(0, 1, (R, W)).astype(np.float32)
+    u = rng.normal(0, 1.5, (R, W)).astype(np.float32)
+    seeds = rng.integers(0, 2 ** 63, R, dtype=np.uint64)
+    T = np.where(np.arange(R) % 4 == 0, 0.0, 0.9).astype(np.float32)
+    empty = np.zeros((R, 0), np.int32)
+    a = oracle.cfg_merge_sample(c, u, [0], [0], 1, W, 0.0, None, R, 0, empty, seeds, T)
+    a2 = oracle.cfg_merge_sample(c, u, [0], [0], 1, W, 0.0, np.zeros((0, W), np.float32), R, 0, empty, seeds, T)
+    b = oracle.verify_sample(u, np.zeros((0, W), np.float32), None, R, 0, empty, seeds, T)
+    assert np.array_equal(a["tokens"], a2["tokens"])
+    assert np.array_equal(a["tokens"][:, :, 0], b["tokens"])
+    sampled = T > 0
+    assert np.all(a["tokens"][~sampled, 0, 0] == np.argmax(u[~sampled], axis=1))
+    assert np.any(a["tokens"][sampled, 0, 0] != np.argmax(u[sampled], axis=1))  # drawn, not the argmax
+
+
 def test_cfg_weight_one_greedy_is_greedy_on_cond():
     rng = np.random.default_rng(22)
     R, k, S, W = 30, 4, 3, 32
