@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads
 from tests.sampling_parity import compare
 from tests.test_gpu_cfg import _oracle as _cfg_oracle
@@ -82,3 +83,72 @@ def test_random_cfg_configuration(sv, i):
                             sigma_h=c["sigma_h"], bump=c["bump"], sigma_d=c["sigma_d"], seed=c["seed"],
                             seed_base=c["seed_base"], greedy_drafts=c["greedy_drafts"])
     compare(_cfg_run(sv, w), _cfg_oracle(w), label=f"cfg fuzz {i}")
+
+
+def greedy_case(i: int):
+    """The i-th greedy configuration (a pure function of i)."""
+    rng = np.random.default_rng(9500 + i)
+    branches = int(rng.choice([1, 1, 2, 3, 8]))
+    k = int(rng.integers(1 if branches > 1 else 0, 41))
+    V = int(rng.choice([int(rng.integers(2, 700)), int(rng.integers(700, 30000)), workloads.V_QWEN]))
+    return dict(R=int(rng.integers(1, 41)), k=k, branches=branches, V=V, dtype=DTYPES[rng.integers(2)],
+                row_pad=int(rng.choice([0, 0, int(rng.integers(1, 9))])), p_full=float(rng.uniform(0.2, 1.0)),
+                p_first=float(rng.uniform(0.2, 1.0)), seed=int(rng.integers(1 << 30)),
+                specials=int(rng.integers(0, 4)), ties=bool(rng.random() < 0.5), rng_seed=9700 + i)
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_random_greedy_configuration(sv, i):
+    """Greedy verification (branches and tree drafts), and the same call with every row's argmax and
+    runner-up, on random shapes with NaN / +-inf rows and planted ties."""
+    from tests.test_gpu_greedy import _check, _check_top2
+
+    c = greedy_case(i)
+    w = workloads.greedy_batch(c["R"], c["k"], c["V"], c["dtype"], branches=c["branches"], p_full=c["p_full"],
+                               p_first=c["p_first"], seed=c["seed"], row_pad=c["row_pad"])
+    t = w["target"].float()
+    rng = np.random.default_rng(c["rng_seed"])
+    rows = t.shape[0]
+    for _ in range(c["specials"]):  # a NaN, +inf or -inf at a random place, or a row of -inf
+        r, x = int(rng.integers(rows)), int(rng.integers(c["V"]))
+        kind = int(rng.integers(4))
+        if kind == 3:
+            t[r, :] = float("-inf")
+        else:
+            t[r, x] = (float("nan"), float("inf"), float("-inf"))[kind]
+    if c["ties"]:  # a copy of a row's maximum at a random other id
+        for r in rng.integers(0, rows, size=min(rows, 5)):
+            m = int(torch.argmax(torch.nan_to_num(t[r], nan=-float("inf"))).item())
+            t[int(r), int(rng.integers(c["V"]))] = t[int(r), m]
+    target = t.to(c["dtype"])
+    if c["row_pad"]:  # keep the padded row stride of the generator
+        full = torch.empty(rows, c["V"] + c["row_pad"], dtype=c["dtype"], device=target.device)
+        full[:, :c["V"]] = target
+        target = full[:, :c["V"]]
+    _check(sv, target, c["R"], c["k"], c["branches"], w["draft"])
+    _check_top2(sv, target, c["R"], c["k"], c["branches"], w["draft"])
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_random_modality_and_accept_scan(sv, i):
+    rng = np.random.default_rng(9900 + i)
+    dtype = DTYPES[rng.integers(2)]
+    N, V = int(rng.integers(1, 200)), int(rng.integers(2, 40000))
+    P = int(rng.integers(1, 65))
+    starts = np.sort(rng.integers(0, V + 1, P)).astype(np.int32)
+    g = torch.Generator(device="cuda").manual_seed(int(rng.integers(1 << 30)))
+    z = (torch.randn(N, V, generator=g, device="cuda") * float(rng.uniform(0.5, 5))).to(dtype)
+    got = sv.infer_modality(z, starts.tolist())
+    torch.cuda.synchronize()
+    want = oracle.infer_modality(workloads.host_rows(z), starts)
+    for key in ("amax", "part", "mask_lo", "mask_hi"):
+        np.testing.assert_array_equal(got[key].cpu().numpy(), want[key], err_msg=key)
+    R, k = int(rng.integers(1, 60)), int(rng.integers(1, 257))
+    acc = (rng.random((R, k)) < float(rng.uniform(0.3, 1.0))).astype(np.uint8)
+    draft = rng.integers(0, 5000, (R, k)).astype(np.int32)
+    fix = rng.integers(0, 5000, (R, k + 1)).astype(np.int32)
+    got = sv.accept_scan(torch.from_numpy(acc).cuda(), torch.from_numpy(draft).cuda(), torch.from_numpy(fix).cuda())
+    torch.cuda.synchronize()
+    want = oracle.accept_scan(acc, draft, fix)
+    np.testing.assert_array_equal(got["accept_len"].cpu().numpy(), want["accept_len"])
+    np.testing.assert_array_equal(got["tokens"].cpu().numpy(), want["tokens"])
