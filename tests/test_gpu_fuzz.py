@@ -1,10 +1,12 @@
-"""Speculative sampling and CFG sampling on seeded random configurations against the oracle:
-both dtypes and their mixes, widths that are and are not multiples of the 16-byte vector, the
-identity map and d2t maps of every density, codebook counts and widths, k from 0 to 9, batches
-of 1 to 12 requests with greedy, sampled and invalid temperatures mixed.  Together they reach the
-bulk-copy row pass and the general one, and race partitions that cut rows at odd places.  Every
-case is compared element by element under the parity rules (tokens, accept lengths and status
-exact outside the decision margin; TV, p and q within 1e-5 relative)."""
+"""Every entry point on seeded random configurations against the oracle.  Speculative and CFG
+sampling: both dtypes and their mixes, widths that are and are not multiples of the 16-byte
+vector, the identity map and d2t maps of every density, codebook counts and widths, k from 0 to
+9, batches of 1 to 12 requests with greedy, sampled and invalid temperatures mixed (the bulk-copy
+row pass and the general one, race partitions that cut rows at odd places).  Greedy verification
+with branches and tree drafts, NaN / +-inf rows and planted ties, with and without the top-2
+output; modality inference over random partitions; the accept scan; hypothesis-pool sessions.
+Sampling outputs follow the parity rules (tokens, accept lengths and status exact outside the
+decision margin; TV, p and q within 1e-5 relative), everything else is compared exactly."""
 import numpy as np
 import pytest
 import torch
@@ -152,3 +154,34 @@ def test_random_modality_and_accept_scan(sv, i):
     want = oracle.accept_scan(acc, draft, fix)
     np.testing.assert_array_equal(got["accept_len"].cpu().numpy(), want["accept_len"])
     np.testing.assert_array_equal(got["tokens"].cpu().numpy(), want["tokens"])
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_random_pool_sessions(sv, i):
+    """Hypothesis pools: appends of random draft blocks (negative ids end a draft early), lookups
+    of the emitted suffix, suffix updates with accept lengths inside and outside [0, k]."""
+    from tests.test_gpu_pool import _append_both, _dev, _lookup_both
+
+    rng = np.random.default_rng(10100 + i)
+    R, Lp, vocab = int(rng.integers(1, 300)), int(rng.integers(0, 5000)), int(rng.integers(2, 60))
+    N, gamma = int(rng.integers(0, 65)), int(rng.integers(0, 257))
+    pool_h = np.full((R, Lp), -2, np.int32)
+    plen_h = np.zeros(R, np.int32)
+    pool_d, plen_d = _dev(pool_h), _dev(plen_h)
+    suffix = rng.integers(-1, vocab, (R, N)).astype(np.int32)
+    for step in range(int(rng.integers(1, 8))):
+        k = int(rng.integers(0, 41))
+        drafts = rng.integers(0, vocab, (R, k)).astype(np.int32)
+        if k:
+            cut = rng.random(R) < 0.3  # some drafts end early
+            drafts[cut, int(rng.integers(k))] = -1
+        pool_h, plen_h = _append_both(sv, pool_d, plen_d, pool_h, plen_h, drafts)
+        _lookup_both(sv, pool_h, plen_h, suffix, gamma, pool_d, plen_d)
+        tokens = rng.integers(0, vocab, (R, k + 1)).astype(np.int32)
+        acc = rng.integers(-2, k + 3, R).astype(np.int32)
+        s_d = _dev(suffix)
+        sv.suffix_append(s_d, _dev(tokens), _dev(acc))
+        want = oracle.suffix_append(suffix, tokens, acc)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(s_d.cpu().numpy(), want, err_msg=f"suffix after step {step}")
+        suffix = want
