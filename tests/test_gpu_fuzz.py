@@ -185,3 +185,25 @@ def test_random_pool_sessions(sv, i):
         torch.cuda.synchronize()
         np.testing.assert_array_equal(s_d.cpu().numpy(), want, err_msg=f"suffix after step {step}")
         suffix = want
+
+
+@pytest.mark.parametrize("i", range(8))
+def test_random_long_draft_blocks(sv, i):
+    """Sampling and CFG with k from 10 to 256 (scans over several 32-position words)."""
+    rng = np.random.default_rng(10300 + i)
+    dt = DTYPES[rng.integers(2)]
+    k = int(rng.integers(10, 257))
+    R = int(rng.integers(1, 5))
+    V = int(rng.choice([int(rng.integers(8, 300)), 8 * int(rng.integers(8, 400))]))
+    Vd = None if rng.random() < 0.4 else max(1, int(rng.integers(1, V + 1)) // 8 * 8)
+    T = [float(TEMPS[j]) for j in rng.integers(0, len(TEMPS), R)]
+    # drafts close to the target: long accepted runs
+    w = workloads.sample_batch(R, k, V, Vd, dt, T=T, sigma_pos=float(rng.uniform(0.01, 0.3)), delta=1.0 if Vd else 0.0,
+                               z_sigma=float(rng.uniform(0.5, 3)), seed=int(rng.integers(1 << 30)),
+                               seed_base=int(rng.integers(1 << 30)))
+    compare(_run(sv, w), _oracle(w), label=f"long k {i}")
+    S, W = int(rng.integers(1, 5)), int(rng.integers(2, 600))
+    kc = int(rng.integers(10, 65))
+    wc = workloads.cfg_batch(R, kc, S, W, float(rng.uniform(1, 4)), T, dt, sigma_h=0.5, bump=float(rng.uniform(4, 12)),
+                             sigma_d=0.05, seed=int(rng.integers(1 << 30)), seed_base=int(rng.integers(1 << 30)))
+    compare(_cfg_run(sv, wc), _cfg_oracle(wc), label=f"long k cfg {i}")
