@@ -15,11 +15,13 @@
 //                      unit at a time.  The draft and target rows stream
 //                      through bulk-copied shared-memory stages: max, sum-exp
 //                      at T, argmax, NaN/inf flags and z at the support
-//                      positions (G).  A second pass over G and the draft
-//                      row gives TV over the full vocabulary, p(x_j), q(x_j)
-//                      and the accept test u_j < p/q.
-//   race_rows_kernel   one CTA per request (or per part of its row for small
-//                      batches): the accept-length scan, then on the one
+//                      positions (G); the fast pass also records, per
+//                      2048-id group, the lane holding the group's maximum.
+//                      A second pass over G and the draft row gives TV over
+//                      the full vocabulary, p(x_j), q(x_j) and the accept test
+//                      u_j < p/q.
+//   race_rows_kernel   the selected rows laid end to end in parts over one
+//                      wave of CTAs: the accept-length scan, then on the one
 //                      selected row (residual max(0, p - q) at the first
 //                      rejection, or p at the bonus row) the exponential race
 //                      over every id with Philox uniforms, pruned by a bound on
@@ -1652,13 +1654,16 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
 // the whole row: argmin over the ids with w_x > 0 of E_x / w_x, E_x = -ln u_x,
 // u_x the Philox uniform of id x (counter (x >> 2, row, tag, 0), word x & 3).
 //
-// race_rows_kernel: one CTA per request, or per part of its row when the batch
-// has fewer requests than the GPU has CTA slots (then the parts meet in a
-// packed 64-bit per-request minimum and the part that finishes last commits).
-// Warp 0 scans the accept flags for n.  Each warp streams 256-id steps of the
-// selected row (the next step's loads in flight) and keeps a running minimum
-// key; a bound B of the row's minimum key is shared through shared memory
-// (seeded with the key of the row's argmax).  An id can win only if
+// race_rows_kernel: the selected rows, each a fixed part cost followed by its
+// ids, are cut into equal shares over one wave of CTAs (two per SM); the parts
+// of a request meet in a packed 64-bit (key, id) minimum and the part that
+// finishes last commits.  Warp 0 scans the accept flags for n.  Each warp
+// streams 256-id steps of its part (the next step's loads in flight) and
+// keeps a running minimum key; a bound B of the row's minimum key is shared
+// through shared memory and, between the parts of a request, through the
+// workspace, seeded with the exact keys of the largest logit of every group
+// the part overlaps (lanes recorded by the fast row pass; else every lane's
+// largest logit over the part).  An id can win only if
 // 1 - u <= E <= B w (E = -ln u >= 1 - u) and 1 - u >= 2^-24, so it needs
 // p B >= 2^-24: ids whose scaled logit t = z c - m is below
 // lg2(S) - 24 - lg2(B) are skipped without an exponential, a Philox block is
