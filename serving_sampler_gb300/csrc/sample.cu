@@ -1966,9 +1966,9 @@ __device__ __forceinline__ void race_block(const SampleArgs& A, const RaceRow& R
     }
 }
 
-// Pass 2: the race over ids [x_lo, x_hi) by one warp, against the shared bound; returns the warp's
-// packed (key, id) minimum to every lane.  Each lane tests its two blocks of four ids per step on
-// their largest raw logit alone; the blocks that pass go to the warp's queue in shared memory,
+// Pass 2: the race over ids [x_lo, x_hi) by one warp, against the shared bound (refreshed after every
+// step); returns the warp's packed (key, id) minimum to every lane.  Each lane tests its two blocks
+// of four ids per step on their largest raw logit alone; the blocks that pass go to the warp's queue in shared memory,
 // which the warp works off 32 blocks at a time, one per lane, so that the exponentials and the
 // Philox rounds run with every lane busy.
 template <int DT, int DD, int YM>
@@ -1984,40 +1984,39 @@ __device__ unsigned long long race_pass(const SampleArgs& A, const RaceRow& Rr, 
     float zfl = tfl > -INFINITY ? (tfl + Rr.m) / Rr.c : -INFINITY;  // the same floor on raw logits
     uint32_t qh = 0, qn = 0;  // the queue's head and length (warp-uniform)
     constexpr int ZW = DT == SV_BF16 ? 1 : 2;
-    constexpr int kBatch = 2;  // steps whose loads are in flight together
     const int32_t step = kRaceStep * nwarps;
-    for (int32_t xb0 = x_lo + kRaceStep * warp; xb0 < x_hi; xb0 += kBatch * step) {
-        uint4 zb[kBatch][ZW];
+    // a step's target logits are loaded while the step before it is tested
+    uint4 zn[ZW];
+    load_z8<DT>(A, Rr, x_lo + kRaceStep * warp + 8 * lane, x_hi, zn);
+    for (int32_t xs = x_lo + kRaceStep * warp; xs < x_hi; xs += step) {
+        uint4 zq[ZW];
 #pragma unroll
-        for (int b = 0; b < kBatch; ++b) load_z8<DT>(A, Rr, xb0 + b * step + 8 * lane, x_hi, zb[b]);
-        // the bound the request's other parts have reached (read now, used at the batch's end)
+        for (int i = 0; i < ZW; ++i) zq[i] = zn[i];
+        if (xs + step < x_hi) load_z8<DT>(A, Rr, xs + step + 8 * lane, x_hi, zn);
+        // the bound the request's other parts have reached (read now, used at the step's end)
         const unsigned int gb = Rr.bound_g ? *reinterpret_cast<volatile unsigned int*>(Rr.bound_g) : 0x7F800000u;
+        const int32_t x = xs + 8 * lane;
+        // the blocks that can hold a winner join the queue (at most 31 + 32 entries at a time)
 #pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-            const int32_t x = xb0 + b * step + 8 * lane;
-            // the blocks that can hold a winner join the queue (at most 31 + 32 entries at a time)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const bool pass = max4<DT>(zb[b], h) >= zfl;  // false past the end (-inf)
-                const unsigned bal = __ballot_sync(0xffffffffu, pass);
-                if (pass) {
-                    const uint32_t s = (qh + qn + __popc(bal & lt)) & 63u;
-                    q.x[s] = x + 4 * h;
-                    if constexpr (DT == SV_BF16)
-                        q.z[s] = h == 0 ? make_uint4(zb[b][0].x, zb[b][0].y, 0u, 0u)
-                                        : make_uint4(zb[b][0].z, zb[b][0].w, 0u, 0u);
-                    else
-                        q.z[s] = zb[b][h];
-                }
-                qn += __popc(bal);
+        for (int h = 0; h < 2; ++h) {
+            const bool pass = max4<DT>(zq, h) >= zfl;  // false past the end (-inf)
+            const unsigned bal = __ballot_sync(0xffffffffu, pass);
+            if (pass) {
+                const uint32_t s = (qh + qn + __popc(bal & lt)) & 63u;
+                q.x[s] = x + 4 * h;
+                if constexpr (DT == SV_BF16)
+                    q.z[s] = h == 0 ? make_uint4(zq[0].x, zq[0].y, 0u, 0u) : make_uint4(zq[0].z, zq[0].w, 0u, 0u);
+                else
+                    q.z[s] = zq[h];
+            }
+            qn += __popc(bal);
+            __syncwarp();
+            if (qn >= 32) {  // warp-uniform
+                const uint32_t s = (qh + lane) & 63u;
+                race_block<DT, DD, YM>(A, Rr, resid, q.x[s], q.z[s], tfl, B * kRaceSlack, best, bx);
+                qh = (qh + 32) & 63u;
+                qn -= 32;
                 __syncwarp();
-                if (qn >= 32) {  // warp-uniform
-                    const uint32_t s = (qh + lane) & 63u;
-                    race_block<DT, DD, YM>(A, Rr, resid, q.x[s], q.z[s], tfl, B * kRaceSlack, best, bx);
-                    qh = (qh + 32) & 63u;
-                    qn -= 32;
-                    __syncwarp();
-                }
             }
         }
         // a lower key lowers this lane's bound and the shared ones; the shared bounds lower this lane's
