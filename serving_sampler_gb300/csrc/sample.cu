@@ -1655,9 +1655,10 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
 // u_x the Philox uniform of id x (counter (x >> 2, row, tag, 0), word x & 3).
 //
 // race_rows_kernel: the selected rows, each a fixed part cost followed by its
-// ids, are cut into equal shares over one wave of CTAs (two per SM); the parts
-// of a request meet in a packed 64-bit (key, id) minimum and the part that
-// finishes last commits.  Warp 0 scans the accept flags for n.  Each warp
+// ids, are cut into equal shares over one wave of CTAs (two per SM); a request
+// with T <= 0 (verified greedily whatever its rows hold) takes only the cost of
+// its decisions and commit.  The parts of a request meet in a packed 64-bit
+// (key, id) minimum and the part that finishes last commits.  Warp 0 scans the accept flags for n.  Each warp
 // streams 256-id steps of its part (the next step's loads in flight) and
 // keeps a running minimum key; a bound B of the row's minimum key is shared
 // through shared memory and, between the parts of a request, through the
@@ -1679,6 +1680,8 @@ constexpr int32_t kRaceStep = 256;                // ids per warp step, eight pe
 // a part's fixed cost (decisions, seeds, setup) in ids of its race, measured on the sampling
 // workload: parts are cut so that every CTA carries the same ids plus this cost per part
 constexpr int64_t kRacePartIds = 16384;
+constexpr int64_t kRaceGreedyIds = 2048;  // the same for a request verified greedily (T <= 0)
+constexpr int64_t kRaceMinShare = 2LL * kRaceWarps * kRaceStep;  // at least two steps per warp
 constexpr uint32_t kRaceSmemRow = 96 * 1024;      // draft rows up to this size are staged in shared memory
 constexpr float kRaceSlack = 1.0f + 1.0f / 1024.0f;
 constexpr float kRaceMinGap = 5.9604645e-8f;      // 2^-24: the smallest 1 - u
@@ -2040,10 +2043,17 @@ __device__ unsigned long long race_pass(const SampleArgs& A, const RaceRow& Rr, 
     return warp_min_u64(bx == INT32_MAX ? kNoKey : pack_key(best, bx));
 }
 
+// a request's length on the partition line: its part cost, then its row's ids padded to whole
+// steps; a request with T <= 0 (NaN included) is verified greedily and races nothing
+__device__ __forceinline__ int64_t race_line_len(float T, int64_t Vp)
+{
+    return T > 0.f ? kRacePartIds + Vp : kRaceGreedyIds;
+}
+
 }  // namespace
 
 template <int DT, int DD, int YM>
-__global__ void __launch_bounds__(kRaceThreads, 2) race_rows_kernel(SampleArgs A, int64_t share)
+__global__ void __launch_bounds__(kRaceThreads, 2) race_rows_kernel(SampleArgs A)
 {
     extern __shared__ __align__(16) unsigned char ysm_raw[];  // the selected draft row (d2t residual rows)
     __shared__ int32_t n_s, last_s;
@@ -2052,29 +2062,76 @@ __global__ void __launch_bounds__(kRaceThreads, 2) race_rows_kernel(SampleArgs A
     __shared__ unsigned long long wbest_s[kRaceWarps];
     __shared__ unsigned long long best_s;
     __shared__ uint32_t red_u[kRaceWarps];
-    __shared__ RaceQ queue_s[kRaceWarps];  // every warp's queue of blocks for pass 2
+    __shared__ long long line_s[kRaceWarps];  // the partition line's per-warp sums, then their prefix
+    __shared__ long long p0_s;                // where the request holding this CTA's first position starts
+    __shared__ int32_t r0_s;                  // that request
+    __shared__ RaceQ queue_s[kRaceWarps];     // every warp's queue of blocks for pass 2
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int32_t k = A.k;
-    // The rows, padded to whole 256-id steps, laid end to end: this CTA takes [g_lo, g_hi).
     const int64_t Vp = (static_cast<int64_t>(A.V) + kRaceStep - 1) / kRaceStep * kRaceStep;
-    // the partition line: every row is its part cost, then its ids padded to whole steps
-    const int64_t Vv = kRacePartIds + Vp;
-    const int64_t total = static_cast<int64_t>(A.R) * Vv;
-    const int64_t g_lo = static_cast<int64_t>(blockIdx.x) * share, g_hi = min(total, g_lo + share);
+    // ---- the partition line, from the inputs alone (taken while the row pass ends): thread t sums
+    // the lengths of a contiguous run of requests, a block scan gives every run's start ----
+    const int32_t per = (A.R + kRaceThreads - 1) / kRaceThreads;
+    const int32_t ra = min(A.R, tid * per), rb = min(A.R, ra + per);
+    long long run = 0;
+    for (int32_t r = ra; r < rb; ++r) run += race_line_len(A.temp[r], Vp);
+    long long incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) line_s[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        long long v = lane < kRaceWarps ? line_s[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long u = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += u;
+        }
+        if (lane < kRaceWarps) line_s[lane] = v;
+    }
+    __syncthreads();
+    const int64_t L = line_s[kRaceWarps - 1];
+    // equal shares over the grid, each at least two steps per warp and a whole number of steps
+    int64_t share = max(kRaceMinShare, (L + gridDim.x - 1) / gridDim.x);
+    share = (share + kRaceStep - 1) / kRaceStep * kRaceStep;
+    const int64_t g_lo = static_cast<int64_t>(blockIdx.x) * share, g_hi = min(L, g_lo + share);
+    if (g_lo >= L) return;  // nothing on the line for this CTA (block-uniform)
+    {
+        int64_t pos = incl - run + (warp > 0 ? line_s[warp - 1] : 0);  // where this thread's run starts
+        for (int32_t r = ra; r < rb; ++r) {
+            const int64_t len = race_line_len(A.temp[r], Vp);
+            if (pos <= g_lo && g_lo < pos + len) {
+                r0_s = r;
+                p0_s = pos;
+            }
+            pos += len;
+        }
+    }
+    __syncthreads();
     pdl_wait_primary();
-    for (int64_t g = g_lo; g < g_hi;) {
-        const int32_t r = static_cast<int32_t>(g / Vv);
-        const int64_t ids0 = static_cast<int64_t>(r) * Vv + kRacePartIds;  // where the row's ids start
-        const int32_t x_lo = static_cast<int32_t>(g > ids0 ? g - ids0 : 0);
-        const int32_t x_hi = static_cast<int32_t>(min(Vp, g_hi - ids0));
-        g = ids0 + Vp;
-        if (x_hi <= x_lo) continue;  // this share holds only the row's part cost (block-uniform)
-        // the CTAs that share request r's row, and whether this one holds its first part
-        const int32_t parts = static_cast<int32_t>((ids0 + Vp - 1) / share - ids0 / share + 1);
-        const bool first = x_lo == 0;
+    int64_t pos = p0_s;
+    for (int32_t r = r0_s; r < A.R && pos < g_hi; ++r) {
+        const float T = A.temp[r];
+        const int64_t len = race_line_len(T, Vp);
+        const int64_t start = pos;
+        pos += len;
+        int32_t x_lo = 0, x_hi = 0, parts = 1;
+        if (T > 0.f) {
+            const int64_t ids0 = start + kRacePartIds;  // where the row's ids start
+            x_lo = static_cast<int32_t>(g_lo > ids0 ? g_lo - ids0 : 0);
+            x_hi = static_cast<int32_t>(min(Vp, g_hi - ids0));
+            if (x_hi <= x_lo) continue;  // this share holds only the row's part cost (block-uniform)
+            // the CTAs that share request r's row
+            parts = static_cast<int32_t>((ids0 + Vp - 1) / share - ids0 / share + 1);
+        } else if (start < g_lo) {
+            continue;  // a greedily verified request is committed by the CTA holding its start
+        }
+        const bool first = x_lo == 0;  // this CTA holds the row's first part (commits a greedy request)
         const RowStat* st = A.stats + static_cast<int64_t>(r) * (k + 1);
         const int32_t* d = A.draft + static_cast<int64_t>(r) * k;
-        const float T = A.temp[r];
         // ---- the request's decisions (warp 0, ballots) ----
         if (tid < 32) {
             uint32_t fl = 0;
@@ -2460,16 +2517,13 @@ static cudaError_t launch_sample_t(const Rows& t, const Rows& d, const int32_t* 
         e = cudaLaunchKernelEx(&cfg, sample_rows_kernel<DT, DD>, A);
     }
     if (e != cudaSuccess) return e;
-    // the race: the rows, each its part cost then its ids padded to whole 256-id steps, laid end to
-    // end and cut in equal shares over one wave of CTAs (two per SM), each share at least two steps
-    // per warp; a request's row is split over several CTAs
+    // the race: one wave of CTAs (two per SM), or fewer when even the longest partition line (every
+    // request sampled) gives no CTA beyond the first ones a full minimum share; the kernel cuts the
+    // line itself from the temperatures
     const int64_t slots = 2LL * (sms > 0 ? sms : 148);
     const int64_t Vp = (static_cast<int64_t>(t.width) + kRaceStep - 1) / kRaceStep * kRaceStep;
-    const int64_t total_ids = static_cast<int64_t>(R) * (kRacePartIds + Vp);  // the partition line
-    const int64_t min_share = 2LL * kRaceWarps * kRaceStep;
-    int64_t share = std::max<int64_t>(min_share, (total_ids + slots - 1) / slots);
-    share = (share + kRaceStep - 1) / kRaceStep * kRaceStep;
-    const int64_t rgrid = (total_ids + share - 1) / share;
+    const int64_t line_max = static_cast<int64_t>(R) * (kRacePartIds + Vp);
+    const int64_t rgrid = std::max<int64_t>(1, std::min<int64_t>(slots, (line_max + kRaceMinShare - 1) / kRaceMinShare));
     const uint32_t ybytes = static_cast<uint32_t>(d.width) * d.esize;
     const bool yshared = !identity && A.dbulk && ybytes <= kRaceSmemRow && ybytes % 16 == 0;
     const size_t race_smem = yshared ? ybytes : 0;
@@ -2484,7 +2538,7 @@ static cudaError_t launch_sample_t(const Rows& t, const Rows& d, const int32_t* 
     cfg2.stream = stream;
     cfg2.attrs = attr;
     cfg2.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg2, race, A, share);
+    return cudaLaunchKernelEx(&cfg2, race, A);
 }
 
 cudaError_t launch_verify_sample(const Rows& target, const Rows& draft_logits, const int32_t* d2t,
