@@ -131,6 +131,27 @@ def test_sweep_point_mixed_greedy_and_sampling(sv, dtype):
     assert np.isnan(got["tv"][greedy]).all() and not np.isnan(got["tv"][~greedy]).any()
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_race_line_with_mostly_greedy_requests(sv, dtype):
+    """The race's partition line gives a request with T <= 0 (NaN included) only the cost of its
+    decisions: 3,000 requests, nine in ten verified greedily, the sampled ones spread out and in
+    one dense run, so that some CTAs hold nothing but greedy commits, some many sampled rows and
+    some both."""
+    R, k = 3000, 3
+    rng = np.random.default_rng(17)
+    T = np.where(rng.random(R) < 0.1, rng.choice([0.5, 0.8, 1.3], R), rng.choice([0.0, -0.5, np.nan], R))
+    T[2000:2060] = 0.9  # a run of sampled requests
+    w = workloads.sample_batch(R, k, 6000, 1500, dtype, T=T.astype(np.float32).tolist(), sigma_pos=0.8,
+                               delta=2.7, seed=71, seed_base=913)
+    got, want = _run(sv, w), _oracle(w)
+    compare(got, want)
+    greedy = ~(T > 0)
+    assert greedy.sum() > 2500 and (~greedy).sum() > 300
+    assert np.isnan(got["tv"][greedy]).all() and not np.isnan(got["tv"][~greedy]).any()
+    bad_temp = np.isnan(T) | (T < 0)
+    assert ((got["status"][bad_temp] & 16) != 0).all() and ((got["status"][~bad_temp] & 16) == 0).all()
+
+
 def test_identity_bf16_shapes(sv):
     w = workloads.sample_batch(12, 6, 5000, None, torch.bfloat16, T=0.9, sigma_pos=0.5, seed=4)
     compare(_run(sv, w), _oracle(w))
