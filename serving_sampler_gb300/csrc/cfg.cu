@@ -30,7 +30,6 @@ namespace sv {
 namespace {
 
 constexpr int32_t kCfgMaxW = 16384;  // widest codebook
-constexpr float kLog2eC = 1.4426950408889634f;
 
 enum : uint32_t { kCfgBad = 1u, kCfgOffSupport = 2u };
 
@@ -159,7 +158,7 @@ __global__ void __launch_bounds__(32 * kCfgWarpRows, 4) cfg_rows_warp_kernel(Cfg
     // follows the temperature alone
     const bool sampling = T > 0.f && (A.dbase != nullptr || k == 0);
     const bool has_draft = sampling && j < k;
-    const float c = sampling ? kLog2eC / T : 0.f;
+    const float c = sampling ? temp_scale(T) : 0.f;
     const unsigned long long w2 = pack2(A.shape.w, A.shape.w), c2 = pack2(c, c);
     const int64_t off = unit * A.stride + static_cast<int64_t>(A.shape.data_off[s]) * (DT == SV_BF16 ? 2 : 4);
     const char* cp = A.cbase + off;
@@ -455,7 +454,7 @@ __global__ void __launch_bounds__(kCfgRaceThreads) cfg_race_kernel(CfgArgs A)
         tok_local = d[n * S + s] - A.shape.id_base[s];
     } else {
         const bool residual = n < k;
-        const float c = kLog2eC / T;
+        const float c = temp_scale(T);
         const unsigned long long w2 = pack2(A.shape.w, A.shape.w), c2 = pack2(c, c);
         const unsigned long long nm2 = pack2(-sn.m, -sn.m), nd2 = pack2(-sn.mq, -sn.mq);
         const unsigned long long iS2 = pack2(1.f / sn.s, 1.f / sn.s);

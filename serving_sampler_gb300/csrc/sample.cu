@@ -48,7 +48,6 @@ constexpr int kStages = 4;
 constexpr int kRowHeader = 128;
 constexpr uint32_t kSmemBudget = 220 * 1024;
 constexpr int32_t kMaxPlanWords = 25600;  // d2t mode supports V <= 819,200
-constexpr float kLog2e = 1.4426950408889634f;
 
 enum : uint32_t { kFlagAllNegInf = 8u, kFlagDraftBad = 16u, kFlagOffSupport = 32u };
 
@@ -520,7 +519,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) sample_rows_kernel(SampleArgs 
         const float T = A.temp[r];
         const bool sampling = T > 0.f;
         const bool has_draft = sampling && j < A.k;
-        const float c = sampling ? kLog2e / T : 0.f;
+        const float c = sampling ? temp_scale(T) : 0.f;
         const char* trow = A.tbase + unit * A.tstride;
         const char* drow = has_draft ? A.dbase + (static_cast<int64_t>(r) * A.k + j) * A.dstride : nullptr;
         const int32_t xj = has_draft ? A.draft[static_cast<int64_t>(r) * A.k + j] : -1;
@@ -595,13 +594,13 @@ __global__ void __launch_bounds__(kRowThreads, 1) sample_rows_kernel(SampleArgs 
                     f = -INFINITY;
                 }
                 if (f == INFINITY) dflags |= kFlagPosInf;
-                const float t = f * c;
+                const float t = f * c;  // a candidate reference; the term itself as every other term
                 if (t > -INFINITY) {
                     if (t > dl.m) {
                         dl.s = dl.m == -INFINITY ? 0.f : dl.s * ex2(dl.m - t);
                         dl.m = t;
                     }
-                    dl.s += ex2(t - dl.m);
+                    dl.s += ex2(fmaf(f, c, -dl.m));
                 }
             }
         }
@@ -1269,7 +1268,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
             const FastUnit u = fast_unit(A, unit, T);
             const int64_t un = unit + gridDim.x;
             const float T_next = un < units ? unit_temp(A, un) : 0.f;  // for the next unit, loaded early
-            const float c = u.sampling ? kLog2e / T : 0.f;
+            const float c = u.sampling ? temp_scale(T) : 0.f;
             const unsigned long long c2 = pack2(c, c);
             const int32_t xj = u.has_draft ? A.draft[static_cast<int64_t>(u.r) * A.k + u.j] : -1;
             const int32_t q0 = warp_first(u.rot, w);
@@ -1431,7 +1430,7 @@ __global__ void __launch_bounds__(kFastThreads, 1) sample_rows_fast_kernel(Sampl
         const uint32_t b = n % kNG;
         const float T = unit_temp(A, unit);
         const FastUnit u = fast_unit(A, unit, T);
-        const float c = u.sampling ? kLog2e / T : 0.f;
+        const float c = u.sampling ? temp_scale(T) : 0.f;
         const int32_t xj = u.has_draft ? A.draft[static_cast<int64_t>(u.r) * A.k + u.j] : -1;
         const uint64_t seed = (u.has_draft && ttid == 0) ? A.seeds[u.r] : 0ull;  // for the accept test
         const unsigned char* G = gbase + b * gbytes;
@@ -2174,7 +2173,7 @@ __global__ void __launch_bounds__(kRaceThreads, 2) race_rows_kernel(SampleArgs A
             Rr.drow = residual ? A.dbase + (static_cast<int64_t>(r) * k + n) * A.dstride : nullptr;
             Rr.ysm = nullptr;
             Rr.ysmf = nullptr;
-            Rr.c = kLog2e / T;
+            Rr.c = temp_scale(T);
             Rr.m = rs.m;
             Rr.S = rs.s;
             Rr.invS = 1.f / rs.s;

@@ -202,6 +202,15 @@ __device__ __forceinline__ void sts_u16(uint32_t addr, uint32_t v)
     asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "r"(v));
 }
 
+// ---- the temperature's scale of logits in log2 units ------------------------
+// c = log2(e) / T for T > 0, held at or above 2^-100 so that T = +inf (every logit the same
+// weight) still maps a -inf logit to -inf rather than to -inf * 0 = NaN; any finite logit of
+// magnitude below 2^70 then scales to less than 2^-30 and weighs 1 in fp32, as at c = 0.
+__device__ __forceinline__ float temp_scale(float T)
+{
+    return fmaxf(1.4426950408889634f / T, 0x1p-100f);
+}
+
 // ---- fp32 pairs, exponentials, loads and warp maxima shared by the kernels ----
 __device__ __forceinline__ float ex2(float x)
 {

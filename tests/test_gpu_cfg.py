@@ -40,6 +40,15 @@ def test_cfg_sampling(sv, R, k, S, W, dtype, T):
     compare(_run(sv, w), _oracle(w))
 
 
+@pytest.mark.parametrize("dtype,W", [(torch.bfloat16, 4096), (torch.float32, 1000)])
+def test_cfg_extreme_temperatures(sv, dtype, W):
+    """T = +inf (every codebook id the same weight), 1e30, 1e-4 and 1e-6 (one-hot) beside an
+    ordinary and a greedy request, per codebook as the oracle."""
+    T = [float("inf"), 1e30, 1e-4, 1e-6, 0.8, 0.0] * 2
+    w = workloads.cfg_batch(len(T), 3, 4, W, 3.0, T, dtype, seed=W + 5)
+    compare(_run(sv, w), _oracle(w))
+
+
 def test_cfg_greedy_and_partition_offsets(sv):
     R, k, S, W = 6, 3, 4, 512
     offs = [100 + W * s for s in range(S)]

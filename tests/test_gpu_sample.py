@@ -152,6 +152,20 @@ def test_race_line_with_mostly_greedy_requests(sv, dtype):
     assert ((got["status"][bad_temp] & 16) != 0).all() and ((got["status"][~bad_temp] & 16) == 0).all()
 
 
+@pytest.mark.parametrize("dtype,Vd", [(torch.bfloat16, 700), (torch.float32, 700), (torch.float32, None),
+                                      (torch.bfloat16, 1024)])
+def test_extreme_temperatures(sv, dtype, Vd):
+    """T = +inf (p and q uniform over their vocabularies), T = 1e30, and T = 1e-4 / 1e-6 (p and q
+    one-hot at their argmaxes) beside an ordinary and a greedy request: accept lengths, tokens, TV,
+    p and q as the oracle's (a 700-id draft row has a 4-id tail past its last 16-byte vector; 1,024
+    ids take the bulk-copy row pass)."""
+    T = [float("inf"), 1e30, 1e-6, 1e-4, 0.7, 0.0] * 4
+    w = workloads.sample_batch(len(T), 3, 3000, Vd, dtype, T=T, sigma_pos=0.8, delta=2.7, seed=5, seed_base=9)
+    got, want = _run(sv, w), _oracle(w)
+    compare(got, want)
+    assert not np.isnan(got["tv"][np.array(T) > 0]).any()
+
+
 def test_identity_bf16_shapes(sv):
     w = workloads.sample_batch(12, 6, 5000, None, torch.bfloat16, T=0.9, sigma_pos=0.5, seed=4)
     compare(_run(sv, w), _oracle(w))
