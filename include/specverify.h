@@ -226,7 +226,10 @@ int sv_verify_greedy_noalloc(sv_rows target, int32_t R, int32_t k, int32_t branc
  *                 (then d2t may be NULL): skips building it in the call.
  *   draft         int32 [R, k] draft tokens as TARGET ids.
  *   seeds         uint64 [R] Philox key of each request.
- *   temperature   float [R]; T > 0 samples, T <= 0 verifies greedily.
+ *   temperature   float [R]; T > 0 samples, T <= 0 verifies greedily.  T = +inf
+ *                 weighs every finite logit the same; the kernels scale logits
+ *                 by log2(e)/T in fp32, so T below ~1e-7 with logits near 100
+ *                 is outside their range.
  *   accept_len    int32 [R] out; tokens int32 [R, k + 1] out (-1 padded).
  *   tv, p_draft, q_draft  float [R, k] out or NULL: TV(p_j, q_j) over the
  *                 full target vocabulary, p_j(x_j) and q_j(x_j) for every
