@@ -180,6 +180,26 @@ def test_alpha_equals_one_minus_tv(T):
     assert np.sum(np.maximum(0.0, p - q)) == pytest.approx(tv[0], abs=1e-12)
 
 
+def test_infinite_and_tiny_temperatures_closed_forms():
+    # T = +inf: p uniform over the V target ids and q over the Vd support ids, so
+    # TV = 1 - Vd / V, every on-support draft has p/q = Vd / V and every off-support one is
+    # rejected.  T -> 0: p and q one-hot at their argmaxes, TV 0 or 1.
+    rng = np.random.default_rng(21)
+    V, Vd = 40, 12
+    d2t = rng.permutation(V)[:Vd].astype(np.int32)
+    z = rng.normal(0, 1.5, V).astype(np.float32)
+    y = (z[d2t] + rng.normal(0, 0.5, Vd)).astype(np.float32)
+    p, q, tv, out = _all_draft_tokens(z, y, d2t, V, T=np.inf)
+    assert np.allclose(p, 1.0 / V, rtol=1e-12)
+    assert np.allclose(q[d2t], 1.0 / Vd, rtol=1e-12) and np.all(np.delete(q, d2t) == 0)
+    assert np.allclose(tv, 1.0 - Vd / V, atol=1e-12)
+    p, q, tv, out = _all_draft_tokens(z, y, d2t, V, T=1e-6)
+    zmax, ymax = int(np.argmax(z)), int(d2t[np.argmax(y)])
+    assert p[zmax] == 1.0 and np.all(np.delete(p, zmax) == 0.0)
+    assert q[ymax] == 1.0 and np.all(np.delete(q, ymax) == 0.0)
+    assert np.all(tv == (0.0 if zmax == ymax else 1.0))
+
+
 def test_truncated_vocabulary_tv_over_full_support():
     rng = np.random.default_rng(5)
     V, Vd = 40, 12
